@@ -1,0 +1,417 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: values printed
+on the pages (tests/golden), library routines (torch's fp8 cast, scipy's
+Hadamard matrix, Python's sort), closed forms, invariants and brute force.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import scipy.linalg
+import torch
+
+import inputs
+import oracle
+from conftest import golden_rows
+
+D, H = 128, 32
+
+
+# ------------------------------------------------------------------ codecs --
+
+def test_e2m1_values_match_page_table():
+    for code, mag in golden_rows("e2m1_values.txt"):
+        c, m = int(code), float(mag)
+        assert oracle.e2m1_value(c) == m
+        assert oracle.e2m1_value(c | 8) == -m
+    distinct = {oracle.e2m1_value(c) for c in range(16)}
+    assert len(distinct) == 15  # +0 and -0 compare equal: 15 values
+
+
+def test_e2m1_rounding_golden_midpoints():
+    for x, code in golden_rows("e2m1_rounding.txt"):
+        assert oracle.e2m1_encode(float(x)) == int(code), x
+        assert oracle.e2m1_encode(-float(x)) == int(code) | 8, x
+
+
+def test_e2m1_encode_is_nearest_and_monotone():
+    xs = np.linspace(0, 8, 20001, dtype=np.float32)
+    vals = np.array([oracle.e2m1_value(c) for c in range(8)])
+    prev = 0
+    for x in xs:
+        c = oracle.e2m1_encode(float(x))
+        assert c >= prev
+        prev = c
+        err = abs(float(x) - vals[c])
+        assert err <= np.min(np.abs(float(x) - vals)) + 0.0
+
+
+def test_e4m3_decode_matches_torch_all_codes():
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for c in range(256):
+        v = oracle.e4m3_value(c)
+        if math.isnan(ref[c]):
+            assert math.isnan(v)
+        else:
+            assert v == ref[c], c
+    assert oracle.e4m3_value(0x7E) == 448.0  # 448 * 6 = 2688 (page: 去掉全局 scale 之后范围仍然够用)
+
+
+def test_e4m3_encode_matches_torch_cast_in_range():
+    rng = np.random.default_rng(0)
+    xs = np.concatenate([
+        np.linspace(0, 448, 50001),
+        np.exp(rng.uniform(np.log(1e-4), np.log(448), 50000)),
+        # exact midpoints between neighbouring codes: ties go to the even code
+        np.array([(oracle.e4m3_value(c) + oracle.e4m3_value(c + 1)) / 2 for c in range(126)]),
+    ]).astype(np.float32)
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    mine = np.array([oracle.e4m3_encode(float(x)) for x in xs], dtype=np.uint8)
+    assert (mine == ref).all()
+    # negative values keep their sign
+    neg = torch.from_numpy(-xs[:2000]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    mine_neg = np.array([oracle.e4m3_encode(-float(x)) for x in xs[:2000]], dtype=np.uint8)
+    nz = xs[:2000] != 0
+    assert (mine_neg[nz] == neg[nz]).all()
+
+
+def test_e4m3_saturates_at_448():
+    for x in [448.0, 449.0, 464.0, 480.0, 1e6]:
+        assert oracle.e4m3_encode(x) == 0x7E
+
+
+# ---------------------------------------------------------------- rotation --
+
+def test_fwht_is_sylvester_hadamard():
+    cols = np.stack([oracle.fwht128(np.eye(D, dtype=np.float32)[i]) for i in range(D)], 1)
+    assert (cols == scipy.linalg.hadamard(D)).all()
+    assert (cols @ cols.T == D * np.eye(D)).all()
+
+
+def test_fwht_twice_is_128x_on_small_integers():
+    rng = np.random.default_rng(1)
+    x = rng.integers(-50, 50, D).astype(np.float32)
+    assert (oracle.fwht128(oracle.fwht128(x)) == D * x).all()
+
+
+def test_rotation_preserves_dot_products():
+    rng = np.random.default_rng(2)
+    q = rng.standard_normal(D)
+    k = rng.standard_normal(D)
+    s = rng.choice([-1.0, 1.0], D)
+    Hm = scipy.linalg.hadamard(D).astype(np.float64)
+    assert abs((Hm @ (s * q)) @ (Hm @ (s * k)) / D - q @ k) < 1e-9
+
+
+# ---------------------------------------------------------------- quantise --
+
+def _rand_tensor(seed, rows):
+    return inputs.normal_bf16(seed, 99, rows * D).reshape(rows, D)
+
+
+def test_quantize_tensor_scale_and_range():
+    x = _rand_tensor(3, 40)
+    s = inputs.signs(3)
+    rec, g = oracle.quantize(x, s)
+    Hm = scipy.linalg.hadamard(D).astype(np.float64)
+    y = (inputs.bf16_to_f32(x).astype(np.float64) * s) @ Hm.T
+    amax = np.abs(y).max()
+    assert g == pytest.approx(amax / 2688.0, rel=1e-6)
+    dec = oracle.decode_rows(rec, 40, g)
+    # largest representable magnitude is 6 * 448 * g = amax_T
+    assert np.abs(dec).max() <= 6 * 448 * g * (1 + 1e-6)
+    assert np.abs(dec).max() >= amax * (1 - 0.07)
+
+
+def test_quantize_error_within_half_step():
+    x = _rand_tensor(4, 64)
+    s = inputs.signs(4)
+    rec, g = oracle.quantize(x, s)
+    Hm = scipy.linalg.hadamard(D).astype(np.float64)
+    y = (inputs.bf16_to_f32(x).astype(np.float64) * s) @ Hm.T
+    dec = oracle.decode_rows(rec, 64, g)
+    for r in range(64):
+        for grp in range(8):
+            sl = slice(16 * grp, 16 * grp + 16)
+            yb, db = y[r, sl], dec[r, sl]
+            amax_b = np.abs(yb).max()
+            nz = np.abs(db[db != 0])
+            sc = nz.min() / 0.5 if nz.size else 0.0  # not the scale itself; only a bound below
+            # decoded block max within one E4M3 step (12.5%) of the true block max
+            assert np.abs(db).max() <= amax_b * 1.13 + 1e-12
+            assert np.abs(db).max() >= amax_b / 1.13 - 1e-12
+            # every element within half the widest E2M1 gap (1.0 between 4 and 6) of
+            # the block scale, which is at most amax_b / 6 * 1.0625
+            assert np.all(np.abs(yb - db) <= amax_b / 6 * 1.0625 * 1.0 + 1e-9)
+            del sc
+
+
+def test_quantize_mode1_reuses_scale_and_is_deterministic():
+    x = _rand_tensor(5, 17)
+    s = inputs.signs(5)
+    rec0, g0 = oracle.quantize(x, s)
+    rec1, g1 = oracle.quantize(x, s, g=g0)
+    assert g1 == g0 and (rec0 == rec1).all()
+    assert rec0.size == 3 * 576
+    # padding rows of the last record are zero
+    dec = oracle.decode_row(rec0, 17, g0)
+    assert (dec == 0).all()
+
+
+def test_quantize_zero_tensor():
+    x = np.zeros((8, D), dtype=np.uint16)
+    rec, g = oracle.quantize(x, np.ones(D, dtype=np.int8))
+    assert g == 1.0 and (rec == 0).all()
+
+
+# ------------------------------------------------------------------- score --
+
+def _sparse_exact_case(seed):
+    """q, k whose rotated rows have at most two non-zeros from the E2M1 set, so
+    that NVFP4 holds them exactly (up to the fp32 tensor scale)."""
+    rng = np.random.default_rng(seed)
+    Hm = scipy.linalg.hadamard(D).astype(np.float64)
+    s = np.ones(D, dtype=np.int8)
+
+    def rows(n):
+        ys = np.zeros((n, D))
+        for r in range(n):
+            # both non-zeros in one 16-element group, whose block scale then
+            # decodes to g * 448, so every E2M1 value is held exactly
+            grp = rng.integers(0, D // 16)
+            i, j = grp * 16 + rng.choice(16, 2, replace=False)
+            ys[r, i] = 6.0 * rng.choice([-1, 1])
+            ys[r, j] = rng.choice([0.5, 1, 1.5, 2, 3, 4, 6]) * rng.choice([-1, 1])
+        xs = ys @ Hm / D  # H^-1 = H / 128; entries are (+-a +- b)/128: exact in bf16
+        b = (xs.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        assert (inputs.bf16_to_f32(b) == xs).all()
+        return b, xs
+
+    qb, qx = rows(H)
+    kb, kx = rows(50)
+    return s, qb, qx, kb, kx
+
+
+def test_score_equals_unrotated_formula_when_quantisation_is_exact():
+    s, qb, qx, kb, kx = _sparse_exact_case(6)
+    qrec, gq = oracle.quantize(qb, s)
+    krec, gk = oracle.quantize(kb, s)
+    w = np.random.default_rng(7).standard_normal(H).astype(np.float32)
+    scores, macs = oracle.score_full(qrec, gq, w, krec, gk, 50)
+    # page formula on the original (unrotated) vectors, in double
+    ref = np.maximum(kx @ qx.T, 0.0) @ w.astype(np.float64)
+    assert np.allclose(scores, ref, rtol=2e-6, atol=1e-9)
+    assert macs == 50 * 4096
+
+
+def test_score_single_head_is_relu_of_decoded_gemv():
+    wl = inputs.workload(0)
+    s = wl.signs()
+    qrec, gq = oracle.quantize(wl.q_bf16(0, 0), s)
+    krec, gk = oracle.quantize(wl.k_bf16(0, 0, rows=300), s)
+    qd = oracle.decode_rows(qrec, H, gq)
+    kd = oracle.decode_rows(krec, 300, gk)
+    for j in (0, 13, 31):
+        w = np.zeros(H, dtype=np.float32)
+        w[j] = 1.0
+        sc, _ = oracle.score_full(qrec, gq, w, krec, gk, 300)
+        ref = np.maximum(kd @ qd[j], 0.0) / 128.0
+        assert np.allclose(sc, ref.astype(np.float32), rtol=1e-6, atol=0)
+
+
+def test_score_tracks_unquantised_formula():
+    wl = inputs.workload(0)
+    s = wl.signs()
+    qb, kb = wl.q_bf16(0, 0), wl.k_bf16(0, 0, rows=2000)
+    qrec, gq = oracle.quantize(qb, s)
+    krec, gk = oracle.quantize(kb, s)
+    w = wl.w(0, 0)
+    sc, _ = oracle.score_full(qrec, gq, w, krec, gk, 2000)
+    ref = np.maximum(inputs.bf16_to_f32(kb).astype(np.float64) @ inputs.bf16_to_f32(qb).astype(np.float64).T,
+                     0.0) @ w.astype(np.float64)
+    assert np.corrcoef(sc, ref)[0, 1] > 0.97
+    # a transposed or sign-flipped operand destroys the correlation
+    bad = np.maximum(-(inputs.bf16_to_f32(kb).astype(np.float64) @ inputs.bf16_to_f32(qb).astype(np.float64).T),
+                     0.0) @ w.astype(np.float64)
+    assert np.corrcoef(sc, bad)[0, 1] < 0.5
+
+
+def test_score_rows_matches_full_and_tolerance_positive():
+    wl = inputs.workload(0)
+    s = wl.signs()
+    qrec, gq = oracle.quantize(wl.q_bf16(0, 0), s)
+    krec, gk = oracle.quantize(wl.k_bf16(0, 0, rows=500), s)
+    w = wl.w(0, 0)
+    full, _ = oracle.score_full(qrec, gq, w, krec, gk, 500)
+    rows = np.array([0, 7, 8, 123, 499])
+    part, tol = oracle.score_rows(qrec, gq, w, krec, gk, rows)
+    assert (part == full[rows]).all()
+    assert (tol > 0).all()
+    # the bound exceeds the largest possible fp32 rounding of the score itself
+    assert (tol > np.abs(part) * 2e-7).all()
+
+
+def test_mac_counts_reproduce_page_totals():
+    per_key = 4096
+    for name, keys, printed, sig in golden_rows("mac_counts.txt"):
+        keys, printed, sig = int(keys), float(printed), int(sig)
+        got = keys * per_key
+        if sig == 0:
+            assert got == printed, name
+        else:  # the page rounds to `sig` significant figures
+            assert float(f"{got:.{sig - 1}e}") == printed, (name, got, printed)
+    # per key, counted by the oracle itself on a pooled Reindex layer
+    wl = inputs.workload(0)
+    s = wl.signs()
+    qrec, gq = oracle.quantize(wl.q_bf16(0, 0), s)
+    krec, gk = oracle.quantize(wl.k_bf16(0, 0, rows=16384), s)
+    ids = np.arange(2048, dtype=np.int32)
+    _, macs = oracle.score_pool(qrec, gq, wl.w(0, 0), krec, gk, 16384, ids, 2048)
+    assert macs == 16384 * 4096  # ~6.7e7 per pooled layer
+
+
+# ------------------------------------------------------------------- top-k --
+
+def test_topk_brute_force_small():
+    rng = np.random.default_rng(8)
+    for n in range(0, 9):
+        for trial in range(30):
+            vals = rng.choice([-1.5, -0.0, 0.0, 0.25, 1.0, 2.0], n).astype(np.float32)
+            for k in (1, 3, 8):
+                idx, val = oracle.topk(vals, n, k)
+                ref = sorted(range(n), key=lambda i: (-float(vals[i]), i))[:k]
+                m = len(ref)
+                assert list(idx[:m]) == ref
+                assert (idx[m:] == -1).all() and np.isneginf(val[m:]).all()
+                assert (val[:m] == vals[ref]).all()
+
+
+def test_topk_all_equal_gives_lowest_indices():
+    vals = np.full(5000, 3.25, dtype=np.float32)
+    idx, _ = oracle.topk(vals, 5000, 512)
+    assert (idx == np.arange(512)).all()
+
+
+def test_topk_signed_zero_ties_by_index():
+    vals = np.array([-0.0, 0.0, -0.0, -1.0], dtype=np.float32)
+    idx, _ = oracle.topk(vals, 4, 3)
+    assert list(idx) == [0, 1, 2]
+
+
+# -------------------------------------------------------------------- pool --
+
+def _check_pool_definition(scores, n_vis, bs, keep, ids, nk, npool, mask):
+    nblk = -(-n_vis // bs)
+    bval = np.full(nblk, -np.inf)
+    for b in range(nblk):
+        bval[b] = scores[b * bs:min(n_vis, b * bs + bs)].max()
+    if n_vis:
+        bval[(n_vis - 1) // bs] = np.inf
+    K = set(ids[:nk].tolist())
+    assert list(ids[:nk]) == sorted(K)
+    assert nk == min(keep, nblk)
+    if n_vis:
+        assert (n_vis - 1) // bs in K
+    for b in K:
+        for c in set(range(nblk)) - K:
+            assert (bval[b], -b) > (bval[c], -c)
+    exp_mask = np.array([1 if (sidx // bs) in K else 0 for sidx in range(n_vis)], dtype=np.uint8)
+    assert (mask == exp_mask).all()
+    assert npool == exp_mask.sum()
+
+
+def test_pool_brute_force_tiny():
+    rng = np.random.default_rng(9)
+    for bs in (1, 2, 3, 4):
+        for keep in range(1, 9):
+            for n_vis in (1, 2, 5, 9, 17, 33, 64):
+                scores = rng.choice([-2.0, -1.0, 0.0, 0.5, 1.0, 3.0], n_vis).astype(np.float32)
+                ids, nk, npool, mask = oracle.pool(scores, n_vis, bs, keep)
+                _check_pool_definition(scores, n_vis, bs, keep, ids, nk, npool, mask)
+
+
+def test_pool_page_figure_block4_keep6():
+    rng = np.random.default_rng(10)
+    scores = rng.standard_normal(60).astype(np.float32)
+    ids, nk, npool, mask = oracle.pool(scores, 58, 4, 6)
+    assert nk == 6 and npool <= 24
+    _check_pool_definition(scores, 58, 4, 6, ids, nk, npool, mask)
+
+
+def test_pool_short_context_keeps_everything():
+    rng = np.random.default_rng(11)
+    for n_vis in (1, 100, 16383, 16384):
+        scores = rng.standard_normal(n_vis).astype(np.float32)
+        ids, nk, npool, mask = oracle.pool(scores, n_vis)
+        assert npool == n_vis and mask.all()
+        assert nk == -(-n_vis // 8)
+
+
+def test_pool_bound_pin_and_nesting():
+    rng = np.random.default_rng(12)
+    n_vis = 50001
+    scores = rng.standard_normal(n_vis).astype(np.float32)
+    ids, nk, npool, mask = oracle.pool(scores, n_vis)
+    assert nk == 2048 and npool <= 16384
+    assert (n_vis - 1) // 8 == ids[nk - 1]
+    assert npool == 2047 * 8 + 1  # the pinned block holds only one visible position
+    top, _ = oracle.topk(scores, n_vis, 512)
+    assert mask[top].all()  # top-512 inside the pool inside the visible range
+
+
+def test_pool_drops_minus_inf_blocks():
+    scores = np.array([-np.inf] * 8 + [1.0] * 8 + [-np.inf] * 8 + [2.0], dtype=np.float32)
+    ids, nk, npool, mask = oracle.pool(scores, 25, 8, 4)
+    assert list(ids[:nk]) == [1, 3] and npool == 9
+
+
+# ----------------------------------------------------------------- reindex --
+
+def test_pooled_reindex_equals_page_masked_form():
+    wl = inputs.workload(0)
+    s = wl.signs()
+    n_vis = 20003
+    krec, gk = oracle.quantize(wl.k_bf16(0, 0, rows=n_vis), s)
+    q0, g0 = oracle.quantize(wl.q_bf16(0, 0), s)
+    q1, g1 = oracle.quantize(wl.q_bf16(1, 0), s)
+    full0, _ = oracle.score_full(q0, g0, wl.w(0, 0), krec, gk, n_vis)
+    ids, nk, npool, mask = oracle.pool(full0, n_vis)
+    assert nk == 2048
+    ps, _ = oracle.score_pool(q1, g1, wl.w(1, 0), krec, gk, n_vis, ids, nk)
+    assert np.isneginf(ps[npool:]).all() and np.isfinite(ps[:npool]).all()
+    idx, val = oracle.topk_pool(ps, npool, ids)
+    full1, _ = oracle.score_full(q1, g1, wl.w(1, 0), krec, gk, n_vis)
+    midx, mval = oracle.topk_masked(full1, n_vis, mask)
+    assert (idx == midx).all() and (val == mval).all()
+    assert mask[idx].all()
+
+
+# --------------------------------------------------------------- generator --
+
+def test_splitmix64_published_vector():
+    G = 0x9E3779B97F4A7C15
+    want = [int(r[0]) for r in golden_rows("splitmix64.txt")]
+    got = [inputs.lib().gen_mix64((1234567 + G * (i + 1)) % (1 << 64)) for i in range(5)]
+    assert got == want
+
+
+def test_generator_normal_moments_and_determinism():
+    a = inputs.bf16_to_f32(inputs.normal_bf16(0, 5, 400000)).astype(np.float64)
+    assert abs(a.mean()) < 0.01 and abs(a.var() - 1) < 0.01
+    assert abs(((a - a.mean()) ** 4).mean() / a.var() ** 2 - 3) < 0.05
+    b = inputs.normal_bf16(0, 5, 1000, first=1000)
+    assert (inputs.normal_bf16(0, 5, 2000)[1000:] == b).all()
+    w = inputs.normal_f32(0, 6, 200000, sigma=(1 / 32) ** 0.5)
+    assert abs(w.var() - 1 / 32) < 1e-3
+
+
+def test_workload_recipes():
+    w1 = inputs.workload(1)
+    assert w1.B == 16 and all(4096 <= n <= 131072 for n in w1.seq_len)
+    w4 = inputs.workload(4)
+    assert w4.B == 8192 and w4.n_visible[0] == 122881 and w4.n_visible[-1] == 131072
+    w2 = inputs.workload(2)
+    assert w2.B == 64 and w2.seq_len[0] == 1 << 20 and w2.reindex_layers == 4
