@@ -1,0 +1,238 @@
+/*
+ * libhsi -- the decode-time hot path of DeepSeek-V4.1's Hierarchical Sparse
+ * Indexer on one GB300 (sm_103a).
+ *
+ * The method (sources are the pages' titles and sections):
+ *  - Lightning-indexer score, "DeepSeek-V4.1 模型结构（3）：序列维度（下），
+ *    Hierarchical Sparse Indexer 与 FP4 KV cache", section "Reindex 层每个 token
+ *    要给 100 万条打分", equation I_{t,s} = sum_{j=1..32} w_{t,j} ReLU(q_{t,j} . k_s),
+ *    32 heads x 128 dims, FP4 q and k.
+ *  - Per-layer top-512 and the two-level candidate pool (blocks of 8, block
+ *    score = max, keep 2048 blocks), same page, section "用浅层的打分结果限制深层
+ *    的打分范围"; pinning of the newest block and the per-query boolean table,
+ *    section "候选池的三个细节在代码里".
+ *  - Reindex layers score only inside the pool; a deployed kernel reads only
+ *    the pooled indexer K (same section, last paragraph).
+ *  - Random Hadamard rotation before FP4 quantisation, "DeepSeek-V4 模型结构（2）：
+ *    序列维度（中），Lightning Indexer 与稀疏选择", Q&A on quantisation.
+ *
+ * Conventions for every call:
+ *  - Pointers marked (dev) are device pointers, (host) host pointers. The
+ *    caller owns every buffer; no call allocates or frees memory.
+ *  - Every call is enqueued on `stream` and returns without synchronising.
+ *    Host-side argument errors are returned at once and launch nothing.
+ *  - A kernel that detects a problem on the device (a bounded wait that ran
+ *    out, a malformed argument only visible on the device) records it in a
+ *    sticky device error word; hsi_device_error() reports and clears it.
+ *  - Scratch memory is passed in as (ws, ws_bytes); hsi_workspace_size() says
+ *    how much a call needs. ws must be 256-byte aligned.
+ *  - The library runs only on compute capability 10.3 devices.
+ */
+#ifndef HSI_H_
+#define HSI_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    HSI_OK = 0,
+    HSI_ERR_INVALID_ARG = -1,    /* a null pointer, a bad size or a misaligned buffer */
+    HSI_ERR_UNSUPPORTED = -2,    /* a valid request this build does not serve (device, shape) */
+    HSI_ERR_CUDA = -3,           /* a CUDA runtime call failed (launch, attribute, sync) */
+    HSI_ERR_DEVICE_TIMEOUT = -4, /* a kernel's bounded wait ran out (reported by hsi_device_error) */
+    HSI_ERR_WORKSPACE = -5,      /* ws is NULL, too small or not 256-byte aligned */
+    HSI_ERR_DEVICE_ARG = -6      /* a kernel found a bad device-side argument (reported by hsi_device_error) */
+} hsi_status;
+
+#define HSI_HEADS 32      /* indexer heads H */
+#define HSI_DIM 128       /* head dimension d */
+#define HSI_REC_ROWS 8    /* rows per NVFP4 block record */
+#define HSI_REC_BYTES 576 /* bytes per NVFP4 block record: 8 rows x (64 B codes + 8 B scales) */
+
+/*
+ * NVFP4 block-record storage, used for indexer queries and indexer K.
+ *
+ * A tensor of R rows of 128 values is stored as ceil(R/8) records of 576 bytes
+ * plus one fp32 tensor scale g. Record i holds rows 8i .. 8i+7 (missing rows
+ * of the last record are zero):
+ *   bytes [0, 512):   E2M1 codes. Value e (0..127) of row r sits in byte
+ *                     (e/32)*128 + r*16 + (e%32)/2, low nibble for even e,
+ *                     high nibble for odd e (bit 3 of a code is its sign).
+ *   bytes [512, 576): E4M3 block scales. The scale of row r, values
+ *                     16j .. 16j+15, is byte 512 + r*8 + j.
+ * The decoded value is E2M1(code) * E4M3(scale) * g. A query (32 heads) is
+ * 4 records; a K cache of n keys is ceil(n/8) records, and its block of
+ * positions 8b .. 8b+7 is exactly record b: 8 keys x 72 B = 576 B.
+ */
+
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Rotate and quantise bf16 rows to NVFP4 block records.
+ * Page: "DeepSeek-V4 模型结构（2）", Q&A on quantisation (random Hadamard
+ * rotation before FP4); "DeepSeek-V4.1 模型结构（3）", section "E2M1 只能表示
+ * 15 个值" (q = round_E2M1(x/s), s = max|x|/6) and section "去掉全局 scale 之后
+ * 范围仍然够用" (448 x 6 = 2688).
+ *
+ * Per row: y = H (signs .* x), H the unnormalised 128-point Sylvester Hadamard
+ * transform evaluated in fp32 stage by stage (h = 1, 2, ..., 64). Per tensor:
+ * g = amax|y| / 2688 (g = 1 for an all-zero tensor). Per 16 values:
+ * sb = E4M3_RN(amax_b / (6 g)), code = E2M1_RN(y / (E4M3(sb) g)) (0 when that
+ * scale is 0). Rounding is to nearest, ties to even, saturating at 448 / 6.
+ *
+ *  x         (dev)  bf16 bit patterns [n_tensors * rows_per_tensor][128].
+ *  signs     (host) 128 values, each +1 or -1 (the rotation's random signs;
+ *                   queries and keys scored together must share them).
+ *  mode      0: compute g per tensor and write it to g; 1: read g (> 0) from g.
+ *  g         (dev)  fp32 [n_tensors].
+ *  rec       (dev)  out: n_tensors * ceil(rows_per_tensor/8) records; tensor t
+ *                   starts at record t * ceil(rows_per_tensor/8).
+ *  ws        (dev)  mode 0: 4 * n_tensors bytes. Mode 1: may be NULL.
+ * Errors: INVALID_ARG for null pointers, non-positive sizes, signs not +-1,
+ * unaligned rec (16 B) or x (16 B); WORKSPACE when ws is short in mode 0.
+ */
+hsi_status hsi_quantize_nvfp4(const uint16_t* x, int64_t n_tensors, int64_t rows_per_tensor,
+                              const int8_t* signs, int mode, float* g, uint8_t* rec, void* ws,
+                              size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Lightning-indexer scores of every visible key (a Full layer).
+ * Page: "DeepSeek-V4.1 模型结构（3）", section "Reindex 层每个 token 要给 100 万条打分"
+ * (the equation); section "用浅层的打分结果限制深层的打分范围" (the Full layer
+ * scores all visible positions).
+ *
+ *   scores[b][s] = (g_q[b] g_k[b] / 128) * sum_j w[b][j] * max(a_j, 0),
+ *   a_j = sum_d qhat[b][j][d] * khat_s[d]      (0 <= s < n_visible[b])
+ * with qhat, khat the decoded values without tensor scales; the factor 1/128
+ * undoes the unnormalised rotation of both operands. The contraction runs on
+ * the tensor cores (FP4 x FP4, fp32 accumulation); ReLU and the weighted head
+ * sum are fused, so per-head logits never reach memory.
+ *
+ *  q_rec   (dev) B*4 records (query b = records 4b .. 4b+3); g_q (dev) [B].
+ *  w       (dev) fp32 [B][32].
+ *  k_rec   (dev) base of the K records; query b reads the cache starting at
+ *                record k_rec_off[b] (dev, int64 [B]); g_k (dev) [B] is that
+ *                cache's tensor scale.
+ *  n_visible (dev) int32 [B], 0 <= n_visible[b] <= max_visible (host bound).
+ *  group   1, or 4: queries 4i .. 4i+3 share one cache (equal k_rec_off and
+ *          g_k) and are scored in one tensor-core tile (chunked prefill);
+ *          B must then be a multiple of 4.
+ *  scores  (dev) fp32 [B][ld]; entries s < n_visible[b] are written, the
+ *          rest are left untouched. ld >= max_visible.
+ *  block_max (dev, may be NULL) fp32 [B][ldb]: the max of each run of 8
+ *          consecutive visible scores (block b8 = positions 8*b8 .. 8*b8+7,
+ *          invisible positions count as -inf), for the blocks that hold a
+ *          visible position. ldb >= ceil(max_visible/8).
+ *  ws      may be NULL (0 bytes needed).
+ */
+hsi_status hsi_score_full(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
+                          const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible,
+                          int32_t B, int64_t max_visible, int32_t group, float* scores, int64_t ld,
+                          float* block_max, int64_t ldb, void* ws, size_t ws_bytes,
+                          cudaStream_t stream);
+
+/*
+ * Exact per-query top-k of fp32 scores.
+ * Page: "DeepSeek-V4.1 模型结构（3）", section "用浅层的打分结果限制深层的打分范围"
+ * (each Full and Reindex layer keeps its own top-512).
+ *
+ * For query b the eligible entries are i < n_valid[b] of row scores[b][.]
+ * (ld floats per row). Order: value descending (-0 and +0 compare equal),
+ * ties by index ascending. Writes min(k, n_valid[b]) entries to out_idx[b][.]
+ * and out_val[b][.] in that order and pads the rest with -1 / -inf.
+ * Scores must not be NaN.
+ *
+ *  block_ids (dev, may be NULL) int32 [B][ld_blocks]: when given, an eligible
+ *          local index i is reported as the position block_ids[b][i/block_size]
+ *          * block_size + i % block_size (pool-local -> global; the block ids
+ *          must be ascending so that the tie order carries over).
+ *  max_valid (host) upper bound of n_valid; k in [1, 2048].
+ *  ws      (dev) hsi_workspace_size(HSI_WS_TOPK, B, max_valid, k) bytes.
+ */
+hsi_status hsi_topk(const float* scores, int64_t ld, const int32_t* n_valid, int32_t B, int64_t max_valid,
+                    int32_t k, const int32_t* block_ids, int64_t ld_blocks, int32_t block_size,
+                    int32_t* out_idx, float* out_val, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * The candidate pool of each query.
+ * Page: "DeepSeek-V4.1 模型结构（3）", sections "用浅层的打分结果限制深层的打分范围"
+ * (blocks of 8, block score = max, top 2048 blocks, at most 16384 positions)
+ * and "候选池的三个细节在代码里" (the newest block pinned, -inf padding, blocks
+ * whose value is -inf dropped, a per-query boolean table).
+ *
+ * Query b sees positions [0, n_visible[b]). Blocks are runs of block_size
+ * positions; a block's value is the max of its visible scores; the block of
+ * position n_visible[b]-1 gets +inf. The pool keeps the first
+ * min(n_keep, nblk) blocks by (value desc, block index asc) whose value is
+ * > -inf, intersected with the visible positions.
+ *
+ *  scores  (dev) fp32 [B][ld] (read for s < n_visible[b]); may be NULL when
+ *          block_max is given.
+ *  block_max (dev, may be NULL) fp32 [B][ldb]: precomputed block maxima for
+ *          block_size 8, as hsi_score_full writes them.
+ *  block_ids (dev) out int32 [B][n_keep]: kept block indices ascending, -1 padded.
+ *  n_kept  (dev) out int32 [B]: number of kept blocks.
+ *  n_pool  (dev) out int32 [B]: number of visible positions in the pool (the
+ *          kept blocks' positions in block-list order, less the invisible tail
+ *          of the newest block, which is always last).
+ *  pool_bits (dev, may be NULL) out uint32 [B][ld_bits]: the boolean table,
+ *          bit s%32 of word s/32 set iff position s is in the pool; words up to
+ *          ceil(n_visible[b]/32) are written. ld_bits >= ceil(max_visible/32).
+ *  block_size in [1, 64]; n_keep in [1, 4096].
+ *  ws      (dev) hsi_workspace_size(HSI_WS_POOL, B, max_visible, n_keep) bytes.
+ */
+hsi_status hsi_candidate_pool(const float* scores, int64_t ld, const float* block_max, int64_t ldb,
+                              const int32_t* n_visible, int32_t B, int64_t max_visible, int32_t block_size,
+                              int32_t n_keep, int32_t* block_ids, int32_t* n_kept, int32_t* n_pool,
+                              uint32_t* pool_bits, int64_t ld_bits, void* ws, size_t ws_bytes,
+                              cudaStream_t stream);
+
+/*
+ * Reindex-layer scores restricted to the pool, reading only pooled K.
+ * Page: "DeepSeek-V4.1 模型结构（3）", section "用浅层的打分结果限制深层的打分范围"
+ * (Reindex layers score only pooled positions, 16384 x 4096 MACs per token)
+ * and the last paragraph of "候选池的三个细节在代码里" (a deployed kernel fetches
+ * only the pooled indexer K).
+ *
+ * Slot i = 8j + r of query b holds the score of position block_ids[b][j]*8 + r
+ * (same formula as hsi_score_full), -inf if that position is not visible.
+ * Slots i < 8 * n_kept[b] are written; the rest are left untouched. Each
+ * pooled block is one 576-byte K record, fetched whole.
+ *
+ *  block_ids, n_kept: as written by hsi_candidate_pool with block_size 8.
+ *  pool_scores (dev) fp32 [B][ld], ld >= 8 * n_keep.
+ *  ws      may be NULL.
+ */
+hsi_status hsi_score_pool(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
+                          const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible,
+                          const int32_t* block_ids, const int32_t* n_kept, int32_t n_keep, int32_t B,
+                          float* pool_scores, int64_t ld, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+typedef enum { HSI_WS_QUANTIZE = 0, HSI_WS_SCORE = 1, HSI_WS_TOPK = 2, HSI_WS_POOL = 3 } hsi_ws_kind;
+
+/* Scratch bytes a call needs for B queries of at most max_n entries.
+ * QUANTIZE: B = number of tensors (max_n, k unused). SCORE: 0. TOPK: max_n =
+ * max_valid (k unused). POOL: max_n = max_visible and k = block_size. */
+size_t hsi_workspace_size(hsi_ws_kind kind, int32_t B, int64_t max_n, int32_t k);
+
+/* Synchronise `stream`, then report and clear the sticky device error word of
+ * the current device: HSI_OK, HSI_ERR_DEVICE_TIMEOUT or HSI_ERR_DEVICE_ARG
+ * (or HSI_ERR_CUDA if the synchronisation itself failed). */
+hsi_status hsi_device_error(cudaStream_t stream);
+
+/* HSI_OK if the current device is compute capability 10.3, else UNSUPPORTED. */
+hsi_status hsi_device_check(void);
+
+/* A static English description of a status code. */
+const char* hsi_status_string(hsi_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HSI_H_ */

@@ -1,0 +1,177 @@
+"""Python binding of libhsi, the GB300 hot path of the Hierarchical Sparse Indexer.
+
+Argument marshalling only: every function passes device pointers of torch
+tensors, sizes and the current CUDA stream to the C ABI declared in
+``include/hsi.h`` and raises ``HsiError`` on a non-OK status. No step of the
+path runs in Python or torch. The library must have been built (``build()``);
+importing this module on a machine without it raises at the first call.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_PKG)
+_CSRC = os.path.join(_PKG, "csrc")
+_SO = os.path.join(_PKG, "libhsi.so")
+_lib = None
+
+HEADS, DIM, REC_ROWS, REC_BYTES = 32, 128, 8, 576
+
+STATUS = {0: "HSI_OK", -1: "HSI_ERR_INVALID_ARG", -2: "HSI_ERR_UNSUPPORTED", -3: "HSI_ERR_CUDA",
+          -4: "HSI_ERR_DEVICE_TIMEOUT", -5: "HSI_ERR_WORKSPACE", -6: "HSI_ERR_DEVICE_ARG"}
+WS_QUANTIZE, WS_SCORE, WS_TOPK, WS_POOL = 0, 1, 2, 3
+
+EXPORTS = ["hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
+           "hsi_workspace_size", "hsi_device_error", "hsi_device_check", "hsi_status_string"]
+
+
+class HsiError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {STATUS.get(status, status)}")
+
+
+def nvcc_command(out: str = _SO) -> list[str]:
+    return ["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
+            "-Xcompiler", "-fPIC", "-shared", "-o", out, os.path.join(_CSRC, "hsi.cu")]
+
+
+def build(force: bool = False) -> str:
+    """Compile libhsi.so for sm_103a in the package directory."""
+    srcs = [os.path.join(_CSRC, f) for f in os.listdir(_CSRC)] + [os.path.join(_ROOT, "include", "hsi.h")]
+    newest = max(os.path.getmtime(s) for s in srcs)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < newest:
+        tmp = _SO + f".tmp{os.getpid()}"
+        subprocess.check_call(nvcc_command(tmp))
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_SO):
+            raise RuntimeError(f"libhsi is not built ({_SO} missing); run __graft_entry__.build()")
+        L = ctypes.CDLL(_SO)
+        vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+        L.hsi_quantize_nvfp4.argtypes = [vp, i64, i64, vp, ctypes.c_int, vp, vp, vp, sz, vp]
+        L.hsi_score_full.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, vp, i64, vp, i64, vp, sz, vp]
+        L.hsi_topk.argtypes = [vp, i64, vp, i32, i64, i32, vp, i64, i32, vp, vp, vp, sz, vp]
+        L.hsi_candidate_pool.argtypes = [vp, i64, vp, i64, vp, i32, i64, i32, i32, vp, vp, vp, vp, i64, vp, sz, vp]
+        L.hsi_score_pool.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i64, vp, sz, vp]
+        L.hsi_workspace_size.argtypes = [ctypes.c_int, i32, i64, i32]
+        L.hsi_workspace_size.restype = sz
+        L.hsi_device_error.argtypes = [vp]
+        L.hsi_device_check.argtypes = []
+        L.hsi_status_string.argtypes = [ctypes.c_int]
+        L.hsi_status_string.restype = ctypes.c_char_p
+        for name in ("hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
+                     "hsi_device_error", "hsi_device_check"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check(fn: str, st: int):
+    if st != 0:
+        raise HsiError(fn, st)
+
+
+def workspace_size(kind: int, B: int, max_n: int, k: int = 0) -> int:
+    return int(lib().hsi_workspace_size(kind, B, max_n, k))
+
+
+def workspace(kind: int, B: int, max_n: int, k: int = 0, device="cuda") -> torch.Tensor | None:
+    """A caller-owned scratch buffer for one call (256-byte aligned by torch)."""
+    n = workspace_size(kind, B, max_n, k)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
+def device_check():
+    _check("hsi_device_check", lib().hsi_device_check())
+
+
+def device_error(stream=None) -> int:
+    """Synchronise, then return and clear the sticky device status (0 = OK)."""
+    return int(lib().hsi_device_error(_stream(stream)))
+
+
+def n_records(rows: int) -> int:
+    return (rows + REC_ROWS - 1) // REC_ROWS
+
+
+def quantize_nvfp4(x: torch.Tensor, n_tensors: int, rows_per_tensor: int, signs, g: torch.Tensor,
+                   rec: torch.Tensor, mode: int = 0, ws: torch.Tensor | None = None, stream=None):
+    """x: bf16 (or its int16 bits) [n_tensors*rows_per_tensor, 128] on the device."""
+    s8 = (ctypes.c_int8 * 128)(*[int(v) for v in signs])
+    if mode == 0 and ws is None:
+        ws = workspace(WS_QUANTIZE, n_tensors, 0, device=x.device)
+    _check("hsi_quantize_nvfp4", lib().hsi_quantize_nvfp4(
+        _ptr(x), n_tensors, rows_per_tensor, s8, mode, _ptr(g), _ptr(rec), _ptr(ws),
+        0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def score_full(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B, max_visible, scores, ld=None,
+               block_max=None, ldb=0, group=1, stream=None):
+    ld = scores.shape[-1] if ld is None else ld
+    if block_max is not None and not ldb:
+        ldb = block_max.shape[-1]
+    _check("hsi_score_full", lib().hsi_score_full(
+        _ptr(q_rec), _ptr(g_q), _ptr(w), _ptr(k_rec), _ptr(g_k), _ptr(k_rec_off), _ptr(n_visible), B,
+        max_visible, group, _ptr(scores), ld, _ptr(block_max), ldb, None, 0, _stream(stream)))
+
+
+def topk(scores, n_valid, B, max_valid, k, out_idx, out_val, ld=None, block_ids=None, ld_blocks=0,
+         block_size=8, ws=None, stream=None):
+    ld = scores.shape[-1] if ld is None else ld
+    if ws is None:
+        ws = workspace(WS_TOPK, B, max_valid, k, device=scores.device)
+    if block_ids is not None and not ld_blocks:
+        ld_blocks = block_ids.shape[-1]
+    _check("hsi_topk", lib().hsi_topk(
+        _ptr(scores), ld, _ptr(n_valid), B, max_valid, k, _ptr(block_ids), ld_blocks, block_size,
+        _ptr(out_idx), _ptr(out_val), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def candidate_pool(n_visible, B, max_visible, block_ids, n_kept, n_pool, scores=None, ld=0, block_max=None,
+                   ldb=0, block_size=8, n_keep=2048, pool_bits=None, ld_bits=0, ws=None, stream=None):
+    if scores is not None and not ld:
+        ld = scores.shape[-1]
+    if block_max is not None and not ldb:
+        ldb = block_max.shape[-1]
+    if pool_bits is not None and not ld_bits:
+        ld_bits = pool_bits.shape[-1]
+    if ws is None:
+        dev = (scores if scores is not None else block_max).device
+        ws = workspace(WS_POOL, B, max_visible, block_size, device=dev)
+    _check("hsi_candidate_pool", lib().hsi_candidate_pool(
+        _ptr(scores), ld, _ptr(block_max), ldb, _ptr(n_visible), B, max_visible, block_size, n_keep,
+        _ptr(block_ids), _ptr(n_kept), _ptr(n_pool), _ptr(pool_bits), ld_bits, _ptr(ws),
+        0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def score_pool(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, block_ids, n_kept, n_keep, B, pool_scores,
+               ld=None, stream=None):
+    ld = pool_scores.shape[-1] if ld is None else ld
+    _check("hsi_score_pool", lib().hsi_score_pool(
+        _ptr(q_rec), _ptr(g_q), _ptr(w), _ptr(k_rec), _ptr(g_k), _ptr(k_rec_off), _ptr(n_visible),
+        _ptr(block_ids), _ptr(n_kept), n_keep, B, _ptr(pool_scores), ld, None, 0, _stream(stream)))

@@ -1,0 +1,52 @@
+// Shared device-side definitions: the sticky error word and small helpers.
+#pragma once
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace hsi {
+
+// Device error codes (bit flags, OR-ed into the sticky word).
+enum : uint32_t {
+    DEVERR_TIMEOUT = 1u,  // a bounded wait ran out
+    DEVERR_ARG = 2u,      // a device-side argument was malformed
+};
+
+// The sticky error word of this module on the current device (the library is
+// one translation unit, so this is its only definition).
+__device__ uint32_t g_hsi_error = 0;
+
+__device__ __forceinline__ void raise_error(uint32_t code) { atomicOr(&g_hsi_error, code); }
+
+// Wait for the phase of `bar` with the given parity to complete, bounded in
+// wall-clock time. Returns false (after setting *abort and the device error
+// word on a timeout) when the wait gave up, either by running out or because
+// another warp of the block has already aborted.
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > HSI_WAIT_TIMEOUT_NS) {
+            raise_error(DEVERR_TIMEOUT);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+// Order-preserving map of an fp32 score to a uint32 key (larger score ->
+// larger key); -0 maps like +0. Scores must not be NaN.
+__device__ __forceinline__ uint32_t order_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+    const uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+    return __uint_as_float(u);
+}
+
+}  // namespace hsi

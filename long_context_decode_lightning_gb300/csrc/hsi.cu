@@ -1,0 +1,345 @@
+// libhsi: the C-ABI entry points. Host-side validation, workspace carving and
+// kernel launches; all arithmetic of the path runs in the kernels included here.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/hsi.h"
+#include "common.cuh"
+#include "quantize.cuh"
+#include "score.cuh"
+#include "select.cuh"
+
+using namespace hsi;
+
+namespace {
+
+constexpr int kDecodeStages = 8;
+constexpr int kGatherStages = 8;
+constexpr int kPrefillStages = 6;
+constexpr int kCandCap = 16384;  // survivors of the histogram pass kept per query
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+hsi_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? HSI_OK : HSI_ERR_CUDA; }
+
+hsi_status launch_ok() { return cuda_ok(cudaGetLastError()); }
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace of the selection passes for B queries of at most max_items items.
+struct SelWs {
+    uint32_t* hist;
+    uint32_t* cnt;
+    uint32_t* ckey;
+    uint32_t* cidx;
+    float* bmax;
+};
+
+size_t sel_ws_bytes(int32_t B, int64_t max_items, bool need_bmax, int64_t max_blocks) {
+    size_t s = 0;
+    if (max_items > SEL_CAP) {
+        s += align_up((size_t)B * HIST_BINS * 4, 256);
+        s += align_up((size_t)B * 4, 256);
+        s += 2 * align_up((size_t)B * kCandCap * 4, 256);
+    }
+    if (need_bmax) s += align_up((size_t)B * (size_t)max_blocks * 4, 256);
+    return s;
+}
+
+SelWs carve_sel(void* ws, int32_t B, int64_t max_items, bool need_bmax, int64_t max_blocks) {
+    SelWs w{};
+    uint8_t* p = static_cast<uint8_t*>(ws);
+    if (max_items > SEL_CAP) {
+        w.hist = reinterpret_cast<uint32_t*>(p);
+        p += align_up((size_t)B * HIST_BINS * 4, 256);
+        w.cnt = reinterpret_cast<uint32_t*>(p);
+        p += align_up((size_t)B * 4, 256);
+        w.ckey = reinterpret_cast<uint32_t*>(p);
+        p += align_up((size_t)B * kCandCap * 4, 256);
+        w.cidx = reinterpret_cast<uint32_t*>(p);
+        p += align_up((size_t)B * kCandCap * 4, 256);
+    }
+    if (need_bmax) w.bmax = reinterpret_cast<float*>(p);
+    return w;
+}
+
+hsi_status run_select(SelParams sp, int64_t max_items, cudaStream_t s) {
+    if (max_items > SEL_CAP) {
+        if (cudaMemsetAsync(sp.hist, 0, (size_t)sp.B * HIST_BINS * 4, s) != cudaSuccess) return HSI_ERR_CUDA;
+        if (cudaMemsetAsync(sp.cand_cnt, 0, (size_t)sp.B * 4, s) != cudaSuccess) return HSI_ERR_CUDA;
+        const dim3 grid((unsigned)((max_items + SCAN_CHUNK - 1) / SCAN_CHUNK), (unsigned)sp.B);
+        sel_hist_kernel<<<grid, SCAN_THREADS, 0, s>>>(sp);
+        if (launch_ok() != HSI_OK) return HSI_ERR_CUDA;
+        sel_collect_kernel<<<grid, SCAN_THREADS, 0, s>>>(sp);
+        if (launch_ok() != HSI_OK) return HSI_ERR_CUDA;
+    }
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(sel_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)sizeof(SelSmem)) != cudaSuccess)
+            return HSI_ERR_CUDA;
+        attr_set = true;
+    }
+    sel_final_kernel<<<sp.B, SEL_THREADS, sizeof(SelSmem), s>>>(sp);
+    return launch_ok();
+}
+
+template <int NQ, bool GATHER, int STAGES>
+hsi_status launch_score(const ScoreParams& p, cudaStream_t s) {
+    using C = ScoreCfg<NQ, GATHER, STAGES>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(score_kernel<NQ, GATHER, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::SMEM_BYTES) != cudaSuccess)
+            return HSI_ERR_CUDA;
+        attr_set = true;
+    }
+    const int sms = sm_count();
+    if (sms <= 0) return HSI_ERR_CUDA;
+    score_kernel<NQ, GATHER, STAGES><<<sms, C::THREADS, C::SMEM_BYTES, s>>>(p);
+    return launch_ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* hsi_status_string(hsi_status st) {
+    switch (st) {
+        case HSI_OK: return "ok";
+        case HSI_ERR_INVALID_ARG: return "invalid argument";
+        case HSI_ERR_UNSUPPORTED: return "unsupported device or shape";
+        case HSI_ERR_CUDA: return "CUDA runtime error";
+        case HSI_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait ran out";
+        case HSI_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+        case HSI_ERR_DEVICE_ARG: return "a kernel found a malformed device-side argument";
+    }
+    return "unknown status";
+}
+
+hsi_status hsi_device_check(void) {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return HSI_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return HSI_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return HSI_ERR_CUDA;
+    return (major == 10 && minor == 3) ? HSI_OK : HSI_ERR_UNSUPPORTED;
+}
+
+hsi_status hsi_device_error(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return HSI_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_hsi_error, sizeof(word)) != cudaSuccess) return HSI_ERR_CUDA;
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_hsi_error, &zero, sizeof(zero)) != cudaSuccess) return HSI_ERR_CUDA;
+    if (word & DEVERR_TIMEOUT) return HSI_ERR_DEVICE_TIMEOUT;
+    if (word & DEVERR_ARG) return HSI_ERR_DEVICE_ARG;
+    return HSI_OK;
+}
+
+size_t hsi_workspace_size(hsi_ws_kind kind, int32_t B, int64_t max_n, int32_t k) {
+    if (B <= 0 || max_n < 0) return 0;
+    switch (kind) {
+        case HSI_WS_QUANTIZE: return align_up((size_t)B * 4, 256);
+        case HSI_WS_SCORE: return 0;
+        case HSI_WS_TOPK: return sel_ws_bytes(B, max_n, false, 0);
+        case HSI_WS_POOL: {
+            // k is the block size here; block maxima are computed into the
+            // workspace when they are not given
+            const int64_t bs = k < 1 ? 1 : k;
+            const int64_t nb = (max_n + bs - 1) / bs;
+            return sel_ws_bytes(B, nb, true, nb);
+        }
+    }
+    return 0;
+}
+
+hsi_status hsi_quantize_nvfp4(const uint16_t* x, int64_t n_tensors, int64_t rows_per_tensor, const int8_t* signs,
+                              int mode, float* g, uint8_t* rec, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!x || !signs || !g || !rec || n_tensors <= 0 || rows_per_tensor <= 0) return HSI_ERR_INVALID_ARG;
+    if (mode != 0 && mode != 1) return HSI_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(rec, 16) || !aligned(g, 4)) return HSI_ERR_INVALID_ARG;
+    QuantParams p{};
+    p.x = x;
+    p.n_tensors = n_tensors;
+    p.rpt = rows_per_tensor;
+    p.rec_per_tensor = (rows_per_tensor + 7) / 8;
+    for (int d = 0; d < 128; ++d) {
+        if (signs[d] != 1 && signs[d] != -1) return HSI_ERR_INVALID_ARG;
+        if (signs[d] < 0) p.neg_mask[d >> 5] |= 1u << (d & 31);
+    }
+    p.g = g;
+    p.rec = rec;
+    if (mode == 0) {
+        if (!ws || ws_bytes < (size_t)n_tensors * 4 || !aligned(ws, 256)) return HSI_ERR_WORKSPACE;
+        p.amax_bits = static_cast<uint32_t*>(ws);
+        if (cudaMemsetAsync(ws, 0, (size_t)n_tensors * 4, stream) != cudaSuccess) return HSI_ERR_CUDA;
+        const int64_t rows = n_tensors * rows_per_tensor;
+        quant_amax_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
+        if (launch_ok() != HSI_OK) return HSI_ERR_CUDA;
+        quant_scale_kernel<<<(unsigned)((n_tensors + 255) / 256), 256, 0, stream>>>(p);
+        if (launch_ok() != HSI_OK) return HSI_ERR_CUDA;
+    }
+    const int64_t prows = n_tensors * p.rec_per_tensor * 8;
+    quant_encode_kernel<<<(unsigned)((prows + 7) / 8), 256, 0, stream>>>(p);
+    return launch_ok();
+}
+
+static hsi_status check_score_common(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
+                                     const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible,
+                                     int32_t B) {
+    if (!q_rec || !g_q || !w || !k_rec || !g_k || !k_rec_off || !n_visible || B <= 0) return HSI_ERR_INVALID_ARG;
+    if (!aligned(q_rec, 16) || !aligned(k_rec, 16) || !aligned(w, 16)) return HSI_ERR_INVALID_ARG;
+    return HSI_OK;
+}
+
+hsi_status hsi_score_full(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
+                          const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible, int32_t B,
+                          int64_t max_visible, int32_t group, float* scores, int64_t ld, float* block_max,
+                          int64_t ldb, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    (void)ws;
+    (void)ws_bytes;
+    hsi_status st = check_score_common(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B);
+    if (st != HSI_OK) return st;
+    if (!scores || max_visible < 0 || max_visible > (int64_t)INT32_MAX - 128 || ld < max_visible)
+        return HSI_ERR_INVALID_ARG;
+    if (block_max && ldb < (max_visible + 7) / 8) return HSI_ERR_INVALID_ARG;
+    if (group != 1 && group != 4) return HSI_ERR_UNSUPPORTED;
+    if (B % group) return HSI_ERR_INVALID_ARG;
+    ScoreParams p{};
+    p.q_rec = q_rec;
+    p.g_q = g_q;
+    p.w = w;
+    p.k_rec = k_rec;
+    p.g_k = g_k;
+    p.k_off = k_rec_off;
+    p.n_vis = n_visible;
+    p.B = B;
+    p.ngroups = B / group;
+    p.scores = scores;
+    p.ld = ld;
+    p.bmax = block_max;
+    p.ldb = ldb;
+    if (group == 1) return launch_score<1, false, kDecodeStages>(p, stream);
+    return launch_score<4, false, kPrefillStages>(p, stream);
+}
+
+hsi_status hsi_score_pool(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
+                          const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible,
+                          const int32_t* block_ids, const int32_t* n_kept, int32_t n_keep, int32_t B,
+                          float* pool_scores, int64_t ld, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    (void)ws;
+    (void)ws_bytes;
+    hsi_status st = check_score_common(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B);
+    if (st != HSI_OK) return st;
+    if (!block_ids || !n_kept || !pool_scores || n_keep <= 0 || n_keep > (1 << 20) || ld < (int64_t)n_keep * 8)
+        return HSI_ERR_INVALID_ARG;
+    ScoreParams p{};
+    p.q_rec = q_rec;
+    p.g_q = g_q;
+    p.w = w;
+    p.k_rec = k_rec;
+    p.g_k = g_k;
+    p.k_off = k_rec_off;
+    p.n_vis = n_visible;
+    p.B = B;
+    p.ngroups = B;
+    p.block_ids = block_ids;
+    p.n_kept = n_kept;
+    p.n_keep = n_keep;
+    p.pool_scores = pool_scores;
+    p.ld_pool = ld;
+    return launch_score<1, true, kGatherStages>(p, stream);
+}
+
+hsi_status hsi_topk(const float* scores, int64_t ld, const int32_t* n_valid, int32_t B, int64_t max_valid, int32_t k,
+                    const int32_t* block_ids, int64_t ld_blocks, int32_t block_size, int32_t* out_idx,
+                    float* out_val, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!scores || !n_valid || !out_idx || !out_val || B <= 0 || max_valid < 0 || ld < max_valid)
+        return HSI_ERR_INVALID_ARG;
+    if (max_valid > (int64_t)INT32_MAX) return HSI_ERR_INVALID_ARG;
+    if (k < 1 || k > 2048) return HSI_ERR_INVALID_ARG;
+    if (block_ids && (block_size < 1 || ld_blocks < (max_valid + block_size - 1) / block_size))
+        return HSI_ERR_INVALID_ARG;
+    const size_t need = sel_ws_bytes(B, max_valid, false, 0);
+    if (need && (!ws || ws_bytes < need || !aligned(ws, 256))) return HSI_ERR_WORKSPACE;
+    SelWs wsp = carve_sel(ws, B, max_valid, false, 0);
+    SelParams sp{};
+    sp.src = scores;
+    sp.ld = ld;
+    sp.n_src = n_valid;
+    sp.div = 1;
+    sp.B = B;
+    sp.k = k;
+    sp.mode = SEL_TOPK;
+    sp.hist = wsp.hist;
+    sp.cand_cnt = wsp.cnt;
+    sp.cand_key = wsp.ckey;
+    sp.cand_idx = wsp.cidx;
+    sp.cap = kCandCap;
+    sp.block_ids = block_ids;
+    sp.ld_blocks = ld_blocks;
+    sp.block_size = block_size;
+    sp.out_idx = out_idx;
+    sp.out_val = out_val;
+    return run_select(sp, max_valid, stream);
+}
+
+hsi_status hsi_candidate_pool(const float* scores, int64_t ld, const float* block_max, int64_t ldb,
+                              const int32_t* n_visible, int32_t B, int64_t max_visible, int32_t block_size,
+                              int32_t n_keep, int32_t* block_ids, int32_t* n_kept, int32_t* n_pool,
+                              uint32_t* pool_bits, int64_t ld_bits, void* ws, size_t ws_bytes,
+                              cudaStream_t stream) {
+    if (!n_visible || !block_ids || !n_kept || !n_pool || B <= 0 || max_visible < 0) return HSI_ERR_INVALID_ARG;
+    if (max_visible > (int64_t)INT32_MAX) return HSI_ERR_INVALID_ARG;
+    if (block_size < 1 || block_size > 64 || n_keep < 1 || n_keep > SEL_MAXK) return HSI_ERR_INVALID_ARG;
+    const int64_t max_blocks = (max_visible + block_size - 1) / block_size;
+    if (block_max) {
+        if (block_size != 8 || ldb < max_blocks) return HSI_ERR_INVALID_ARG;
+    } else {
+        if (!scores || ld < max_visible) return HSI_ERR_INVALID_ARG;
+    }
+    if (pool_bits && ld_bits < (max_visible + 31) / 32) return HSI_ERR_INVALID_ARG;
+    const bool need_bmax = block_max == nullptr;
+    const size_t need = sel_ws_bytes(B, max_blocks, need_bmax, max_blocks);
+    if (need && (!ws || ws_bytes < need || !aligned(ws, 256))) return HSI_ERR_WORKSPACE;
+    SelWs wsp = carve_sel(ws, B, max_blocks, need_bmax, max_blocks);
+    const float* bm = block_max;
+    int64_t bld = ldb;
+    if (need_bmax) {
+        const dim3 grid((unsigned)((max_blocks + 255) / 256 > 0 ? (max_blocks + 255) / 256 : 1), (unsigned)B);
+        block_max_kernel<<<grid, 256, 0, stream>>>(scores, ld, n_visible, block_size, wsp.bmax, max_blocks);
+        if (launch_ok() != HSI_OK) return HSI_ERR_CUDA;
+        bm = wsp.bmax;
+        bld = max_blocks;
+    }
+    SelParams sp{};
+    sp.src = bm;
+    sp.ld = bld;
+    sp.n_src = n_visible;
+    sp.div = block_size;
+    sp.B = B;
+    sp.k = n_keep;
+    sp.mode = SEL_POOL;
+    sp.hist = wsp.hist;
+    sp.cand_cnt = wsp.cnt;
+    sp.cand_key = wsp.ckey;
+    sp.cand_idx = wsp.cidx;
+    sp.cap = kCandCap;
+    sp.blk_out = block_ids;
+    sp.n_kept = n_kept;
+    sp.n_pool = n_pool;
+    sp.bits = pool_bits;
+    sp.ld_bits = ld_bits;
+    return run_select(sp, max_blocks, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,146 @@
+// K1: random-sign Hadamard rotation + NVFP4 quantisation into block records.
+//
+// One warp per row of 128 values; lane l holds values 4l .. 4l+3. The
+// unnormalised Sylvester transform runs stage by stage (h = 1, 2, ..., 64):
+// the first two stages inside a lane, the last five across lanes with shuffles.
+// Every output of a stage is the same single IEEE add or subtract of the same
+// two operands regardless of which lane computes it, so the result is
+// bit-identical to any other stage-ordered evaluation in fp32.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace hsi {
+
+struct QuantParams {
+    const uint16_t* x;      // bf16 bits [n_tensors * rpt][128]
+    int64_t n_tensors;
+    int64_t rpt;            // rows per tensor
+    int64_t rec_per_tensor; // ceil(rpt / 8)
+    uint32_t neg_mask[4];   // bit d set: sign d is -1
+    float* g;               // [n_tensors]
+    uint32_t* amax_bits;    // [n_tensors] (mode 0)
+    uint8_t* rec;
+};
+
+// y = H (s .* x) for this warp's row; v holds values 4*lane .. 4*lane+3.
+__device__ __forceinline__ void rotate_row_warp(const QuantParams& p, int64_t row, float (&v)[4]) {
+    const int lane = threadIdx.x & 31;
+    const uint2 raw = *reinterpret_cast<const uint2*>(p.x + row * 128 + lane * 4);
+    const int wsel = lane >> 3;  // select without dynamic indexing of the parameter array
+    const uint32_t word = wsel == 0 ? p.neg_mask[0] : wsel == 1 ? p.neg_mask[1] : wsel == 2 ? p.neg_mask[2] : p.neg_mask[3];
+    const uint32_t bits = word >> ((lane & 7) * 4);
+    uint32_t h[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float f = __uint_as_float(h[i] << 16);
+        v[i] = ((bits >> i) & 1u) ? -f : f;
+    }
+    // h = 1 and h = 2: inside the lane.
+    {
+        float a0 = v[0], a1 = v[1], a2 = v[2], a3 = v[3];
+        v[0] = __fadd_rn(a0, a1);
+        v[1] = __fsub_rn(a0, a1);
+        v[2] = __fadd_rn(a2, a3);
+        v[3] = __fsub_rn(a2, a3);
+        a0 = v[0], a1 = v[1], a2 = v[2], a3 = v[3];
+        v[0] = __fadd_rn(a0, a2);
+        v[2] = __fsub_rn(a0, a2);
+        v[1] = __fadd_rn(a1, a3);
+        v[3] = __fsub_rn(a1, a3);
+    }
+    // h = 4 .. 64: partner lane differs in bit log2(h) - 2.
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float other = __shfl_xor_sync(0xFFFFFFFFu, v[i], m);
+            // lower element a, upper element b: lower <- a + b, upper <- a - b
+            v[i] = upper ? __fsub_rn(other, v[i]) : __fadd_rn(v[i], other);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) quant_amax_kernel(QuantParams p) {
+    const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int64_t total = p.n_tensors * p.rpt;
+    if (warp >= total) return;
+    float v[4];
+    rotate_row_warp(p, warp, v);
+    float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if ((threadIdx.x & 31) == 0) atomicMax(&p.amax_bits[warp / p.rpt], __float_as_uint(m));
+}
+
+__global__ void quant_scale_kernel(QuantParams p) {
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= p.n_tensors) return;
+    const float amax = __uint_as_float(p.amax_bits[t]);
+    p.g[t] = amax > 0.0f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
+}
+
+// E4M3 bits -> fp32, exact (OCP FP8 E4M3: bias 7, subnormals m/8 * 2^-6).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+    const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+    const float mag = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0.001953125f;
+    return (b & 0x80u) ? -mag : mag;
+}
+
+__device__ __forceinline__ uint32_t f32_to_e4m3_rn_sat(float x) {
+    uint32_t out;
+    asm("{\n\t.reg .b16 t;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\t"
+        "cvt.u32.u16 %0, t;\n\t}"
+        : "=r"(out)
+        : "f"(0.0f), "f"(x));
+    return out & 0xFFu;
+}
+
+// Four values -> four E2M1 codes, value 0 in the lowest nibble.
+__device__ __forceinline__ uint32_t f32x4_to_e2m1x4(float a, float b, float c, float d) {
+    unsigned short out;
+    asm("{\n\t.reg .b8 lo, hi;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 hi, %4, %3;\n\t"
+        "mov.b16 %0, {lo, hi};\n\t}"
+        : "=h"(out)
+        : "f"(a), "f"(b), "f"(c), "f"(d));
+    return out;
+}
+
+__global__ void __launch_bounds__(256) quant_encode_kernel(QuantParams p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t prow = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // padded row index
+    const int64_t padded_rows = p.rec_per_tensor * 8;
+    if (prow >= p.n_tensors * padded_rows) return;
+    const int64_t t = prow / padded_rows;
+    const int64_t r = prow % padded_rows;
+    uint8_t* rec = p.rec + (t * p.rec_per_tensor + r / 8) * 576;
+    const int rr = (int)(r & 7);
+    uint16_t codes = 0;
+    uint8_t scale = 0;
+    if (r < p.rpt) {
+        float v[4];
+        rotate_row_warp(p, t * p.rpt + r, v);
+        const float g = p.g[t];
+        float ab = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+        ab = fmaxf(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 1));
+        ab = fmaxf(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 2));  // max over values 16j .. 16j+15
+        const uint32_t sb = f32_to_e4m3_rn_sat(__fdiv_rn(ab, __fmul_rn(6.0f, g)));
+        const float sc = __fmul_rn(e4m3_to_f32(sb), g);
+        if (sc != 0.0f) {
+            codes = (uint16_t)f32x4_to_e2m1x4(__fdiv_rn(v[0], sc), __fdiv_rn(v[1], sc), __fdiv_rn(v[2], sc),
+                                              __fdiv_rn(v[3], sc));
+        }
+        scale = (uint8_t)sb;
+    }
+    // values 4*lane .. 4*lane+3 -> two bytes at (e/32)*128 + rr*16 + (e%32)/2
+    *reinterpret_cast<uint16_t*>(rec + (lane >> 3) * 128 + rr * 16 + (lane & 7) * 2) = codes;
+    if ((lane & 3) == 0) rec[512 + rr * 8 + (lane >> 2)] = scale;
+}
+
+}  // namespace hsi

@@ -1,0 +1,490 @@
+// K3 / K4: exact per-query selection over fp32 scores.
+//
+// Both the top-k of a score row and the candidate pool (a top-n_keep over
+// block maxima, ids then sorted ascending) are "the k best items by (key desc,
+// index asc)" with key = order_key(value). One routine serves both:
+//
+//   * items of a query that fit in shared memory (<= SEL_CAP) are loaded once
+//     and selected in shared memory by a 4-pass 8-bit radix select, with
+//     per-warp histograms;
+//   * longer rows first go through a 4096-bin histogram of the top 12 key bits
+//     (many CTAs per query, shared-memory atomics merged into a global
+//     histogram) and a collect pass that keeps only items in or above the bin
+//     that holds the k-th key; the survivors (about k plus one bin) are then
+//     selected in shared memory;
+//   * if the survivors overflow their buffer (heavily tied inputs), the same
+//     select runs directly over the row in global memory.
+// Ties at the threshold key are broken by index with a second radix select
+// over ~index among the tied items, so the result is exact in every case.
+#pragma once
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace hsi {
+
+constexpr int SEL_THREADS = 1024;
+constexpr int SEL_WARPS = SEL_THREADS / 32;
+constexpr int SEL_CAP = 16384;      // items held in shared memory by one CTA
+constexpr int SEL_MAXK = 4096;      // largest k (top-k) or n_keep (pool)
+constexpr int HIST_BINS = 4096;     // top 12 bits of the key
+constexpr int SCAN_THREADS = 512;
+constexpr int SCAN_CHUNK = 16384;   // items per CTA in the histogram / collect passes
+
+constexpr uint32_t KEY_POS_INF = 0xFF800000u;  // order_key(+inf)
+constexpr uint32_t KEY_NEG_INF = 0x007FFFFFu;  // order_key(-inf)
+
+enum : int { SEL_TOPK = 0, SEL_POOL = 1 };
+
+struct SelParams {
+    // items: item i of query b is src[b*ld + i], i < n_items(b)
+    const float* src;
+    int64_t ld;
+    const int32_t* n_src;  // [B]; n_items(b) = ceil(n_src[b] / div)
+    int32_t div;
+    int32_t B;
+    int32_t k;
+    int32_t mode;  // SEL_TOPK or SEL_POOL (pin the last item to +inf, drop -inf items)
+    // workspace
+    uint32_t* hist;      // [B][HIST_BINS]
+    uint32_t* cand_cnt;  // [B]
+    uint32_t* cand_key;  // [B][cap]
+    uint32_t* cand_idx;  // [B][cap]
+    int32_t cap;
+    // top-k outputs
+    const int32_t* block_ids;
+    int64_t ld_blocks;
+    int32_t block_size;
+    int32_t* out_idx;
+    float* out_val;
+    // pool outputs (block size = div)
+    int32_t* blk_out;  // [B][k]
+    int32_t* n_kept;
+    int32_t* n_pool;
+    uint32_t* bits;
+    int64_t ld_bits;
+};
+
+__device__ __forceinline__ int64_t sel_items(const SelParams& p, int b) {
+    const int64_t n = p.n_src[b];
+    return n <= 0 ? 0 : (n + p.div - 1) / p.div;
+}
+
+// Key of item i (n = item count); `ok` says whether the item is eligible.
+__device__ __forceinline__ uint32_t sel_key(const SelParams& p, int b, int64_t i, int64_t n, bool& ok) {
+    uint32_t key = order_key(p.src[(int64_t)b * p.ld + i]);
+    if (p.mode == SEL_POOL) {
+        if (i == n - 1) key = KEY_POS_INF;  // the block of the newest position
+        ok = key != KEY_NEG_INF;
+    } else {
+        ok = true;
+    }
+    return key;
+}
+
+// ------------------------------------------------------------ scan passes --
+
+__global__ void __launch_bounds__(SCAN_THREADS) sel_hist_kernel(SelParams p) {
+    __shared__ uint32_t sh[HIST_BINS];
+    const int b = blockIdx.y;
+    const int64_t n = sel_items(p, b);
+    const int64_t lo = (int64_t)blockIdx.x * SCAN_CHUNK;
+    if (lo >= n) return;
+    const int64_t hi = min(n, lo + SCAN_CHUNK);
+    for (int i = threadIdx.x; i < HIST_BINS; i += SCAN_THREADS) sh[i] = 0;
+    __syncthreads();
+    for (int64_t i = lo + threadIdx.x; i < hi; i += SCAN_THREADS) {
+        bool ok;
+        const uint32_t key = sel_key(p, b, i, n, ok);
+        if (ok) atomicAdd(&sh[key >> 20], 1u);
+    }
+    __syncthreads();
+    uint32_t* gh = p.hist + (int64_t)b * HIST_BINS;
+    for (int i = threadIdx.x; i < HIST_BINS; i += SCAN_THREADS)
+        if (sh[i]) atomicAdd(&gh[i], sh[i]);
+}
+
+// The largest bin t such that the items in bins >= t number at least k (0 if
+// there are fewer than k items). Whole block; SCAN_THREADS * 8 == HIST_BINS.
+__device__ uint32_t threshold_bin(const uint32_t* gh, int k, uint32_t* scratch /*SCAN_THREADS+1*/) {
+    static_assert(SCAN_THREADS * 8 == HIST_BINS, "bins per thread");
+    const int t = threadIdx.x;
+    uint32_t c[8];
+    uint32_t s = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        c[i] = gh[t * 8 + i];
+        s += c[i];
+    }
+    scratch[t] = s;
+    __syncthreads();
+    // suffix sums over threads, from the top (Hillis-Steele on the reversed order)
+    for (int off = 1; off < SCAN_THREADS; off <<= 1) {
+        const uint32_t add = (t + off < SCAN_THREADS) ? scratch[t + off] : 0u;
+        __syncthreads();
+        scratch[t] += add;
+        __syncthreads();
+    }
+    const uint32_t incl = scratch[t];      // items in bins >= t*8
+    const uint32_t excl = incl - s;        // items in bins >= t*8 + 8
+    __syncthreads();
+    if (t == 0) scratch[SCAN_THREADS] = 0;
+    __syncthreads();
+    if (excl < (uint32_t)k && incl >= (uint32_t)k) {
+        uint32_t run = excl;
+        for (int i = 7; i >= 0; --i) {
+            run += c[i];
+            if (run >= (uint32_t)k) {
+                scratch[SCAN_THREADS] = (uint32_t)(t * 8 + i);
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    return scratch[SCAN_THREADS];
+}
+
+__global__ void __launch_bounds__(SCAN_THREADS) sel_collect_kernel(SelParams p) {
+    __shared__ uint32_t scratch[SCAN_THREADS + 1];
+    const int b = blockIdx.y;
+    const int64_t n = sel_items(p, b);
+    const int64_t lo = (int64_t)blockIdx.x * SCAN_CHUNK;
+    if (lo >= n) return;
+    const int64_t hi = min(n, lo + SCAN_CHUNK);
+    const uint32_t thr = threshold_bin(p.hist + (int64_t)b * HIST_BINS, p.k, scratch);
+    const int lane = threadIdx.x & 31;
+    uint32_t* cnt = p.cand_cnt + b;
+    uint32_t* ck = p.cand_key + (int64_t)b * p.cap;
+    uint32_t* ci = p.cand_idx + (int64_t)b * p.cap;
+    for (int64_t base = lo; base < hi; base += SCAN_THREADS) {
+        const int64_t i = base + threadIdx.x;
+        bool ok = false;
+        uint32_t key = 0;
+        if (i < hi) key = sel_key(p, b, i, n, ok);
+        const bool take = ok && (key >> 20) >= thr;
+        const uint32_t m = __ballot_sync(0xFFFFFFFFu, take);
+        if (m) {
+            uint32_t pos0 = 0;
+            if (lane == 0) pos0 = atomicAdd(cnt, (uint32_t)__popc(m));
+            pos0 = __shfl_sync(0xFFFFFFFFu, pos0, 0);
+            if (take) {
+                const uint32_t pos = pos0 + __popc(m & ((1u << lane) - 1u));
+                if (pos < (uint32_t)p.cap) {
+                    ck[pos] = key;
+                    ci[pos] = (uint32_t)i;
+                }
+            }
+        }
+    }
+}
+
+// -------------------------------------------------------- block select --
+
+struct SelSmem {
+    uint32_t whist[SEL_WARPS][256];
+    uint32_t hsum[256];
+    unsigned long long win[SEL_MAXK];
+    uint32_t bcast[8];
+    uint32_t keys[SEL_CAP];
+    uint32_t idx[SEL_CAP];
+};
+
+// Sources of items for the block select.
+struct SmemSrc {  // keys and indices in shared memory
+    const uint32_t* keys;
+    const uint32_t* ids;
+    int64_t n;
+    __device__ uint32_t key(int64_t j, bool& ok) const {
+        ok = true;
+        return keys[j];
+    }
+    __device__ uint32_t idx(int64_t j) const { return ids[j]; }
+};
+struct RowSrc {  // the row in global memory
+    const SelParams* p;
+    int b;
+    int64_t n;
+    __device__ uint32_t key(int64_t j, bool& ok) const { return sel_key(*p, b, j, n, ok); }
+    __device__ uint32_t idx(int64_t j) const { return (uint32_t)j; }
+};
+
+// One radix pass: histogram of bits [shift, shift+8) over eligible items whose
+// (selector & mask) == prefix, then the digit holding the `need`-th largest.
+// sel = 0 selects on the key, sel = 1 on ~index among items with key == T.
+// Returns the digit; *above = items with a larger digit; *at = items at it;
+// *total = all counted items.
+template <class Src>
+__device__ uint32_t radix_pass(const Src& src, SelSmem& s, int sel, uint32_t T, uint32_t prefix, uint32_t mask,
+                               int shift, uint32_t need, uint32_t* above, uint32_t* at, uint32_t* total) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int i = tid; i < SEL_WARPS * 256; i += SEL_THREADS) (&s.whist[0][0])[i] = 0;
+    __syncthreads();
+    for (int64_t j = tid; j < src.n; j += SEL_THREADS) {
+        bool ok;
+        const uint32_t key = src.key(j, ok);
+        if (!ok) continue;
+        uint32_t v;
+        if (sel == 0) {
+            v = key;
+        } else {
+            if (key != T) continue;
+            v = ~src.idx(j);
+        }
+        if ((v & mask) == prefix) atomicAdd(&s.whist[warp][(v >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (tid < 256) {
+        uint32_t t = 0;
+#pragma unroll 8
+        for (int w = 0; w < SEL_WARPS; ++w) t += s.whist[w][tid];
+        s.hsum[tid] = t;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t c[8], sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            c[i] = s.hsum[lane * 8 + i];
+            sum += c[i];
+        }
+        // inclusive suffix over lanes (lane 31 holds the top bins)
+        uint32_t suf = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t o = __shfl_down_sync(0xFFFFFFFFu, suf, off);
+            if (lane + off < 32) suf += o;
+        }
+        const uint32_t tot = __shfl_sync(0xFFFFFFFFu, suf, 0);
+        const uint32_t excl = suf - sum;
+        if (lane == 0) {
+            s.bcast[0] = 0;
+            s.bcast[1] = 0;
+            s.bcast[2] = 0;
+            s.bcast[3] = tot;
+        }
+        __syncwarp();
+        if (excl < need && suf >= need) {
+            uint32_t run = excl;
+            for (int i = 7; i >= 0; --i) {
+                if (run + c[i] >= need) {
+                    s.bcast[0] = (uint32_t)(lane * 8 + i);
+                    s.bcast[1] = run;
+                    s.bcast[2] = c[i];
+                    break;
+                }
+                run += c[i];
+            }
+        }
+    }
+    __syncthreads();
+    const uint32_t d = s.bcast[0];
+    *above = s.bcast[1];
+    *at = s.bcast[2];
+    *total = s.bcast[3];
+    __syncthreads();
+    return d;
+}
+
+// Sort s.win[0 .. count) descending (bitonic over the next power of two).
+__device__ void sort_desc(SelSmem& s, int count) {
+    int m = 1;
+    while (m < count) m <<= 1;
+    for (int i = count + threadIdx.x; i < m; i += SEL_THREADS) s.win[i] = 0ull;
+    __syncthreads();
+    for (int size = 2; size <= m; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < m / 2; i += SEL_THREADS) {
+                const int lo = 2 * i - (i & (stride - 1));
+                const int hi = lo + stride;
+                const bool desc = ((lo & size) == 0);
+                const unsigned long long a = s.win[lo], c = s.win[hi];
+                if ((a < c) == desc) {
+                    s.win[lo] = c;
+                    s.win[hi] = a;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// Select the k best eligible items of src into s.win as (key << 32 | ~idx)
+// (top-k) or (~idx) (pool: ascending ids after the descending sort), sorted.
+// Returns the number selected, min(k, eligible).
+template <class Src>
+__device__ int block_select(const Src& src, SelSmem& s, int k, bool ids_only) {
+    uint32_t above, at, total;
+    uint32_t prefix = 0, mask = 0, need = (uint32_t)k;
+    // pass 0 also counts the eligible items
+    uint32_t d = radix_pass(src, s, 0, 0, 0, 0, 24, need, &above, &at, &total);
+    const bool take_all = total <= (uint32_t)k;
+    uint32_t T = 0, T2 = 0;
+    bool tie_split = false;
+    if (!take_all) {
+        need -= above;
+        prefix = d << 24;
+        mask = 0xFF000000u;
+        for (int shift = 16; shift >= 0; shift -= 8) {
+            d = radix_pass(src, s, 0, 0, prefix, mask, shift, need, &above, &at, &total);
+            need -= above;
+            prefix |= d << shift;
+            mask |= 0xFFu << shift;
+        }
+        T = prefix;           // the k-th largest key
+        tie_split = at > need;  // more items equal T than places left
+        if (tie_split) {
+            uint32_t p2 = 0, m2 = 0, need2 = need;
+            for (int shift = 24; shift >= 0; shift -= 8) {
+                d = radix_pass(src, s, 1, T, p2, m2, shift, need2, &above, &at, &total);
+                need2 -= above;
+                p2 |= d << shift;
+                m2 |= 0xFFu << shift;
+            }
+            T2 = p2;  // ~index of the last tied item taken
+        }
+    }
+    if (threadIdx.x == 0) s.bcast[4] = 0;
+    __syncthreads();
+    for (int64_t j = threadIdx.x; j < src.n; j += SEL_THREADS) {
+        bool ok;
+        const uint32_t key = src.key(j, ok);
+        if (!ok) continue;
+        bool take;
+        if (take_all) {
+            take = true;
+        } else if (key != T) {
+            take = key > T;
+        } else {
+            take = !tie_split || (~src.idx(j)) >= T2;
+        }
+        if (take) {
+            const uint32_t pos = atomicAdd(&s.bcast[4], 1u);
+            const uint32_t ni = ~src.idx(j);
+            s.win[pos] = ids_only ? (unsigned long long)ni : (((unsigned long long)key << 32) | ni);
+        }
+    }
+    __syncthreads();
+    const int count = (int)s.bcast[4];
+    __syncthreads();
+    sort_desc(s, count);
+    return count;
+}
+
+__global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    SelSmem& s = *reinterpret_cast<SelSmem*>(smem_raw);
+    const int b = blockIdx.x;
+    const int64_t n = sel_items(p, b);
+    int count;
+    const bool ids_only = p.mode == SEL_POOL;
+    if (n <= SEL_CAP) {
+        for (int64_t j = threadIdx.x; j < n; j += SEL_THREADS) {
+            bool ok;
+            const uint32_t key = sel_key(p, b, j, n, ok);
+            s.keys[j] = ok ? key : 0u;  // key 0 is never a real key (it is a NaN pattern)
+            s.idx[j] = (uint32_t)j;
+        }
+        __syncthreads();
+        struct Filt : SmemSrc {
+            __device__ uint32_t key(int64_t j, bool& ok) const {
+                ok = keys[j] != 0u;
+                return keys[j];
+            }
+        };
+        Filt src;
+        src.keys = s.keys;
+        src.ids = s.idx;
+        src.n = n;
+        count = block_select(src, s, p.k, ids_only);
+    } else {
+        const uint32_t c = p.cand_cnt[b];
+        if (c <= (uint32_t)p.cap && c <= (uint32_t)SEL_CAP) {
+            const uint32_t* ck = p.cand_key + (int64_t)b * p.cap;
+            const uint32_t* ci = p.cand_idx + (int64_t)b * p.cap;
+            for (uint32_t j = threadIdx.x; j < c; j += SEL_THREADS) {
+                s.keys[j] = ck[j];
+                s.idx[j] = ci[j];
+            }
+            __syncthreads();
+            SmemSrc src{s.keys, s.idx, (int64_t)c};
+            count = block_select(src, s, p.k, ids_only);
+        } else {
+            RowSrc src{&p, b, n};
+            count = block_select(src, s, p.k, ids_only);
+        }
+    }
+    if (p.mode == SEL_TOPK) {
+        int32_t* oi = p.out_idx + (int64_t)b * p.k;
+        float* ov = p.out_val + (int64_t)b * p.k;
+        for (int t = threadIdx.x; t < p.k; t += SEL_THREADS) {
+            if (t < count) {
+                const unsigned long long w = s.win[t];
+                int64_t i = (int64_t)(uint32_t)~(uint32_t)(w & 0xFFFFFFFFull);
+                if (p.block_ids) {
+                    const int64_t blk = p.block_ids[(int64_t)b * p.ld_blocks + i / p.block_size];
+                    i = blk * p.block_size + i % p.block_size;
+                }
+                oi[t] = (int32_t)i;
+                ov[t] = key_to_float((uint32_t)(w >> 32));
+            } else {
+                oi[t] = -1;
+                ov[t] = __uint_as_float(0xFF800000u);
+            }
+        }
+    } else {
+        // pool: ascending block ids, the visible-position count and the bit table
+        const int bs = p.div;
+        const int64_t n_vis = p.n_src[b];
+        int32_t* bo = p.blk_out + (int64_t)b * p.k;
+        if (threadIdx.x == 0) s.bcast[5] = 0;
+        uint32_t* bits = p.bits ? p.bits + (int64_t)b * p.ld_bits : nullptr;
+        if (bits) {
+            const int64_t words = (n_vis + 31) / 32;
+            for (int64_t wd = threadIdx.x; wd < words; wd += SEL_THREADS) bits[wd] = 0u;
+        }
+        __syncthreads();
+        for (int t = threadIdx.x; t < p.k; t += SEL_THREADS) {
+            if (t < count) {
+                const int64_t blk = (int64_t)(uint32_t)~(uint32_t)(s.win[t] & 0xFFFFFFFFull);
+                bo[t] = (int32_t)blk;
+                const int64_t a = blk * bs, e = min(n_vis, a + bs);
+                atomicAdd(&s.bcast[5], (uint32_t)(e - a));
+                if (bits) {
+                    for (int64_t pos = a; pos < e;) {
+                        const int64_t wd = pos >> 5;
+                        const int64_t we = min(e, (wd + 1) << 5);
+                        const int lo = (int)(pos & 31), cnt = (int)(we - pos);
+                        const uint32_t m = (cnt == 32) ? 0xFFFFFFFFu : (((1u << cnt) - 1u) << lo);
+                        atomicOr(&bits[wd], m);
+                        pos = we;
+                    }
+                }
+            } else {
+                bo[t] = -1;
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            p.n_kept[b] = count;
+            p.n_pool[b] = (int32_t)s.bcast[5];
+        }
+    }
+}
+
+// Block maxima of a score row: bmax[b][j] = max of scores[b][j*bs .. j*bs+bs)
+// over visible positions (< n_visible[b]), for j < ceil(n_visible[b]/bs).
+__global__ void block_max_kernel(const float* scores, int64_t ld, const int32_t* n_vis, int32_t bs, float* bmax,
+                                 int64_t ldb) {
+    const int b = blockIdx.y;
+    const int64_t n = n_vis[b];
+    const int64_t nblk = (n + bs - 1) / bs;
+    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= nblk) return;
+    const float* row = scores + (int64_t)b * ld;
+    float m = __uint_as_float(0xFF800000u);
+    const int64_t a = j * bs, e = min(n, a + bs);
+    for (int64_t i = a; i < e; ++i) m = fmaxf(m, row[i]);
+    bmax[(int64_t)b * ldb + j] = m;
+}
+
+}  // namespace hsi

@@ -1,0 +1,72 @@
+"""Shared set-up for the GPU parity tests: seeded inputs pushed through both the
+CUDA path (via the C ABI) and the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import inputs
+import oracle
+
+import long_context_decode_lightning_gb300 as hsi
+
+DEV = "cuda"
+
+
+def dev_bf16(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(DEV)
+
+
+def gpu_quantize(x_bf16: np.ndarray, n_tensors: int, rpt: int, signs, mode=0, g=None):
+    x = dev_bf16(x_bf16.reshape(n_tensors * rpt, 128))
+    rec = torch.empty(n_tensors * hsi.n_records(rpt) * hsi.REC_BYTES, dtype=torch.uint8, device=DEV)
+    gt = torch.empty(n_tensors, dtype=torch.float32, device=DEV) if g is None else \
+        torch.tensor(g, dtype=torch.float32, device=DEV)
+    hsi.quantize_nvfp4(x, n_tensors, rpt, signs, gt, rec, mode=mode)
+    return rec, gt
+
+
+class Caches:
+    """K caches of several sequences in one buffer of block records."""
+
+    def __init__(self, wl: inputs.Workload, layer: int, seqs, lengths):
+        self.signs = wl.signs()
+        self.lengths = list(lengths)
+        self.rec_off = []
+        self.host_rec, self.host_g = [], []
+        parts, gs = [], []
+        off = 0
+        for s, n in zip(seqs, lengths):
+            kb = wl.k_bf16(layer, s, rows=n)
+            rec, g = gpu_quantize(kb, 1, n, self.signs)
+            parts.append(rec)
+            gs.append(g)
+            self.rec_off.append(off)
+            off += hsi.n_records(n)
+            self.host_rec.append(kb)
+        self.k_rec = torch.cat(parts)
+        self.g = torch.cat(gs)
+
+    def oracle_rec(self, i):
+        rec, g = oracle.quantize(self.host_rec[i], self.signs)
+        return rec, g
+
+
+def gpu_queries(wl: inputs.Workload, layer: int, queries):
+    qb = np.concatenate([wl.q_bf16(layer, b) for b in queries])
+    rec, g = gpu_quantize(qb, len(queries), 32, wl.signs())
+    w = torch.from_numpy(np.stack([wl.w(layer, b) for b in queries])).to(DEV)
+    return rec, g, w
+
+
+def oracle_query(wl, layer, b):
+    rec, g = oracle.quantize(wl.q_bf16(layer, b), wl.signs())
+    return rec, g, wl.w(layer, b)
+
+
+def i32(v):
+    return torch.tensor(v, dtype=torch.int32, device=DEV)
+
+
+def i64(v):
+    return torch.tensor(v, dtype=torch.int64, device=DEV)

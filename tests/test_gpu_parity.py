@@ -1,0 +1,266 @@
+"""Parity of the CUDA path (through the C ABI) with the oracle, stage by stage.
+
+Bars: quantisation bit-exact; scores within
+|d| <= 1e-4 * sum_j |w_j| * sum_d |qhat_jd khat_d| (scales applied) per pair;
+top-k, pool and Reindex top-k bit-exact when fed the same fp32 scores.
+"""
+import numpy as np
+import pytest
+import torch
+
+import inputs
+import oracle
+from cases import DEV, Caches, gpu_queries, gpu_quantize, i32, i64, oracle_query
+
+import long_context_decode_lightning_gb300 as hsi
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    hsi.build()
+    hsi.device_check()
+    yield
+    assert hsi.device_error() == 0
+
+
+# ---------------------------------------------------------------- quantise --
+
+@pytest.mark.parametrize("rows,tensors", [(1, 1), (7, 3), (32, 5), (1000, 2), (4099, 1)])
+def test_quantize_bit_exact(rows, tensors):
+    wl = inputs.workload(0)
+    s = wl.signs()
+    x = inputs.normal_bf16(11, 77, tensors * rows * 128).reshape(tensors * rows, 128)
+    rec, g = gpu_quantize(x, tensors, rows, s)
+    nrec = hsi.n_records(rows)
+    got = rec.cpu().numpy().reshape(tensors, nrec * 576)
+    gg = g.cpu().numpy()
+    for t in range(tensors):
+        ref, gr = oracle.quantize(x[t * rows:(t + 1) * rows], s)
+        assert np.float32(gr) == gg[t]
+        assert np.array_equal(got[t], ref), f"tensor {t}: {np.flatnonzero(got[t] != ref)[:10]}"
+
+
+def test_quantize_mode1_and_extremes():
+    s = np.where(np.arange(128) % 3 == 0, -1, 1).astype(np.int8)
+    rng = np.random.default_rng(3)
+    f = (rng.standard_normal((64, 128)) * np.exp(rng.uniform(-20, 20, (64, 1)))).astype(np.float32)
+    f[5] = 0.0
+    f[6, :] = 1e-30
+    x = (f.view(np.uint32) >> 16).astype(np.uint16)
+    rec, g = gpu_quantize(x, 1, 64, s)
+    ref, gr = oracle.quantize(x, s)
+    assert np.array_equal(rec.cpu().numpy(), ref)
+    rec1, _ = gpu_quantize(x, 1, 64, s, mode=1, g=[gr * 0.5])
+    ref1, _ = oracle.quantize(x, s, g=np.float32(gr * 0.5))
+    assert np.array_equal(rec1.cpu().numpy(), ref1)
+
+
+# ------------------------------------------------------------------- score --
+
+def _score_case(wl, lengths, layer=0):
+    B = len(lengths)
+    caches = Caches(wl, layer, range(B), lengths)
+    q_rec, g_q, w = gpu_queries(wl, layer, range(B))
+    maxv = max(lengths)
+    scores = torch.full((B, maxv), float("nan"), device=DEV)
+    bmax = torch.full((B, hsi.n_records(maxv)), float("nan"), device=DEV)
+    hsi.score_full(q_rec, g_q, w, caches.k_rec, caches.g, i64(caches.rec_off), i32(lengths), B, maxv, scores,
+                   block_max=bmax)
+    assert hsi.device_error() == 0
+    return caches, scores.cpu().numpy(), bmax.cpu().numpy()
+
+
+@pytest.mark.parametrize("lengths", [[1], [7], [128], [129], [5000], [300, 1, 4097, 2048, 131]])
+def test_score_full_within_tolerance(lengths):
+    wl = inputs.workload(1)
+    caches, sg, bm = _score_case(wl, lengths)
+    for b, n in enumerate(lengths):
+        krec, gk = caches.oracle_rec(b)
+        qrec, gq, w = oracle_query(wl, 0, b)
+        ref, tol = oracle.score_rows(qrec, gq, w, krec, gk, np.arange(n))
+        d = np.abs(sg[b, :n].astype(np.float64) - ref)
+        assert np.all(d <= tol), f"query {b}: worst {np.max(d / tol):.3g} x tol"
+        assert np.all(np.isnan(sg[b, n:])), "wrote past n_visible"
+        nb = hsi.n_records(n)
+        exp = np.array([sg[b, 8 * j:min(n, 8 * j + 8)].max() for j in range(nb)], dtype=np.float32)
+        assert np.array_equal(bm[b, :nb], exp)
+
+
+def test_score_full_pairs_scored_mac_identity():
+    # special case: one head weighted 1, others 0 -> ReLU of one decoded dot product
+    wl = inputs.workload(0)
+    n = 777
+    caches = Caches(wl, 0, [0], [n])
+    q_rec, g_q, _ = gpu_queries(wl, 0, [0])
+    krec, gk = caches.oracle_rec(0)
+    qrec_o, gq_o, _ = oracle_query(wl, 0, 0)
+    qd = oracle.decode_rows(qrec_o, 32, gq_o)
+    kd = oracle.decode_rows(krec, n, gk)
+    for j in (0, 17, 31):
+        w = torch.zeros(1, 32, device=DEV)
+        w[0, j] = 1.0
+        scores = torch.empty(1, n, device=DEV)
+        hsi.score_full(q_rec, g_q, w, caches.k_rec, caches.g, i64([0]), i32([n]), 1, n, scores)
+        ref = np.maximum(kd @ qd[j], 0.0) / 128.0
+        tol = 1e-4 * (np.abs(kd) @ np.abs(qd[j])) / 128.0
+        assert np.all(np.abs(scores.cpu().numpy()[0] - ref) <= tol)
+
+
+# ------------------------------------------------------------------- top-k --
+
+def _gpu_topk(scores_np, n_valid, k, block_ids=None, block_size=8):
+    B, ld = scores_np.shape
+    s = torch.from_numpy(np.ascontiguousarray(scores_np)).to(DEV)
+    idx = torch.empty(B, k, dtype=torch.int32, device=DEV)
+    val = torch.empty(B, k, dtype=torch.float32, device=DEV)
+    bid = None if block_ids is None else torch.from_numpy(block_ids).to(DEV)
+    hsi.topk(s, i32(n_valid), B, max(n_valid), k, idx, val, block_ids=bid, block_size=block_size)
+    assert hsi.device_error() == 0
+    return idx.cpu().numpy(), val.cpu().numpy()
+
+
+@pytest.mark.parametrize("n,k", [(1, 512), (100, 512), (511, 512), (512, 512), (513, 512), (16384, 512),
+                                 (16385, 512), (100000, 512), (300000, 2048), (5000, 1)])
+def test_topk_bit_exact(n, k):
+    rng = np.random.default_rng(n + k)
+    sc = rng.standard_normal((3, n)).astype(np.float32) * 4
+    sc[1, ::7] = sc[1, min(3, n - 1)]  # many exact ties
+    sc[2, : n // 2] = -0.0
+    sc[2, n // 2:] = 0.0
+    gi, gv = _gpu_topk(sc, [n, n, n], k)
+    for b in range(3):
+        ri, rv = oracle.topk(sc[b], n, k)
+        assert np.array_equal(gi[b], ri), f"row {b}"
+        assert np.array_equal(gv[b][ri >= 0], rv[ri >= 0])
+
+
+def test_topk_ragged_rows_and_all_equal():
+    n = [1, 20000, 40000, 3]
+    ld = max(n)
+    sc = np.full((4, ld), 2.5, dtype=np.float32)
+    gi, _ = _gpu_topk(sc, n, 512)
+    for b in range(4):
+        ri, _ = oracle.topk(sc[b], n[b], 512)
+        assert np.array_equal(gi[b], ri)
+
+
+def test_topk_with_block_map():
+    rng = np.random.default_rng(5)
+    ids = np.sort(rng.choice(100000, 2048, replace=False)).astype(np.int32)[None, :]
+    ps = rng.standard_normal((1, 2048 * 8)).astype(np.float32)
+    npool = 2048 * 8 - 5
+    gi, gv = _gpu_topk(ps, [npool], 512, block_ids=ids)
+    ri, rv = oracle.topk_pool(ps[0], npool, ids[0])
+    assert np.array_equal(gi[0], ri) and np.array_equal(gv[0], rv)
+
+
+# -------------------------------------------------------------------- pool --
+
+def _gpu_pool(scores_np, n_vis, bs=8, keep=2048, use_bmax=False):
+    B, ld = scores_np.shape
+    s = torch.from_numpy(np.ascontiguousarray(scores_np)).to(DEV)
+    ids = torch.empty(B, keep, dtype=torch.int32, device=DEV)
+    nk = torch.empty(B, dtype=torch.int32, device=DEV)
+    npool = torch.empty(B, dtype=torch.int32, device=DEV)
+    bits = torch.empty(B, (ld + 31) // 32, dtype=torch.int32, device=DEV)
+    if use_bmax:
+        nb = (ld + bs - 1) // bs
+        bm = np.full((B, nb), -np.inf, dtype=np.float32)
+        for b in range(B):
+            for j in range((n_vis[b] + bs - 1) // bs):
+                bm[b, j] = scores_np[b, j * bs:min(n_vis[b], j * bs + bs)].max()
+        hsi.candidate_pool(i32(n_vis), B, max(n_vis), ids, nk, npool, block_max=torch.from_numpy(bm).to(DEV),
+                           block_size=bs, n_keep=keep, pool_bits=bits)
+    else:
+        hsi.candidate_pool(i32(n_vis), B, max(n_vis), ids, nk, npool, scores=s, block_size=bs, n_keep=keep,
+                           pool_bits=bits)
+    assert hsi.device_error() == 0
+    return ids.cpu().numpy(), nk.cpu().numpy(), npool.cpu().numpy(), bits.cpu().numpy().view(np.uint32)
+
+
+def _bits_to_mask(bits_row, n):
+    return ((bits_row[np.arange(n) // 32] >> (np.arange(n) % 32)) & 1).astype(np.uint8)
+
+
+@pytest.mark.parametrize("n_vis", [[1], [9], [16384], [16385], [20001, 131072, 50], [1048576]])
+@pytest.mark.parametrize("use_bmax", [False, True])
+def test_pool_bit_exact(n_vis, use_bmax):
+    rng = np.random.default_rng(sum(n_vis))
+    ld = max(n_vis)
+    sc = rng.standard_normal((len(n_vis), ld)).astype(np.float32)
+    if len(n_vis) > 1:
+        sc[1, ::3] = 1.0  # ties between block maxima
+    gi, gk, gp, gb = _gpu_pool(sc, n_vis, use_bmax=use_bmax)
+    for b, n in enumerate(n_vis):
+        ri, rk, rp, rm = oracle.pool(sc[b], n)
+        assert gk[b] == rk and gp[b] == rp
+        assert np.array_equal(gi[b][:rk], ri[:rk]) and (gi[b][rk:] == -1).all()
+        assert np.array_equal(_bits_to_mask(gb[b], n), rm)
+
+
+@pytest.mark.parametrize("bs,keep", [(4, 6), (1, 5), (3, 100), (8, 1)])
+def test_pool_small_block_and_keep(bs, keep):
+    rng = np.random.default_rng(bs * 100 + keep)
+    n_vis = [61, 1, 200, 997]
+    sc = rng.choice([-1.0, 0.0, 0.5, 2.0], (4, 997)).astype(np.float32)
+    gi, gk, gp, gb = _gpu_pool(sc, n_vis, bs=bs, keep=keep)
+    for b, n in enumerate(n_vis):
+        ri, rk, rp, rm = oracle.pool(sc[b], n, bs, keep)
+        assert gk[b] == rk and gp[b] == rp
+        assert np.array_equal(gi[b][:rk], ri[:rk])
+        assert np.array_equal(_bits_to_mask(gb[b], n), rm)
+
+
+# ------------------------------------------------------------ pooled score --
+
+@pytest.mark.parametrize("lengths", [[20000], [3, 16384, 16391, 70001]])
+def test_score_pool_within_tolerance_and_reindex_topk(lengths):
+    wl = inputs.workload(1)
+    B = len(lengths)
+    caches, sg, _ = _score_case(wl, lengths, layer=0)
+    gi, gk, gp, _ = _gpu_pool(sg, lengths)
+    q_rec, g_q, w = gpu_queries(wl, 1, range(B))
+    ps = torch.full((B, 2048 * 8), float("nan"), device=DEV)
+    hsi.score_pool(q_rec, g_q, w, caches.k_rec, caches.g, i64(caches.rec_off), i32(lengths),
+                   torch.from_numpy(gi).to(DEV), i32(gk.tolist()), 2048, B, ps)
+    assert hsi.device_error() == 0
+    psg = ps.cpu().numpy()
+    for b, n in enumerate(lengths):
+        krec, gkk = caches.oracle_rec(b)
+        qrec, gq, wq = oracle_query(wl, 1, b)
+        ref, _ = oracle.score_pool(qrec, gq, wq, krec, gkk, n, gi[b], gk[b])
+        m = int(gp[b])
+        pos = np.array([gi[b][i // 8] * 8 + i % 8 for i in range(m)])
+        _, tol = oracle.score_rows(qrec, gq, wq, krec, gkk, pos)
+        assert np.all(np.abs(psg[b, :m] - ref[:m]) <= tol)
+        assert np.isneginf(psg[b, m:8 * gk[b]]).all()
+        assert np.isnan(psg[b, 8 * gk[b]:]).all()
+    # Reindex top-512 on the GPU's pooled scores, bit-exact, global positions
+    ri_g, _ = _gpu_topk(psg, gp.tolist(), 512, block_ids=gi)
+    for b in range(B):
+        ri, _ = oracle.topk_pool(psg[b], int(gp[b]), gi[b])
+        assert np.array_equal(ri_g[b], ri)
+
+
+# ---------------------------------------------------------------- end to end --
+
+def test_end_to_end_topk_sets_match_except_near_ties():
+    """Oracle's own path vs the GPU path: sets agree except positions whose
+    oracle score is within the tolerance of the k-th score."""
+    wl = inputs.workload(0)
+    n = 32768
+    caches, sg, _ = _score_case(wl, [n])
+    gidx, _ = _gpu_topk(sg, [n], 512)
+    krec, gk = caches.oracle_rec(0)
+    qrec, gq, w = oracle_query(wl, 0, 0)
+    so, _ = oracle.score_full(qrec, gq, w, krec, gk, n)
+    _, tol = oracle.score_rows(qrec, gq, w, krec, gk, np.arange(n))
+    oidx, oval = oracle.topk(so, n, 512)
+    kth = oval[-1]
+    diff = set(gidx[0].tolist()) ^ set(oidx.tolist())
+    for p in diff:
+        assert abs(so[p] - kth) <= 2 * tol[p], p
