@@ -1,0 +1,465 @@
+#!/usr/bin/env python3
+"""Throughput of the Hierarchical Sparse Indexer decode hot path on GB300.
+
+One step = one pass of the whole path over the resident workload:
+  per Full layer: quantise q (NVFP4), score every visible key (tcgen05 FP4),
+                  exact top-512;
+  then (decoder workloads): the candidate pool from the fused block maxima
+                  (blocks of 8, keep 2048, newest pinned, boolean bit table),
+                  and per Reindex layer: quantise q, score only the pooled
+                  keys (whole 576-byte blocks gathered), exact top-512.
+The default workload is 64 decode queries at 1,048,576 visible keys each with
+4 Reindex layers. K caches are generated from the seeded recipe, quantised on
+the GPU and stay resident (4.83 GB > L2, so no L2 flush is needed).
+
+Output: one JSON line (rank 0). `value` is (query, key) pairs scored per
+second over the whole job; `e2e` repeats the measurement with each step's
+inputs (bf16 q, w) copied from pinned host memory and its results (top-512
+indices and values of every layer) copied back inside the timed region.
+`--impl reference` times the CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import inputs  # noqa: E402
+
+METRIC = "indexer (query,key) pairs scored/s + top-512/s at 1M ctx; % FP4-TC/HBM roofline"
+UNIT = "pairs/s"
+K_TOP = 512
+REC = 576
+KEY_BYTES = 72  # NVFP4 indexer key: 64 B of E2M1 codes + 8 B of E4M3 scales
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "score_full_decode_b64_n1m.md")
+KERNEL_SOURCES = ["score.cuh", "ptx.cuh", "common.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["hsi", "reference"], default="hsi")
+    ap.add_argument("--workload", type=int, default=2, help="0..3 (see inputs.workload)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true", help="cudaProfilerStart/Stop around the timed steps")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers --
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "long_context_decode_lightning_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """dram bytes per launch of the scoring kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    try:
+        txt = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
+    if not m or not h or h.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(prefix="hsi_clocks_", suffix=".csv")
+        self.proc = None
+        self.gpu = gpu_index
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# -------------------------------------------------------- device workload --
+
+class DeviceWorkload:
+    """The workload resident on one GPU, and one step of the path over it."""
+
+    def __init__(self, wl: inputs.Workload, dev, log):
+        import torch
+
+        import long_context_decode_lightning_gb300 as hsi
+        self.torch, self.hsi, self.wl, self.dev = torch, hsi, wl, dev
+        B = wl.B
+        self.B = B
+        self.maxv = max(wl.n_visible)
+        signs = wl.signs()
+        seqs = sorted(set(wl.query_seq))
+        # --- K caches: one record buffer per Full layer, sequences back to back
+        self.k_rec, self.g_k = [], []
+        rec_off = {}
+        off = 0
+        for s in seqs:
+            rec_off[s] = off
+            off += hsi.n_records(wl.seq_len[s])
+        t0 = time.time()
+        stage = [torch.empty(max(wl.seq_len) * 128, dtype=torch.int16).pin_memory() for _ in range(2)]
+        stage_dev = [torch.empty(max(wl.seq_len) * 128, dtype=torch.int16, device=dev) for _ in range(2)]
+        done = [torch.cuda.Event(), torch.cuda.Event()]
+        qws = hsi.workspace(hsi.WS_QUANTIZE, 1, 0, device=dev)
+        i = 0
+        for layer in range(wl.full_layers):
+            krec = torch.empty(off * REC, dtype=torch.uint8, device=dev)
+            gseq = torch.empty(len(seqs), dtype=torch.float32, device=dev)
+            for si, s in enumerate(seqs):
+                n = wl.seq_len[s]
+                j = i % 2
+                done[j].synchronize()
+                host = stage[j][: n * 128].numpy().view(np.uint16)
+                inputs.normal_bf16(wl.seed, inputs.tensor_id(inputs.KIND_K, layer, s), n * 128, out=host)
+                stage_dev[j][: n * 128].copy_(stage[j][: n * 128], non_blocking=True)
+                hsi.quantize_nvfp4(stage_dev[j][: n * 128].view(n, 128), 1, n, signs, gseq[si:si + 1],
+                                   krec[rec_off[s] * REC:(rec_off[s] + hsi.n_records(n)) * REC], ws=qws)
+                done[j].record()
+                i += 1
+            self.k_rec.append(krec)
+            self.g_k.append(torch.stack([gseq[seqs.index(s)] for s in wl.query_seq]).contiguous())
+        torch.cuda.synchronize()
+        del stage, stage_dev
+        log(f"K caches generated and quantised in {time.time() - t0:.1f} s ({off * REC * wl.full_layers / 1e9:.2f} GB)")
+        self.k_off = torch.tensor([rec_off[s] for s in wl.query_seq], dtype=torch.int64, device=dev)
+        self.n_vis = torch.tensor(wl.n_visible, dtype=torch.int32, device=dev)
+        # --- per-step inputs: bf16 q and fp32 w of every layer, one contiguous buffer
+        self.layers = wl.full_layers + (wl.reindex_layers if wl.build_pool else 0)
+        L = self.layers
+        q_host = np.stack([np.concatenate([wl.q_bf16(l, b) for b in range(B)]) for l in range(L)])  # [L][B*32][128]
+        w_host = np.stack([np.stack([wl.w(l, b) for b in range(B)]) for l in range(L)])  # [L][B][32]
+        self.q_bytes = q_host.nbytes
+        self.in_host = torch.empty(q_host.nbytes + w_host.nbytes, dtype=torch.uint8).pin_memory()
+        self.in_host[: q_host.nbytes].numpy()[:] = q_host.reshape(-1).view(np.uint8)
+        self.in_host[q_host.nbytes:].numpy()[:] = w_host.reshape(-1).view(np.uint8)
+        self.in_dev = self.in_host.to(dev)
+        self.q = self.in_dev[: q_host.nbytes].view(torch.int16).view(L, B * 32, 128)
+        self.w = self.in_dev[q_host.nbytes:].view(torch.float32).view(L, B, 32)
+        # --- outputs and scratch
+        self.q_rec = torch.empty(L, B * 4 * REC, dtype=torch.uint8, device=dev)
+        self.g_q = torch.empty(L, B, dtype=torch.float32, device=dev)
+        self.scores = torch.empty(B, self.maxv, dtype=torch.float32, device=dev)
+        self.bmax = torch.empty(B, hsi.n_records(self.maxv), dtype=torch.float32, device=dev)
+        self.out_dev = torch.empty(L * B * K_TOP * 8, dtype=torch.uint8, device=dev)
+        self.out_host = torch.empty_like(self.out_dev, device="cpu").pin_memory()
+        self.idx = self.out_dev[: L * B * K_TOP * 4].view(torch.int32).view(L, B, K_TOP)
+        self.val = self.out_dev[L * B * K_TOP * 4:].view(torch.float32).view(L, B, K_TOP)
+        self.ws_q = hsi.workspace(hsi.WS_QUANTIZE, B, 0, device=dev)
+        self.ws_topk = hsi.workspace(hsi.WS_TOPK, B, self.maxv, K_TOP, device=dev)
+        if wl.build_pool:
+            self.ids = torch.empty(B, wl.n_keep, dtype=torch.int32, device=dev)
+            self.nk = torch.empty(B, dtype=torch.int32, device=dev)
+            self.npool = torch.empty(B, dtype=torch.int32, device=dev)
+            self.bits = torch.empty(B, (self.maxv + 31) // 32, dtype=torch.int32, device=dev)
+            self.ws_pool = hsi.workspace(hsi.WS_POOL, B, self.maxv, 8, device=dev)
+            self.pool_scores = torch.empty(B, wl.n_keep * 8, dtype=torch.float32, device=dev)
+            self.ws_rtopk = hsi.workspace(hsi.WS_TOPK, B, wl.n_keep * 8, K_TOP, device=dev)
+        self.ev_score = []
+        self.pool_sum = None
+
+    def step(self, time_score=False):
+        hsi, wl, B = self.hsi, self.wl, self.B
+        torch = self.torch
+        signs = self.wl_signs if hasattr(self, "wl_signs") else None
+        if signs is None:
+            self.wl_signs = signs = wl.signs()
+        for l in range(wl.full_layers):
+            hsi.quantize_nvfp4(self.q[l], B, 32, signs, self.g_q[l], self.q_rec[l], ws=self.ws_q)
+            if time_score:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+            hsi.score_full(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[l], self.g_k[l], self.k_off, self.n_vis,
+                           B, self.maxv, self.scores, block_max=self.bmax if wl.build_pool else None)
+            if time_score:
+                e1.record()
+                self.ev_score.append((e0, e1))
+            hsi.topk(self.scores, self.n_vis, B, self.maxv, K_TOP, self.idx[l], self.val[l], ws=self.ws_topk)
+        if not wl.build_pool:
+            return
+        hsi.candidate_pool(self.n_vis, B, self.maxv, self.ids, self.nk, self.npool, block_max=self.bmax,
+                           block_size=wl.block_size, n_keep=wl.n_keep, pool_bits=self.bits, ws=self.ws_pool)
+        for r in range(wl.reindex_layers):
+            l = wl.full_layers + r
+            hsi.quantize_nvfp4(self.q[l], B, 32, signs, self.g_q[l], self.q_rec[l], ws=self.ws_q)
+            hsi.score_pool(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0], self.k_off, self.n_vis,
+                           self.ids, self.nk, wl.n_keep, B, self.pool_scores)
+            hsi.topk(self.pool_scores, self.npool, B, wl.n_keep * 8, K_TOP, self.idx[l], self.val[l],
+                     block_ids=self.ids, ws=self.ws_rtopk)
+
+    def step_e2e(self):
+        self.in_dev.copy_(self.in_host, non_blocking=True)
+        self.step()
+        self.out_host.copy_(self.out_dev, non_blocking=True)
+
+    def pairs_per_step(self):
+        full = self.wl.full_layers * int(sum(self.wl.n_visible))
+        pooled = 0
+        if self.wl.build_pool:
+            if self.pool_sum is None:
+                self.torch.cuda.synchronize()
+                self.pool_sum = int(self.npool.sum().item())
+            pooled = self.wl.reindex_layers * self.pool_sum
+        return full + pooled, full, pooled
+
+    def score_bytes_per_launch(self):
+        """Algorithmic bytes of one hsi_score_full launch: 72 B per visible key
+        read, 4 B per score and 4 B per block maximum written, q/w/scales read."""
+        n = int(sum(self.wl.n_visible))
+        nb = sum((v + 7) // 8 for v in self.wl.n_visible)
+        return n * KEY_BYTES + n * 4 + (nb * 4 if self.wl.build_pool else 0) + self.B * (4 * REC + 32 * 4 + 8)
+
+
+# ----------------------------------------------------------- CPU oracle --
+
+def oracle_sample_setup(wl: inputs.Workload, nq: int):
+    """Oracle inputs for the first nq queries (quantised by the oracle itself)."""
+    import oracle
+    signs = wl.signs()
+    L = wl.full_layers + (wl.reindex_layers if wl.build_pool else 0)
+
+    def prep(b):
+        s = wl.query_seq[b]
+        ks = [oracle.quantize(wl.k_bf16(l, s), signs) for l in range(wl.full_layers)]
+        qs = [oracle.quantize(wl.q_bf16(l, b), signs) + (wl.w(l, b),) for l in range(L)]
+        return ks, qs
+
+    return oracle.map_queries(prep, list(range(nq)), threads=nq)
+
+
+def oracle_query_step(wl: inputs.Workload, b: int, ks, qs):
+    """The whole path for one query on the oracle; returns pairs scored."""
+    import oracle
+    n = wl.n_visible[b]
+    pairs = 0
+    scores = None
+    for l in range(wl.full_layers):
+        qrec, gq, w = qs[l]
+        krec, gk = ks[l]
+        scores, _ = oracle.score_full(qrec, gq, w, krec, gk, n)
+        oracle.topk(scores, n, K_TOP)
+        pairs += n
+    if wl.build_pool:
+        ids, nk, npool, _ = oracle.pool(scores, n, wl.block_size, wl.n_keep, want_mask=True)
+        krec, gk = ks[0]
+        for r in range(wl.reindex_layers):
+            qrec, gq, w = qs[wl.full_layers + r]
+            ps, _ = oracle.score_pool(qrec, gq, w, krec, gk, n, ids, nk, wl.n_keep, wl.block_size)
+            oracle.topk_pool(ps, npool, ids, K_TOP, wl.block_size)
+            pairs += npool
+    return pairs
+
+
+def oracle_timed(wl, prepared, nq):
+    import oracle
+    t0 = time.perf_counter()
+    pairs = oracle.map_queries(lambda b: oracle_query_step(wl, b, *prepared[b]), list(range(nq)), threads=nq)
+    return sum(pairs), time.perf_counter() - t0
+
+
+def cpu_sample_size(wl: inputs.Workload):
+    return max(1, min(16, os.cpu_count() or 1, wl.B))
+
+
+# ------------------------------------------------------------------- main --
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    log = (lambda m: print(f"[bench] {m}", file=sys.stderr, flush=True)) if rank == 0 else (lambda m: None)
+    wl = inputs.workload(args.workload)
+    config = {"workload": wl.name, "queries": wl.B, "context": max(wl.n_visible), "full_layers": wl.full_layers,
+              "reindex_layers": wl.reindex_layers if wl.build_pool else 0, "k": K_TOP,
+              "block": wl.block_size if wl.build_pool else None, "keep": wl.n_keep if wl.build_pool else None,
+              "l2": "no flush: resident inputs exceed L2"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        nq = cpu_sample_size(wl)
+        log(f"oracle sample: {nq} queries of {wl.name}")
+        prepared = oracle_sample_setup(wl, nq)
+        for _ in range(args.warmup):
+            oracle_timed(wl, prepared, nq)
+        tot_pairs, tot_t = 0, 0.0
+        for _ in range(args.steps):
+            p, t = oracle_timed(wl, prepared, nq)
+            tot_pairs += p
+            tot_t += t
+        v = tot_pairs / tot_t
+        sample = f"{nq} of {wl.B} queries per step, full path per query, one thread per query"
+        print(json.dumps({"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * tot_t / args.steps,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": config,
+                          "cpu_baseline": {"value": v, "unit": UNIT, "cores": nq, "kind": "oracle", "sample": sample},
+                          "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+              flush=True)
+        return
+
+    import torch
+    import long_context_decode_lightning_gb300 as hsi
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hsi.build() if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    hsi.device_check()
+    W = DeviceWorkload(wl, dev, log)
+    for _ in range(args.warmup):
+        W.step()
+    torch.cuda.synchronize()
+    assert hsi.device_error() == 0, "device error during warm-up"
+    pairs, pairs_full, pairs_pool = W.pairs_per_step()
+    launches0 = hsi.kernel_launches()
+
+    def timed(fn, K, sync_each=False):
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            fn()
+            if sync_each:
+                torch.cuda.current_stream().synchronize()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    with ClockSampler(local) as clk:
+        if args.profile:
+            torch.cuda.profiler.start()
+        ms = timed(lambda: W.step(time_score=True), args.steps)
+        if args.profile:
+            torch.cuda.profiler.stop()
+    launches = hsi.kernel_launches() - launches0
+    assert hsi.device_error() == 0, "device error during the timed steps"
+    score_ms = float(np.mean([a.elapsed_time(b) for a, b in W.ev_score]))
+    # end to end: host inputs in, host results out, every step
+    for _ in range(2):
+        W.step_e2e()
+    ms_e2e = timed(W.step_e2e, args.steps, sync_each=True)
+    assert hsi.device_error() == 0, "device error during the end-to-end steps"
+
+    value = pairs * world * args.steps / (ms / 1e3)
+    value_e2e = pairs * world * args.steps / (ms_e2e / 1e3)
+    sel = W.B * W.layers * world * args.steps / (ms / 1e3)
+    peaks, peak_kind = measured_peaks()
+    bytes_launch = W.score_bytes_per_launch()
+    achieved = bytes_launch / (score_ms / 1e3) / 1e9
+    traffic = recorded_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, e4m3 block scales, fp32 accumulate)",
+        "data": "synthetic", "config": config,
+        "top512_selections_per_s": sel,
+        "pairs_per_step": {"full": pairs_full, "pooled": pairs_pool},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                     "frac": achieved / float(peaks["hbm_gbs"]), "traffic": traffic,
+                     "kernel": "hsi_score_full (score_kernel<1,false>)",
+                     "bytes_per_launch": bytes_launch, "ms_per_launch": score_ms,
+                     "peak_kind": f"{peak_kind} copy bandwidth"},
+        "e2e": {"value": value_e2e, "unit": UNIT, "h2d_bytes_per_step": int(W.in_host.numel()),
+                "d2h_bytes_per_step": int(W.out_host.numel()), "ms_per_step": ms_e2e / args.steps},
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        nq = cpu_sample_size(wl)
+        log(f"cpu baseline: oracle on {nq} queries")
+        prepared = oracle_sample_setup(wl, nq)
+        p, t = oracle_timed(wl, prepared, nq)
+        line["cpu_baseline"] = {"value": p / t, "unit": UNIT, "cores": nq, "kind": "oracle",
+                                "sample": f"{nq} of {wl.B} queries, whole path per query (one thread each), "
+                                          f"{t:.1f} s wall"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

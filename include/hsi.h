@@ -232,6 +232,10 @@ hsi_status hsi_device_check(void);
 /* A static English description of a status code. */
 const char* hsi_status_string(hsi_status status);
 
+/* Number of kernels this library has launched in this process (all devices,
+ * all streams), for tracing and launch accounting. */
+uint64_t hsi_kernel_launches(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -27,7 +27,8 @@ STATUS = {0: "HSI_OK", -1: "HSI_ERR_INVALID_ARG", -2: "HSI_ERR_UNSUPPORTED", -3:
 WS_QUANTIZE, WS_SCORE, WS_TOPK, WS_POOL = 0, 1, 2, 3
 
 EXPORTS = ["hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
-           "hsi_workspace_size", "hsi_device_error", "hsi_device_check", "hsi_status_string"]
+           "hsi_workspace_size", "hsi_device_error", "hsi_device_check", "hsi_status_string",
+           "hsi_kernel_launches"]
 
 
 class HsiError(RuntimeError):
@@ -71,6 +72,8 @@ def lib() -> ctypes.CDLL:
         L.hsi_device_check.argtypes = []
         L.hsi_status_string.argtypes = [ctypes.c_int]
         L.hsi_status_string.restype = ctypes.c_char_p
+        L.hsi_kernel_launches.argtypes = []
+        L.hsi_kernel_launches.restype = ctypes.c_uint64
         for name in ("hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
                      "hsi_device_error", "hsi_device_check"):
             getattr(L, name).restype = ctypes.c_int
@@ -104,6 +107,11 @@ def workspace(kind: int, B: int, max_n: int, k: int = 0, device="cuda") -> torch
     """A caller-owned scratch buffer for one call (256-byte aligned by torch)."""
     n = workspace_size(kind, B, max_n, k)
     return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
+def kernel_launches() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(lib().hsi_kernel_launches())
 
 
 def device_check():

@@ -2,6 +2,7 @@
 // kernel launches; all arithmetic of the path runs in the kernels included here.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -24,7 +25,13 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 hsi_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? HSI_OK : HSI_ERR_CUDA; }
 
-hsi_status launch_ok() { return cuda_ok(cudaGetLastError()); }
+std::atomic<uint64_t> g_launches{0};
+
+// Every kernel launch of the library is followed by this check.
+hsi_status launch_ok() {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_ok(cudaGetLastError());
+}
 
 int sm_count() {
     int dev = 0, n = 0;
@@ -125,6 +132,8 @@ const char* hsi_status_string(hsi_status st) {
     }
     return "unknown status";
 }
+
+uint64_t hsi_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 hsi_status hsi_device_check(void) {
     int dev = 0, major = 0, minor = 0;
