@@ -55,6 +55,7 @@ def parse():
     ap.add_argument("--workload", type=int, default=2, help="0..3 (see inputs.workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true", help="cudaProfilerStart/Stop around the timed steps")
+    ap.add_argument("--queries", type=int, default=0, help="use only the first N queries (profiling captures)")
     return ap.parse_args()
 
 
@@ -341,6 +342,10 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     log = (lambda m: print(f"[bench] {m}", file=sys.stderr, flush=True)) if rank == 0 else (lambda m: None)
     wl = inputs.workload(args.workload)
+    if args.queries:
+        wl.query_seq = wl.query_seq[: args.queries]
+        wl.n_visible = wl.n_visible[: args.queries]
+        wl.name += f"_first{args.queries}"
     config = {"workload": wl.name, "queries": wl.B, "context": max(wl.n_visible), "full_layers": wl.full_layers,
               "reindex_layers": wl.reindex_layers if wl.build_pool else 0, "k": K_TOP,
               "block": wl.block_size if wl.build_pool else None, "keep": wl.n_keep if wl.build_pool else None,

@@ -205,7 +205,8 @@ hsi_status hsi_candidate_pool(const float* scores, int64_t ld, const float* bloc
  * Slots i < 8 * n_kept[b] are written; the rest are left untouched. Each
  * pooled block is one 576-byte K record, fetched whole.
  *
- *  block_ids, n_kept: as written by hsi_candidate_pool with block_size 8.
+ *  block_ids, n_kept: as written by hsi_candidate_pool with block_size 8;
+ *          block_ids 16-byte aligned, n_keep a multiple of 32.
  *  pool_scores (dev) fp32 [B][ld], ld >= 8 * n_keep.
  *  ws      may be NULL.
  */
@@ -235,6 +236,25 @@ const char* hsi_status_string(hsi_status status);
 /* Number of kernels this library has launched in this process (all devices,
  * all streams), for tracing and launch accounting. */
 uint64_t hsi_kernel_launches(void);
+
+/*
+ * Calibration: the rooflines of the running GPU, measured with the same
+ * instructions the path uses (no counterpart on the pages; the report states
+ * these beside every roofline fraction).
+ *
+ * hsi_calib_read streams `bytes` of `buf` (dev, 16-byte aligned) once.
+ * method 0: 16-byte loads from every SM; method 1: one contiguous slice per SM
+ * through a ring of `stages` shared-memory buffers of `chunk` bytes filled by
+ * bulk copies (chunk a multiple of 16). Time it with events on `stream`.
+ * `sink` (dev) is a scratch counter that keeps the loads live.
+ *
+ * hsi_calib_mma issues `iters` back-to-back tcgen05.mma kind::mxf4nvf4 of
+ * M = 128, N = n (32, 64, 128 or 256), K = 64 per SM on shared-memory operands:
+ * 2 * 128 * n * 64 * iters FP4 flops per SM.
+ */
+hsi_status hsi_calib_read(const void* buf, size_t bytes, int method, int chunk, int stages,
+                          unsigned long long* sink, cudaStream_t stream);
+hsi_status hsi_calib_mma(int n, int iters, unsigned long long* sink, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

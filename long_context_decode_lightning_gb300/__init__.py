@@ -28,7 +28,7 @@ WS_QUANTIZE, WS_SCORE, WS_TOPK, WS_POOL = 0, 1, 2, 3
 
 EXPORTS = ["hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
            "hsi_workspace_size", "hsi_device_error", "hsi_device_check", "hsi_status_string",
-           "hsi_kernel_launches"]
+           "hsi_kernel_launches", "hsi_calib_read", "hsi_calib_mma"]
 
 
 class HsiError(RuntimeError):
@@ -72,10 +72,12 @@ def lib() -> ctypes.CDLL:
         L.hsi_device_check.argtypes = []
         L.hsi_status_string.argtypes = [ctypes.c_int]
         L.hsi_status_string.restype = ctypes.c_char_p
+        L.hsi_calib_read.argtypes = [vp, sz, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp]
+        L.hsi_calib_mma.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp]
         L.hsi_kernel_launches.argtypes = []
         L.hsi_kernel_launches.restype = ctypes.c_uint64
         for name in ("hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
-                     "hsi_device_error", "hsi_device_check"):
+                     "hsi_device_error", "hsi_device_check", "hsi_calib_read", "hsi_calib_mma"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -121,6 +123,17 @@ def device_check():
 def device_error(stream=None) -> int:
     """Synchronise, then return and clear the sticky device status (0 = OK)."""
     return int(lib().hsi_device_error(_stream(stream)))
+
+
+def calib_read(buf: torch.Tensor, method: int = 0, chunk: int = 9216, stages: int = 12, sink=None, stream=None):
+    sink = torch.zeros(1, dtype=torch.int64, device=buf.device) if sink is None else sink
+    _check("hsi_calib_read", lib().hsi_calib_read(_ptr(buf), buf.numel() * buf.element_size(), method, chunk,
+                                                  stages, _ptr(sink), _stream(stream)))
+
+
+def calib_mma(n: int, iters: int, sink=None, device="cuda", stream=None):
+    sink = torch.zeros(1, dtype=torch.int64, device=device) if sink is None else sink
+    _check("hsi_calib_mma", lib().hsi_calib_mma(n, iters, _ptr(sink), _stream(stream)))
 
 
 def n_records(rows: int) -> int:

@@ -18,6 +18,27 @@ __device__ uint32_t g_hsi_error = 0;
 
 __device__ __forceinline__ void raise_error(uint32_t code) { atomicOr(&g_hsi_error, code); }
 
+// Optional wait tracing (build with -DHSI_TRACE): cycles each warp role spent
+// blocked in each kind of wait, and its total loop cycles, summed over CTAs.
+#ifdef HSI_TRACE
+constexpr int TRACE_SLOTS = 32;
+__device__ unsigned long long g_hsi_trace[TRACE_SLOTS];
+#endif
+
+struct WaitTrace {
+#ifdef HSI_TRACE
+    unsigned long long c[TRACE_SLOTS] = {};
+    __device__ void add(int i, unsigned long long v) { c[i] += v; }
+    __device__ void flush() {
+        for (int i = 0; i < TRACE_SLOTS; ++i)
+            if (c[i]) atomicAdd(&g_hsi_trace[i], c[i]);
+    }
+#else
+    __device__ void add(int, unsigned long long) {}
+    __device__ void flush() {}
+#endif
+};
+
 // Wait for the phase of `bar` with the given parity to complete, bounded in
 // wall-clock time. Returns false (after setting *abort and the device error
 // word on a timeout) when the wait gave up, either by running out or because

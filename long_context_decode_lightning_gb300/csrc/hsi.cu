@@ -7,6 +7,7 @@
 #include <cstring>
 
 #include "../../include/hsi.h"
+#include "calib.cuh"
 #include "common.cuh"
 #include "quantize.cuh"
 #include "score.cuh"
@@ -16,9 +17,10 @@ using namespace hsi;
 
 namespace {
 
-constexpr int kDecodeStages = 8;
-constexpr int kGatherStages = 8;
-constexpr int kPrefillStages = 6;
+// Stage ring depth and 128-key tiles per stage of each scoring variant.
+constexpr int kDecodeStages = 10, kDecodeUT = 2;
+constexpr int kGatherStages = 10, kGatherUT = 2;
+constexpr int kPrefillStages = 8, kPrefillUT = 1;
 constexpr int kCandCap = 16384;  // survivors of the histogram pass kept per query
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -100,19 +102,19 @@ hsi_status run_select(SelParams sp, int64_t max_items, cudaStream_t s) {
     return launch_ok();
 }
 
-template <int NQ, bool GATHER, int STAGES>
+template <int NQ, bool GATHER, int STAGES, int UT>
 hsi_status launch_score(const ScoreParams& p, cudaStream_t s) {
-    using C = ScoreCfg<NQ, GATHER, STAGES>;
+    using C = ScoreCfg<NQ, GATHER, STAGES, UT>;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(score_kernel<NQ, GATHER, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(score_kernel<NQ, GATHER, STAGES, UT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::SMEM_BYTES) != cudaSuccess)
             return HSI_ERR_CUDA;
         attr_set = true;
     }
     const int sms = sm_count();
     if (sms <= 0) return HSI_ERR_CUDA;
-    score_kernel<NQ, GATHER, STAGES><<<sms, C::THREADS, C::SMEM_BYTES, s>>>(p);
+    score_kernel<NQ, GATHER, STAGES, UT><<<sms, C::THREADS, C::SMEM_BYTES, s>>>(p);
     return launch_ok();
 }
 
@@ -134,6 +136,18 @@ const char* hsi_status_string(hsi_status st) {
 }
 
 uint64_t hsi_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+#ifdef HSI_TRACE
+// Trace builds only: copy out and clear the wait-cycle counters.
+int hsi_trace_read(unsigned long long* out, int n) {
+    if (n > TRACE_SLOTS) n = TRACE_SLOTS;
+    if (cudaDeviceSynchronize() != cudaSuccess) return HSI_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(out, g_hsi_trace, n * sizeof(unsigned long long)) != cudaSuccess) return HSI_ERR_CUDA;
+    static const unsigned long long zeros[TRACE_SLOTS] = {};
+    if (cudaMemcpyToSymbol(g_hsi_trace, zeros, sizeof(zeros)) != cudaSuccess) return HSI_ERR_CUDA;
+    return HSI_OK;
+}
+#endif
 
 hsi_status hsi_device_check(void) {
     int dev = 0, major = 0, minor = 0;
@@ -237,8 +251,8 @@ hsi_status hsi_score_full(const uint8_t* q_rec, const float* g_q, const float* w
     p.ld = ld;
     p.bmax = block_max;
     p.ldb = ldb;
-    if (group == 1) return launch_score<1, false, kDecodeStages>(p, stream);
-    return launch_score<4, false, kPrefillStages>(p, stream);
+    if (group == 1) return launch_score<1, false, kDecodeStages, kDecodeUT>(p, stream);
+    return launch_score<4, false, kPrefillStages, kPrefillUT>(p, stream);
 }
 
 hsi_status hsi_score_pool(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
@@ -249,7 +263,8 @@ hsi_status hsi_score_pool(const uint8_t* q_rec, const float* g_q, const float* w
     (void)ws_bytes;
     hsi_status st = check_score_common(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B);
     if (st != HSI_OK) return st;
-    if (!block_ids || !n_kept || !pool_scores || n_keep <= 0 || n_keep > (1 << 20) || ld < (int64_t)n_keep * 8)
+    if (!block_ids || !n_kept || !pool_scores || n_keep <= 0 || n_keep > (1 << 20) || n_keep % (16 * kGatherUT) ||
+        ld < (int64_t)n_keep * 8 || !aligned(block_ids, 16))
         return HSI_ERR_INVALID_ARG;
     ScoreParams p{};
     p.q_rec = q_rec;
@@ -266,7 +281,7 @@ hsi_status hsi_score_pool(const uint8_t* q_rec, const float* g_q, const float* w
     p.n_keep = n_keep;
     p.pool_scores = pool_scores;
     p.ld_pool = ld;
-    return launch_score<1, true, kGatherStages>(p, stream);
+    return launch_score<1, true, kGatherStages, kGatherUT>(p, stream);
 }
 
 hsi_status hsi_topk(const float* scores, int64_t ld, const int32_t* n_valid, int32_t B, int64_t max_valid, int32_t k,
@@ -349,6 +364,39 @@ hsi_status hsi_candidate_pool(const float* scores, int64_t ld, const float* bloc
     sp.bits = pool_bits;
     sp.ld_bits = ld_bits;
     return run_select(sp, max_blocks, stream);
+}
+
+hsi_status hsi_calib_read(const void* buf, size_t bytes, int method, int chunk, int stages,
+                          unsigned long long* sink, cudaStream_t stream) {
+    if (!buf || !sink || bytes < 16 || !aligned(buf, 16)) return HSI_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    if (sms <= 0) return HSI_ERR_CUDA;
+    if (method == 0) {
+        calib_read_ldg_kernel<<<sms * 4, 512, 0, stream>>>(static_cast<const uint4*>(buf), bytes / 16, sink);
+        return launch_ok();
+    }
+    if (method != 1 || chunk < 16 || chunk % 16 || stages < 1) return HSI_ERR_INVALID_ARG;
+    const size_t smem = (size_t)stages * chunk + 2 * (size_t)stages * 8 + 1024;
+    if (smem > 227 * 1024 || (size_t)chunk * sms > bytes) return HSI_ERR_INVALID_ARG;
+    if (cudaFuncSetAttribute(calib_read_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return HSI_ERR_CUDA;
+    calib_read_bulk_kernel<<<sms, 64, smem, stream>>>(static_cast<const uint8_t*>(buf), bytes, chunk, stages, sink);
+    return launch_ok();
+}
+
+hsi_status hsi_calib_mma(int n, int iters, unsigned long long* sink, cudaStream_t stream) {
+    if (!sink || iters < 1) return HSI_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    if (sms <= 0) return HSI_ERR_CUDA;
+    switch (n) {
+        case 32: calib_mma_kernel<32><<<sms, 128, 0, stream>>>(iters, sink); break;
+        case 64: calib_mma_kernel<64><<<sms, 128, 0, stream>>>(iters, sink); break;
+        case 128: calib_mma_kernel<128><<<sms, 128, 0, stream>>>(iters, sink); break;
+        case 256: calib_mma_kernel<256><<<sms, 128, 0, stream>>>(iters, sink); break;
+        default: return HSI_ERR_UNSUPPORTED;
+    }
+    return launch_ok();
 }
 
 }  // extern "C"

@@ -2,32 +2,39 @@
 //
 //   I = (g_q g_k / 128) * sum_j w_j * ReLU(q_j . k)
 //
-// One tile = 128 keys (16 NVFP4 block records of 8 keys) x one query group
-// (NQ queries x 32 heads). The contraction D[key][head] = K_tile . Q^T is
-// tcgen05.mma kind::mxf4nvf4 with per-16-element E4M3 scales (M = 128,
-// N = 32 NQ, K = 128 as two K = 64 steps), accumulated in fp32 in Tensor
-// Memory. The epilogue reads D from TMEM (one key per thread), applies ReLU
-// and the head weights and writes one fp32 score per key, so per-head logits
-// never leave the SM.
+// One unit = UT tiles of 128 keys (16 NVFP4 block records of 8 keys each) x
+// one query group (NQ queries x 32 heads). Per tile the contraction
+// D[key][head] = K_tile . Q^T is tcgen05.mma kind::mxf4nvf4 with
+// per-16-element E4M3 scales (M = 128, N = 32 NQ, K = 128 as two K = 64
+// steps), accumulated in fp32 in Tensor Memory. The epilogue reads D from TMEM
+// (one key per thread), applies ReLU and the head weights and writes one fp32
+// score per key, so per-head logits never leave the SM.
 //
 // Warp roles in a persistent CTA (one per SM):
-//   warp 0      producer: bulk copies (TMA engine) of K records into a ring of
-//               shared-memory stages and of the group's q records into one of
-//               two q slots. Full scan: one copy of up to 16 consecutive
-//               records per tile. Pool gather: one 576-byte copy per pooled
-//               block (a whole 8-key block: codes and scales).
-//   warp 1      MMA issuer: rearranges each tile's scales into the 32x16-byte
-//               layout tcgen05.cp takes, copies them to TMEM and issues the
-//               MMAs; owns the TMEM allocation.
-//   warps 2..5  epilogue (each owns one 32-lane quarter of TMEM).
+//   warp 0       producer: bulk copies (TMA engine) of K records into a ring of
+//                shared-memory stages, one stage per unit, and of the group's q
+//                records into one of two q slots. Full scan: one copy of up to
+//                16 UT consecutive records (18 KB for UT = 2: below that size
+//                the per-copy rate, not HBM, limits a bulk-copy stream). Pool
+//                gather: one 576-byte copy per pooled block (a whole 8-key
+//                block, codes and scales); the block ids themselves are
+//                prefetched IDS_AHEAD units ahead, also by bulk copy.
+//   warp 1       MMA issuer; owns the TMEM allocation.
+//   warps 2..5   scale warpgroup: writes each unit's (and each q group's) E4M3
+//                scales from the records in shared memory straight into TMEM
+//                (tcgen05.st, one 32-lane quarter per warp) in the layout the
+//                block-scaled MMA reads, so no copy instruction occupies the
+//                tensor pipe.
+//   warps 6..13  epilogue, two groups of four warps (one per TMEM quarter);
+//                group e takes the units u with u % 2 == e.
 // The block records are used in place as the MMA operands: a record is eight
-// rows of four 8x16-byte core matrices (K-major, no swizzle, core matrices 128 B
-// apart along K, records 576 B apart along M/N).
+// rows of four 8x16-byte core matrices (K-major, no swizzle, core matrices
+// 128 B apart along K, records 576 B apart along M/N).
 //
-// Work: tiles of all queries are numbered in order (query group, then key
-// tile) and each CTA takes one contiguous range, so it reloads q only when the
-// group changes. Every wait is bounded; on a timeout the CTA records the error,
-// drains its copies and MMAs, frees TMEM and returns.
+// Work: units of all queries are numbered in order (query group, then key
+// range) and each CTA takes one contiguous range, so it reloads q only when
+// the group changes. Every wait is bounded; on a timeout the CTA records the
+// error, drains its copies and MMAs, frees TMEM and returns.
 #pragma once
 #include <cstdint>
 
@@ -36,8 +43,8 @@
 namespace hsi {
 
 constexpr int REC = 576;
-constexpr int TILE_RECS = 16;
 constexpr int TILE_KEYS = 128;
+constexpr int IDS_AHEAD = 8;  // gather: units of block ids prefetched ahead
 
 struct ScoreParams {
     const uint8_t* q_rec;
@@ -57,33 +64,46 @@ struct ScoreParams {
     // pool gather
     const int32_t* block_ids;
     const int32_t* n_kept;
-    int32_t n_keep;
+    int32_t n_keep;  // multiple of 16 UT
     float* pool_scores;
     int64_t ld_pool;
 };
 
-template <int NQ, bool GATHER, int STAGES>
+template <int NQ, bool GATHER, int STAGES, int UT>
 struct ScoreCfg {
     static constexpr int N = 32 * NQ;
+    static constexpr int UNIT_RECS = 16 * UT;
+    static constexpr int UNIT_KEYS = TILE_KEYS * UT;
+    static constexpr int NACC = NQ == 1 ? 4 : 2;  // accumulator sets (one set = UT tiles)
     static constexpr int Q_BYTES = NQ * 4 * REC;
-    static constexpr int STAGE_BYTES = TILE_RECS * REC + 2 * 512;  // records + two SFA atoms
-    static constexpr int QSLOT_BYTES = ((Q_BYTES + 127) / 128) * 128 + 2 * 512;
-    static constexpr int EPI_WARPS = 4;
-    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-    // TMEM columns: two accumulators, two SFA buffers (2 chunks x 4), two SFB slots
+    static constexpr int STAGE_BYTES = UNIT_RECS * REC;
+    static constexpr int QSLOT_BYTES = ((Q_BYTES + 127) / 128) * 128;
+    static constexpr int FIRST_SF_WARP = 2;
+    static constexpr int FIRST_EPI_WARP = 6;
+    static constexpr int EPI_GROUPS = 2;
+    static constexpr int THREADS = 32 * (FIRST_EPI_WARP + 4 * EPI_GROUPS);
+    // TMEM columns: accumulators, one SFA set per stage (UT tiles x 2 chunks x 4),
+    // one SFB set per q slot (2 chunks x 4)
     static constexpr int COL_ACC = 0;
-    static constexpr int COL_SFA = 2 * N;
-    static constexpr int COL_SFB = 2 * N + 16;
-    static constexpr int COLS_USED = 2 * N + 32;
+    static constexpr int COL_SFA = NACC * UT * N;
+    static constexpr int COL_SFB = COL_SFA + STAGES * UT * 8;
+    static constexpr int COLS_USED = COL_SFB + 16;
     static constexpr int TMEM_COLS = COLS_USED <= 32 ? 32 : COLS_USED <= 64 ? 64 : COLS_USED <= 128 ? 128
                                      : COLS_USED <= 256 ? 256 : 512;
     static constexpr int OFF_STAGES = 0;
     static constexpr int OFF_QSLOTS = STAGES * STAGE_BYTES;
-    static constexpr int OFF_BARS = OFF_QSLOTS + 2 * QSLOT_BYTES;
-    static constexpr int NBARS = 2 * STAGES + 8 + 1;
+    static constexpr int OFF_IDS = OFF_QSLOTS + 2 * QSLOT_BYTES;
+    static constexpr int IDS_BYTES = GATHER ? IDS_AHEAD * UNIT_RECS * 4 : 0;
+    static constexpr int OFF_BARS = OFF_IDS + IDS_BYTES;
+    // full, sfready, empty per stage; acc_full, acc_empty per accumulator set;
+    // q_full, q_ready, q_empty per slot; ids_full per id slot; drain
+    static constexpr int NBARS = 3 * STAGES + 2 * NACC + 6 + (GATHER ? IDS_AHEAD : 0) + 1;
     static constexpr int SMEM_BYTES = OFF_BARS + NBARS * 8 + 64 + 1024;  // + alignment slack
-    static_assert(NQ <= 4, "one 128-row scale atom per K chunk for B");
+    static_assert(NQ <= 4, "B scale rows fit one 128-row layout");
     static_assert(COLS_USED <= 512, "TMEM");
+    static_assert(NACC % EPI_GROUPS == 0, "accumulator sets split evenly between epilogue groups");
+    static_assert(!GATHER || (NQ == 1 && UNIT_RECS <= 32), "gather: one block per producer lane");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
 struct ScoreShared {  // small control block after the barriers
@@ -141,6 +161,27 @@ __device__ __forceinline__ bool wait_role(uint64_t* bar, uint32_t parity, ScoreS
     return wait_bounded(bar, parity, (volatile int*)&sh->abort);
 }
 
+// Trace slots: which role waited on what (only with -DHSI_TRACE).
+enum : int {
+    TR_PROD_QEMPTY = 0, TR_PROD_EMPTY, TR_PROD_IDS, TR_SF_QFULL, TR_SF_FULL, TR_MMA_QREADY, TR_MMA_SFREADY,
+    TR_MMA_ACCEMPTY, TR_EPI_ACCFULL, TR_PROD_TOTAL = 16, TR_SF_TOTAL, TR_MMA_TOTAL, TR_EPI_TOTAL, TR_UNITS
+};
+
+__device__ __forceinline__ bool wait_traced(uint64_t* bar, uint32_t parity, ScoreShared* sh, WaitTrace& tr,
+                                            int slot) {
+#ifdef HSI_TRACE
+    // (try_wait itself blocks for a while, so time the whole wait)
+    const long long t0 = clock64();
+    const bool ok = wait_role(bar, parity, sh);
+    tr.add(slot, (unsigned long long)(clock64() - t0));
+    return ok;
+#else
+    (void)tr;
+    (void)slot;
+    return wait_role(bar, parity, sh);
+#endif
+}
+
 // Bounded wait that ignores the abort flag (teardown: drain what is in flight).
 __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
@@ -152,56 +193,71 @@ __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
     }
 }
 
-template <int NQ, bool GATHER>
-__device__ __forceinline__ int group_tiles(const ScoreParams& p, int g) {
+template <int NQ, bool GATHER, int UT>
+__device__ __forceinline__ int group_units(const ScoreParams& p, int g) {
     if (GATHER) {
         const int nk = p.n_kept[g];
-        return nk <= 0 ? 0 : (min(nk, p.n_keep) + TILE_RECS - 1) / TILE_RECS;
+        return nk <= 0 ? 0 : (min(nk, p.n_keep) + 16 * UT - 1) / (16 * UT);
     } else {
         int m = 0;
 #pragma unroll
         for (int i = 0; i < NQ; ++i) m = max(m, p.n_vis[g * NQ + i]);
-        return (m + TILE_KEYS - 1) / TILE_KEYS;
+        return (m + TILE_KEYS * UT - 1) / (TILE_KEYS * UT);
     }
 }
 
-// Scale factors of 128 rows (16 records at stride 576) -> two 32x16-byte atoms:
-// atom kk, byte (m%32)*16 + (m/32)*4 + i holds the scale of row m, values
-// 64kk + 16i .. +16. Whole warp.
-__device__ __forceinline__ void permute_sf(const uint8_t* recs, int nrows, uint8_t* atoms) {
-    const int lane = threadIdx.x & 31;
-    uint32_t lo[4], hi[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const int m = lane + 32 * c;
-        if (m < nrows) {
-            const uint2 v = *reinterpret_cast<const uint2*>(recs + (m >> 3) * REC + 512 + (m & 7) * 8);
-            lo[c] = v.x;
-            hi[c] = v.y;
-        } else {
-            lo[c] = 0u;
-            hi[c] = 0u;
+// Walks the units (group, unit in group) of this CTA's range in order.
+template <int NQ, bool GATHER, int UT>
+struct UnitIter {
+    int g, t, nunits;
+    __device__ void init(const ScoreParams& p, const ScoreShared* sh) {
+        g = sh->g0;
+        t = sh->t0;
+        nunits = sh->count > 0 ? group_units<NQ, GATHER, UT>(p, g) : 0;
+    }
+    __device__ void next(const ScoreParams& p) {
+        if (++t == nunits) {
+            t = 0;
+            do {
+                ++g;
+            } while (g < p.ngroups && (nunits = group_units<NQ, GATHER, UT>(p, g)) == 0);
         }
     }
-    *reinterpret_cast<uint4*>(atoms + lane * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    *reinterpret_cast<uint4*>(atoms + 512 + lane * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+};
+
+// The scales of rows r, r+32, r+64, r+96 of records at `recs` (nrows valid
+// rows) in the layout of one 32-lane TMEM quarter: column c holds row r+32c,
+// columns 0-3 the first 64 values (K step 0), columns 4-7 the last 64.
+__device__ __forceinline__ void sf_quarter(const uint8_t* recs, int nrows, int r, uint32_t (&v)[8]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int m = r + 32 * c;
+        uint2 x = make_uint2(0u, 0u);
+        if (m < nrows) x = *reinterpret_cast<const uint2*>(recs + (m >> 3) * REC + 512 + (m & 7) * 8);
+        v[c] = x.x;
+        v[4 + c] = x.y;
+    }
 }
 
-template <int NQ, bool GATHER, int STAGES>
-__global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES>::THREADS, 1) score_kernel(ScoreParams p) {
-    using C = ScoreCfg<NQ, GATHER, STAGES>;
+template <int NQ, bool GATHER, int STAGES, int UT>
+__global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) score_kernel(ScoreParams p) {
+    using C = ScoreCfg<NQ, GATHER, STAGES, UT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem + C::OFF_STAGES;
     uint8_t* qslots = smem + C::OFF_QSLOTS;
+    int32_t* ids_ring = reinterpret_cast<int32_t*>(smem + C::OFF_IDS);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
     uint64_t* full = bars;
-    uint64_t* empty = bars + STAGES;
-    uint64_t* acc_full = bars + 2 * STAGES;
-    uint64_t* acc_empty = acc_full + 2;
-    uint64_t* q_full = acc_full + 4;
-    uint64_t* q_empty = acc_full + 6;
-    uint64_t* drain = acc_full + 8;
+    uint64_t* sfready = full + STAGES;
+    uint64_t* empty = sfready + STAGES;
+    uint64_t* acc_full = empty + STAGES;
+    uint64_t* acc_empty = acc_full + C::NACC;
+    uint64_t* q_full = acc_empty + C::NACC;
+    uint64_t* q_ready = q_full + 2;
+    uint64_t* q_empty = q_ready + 2;
+    uint64_t* ids_full = q_empty + 2;
+    uint64_t* drain = ids_full + (GATHER ? IDS_AHEAD : 0);
     ScoreShared* sh = reinterpret_cast<ScoreShared*>(bars + C::NBARS);
     __shared__ long long part[C::THREADS + 1];
 
@@ -210,39 +266,74 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES>::THREADS, 1) scor
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
+            mbar_init(&sfready[s], 4);
             mbar_init(&empty[s], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::NACC; ++i) {
             mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_empty[i], C::EPI_WARPS);
+            mbar_init(&acc_empty[i], 4);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&q_full[i], 1);
+            mbar_init(&q_ready[i], 4);
             mbar_init(&q_empty[i], 1);
         }
+        if (GATHER)
+            for (int i = 0; i < IDS_AHEAD; ++i) mbar_init(&ids_full[i], 1);
         mbar_init(drain, 1);
         sh->abort = 0;
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(&sh->tmem_base, C::TMEM_COLS);
-    schedule_range(p.ngroups, [&](int g) { return group_tiles<NQ, GATHER>(p, g); }, sh, part);
+    schedule_range(p.ngroups, [&](int g) { return group_units<NQ, GATHER, UT>(p, g); }, sh, part);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh->tmem_base;
     const long long count = sh->count;
+    WaitTrace tr;
+#ifdef HSI_TRACE
+    const long long t_start = clock64();
+#endif
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        int g = sh->g0, t = sh->t0, ntiles = count > 0 ? group_tiles<NQ, GATHER>(p, g) : 0;
+        UnitIter<NQ, GATHER, UT> it;
+        it.init(p, sh);
+        UnitIter<NQ, GATHER, UT> ahead;  // gather: the unit whose block ids are fetched next
+        ahead.init(p, sh);
+        long long fetched = 0;
+        auto fetch_ids = [&]() {  // lane 0: bulk-copy the block ids of unit `fetched`
+            const int slot = (int)(fetched % IDS_AHEAD);
+            mbar_arrive_expect_tx(&ids_full[slot], C::UNIT_RECS * 4);
+            bulk_g2s(ids_ring + slot * C::UNIT_RECS,
+                     p.block_ids + (int64_t)ahead.g * p.n_keep + (int64_t)ahead.t * C::UNIT_RECS, C::UNIT_RECS * 4,
+                     &ids_full[slot]);
+            ahead.next(p);
+            ++fetched;
+        };
+        if (GATHER && lane == 0)
+            while (fetched < count && fetched < IDS_AHEAD) fetch_ids();
         int cur_g = -1, gc = -1;
-        // what was issued, for the drain at teardown
+        int64_t k_base = 0;    // first record of the group's cache
+        int64_t nrec_all = 0;  // records holding visible keys
+        int nk = 0;            // gather: kept blocks
         long long issued_units = 0;
         int last_q_gc[2] = {-1, -1};
         for (long long u = 0; u < count; ++u) {
+            const int g = it.g, t = it.t;
             if (g != cur_g) {
                 cur_g = g;
                 ++gc;
+                const int b0 = g * NQ;
+                k_base = p.k_off[b0];
+                int maxv = 0;
+#pragma unroll
+                for (int i = 0; i < NQ; ++i) maxv = max(maxv, p.n_vis[b0 + i]);
+                nrec_all = (maxv + 7) / 8;
+                if (GATHER) nk = min(p.n_kept[b0], p.n_keep);
                 const int slot = gc & 1;
-                if (!wait_role(&q_empty[slot], ((gc >> 1) & 1) ^ 1, sh)) break;
+                if (!wait_traced(&q_empty[slot], ((gc >> 1) & 1) ^ 1, sh, tr, TR_PROD_QEMPTY)) break;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&q_full[slot], C::Q_BYTES);
                     bulk_g2s(qslots + slot * C::QSLOT_BYTES, p.q_rec + (int64_t)g * NQ * 4 * REC, C::Q_BYTES,
@@ -252,44 +343,42 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES>::THREADS, 1) scor
             }
             const int s = (int)(u % STAGES);
             const uint32_t ph = (uint32_t)((u / STAGES) & 1);
-            if (!wait_role(&empty[s], ph ^ 1, sh)) break;
+            if (GATHER) {
+                const int islot = (int)(u % IDS_AHEAD);
+                if (!wait_traced(&ids_full[islot], (uint32_t)((u / IDS_AHEAD) & 1), sh, tr, TR_PROD_IDS)) break;
+            }
+            if (!wait_traced(&empty[s], ph ^ 1, sh, tr, TR_PROD_EMPTY)) break;
             uint8_t* dst = stages + s * C::STAGE_BYTES;
             if (!GATHER) {
-                const int b0 = g * NQ;
-                int maxv = 0;
-#pragma unroll
-                for (int i = 0; i < NQ; ++i) maxv = max(maxv, p.n_vis[b0 + i]);
-                const int64_t nrec_all = (maxv + 7) / 8;
-                const int nrec = (int)min((int64_t)TILE_RECS, nrec_all - (int64_t)t * TILE_RECS);
+                const int nrec = (int)min((int64_t)C::UNIT_RECS, nrec_all - (int64_t)t * C::UNIT_RECS);
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&full[s], (uint32_t)(nrec * REC));
-                    bulk_g2s(dst, p.k_rec + (p.k_off[b0] + (int64_t)t * TILE_RECS) * REC, (uint32_t)(nrec * REC),
+                    bulk_g2s(dst, p.k_rec + (k_base + (int64_t)t * C::UNIT_RECS) * REC, (uint32_t)(nrec * REC),
                              &full[s]);
                 }
             } else {
-                const int b = g;
-                const int nk = min(p.n_kept[b], p.n_keep);
-                const int j = t * TILE_RECS + lane;
-                const int64_t nrec_vis = ((int64_t)p.n_vis[b] + 7) / 8;
+                const int j = t * C::UNIT_RECS + lane;
                 bool ok = false;
                 int64_t id = 0;
-                if (lane < TILE_RECS && j < nk) {
-                    id = p.block_ids[(int64_t)b * p.n_keep + j];
-                    ok = id >= 0 && id < nrec_vis;
+                if (lane < C::UNIT_RECS && j < nk) {
+                    id = ids_ring[(u % IDS_AHEAD) * C::UNIT_RECS + lane];
+                    ok = id >= 0 && id < nrec_all;
                     if (!ok) raise_error(DEVERR_ARG);
                 }
                 const uint32_t m = __ballot_sync(0xFFFFFFFFu, ok);
-                if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(__popc(m) * REC));
+                __syncwarp();  // every lane has read its id before the slot is refilled
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)(__popc(m) * REC));
+                    if (fetched < count) {
+                        fence_proxy_async_smem();  // the slot's reads precede the copy that refills it
+                        fetch_ids();
+                    }
+                }
                 __syncwarp();
-                if (ok) bulk_g2s(dst + lane * REC, p.k_rec + (p.k_off[b] + id) * REC, REC, &full[s]);
+                if (ok) bulk_g2s(dst + lane * REC, p.k_rec + (k_base + id) * REC, REC, &full[s]);
             }
             issued_units = u + 1;
-            if (++t == ntiles) {
-                t = 0;
-                do {
-                    ++g;
-                } while (g < p.ngroups && (ntiles = group_tiles<NQ, GATHER>(p, g)) == 0);
-            }
+            it.next(p);
         }
         // drain: every copy issued must have landed before the CTA exits
         if (lane == 0) {
@@ -299,87 +388,115 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES>::THREADS, 1) scor
             }
             for (int slot = 0; slot < 2; ++slot)
                 if (last_q_gc[slot] >= 0) wait_drain(&q_full[slot], (uint32_t)((last_q_gc[slot] >> 1) & 1));
+            if (GATHER)
+                for (int i = 0; i < IDS_AHEAD && i < fetched; ++i) {
+                    const long long last = i + ((fetched - 1 - i) / IDS_AHEAD) * IDS_AHEAD;
+                    wait_drain(&ids_full[i], (uint32_t)((last / IDS_AHEAD) & 1));
+                }
         }
     } else if (warp == 1) {
         // ----------------------------------------------------------------- MMA
-        int g = sh->g0, t = sh->t0, ntiles = count > 0 ? group_tiles<NQ, GATHER>(p, g) : 0;
+        UnitIter<NQ, GATHER, UT> it;
+        it.init(p, sh);
         int cur_g = -1, gc = -1;
         constexpr uint32_t idesc = idesc_nvf4(128, C::N);
         for (long long u = 0; u < count; ++u) {
-            if (g != cur_g) {
+            if (it.g != cur_g) {
                 if (cur_g >= 0 && lane == 0) tc_commit(&q_empty[gc & 1]);  // old slot free once its MMAs finish
-                cur_g = g;
+                cur_g = it.g;
                 ++gc;
-                const int slot = gc & 1;
-                if (!wait_role(&q_full[slot], (gc >> 1) & 1, sh)) break;
-                uint8_t* qs = qslots + slot * C::QSLOT_BYTES;
-                uint8_t* atoms = qs + C::QSLOT_BYTES - 1024;
-                permute_sf(qs, C::N, atoms);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tc_fence_after();
-                    const uint32_t sfb = tmem + C::COL_SFB + slot * 8;
-                    tc_cp_32x128b_x4(sfb, smem_desc(smem_u32(atoms), 128, 128));
-                    tc_cp_32x128b_x4(sfb + 4, smem_desc(smem_u32(atoms + 512), 128, 128));
-                }
-                __syncwarp();
+                if (!wait_traced(&q_ready[gc & 1], (gc >> 1) & 1, sh, tr, TR_MMA_QREADY)) break;
             }
             const int s = (int)(u % STAGES);
             const uint32_t ph = (uint32_t)((u / STAGES) & 1);
-            const int acc = (int)(u & 1);
-            const uint32_t aph = (uint32_t)((u >> 1) & 1);
-            if (!wait_role(&full[s], ph, sh)) break;
-            uint8_t* st = stages + s * C::STAGE_BYTES;
-            uint8_t* sfa_atoms = st + TILE_RECS * REC;
-            permute_sf(st, TILE_KEYS, sfa_atoms);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (!wait_role(&acc_empty[acc], aph ^ 1, sh)) break;
+            const int a = (int)(u % C::NACC);
+            const uint32_t aph = (uint32_t)((u / C::NACC) & 1);
+            if (!wait_traced(&sfready[s], ph, sh, tr, TR_MMA_SFREADY)) break;
+            if (!wait_traced(&acc_empty[a], aph ^ 1, sh, tr, TR_MMA_ACCEMPTY)) break;
             if (lane == 0) {
                 tc_fence_after();
-                const uint32_t sfa = tmem + C::COL_SFA + acc * 8;
-                const uint32_t sfb = tmem + C::COL_SFB + (gc & 1) * 8;
-                tc_cp_32x128b_x4(sfa, smem_desc(smem_u32(sfa_atoms), 128, 128));
-                tc_cp_32x128b_x4(sfa + 4, smem_desc(smem_u32(sfa_atoms + 512), 128, 128));
-                const uint32_t a0 = smem_u32(st);
+                const uint32_t a0 = smem_u32(stages + s * C::STAGE_BYTES);
                 const uint32_t b0 = smem_u32(qslots + (gc & 1) * C::QSLOT_BYTES);
-                const uint32_t d = tmem + C::COL_ACC + acc * C::N;
+                const uint32_t sfb = tmem + C::COL_SFB + (gc & 1) * 8;
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    mma_nvf4(d, smem_desc(a0 + kk * 256, 128, REC), smem_desc(b0 + kk * 256, 128, REC), idesc,
-                             sfa + kk * 4, sfb + kk * 4, kk);
+                for (int st = 0; st < UT; ++st) {
+                    const uint32_t d = tmem + C::COL_ACC + (a * UT + st) * C::N;
+                    const uint32_t sfa = tmem + C::COL_SFA + (s * UT + st) * 8;
+                    const uint32_t at = a0 + st * 16 * REC;
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk)
+                        mma_nvf4(d, smem_desc(at + kk * 256, 128, REC), smem_desc(b0 + kk * 256, 128, REC), idesc,
+                                 sfa + kk * 4, sfb + kk * 4, kk);
                 }
                 tc_commit(&empty[s]);
-                tc_commit(&acc_full[acc]);
+                tc_commit(&acc_full[a]);
             }
             __syncwarp();
-            if (++t == ntiles) {
-                t = 0;
-                do {
-                    ++g;
-                } while (g < p.ngroups && (ntiles = group_tiles<NQ, GATHER>(p, g)) == 0);
-            }
+            it.next(p);
         }
-        // drain: every MMA / copy into TMEM done before the allocation is freed
+        // drain: every MMA into TMEM done before the allocation is freed
         if (lane == 0) {
             tc_commit(drain);
             wait_drain(drain, 0);
         }
         __syncwarp();
+    } else if (warp < C::FIRST_EPI_WARP) {
+        // ---------------------------------------------------- scale warpgroup
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        UnitIter<NQ, GATHER, UT> it;
+        it.init(p, sh);
+        int cur_g = -1, gc = -1;
+        for (long long u = 0; u < count; ++u) {
+            if (it.g != cur_g) {
+                cur_g = it.g;
+                ++gc;
+                const int slot = gc & 1;
+                if (!wait_traced(&q_full[slot], (gc >> 1) & 1, sh, tr, TR_SF_QFULL)) break;
+                uint32_t v[8];
+                sf_quarter(qslots + slot * C::QSLOT_BYTES, C::N, lane, v);
+                tmem_st8_wait(tmem + lane_base + C::COL_SFB + slot * 8, v);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&q_ready[slot]);
+            }
+            const int s = (int)(u % STAGES);
+            const uint32_t ph = (uint32_t)((u / STAGES) & 1);
+            if (!wait_traced(&full[s], ph, sh, tr, TR_SF_FULL)) break;
+            const uint8_t* st_recs = stages + s * C::STAGE_BYTES;
+#pragma unroll
+            for (int st = 0; st < UT; ++st) {
+                uint32_t v[8];
+                sf_quarter(st_recs + st * 16 * REC, TILE_KEYS, lane, v);
+                tmem_st8_wait(tmem + lane_base + C::COL_SFA + (s * UT + st) * 8, v);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sfready[s]);
+            it.next(p);
+        }
     } else {
         // ------------------------------------------------------------ epilogue
+        const int grp = (warp - C::FIRST_EPI_WARP) >> 2;
         const int quarter = warp & 3;
-        const int row = quarter * 32 + lane;  // key within the tile
-        int g = sh->g0, t = sh->t0, ntiles = count > 0 ? group_tiles<NQ, GATHER>(p, g) : 0;
+        const int row = quarter * 32 + lane;  // key within a 128-key tile
+        UnitIter<NQ, GATHER, UT> it;
+        it.init(p, sh);
         int cur_g = -1;
         float wq[NQ][32];
+        int nv[NQ];
+        int nk = 0;
         for (long long u = 0; u < count; ++u) {
+            if ((int)(u % C::EPI_GROUPS) != grp) {
+                it.next(p);
+                continue;
+            }
+            const int g = it.g, t = it.t;
             if (g != cur_g) {
                 cur_g = g;
 #pragma unroll
                 for (int qi = 0; qi < NQ; ++qi) {
                     const int b = g * NQ + qi;
+                    nv[qi] = p.n_vis[b];
                     const float sc = p.g_q[b] * p.g_k[b] * 0.0078125f;
                     const float4* wv = reinterpret_cast<const float4*>(p.w + (int64_t)b * 32);
 #pragma unroll
@@ -391,58 +508,69 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES>::THREADS, 1) scor
                         wq[qi][4 * j4 + 3] = v.w * sc;
                     }
                 }
+                if (GATHER) nk = min(p.n_kept[g], p.n_keep);
             }
-            const int acc = (int)(u & 1);
-            const uint32_t aph = (uint32_t)((u >> 1) & 1);
-            if (!wait_role(&acc_full[acc], aph, sh)) break;
+            const int a = (int)(u % C::NACC);
+            const uint32_t aph = (uint32_t)((u / C::NACC) & 1);
+            // gather: the positions of this thread's slots, loaded before the wait
+            int64_t pos[UT];
+#pragma unroll
+            for (int st = 0; st < UT; ++st) {
+                pos[st] = -1;
+                const int slot_i = (t * UT + st) * TILE_KEYS + row;
+                if (GATHER && (slot_i >> 3) < nk)
+                    pos[st] = (int64_t)__ldg(p.block_ids + (int64_t)g * p.n_keep + (slot_i >> 3)) * 8 + (slot_i & 7);
+            }
+            if (!wait_traced(&acc_full[a], aph, sh, tr, TR_EPI_ACCFULL)) break;
             tc_fence_after();
-            const uint32_t dbase = tmem + ((uint32_t)(quarter * 32) << 16) + C::COL_ACC + acc * C::N;
 #pragma unroll
-            for (int qi = 0; qi < NQ; ++qi) {
-                float a[32];
-                tmem_ld32(dbase + qi * 32, a);
-                float s0 = 0.f, s1 = 0.f;
+            for (int st = 0; st < UT; ++st) {
+                const uint32_t dbase = tmem + ((uint32_t)(quarter * 32) << 16) + C::COL_ACC + (a * UT + st) * C::N;
+                const int key = (t * UT + st) * TILE_KEYS + row;  // key (full scan) or pool slot (gather)
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    s0 = fmaf(wq[qi][j], fmaxf(a[j], 0.f), s0);
-                    s1 = fmaf(wq[qi][j + 1], fmaxf(a[j + 1], 0.f), s1);
-                }
-                const float sc = s0 + s1;
-                const int b = g * NQ + qi;
-                if (!GATHER) {
-                    const int nv = p.n_vis[b];
-                    const int key = t * TILE_KEYS + row;
-                    const bool vis = key < nv;
-                    if (vis) p.scores[(int64_t)b * p.ld + key] = sc;
-                    if (p.bmax) {
-                        float m = vis ? sc : __uint_as_float(0xFF800000u);
-                        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-                        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-                        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-                        if ((lane & 7) == 0 && vis) p.bmax[(int64_t)b * p.ldb + key / 8] = m;
+                for (int qi = 0; qi < NQ; ++qi) {
+                    float x[32];
+                    tmem_ld32(dbase + qi * 32, x);
+                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        s0 = fmaf(wq[qi][j], fmaxf(x[j], 0.f), s0);
+                        s1 = fmaf(wq[qi][j + 1], fmaxf(x[j + 1], 0.f), s1);
+                        s2 = fmaf(wq[qi][j + 2], fmaxf(x[j + 2], 0.f), s2);
+                        s3 = fmaf(wq[qi][j + 3], fmaxf(x[j + 3], 0.f), s3);
                     }
-                } else {
-                    const int slot = t * TILE_KEYS + row;
-                    const int j = slot >> 3;
-                    const int nk = min(p.n_kept[b], p.n_keep);
-                    if (j < nk) {
-                        const int64_t pos = (int64_t)p.block_ids[(int64_t)b * p.n_keep + j] * 8 + (slot & 7);
-                        const float v = pos < p.n_vis[b] ? sc : __uint_as_float(0xFF800000u);
-                        p.pool_scores[(int64_t)b * p.ld_pool + slot] = v;
+                    const float sc = (s0 + s1) + (s2 + s3);
+                    const int b = g * NQ + qi;
+                    if (!GATHER) {
+                        const bool vis = key < nv[qi];
+                        if (vis) p.scores[(int64_t)b * p.ld + key] = sc;
+                        if (p.bmax) {
+                            float m = vis ? sc : __uint_as_float(0xFF800000u);
+                            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+                            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+                            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+                            if ((lane & 7) == 0 && vis) p.bmax[(int64_t)b * p.ldb + key / 8] = m;
+                        }
+                    } else if (pos[st] >= 0) {
+                        const float v = pos[st] < nv[qi] ? sc : __uint_as_float(0xFF800000u);
+                        p.pool_scores[(int64_t)b * p.ld_pool + key] = v;
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[acc]);
-            if (++t == ntiles) {
-                t = 0;
-                do {
-                    ++g;
-                } while (g < p.ngroups && (ntiles = group_tiles<NQ, GATHER>(p, g)) == 0);
-            }
+            if (lane == 0) mbar_arrive(&acc_empty[a]);
+            it.next(p);
         }
     }
+#ifdef HSI_TRACE
+    if (lane == 0 && (warp <= C::FIRST_SF_WARP || warp == C::FIRST_EPI_WARP)) {
+        const int slot = warp == 0 ? TR_PROD_TOTAL : warp == 1 ? TR_MMA_TOTAL : warp == 2 ? TR_SF_TOTAL : TR_EPI_TOTAL;
+        tr.add(slot, (unsigned long long)(clock64() - t_start));
+        if (warp == 0) tr.add(TR_UNITS, (unsigned long long)count);
+        tr.flush();
+    }
+#endif
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
