@@ -229,13 +229,14 @@ class DeviceWorkload:
             self.ws_rtopk = hsi.workspace(hsi.WS_TOPK, B, wl.n_keep * 8, K_TOP, device=dev)
         self.ev_score = []
         self.pool_sum = None
+        self.wl_signs = signs
+        self.graphs = []
 
     def step(self, time_score=False):
+        """One step as individual launches (no graph)."""
         hsi, wl, B = self.hsi, self.wl, self.B
         torch = self.torch
-        signs = self.wl_signs if hasattr(self, "wl_signs") else None
-        if signs is None:
-            self.wl_signs = signs = wl.signs()
+        signs = self.wl_signs
         for l in range(wl.full_layers):
             hsi.quantize_nvfp4(self.q[l], B, 32, signs, self.g_q[l], self.q_rec[l], ws=self.ws_q)
             if time_score:
@@ -259,9 +260,68 @@ class DeviceWorkload:
             hsi.topk(self.pool_scores, self.npool, B, wl.n_keep * 8, K_TOP, self.idx[l], self.val[l],
                      block_ids=self.ids, ws=self.ws_rtopk)
 
+    # -- the step as CUDA graphs: [q quantisation] [score_full] [the rest], per
+    # Full layer, so that the scoring kernel can be timed between replays
+    def segments(self):
+        hsi, wl, B = self.hsi, self.wl, self.B
+        signs = self.wl_signs
+        segs = []
+        for l in range(wl.full_layers):
+            segs.append(("pre", lambda l=l: hsi.quantize_nvfp4(self.q[l], B, 32, signs, self.g_q[l], self.q_rec[l],
+                                                               ws=self.ws_q)))
+            segs.append(("score", lambda l=l: hsi.score_full(
+                self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[l], self.g_k[l], self.k_off, self.n_vis, B,
+                self.maxv, self.scores, block_max=self.bmax if wl.build_pool else None)))
+            segs.append(("post", lambda l=l: hsi.topk(self.scores, self.n_vis, B, self.maxv, K_TOP, self.idx[l],
+                                                      self.val[l], ws=self.ws_topk)))
+        if wl.build_pool:
+            def rest():
+                hsi.candidate_pool(self.n_vis, B, self.maxv, self.ids, self.nk, self.npool, block_max=self.bmax,
+                                   block_size=wl.block_size, n_keep=wl.n_keep, pool_bits=self.bits, ws=self.ws_pool)
+                for r in range(wl.reindex_layers):
+                    l = wl.full_layers + r
+                    hsi.quantize_nvfp4(self.q[l], B, 32, signs, self.g_q[l], self.q_rec[l], ws=self.ws_q)
+                    hsi.score_pool(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0], self.k_off,
+                                   self.n_vis, self.ids, self.nk, wl.n_keep, B, self.pool_scores)
+                    hsi.topk(self.pool_scores, self.npool, B, wl.n_keep * 8, K_TOP, self.idx[l], self.val[l],
+                             block_ids=self.ids, ws=self.ws_rtopk)
+            segs.append(("post", rest))
+        merged = []
+        for kind, fn in segs:  # fuse neighbouring non-scoring segments into one graph
+            if merged and kind != "score" and merged[-1][0] != "score":
+                prev = merged[-1][1]
+                merged[-1] = (merged[-1][0], lambda a=prev, b=fn: (a(), b()))
+            else:
+                merged.append((kind, fn))
+        return merged
+
+    def capture(self):
+        torch = self.torch
+        self.step()  # also sets every kernel's attributes before capture
+        torch.cuda.synchronize()
+        self.graphs = []
+        for kind, fn in self.segments():
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            self.graphs.append((kind, g))
+        torch.cuda.synchronize()
+
+    def replay(self, time_score=False):
+        torch = self.torch
+        for kind, g in self.graphs:
+            if time_score and kind == "score":
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                g.replay()
+                e1.record()
+                self.ev_score.append((e0, e1))
+            else:
+                g.replay()
+
     def step_e2e(self):
         self.in_dev.copy_(self.in_host, non_blocking=True)
-        self.step()
+        self.replay()
         self.out_host.copy_(self.out_dev, non_blocking=True)
 
     def pairs_per_step(self):
@@ -387,12 +447,16 @@ def main():
         dist.barrier()
     hsi.device_check()
     W = DeviceWorkload(wl, dev, log)
+    l0 = hsi.kernel_launches()
+    W.step()
+    torch.cuda.synchronize()
+    launches_per_step = hsi.kernel_launches() - l0
+    W.capture()
     for _ in range(args.warmup):
-        W.step()
+        W.replay()
     torch.cuda.synchronize()
     assert hsi.device_error() == 0, "device error during warm-up"
     pairs, pairs_full, pairs_pool = W.pairs_per_step()
-    launches0 = hsi.kernel_launches()
 
     def timed(fn, K, sync_each=False):
         if world > 1:
@@ -416,10 +480,10 @@ def main():
     with ClockSampler(local) as clk:
         if args.profile:
             torch.cuda.profiler.start()
-        ms = timed(lambda: W.step(time_score=True), args.steps)
+        ms = timed(lambda: W.replay(time_score=True), args.steps)
         if args.profile:
             torch.cuda.profiler.stop()
-    launches = hsi.kernel_launches() - launches0
+    launches = launches_per_step * args.steps  # graph replays of the captured launches
     assert hsi.device_error() == 0, "device error during the timed steps"
     score_ms = float(np.mean([a.elapsed_time(b) for a, b in W.ev_score]))
     # end to end: host inputs in, host results out, every step

@@ -23,6 +23,8 @@ __device__ __forceinline__ void raise_error(uint32_t code) { atomicOr(&g_hsi_err
 #ifdef HSI_TRACE
 constexpr int TRACE_SLOTS = 32;
 __device__ unsigned long long g_hsi_trace[TRACE_SLOTS];
+// per-CTA wall-clock marks (ns): entry, work start, work end, exit
+__device__ unsigned long long g_hsi_marks[1024][4];
 #endif
 
 struct WaitTrace {

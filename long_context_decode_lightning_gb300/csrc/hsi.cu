@@ -147,6 +147,12 @@ int hsi_trace_read(unsigned long long* out, int n) {
     if (cudaMemcpyToSymbol(g_hsi_trace, zeros, sizeof(zeros)) != cudaSuccess) return HSI_ERR_CUDA;
     return HSI_OK;
 }
+
+int hsi_trace_marks(unsigned long long* out /* [1024][4] */) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return HSI_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(out, g_hsi_marks, sizeof(g_hsi_marks)) != cudaSuccess) return HSI_ERR_CUDA;
+    return HSI_OK;
+}
 #endif
 
 hsi_status hsi_device_check(void) {

@@ -78,10 +78,13 @@ struct ScoreCfg {
     static constexpr int Q_BYTES = NQ * 4 * REC;
     static constexpr int STAGE_BYTES = UNIT_RECS * REC;
     static constexpr int QSLOT_BYTES = ((Q_BYTES + 127) / 128) * 128;
-    static constexpr int FIRST_SF_WARP = 2;
-    static constexpr int FIRST_EPI_WARP = 6;
-    static constexpr int EPI_GROUPS = 2;
+    static constexpr int PROD_WARPS = GATHER ? 4 : 1;  // gather: a warpgroup of 16-byte async copies
+    static constexpr int MMA_WARP = PROD_WARPS;
+    static constexpr int FIRST_SF_WARP = PROD_WARPS + 1;
+    static constexpr int FIRST_EPI_WARP = FIRST_SF_WARP + 4;
+    static constexpr int EPI_GROUPS = GATHER ? 1 : 2;
     static constexpr int THREADS = 32 * (FIRST_EPI_WARP + 4 * EPI_GROUPS);
+    static constexpr int COPY_AHEAD = 4;  // gather: units of async copies in flight per producer thread
     // TMEM columns: accumulators, one SFA set per stage (UT tiles x 2 chunks x 4),
     // one SFB set per q slot (2 chunks x 4)
     static constexpr int COL_ACC = 0;
@@ -96,13 +99,14 @@ struct ScoreCfg {
     static constexpr int IDS_BYTES = GATHER ? IDS_AHEAD * UNIT_RECS * 4 : 0;
     static constexpr int OFF_BARS = OFF_IDS + IDS_BYTES;
     // full, sfready, empty per stage; acc_full, acc_empty per accumulator set;
-    // q_full, q_ready, q_empty per slot; ids_full per id slot; drain
-    static constexpr int NBARS = 3 * STAGES + 2 * NACC + 6 + (GATHER ? IDS_AHEAD : 0) + 1;
+    // q_full, q_ready, q_empty per slot; ids_full, ids_free per id slot; drain
+    static constexpr int NBARS = 3 * STAGES + 2 * NACC + 6 + (GATHER ? 2 * IDS_AHEAD : 0) + 1;
     static constexpr int SMEM_BYTES = OFF_BARS + NBARS * 8 + 64 + 1024;  // + alignment slack
     static_assert(NQ <= 4, "B scale rows fit one 128-row layout");
     static_assert(COLS_USED <= 512, "TMEM");
     static_assert(NACC % EPI_GROUPS == 0, "accumulator sets split evenly between epilogue groups");
-    static_assert(!GATHER || (NQ == 1 && UNIT_RECS <= 32), "gather: one block per producer lane");
+    static_assert(!GATHER || (NQ == 1 && UNIT_RECS == 32), "gather: 4 producer threads per block");
+    static_assert(!GATHER || COPY_AHEAD < STAGES, "gather: copies in flight fit the ring");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
@@ -114,7 +118,8 @@ struct ScoreShared {  // small control block after the barriers
     long long count;
 };
 
-// Whole block: this CTA's first unit (g0, t0) and unit count.
+// Whole block (at most 1024 threads): this CTA's first unit (g0, t0) and unit
+// count. part_smem holds at least 65 entries.
 template <class TilesFn>
 __device__ void schedule_range(int ngroups, TilesFn tiles, ScoreShared* sh, long long* part_smem) {
     const int tid = threadIdx.x, nt = blockDim.x;
@@ -122,25 +127,36 @@ __device__ void schedule_range(int ngroups, TilesFn tiles, ScoreShared* sh, long
     const int ga = min(ngroups, tid * per), gb = min(ngroups, ga + per);
     long long mine = 0;
     for (int g = ga; g < gb; ++g) mine += tiles(g);
-    part_smem[tid] = mine;
+    // exclusive prefix of the per-thread counts: warp scans, then a scan of warp totals
+    const int lane = tid & 31, wid = tid >> 5, nw = (nt + 31) >> 5;
+    long long incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) part_smem[wid] = incl;
     __syncthreads();
-    if (tid == 0) {
-        long long run = 0;
-        for (int i = 0; i < nt; ++i) {
-            const long long v = part_smem[i];
-            part_smem[i] = run;
-            run += v;
+    if (wid == 0) {
+        long long wt = lane < nw ? part_smem[lane] : 0, wincl = wt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long v = __shfl_up_sync(0xFFFFFFFFu, wincl, o);
+            if (lane >= o) wincl += v;
         }
-        part_smem[nt] = run;
-        sh->count = 0;
-        sh->g0 = ngroups;
-        sh->t0 = 0;
+        if (lane < nw) part_smem[32 + lane] = wincl - wt;  // exclusive warp offsets
+        if (lane == 31) part_smem[64] = wincl;              // total
+        if (lane == 0) {
+            sh->count = 0;
+            sh->g0 = ngroups;
+            sh->t0 = 0;
+        }
     }
     __syncthreads();
-    const long long total = part_smem[nt];
+    const long long base = part_smem[32 + wid] + incl - mine;
+    const long long total = part_smem[64];
     const long long lo = total * blockIdx.x / gridDim.x;
     const long long hi = total * (blockIdx.x + 1) / gridDim.x;
-    const long long base = part_smem[tid];
     if (lo < hi && mine > 0 && lo >= base && lo < base + mine) {
         long long run = base;
         for (int g = ga; g < gb; ++g) {
@@ -164,9 +180,20 @@ __device__ __forceinline__ bool wait_role(uint64_t* bar, uint32_t parity, ScoreS
 // Trace slots: which role waited on what (only with -DHSI_TRACE).
 enum : int {
     TR_PROD_QEMPTY = 0, TR_PROD_EMPTY, TR_PROD_IDS, TR_SF_QFULL, TR_SF_FULL, TR_MMA_QREADY, TR_MMA_SFREADY,
-    TR_MMA_ACCEMPTY, TR_EPI_ACCFULL, TR_PROD_TOTAL = 16, TR_SF_TOTAL, TR_MMA_TOTAL, TR_EPI_TOTAL, TR_UNITS
+    TR_MMA_ACCEMPTY, TR_EPI_ACCFULL, TR_MMA_ISSUE, TR_SF_WORK, TR_EPI_WORK, TR_PROD_ISSUE,
+    TR_PROD_TOTAL = 16, TR_SF_TOTAL, TR_MMA_TOTAL, TR_EPI_TOTAL, TR_UNITS
 };
 
+#ifdef HSI_TRACE
+#define HSI_TSTART(v) const long long v = clock64()
+#define HSI_TEND(v, slot) tr.add(slot, (unsigned long long)(clock64() - v))
+#else
+#define HSI_TSTART(v)
+#define HSI_TEND(v, slot)
+#endif
+
+// Whole warp: wait, then agree, so that a warp leaves its loop as one (its
+// .sync.aligned tcgen05 instructions and __syncwarp need every lane).
 __device__ __forceinline__ bool wait_traced(uint64_t* bar, uint32_t parity, ScoreShared* sh, WaitTrace& tr,
                                             int slot) {
 #ifdef HSI_TRACE
@@ -174,12 +201,12 @@ __device__ __forceinline__ bool wait_traced(uint64_t* bar, uint32_t parity, Scor
     const long long t0 = clock64();
     const bool ok = wait_role(bar, parity, sh);
     tr.add(slot, (unsigned long long)(clock64() - t0));
-    return ok;
 #else
     (void)tr;
     (void)slot;
-    return wait_role(bar, parity, sh);
+    const bool ok = wait_role(bar, parity, sh);
 #endif
+    return __all_sync(0xFFFFFFFFu, ok);
 }
 
 // Bounded wait that ignores the abort flag (teardown: drain what is in flight).
@@ -225,6 +252,27 @@ struct UnitIter {
     }
 };
 
+// Position in a ring of n slots and the phase parity of the current lap.
+struct Ring {
+    int i = 0;
+    uint32_t ph = 0;
+    __device__ __forceinline__ void next(int n) {
+        if (++i == n) {
+            i = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // The scales of rows r, r+32, r+64, r+96 of records at `recs` (nrows valid
 // rows) in the layout of one 32-lane TMEM quarter: column c holds row r+32c,
 // columns 0-3 the first 64 values (K step 0), columns 4-7 the last 64.
@@ -257,18 +305,25 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
     uint64_t* q_ready = q_full + 2;
     uint64_t* q_empty = q_ready + 2;
     uint64_t* ids_full = q_empty + 2;
-    uint64_t* drain = ids_full + (GATHER ? IDS_AHEAD : 0);
+    uint64_t* ids_free = ids_full + (GATHER ? IDS_AHEAD : 0);
+    uint64_t* drain = ids_free + (GATHER ? IDS_AHEAD : 0);
     ScoreShared* sh = reinterpret_cast<ScoreShared*>(bars + C::NBARS);
-    __shared__ long long part[C::THREADS + 1];
+    __shared__ long long part[65];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#ifdef HSI_TRACE
+    if (threadIdx.x == 0 && blockIdx.x < 1024) g_hsi_marks[blockIdx.x][0] = globaltimer_ns();
+#endif
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
+    if (warp == 0) {
+        for (int s = lane; s < STAGES; s += 32) {
+            mbar_init(&full[s], GATHER ? C::PROD_WARPS : 1);
             mbar_init(&sfready[s], 4);
             mbar_init(&empty[s], 1);
         }
+        fence_mbar_init();
+    }
+    if (threadIdx.x == 0) {
         for (int i = 0; i < C::NACC; ++i) {
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_empty[i], 4);
@@ -279,12 +334,15 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
             mbar_init(&q_empty[i], 1);
         }
         if (GATHER)
-            for (int i = 0; i < IDS_AHEAD; ++i) mbar_init(&ids_full[i], 1);
+            for (int i = 0; i < IDS_AHEAD; ++i) {
+                mbar_init(&ids_full[i], 1);
+                mbar_init(&ids_free[i], C::PROD_WARPS);
+            }
         mbar_init(drain, 1);
         sh->abort = 0;
         fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(&sh->tmem_base, C::TMEM_COLS);
+    if (warp == C::MMA_WARP) tmem_alloc(&sh->tmem_base, C::TMEM_COLS);
     schedule_range(p.ngroups, [&](int g) { return group_units<NQ, GATHER, UT>(p, g); }, sh, part);
     tc_fence_before();
     __syncthreads();
@@ -294,32 +352,39 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
     WaitTrace tr;
 #ifdef HSI_TRACE
     const long long t_start = clock64();
+    if (threadIdx.x == 0 && blockIdx.x < 1024) g_hsi_marks[blockIdx.x][1] = globaltimer_ns();
 #endif
 
-    if (warp == 0) {
+    if (warp < C::PROD_WARPS) {
         // ------------------------------------------------------------ producer
+        // warp 0 lane 0 also loads each group's q records and (gather) the
+        // block ids, IDS_AHEAD units ahead.
         UnitIter<NQ, GATHER, UT> it;
         it.init(p, sh);
         UnitIter<NQ, GATHER, UT> ahead;  // gather: the unit whose block ids are fetched next
         ahead.init(p, sh);
-        long long fetched = 0;
-        auto fetch_ids = [&]() {  // lane 0: bulk-copy the block ids of unit `fetched`
+        long long fetched = 0;  // kept identical in every lane of warp 0
+        const bool leader = threadIdx.x == 0;
+        auto fetch_ids = [&]() {  // warp 0: lane 0 bulk-copies the block ids of unit `fetched`
             const int slot = (int)(fetched % IDS_AHEAD);
-            mbar_arrive_expect_tx(&ids_full[slot], C::UNIT_RECS * 4);
-            bulk_g2s(ids_ring + slot * C::UNIT_RECS,
-                     p.block_ids + (int64_t)ahead.g * p.n_keep + (int64_t)ahead.t * C::UNIT_RECS, C::UNIT_RECS * 4,
-                     &ids_full[slot]);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&ids_full[slot], C::UNIT_RECS * 4);
+                bulk_g2s(ids_ring + slot * C::UNIT_RECS,
+                         p.block_ids + (int64_t)ahead.g * p.n_keep + (int64_t)ahead.t * C::UNIT_RECS,
+                         C::UNIT_RECS * 4, &ids_full[slot]);
+            }
             ahead.next(p);
             ++fetched;
         };
-        if (GATHER && lane == 0)
-            while (fetched < count && fetched < IDS_AHEAD) fetch_ids();
+        if (GATHER && warp == 0)
+            while (fetched < count && fetched < IDS_AHEAD - 1) fetch_ids();
         int cur_g = -1, gc = -1;
         int64_t k_base = 0;    // first record of the group's cache
         int64_t nrec_all = 0;  // records holding visible keys
         int nk = 0;            // gather: kept blocks
         long long issued_units = 0;
         int last_q_gc[2] = {-1, -1};
+        Ring st;
         for (long long u = 0; u < count; ++u) {
             const int g = it.g, t = it.t;
             if (g != cur_g) {
@@ -333,73 +398,99 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                 nrec_all = (maxv + 7) / 8;
                 if (GATHER) nk = min(p.n_kept[b0], p.n_keep);
                 const int slot = gc & 1;
-                if (!wait_traced(&q_empty[slot], ((gc >> 1) & 1) ^ 1, sh, tr, TR_PROD_QEMPTY)) break;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&q_full[slot], C::Q_BYTES);
-                    bulk_g2s(qslots + slot * C::QSLOT_BYTES, p.q_rec + (int64_t)g * NQ * 4 * REC, C::Q_BYTES,
-                             &q_full[slot]);
+                if (warp == 0) {
+                    if (!wait_traced(&q_empty[slot], ((gc >> 1) & 1) ^ 1, sh, tr, TR_PROD_QEMPTY)) break;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&q_full[slot], C::Q_BYTES);
+                        bulk_g2s(qslots + slot * C::QSLOT_BYTES, p.q_rec + (int64_t)g * NQ * 4 * REC, C::Q_BYTES,
+                                 &q_full[slot]);
+                    }
+                    last_q_gc[slot] = gc;
                 }
-                last_q_gc[slot] = gc;
             }
-            const int s = (int)(u % STAGES);
-            const uint32_t ph = (uint32_t)((u / STAGES) & 1);
             if (GATHER) {
                 const int islot = (int)(u % IDS_AHEAD);
                 if (!wait_traced(&ids_full[islot], (uint32_t)((u / IDS_AHEAD) & 1), sh, tr, TR_PROD_IDS)) break;
             }
-            if (!wait_traced(&empty[s], ph ^ 1, sh, tr, TR_PROD_EMPTY)) break;
-            uint8_t* dst = stages + s * C::STAGE_BYTES;
+            if (!wait_traced(&empty[st.i], st.ph ^ 1u, sh, tr, TR_PROD_EMPTY)) break;
+            HSI_TSTART(t_prod);
+            uint8_t* dst = stages + st.i * C::STAGE_BYTES;
             if (!GATHER) {
                 const int nrec = (int)min((int64_t)C::UNIT_RECS, nrec_all - (int64_t)t * C::UNIT_RECS);
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)(nrec * REC));
+                    mbar_arrive_expect_tx(&full[st.i], (uint32_t)(nrec * REC));
                     bulk_g2s(dst, p.k_rec + (k_base + (int64_t)t * C::UNIT_RECS) * REC, (uint32_t)(nrec * REC),
-                             &full[s]);
+                             &full[st.i]);
                 }
             } else {
-                const int j = t * C::UNIT_RECS + lane;
-                bool ok = false;
-                int64_t id = 0;
-                if (lane < C::UNIT_RECS && j < nk) {
-                    id = ids_ring[(u % IDS_AHEAD) * C::UNIT_RECS + lane];
-                    ok = id >= 0 && id < nrec_all;
-                    if (!ok) raise_error(DEVERR_ARG);
-                }
-                const uint32_t m = __ballot_sync(0xFFFFFFFFu, ok);
-                __syncwarp();  // every lane has read its id before the slot is refilled
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)(__popc(m) * REC));
-                    if (fetched < count) {
-                        fence_proxy_async_smem();  // the slot's reads precede the copy that refills it
-                        fetch_ids();
-                    }
-                }
+                // 4 threads per pooled block, 9 x 16 bytes each (576 B per block)
+                const int islot = (int)(u % IDS_AHEAD);
+                const int blk = threadIdx.x >> 2, prt = threadIdx.x & 3;
+                const int j = t * C::UNIT_RECS + blk;
+                const int64_t id = ids_ring[islot * C::UNIT_RECS + blk];
                 __syncwarp();
-                if (ok) bulk_g2s(dst + lane * REC, p.k_rec + (k_base + id) * REC, REC, &full[s]);
+                if (lane == 0) mbar_arrive(&ids_free[islot]);
+                const bool ok = j < nk && id >= 0 && id < nrec_all;
+                if (j < nk && !ok && prt == 0) raise_error(DEVERR_ARG);
+                if (ok) {
+                    const uint8_t* src = p.k_rec + (k_base + id) * REC;
+                    uint8_t* d = dst + blk * REC;
+#pragma unroll
+                    for (int c = 0; c < 9; ++c) cp_async16(d + (c * 4 + prt) * 16, src + (c * 4 + prt) * 16);
+                }
+                cp_async_commit();
+                // refill the id slot of the previous unit once every producer warp has read it
+                if (warp == 0 && fetched < count) {
+                    if (u >= 1) {
+                        const int prev = (int)((u - 1) % IDS_AHEAD);
+                        if (!wait_traced(&ids_free[prev], (uint32_t)(((u - 1) / IDS_AHEAD) & 1), sh, tr,
+                                         TR_PROD_IDS))
+                            break;
+                        fence_proxy_async_smem();  // the slot's reads precede the copy that refills it
+                    }
+                    fetch_ids();
+                }
+                // the unit COPY_AHEAD back has landed: publish it
+                if (u >= C::COPY_AHEAD) {
+                    cp_async_wait<C::COPY_AHEAD>();
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&full[(st.i + STAGES - C::COPY_AHEAD) % STAGES]);
+                }
             }
             issued_units = u + 1;
+            HSI_TEND(t_prod, TR_PROD_ISSUE);
+            st.next(STAGES);
             it.next(p);
         }
-        // drain: every copy issued must have landed before the CTA exits
-        if (lane == 0) {
-            for (int s = 0; s < STAGES && s < issued_units; ++s) {
-                const long long last = s + ((issued_units - 1 - s) / STAGES) * STAGES;  // last unit on stage s
-                wait_drain(&full[s], (uint32_t)((last / STAGES) & 1));
-            }
+        if (GATHER) {
+            // publish the units still in flight, then nothing is left pending
+            cp_async_wait<0>();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                for (long long v = issued_units > C::COPY_AHEAD ? issued_units - C::COPY_AHEAD : 0; v < issued_units;
+                     ++v)
+                    mbar_arrive(&full[(int)(v % STAGES)]);
+        }
+        // drain: every bulk copy issued must have landed before the CTA exits
+        if (leader) {
+            if (!GATHER)
+                for (long long v = issued_units > STAGES ? issued_units - STAGES : 0; v < issued_units; ++v)
+                    wait_drain(&full[(int)(v % STAGES)], (uint32_t)((v / STAGES) & 1));
             for (int slot = 0; slot < 2; ++slot)
                 if (last_q_gc[slot] >= 0) wait_drain(&q_full[slot], (uint32_t)((last_q_gc[slot] >> 1) & 1));
             if (GATHER)
-                for (int i = 0; i < IDS_AHEAD && i < fetched; ++i) {
-                    const long long last = i + ((fetched - 1 - i) / IDS_AHEAD) * IDS_AHEAD;
-                    wait_drain(&ids_full[i], (uint32_t)((last / IDS_AHEAD) & 1));
-                }
+                for (long long v = fetched > IDS_AHEAD ? fetched - IDS_AHEAD : 0; v < fetched; ++v)
+                    wait_drain(&ids_full[(int)(v % IDS_AHEAD)], (uint32_t)((v / IDS_AHEAD) & 1));
         }
-    } else if (warp == 1) {
+    } else if (warp == C::MMA_WARP) {
         // ----------------------------------------------------------------- MMA
         UnitIter<NQ, GATHER, UT> it;
         it.init(p, sh);
         int cur_g = -1, gc = -1;
         constexpr uint32_t idesc = idesc_nvf4(128, C::N);
+        Ring st, ac;
         for (long long u = 0; u < count; ++u) {
             if (it.g != cur_g) {
                 if (cur_g >= 0 && lane == 0) tc_commit(&q_empty[gc & 1]);  // old slot free once its MMAs finish
@@ -407,31 +498,31 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                 ++gc;
                 if (!wait_traced(&q_ready[gc & 1], (gc >> 1) & 1, sh, tr, TR_MMA_QREADY)) break;
             }
-            const int s = (int)(u % STAGES);
-            const uint32_t ph = (uint32_t)((u / STAGES) & 1);
-            const int a = (int)(u % C::NACC);
-            const uint32_t aph = (uint32_t)((u / C::NACC) & 1);
-            if (!wait_traced(&sfready[s], ph, sh, tr, TR_MMA_SFREADY)) break;
-            if (!wait_traced(&acc_empty[a], aph ^ 1, sh, tr, TR_MMA_ACCEMPTY)) break;
+            if (!wait_traced(&sfready[st.i], st.ph, sh, tr, TR_MMA_SFREADY)) break;
+            if (!wait_traced(&acc_empty[ac.i], ac.ph ^ 1u, sh, tr, TR_MMA_ACCEMPTY)) break;
+            HSI_TSTART(t_issue);
             if (lane == 0) {
                 tc_fence_after();
-                const uint32_t a0 = smem_u32(stages + s * C::STAGE_BYTES);
+                const uint32_t a0 = smem_u32(stages + st.i * C::STAGE_BYTES);
                 const uint32_t b0 = smem_u32(qslots + (gc & 1) * C::QSLOT_BYTES);
                 const uint32_t sfb = tmem + C::COL_SFB + (gc & 1) * 8;
 #pragma unroll
-                for (int st = 0; st < UT; ++st) {
-                    const uint32_t d = tmem + C::COL_ACC + (a * UT + st) * C::N;
-                    const uint32_t sfa = tmem + C::COL_SFA + (s * UT + st) * 8;
-                    const uint32_t at = a0 + st * 16 * REC;
+                for (int sub = 0; sub < UT; ++sub) {
+                    const uint32_t d = tmem + C::COL_ACC + (ac.i * UT + sub) * C::N;
+                    const uint32_t sfa = tmem + C::COL_SFA + (st.i * UT + sub) * 8;
+                    const uint32_t at = a0 + sub * 16 * REC;
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk)
                         mma_nvf4(d, smem_desc(at + kk * 256, 128, REC), smem_desc(b0 + kk * 256, 128, REC), idesc,
                                  sfa + kk * 4, sfb + kk * 4, kk);
                 }
-                tc_commit(&empty[s]);
-                tc_commit(&acc_full[a]);
+                // one commit: the epilogue that sees it also frees the stage
+                tc_commit(&acc_full[ac.i]);
             }
             __syncwarp();
+            HSI_TEND(t_issue, TR_MMA_ISSUE);
+            st.next(STAGES);
+            ac.next(C::NACC);
             it.next(p);
         }
         // drain: every MMA into TMEM done before the allocation is freed
@@ -446,6 +537,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
         UnitIter<NQ, GATHER, UT> it;
         it.init(p, sh);
         int cur_g = -1, gc = -1;
+        Ring st;
         for (long long u = 0; u < count; ++u) {
             if (it.g != cur_g) {
                 cur_g = it.g;
@@ -459,25 +551,27 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&q_ready[slot]);
             }
-            const int s = (int)(u % STAGES);
-            const uint32_t ph = (uint32_t)((u / STAGES) & 1);
-            if (!wait_traced(&full[s], ph, sh, tr, TR_SF_FULL)) break;
-            const uint8_t* st_recs = stages + s * C::STAGE_BYTES;
+            if (!wait_traced(&full[st.i], st.ph, sh, tr, TR_SF_FULL)) break;
+            const uint8_t* st_recs = stages + st.i * C::STAGE_BYTES;
+            HSI_TSTART(t_sf);
 #pragma unroll
-            for (int st = 0; st < UT; ++st) {
+            for (int sub = 0; sub < UT; ++sub) {
                 uint32_t v[8];
-                sf_quarter(st_recs + st * 16 * REC, TILE_KEYS, lane, v);
-                tmem_st8_wait(tmem + lane_base + C::COL_SFA + (s * UT + st) * 8, v);
+                sf_quarter(st_recs + sub * 16 * REC, TILE_KEYS, lane, v);
+                tmem_st8_wait(tmem + lane_base + C::COL_SFA + (st.i * UT + sub) * 8, v);
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sfready[s]);
+            if (lane == 0) mbar_arrive(&sfready[st.i]);
+            HSI_TEND(t_sf, TR_SF_WORK);
+            st.next(STAGES);
             it.next(p);
         }
     } else {
         // ------------------------------------------------------------ epilogue
         const int grp = (warp - C::FIRST_EPI_WARP) >> 2;
         const int quarter = warp & 3;
+        const bool group_leader = (warp - C::FIRST_EPI_WARP) % 4 == 0 && lane == 0;
         const int row = quarter * 32 + lane;  // key within a 128-key tile
         UnitIter<NQ, GATHER, UT> it;
         it.init(p, sh);
@@ -485,11 +579,17 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
         float wq[NQ][32];
         int nv[NQ];
         int nk = 0;
+        Ring st, ac;
+        int turn = 0;
         for (long long u = 0; u < count; ++u) {
-            if ((int)(u % C::EPI_GROUPS) != grp) {
+            if (turn != grp) {
+                if (++turn == C::EPI_GROUPS) turn = 0;
+                st.next(STAGES);
+                ac.next(C::NACC);
                 it.next(p);
                 continue;
             }
+            if (++turn == C::EPI_GROUPS) turn = 0;
             const int g = it.g, t = it.t;
             if (g != cur_g) {
                 cur_g = g;
@@ -510,23 +610,24 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                 }
                 if (GATHER) nk = min(p.n_kept[g], p.n_keep);
             }
-            const int a = (int)(u % C::NACC);
-            const uint32_t aph = (uint32_t)((u / C::NACC) & 1);
             // gather: the positions of this thread's slots, loaded before the wait
             int64_t pos[UT];
 #pragma unroll
-            for (int st = 0; st < UT; ++st) {
-                pos[st] = -1;
-                const int slot_i = (t * UT + st) * TILE_KEYS + row;
+            for (int sub = 0; sub < UT; ++sub) {
+                pos[sub] = -1;
+                const int slot_i = (t * UT + sub) * TILE_KEYS + row;
                 if (GATHER && (slot_i >> 3) < nk)
-                    pos[st] = (int64_t)__ldg(p.block_ids + (int64_t)g * p.n_keep + (slot_i >> 3)) * 8 + (slot_i & 7);
+                    pos[sub] = (int64_t)__ldg(p.block_ids + (int64_t)g * p.n_keep + (slot_i >> 3)) * 8 + (slot_i & 7);
             }
-            if (!wait_traced(&acc_full[a], aph, sh, tr, TR_EPI_ACCFULL)) break;
+            if (!wait_traced(&acc_full[ac.i], ac.ph, sh, tr, TR_EPI_ACCFULL)) break;
+            HSI_TSTART(t_epi);
             tc_fence_after();
+            if (group_leader) mbar_arrive(&empty[st.i]);  // the MMAs have read the stage
 #pragma unroll
-            for (int st = 0; st < UT; ++st) {
-                const uint32_t dbase = tmem + ((uint32_t)(quarter * 32) << 16) + C::COL_ACC + (a * UT + st) * C::N;
-                const int key = (t * UT + st) * TILE_KEYS + row;  // key (full scan) or pool slot (gather)
+            for (int sub = 0; sub < UT; ++sub) {
+                const uint32_t dbase =
+                    tmem + ((uint32_t)(quarter * 32) << 16) + C::COL_ACC + (ac.i * UT + sub) * C::N;
+                const int key = (t * UT + sub) * TILE_KEYS + row;  // key (full scan) or pool slot (gather)
 #pragma unroll
                 for (int qi = 0; qi < NQ; ++qi) {
                     float x[32];
@@ -551,30 +652,40 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                             m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
                             if ((lane & 7) == 0 && vis) p.bmax[(int64_t)b * p.ldb + key / 8] = m;
                         }
-                    } else if (pos[st] >= 0) {
-                        const float v = pos[st] < nv[qi] ? sc : __uint_as_float(0xFF800000u);
+                    } else if (pos[sub] >= 0) {
+                        const float v = pos[sub] < nv[qi] ? sc : __uint_as_float(0xFF800000u);
                         p.pool_scores[(int64_t)b * p.ld_pool + key] = v;
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[a]);
+            if (lane == 0) mbar_arrive(&acc_empty[ac.i]);
+            HSI_TEND(t_epi, TR_EPI_WORK);
+            st.next(STAGES);
+            ac.next(C::NACC);
             it.next(p);
         }
     }
 #ifdef HSI_TRACE
-    if (lane == 0 && (warp <= C::FIRST_SF_WARP || warp == C::FIRST_EPI_WARP)) {
-        const int slot = warp == 0 ? TR_PROD_TOTAL : warp == 1 ? TR_MMA_TOTAL : warp == 2 ? TR_SF_TOTAL : TR_EPI_TOTAL;
+    if (lane == 0 && (warp == 0 || warp == C::MMA_WARP || warp == C::FIRST_SF_WARP || warp == C::FIRST_EPI_WARP)) {
+        const int slot = warp == 0 ? TR_PROD_TOTAL
+                         : warp == C::MMA_WARP ? TR_MMA_TOTAL
+                         : warp == C::FIRST_SF_WARP ? TR_SF_TOTAL
+                                                    : TR_EPI_TOTAL;
         tr.add(slot, (unsigned long long)(clock64() - t_start));
         if (warp == 0) tr.add(TR_UNITS, (unsigned long long)count);
         tr.flush();
+        if (warp == 0 && blockIdx.x < 1024) g_hsi_marks[blockIdx.x][2] = globaltimer_ns();
     }
 #endif
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+    if (warp == C::MMA_WARP) tmem_dealloc(tmem, C::TMEM_COLS);
+#ifdef HSI_TRACE
+    if (threadIdx.x == 0 && blockIdx.x < 1024) g_hsi_marks[blockIdx.x][3] = globaltimer_ns();
+#endif
 }
 
 }  // namespace hsi
