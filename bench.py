@@ -219,6 +219,7 @@ class DeviceWorkload:
         self.val = self.out_dev[L * B * K_TOP * 4:].view(torch.float32).view(L, B, K_TOP)
         self.ws_q = hsi.workspace(hsi.WS_QUANTIZE, B, 0, device=dev)
         self.ws_topk = hsi.workspace(hsi.WS_TOPK, B, self.maxv, K_TOP, device=dev)
+        self.ws_full = hsi.workspace(hsi.WS_FULL_LAYER, B, self.maxv, K_TOP, device=dev)
         if wl.build_pool:
             self.ids = torch.empty(B, wl.n_keep, dtype=torch.int32, device=dev)
             self.nk = torch.empty(B, dtype=torch.int32, device=dev)
@@ -226,42 +227,19 @@ class DeviceWorkload:
             self.bits = torch.empty(B, (self.maxv + 31) // 32, dtype=torch.int32, device=dev)
             self.ws_pool = hsi.workspace(hsi.WS_POOL, B, self.maxv, 8, device=dev)
             self.pool_scores = torch.empty(B, wl.n_keep * 8, dtype=torch.float32, device=dev)
-            self.ws_rtopk = hsi.workspace(hsi.WS_TOPK, B, wl.n_keep * 8, K_TOP, device=dev)
+            self.ws_rtopk = hsi.workspace(hsi.WS_REINDEX_LAYER, B, wl.n_keep * 8, K_TOP, device=dev)
         self.ev_score = []
         self.pool_sum = None
         self.wl_signs = signs
         self.graphs = []
 
-    def step(self, time_score=False):
-        """One step as individual launches (no graph)."""
-        hsi, wl, B = self.hsi, self.wl, self.B
-        torch = self.torch
-        signs = self.wl_signs
-        for l in range(wl.full_layers):
-            hsi.quantize_nvfp4(self.q[l], B, 32, signs, self.g_q[l], self.q_rec[l], ws=self.ws_q)
-            if time_score:
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-            hsi.score_full(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[l], self.g_k[l], self.k_off, self.n_vis,
-                           B, self.maxv, self.scores, block_max=self.bmax if wl.build_pool else None)
-            if time_score:
-                e1.record()
-                self.ev_score.append((e0, e1))
-            hsi.topk(self.scores, self.n_vis, B, self.maxv, K_TOP, self.idx[l], self.val[l], ws=self.ws_topk)
-        if not wl.build_pool:
-            return
-        hsi.candidate_pool(self.n_vis, B, self.maxv, self.ids, self.nk, self.npool, block_max=self.bmax,
-                           block_size=wl.block_size, n_keep=wl.n_keep, pool_bits=self.bits, ws=self.ws_pool)
-        for r in range(wl.reindex_layers):
-            l = wl.full_layers + r
-            hsi.quantize_nvfp4(self.q[l], B, 32, signs, self.g_q[l], self.q_rec[l], ws=self.ws_q)
-            hsi.score_pool(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0], self.k_off, self.n_vis,
-                           self.ids, self.nk, wl.n_keep, B, self.pool_scores)
-            hsi.topk(self.pool_scores, self.npool, B, wl.n_keep * 8, K_TOP, self.idx[l], self.val[l],
-                     block_ids=self.ids, ws=self.ws_rtopk)
+    def step(self):
+        """One step as individual launches (the same calls the graphs hold)."""
+        for _, fn in self.segments():
+            fn()
 
-    # -- the step as CUDA graphs: [q quantisation] [score_full] [the rest], per
-    # Full layer, so that the scoring kernel can be timed between replays
+    # -- the step as CUDA graphs: [q quantisation] [scoring] [selection and the
+    # rest], per Full layer, so that the scoring kernel can be timed between replays
     def segments(self):
         hsi, wl, B = self.hsi, self.wl, self.B
         signs = self.wl_signs
@@ -269,22 +247,24 @@ class DeviceWorkload:
         for l in range(wl.full_layers):
             segs.append(("pre", lambda l=l: hsi.quantize_nvfp4(self.q[l], B, 32, signs, self.g_q[l], self.q_rec[l],
                                                                ws=self.ws_q)))
-            segs.append(("score", lambda l=l: hsi.score_full(
-                self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[l], self.g_k[l], self.k_off, self.n_vis, B,
-                self.maxv, self.scores, block_max=self.bmax if wl.build_pool else None)))
-            segs.append(("post", lambda l=l: hsi.topk(self.scores, self.n_vis, B, self.maxv, K_TOP, self.idx[l],
-                                                      self.val[l], ws=self.ws_topk)))
+            # the Full layer (scores, top-512, pool) as the fused call, issued as
+            # its two phases so that the scoring kernel can be timed alone
+            pool = wl.build_pool and l == wl.full_layers - 1
+            for kind, ph in (("score", 1), ("post", 2)):
+                segs.append((kind, lambda l=l, pool=pool, ph=ph: hsi.full_layer(
+                    self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[l], self.g_k[l], self.k_off, self.n_vis, B,
+                    self.maxv, self.scores, K_TOP, self.idx[l], self.val[l],
+                    block_ids=self.ids if pool else None, n_kept=self.nk if pool else None,
+                    n_pool=self.npool if pool else None, pool_bits=self.bits if pool else None,
+                    n_keep=wl.n_keep, ws=self.ws_full, phases=ph)))
         if wl.build_pool:
             def rest():
-                hsi.candidate_pool(self.n_vis, B, self.maxv, self.ids, self.nk, self.npool, block_max=self.bmax,
-                                   block_size=wl.block_size, n_keep=wl.n_keep, pool_bits=self.bits, ws=self.ws_pool)
                 for r in range(wl.reindex_layers):
                     l = wl.full_layers + r
                     hsi.quantize_nvfp4(self.q[l], B, 32, signs, self.g_q[l], self.q_rec[l], ws=self.ws_q)
-                    hsi.score_pool(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0], self.k_off,
-                                   self.n_vis, self.ids, self.nk, wl.n_keep, B, self.pool_scores)
-                    hsi.topk(self.pool_scores, self.npool, B, wl.n_keep * 8, K_TOP, self.idx[l], self.val[l],
-                             block_ids=self.ids, ws=self.ws_rtopk)
+                    hsi.reindex_layer(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0], self.k_off,
+                                      self.n_vis, self.ids, self.nk, self.npool, B, self.pool_scores, K_TOP,
+                                      self.idx[l], self.val[l], n_keep=wl.n_keep, ws=self.ws_rtopk)
             segs.append(("post", rest))
         merged = []
         for kind, fn in segs:  # fuse neighbouring non-scoring segments into one graph

@@ -215,11 +215,63 @@ hsi_status hsi_score_pool(const uint8_t* q_rec, const float* g_q, const float* w
                           const int32_t* block_ids, const int32_t* n_kept, int32_t n_keep, int32_t B,
                           float* pool_scores, int64_t ld, void* ws, size_t ws_bytes, cudaStream_t stream);
 
-typedef enum { HSI_WS_QUANTIZE = 0, HSI_WS_SCORE = 1, HSI_WS_TOPK = 2, HSI_WS_POOL = 3 } hsi_ws_kind;
+/*
+ * A decoder Full layer in one call: hsi_score_full, then the top-k of the
+ * scores, then (block_ids != NULL) the candidate pool with blocks of 8, with
+ * the selections' key histograms accumulated inside the scoring kernel
+ * instead of in separate passes. Results equal those of the three separate
+ * calls (same scores, same top-k, same pool).
+ * Page: "DeepSeek-V4.1 模型结构（3）", section "用浅层的打分结果限制深层的打分范围"
+ * (the Full layer scores every visible position, keeps its top-512 and builds
+ * the pool from the same scores).
+ *
+ *  Arguments as in hsi_score_full (group 1), hsi_topk (n_valid = n_visible)
+ *  and hsi_candidate_pool (block_size 8). scores [B][ld] is written.
+ *  block_ids NULL: no pool (n_kept, n_pool, pool_bits ignored).
+ *  phases  HSI_PHASE_ALL, or the two halves as separate calls with the same
+ *          arguments and workspace, scoring first (the workspace carries the
+ *          histograms from one to the other): HSI_PHASE_SCORE, HSI_PHASE_SELECT.
+ *  ws      (dev) hsi_workspace_size(HSI_WS_FULL_LAYER, B, max_visible, k).
+ */
+#define HSI_PHASE_SCORE 1
+#define HSI_PHASE_SELECT 2
+#define HSI_PHASE_ALL 3
+hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
+                          const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible, int32_t B,
+                          int64_t max_visible, float* scores, int64_t ld, int32_t k, int32_t* top_idx,
+                          float* top_val, int32_t n_keep, int32_t* block_ids, int32_t* n_kept, int32_t* n_pool,
+                          uint32_t* pool_bits, int64_t ld_bits, int32_t phases, void* ws, size_t ws_bytes,
+                          cudaStream_t stream);
+
+/*
+ * A decoder Reindex layer in one call: hsi_score_pool, then the top-k inside
+ * the pool reported as global positions (hsi_topk with the block map).
+ * Page: "DeepSeek-V4.1 模型结构（3）", section "用浅层的打分结果限制深层的打分范围"
+ * (Reindex layers score only pooled positions and keep their own top-512).
+ *
+ *  n_pool (dev) int32 [B] as written by hsi_candidate_pool / hsi_full_layer.
+ *  pool_scores [B][ld], ld >= 8 * n_keep, is written.
+ *  ws      (dev) hsi_workspace_size(HSI_WS_REINDEX_LAYER, B, 8 * n_keep, k).
+ */
+hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
+                             const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible,
+                             const int32_t* block_ids, const int32_t* n_kept, const int32_t* n_pool, int32_t n_keep,
+                             int32_t B, float* pool_scores, int64_t ld, int32_t k, int32_t* top_idx, float* top_val,
+                             void* ws, size_t ws_bytes, cudaStream_t stream);
+
+typedef enum {
+    HSI_WS_QUANTIZE = 0,
+    HSI_WS_SCORE = 1,
+    HSI_WS_TOPK = 2,
+    HSI_WS_POOL = 3,
+    HSI_WS_FULL_LAYER = 4,
+    HSI_WS_REINDEX_LAYER = 5
+} hsi_ws_kind;
 
 /* Scratch bytes a call needs for B queries of at most max_n entries.
  * QUANTIZE: B = number of tensors (max_n, k unused). SCORE: 0. TOPK: max_n =
- * max_valid (k unused). POOL: max_n = max_visible and k = block_size. */
+ * max_valid (k unused). POOL: max_n = max_visible and k = block_size.
+ * FULL_LAYER: max_n = max_visible. REINDEX_LAYER: max_n = 8 * n_keep. */
 size_t hsi_workspace_size(hsi_ws_kind kind, int32_t B, int64_t max_n, int32_t k);
 
 /* Synchronise `stream`, then report and clear the sticky device error word of

@@ -24,11 +24,11 @@ HEADS, DIM, REC_ROWS, REC_BYTES = 32, 128, 8, 576
 
 STATUS = {0: "HSI_OK", -1: "HSI_ERR_INVALID_ARG", -2: "HSI_ERR_UNSUPPORTED", -3: "HSI_ERR_CUDA",
           -4: "HSI_ERR_DEVICE_TIMEOUT", -5: "HSI_ERR_WORKSPACE", -6: "HSI_ERR_DEVICE_ARG"}
-WS_QUANTIZE, WS_SCORE, WS_TOPK, WS_POOL = 0, 1, 2, 3
+WS_QUANTIZE, WS_SCORE, WS_TOPK, WS_POOL, WS_FULL_LAYER, WS_REINDEX_LAYER = 0, 1, 2, 3, 4, 5
 
 EXPORTS = ["hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
            "hsi_workspace_size", "hsi_device_error", "hsi_device_check", "hsi_status_string",
-           "hsi_kernel_launches", "hsi_calib_read", "hsi_calib_mma"]
+           "hsi_kernel_launches", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer", "hsi_reindex_layer"]
 
 
 class HsiError(RuntimeError):
@@ -66,6 +66,10 @@ def lib() -> ctypes.CDLL:
         L.hsi_topk.argtypes = [vp, i64, vp, i32, i64, i32, vp, i64, i32, vp, vp, vp, sz, vp]
         L.hsi_candidate_pool.argtypes = [vp, i64, vp, i64, vp, i32, i64, i32, i32, vp, vp, vp, vp, i64, vp, sz, vp]
         L.hsi_score_pool.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i64, vp, sz, vp]
+        L.hsi_full_layer.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, vp, i64, i32, vp, vp, i32, vp, vp, vp,
+                                     vp, i64, i32, vp, sz, vp]
+        L.hsi_reindex_layer.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i64, i32, vp, vp, vp,
+                                        sz, vp]
         L.hsi_workspace_size.argtypes = [ctypes.c_int, i32, i64, i32]
         L.hsi_workspace_size.restype = sz
         L.hsi_device_error.argtypes = [vp]
@@ -77,7 +81,8 @@ def lib() -> ctypes.CDLL:
         L.hsi_kernel_launches.argtypes = []
         L.hsi_kernel_launches.restype = ctypes.c_uint64
         for name in ("hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
-                     "hsi_device_error", "hsi_device_check", "hsi_calib_read", "hsi_calib_mma"):
+                     "hsi_device_error", "hsi_device_check", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer",
+                     "hsi_reindex_layer"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -196,3 +201,31 @@ def score_pool(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, block_ids, n_kep
     _check("hsi_score_pool", lib().hsi_score_pool(
         _ptr(q_rec), _ptr(g_q), _ptr(w), _ptr(k_rec), _ptr(g_k), _ptr(k_rec_off), _ptr(n_visible),
         _ptr(block_ids), _ptr(n_kept), n_keep, B, _ptr(pool_scores), ld, None, 0, _stream(stream)))
+
+
+def full_layer(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B, max_visible, scores, k, top_idx, top_val,
+               block_ids=None, n_kept=None, n_pool=None, pool_bits=None, n_keep=2048, ld=None, ld_bits=0, ws=None,
+               phases=3, stream=None):
+    """Full layer: scores, top-k and (block_ids given) the candidate pool.
+    phases: 1 scoring only, 2 selection only (after 1, same workspace), 3 both."""
+    ld = scores.shape[-1] if ld is None else ld
+    if pool_bits is not None and not ld_bits:
+        ld_bits = pool_bits.shape[-1]
+    if ws is None:
+        ws = workspace(WS_FULL_LAYER, B, max_visible, k, device=scores.device)
+    _check("hsi_full_layer", lib().hsi_full_layer(
+        _ptr(q_rec), _ptr(g_q), _ptr(w), _ptr(k_rec), _ptr(g_k), _ptr(k_rec_off), _ptr(n_visible), B, max_visible,
+        _ptr(scores), ld, k, _ptr(top_idx), _ptr(top_val), n_keep, _ptr(block_ids), _ptr(n_kept), _ptr(n_pool),
+        _ptr(pool_bits), ld_bits, phases, _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def reindex_layer(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, block_ids, n_kept, n_pool, B, pool_scores, k,
+                  top_idx, top_val, n_keep=2048, ld=None, ws=None, stream=None):
+    """Reindex layer: pooled scores and the top-k inside the pool (global positions)."""
+    ld = pool_scores.shape[-1] if ld is None else ld
+    if ws is None:
+        ws = workspace(WS_REINDEX_LAYER, B, 8 * n_keep, k, device=pool_scores.device)
+    _check("hsi_reindex_layer", lib().hsi_reindex_layer(
+        _ptr(q_rec), _ptr(g_q), _ptr(w), _ptr(k_rec), _ptr(g_k), _ptr(k_rec_off), _ptr(n_visible), _ptr(block_ids),
+        _ptr(n_kept), _ptr(n_pool), n_keep, B, _ptr(pool_scores), ld, k, _ptr(top_idx), _ptr(top_val), _ptr(ws),
+        0 if ws is None else ws.numel(), _stream(stream)))

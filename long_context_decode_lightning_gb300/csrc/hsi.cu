@@ -18,10 +18,10 @@ using namespace hsi;
 namespace {
 
 // Stage ring depth and 128-key tiles per stage of each scoring variant.
-constexpr int kDecodeStages = 10, kDecodeUT = 2;
+constexpr int kDecodeStages = 8, kDecodeUT = 2;
 constexpr int kGatherStages = 10, kGatherUT = 2;
 constexpr int kPrefillStages = 8, kPrefillUT = 1;
-constexpr int kCandCap = 16384;  // survivors of the histogram pass kept per query
+constexpr int kCandCap = 65536;  // survivors of the histogram pass kept per query
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -47,7 +47,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Workspace of the selection passes for B queries of at most max_items items.
 struct SelWs {
     uint32_t* hist;
-    uint32_t* cnt;
+    uint32_t* cnt;  // [B] survivor counts, then [B] threshold bins
     uint32_t* ckey;
     uint32_t* cidx;
     float* bmax;
@@ -57,7 +57,7 @@ size_t sel_ws_bytes(int32_t B, int64_t max_items, bool need_bmax, int64_t max_bl
     size_t s = 0;
     if (max_items > SEL_CAP) {
         s += align_up((size_t)B * HIST_BINS * 4, 256);
-        s += align_up((size_t)B * 4, 256);
+        s += align_up((size_t)B * 8, 256);
         s += 2 * align_up((size_t)B * kCandCap * 4, 256);
     }
     if (need_bmax) s += align_up((size_t)B * (size_t)max_blocks * 4, 256);
@@ -71,7 +71,7 @@ SelWs carve_sel(void* ws, int32_t B, int64_t max_items, bool need_bmax, int64_t 
         w.hist = reinterpret_cast<uint32_t*>(p);
         p += align_up((size_t)B * HIST_BINS * 4, 256);
         w.cnt = reinterpret_cast<uint32_t*>(p);
-        p += align_up((size_t)B * 4, 256);
+        p += align_up((size_t)B * 8, 256);
         w.ckey = reinterpret_cast<uint32_t*>(p);
         p += align_up((size_t)B * kCandCap * 4, 256);
         w.cidx = reinterpret_cast<uint32_t*>(p);
@@ -81,12 +81,18 @@ SelWs carve_sel(void* ws, int32_t B, int64_t max_items, bool need_bmax, int64_t 
     return w;
 }
 
-hsi_status run_select(SelParams sp, int64_t max_items, cudaStream_t s) {
+// The selection passes. With hist_ready, sp.hist already holds the key
+// histogram (fused into the scoring kernel) and the histogram pass is skipped.
+hsi_status run_select(SelParams sp, int64_t max_items, cudaStream_t s, bool hist_ready = false) {
     if (max_items > SEL_CAP) {
-        if (cudaMemsetAsync(sp.hist, 0, (size_t)sp.B * HIST_BINS * 4, s) != cudaSuccess) return HSI_ERR_CUDA;
         if (cudaMemsetAsync(sp.cand_cnt, 0, (size_t)sp.B * 4, s) != cudaSuccess) return HSI_ERR_CUDA;
         const dim3 grid((unsigned)((max_items + SCAN_CHUNK - 1) / SCAN_CHUNK), (unsigned)sp.B);
-        sel_hist_kernel<<<grid, SCAN_THREADS, 0, s>>>(sp);
+        if (!hist_ready) {
+            if (cudaMemsetAsync(sp.hist, 0, (size_t)sp.B * HIST_BINS * 4, s) != cudaSuccess) return HSI_ERR_CUDA;
+            sel_hist_kernel<<<grid, SCAN_THREADS, 0, s>>>(sp);
+            if (launch_ok() != HSI_OK) return HSI_ERR_CUDA;
+        }
+        sel_thresh_kernel<<<sp.B, SCAN_THREADS, 0, s>>>(sp);
         if (launch_ok() != HSI_OK) return HSI_ERR_CUDA;
         sel_collect_kernel<<<grid, SCAN_THREADS, 0, s>>>(sp);
         if (launch_ok() != HSI_OK) return HSI_ERR_CUDA;
@@ -180,6 +186,12 @@ size_t hsi_workspace_size(hsi_ws_kind kind, int32_t B, int64_t max_n, int32_t k)
         case HSI_WS_QUANTIZE: return align_up((size_t)B * 4, 256);
         case HSI_WS_SCORE: return 0;
         case HSI_WS_TOPK: return sel_ws_bytes(B, max_n, false, 0);
+        case HSI_WS_FULL_LAYER: {
+            const int64_t nb = (max_n + 7) / 8;
+            return sel_ws_bytes(B, max_n > nb ? max_n : nb, false, 0) + align_up((size_t)B * HIST_BINS * 4, 256) +
+                   align_up((size_t)B * (size_t)nb * 4, 256);
+        }
+        case HSI_WS_REINDEX_LAYER: return sel_ws_bytes(B, max_n, false, 0);
         case HSI_WS_POOL: {
             // k is the block size here; block maxima are computed into the
             // workspace when they are not given
@@ -207,8 +219,12 @@ hsi_status hsi_quantize_nvfp4(const uint16_t* x, int64_t n_tensors, int64_t rows
     }
     p.g = g;
     p.rec = rec;
+    if (mode == 0 && (!ws || ws_bytes < (size_t)n_tensors * 4 || !aligned(ws, 256))) return HSI_ERR_WORKSPACE;
+    if (rows_per_tensor <= QUANT_SMALL_ROWS && n_tensors <= INT32_MAX) {
+        quant_small_kernel<<<(unsigned)n_tensors, 256, 0, stream>>>(p, mode);
+        return launch_ok();
+    }
     if (mode == 0) {
-        if (!ws || ws_bytes < (size_t)n_tensors * 4 || !aligned(ws, 256)) return HSI_ERR_WORKSPACE;
         p.amax_bits = static_cast<uint32_t*>(ws);
         if (cudaMemsetAsync(ws, 0, (size_t)n_tensors * 4, stream) != cudaSuccess) return HSI_ERR_CUDA;
         const int64_t rows = n_tensors * rows_per_tensor;
@@ -314,6 +330,7 @@ hsi_status hsi_topk(const float* scores, int64_t ld, const int32_t* n_valid, int
     sp.cand_cnt = wsp.cnt;
     sp.cand_key = wsp.ckey;
     sp.cand_idx = wsp.cidx;
+    sp.thr = wsp.cnt ? wsp.cnt + B : nullptr;
     sp.cap = kCandCap;
     sp.block_ids = block_ids;
     sp.ld_blocks = ld_blocks;
@@ -363,6 +380,7 @@ hsi_status hsi_candidate_pool(const float* scores, int64_t ld, const float* bloc
     sp.cand_cnt = wsp.cnt;
     sp.cand_key = wsp.ckey;
     sp.cand_idx = wsp.cidx;
+    sp.thr = wsp.cnt ? wsp.cnt + B : nullptr;
     sp.cap = kCandCap;
     sp.blk_out = block_ids;
     sp.n_kept = n_kept;
@@ -403,6 +421,104 @@ hsi_status hsi_calib_mma(int n, int iters, unsigned long long* sink, cudaStream_
         default: return HSI_ERR_UNSUPPORTED;
     }
     return launch_ok();
+}
+
+hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
+                          const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible, int32_t B,
+                          int64_t max_visible, float* scores, int64_t ld, int32_t k, int32_t* top_idx,
+                          float* top_val, int32_t n_keep, int32_t* block_ids, int32_t* n_kept, int32_t* n_pool,
+                          uint32_t* pool_bits, int64_t ld_bits, int32_t phases, void* ws, size_t ws_bytes,
+                          cudaStream_t stream) {
+    if (phases < 1 || phases > 3) return HSI_ERR_INVALID_ARG;
+    hsi_status st = check_score_common(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B);
+    if (st != HSI_OK) return st;
+    if (!scores || !top_idx || !top_val || max_visible < 0 || max_visible > (int64_t)INT32_MAX - 256 ||
+        ld < max_visible || k < 1 || k > 2048)
+        return HSI_ERR_INVALID_ARG;
+    const bool pool = block_ids != nullptr;
+    if (pool && (!n_kept || !n_pool || n_keep < 1 || n_keep > SEL_MAXK)) return HSI_ERR_INVALID_ARG;
+    if (pool_bits && ld_bits < (max_visible + 31) / 32) return HSI_ERR_INVALID_ARG;
+    const int64_t nb = (max_visible + 7) / 8;
+    const size_t need = hsi_workspace_size(HSI_WS_FULL_LAYER, B, max_visible, k);
+    if (!ws || ws_bytes < need || !aligned(ws, 256)) return HSI_ERR_WORKSPACE;
+    // workspace: selection buffers (shared by the two selections, which run in
+    // turn), the block-max histogram, the block maxima
+    SelWs wsp = carve_sel(ws, B, max_visible > nb ? max_visible : nb, false, 0);
+    uint8_t* tail = static_cast<uint8_t*>(ws) + sel_ws_bytes(B, max_visible > nb ? max_visible : nb, false, 0);
+    uint32_t* bhist = reinterpret_cast<uint32_t*>(tail);
+    float* bmax = reinterpret_cast<float*>(tail + align_up((size_t)B * HIST_BINS * 4, 256));
+    const bool big_topk = max_visible > SEL_CAP, big_pool = pool && nb > SEL_CAP;
+    if (phases & 1) {
+    if (big_topk && cudaMemsetAsync(wsp.hist, 0, (size_t)B * HIST_BINS * 4, stream) != cudaSuccess)
+        return HSI_ERR_CUDA;
+    if (big_pool && cudaMemsetAsync(bhist, 0, (size_t)B * HIST_BINS * 4, stream) != cudaSuccess)
+        return HSI_ERR_CUDA;
+    ScoreParams p{};
+    p.q_rec = q_rec;
+    p.g_q = g_q;
+    p.w = w;
+    p.k_rec = k_rec;
+    p.g_k = g_k;
+    p.k_off = k_rec_off;
+    p.n_vis = n_visible;
+    p.B = B;
+    p.ngroups = B;
+    p.scores = scores;
+    p.ld = ld;
+    p.bmax = pool ? bmax : nullptr;
+    p.ldb = nb;
+    p.key_hist = big_topk ? wsp.hist : nullptr;
+    p.bmax_hist = big_pool ? bhist : nullptr;
+    st = launch_score<1, false, kDecodeStages, kDecodeUT>(p, stream);
+    if (st != HSI_OK) return st;
+    }
+    if (!(phases & 2)) return HSI_OK;
+    SelParams sp{};
+    sp.src = scores;
+    sp.ld = ld;
+    sp.n_src = n_visible;
+    sp.div = 1;
+    sp.B = B;
+    sp.k = k;
+    sp.mode = SEL_TOPK;
+    sp.hist = wsp.hist;
+    sp.cand_cnt = wsp.cnt;
+    sp.cand_key = wsp.ckey;
+    sp.cand_idx = wsp.cidx;
+    sp.thr = wsp.cnt ? wsp.cnt + B : nullptr;
+    sp.cap = kCandCap;
+    sp.out_idx = top_idx;
+    sp.out_val = top_val;
+    st = run_select(sp, max_visible, stream, true);
+    if (st != HSI_OK || !pool) return st;
+    SelParams pp = sp;
+    pp.src = bmax;
+    pp.ld = nb;
+    pp.div = 8;
+    pp.k = n_keep;
+    pp.mode = SEL_POOL;
+    pp.hist = bhist;
+    pp.out_idx = nullptr;
+    pp.out_val = nullptr;
+    pp.blk_out = block_ids;
+    pp.n_kept = n_kept;
+    pp.n_pool = n_pool;
+    pp.bits = pool_bits;
+    pp.ld_bits = ld_bits;
+    return run_select(pp, nb, stream, true);
+}
+
+hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
+                             const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible,
+                             const int32_t* block_ids, const int32_t* n_kept, const int32_t* n_pool, int32_t n_keep,
+                             int32_t B, float* pool_scores, int64_t ld, int32_t k, int32_t* top_idx, float* top_val,
+                             void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!n_pool) return HSI_ERR_INVALID_ARG;
+    hsi_status st = hsi_score_pool(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, block_ids, n_kept, n_keep, B,
+                                   pool_scores, ld, nullptr, 0, stream);
+    if (st != HSI_OK) return st;
+    return hsi_topk(pool_scores, ld, n_pool, B, (int64_t)n_keep * 8, k, block_ids, n_keep, 8, top_idx, top_val, ws,
+                    ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -112,21 +112,16 @@ __device__ __forceinline__ uint32_t f32x4_to_e2m1x4(float a, float b, float c, f
     return out;
 }
 
-__global__ void __launch_bounds__(256) quant_encode_kernel(QuantParams p) {
+// Encode one rotated row (this warp's v, tensor scale g) into row r of tensor
+// t's records; rows at or past rpt are written as zeros.
+__device__ __forceinline__ void encode_row_warp(const QuantParams& p, int64_t t, int64_t r, const float (&v)[4],
+                                                float g) {
     const int lane = threadIdx.x & 31;
-    const int64_t prow = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // padded row index
-    const int64_t padded_rows = p.rec_per_tensor * 8;
-    if (prow >= p.n_tensors * padded_rows) return;
-    const int64_t t = prow / padded_rows;
-    const int64_t r = prow % padded_rows;
     uint8_t* rec = p.rec + (t * p.rec_per_tensor + r / 8) * 576;
     const int rr = (int)(r & 7);
     uint16_t codes = 0;
     uint8_t scale = 0;
     if (r < p.rpt) {
-        float v[4];
-        rotate_row_warp(p, t * p.rpt + r, v);
-        const float g = p.g[t];
         float ab = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
         ab = fmaxf(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 1));
         ab = fmaxf(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 2));  // max over values 16j .. 16j+15
@@ -141,6 +136,59 @@ __global__ void __launch_bounds__(256) quant_encode_kernel(QuantParams p) {
     // values 4*lane .. 4*lane+3 -> two bytes at (e/32)*128 + rr*16 + (e%32)/2
     *reinterpret_cast<uint16_t*>(rec + (lane >> 3) * 128 + rr * 16 + (lane & 7) * 2) = codes;
     if ((lane & 3) == 0) rec[512 + rr * 8 + (lane >> 2)] = scale;
+}
+
+__global__ void __launch_bounds__(256) quant_encode_kernel(QuantParams p) {
+    const int64_t prow = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // padded row index
+    const int64_t padded_rows = p.rec_per_tensor * 8;
+    if (prow >= p.n_tensors * padded_rows) return;
+    const int64_t t = prow / padded_rows;
+    const int64_t r = prow % padded_rows;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (r < p.rpt) rotate_row_warp(p, t * p.rpt + r, v);
+    encode_row_warp(p, t, r, v, r < p.rpt ? p.g[t] : 1.0f);
+}
+
+// Small tensors (at most QUANT_SMALL_ROWS rows, e.g. the 32 heads of a query):
+// one CTA per tensor rotates every row once, finds the tensor scale (mode 0)
+// and encodes, in a single launch.
+constexpr int QUANT_SMALL_ROWS = 64;
+
+__global__ void __launch_bounds__(256) quant_small_kernel(QuantParams p, int mode) {
+    __shared__ float wmax[8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t = blockIdx.x;
+    constexpr int RPW = QUANT_SMALL_ROWS / 8;  // rows per warp
+    float v[RPW][4];
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+        const int64_t r = warp + 8 * i;
+        v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.f;
+        if (r < p.rpt) {
+            rotate_row_warp(p, t * p.rpt + r, v[i]);
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i][0]), fabsf(v[i][1])), fmaxf(fabsf(v[i][2]), fabsf(v[i][3]))));
+        }
+    }
+    float g;
+    if (mode == 0) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        if (lane == 0) wmax[warp] = m;
+        __syncthreads();
+        float amax = wmax[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) amax = fmaxf(amax, wmax[i]);
+        g = amax > 0.0f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
+        if (threadIdx.x == 0) p.g[t] = g;
+    } else {
+        g = p.g[t];
+    }
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+        const int64_t r = warp + 8 * i;
+        if (r < p.rec_per_tensor * 8) encode_row_warp(p, t, r, v[i], g);
+    }
 }
 
 }  // namespace hsi

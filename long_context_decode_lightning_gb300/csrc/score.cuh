@@ -61,6 +61,11 @@ struct ScoreParams {
     int64_t ld;
     float* bmax;
     int64_t ldb;
+    // optional (single-query groups): 4096-bin histograms of the top 12 bits of
+    // the order keys of the scores and of the block maxima (the newest block
+    // counted as +inf), [B][4096], added to
+    uint32_t* key_hist;
+    uint32_t* bmax_hist;
     // pool gather
     const int32_t* block_ids;
     const int32_t* n_kept;
@@ -97,7 +102,11 @@ struct ScoreCfg {
     static constexpr int OFF_QSLOTS = STAGES * STAGE_BYTES;
     static constexpr int OFF_IDS = OFF_QSLOTS + 2 * QSLOT_BYTES;
     static constexpr int IDS_BYTES = GATHER ? IDS_AHEAD * UNIT_RECS * 4 : 0;
-    static constexpr int OFF_BARS = OFF_IDS + IDS_BYTES;
+    // histogram slots for the first HIST_SLOTS queries of the CTA's range
+    static constexpr int HIST_SLOTS = (!GATHER && NQ == 1) ? 2 : 0;
+    static constexpr int OFF_HIST = OFF_IDS + IDS_BYTES;
+    static constexpr int HIST_BYTES = HIST_SLOTS * 2 * 4096 * 4;
+    static constexpr int OFF_BARS = OFF_HIST + HIST_BYTES;
     // full, sfready, empty per stage; acc_full, acc_empty per accumulator set;
     // q_full, q_ready, q_empty per slot; ids_full, ids_free per id slot; drain
     static constexpr int NBARS = 3 * STAGES + 2 * NACC + 6 + (GATHER ? 2 * IDS_AHEAD : 0) + 1;
@@ -209,6 +218,20 @@ __device__ __forceinline__ bool wait_traced(uint64_t* bar, uint32_t parity, Scor
     return __all_sync(0xFFFFFFFFu, ok);
 }
 
+// Single-thread variant of wait_traced (no warp vote).
+__device__ __forceinline__ bool wait_one(uint64_t* bar, uint32_t parity, ScoreShared* sh, WaitTrace& tr, int slot) {
+#ifdef HSI_TRACE
+    const long long t0 = clock64();
+    const bool ok = wait_role(bar, parity, sh);
+    tr.add(slot, (unsigned long long)(clock64() - t0));
+    return ok;
+#else
+    (void)tr;
+    (void)slot;
+    return wait_role(bar, parity, sh);
+#endif
+}
+
 // Bounded wait that ignores the abort flag (teardown: drain what is in flight).
 __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
@@ -295,6 +318,10 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
     uint8_t* stages = smem + C::OFF_STAGES;
     uint8_t* qslots = smem + C::OFF_QSLOTS;
     int32_t* ids_ring = reinterpret_cast<int32_t*>(smem + C::OFF_IDS);
+    uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + C::OFF_HIST);  // [slot][key, bmax][4096]
+    const bool fuse_hist = C::HIST_SLOTS > 0 && (p.key_hist || p.bmax_hist);
+    if (fuse_hist)
+        for (int i = threadIdx.x; i < C::HIST_BYTES / 4; i += blockDim.x) hist_s[i] = 0u;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
     uint64_t* full = bars;
     uint64_t* sfready = full + STAGES;
@@ -486,22 +513,23 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
         }
     } else if (warp == C::MMA_WARP) {
         // ----------------------------------------------------------------- MMA
-        UnitIter<NQ, GATHER, UT> it;
-        it.init(p, sh);
-        int cur_g = -1, gc = -1;
-        constexpr uint32_t idesc = idesc_nvf4(128, C::N);
-        Ring st, ac;
-        for (long long u = 0; u < count; ++u) {
-            if (it.g != cur_g) {
-                if (cur_g >= 0 && lane == 0) tc_commit(&q_empty[gc & 1]);  // old slot free once its MMAs finish
-                cur_g = it.g;
-                ++gc;
-                if (!wait_traced(&q_ready[gc & 1], (gc >> 1) & 1, sh, tr, TR_MMA_QREADY)) break;
-            }
-            if (!wait_traced(&sfready[st.i], st.ph, sh, tr, TR_MMA_SFREADY)) break;
-            if (!wait_traced(&acc_empty[ac.i], ac.ph ^ 1u, sh, tr, TR_MMA_ACCEMPTY)) break;
-            HSI_TSTART(t_issue);
-            if (lane == 0) {
+        // one thread issues everything; the rest of the warp waits at the end
+        if (lane == 0) {
+            UnitIter<NQ, GATHER, UT> it;
+            it.init(p, sh);
+            int cur_g = -1, gc = -1;
+            constexpr uint32_t idesc = idesc_nvf4(128, C::N);
+            Ring st, ac;
+            for (long long u = 0; u < count; ++u) {
+                if (it.g != cur_g) {
+                    if (cur_g >= 0) tc_commit(&q_empty[gc & 1]);  // old slot free once its MMAs finish
+                    cur_g = it.g;
+                    ++gc;
+                    if (!wait_one(&q_ready[gc & 1], (gc >> 1) & 1, sh, tr, TR_MMA_QREADY)) break;
+                }
+                if (!wait_one(&sfready[st.i], st.ph, sh, tr, TR_MMA_SFREADY)) break;
+                if (!wait_one(&acc_empty[ac.i], ac.ph ^ 1u, sh, tr, TR_MMA_ACCEMPTY)) break;
+                HSI_TSTART(t_issue);
                 tc_fence_after();
                 const uint32_t a0 = smem_u32(stages + st.i * C::STAGE_BYTES);
                 const uint32_t b0 = smem_u32(qslots + (gc & 1) * C::QSLOT_BYTES);
@@ -518,15 +546,12 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                 }
                 // one commit: the epilogue that sees it also frees the stage
                 tc_commit(&acc_full[ac.i]);
+                HSI_TEND(t_issue, TR_MMA_ISSUE);
+                st.next(STAGES);
+                ac.next(C::NACC);
+                it.next(p);
             }
-            __syncwarp();
-            HSI_TEND(t_issue, TR_MMA_ISSUE);
-            st.next(STAGES);
-            ac.next(C::NACC);
-            it.next(p);
-        }
-        // drain: every MMA into TMEM done before the allocation is freed
-        if (lane == 0) {
+            // drain: every MMA into TMEM done before the allocation is freed
             tc_commit(drain);
             wait_drain(drain, 0);
         }
@@ -575,6 +600,13 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
         const int row = quarter * 32 + lane;  // key within a 128-key tile
         UnitIter<NQ, GATHER, UT> it;
         it.init(p, sh);
+        const int b_first = sh->g0 * NQ;
+        // histogram bins of query b: shared-memory slot, or global past the slots
+        auto hist_of = [&](int b, int which) -> uint32_t* {
+            const int slot = b - b_first;
+            if (slot >= 0 && slot < C::HIST_SLOTS) return hist_s + (slot * 2 + which) * 4096;
+            return (which == 0 ? p.key_hist : p.bmax_hist) + (int64_t)b * 4096;
+        };
         int cur_g = -1;
         float wq[NQ][32];
         int nv[NQ];
@@ -645,12 +677,21 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                     if (!GATHER) {
                         const bool vis = key < nv[qi];
                         if (vis) p.scores[(int64_t)b * p.ld + key] = sc;
+                        if (fuse_hist && p.key_hist && vis) atomicAdd(hist_of(b, 0) + (order_key(sc) >> 20), 1u);
                         if (p.bmax) {
                             float m = vis ? sc : __uint_as_float(0xFF800000u);
                             m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
                             m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
                             m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-                            if ((lane & 7) == 0 && vis) p.bmax[(int64_t)b * p.ldb + key / 8] = m;
+                            if ((lane & 7) == 0 && vis) {
+                                p.bmax[(int64_t)b * p.ldb + key / 8] = m;
+                                if (fuse_hist && p.bmax_hist) {
+                                    // the pool pins the newest block; -inf blocks are not eligible
+                                    const bool newest = key / 8 == (nv[qi] - 1) / 8;
+                                    const uint32_t bk = newest ? 0xFF800000u : order_key(m);
+                                    if (bk != 0x007FFFFFu) atomicAdd(hist_of(b, 1) + (bk >> 20), 1u);
+                                }
+                            }
                         }
                     } else if (pos[sub] >= 0) {
                         const float v = pos[sub] < nv[qi] ? sc : __uint_as_float(0xFF800000u);
@@ -683,6 +724,16 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
     __syncthreads();
     tc_fence_after();
     if (warp == C::MMA_WARP) tmem_dealloc(tmem, C::TMEM_COLS);
+    if (fuse_hist) {  // merge the shared-memory slots into the global histograms
+        const int b_first = sh->g0 * NQ;
+        for (int i = threadIdx.x; i < C::HIST_SLOTS * 2 * 4096; i += blockDim.x) {
+            const uint32_t v = hist_s[i];
+            const int slot = i / (2 * 4096), which = (i / 4096) & 1, bin = i & 4095;
+            const int b = b_first + slot;
+            uint32_t* g = which == 0 ? p.key_hist : p.bmax_hist;
+            if (v && g && b < p.B) atomicAdd(g + (int64_t)b * 4096 + bin, v);
+        }
+    }
 #ifdef HSI_TRACE
     if (threadIdx.x == 0 && blockIdx.x < 1024) g_hsi_marks[blockIdx.x][3] = globaltimer_ns();
 #endif

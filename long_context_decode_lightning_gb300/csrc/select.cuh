@@ -50,6 +50,7 @@ struct SelParams {
     uint32_t* cand_cnt;  // [B]
     uint32_t* cand_key;  // [B][cap]
     uint32_t* cand_idx;  // [B][cap]
+    uint32_t* thr;       // [B] bin (top 12 key bits) holding the k-th key
     int32_t cap;
     // top-k outputs
     const int32_t* block_ids;
@@ -84,6 +85,29 @@ __device__ __forceinline__ uint32_t sel_key(const SelParams& p, int b, int64_t i
 
 // ------------------------------------------------------------ scan passes --
 
+// Four consecutive items of a row starting at `base` (< hi): keys and eligibility.
+__device__ __forceinline__ void sel_key4(const SelParams& p, int b, const float* row, bool vec, int64_t base,
+                                         int64_t hi, int64_t n, uint32_t (&key)[4], bool (&ok)[4]) {
+    float v[4];
+    if (vec && base + 3 < hi) {
+        const float4 f = *reinterpret_cast<const float4*>(row + base);
+        v[0] = f.x, v[1] = f.y, v[2] = f.z, v[3] = f.w;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = base + i < hi ? row[base + i] : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t idx = base + i;
+        key[i] = order_key(v[i]);
+        ok[i] = idx < hi;
+        if (p.mode == SEL_POOL) {
+            if (idx == n - 1) key[i] = KEY_POS_INF;  // the block of the newest position
+            ok[i] = ok[i] && key[i] != KEY_NEG_INF;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(SCAN_THREADS) sel_hist_kernel(SelParams p) {
     __shared__ uint32_t sh[HIST_BINS];
     const int b = blockIdx.y;
@@ -93,10 +117,16 @@ __global__ void __launch_bounds__(SCAN_THREADS) sel_hist_kernel(SelParams p) {
     const int64_t hi = min(n, lo + SCAN_CHUNK);
     for (int i = threadIdx.x; i < HIST_BINS; i += SCAN_THREADS) sh[i] = 0;
     __syncthreads();
-    for (int64_t i = lo + threadIdx.x; i < hi; i += SCAN_THREADS) {
-        bool ok;
-        const uint32_t key = sel_key(p, b, i, n, ok);
-        if (ok) atomicAdd(&sh[key >> 20], 1u);
+    const float* row = p.src + (int64_t)b * p.ld;
+    const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
+    for (int64_t base0 = lo; base0 < hi; base0 += 4 * SCAN_THREADS) {  // uniform trip count per warp
+        const int64_t base = base0 + 4 * threadIdx.x;
+        uint32_t key[4];
+        bool ok[4];
+        sel_key4(p, b, row, vec, base, hi, n, key, ok);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (ok[i]) atomicAdd(&sh[key[i] >> 20], 1u);
     }
     __syncthreads();
     uint32_t* gh = p.hist + (int64_t)b * HIST_BINS;
@@ -144,36 +174,54 @@ __device__ uint32_t threshold_bin(const uint32_t* gh, int k, uint32_t* scratch /
     return scratch[SCAN_THREADS];
 }
 
-__global__ void __launch_bounds__(SCAN_THREADS) sel_collect_kernel(SelParams p) {
+// One CTA per query: the threshold bin from the merged histogram.
+__global__ void __launch_bounds__(SCAN_THREADS) sel_thresh_kernel(SelParams p) {
     __shared__ uint32_t scratch[SCAN_THREADS + 1];
+    const int b = blockIdx.x;
+    const uint32_t thr = threshold_bin(p.hist + (int64_t)b * HIST_BINS, p.k, scratch);
+    if (threadIdx.x == 0) p.thr[b] = thr;
+}
+
+__global__ void __launch_bounds__(SCAN_THREADS) sel_collect_kernel(SelParams p) {
     const int b = blockIdx.y;
     const int64_t n = sel_items(p, b);
     const int64_t lo = (int64_t)blockIdx.x * SCAN_CHUNK;
     if (lo >= n) return;
     const int64_t hi = min(n, lo + SCAN_CHUNK);
-    const uint32_t thr = threshold_bin(p.hist + (int64_t)b * HIST_BINS, p.k, scratch);
+    const uint32_t thr = p.thr[b];
     const int lane = threadIdx.x & 31;
     uint32_t* cnt = p.cand_cnt + b;
     uint32_t* ck = p.cand_key + (int64_t)b * p.cap;
     uint32_t* ci = p.cand_idx + (int64_t)b * p.cap;
-    for (int64_t base = lo; base < hi; base += SCAN_THREADS) {
-        const int64_t i = base + threadIdx.x;
-        bool ok = false;
-        uint32_t key = 0;
-        if (i < hi) key = sel_key(p, b, i, n, ok);
-        const bool take = ok && (key >> 20) >= thr;
-        const uint32_t m = __ballot_sync(0xFFFFFFFFu, take);
-        if (m) {
-            uint32_t pos0 = 0;
-            if (lane == 0) pos0 = atomicAdd(cnt, (uint32_t)__popc(m));
-            pos0 = __shfl_sync(0xFFFFFFFFu, pos0, 0);
-            if (take) {
-                const uint32_t pos = pos0 + __popc(m & ((1u << lane) - 1u));
-                if (pos < (uint32_t)p.cap) {
-                    ck[pos] = key;
-                    ci[pos] = (uint32_t)i;
+    const float* row = p.src + (int64_t)b * p.ld;
+    const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
+    // 4 items per thread per round; at most one global reservation per warp per round
+    for (int64_t base0 = lo; base0 < hi; base0 += 4 * SCAN_THREADS) {
+        const int64_t base = base0 + 4 * threadIdx.x;
+        uint32_t key[4];
+        bool ok[4];
+        sel_key4(p, b, row, vec, base, hi, n, key, ok);
+        uint32_t m[4], tot = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ok[i] = ok[i] && (key[i] >> 20) >= thr;
+            m[i] = __ballot_sync(0xFFFFFFFFu, ok[i]);
+            tot += __popc(m[i]);
+        }
+        if (tot == 0) continue;
+        uint32_t pos = 0;
+        if (lane == 0) pos = atomicAdd(cnt, tot);
+        pos = __shfl_sync(0xFFFFFFFFu, pos, 0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (ok[i]) {
+                const uint32_t at = pos + __popc(m[i] & ((1u << lane) - 1u));
+                if (at < (uint32_t)p.cap) {
+                    ck[at] = key[i];
+                    ci[at] = (uint32_t)(base + i);
                 }
             }
+            pos += __popc(m[i]);
         }
     }
 }
@@ -191,6 +239,16 @@ struct SelSmem {
 
 // Sources of items for the block select.
 struct SmemSrc {  // keys and indices in shared memory
+    const uint32_t* keys;
+    const uint32_t* ids;
+    int64_t n;
+    __device__ uint32_t key(int64_t j, bool& ok) const {
+        ok = true;
+        return keys[j];
+    }
+    __device__ uint32_t idx(int64_t j) const { return ids[j]; }
+};
+struct GlobalSrc {  // survivor keys and indices in global memory
     const uint32_t* keys;
     const uint32_t* ids;
     int64_t n;
@@ -219,18 +277,18 @@ __device__ uint32_t radix_pass(const Src& src, SelSmem& s, int sel, uint32_t T, 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     for (int i = tid; i < SEL_WARPS * 256; i += SEL_THREADS) (&s.whist[0][0])[i] = 0;
     __syncthreads();
-    for (int64_t j = tid; j < src.n; j += SEL_THREADS) {
-        bool ok;
-        const uint32_t key = src.key(j, ok);
-        if (!ok) continue;
-        uint32_t v;
-        if (sel == 0) {
-            v = key;
-        } else {
-            if (key != T) continue;
-            v = ~src.idx(j);
+    for (int64_t j0 = 0; j0 < src.n; j0 += SEL_THREADS) {  // uniform trip count per warp
+        const int64_t j = j0 + tid;
+        uint32_t bin = 0xFFFFFFFFu;
+        if (j < src.n) {
+            bool ok;
+            const uint32_t key = src.key(j, ok);
+            if (ok && (sel == 0 || key == T)) {
+                const uint32_t v = sel == 0 ? key : ~src.idx(j);
+                if ((v & mask) == prefix) bin = (v >> shift) & 255u;
+            }
         }
-        if ((v & mask) == prefix) atomicAdd(&s.whist[warp][(v >> shift) & 255u], 1u);
+        if (bin != 0xFFFFFFFFu) atomicAdd(&s.whist[warp][bin], 1u);
     }
     __syncthreads();
     if (tid < 256) {
@@ -308,34 +366,32 @@ __device__ void sort_desc(SelSmem& s, int count) {
     }
 }
 
-// Select the k best eligible items of src into s.win as (key << 32 | ~idx)
-// (top-k) or (~idx) (pool: ascending ids after the descending sort), sorted.
-// Returns the number selected, min(k, eligible).
+// After the first radix pass (digit d0 of the top 8 key bits, `above` items
+// above it): the remaining passes, the tie split at the k-th key and the
+// gather of the winners into s.win as (key << 32 | ~idx) (top-k) or (~idx)
+// (pool: ascending ids after the descending sort), sorted. Items of src whose
+// top byte is below d0 may be absent.
 template <class Src>
-__device__ int block_select(const Src& src, SelSmem& s, int k, bool ids_only) {
-    uint32_t above, at, total;
-    uint32_t prefix = 0, mask = 0, need = (uint32_t)k;
-    // pass 0 also counts the eligible items
-    uint32_t d = radix_pass(src, s, 0, 0, 0, 0, 24, need, &above, &at, &total);
-    const bool take_all = total <= (uint32_t)k;
+__device__ int select_finish(const Src& src, SelSmem& s, int k, bool ids_only, bool take_all, uint32_t d0,
+                             uint32_t above0) {
+    uint32_t above, at = 0, total;
     uint32_t T = 0, T2 = 0;
     bool tie_split = false;
     if (!take_all) {
-        need -= above;
-        prefix = d << 24;
-        mask = 0xFF000000u;
+        uint32_t need = (uint32_t)k - above0;
+        uint32_t prefix = d0 << 24, mask = 0xFF000000u;
         for (int shift = 16; shift >= 0; shift -= 8) {
-            d = radix_pass(src, s, 0, 0, prefix, mask, shift, need, &above, &at, &total);
+            const uint32_t d = radix_pass(src, s, 0, 0, prefix, mask, shift, need, &above, &at, &total);
             need -= above;
             prefix |= d << shift;
             mask |= 0xFFu << shift;
         }
-        T = prefix;           // the k-th largest key
+        T = prefix;             // the k-th largest key
         tie_split = at > need;  // more items equal T than places left
         if (tie_split) {
             uint32_t p2 = 0, m2 = 0, need2 = need;
             for (int shift = 24; shift >= 0; shift -= 8) {
-                d = radix_pass(src, s, 1, T, p2, m2, shift, need2, &above, &at, &total);
+                const uint32_t d = radix_pass(src, s, 1, T, p2, m2, shift, need2, &above, &at, &total);
                 need2 -= above;
                 p2 |= d << shift;
                 m2 |= 0xFFu << shift;
@@ -370,6 +426,60 @@ __device__ int block_select(const Src& src, SelSmem& s, int k, bool ids_only) {
     return count;
 }
 
+// The k best eligible items of src (see select_finish). After the first
+// radix pass the items that can still win (top byte >= the threshold digit)
+// are packed into s.keys / s.idx when they fit, so the later passes run over
+// those only. IN_SMEM: src itself lives in s.keys / s.idx (then it always
+// fits; the items go through registers so none is overwritten before it is
+// read).
+template <bool IN_SMEM, class Src>
+__device__ int block_select(const Src& src, SelSmem& s, int k, bool ids_only) {
+    uint32_t above, at, total;
+    const uint32_t d0 = radix_pass(src, s, 0, 0, 0, 0, 24, (uint32_t)k, &above, &at, &total);
+    const bool take_all = total <= (uint32_t)k;
+    if (take_all) return select_finish(src, s, k, ids_only, true, d0, above);
+    if (threadIdx.x == 0) s.bcast[6] = 0;
+    if (IN_SMEM) {
+        constexpr int PER = SEL_CAP / SEL_THREADS;
+        uint32_t kk[PER], ii[PER];
+        bool keep[PER];
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int64_t j = threadIdx.x + (int64_t)i * SEL_THREADS;
+            keep[i] = false;
+            if (j < src.n) {
+                bool ok;
+                kk[i] = src.key(j, ok);
+                ii[i] = src.idx(j);
+                keep[i] = ok && (kk[i] >> 24) >= d0;
+            }
+        }
+        __syncthreads();  // every item is in registers before any is overwritten
+#pragma unroll
+        for (int i = 0; i < PER; ++i)
+            if (keep[i]) {
+                const uint32_t pos = atomicAdd(&s.bcast[6], 1u);
+                s.keys[pos] = kk[i];
+                s.idx[pos] = ii[i];
+            }
+    } else {
+        if (above + at > (uint32_t)SEL_CAP) return select_finish(src, s, k, ids_only, false, d0, above);
+        __syncthreads();
+        for (int64_t j = threadIdx.x; j < src.n; j += SEL_THREADS) {
+            bool ok;
+            const uint32_t key = src.key(j, ok);
+            if (ok && (key >> 24) >= d0) {
+                const uint32_t pos = atomicAdd(&s.bcast[6], 1u);
+                s.keys[pos] = key;
+                s.idx[pos] = src.idx(j);
+            }
+        }
+    }
+    __syncthreads();
+    SmemSrc packed{s.keys, s.idx, (int64_t)s.bcast[6]};
+    return select_finish(packed, s, k, ids_only, false, d0, above);
+}
+
 __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SelSmem& s = *reinterpret_cast<SelSmem*>(smem_raw);
@@ -395,22 +505,25 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) 
         src.keys = s.keys;
         src.ids = s.idx;
         src.n = n;
-        count = block_select(src, s, p.k, ids_only);
+        count = block_select<true>(src, s, p.k, ids_only);
     } else {
         const uint32_t c = p.cand_cnt[b];
-        if (c <= (uint32_t)p.cap && c <= (uint32_t)SEL_CAP) {
-            const uint32_t* ck = p.cand_key + (int64_t)b * p.cap;
-            const uint32_t* ci = p.cand_idx + (int64_t)b * p.cap;
+        const uint32_t* ck = p.cand_key + (int64_t)b * p.cap;
+        const uint32_t* ci = p.cand_idx + (int64_t)b * p.cap;
+        if (c <= (uint32_t)SEL_CAP) {  // the survivors fit: select in shared memory
             for (uint32_t j = threadIdx.x; j < c; j += SEL_THREADS) {
                 s.keys[j] = ck[j];
                 s.idx[j] = ci[j];
             }
             __syncthreads();
             SmemSrc src{s.keys, s.idx, (int64_t)c};
-            count = block_select(src, s, p.k, ids_only);
-        } else {
+            count = block_select<true>(src, s, p.k, ids_only);
+        } else if (c <= (uint32_t)p.cap) {  // all survivors kept: select over them in L2
+            GlobalSrc src{ck, ci, (int64_t)c};
+            count = block_select<false>(src, s, p.k, ids_only);
+        } else {  // survivors overflowed (heavy ties): select over the whole row
             RowSrc src{&p, b, n};
-            count = block_select(src, s, p.k, ids_only);
+            count = block_select<false>(src, s, p.k, ids_only);
         }
     }
     if (p.mode == SEL_TOPK) {

@@ -139,11 +139,13 @@ def test_topk_bit_exact(n, k):
 
 
 def test_topk_ragged_rows_and_all_equal():
-    n = [1, 20000, 40000, 3]
+    # all-equal rows exercise every survivor path: shared memory, survivors in
+    # L2 (40000 > 16384), survivor overflow with a re-read of the row (100000)
+    n = [1, 20000, 40000, 3, 100000]
     ld = max(n)
-    sc = np.full((4, ld), 2.5, dtype=np.float32)
+    sc = np.full((len(n), ld), 2.5, dtype=np.float32)
     gi, _ = _gpu_topk(sc, n, 512)
-    for b in range(4):
+    for b in range(len(n)):
         ri, _ = oracle.topk(sc[b], n[b], 512)
         assert np.array_equal(gi[b], ri)
 
@@ -264,3 +266,65 @@ def test_end_to_end_topk_sets_match_except_near_ties():
     diff = set(gidx[0].tolist()) ^ set(oidx.tolist())
     for p in diff:
         assert abs(so[p] - kth) <= 2 * tol[p], p
+
+
+# ------------------------------------------------------- composite layers --
+
+@pytest.mark.parametrize("lengths", [[3, 20000, 200003], [16384, 131073]])
+def test_full_and_reindex_layer_match_separate_calls(lengths):
+    """hsi_full_layer (histograms fused into the scoring kernel) and
+    hsi_reindex_layer give exactly what the separate calls give."""
+    wl = inputs.workload(1)
+    B, maxv = len(lengths), max(lengths)
+    caches = Caches(wl, 0, range(B), lengths)
+    q_rec, g_q, w = gpu_queries(wl, 0, range(B))
+    nv, off = i32(lengths), i64(caches.rec_off)
+    s_sep = torch.empty(B, maxv, device=DEV)
+    bm = torch.empty(B, hsi.n_records(maxv), device=DEV)
+    hsi.score_full(q_rec, g_q, w, caches.k_rec, caches.g, off, nv, B, maxv, s_sep, block_max=bm)
+    i_sep = torch.empty(B, 512, dtype=torch.int32, device=DEV)
+    v_sep = torch.empty(B, 512, device=DEV)
+    hsi.topk(s_sep, nv, B, maxv, 512, i_sep, v_sep)
+    ids_sep = torch.empty(B, 2048, dtype=torch.int32, device=DEV)
+    nk_sep, np_sep = torch.empty(B, dtype=torch.int32, device=DEV), torch.empty(B, dtype=torch.int32, device=DEV)
+    bits_sep = torch.zeros(B, (maxv + 31) // 32, dtype=torch.int32, device=DEV)
+    hsi.candidate_pool(nv, B, maxv, ids_sep, nk_sep, np_sep, scores=s_sep, pool_bits=bits_sep)
+
+    s_f = torch.empty(B, maxv, device=DEV)
+    i_f = torch.empty(B, 512, dtype=torch.int32, device=DEV)
+    v_f = torch.empty(B, 512, device=DEV)
+    ids_f = torch.empty(B, 2048, dtype=torch.int32, device=DEV)
+    nk_f, np_f = torch.empty(B, dtype=torch.int32, device=DEV), torch.empty(B, dtype=torch.int32, device=DEV)
+    bits_f = torch.zeros(B, (maxv + 31) // 32, dtype=torch.int32, device=DEV)
+    hsi.full_layer(q_rec, g_q, w, caches.k_rec, caches.g, off, nv, B, maxv, s_f, 512, i_f, v_f, block_ids=ids_f,
+                   n_kept=nk_f, n_pool=np_f, pool_bits=bits_f)
+    assert hsi.device_error() == 0
+    for b, n in enumerate(lengths):
+        assert torch.equal(s_f[b, :n], s_sep[b, :n])
+    assert torch.equal(i_f, i_sep) and torch.equal(v_f, v_sep)
+    assert torch.equal(nk_f, nk_sep) and torch.equal(np_f, np_sep)
+    for b in range(B):
+        k = int(nk_sep[b])
+        assert torch.equal(ids_f[b, :k], ids_sep[b, :k])
+        words = (lengths[b] + 31) // 32
+        assert torch.equal(bits_f[b, :words], bits_sep[b, :words])
+    # oracle on the GPU scores: the fused path is still the exact selection
+    sg = s_f.cpu().numpy()
+    for b, n in enumerate(lengths):
+        ri, _ = oracle.topk(sg[b], n, 512)
+        assert np.array_equal(i_f.cpu().numpy()[b], ri)
+        oi, onk, onp, _ = oracle.pool(sg[b], n)
+        assert int(nk_f[b]) == onk and np.array_equal(ids_f.cpu().numpy()[b][:onk], oi[:onk])
+
+    q1, g1, w1 = gpu_queries(wl, 1, range(B))
+    ps_sep = torch.empty(B, 2048 * 8, device=DEV)
+    hsi.score_pool(q1, g1, w1, caches.k_rec, caches.g, off, nv, ids_f, nk_f, 2048, B, ps_sep)
+    ri_sep = torch.empty(B, 512, dtype=torch.int32, device=DEV)
+    rv_sep = torch.empty(B, 512, device=DEV)
+    hsi.topk(ps_sep, np_f, B, 2048 * 8, 512, ri_sep, rv_sep, block_ids=ids_f)
+    ps_r = torch.empty(B, 2048 * 8, device=DEV)
+    ri_r = torch.empty(B, 512, dtype=torch.int32, device=DEV)
+    rv_r = torch.empty(B, 512, device=DEV)
+    hsi.reindex_layer(q1, g1, w1, caches.k_rec, caches.g, off, nv, ids_f, nk_f, np_f, B, ps_r, 512, ri_r, rv_r)
+    assert hsi.device_error() == 0
+    assert torch.equal(ri_r, ri_sep) and torch.equal(rv_r, rv_sep)
