@@ -47,7 +47,8 @@ typedef enum {
     HSI_ERR_CUDA = -3,           /* a CUDA runtime call failed (launch, attribute, sync) */
     HSI_ERR_DEVICE_TIMEOUT = -4, /* a kernel's bounded wait ran out (reported by hsi_device_error) */
     HSI_ERR_WORKSPACE = -5,      /* ws is NULL, too small or not 256-byte aligned */
-    HSI_ERR_DEVICE_ARG = -6      /* a kernel found a bad device-side argument (reported by hsi_device_error) */
+    HSI_ERR_DEVICE_ARG = -6,     /* a kernel found a bad device-side argument (reported by hsi_device_error) */
+    HSI_ERR_TOO_LARGE = -7       /* more than the fixed scratch of hsi_topk_noalloc holds */
 } hsi_status;
 
 #define HSI_HEADS 32      /* indexer heads H */
@@ -158,6 +159,31 @@ hsi_status hsi_score_full(const uint8_t* q_rec, const float* g_q, const float* w
 hsi_status hsi_topk(const float* scores, int64_t ld, const int32_t* n_valid, int32_t B, int64_t max_valid,
                     int32_t k, const int32_t* block_ids, int64_t ld_blocks, int32_t block_size,
                     int32_t* out_idx, float* out_val, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * hsi_topk without a workspace: for callers that cannot allocate device
+ * memory and have none to lend -- code running inside a host framework that
+ * owns every byte of device memory through its own pool, or a latency-critical
+ * loop where cudaMalloc's implicit device synchronisation is not acceptable.
+ * The pages have no counterpart; this is a convenience of the library.
+ *
+ * Results are exactly those of hsi_topk with the same arguments. Instead of
+ * `ws`, the long-row passes (rows longer than 16384 items) use one fixed 8 MiB
+ * array compiled into the library, which every GPU that loads the library
+ * keeps until the process exits. That bounds the request: with
+ * max_valid > 16384, B may be at most 56 (HSI_ERR_TOO_LARGE beyond that);
+ * shorter rows use no scratch and have no limit on B.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - Every call on a device shares the array and clears what must start at
+ *    zero itself; calls whose work overlaps on the GPU (other streams, other
+ *    host threads) race on the array and must be ordered by the caller.
+ *  - No call allocates or frees memory.
+ */
+hsi_status hsi_topk_noalloc(const float* scores, int64_t ld, const int32_t* n_valid, int32_t B, int64_t max_valid,
+                            int32_t k, const int32_t* block_ids, int64_t ld_blocks, int32_t block_size,
+                            int32_t* out_idx, float* out_val, cudaStream_t stream);
 
 /*
  * The candidate pool of each query.

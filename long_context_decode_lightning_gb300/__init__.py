@@ -23,12 +23,13 @@ _lib = None
 HEADS, DIM, REC_ROWS, REC_BYTES = 32, 128, 8, 576
 
 STATUS = {0: "HSI_OK", -1: "HSI_ERR_INVALID_ARG", -2: "HSI_ERR_UNSUPPORTED", -3: "HSI_ERR_CUDA",
-          -4: "HSI_ERR_DEVICE_TIMEOUT", -5: "HSI_ERR_WORKSPACE", -6: "HSI_ERR_DEVICE_ARG"}
+          -4: "HSI_ERR_DEVICE_TIMEOUT", -5: "HSI_ERR_WORKSPACE", -6: "HSI_ERR_DEVICE_ARG", -7: "HSI_ERR_TOO_LARGE"}
 WS_QUANTIZE, WS_SCORE, WS_TOPK, WS_POOL, WS_FULL_LAYER, WS_REINDEX_LAYER = 0, 1, 2, 3, 4, 5
 
 EXPORTS = ["hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
            "hsi_workspace_size", "hsi_device_error", "hsi_device_check", "hsi_status_string",
-           "hsi_kernel_launches", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer", "hsi_reindex_layer"]
+           "hsi_kernel_launches", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer", "hsi_reindex_layer",
+           "hsi_topk_noalloc"]
 
 
 class HsiError(RuntimeError):
@@ -70,6 +71,7 @@ def lib() -> ctypes.CDLL:
                                      vp, i64, i32, vp, sz, vp]
         L.hsi_reindex_layer.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i64, i32, vp, vp, vp,
                                         sz, vp]
+        L.hsi_topk_noalloc.argtypes = [vp, i64, vp, i32, i64, i32, vp, i64, i32, vp, vp, vp]
         L.hsi_workspace_size.argtypes = [ctypes.c_int, i32, i64, i32]
         L.hsi_workspace_size.restype = sz
         L.hsi_device_error.argtypes = [vp]
@@ -82,7 +84,7 @@ def lib() -> ctypes.CDLL:
         L.hsi_kernel_launches.restype = ctypes.c_uint64
         for name in ("hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
                      "hsi_device_error", "hsi_device_check", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer",
-                     "hsi_reindex_layer"):
+                     "hsi_reindex_layer", "hsi_topk_noalloc"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -176,6 +178,18 @@ def topk(scores, n_valid, B, max_valid, k, out_idx, out_val, ld=None, block_ids=
     _check("hsi_topk", lib().hsi_topk(
         _ptr(scores), ld, _ptr(n_valid), B, max_valid, k, _ptr(block_ids), ld_blocks, block_size,
         _ptr(out_idx), _ptr(out_val), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def topk_noalloc(scores, n_valid, B, max_valid, k, out_idx, out_val, ld=None, block_ids=None, ld_blocks=0,
+                 block_size=8, stream=None):
+    """hsi_topk for callers that cannot allocate: no workspace argument; the
+    long-row passes use the library's fixed 8 MiB device scratch instead."""
+    ld = scores.shape[-1] if ld is None else ld
+    if block_ids is not None and not ld_blocks:
+        ld_blocks = block_ids.shape[-1]
+    _check("hsi_topk_noalloc", lib().hsi_topk_noalloc(
+        _ptr(scores), ld, _ptr(n_valid), B, max_valid, k, _ptr(block_ids), ld_blocks, block_size,
+        _ptr(out_idx), _ptr(out_val), _stream(stream)))
 
 
 def candidate_pool(n_visible, B, max_visible, block_ids, n_kept, n_pool, scores=None, ld=0, block_max=None,

@@ -5,6 +5,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/hsi.h"
 #include "calib.cuh"
@@ -53,18 +54,18 @@ struct SelWs {
     float* bmax;
 };
 
-size_t sel_ws_bytes(int32_t B, int64_t max_items, bool need_bmax, int64_t max_blocks) {
+size_t sel_ws_bytes(int32_t B, int64_t max_items, bool need_bmax, int64_t max_blocks, int cap = kCandCap) {
     size_t s = 0;
     if (max_items > SEL_CAP) {
         s += align_up((size_t)B * HIST_BINS * 4, 256);
         s += align_up((size_t)B * 8, 256);
-        s += 2 * align_up((size_t)B * kCandCap * 4, 256);
+        s += 2 * align_up((size_t)B * cap * 4, 256);
     }
     if (need_bmax) s += align_up((size_t)B * (size_t)max_blocks * 4, 256);
     return s;
 }
 
-SelWs carve_sel(void* ws, int32_t B, int64_t max_items, bool need_bmax, int64_t max_blocks) {
+SelWs carve_sel(void* ws, int32_t B, int64_t max_items, bool need_bmax, int64_t max_blocks, int cap = kCandCap) {
     SelWs w{};
     uint8_t* p = static_cast<uint8_t*>(ws);
     if (max_items > SEL_CAP) {
@@ -73,9 +74,9 @@ SelWs carve_sel(void* ws, int32_t B, int64_t max_items, bool need_bmax, int64_t 
         w.cnt = reinterpret_cast<uint32_t*>(p);
         p += align_up((size_t)B * 8, 256);
         w.ckey = reinterpret_cast<uint32_t*>(p);
-        p += align_up((size_t)B * kCandCap * 4, 256);
+        p += align_up((size_t)B * cap * 4, 256);
         w.cidx = reinterpret_cast<uint32_t*>(p);
-        p += align_up((size_t)B * kCandCap * 4, 256);
+        p += align_up((size_t)B * cap * 4, 256);
     }
     if (need_bmax) w.bmax = reinterpret_cast<float*>(p);
     return w;
@@ -124,6 +125,38 @@ hsi_status launch_score(const ScoreParams& p, cudaStream_t s) {
     return launch_ok();
 }
 
+// ---- fixed scratch of hsi_topk_noalloc ----------------------------------------
+// A caller that cannot allocate device memory still needs somewhere for the
+// long-row selection passes to keep their histogram and survivors. This array
+// is that place: it lives in the library image, so every GPU that loads the
+// library holds it (8 MiB) until the process exits, and every call of
+// hsi_topk_noalloc on a device shares it.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+constexpr int kNoAllocCandCap = 16384;  // survivors kept per query (more: the row is re-read)
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+void* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// The device address of the scratch on the current device. Host code may not
+// pass g_noalloc_scratch itself to a kernel (on the host that name is only a
+// stand-in for the symbol); the address is looked up once per device, with the
+// device current, and cached.
+hsi_status noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return HSI_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return HSI_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return HSI_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return HSI_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -137,6 +170,7 @@ const char* hsi_status_string(hsi_status st) {
         case HSI_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait ran out";
         case HSI_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
         case HSI_ERR_DEVICE_ARG: return "a kernel found a malformed device-side argument";
+        case HSI_ERR_TOO_LARGE: return "request needs more than the fixed scratch of hsi_topk_noalloc";
     }
     return "unknown status";
 }
@@ -338,6 +372,45 @@ hsi_status hsi_topk(const float* scores, int64_t ld, const int32_t* n_valid, int
     sp.out_idx = out_idx;
     sp.out_val = out_val;
     return run_select(sp, max_valid, stream);
+}
+
+hsi_status hsi_topk_noalloc(const float* scores, int64_t ld, const int32_t* n_valid, int32_t B, int64_t max_valid,
+                            int32_t k, const int32_t* block_ids, int64_t ld_blocks, int32_t block_size,
+                            int32_t* out_idx, float* out_val, cudaStream_t stream) {
+    if (!scores || !n_valid || !out_idx || !out_val || B <= 0 || max_valid < 0 || ld < max_valid)
+        return HSI_ERR_INVALID_ARG;
+    if (max_valid > (int64_t)INT32_MAX) return HSI_ERR_INVALID_ARG;
+    if (k < 1 || k > 2048) return HSI_ERR_INVALID_ARG;
+    if (block_ids && (block_size < 1 || ld_blocks < (max_valid + block_size - 1) / block_size))
+        return HSI_ERR_INVALID_ARG;
+    const size_t need = sel_ws_bytes(B, max_valid, false, 0, kNoAllocCandCap);
+    if (need > kNoAllocScratchBytes) return HSI_ERR_TOO_LARGE;
+    void* ws = nullptr;
+    if (need) {
+        const hsi_status st = noalloc_scratch(&ws);
+        if (st != HSI_OK) return st;
+    }
+    SelWs wsp = carve_sel(ws, B, max_valid, false, 0, kNoAllocCandCap);
+    SelParams sp{};
+    sp.src = scores;
+    sp.ld = ld;
+    sp.n_src = n_valid;
+    sp.div = 1;
+    sp.B = B;
+    sp.k = k;
+    sp.mode = SEL_TOPK;
+    sp.hist = wsp.hist;
+    sp.cand_cnt = wsp.cnt;
+    sp.cand_key = wsp.ckey;
+    sp.cand_idx = wsp.cidx;
+    sp.thr = wsp.cnt ? wsp.cnt + B : nullptr;
+    sp.cap = kNoAllocCandCap;
+    sp.block_ids = block_ids;
+    sp.ld_blocks = ld_blocks;
+    sp.block_size = block_size;
+    sp.out_idx = out_idx;
+    sp.out_val = out_val;
+    return run_select(sp, max_valid, stream);  // clears the histogram and counters first
 }
 
 hsi_status hsi_candidate_pool(const float* scores, int64_t ld, const float* block_max, int64_t ldb,

@@ -1,0 +1,68 @@
+"""hsi_topk_noalloc: the top-k entry point for callers that cannot allocate
+device memory (a host framework owns all of it through its own pool, or the
+caller cannot afford cudaMalloc's device synchronisation) and so cannot hand
+the library a workspace. It must give exactly what hsi_topk gives, call after
+call, with its fixed scratch reused in between.
+
+This file is named to be collected last, so that a run stopping at the first
+failure has run every other test before it."""
+import numpy as np
+import pytest
+import torch
+
+import long_context_decode_lightning_gb300 as hsi
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    hsi.build()
+    hsi.device_check()
+
+
+def _rows(seed, B, n):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    s = torch.randn(B, n, generator=g) * 4
+    s[1 % B, ::5] = s[1 % B, 7]  # ties
+    return s.cuda()
+
+
+def _both(scores, n_valid, k):
+    B, ld = scores.shape
+    nv = torch.tensor(n_valid, dtype=torch.int32, device="cuda")
+    ref_i = torch.empty(B, k, dtype=torch.int32, device="cuda")
+    ref_v = torch.empty(B, k, device="cuda")
+    hsi.topk(scores, nv, B, max(n_valid), k, ref_i, ref_v)
+    got_i = torch.full((B, k), 7, dtype=torch.int32, device="cuda")
+    got_v = torch.full((B, k), 7.0, device="cuda")
+    hsi.topk_noalloc(scores, nv, B, max(n_valid), k, got_i, got_v)
+    assert hsi.device_error() == 0
+    return ref_i, ref_v, got_i, got_v
+
+
+def test_noalloc_matches_topk_on_two_calls_in_a_row():
+    # first call: long rows, so the fixed scratch holds histogram and survivors
+    s1 = _rows(1, 8, 100000)
+    r_i, r_v, g_i, g_v = _both(s1, [100000, 99999, 60000, 16385, 100000, 1, 512, 70000], 512)
+    assert torch.equal(g_i, r_i) and torch.equal(g_v, r_v)
+    # second call: different rows and k; whatever the first call left behind
+    # in the scratch must not leak into this result
+    s2 = _rows(2, 5, 50000)
+    r_i, r_v, g_i, g_v = _both(s2, [50000, 40000, 30000, 20000, 17000], 2048)
+    assert torch.equal(g_i, r_i) and torch.equal(g_v, r_v)
+
+
+def test_noalloc_short_rows_need_no_scratch_and_oversize_is_refused():
+    s = _rows(3, 200, 4000)  # rows of at most 16384 items: any number of queries
+    r_i, r_v, g_i, g_v = _both(s, [4000] * 200, 512)
+    assert torch.equal(g_i, r_i) and torch.equal(g_v, r_v)
+    big = _rows(4, 57, 20000)  # 57 long rows do not fit the fixed scratch
+    nv = torch.full((57,), 20000, dtype=torch.int32, device="cuda")
+    i = torch.empty(57, 512, dtype=torch.int32, device="cuda")
+    v = torch.empty(57, 512, device="cuda")
+    with pytest.raises(hsi.HsiError) as e:
+        hsi.topk_noalloc(big, nv, 57, 20000, 512, i, v)
+    assert e.value.status == -7
