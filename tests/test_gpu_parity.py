@@ -328,3 +328,28 @@ def test_full_and_reindex_layer_match_separate_calls(lengths):
     hsi.reindex_layer(q1, g1, w1, caches.k_rec, caches.g, off, nv, ids_f, nk_f, np_f, B, ps_r, 512, ri_r, rv_r)
     assert hsi.device_error() == 0
     assert torch.equal(ri_r, ri_sep) and torch.equal(rv_r, rv_sep)
+
+
+# ------------------------------------------------------- grouped (prefill) --
+
+@pytest.mark.parametrize("n_cache,n_vis", [(3000, [2990, 2991, 2992, 3000, 5, 6, 7, 8]),
+                                           (20000, [19000 + 37 * i for i in range(12)])])
+def test_score_full_group4_shared_cache(n_cache, n_vis):
+    """Chunked prefill: groups of 4 consecutive queries share one cache and are
+    scored in one N = 128 tensor-core tile; each query keeps its own causal limit."""
+    wl = inputs.workload(4)
+    B = len(n_vis)
+    caches = Caches(wl, 0, [0], [n_cache])
+    q_rec, g_q, w = gpu_queries(wl, 0, range(B))
+    gk = caches.g.repeat(B)
+    off = i64([0] * B)
+    scores = torch.full((B, n_cache), float("nan"), device=DEV)
+    hsi.score_full(q_rec, g_q, w, caches.k_rec, gk, off, i32(n_vis), B, n_cache, scores, group=4)
+    assert hsi.device_error() == 0
+    sg = scores.cpu().numpy()
+    krec, gko = caches.oracle_rec(0)
+    for b, n in enumerate(n_vis):
+        qrec, gq, wo = oracle_query(wl, 0, b)
+        ref, tol = oracle.score_rows(qrec, gq, wo, krec, gko, np.arange(n))
+        assert np.all(np.abs(sg[b, :n] - ref) <= tol), b
+        assert np.isnan(sg[b, n:]).all()
