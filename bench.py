@@ -373,6 +373,23 @@ def cpu_sample_size(wl: inputs.Workload):
     return max(1, min(16, os.cpu_count() or 1, wl.B))
 
 
+# ----------------------------------------------------------- multi-rank --
+
+def max_over_ranks(ms: float, device) -> float:
+    """The slowest rank's time: every rank of the job processed its own units,
+    so the job's throughput is all units over this time."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank: float, world: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: the units of all ranks over the slowest rank's time."""
+    return units_per_rank * world * steps / (ms / 1e3)
+
+
 # ------------------------------------------------------------------- main --
 
 def main():
@@ -451,11 +468,7 @@ def main():
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(ms, dev) if world > 1 else ms
 
     with ClockSampler(local) as clk:
         if args.profile:
@@ -472,9 +485,9 @@ def main():
     ms_e2e = timed(W.step_e2e, args.steps, sync_each=True)
     assert hsi.device_error() == 0, "device error during the end-to-end steps"
 
-    value = pairs * world * args.steps / (ms / 1e3)
-    value_e2e = pairs * world * args.steps / (ms_e2e / 1e3)
-    sel = W.B * W.layers * world * args.steps / (ms / 1e3)
+    value = job_value(pairs, world, args.steps, ms)
+    value_e2e = job_value(pairs, world, args.steps, ms_e2e)
+    sel = job_value(W.B * W.layers, world, args.steps, ms)
     peaks, peak_kind = measured_peaks()
     bytes_launch = W.score_bytes_per_launch()
     achieved = bytes_launch / (score_ms / 1e3) / 1e9

@@ -305,6 +305,21 @@ size_t hsi_workspace_size(hsi_ws_kind kind, int32_t B, int64_t max_n, int32_t k)
  * (or HSI_ERR_CUDA if the synchronisation itself failed). */
 hsi_status hsi_device_error(cudaStream_t stream);
 
+/*
+ * Diagnostics for the failure path (no counterpart on the pages), current
+ * device, synchronous:
+ *  HSI_DEBUG_WAIT_LIMIT_NS: the wall-clock limit of every bounded wait in the
+ *    kernels (default 1 s). When a wait runs out the kernel records
+ *    HSI_ERR_DEVICE_TIMEOUT, drains what it has in flight, frees its TMEM and
+ *    returns; the context stays usable.
+ *  HSI_DEBUG_SKIP_FIRST_COPY: nonzero makes the scoring kernels' producer skip
+ *    the copy of its first unit, so that the consumer's wait runs out (a test
+ *    of the path above). Zero restores normal operation.
+ */
+#define HSI_DEBUG_WAIT_LIMIT_NS 1
+#define HSI_DEBUG_SKIP_FIRST_COPY 2
+hsi_status hsi_debug_set(int what, long long value);
+
 /* HSI_OK if the current device is compute capability 10.3, else UNSUPPORTED. */
 hsi_status hsi_device_check(void);
 

@@ -29,7 +29,7 @@ WS_QUANTIZE, WS_SCORE, WS_TOPK, WS_POOL, WS_FULL_LAYER, WS_REINDEX_LAYER = 0, 1,
 EXPORTS = ["hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
            "hsi_workspace_size", "hsi_device_error", "hsi_device_check", "hsi_status_string",
            "hsi_kernel_launches", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer", "hsi_reindex_layer",
-           "hsi_topk_noalloc"]
+           "hsi_topk_noalloc", "hsi_debug_set"]
 
 
 class HsiError(RuntimeError):
@@ -72,6 +72,7 @@ def lib() -> ctypes.CDLL:
         L.hsi_reindex_layer.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i64, i32, vp, vp, vp,
                                         sz, vp]
         L.hsi_topk_noalloc.argtypes = [vp, i64, vp, i32, i64, i32, vp, i64, i32, vp, vp, vp]
+        L.hsi_debug_set.argtypes = [ctypes.c_int, ctypes.c_longlong]
         L.hsi_workspace_size.argtypes = [ctypes.c_int, i32, i64, i32]
         L.hsi_workspace_size.restype = sz
         L.hsi_device_error.argtypes = [vp]
@@ -84,7 +85,7 @@ def lib() -> ctypes.CDLL:
         L.hsi_kernel_launches.restype = ctypes.c_uint64
         for name in ("hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
                      "hsi_device_error", "hsi_device_check", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer",
-                     "hsi_reindex_layer", "hsi_topk_noalloc"):
+                     "hsi_reindex_layer", "hsi_topk_noalloc", "hsi_debug_set"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -121,6 +122,14 @@ def workspace(kind: int, B: int, max_n: int, k: int = 0, device="cuda") -> torch
 def kernel_launches() -> int:
     """Kernels launched by the library so far in this process."""
     return int(lib().hsi_kernel_launches())
+
+
+DEBUG_WAIT_LIMIT_NS, DEBUG_SKIP_FIRST_COPY = 1, 2
+
+
+def debug_set(what: int, value: int):
+    """Diagnostics: the kernels' wait limit, or the test switch that makes a wait run out."""
+    _check("hsi_debug_set", lib().hsi_debug_set(what, value))
 
 
 def device_check():

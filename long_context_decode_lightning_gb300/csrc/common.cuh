@@ -18,6 +18,12 @@ __device__ uint32_t g_hsi_error = 0;
 
 __device__ __forceinline__ void raise_error(uint32_t code) { atomicOr(&g_hsi_error, code); }
 
+// Diagnostics (set from the host through hsi_debug_set): the wall-clock limit
+// of every bounded wait, and a test switch that makes the scoring kernels'
+// producer skip its first copy so that a consumer's wait runs out.
+__device__ unsigned long long g_hsi_wait_limit_ns = HSI_WAIT_TIMEOUT_NS;
+__device__ int g_hsi_skip_first_copy = 0;
+
 // Optional wait tracing (build with -DHSI_TRACE): cycles each warp role spent
 // blocked in each kind of wait, and its total loop cycles, summed over CTAs.
 #ifdef HSI_TRACE
@@ -48,10 +54,11 @@ struct WaitTrace {
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    const uint64_t limit = *(volatile unsigned long long*)&g_hsi_wait_limit_ns;
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > HSI_WAIT_TIMEOUT_NS) {
+        if (globaltimer_ns() - t0 > limit) {
             raise_error(DEVERR_TIMEOUT);
             *abort = 1;
             return false;

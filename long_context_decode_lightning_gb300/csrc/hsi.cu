@@ -195,6 +195,19 @@ int hsi_trace_marks(unsigned long long* out /* [1024][4] */) {
 }
 #endif
 
+hsi_status hsi_debug_set(int what, long long value) {
+    if (what == HSI_DEBUG_WAIT_LIMIT_NS) {
+        if (value <= 0) return HSI_ERR_INVALID_ARG;
+        const unsigned long long v = (unsigned long long)value;
+        return cuda_ok(cudaMemcpyToSymbol(g_hsi_wait_limit_ns, &v, sizeof(v)));
+    }
+    if (what == HSI_DEBUG_SKIP_FIRST_COPY) {
+        const int v = value != 0;
+        return cuda_ok(cudaMemcpyToSymbol(g_hsi_skip_first_copy, &v, sizeof(v)));
+    }
+    return HSI_ERR_INVALID_ARG;
+}
+
 hsi_status hsi_device_check(void) {
     int dev = 0, major = 0, minor = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return HSI_ERR_CUDA;

@@ -235,8 +235,9 @@ __device__ __forceinline__ bool wait_one(uint64_t* bar, uint32_t parity, ScoreSh
 // Bounded wait that ignores the abort flag (teardown: drain what is in flight).
 __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
+    const uint64_t limit = *(volatile unsigned long long*)&g_hsi_wait_limit_ns;
     while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > HSI_WAIT_TIMEOUT_NS) {
+        if (globaltimer_ns() - t0 > limit) {
             raise_error(DEVERR_TIMEOUT);
             return;
         }
@@ -444,7 +445,8 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
             uint8_t* dst = stages + st.i * C::STAGE_BYTES;
             if (!GATHER) {
                 const int nrec = (int)min((int64_t)C::UNIT_RECS, nrec_all - (int64_t)t * C::UNIT_RECS);
-                if (lane == 0) {
+                const bool skip = u == 0 && *(volatile int*)&g_hsi_skip_first_copy;  // diagnostics only
+                if (lane == 0 && !skip) {
                     mbar_arrive_expect_tx(&full[st.i], (uint32_t)(nrec * REC));
                     bulk_g2s(dst, p.k_rec + (k_base + (int64_t)t * C::UNIT_RECS) * REC, (uint32_t)(nrec * REC),
                              &full[st.i]);
