@@ -12,6 +12,7 @@ namespace hsi {
 // Grid-stride 16-byte loads over the buffer; one xor per CTA keeps them live.
 __global__ void __launch_bounds__(512) calib_read_ldg_kernel(const uint4* __restrict__ buf, size_t n16,
                                                              unsigned long long* sink) {
+    griddep_wait();  // the buffer may have just been written by the previous kernel
     uint32_t x = 0;
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -32,6 +33,7 @@ __global__ void __launch_bounds__(512) calib_read_ldg_kernel(const uint4* __rest
 // warp consumes (waits and releases). Mirrors the scoring kernel's producer.
 __global__ void __launch_bounds__(64, 1) calib_read_bulk_kernel(const uint8_t* __restrict__ buf, size_t bytes,
                                                                int chunk, int stages, unsigned long long* sink) {
+    griddep_wait();  // the buffer may have just been written by the previous kernel
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)stages * chunk);

@@ -18,8 +18,15 @@ using namespace hsi;
 
 namespace {
 
-// Stage ring depth and 128-key tiles per stage of each scoring variant.
-constexpr int kDecodeStages = 8, kDecodeUT = 2;
+// Stage ring depth and 128-key tiles per stage of each scoring variant
+// (the decode pair can be overridden at build time for tuning sweeps).
+#ifndef HSI_DECODE_STAGES
+#define HSI_DECODE_STAGES 4
+#endif
+#ifndef HSI_DECODE_UT
+#define HSI_DECODE_UT 4
+#endif
+constexpr int kDecodeStages = HSI_DECODE_STAGES, kDecodeUT = HSI_DECODE_UT;
 constexpr int kGatherStages = 10, kGatherUT = 2;
 constexpr int kPrefillStages = 8, kPrefillUT = 1;
 constexpr int kCandCap = 65536;  // survivors of the histogram pass kept per query
@@ -34,6 +41,27 @@ std::atomic<uint64_t> g_launches{0};
 hsi_status launch_ok() {
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return cuda_ok(cudaGetLastError());
+}
+
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// while the previous kernel on the stream finishes; it overlaps only its
+// input-independent prologue and waits (griddep_wait) before touching memory
+// the previous kernels write.
+template <typename... KArgs, typename... Args>
+hsi_status launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return e == cudaSuccess ? HSI_OK : HSI_ERR_CUDA;
 }
 
 int sm_count() {
@@ -90,13 +118,11 @@ hsi_status run_select(SelParams sp, int64_t max_items, cudaStream_t s, bool hist
         const dim3 grid((unsigned)((max_items + SCAN_CHUNK - 1) / SCAN_CHUNK), (unsigned)sp.B);
         if (!hist_ready) {
             if (cudaMemsetAsync(sp.hist, 0, (size_t)sp.B * HIST_BINS * 4, s) != cudaSuccess) return HSI_ERR_CUDA;
-            sel_hist_kernel<<<grid, SCAN_THREADS, 0, s>>>(sp);
-            if (launch_ok() != HSI_OK) return HSI_ERR_CUDA;
+            if (launch(sel_hist_kernel, dim3(grid), dim3(SCAN_THREADS), 0, s, sp) != HSI_OK)
+                return HSI_ERR_CUDA;
         }
-        sel_thresh_kernel<<<sp.B, SCAN_THREADS, 0, s>>>(sp);
-        if (launch_ok() != HSI_OK) return HSI_ERR_CUDA;
-        sel_collect_kernel<<<grid, SCAN_THREADS, 0, s>>>(sp);
-        if (launch_ok() != HSI_OK) return HSI_ERR_CUDA;
+        if (launch(sel_thresh_kernel, dim3(sp.B), dim3(SCAN_THREADS), 0, s, sp) != HSI_OK) return HSI_ERR_CUDA;
+        if (launch(sel_collect_kernel, dim3(grid), dim3(SCAN_THREADS), 0, s, sp) != HSI_OK) return HSI_ERR_CUDA;
     }
     static bool attr_set = false;
     if (!attr_set) {
@@ -105,8 +131,7 @@ hsi_status run_select(SelParams sp, int64_t max_items, cudaStream_t s, bool hist
             return HSI_ERR_CUDA;
         attr_set = true;
     }
-    sel_final_kernel<<<sp.B, SEL_THREADS, sizeof(SelSmem), s>>>(sp);
-    return launch_ok();
+    return launch(sel_final_kernel, dim3(sp.B), dim3(SEL_THREADS), sizeof(SelSmem), s, sp);
 }
 
 template <int NQ, bool GATHER, int STAGES, int UT>
@@ -121,8 +146,7 @@ hsi_status launch_score(const ScoreParams& p, cudaStream_t s) {
     }
     const int sms = sm_count();
     if (sms <= 0) return HSI_ERR_CUDA;
-    score_kernel<NQ, GATHER, STAGES, UT><<<sms, C::THREADS, C::SMEM_BYTES, s>>>(p);
-    return launch_ok();
+    return launch(score_kernel<NQ, GATHER, STAGES, UT>, dim3(sms), dim3(C::THREADS), C::SMEM_BYTES, s, p);
 }
 
 // ---- fixed scratch of hsi_topk_noalloc ----------------------------------------
@@ -268,21 +292,20 @@ hsi_status hsi_quantize_nvfp4(const uint16_t* x, int64_t n_tensors, int64_t rows
     p.rec = rec;
     if (mode == 0 && (!ws || ws_bytes < (size_t)n_tensors * 4 || !aligned(ws, 256))) return HSI_ERR_WORKSPACE;
     if (rows_per_tensor <= QUANT_SMALL_ROWS && n_tensors <= INT32_MAX) {
-        quant_small_kernel<<<(unsigned)n_tensors, 256, 0, stream>>>(p, mode);
-        return launch_ok();
+        return launch(quant_small_kernel, dim3((unsigned)n_tensors), dim3(256), 0, stream, p, mode);
     }
     if (mode == 0) {
         p.amax_bits = static_cast<uint32_t*>(ws);
         if (cudaMemsetAsync(ws, 0, (size_t)n_tensors * 4, stream) != cudaSuccess) return HSI_ERR_CUDA;
         const int64_t rows = n_tensors * rows_per_tensor;
-        quant_amax_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
-        if (launch_ok() != HSI_OK) return HSI_ERR_CUDA;
-        quant_scale_kernel<<<(unsigned)((n_tensors + 255) / 256), 256, 0, stream>>>(p);
-        if (launch_ok() != HSI_OK) return HSI_ERR_CUDA;
+        if (launch(quant_amax_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, stream, p) != HSI_OK)
+            return HSI_ERR_CUDA;
+        if (launch(quant_scale_kernel, dim3((unsigned)((n_tensors + 255) / 256)), dim3(256), 0, stream, p) !=
+            HSI_OK)
+            return HSI_ERR_CUDA;
     }
     const int64_t prows = n_tensors * p.rec_per_tensor * 8;
-    quant_encode_kernel<<<(unsigned)((prows + 7) / 8), 256, 0, stream>>>(p);
-    return launch_ok();
+    return launch(quant_encode_kernel, dim3((unsigned)((prows + 7) / 8)), dim3(256), 0, stream, p);
 }
 
 static hsi_status check_score_common(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
@@ -449,8 +472,9 @@ hsi_status hsi_candidate_pool(const float* scores, int64_t ld, const float* bloc
     int64_t bld = ldb;
     if (need_bmax) {
         const dim3 grid((unsigned)((max_blocks + 255) / 256 > 0 ? (max_blocks + 255) / 256 : 1), (unsigned)B);
-        block_max_kernel<<<grid, 256, 0, stream>>>(scores, ld, n_visible, block_size, wsp.bmax, max_blocks);
-        if (launch_ok() != HSI_OK) return HSI_ERR_CUDA;
+        if (launch(block_max_kernel, dim3(grid), dim3(256), 0, stream, scores, ld, n_visible, block_size, wsp.bmax,
+                   max_blocks) != HSI_OK)
+            return HSI_ERR_CUDA;
         bm = wsp.bmax;
         bld = max_blocks;
     }
@@ -482,8 +506,8 @@ hsi_status hsi_calib_read(const void* buf, size_t bytes, int method, int chunk, 
     const int sms = sm_count();
     if (sms <= 0) return HSI_ERR_CUDA;
     if (method == 0) {
-        calib_read_ldg_kernel<<<sms * 4, 512, 0, stream>>>(static_cast<const uint4*>(buf), bytes / 16, sink);
-        return launch_ok();
+        return launch(calib_read_ldg_kernel, dim3(sms * 4), dim3(512), 0, stream, static_cast<const uint4*>(buf),
+                      bytes / 16, sink);
     }
     if (method != 1 || chunk < 16 || chunk % 16 || stages < 1) return HSI_ERR_INVALID_ARG;
     const size_t smem = (size_t)stages * chunk + 2 * (size_t)stages * 8 + 1024;
@@ -491,8 +515,8 @@ hsi_status hsi_calib_read(const void* buf, size_t bytes, int method, int chunk, 
     if (cudaFuncSetAttribute(calib_read_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return HSI_ERR_CUDA;
-    calib_read_bulk_kernel<<<sms, 64, smem, stream>>>(static_cast<const uint8_t*>(buf), bytes, chunk, stages, sink);
-    return launch_ok();
+    return launch(calib_read_bulk_kernel, dim3(sms), dim3(64), smem, stream, static_cast<const uint8_t*>(buf), bytes,
+                  chunk, stages, sink);
 }
 
 hsi_status hsi_calib_mma(int n, int iters, unsigned long long* sink, cudaStream_t stream) {
@@ -533,11 +557,9 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     uint8_t* tail = static_cast<uint8_t*>(ws) + sel_ws_bytes(B, max_visible > nb ? max_visible : nb, false, 0);
     uint32_t* bhist = reinterpret_cast<uint32_t*>(tail);
     float* bmax = reinterpret_cast<float*>(tail + align_up((size_t)B * HIST_BINS * 4, 256));
-    const bool big_topk = max_visible > SEL_CAP, big_pool = pool && nb > SEL_CAP;
+    const bool big_topk = max_visible > SEL_CAP;
     if (phases & 1) {
     if (big_topk && cudaMemsetAsync(wsp.hist, 0, (size_t)B * HIST_BINS * 4, stream) != cudaSuccess)
-        return HSI_ERR_CUDA;
-    if (big_pool && cudaMemsetAsync(bhist, 0, (size_t)B * HIST_BINS * 4, stream) != cudaSuccess)
         return HSI_ERR_CUDA;
     ScoreParams p{};
     p.q_rec = q_rec;
@@ -554,7 +576,6 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     p.bmax = pool ? bmax : nullptr;
     p.ldb = nb;
     p.key_hist = big_topk ? wsp.hist : nullptr;
-    p.bmax_hist = big_pool ? bhist : nullptr;
     st = launch_score<1, false, kDecodeStages, kDecodeUT>(p, stream);
     if (st != HSI_OK) return st;
     }
@@ -591,7 +612,10 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     pp.n_pool = n_pool;
     pp.bits = pool_bits;
     pp.ld_bits = ld_bits;
-    return run_select(pp, nb, stream, true);
+    // the block-max histogram is a separate pass over the block maxima (an
+    // eighth of the scores): counting it in the scoring epilogue, where the
+    // maxima of a warp land in one or two bins, cost more than this pass
+    return run_select(pp, nb, stream, false);
 }
 
 hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,

@@ -30,7 +30,8 @@ __device__ __forceinline__ void rotate_row_warp(const QuantParams& p, int64_t ro
     const int lane = threadIdx.x & 31;
     const uint2 raw = *reinterpret_cast<const uint2*>(p.x + row * 128 + lane * 4);
     const int wsel = lane >> 3;  // select without dynamic indexing of the parameter array
-    const uint32_t word = wsel == 0 ? p.neg_mask[0] : wsel == 1 ? p.neg_mask[1] : wsel == 2 ? p.neg_mask[2] : p.neg_mask[3];
+    const uint32_t word =
+        wsel == 0 ? p.neg_mask[0] : wsel == 1 ? p.neg_mask[1] : wsel == 2 ? p.neg_mask[2] : p.neg_mask[3];
     const uint32_t bits = word >> ((lane & 7) * 4);
     uint32_t h[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
 #pragma unroll
@@ -65,6 +66,8 @@ __device__ __forceinline__ void rotate_row_warp(const QuantParams& p, int64_t ro
 }
 
 __global__ void __launch_bounds__(256) quant_amax_kernel(QuantParams p) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int64_t total = p.n_tensors * p.rpt;
     if (warp >= total) return;
@@ -77,6 +80,8 @@ __global__ void __launch_bounds__(256) quant_amax_kernel(QuantParams p) {
 }
 
 __global__ void quant_scale_kernel(QuantParams p) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= p.n_tensors) return;
     const float amax = __uint_as_float(p.amax_bits[t]);
@@ -139,6 +144,8 @@ __device__ __forceinline__ void encode_row_warp(const QuantParams& p, int64_t t,
 }
 
 __global__ void __launch_bounds__(256) quant_encode_kernel(QuantParams p) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t prow = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // padded row index
     const int64_t padded_rows = p.rec_per_tensor * 8;
     if (prow >= p.n_tensors * padded_rows) return;
@@ -155,6 +162,8 @@ __global__ void __launch_bounds__(256) quant_encode_kernel(QuantParams p) {
 constexpr int QUANT_SMALL_ROWS = 64;
 
 __global__ void __launch_bounds__(256) quant_small_kernel(QuantParams p, int mode) {
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ float wmax[8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t = blockIdx.x;

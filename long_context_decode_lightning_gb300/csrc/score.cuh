@@ -61,11 +61,9 @@ struct ScoreParams {
     int64_t ld;
     float* bmax;
     int64_t ldb;
-    // optional (single-query groups): 4096-bin histograms of the top 12 bits of
-    // the order keys of the scores and of the block maxima (the newest block
-    // counted as +inf), [B][4096], added to
+    // optional (single-query groups): 4096-bin histogram of the top 12 bits of
+    // the order keys of the scores, [B][4096], added to
     uint32_t* key_hist;
-    uint32_t* bmax_hist;
     // pool gather
     const int32_t* block_ids;
     const int32_t* n_kept;
@@ -79,7 +77,7 @@ struct ScoreCfg {
     static constexpr int N = 32 * NQ;
     static constexpr int UNIT_RECS = 16 * UT;
     static constexpr int UNIT_KEYS = TILE_KEYS * UT;
-    static constexpr int NACC = NQ == 1 ? 4 : 2;  // accumulator sets (one set = UT tiles)
+    static constexpr int NACC = (NQ == 1 && UT <= 2) ? 4 : 2;  // accumulator sets (one set = UT tiles)
     static constexpr int Q_BYTES = NQ * 4 * REC;
     static constexpr int STAGE_BYTES = UNIT_RECS * REC;
     static constexpr int QSLOT_BYTES = ((Q_BYTES + 127) / 128) * 128;
@@ -105,11 +103,16 @@ struct ScoreCfg {
     // histogram slots for the first HIST_SLOTS queries of the CTA's range
     static constexpr int HIST_SLOTS = (!GATHER && NQ == 1) ? 2 : 0;
     static constexpr int OFF_HIST = OFF_IDS + IDS_BYTES;
-    static constexpr int HIST_BYTES = HIST_SLOTS * 2 * 4096 * 4;
-    static constexpr int OFF_BARS = OFF_HIST + HIST_BYTES;
-    // full, sfready, empty per stage; acc_full, acc_empty per accumulator set;
+    static constexpr int HIST_BYTES = HIST_SLOTS * 4096 * 4;
+    // multi-query tiles: the scaled head weights of each epilogue warp's queries
+    // live in shared memory (one copy per warp) instead of 32 NQ registers
+    static constexpr int OFF_WQ = OFF_HIST + HIST_BYTES;
+    static constexpr int WQ_BYTES = NQ > 1 ? 4 * EPI_GROUPS * NQ * 32 * 4 : 0;
+    static constexpr int OFF_BARS = OFF_WQ + WQ_BYTES;
+    // full, sfready, empty per stage; acc_full per accumulator set, acc_empty per
+    // tile of a set (the epilogue frees each tile as soon as it has read it);
     // q_full, q_ready, q_empty per slot; ids_full, ids_free per id slot; drain
-    static constexpr int NBARS = 3 * STAGES + 2 * NACC + 6 + (GATHER ? 2 * IDS_AHEAD : 0) + 1;
+    static constexpr int NBARS = 3 * STAGES + NACC * (1 + UT) + 6 + (GATHER ? 2 * IDS_AHEAD : 0) + 1;
     static constexpr int SMEM_BYTES = OFF_BARS + NBARS * 8 + 64 + 1024;  // + alignment slack
     static_assert(NQ <= 4, "B scale rows fit one 128-row layout");
     static_assert(COLS_USED <= 512, "TMEM");
@@ -126,6 +129,7 @@ struct ScoreShared {  // small control block after the barriers
     int t0;
     long long count;
 };
+
 
 // Whole block (at most 1024 threads): this CTA's first unit (g0, t0) and unit
 // count. part_smem holds at least 65 entries.
@@ -319,8 +323,8 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
     uint8_t* stages = smem + C::OFF_STAGES;
     uint8_t* qslots = smem + C::OFF_QSLOTS;
     int32_t* ids_ring = reinterpret_cast<int32_t*>(smem + C::OFF_IDS);
-    uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + C::OFF_HIST);  // [slot][key, bmax][4096]
-    const bool fuse_hist = C::HIST_SLOTS > 0 && (p.key_hist || p.bmax_hist);
+    uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + C::OFF_HIST);  // [slot][4096]
+    const bool fuse_hist = C::HIST_SLOTS > 0 && p.key_hist;
     if (fuse_hist)
         for (int i = threadIdx.x; i < C::HIST_BYTES / 4; i += blockDim.x) hist_s[i] = 0u;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
@@ -329,7 +333,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
     uint64_t* empty = sfready + STAGES;
     uint64_t* acc_full = empty + STAGES;
     uint64_t* acc_empty = acc_full + C::NACC;
-    uint64_t* q_full = acc_empty + C::NACC;
+    uint64_t* q_full = acc_empty + C::NACC * UT;
     uint64_t* q_ready = q_full + 2;
     uint64_t* q_empty = q_ready + 2;
     uint64_t* ids_full = q_empty + 2;
@@ -352,10 +356,8 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
         fence_mbar_init();
     }
     if (threadIdx.x == 0) {
-        for (int i = 0; i < C::NACC; ++i) {
-            mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_empty[i], 4);
-        }
+        for (int i = 0; i < C::NACC; ++i) mbar_init(&acc_full[i], 1);
+        for (int i = 0; i < C::NACC * UT; ++i) mbar_init(&acc_empty[i], 4);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&q_full[i], 1);
             mbar_init(&q_ready[i], 4);
@@ -370,6 +372,9 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
         sh->abort = 0;
         fence_mbar_init();
     }
+    // everything above touches only this CTA's shared memory; inputs come next
+    griddep_wait();
+    griddep_launch_dependents();
     if (warp == C::MMA_WARP) tmem_alloc(&sh->tmem_base, C::TMEM_COLS);
     schedule_range(p.ngroups, [&](int g) { return group_units<NQ, GATHER, UT>(p, g); }, sh, part);
     tc_fence_before();
@@ -530,14 +535,19 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                     if (!wait_one(&q_ready[gc & 1], (gc >> 1) & 1, sh, tr, TR_MMA_QREADY)) break;
                 }
                 if (!wait_one(&sfready[st.i], st.ph, sh, tr, TR_MMA_SFREADY)) break;
-                if (!wait_one(&acc_empty[ac.i], ac.ph ^ 1u, sh, tr, TR_MMA_ACCEMPTY)) break;
                 HSI_TSTART(t_issue);
-                tc_fence_after();
+                bool stop = false;
                 const uint32_t a0 = smem_u32(stages + st.i * C::STAGE_BYTES);
                 const uint32_t b0 = smem_u32(qslots + (gc & 1) * C::QSLOT_BYTES);
                 const uint32_t sfb = tmem + C::COL_SFB + (gc & 1) * 8;
 #pragma unroll
                 for (int sub = 0; sub < UT; ++sub) {
+                    // the epilogue has read this tile of the set's previous unit
+                    if (!wait_one(&acc_empty[ac.i * UT + sub], ac.ph ^ 1u, sh, tr, TR_MMA_ACCEMPTY)) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
                     const uint32_t d = tmem + C::COL_ACC + (ac.i * UT + sub) * C::N;
                     const uint32_t sfa = tmem + C::COL_SFA + (st.i * UT + sub) * 8;
                     const uint32_t at = a0 + sub * 16 * REC;
@@ -546,6 +556,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                         mma_nvf4(d, smem_desc(at + kk * 256, 128, REC), smem_desc(b0 + kk * 256, 128, REC), idesc,
                                  sfa + kk * 4, sfb + kk * 4, kk);
                 }
+                if (stop) break;
                 // one commit: the epilogue that sees it also frees the stage
                 tc_commit(&acc_full[ac.i]);
                 HSI_TEND(t_issue, TR_MMA_ISSUE);
@@ -604,13 +615,14 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
         it.init(p, sh);
         const int b_first = sh->g0 * NQ;
         // histogram bins of query b: shared-memory slot, or global past the slots
-        auto hist_of = [&](int b, int which) -> uint32_t* {
+        auto hist_of = [&](int b) -> uint32_t* {
             const int slot = b - b_first;
-            if (slot >= 0 && slot < C::HIST_SLOTS) return hist_s + (slot * 2 + which) * 4096;
-            return (which == 0 ? p.key_hist : p.bmax_hist) + (int64_t)b * 4096;
+            if (slot >= 0 && slot < C::HIST_SLOTS) return hist_s + slot * 4096;
+            return p.key_hist + (int64_t)b * 4096;
         };
         int cur_g = -1;
-        float wq[NQ][32];
+        float wq[32];  // single query: its scaled head weights
+        float* wq_s = reinterpret_cast<float*>(smem + C::OFF_WQ) + (warp - C::FIRST_EPI_WARP) * NQ * 32;
         int nv[NQ];
         int nk = 0;
         Ring st, ac;
@@ -632,16 +644,22 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                     const int b = g * NQ + qi;
                     nv[qi] = p.n_vis[b];
                     const float sc = p.g_q[b] * p.g_k[b] * 0.0078125f;
-                    const float4* wv = reinterpret_cast<const float4*>(p.w + (int64_t)b * 32);
+                    if constexpr (NQ == 1) {
+                        const float4* wv = reinterpret_cast<const float4*>(p.w + (int64_t)b * 32);
 #pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        const float4 v = __ldg(wv + j4);
-                        wq[qi][4 * j4 + 0] = v.x * sc;
-                        wq[qi][4 * j4 + 1] = v.y * sc;
-                        wq[qi][4 * j4 + 2] = v.z * sc;
-                        wq[qi][4 * j4 + 3] = v.w * sc;
+                        for (int j4 = 0; j4 < 8; ++j4) {
+                            const float4 v = __ldg(wv + j4);
+                            wq[4 * j4 + 0] = v.x * sc;
+                            wq[4 * j4 + 1] = v.y * sc;
+                            wq[4 * j4 + 2] = v.z * sc;
+                            wq[4 * j4 + 3] = v.w * sc;
+                        }
+                    } else {
+                        __syncwarp();  // the previous query's weights are no longer read
+                        wq_s[qi * 32 + lane] = __ldg(p.w + (int64_t)b * 32 + lane) * sc;
                     }
                 }
+                if constexpr (NQ > 1) __syncwarp();
                 if (GATHER) nk = min(p.n_kept[g], p.n_keep);
             }
             // gather: the positions of this thread's slots, loaded before the wait
@@ -666,34 +684,34 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                 for (int qi = 0; qi < NQ; ++qi) {
                     float x[32];
                     tmem_ld32(dbase + qi * 32, x);
+                    if (qi == NQ - 1) {  // the tile is in registers: the MMA may overwrite it
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&acc_empty[ac.i * UT + sub]);
+                    }
                     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
                     for (int j = 0; j < 32; j += 4) {
-                        s0 = fmaf(wq[qi][j], fmaxf(x[j], 0.f), s0);
-                        s1 = fmaf(wq[qi][j + 1], fmaxf(x[j + 1], 0.f), s1);
-                        s2 = fmaf(wq[qi][j + 2], fmaxf(x[j + 2], 0.f), s2);
-                        s3 = fmaf(wq[qi][j + 3], fmaxf(x[j + 3], 0.f), s3);
+                        float4 w4;
+                        if constexpr (NQ == 1) w4 = make_float4(wq[j], wq[j + 1], wq[j + 2], wq[j + 3]);
+                        else w4 = *reinterpret_cast<const float4*>(wq_s + qi * 32 + j);
+                        s0 = fmaf(w4.x, fmaxf(x[j], 0.f), s0);
+                        s1 = fmaf(w4.y, fmaxf(x[j + 1], 0.f), s1);
+                        s2 = fmaf(w4.z, fmaxf(x[j + 2], 0.f), s2);
+                        s3 = fmaf(w4.w, fmaxf(x[j + 3], 0.f), s3);
                     }
                     const float sc = (s0 + s1) + (s2 + s3);
                     const int b = g * NQ + qi;
                     if (!GATHER) {
                         const bool vis = key < nv[qi];
                         if (vis) p.scores[(int64_t)b * p.ld + key] = sc;
-                        if (fuse_hist && p.key_hist && vis) atomicAdd(hist_of(b, 0) + (order_key(sc) >> 20), 1u);
+                        if (fuse_hist && vis) atomicAdd(hist_of(b) + (order_key(sc) >> 20), 1u);
                         if (p.bmax) {
                             float m = vis ? sc : __uint_as_float(0xFF800000u);
                             m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
                             m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
                             m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-                            if ((lane & 7) == 0 && vis) {
-                                p.bmax[(int64_t)b * p.ldb + key / 8] = m;
-                                if (fuse_hist && p.bmax_hist) {
-                                    // the pool pins the newest block; -inf blocks are not eligible
-                                    const bool newest = key / 8 == (nv[qi] - 1) / 8;
-                                    const uint32_t bk = newest ? 0xFF800000u : order_key(m);
-                                    if (bk != 0x007FFFFFu) atomicAdd(hist_of(b, 1) + (bk >> 20), 1u);
-                                }
-                            }
+                            if ((lane & 7) == 0 && vis) p.bmax[(int64_t)b * p.ldb + key / 8] = m;
                         }
                     } else if (pos[sub] >= 0) {
                         const float v = pos[sub] < nv[qi] ? sc : __uint_as_float(0xFF800000u);
@@ -701,9 +719,6 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[ac.i]);
             HSI_TEND(t_epi, TR_EPI_WORK);
             st.next(STAGES);
             ac.next(C::NACC);
@@ -728,12 +743,10 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
     if (warp == C::MMA_WARP) tmem_dealloc(tmem, C::TMEM_COLS);
     if (fuse_hist) {  // merge the shared-memory slots into the global histograms
         const int b_first = sh->g0 * NQ;
-        for (int i = threadIdx.x; i < C::HIST_SLOTS * 2 * 4096; i += blockDim.x) {
+        for (int i = threadIdx.x; i < C::HIST_SLOTS * 4096; i += blockDim.x) {
             const uint32_t v = hist_s[i];
-            const int slot = i / (2 * 4096), which = (i / 4096) & 1, bin = i & 4095;
-            const int b = b_first + slot;
-            uint32_t* g = which == 0 ? p.key_hist : p.bmax_hist;
-            if (v && g && b < p.B) atomicAdd(g + (int64_t)b * 4096 + bin, v);
+            const int b = b_first + i / 4096;
+            if (v && b < p.B) atomicAdd(p.key_hist + (int64_t)b * 4096 + (i & 4095), v);
         }
     }
 #ifdef HSI_TRACE

@@ -109,6 +109,8 @@ __device__ __forceinline__ void sel_key4(const SelParams& p, int b, const float*
 }
 
 __global__ void __launch_bounds__(SCAN_THREADS) sel_hist_kernel(SelParams p) {
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ uint32_t sh[HIST_BINS];
     const int b = blockIdx.y;
     const int64_t n = sel_items(p, b);
@@ -176,6 +178,8 @@ __device__ uint32_t threshold_bin(const uint32_t* gh, int k, uint32_t* scratch /
 
 // One CTA per query: the threshold bin from the merged histogram.
 __global__ void __launch_bounds__(SCAN_THREADS) sel_thresh_kernel(SelParams p) {
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ uint32_t scratch[SCAN_THREADS + 1];
     const int b = blockIdx.x;
     const uint32_t thr = threshold_bin(p.hist + (int64_t)b * HIST_BINS, p.k, scratch);
@@ -183,6 +187,8 @@ __global__ void __launch_bounds__(SCAN_THREADS) sel_thresh_kernel(SelParams p) {
 }
 
 __global__ void __launch_bounds__(SCAN_THREADS) sel_collect_kernel(SelParams p) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int b = blockIdx.y;
     const int64_t n = sel_items(p, b);
     const int64_t lo = (int64_t)blockIdx.x * SCAN_CHUNK;
@@ -481,6 +487,8 @@ __device__ int block_select(const Src& src, SelSmem& s, int k, bool ids_only) {
 }
 
 __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) {
+    griddep_wait();
+    griddep_launch_dependents();
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SelSmem& s = *reinterpret_cast<SelSmem*>(smem_raw);
     const int b = blockIdx.x;
@@ -588,6 +596,8 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) 
 // over visible positions (< n_visible[b]), for j < ceil(n_visible[b]/bs).
 __global__ void block_max_kernel(const float* scores, int64_t ld, const int32_t* n_vis, int32_t bs, float* bmax,
                                  int64_t ldb) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int b = blockIdx.y;
     const int64_t n = n_vis[b];
     const int64_t nblk = (n + bs - 1) / bs;
