@@ -228,6 +228,7 @@ class DeviceWorkload:
             self.ws_pool = hsi.workspace(hsi.WS_POOL, B, self.maxv, 8, device=dev)
             self.pool_scores = torch.empty(B, wl.n_keep * 8, dtype=torch.float32, device=dev)
             self.ws_rtopk = hsi.workspace(hsi.WS_REINDEX_LAYER, B, wl.n_keep * 8, K_TOP, device=dev)
+            self.pool_rec = torch.empty(B, wl.n_keep * REC, dtype=torch.uint8, device=dev)
         self.ev_score = []
         self.pool_sum = None
         self.wl_signs = signs
@@ -259,12 +260,16 @@ class DeviceWorkload:
                     n_keep=wl.n_keep, ws=self.ws_full, phases=ph)))
         if wl.build_pool:
             def rest():
+                # the pooled K records, compacted once for the step's Reindex layers
+                hsi.pool_gather(self.k_rec[0], self.k_off, self.n_vis, self.ids, self.nk, B, self.pool_rec,
+                                n_keep=wl.n_keep)
                 for r in range(wl.reindex_layers):
                     l = wl.full_layers + r
                     hsi.quantize_nvfp4(self.q[l], B, 32, signs, self.g_q[l], self.q_rec[l], ws=self.ws_q)
                     hsi.reindex_layer(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0], self.k_off,
                                       self.n_vis, self.ids, self.nk, self.npool, B, self.pool_scores, K_TOP,
-                                      self.idx[l], self.val[l], n_keep=wl.n_keep, ws=self.ws_rtopk)
+                                      self.idx[l], self.val[l], n_keep=wl.n_keep, ws=self.ws_rtopk,
+                                      pool_rec=self.pool_rec)
             segs.append(("post", rest))
         merged = []
         for kind, fn in segs:  # fuse neighbouring non-scoring segments into one graph
@@ -274,6 +279,39 @@ class DeviceWorkload:
             else:
                 merged.append((kind, fn))
         return merged
+
+    def reindex_timings(self, reps=20):
+        """One Reindex layer, timed alone on the resident pool (CUDA events around
+        `reps` back-to-back calls): the whole layer through the compacted pool,
+        its top-k alone, the compaction, and the gathering scorer."""
+        torch, hsi, wl, B = self.torch, self.hsi, self.wl, self.B
+        l = wl.full_layers
+
+        def t(fn):
+            fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            return 1000.0 * e0.elapsed_time(e1) / reps
+
+        layer = t(lambda: hsi.reindex_layer(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0],
+                                            self.k_off, self.n_vis, self.ids, self.nk, self.npool, B,
+                                            self.pool_scores, K_TOP, self.idx[l], self.val[l], n_keep=wl.n_keep,
+                                            ws=self.ws_rtopk, pool_rec=self.pool_rec))
+        topk = t(lambda: hsi.topk(self.pool_scores, self.npool, B, wl.n_keep * 8, K_TOP, self.idx[l], self.val[l],
+                                  block_ids=self.ids, ws=self.ws_rtopk))
+        compact = t(lambda: hsi.pool_gather(self.k_rec[0], self.k_off, self.n_vis, self.ids, self.nk, B,
+                                            self.pool_rec, n_keep=wl.n_keep))
+        gather = t(lambda: hsi.score_pool(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0],
+                                          self.k_off, self.n_vis, self.ids, self.nk, wl.n_keep, B,
+                                          self.pool_scores))
+        pooled_bytes = int(self.nk.clamp(max=wl.n_keep).sum().item()) * REC
+        return {"layer_us": layer, "topk_us": topk, "scan_us": layer - topk, "compact_us": compact,
+                "gather_score_us": gather, "pooled_bytes_per_layer": pooled_bytes}
 
     def capture(self):
         torch = self.torch
@@ -484,6 +522,8 @@ def main():
         W.step_e2e()
     ms_e2e = timed(W.step_e2e, args.steps, sync_each=True)
     assert hsi.device_error() == 0, "device error during the end-to-end steps"
+    reindex = W.reindex_timings() if wl.build_pool else None
+    assert hsi.device_error() == 0, "device error during the Reindex timings"
 
     value = job_value(pairs, world, args.steps, ms)
     value_e2e = job_value(pairs, world, args.steps, ms_e2e)
@@ -509,6 +549,16 @@ def main():
         "gpu_launches": int(launches),
         "clocks": clk.summary(),
     }
+    if reindex is not None:
+        peak = float(peaks["hbm_gbs"])
+        gbs = lambda us: reindex["pooled_bytes_per_layer"] / (us * 1e-6) / 1e9
+        line["pool_builds_per_s"] = job_value(W.B, world, args.steps, ms)
+        line["reindex"] = dict(reindex, **{
+            "scan_gbs": gbs(reindex["scan_us"]), "scan_frac": gbs(reindex["scan_us"]) / peak,
+            "gather_score_gbs": gbs(reindex["gather_score_us"]),
+            "gather_score_frac": gbs(reindex["gather_score_us"]) / peak,
+            "note": "one layer timed alone on the resident pool; scan = layer minus its top-k; "
+                    "fractions of the measured copy bandwidth for the pooled bytes"})
     if rank == 0 and not args.no_cpu_baseline:
         nq = cpu_sample_size(wl)
         log(f"cpu baseline: oracle on {nq} queries")

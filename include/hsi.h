@@ -242,6 +242,28 @@ hsi_status hsi_score_pool(const uint8_t* q_rec, const float* g_q, const float* w
                           float* pool_scores, int64_t ld, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Compaction of each query's candidate pool, once per decode step: the pooled
+ * 576-byte K records of query b, in block-list order, into one contiguous run,
+ *   pool_rec[b][i] = the record k_rec_off[b] + block_ids[b][i],  i < min(n_kept[b], n_keep).
+ * Records of slots at or past n_kept[b] are left untouched.
+ * Page: "DeepSeek-V4.1 模型结构（3）", section "用浅层的打分结果限制深层的打分范围"
+ * (the Reindex layers score the same indexer K as the Full layer, each with
+ * its own query, inside the same per-query pool): the layers of a step can
+ * then stream the pool instead of each gathering it (hsi_reindex_layer with
+ * pool_rec). The method itself fixes only which records are scored; this
+ * layout is this library's.
+ *
+ *  k_rec, k_rec_off, n_visible: as for hsi_score_full.
+ *  block_ids, n_kept: as written by hsi_candidate_pool (block_size 8).
+ *  pool_rec (dev) [B][n_keep][576] bytes, 16-byte aligned; distinct from k_rec.
+ * A block id outside [0, ceil(n_visible[b] / 8)) is skipped and reported as
+ * HSI_ERR_DEVICE_ARG by hsi_device_error.
+ */
+hsi_status hsi_pool_gather(const uint8_t* k_rec, const int64_t* k_rec_off, const int32_t* n_visible,
+                           const int32_t* block_ids, const int32_t* n_kept, int32_t n_keep, int32_t B,
+                           uint8_t* pool_rec, cudaStream_t stream);
+
+/*
  * A decoder Full layer in one call: hsi_score_full, then the top-k of the
  * scores, then (block_ids != NULL) the candidate pool with blocks of 8, with
  * the selections' key histograms accumulated inside the scoring kernel
@@ -270,18 +292,23 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
                           cudaStream_t stream);
 
 /*
- * A decoder Reindex layer in one call: hsi_score_pool, then the top-k inside
- * the pool reported as global positions (hsi_topk with the block map).
+ * A decoder Reindex layer in one call: the pooled scores (hsi_score_pool),
+ * then the top-k inside the pool reported as global positions (hsi_topk with
+ * the block map).
  * Page: "DeepSeek-V4.1 模型结构（3）", section "用浅层的打分结果限制深层的打分范围"
  * (Reindex layers score only pooled positions and keep their own top-512).
  *
+ *  pool_rec NULL: the pooled records are gathered from k_rec (hsi_score_pool).
+ *          Otherwise (dev) the records hsi_pool_gather wrote for this pool,
+ *          streamed in place of the gather; k_rec is then not read. Both give
+ *          the same pool_scores, top_idx and top_val.
  *  n_pool (dev) int32 [B] as written by hsi_candidate_pool / hsi_full_layer.
- *  pool_scores [B][ld], ld >= 8 * n_keep, is written.
+ *  pool_scores [B][ld], ld >= 8 * n_keep, is written (as by hsi_score_pool).
  *  ws      (dev) hsi_workspace_size(HSI_WS_REINDEX_LAYER, B, 8 * n_keep, k).
  */
 hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
-                             const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible,
-                             const int32_t* block_ids, const int32_t* n_kept, const int32_t* n_pool, int32_t n_keep,
+                             const float* g_k, const int64_t* k_rec_off, const uint8_t* pool_rec,
+                             const int32_t* n_visible, const int32_t* block_ids, const int32_t* n_kept, const int32_t* n_pool, int32_t n_keep,
                              int32_t B, float* pool_scores, int64_t ld, int32_t k, int32_t* top_idx, float* top_val,
                              void* ws, size_t ws_bytes, cudaStream_t stream);
 

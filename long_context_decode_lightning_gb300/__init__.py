@@ -29,7 +29,7 @@ WS_QUANTIZE, WS_SCORE, WS_TOPK, WS_POOL, WS_FULL_LAYER, WS_REINDEX_LAYER = 0, 1,
 EXPORTS = ["hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
            "hsi_workspace_size", "hsi_device_error", "hsi_device_check", "hsi_status_string",
            "hsi_kernel_launches", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer", "hsi_reindex_layer",
-           "hsi_topk_noalloc", "hsi_debug_set"]
+           "hsi_topk_noalloc", "hsi_debug_set", "hsi_pool_gather"]
 
 
 class HsiError(RuntimeError):
@@ -69,8 +69,9 @@ def lib() -> ctypes.CDLL:
         L.hsi_score_pool.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i64, vp, sz, vp]
         L.hsi_full_layer.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, vp, i64, i32, vp, vp, i32, vp, vp, vp,
                                      vp, i64, i32, vp, sz, vp]
-        L.hsi_reindex_layer.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i64, i32, vp, vp, vp,
-                                        sz, vp]
+        L.hsi_reindex_layer.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i64, i32, vp, vp,
+                                        vp, sz, vp]
+        L.hsi_pool_gather.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp, vp]
         L.hsi_topk_noalloc.argtypes = [vp, i64, vp, i32, i64, i32, vp, i64, i32, vp, vp, vp]
         L.hsi_debug_set.argtypes = [ctypes.c_int, ctypes.c_longlong]
         L.hsi_workspace_size.argtypes = [ctypes.c_int, i32, i64, i32]
@@ -85,7 +86,7 @@ def lib() -> ctypes.CDLL:
         L.hsi_kernel_launches.restype = ctypes.c_uint64
         for name in ("hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
                      "hsi_device_error", "hsi_device_check", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer",
-                     "hsi_reindex_layer", "hsi_topk_noalloc", "hsi_debug_set"):
+                     "hsi_reindex_layer", "hsi_topk_noalloc", "hsi_debug_set", "hsi_pool_gather"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -242,13 +243,22 @@ def full_layer(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B, max_visible, 
         _ptr(pool_bits), ld_bits, phases, _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
 
 
+def pool_gather(k_rec, k_rec_off, n_visible, block_ids, n_kept, B, pool_rec, n_keep=2048, stream=None):
+    """Compact each query's pooled K records into pool_rec [B][n_keep][576] (block-list order)."""
+    _check("hsi_pool_gather", lib().hsi_pool_gather(
+        _ptr(k_rec), _ptr(k_rec_off), _ptr(n_visible), _ptr(block_ids), _ptr(n_kept), n_keep, B, _ptr(pool_rec),
+        _stream(stream)))
+
+
 def reindex_layer(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, block_ids, n_kept, n_pool, B, pool_scores, k,
-                  top_idx, top_val, n_keep=2048, ld=None, ws=None, stream=None):
-    """Reindex layer: pooled scores and the top-k inside the pool (global positions)."""
+                  top_idx, top_val, n_keep=2048, ld=None, ws=None, pool_rec=None, stream=None):
+    """Reindex layer: pooled scores and the top-k inside the pool (global positions).
+    pool_rec: the records pool_gather wrote for this pool (streamed), or None (gathered from k_rec)."""
     ld = pool_scores.shape[-1] if ld is None else ld
     if ws is None:
         ws = workspace(WS_REINDEX_LAYER, B, 8 * n_keep, k, device=pool_scores.device)
     _check("hsi_reindex_layer", lib().hsi_reindex_layer(
-        _ptr(q_rec), _ptr(g_q), _ptr(w), _ptr(k_rec), _ptr(g_k), _ptr(k_rec_off), _ptr(n_visible), _ptr(block_ids),
+        _ptr(q_rec), _ptr(g_q), _ptr(w), _ptr(k_rec), _ptr(g_k), _ptr(k_rec_off), _ptr(pool_rec), _ptr(n_visible),
+        _ptr(block_ids),
         _ptr(n_kept), _ptr(n_pool), n_keep, B, _ptr(pool_scores), ld, k, _ptr(top_idx), _ptr(top_val), _ptr(ws),
         0 if ws is None else ws.numel(), _stream(stream)))

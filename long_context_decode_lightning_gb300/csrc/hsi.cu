@@ -10,6 +10,7 @@
 #include "../../include/hsi.h"
 #include "calib.cuh"
 #include "common.cuh"
+#include "gather.cuh"
 #include "quantize.cuh"
 #include "score.cuh"
 #include "select.cuh"
@@ -27,7 +28,13 @@ namespace {
 #define HSI_DECODE_UT 4
 #endif
 constexpr int kDecodeStages = HSI_DECODE_STAGES, kDecodeUT = HSI_DECODE_UT;
-constexpr int kGatherStages = 10, kGatherUT = 2;
+#ifndef HSI_GATHER_STAGES
+#define HSI_GATHER_STAGES 10
+#endif
+#ifndef HSI_GATHER_UT
+#define HSI_GATHER_UT 2
+#endif
+constexpr int kGatherStages = HSI_GATHER_STAGES, kGatherUT = HSI_GATHER_UT;
 constexpr int kPrefillStages = 8, kPrefillUT = 1;
 constexpr int kCandCap = 65536;  // survivors of the histogram pass kept per query
 
@@ -618,14 +625,56 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     return run_select(pp, nb, stream, false);
 }
 
+hsi_status hsi_pool_gather(const uint8_t* k_rec, const int64_t* k_rec_off, const int32_t* n_visible,
+                           const int32_t* block_ids, const int32_t* n_kept, int32_t n_keep, int32_t B,
+                           uint8_t* pool_rec, cudaStream_t stream) {
+    if (!k_rec || !k_rec_off || !n_visible || !block_ids || !n_kept || !pool_rec || B <= 0 || B > 65535 ||
+        n_keep <= 0 || n_keep > (1 << 20) || pool_rec == k_rec)
+        return HSI_ERR_INVALID_ARG;
+    if (!aligned(k_rec, 16) || !aligned(pool_rec, 16)) return HSI_ERR_INVALID_ARG;
+    const int64_t chunks = (int64_t)n_keep * GATHER_CHUNKS;
+    const dim3 grid((unsigned)((chunks + GATHER_THREADS * GATHER_PER_THREAD - 1) / (GATHER_THREADS * GATHER_PER_THREAD)),
+                    (unsigned)B);
+    return launch(pool_gather_kernel, grid, dim3(GATHER_THREADS), 0, stream, reinterpret_cast<const uint4*>(k_rec),
+                  k_rec_off, n_visible, block_ids, n_kept, n_keep, reinterpret_cast<uint4*>(pool_rec));
+}
+
 hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
-                             const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible,
-                             const int32_t* block_ids, const int32_t* n_kept, const int32_t* n_pool, int32_t n_keep,
-                             int32_t B, float* pool_scores, int64_t ld, int32_t k, int32_t* top_idx, float* top_val,
-                             void* ws, size_t ws_bytes, cudaStream_t stream) {
+                             const float* g_k, const int64_t* k_rec_off, const uint8_t* pool_rec,
+                             const int32_t* n_visible, const int32_t* block_ids, const int32_t* n_kept,
+                             const int32_t* n_pool, int32_t n_keep, int32_t B, float* pool_scores, int64_t ld,
+                             int32_t k, int32_t* top_idx, float* top_val, void* ws, size_t ws_bytes,
+                             cudaStream_t stream) {
     if (!n_pool) return HSI_ERR_INVALID_ARG;
-    hsi_status st = hsi_score_pool(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, block_ids, n_kept, n_keep, B,
-                                   pool_scores, ld, nullptr, 0, stream);
+    hsi_status st;
+    if (!pool_rec) {
+        st = hsi_score_pool(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, block_ids, n_kept, n_keep, B,
+                            pool_scores, ld, nullptr, 0, stream);
+    } else {
+        // the compacted pool is a contiguous scan: query b's keys are its pool
+        // slots (n_pool[b] of them visible, the newest block last), its records
+        // n_keep apart; slots up to 8 n_kept[b] past the visible ones get -inf
+        if (!q_rec || !g_q || !w || !g_k || !block_ids || !n_kept || B <= 0 || n_keep <= 0 ||
+            n_keep > (1 << 20) || !pool_scores || ld < (int64_t)n_keep * 8)
+            return HSI_ERR_INVALID_ARG;
+        if (!aligned(q_rec, 16) || !aligned(pool_rec, 16) || !aligned(w, 16)) return HSI_ERR_INVALID_ARG;
+        ScoreParams p{};
+        p.q_rec = q_rec;
+        p.g_q = g_q;
+        p.w = w;
+        p.k_rec = pool_rec;
+        p.g_k = g_k;
+        p.k_off = nullptr;
+        p.k_stride = n_keep;
+        p.n_vis = n_pool;
+        p.B = B;
+        p.ngroups = B;
+        p.scores = pool_scores;
+        p.ld = ld;
+        p.pad_blocks = n_kept;
+        p.n_keep = n_keep;
+        st = launch_score<1, false, kDecodeStages, kDecodeUT>(p, stream);
+    }
     if (st != HSI_OK) return st;
     return hsi_topk(pool_scores, ld, n_pool, B, (int64_t)n_keep * 8, k, block_ids, n_keep, 8, top_idx, top_val, ws,
                     ws_bytes, stream);

@@ -45,6 +45,9 @@ namespace hsi {
 constexpr int REC = 576;
 constexpr int TILE_KEYS = 128;
 constexpr int IDS_AHEAD = 8;  // gather: units of block ids prefetched ahead
+#ifndef HSI_GATHER_BULK
+#define HSI_GATHER_BULK 0
+#endif
 
 struct ScoreParams {
     const uint8_t* q_rec;
@@ -52,7 +55,8 @@ struct ScoreParams {
     const float* w;
     const uint8_t* k_rec;
     const float* g_k;
-    const int64_t* k_off;
+    const int64_t* k_off;  // first record of query b's keys; NULL: b * k_stride
+    int64_t k_stride;
     const int32_t* n_vis;
     int32_t B;
     int32_t ngroups;
@@ -61,6 +65,9 @@ struct ScoreParams {
     int64_t ld;
     float* bmax;
     int64_t ldb;
+    // optional (a scan of pooled records laid out contiguously): keys in
+    // [n_vis[b], 8 min(pad_blocks[b], n_keep)) are written as -inf
+    const int32_t* pad_blocks;
     // optional (single-query groups): 4096-bin histogram of the top 12 bits of
     // the order keys of the scores, [B][4096], added to
     uint32_t* key_hist;
@@ -81,13 +88,18 @@ struct ScoreCfg {
     static constexpr int Q_BYTES = NQ * 4 * REC;
     static constexpr int STAGE_BYTES = UNIT_RECS * REC;
     static constexpr int QSLOT_BYTES = ((Q_BYTES + 127) / 128) * 128;
-    static constexpr int PROD_WARPS = GATHER ? 4 : 1;  // gather: a warpgroup of 16-byte async copies
+    // gather: one bulk copy per pooled block from one warp, or a warpgroup of 16-byte async copies
+    static constexpr bool GBULK = GATHER && HSI_GATHER_BULK;
+    static constexpr int PROD_WARPS = GATHER && !GBULK ? 4 : 1;
     static constexpr int MMA_WARP = PROD_WARPS;
     static constexpr int FIRST_SF_WARP = PROD_WARPS + 1;
     static constexpr int FIRST_EPI_WARP = FIRST_SF_WARP + 4;
     static constexpr int EPI_GROUPS = GATHER ? 1 : 2;
     static constexpr int THREADS = 32 * (FIRST_EPI_WARP + 4 * EPI_GROUPS);
-    static constexpr int COPY_AHEAD = 4;  // gather: units of async copies in flight per producer thread
+#ifndef HSI_COPY_AHEAD
+#define HSI_COPY_AHEAD 4
+#endif
+    static constexpr int COPY_AHEAD = HSI_COPY_AHEAD;  // gather: units of async copies in flight per producer thread
     // TMEM columns: accumulators, one SFA set per stage (UT tiles x 2 chunks x 4),
     // one SFB set per q slot (2 chunks x 4)
     static constexpr int COL_ACC = 0;
@@ -117,8 +129,9 @@ struct ScoreCfg {
     static_assert(NQ <= 4, "B scale rows fit one 128-row layout");
     static_assert(COLS_USED <= 512, "TMEM");
     static_assert(NACC % EPI_GROUPS == 0, "accumulator sets split evenly between epilogue groups");
-    static_assert(!GATHER || (NQ == 1 && UNIT_RECS == 32), "gather: 4 producer threads per block");
-    static_assert(!GATHER || COPY_AHEAD < STAGES, "gather: copies in flight fit the ring");
+    static_assert(!GATHER || (NQ == 1 && (GBULK ? UNIT_RECS % 32 == 0 : UNIT_RECS == 32)),
+                  "gather: one lane per block (bulk) or 4 producer threads per block");
+    static_assert(!GATHER || GBULK || COPY_AHEAD < STAGES, "gather: copies in flight fit the ring");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
@@ -193,7 +206,7 @@ __device__ __forceinline__ bool wait_role(uint64_t* bar, uint32_t parity, ScoreS
 // Trace slots: which role waited on what (only with -DHSI_TRACE).
 enum : int {
     TR_PROD_QEMPTY = 0, TR_PROD_EMPTY, TR_PROD_IDS, TR_SF_QFULL, TR_SF_FULL, TR_MMA_QREADY, TR_MMA_SFREADY,
-    TR_MMA_ACCEMPTY, TR_EPI_ACCFULL, TR_MMA_ISSUE, TR_SF_WORK, TR_EPI_WORK, TR_PROD_ISSUE,
+    TR_MMA_ACCEMPTY, TR_EPI_ACCFULL, TR_MMA_ISSUE, TR_SF_WORK, TR_EPI_WORK, TR_PROD_ISSUE, TR_PROD_LAND,
     TR_PROD_TOTAL = 16, TR_SF_TOTAL, TR_MMA_TOTAL, TR_EPI_TOTAL, TR_UNITS
 };
 
@@ -349,7 +362,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
 
     if (warp == 0) {
         for (int s = lane; s < STAGES; s += 32) {
-            mbar_init(&full[s], GATHER ? C::PROD_WARPS : 1);
+            mbar_init(&full[s], GATHER && !C::GBULK ? C::PROD_WARPS : 1);
             mbar_init(&sfready[s], 4);
             mbar_init(&empty[s], 1);
         }
@@ -424,7 +437,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                 cur_g = g;
                 ++gc;
                 const int b0 = g * NQ;
-                k_base = p.k_off[b0];
+                k_base = p.k_off ? p.k_off[b0] : (int64_t)b0 * p.k_stride;
                 int maxv = 0;
 #pragma unroll
                 for (int i = 0; i < NQ; ++i) maxv = max(maxv, p.n_vis[b0 + i]);
@@ -456,6 +469,42 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                     bulk_g2s(dst, p.k_rec + (k_base + (int64_t)t * C::UNIT_RECS) * REC, (uint32_t)(nrec * REC),
                              &full[st.i]);
                 }
+            } else if constexpr (C::GBULK) {
+                // one lane per pooled block: a 576-byte bulk copy of the whole record
+                constexpr int PER = C::UNIT_RECS / 32;
+                const int islot = (int)(u % IDS_AHEAD);
+                int64_t ids_l[PER];
+                bool ok_l[PER];
+                uint32_t nvalid = 0;
+#pragma unroll
+                for (int i = 0; i < PER; ++i) {
+                    const int blk = lane + 32 * i;
+                    const int j = t * C::UNIT_RECS + blk;
+                    ids_l[i] = ids_ring[islot * C::UNIT_RECS + blk];
+                    ok_l[i] = j < nk && ids_l[i] >= 0 && ids_l[i] < nrec_all;
+                    if (j < nk && !ok_l[i]) raise_error(DEVERR_ARG);
+                    nvalid += __popc(__ballot_sync(0xFFFFFFFFu, ok_l[i]));
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&ids_free[islot]);
+                    mbar_arrive_expect_tx(&full[st.i], nvalid * REC);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < PER; ++i)
+                    if (ok_l[i])
+                        bulk_g2s(dst + (lane + 32 * i) * REC, p.k_rec + (k_base + ids_l[i]) * REC, REC, &full[st.i]);
+                if (fetched < count) {
+                    if (u >= 1) {
+                        const int prev = (int)((u - 1) % IDS_AHEAD);
+                        if (!wait_traced(&ids_free[prev], (uint32_t)(((u - 1) / IDS_AHEAD) & 1), sh, tr,
+                                         TR_PROD_IDS))
+                            break;
+                        fence_proxy_async_smem();  // the slot's reads precede the copy that refills it
+                    }
+                    fetch_ids();
+                }
             } else {
                 // 4 threads per pooled block, 9 x 16 bytes each (576 B per block)
                 const int islot = (int)(u % IDS_AHEAD);
@@ -486,7 +535,9 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                 }
                 // the unit COPY_AHEAD back has landed: publish it
                 if (u >= C::COPY_AHEAD) {
+                    HSI_TSTART(t_land);
                     cp_async_wait<C::COPY_AHEAD>();
+                    HSI_TEND(t_land, TR_PROD_LAND);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&full[(st.i + STAGES - C::COPY_AHEAD) % STAGES]);
@@ -497,7 +548,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
             st.next(STAGES);
             it.next(p);
         }
-        if (GATHER) {
+        if (GATHER && !C::GBULK) {
             // publish the units still in flight, then nothing is left pending
             cp_async_wait<0>();
             fence_proxy_async_smem();
@@ -509,7 +560,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
         }
         // drain: every bulk copy issued must have landed before the CTA exits
         if (leader) {
-            if (!GATHER)
+            if (!GATHER || C::GBULK)
                 for (long long v = issued_units > STAGES ? issued_units - STAGES : 0; v < issued_units; ++v)
                     wait_drain(&full[(int)(v % STAGES)], (uint32_t)((v / STAGES) & 1));
             for (int slot = 0; slot < 2; ++slot)
@@ -623,7 +674,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
         int cur_g = -1;
         float wq[32];  // single query: its scaled head weights
         float* wq_s = reinterpret_cast<float*>(smem + C::OFF_WQ) + (warp - C::FIRST_EPI_WARP) * NQ * 32;
-        int nv[NQ];
+        int nv[NQ], npad[NQ];
         int nk = 0;
         Ring st, ac;
         int turn = 0;
@@ -643,6 +694,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                 for (int qi = 0; qi < NQ; ++qi) {
                     const int b = g * NQ + qi;
                     nv[qi] = p.n_vis[b];
+                    npad[qi] = p.pad_blocks ? 8 * min(p.pad_blocks[b], p.n_keep) : 0;
                     const float sc = p.g_q[b] * p.g_k[b] * 0.0078125f;
                     if constexpr (NQ == 1) {
                         const float4* wv = reinterpret_cast<const float4*>(p.w + (int64_t)b * 32);
@@ -705,6 +757,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                     if (!GATHER) {
                         const bool vis = key < nv[qi];
                         if (vis) p.scores[(int64_t)b * p.ld + key] = sc;
+                        else if (key < npad[qi]) p.scores[(int64_t)b * p.ld + key] = __uint_as_float(0xFF800000u);
                         if (fuse_hist && vis) atomicAdd(hist_of(b) + (order_key(sc) >> 20), 1u);
                         if (p.bmax) {
                             float m = vis ? sc : __uint_as_float(0xFF800000u);

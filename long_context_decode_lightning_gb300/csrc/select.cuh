@@ -241,7 +241,27 @@ struct SelSmem {
     uint32_t bcast[8];
     uint32_t keys[SEL_CAP];
     uint32_t idx[SEL_CAP];
+#ifdef HSI_TRACE
+    long long t_last;
+#endif
 };
+
+// Phase timing of the final selection (only with -DHSI_TRACE): thread 0 adds
+// the cycles since the previous mark to trace slot `slot`.
+#ifdef HSI_TRACE
+#define SEL_MARK(s, slot)                                                                  \
+    do {                                                                                   \
+        if (threadIdx.x == 0) {                                                            \
+            const long long now_ = clock64();                                              \
+            atomicAdd(&g_hsi_trace[slot], (unsigned long long)(now_ - (s).t_last));        \
+            (s).t_last = now_;                                                             \
+        }                                                                                  \
+    } while (0)
+#else
+#define SEL_MARK(s, slot) \
+    do {                  \
+    } while (0)
+#endif
 
 // Sources of items for the block select.
 struct SmemSrc {  // keys and indices in shared memory
@@ -277,9 +297,13 @@ struct RowSrc {  // the row in global memory
 // sel = 0 selects on the key, sel = 1 on ~index among items with key == T.
 // Returns the digit; *above = items with a larger digit; *at = items at it;
 // *total = all counted items.
+// rel: a window of 256 consecutive values of the key's top 16 bits instead,
+// digit = (key >> 16) - prefix for keys above `prefix`, 0 for the rest (every
+// key lies at or below prefix + 255; mask and shift are unused).
 template <class Src>
 __device__ uint32_t radix_pass(const Src& src, SelSmem& s, int sel, uint32_t T, uint32_t prefix, uint32_t mask,
-                               int shift, uint32_t need, uint32_t* above, uint32_t* at, uint32_t* total) {
+                               int shift, uint32_t need, uint32_t* above, uint32_t* at, uint32_t* total,
+                               bool rel = false) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     for (int i = tid; i < SEL_WARPS * 256; i += SEL_THREADS) (&s.whist[0][0])[i] = 0;
     __syncthreads();
@@ -291,7 +315,12 @@ __device__ uint32_t radix_pass(const Src& src, SelSmem& s, int sel, uint32_t T, 
             const uint32_t key = src.key(j, ok);
             if (ok && (sel == 0 || key == T)) {
                 const uint32_t v = sel == 0 ? key : ~src.idx(j);
-                if ((v & mask) == prefix) bin = (v >> shift) & 255u;
+                if (rel) {
+                    const uint32_t hv = v >> 16;
+                    bin = hv > prefix ? min(hv - prefix, 255u) : 0u;
+                } else if ((v & mask) == prefix) {
+                    bin = (v >> shift) & 255u;
+                }
             }
         }
         if (bin != 0xFFFFFFFFu) atomicAdd(&s.whist[warp][bin], 1u);
@@ -349,6 +378,48 @@ __device__ uint32_t radix_pass(const Src& src, SelSmem& s, int sel, uint32_t T, 
     return d;
 }
 
+// Slot of this lane's item in a shared-memory list counted by *counter, one
+// atomic per warp (every lane of the warp calls it; `take` says whether the
+// lane has an item).
+__device__ __forceinline__ uint32_t warp_append(bool take, uint32_t* counter) {
+    const uint32_t m = __ballot_sync(0xFFFFFFFFu, take);
+    const int lane = threadIdx.x & 31;
+    if (!m) return 0u;
+    const int leader = __ffs(m) - 1;
+    uint32_t base = 0;
+    if (lane == leader) base = atomicAdd(counter, (uint32_t)__popc(m));
+    base = __shfl_sync(0xFFFFFFFFu, base, leader);
+    return base + (uint32_t)__popc(m & ((1u << lane) - 1u));
+}
+
+// The largest eligible key of src below +inf (0 if none); *any_inf: whether
+// some eligible key is +inf or above (the pool's pinned block).
+template <class Src>
+__device__ uint32_t max_key(const Src& src, SelSmem& s, bool* any_inf) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t mx = 0;
+    bool inf = false;
+    for (int64_t j = threadIdx.x; j < src.n; j += SEL_THREADS) {
+        bool ok;
+        const uint32_t key = src.key(j, ok);
+        if (ok) {
+            if (key >= KEY_POS_INF) inf = true;
+            else mx = max(mx, key);
+        }
+    }
+    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+    if (lane == 0) s.hsum[warp] = mx;
+    *any_inf = __syncthreads_or(inf);
+    if (warp == 0) {
+        const uint32_t v = __reduce_max_sync(0xFFFFFFFFu, lane < SEL_WARPS ? s.hsum[lane] : 0u);
+        if (lane == 0) s.bcast[7] = v;
+    }
+    __syncthreads();
+    const uint32_t r = s.bcast[7];
+    __syncthreads();
+    return r;
+}
+
 // Sort s.win[0 .. count) descending (bitonic over the next power of two).
 __device__ void sort_desc(SelSmem& s, int count) {
     int m = 1;
@@ -372,26 +443,27 @@ __device__ void sort_desc(SelSmem& s, int count) {
     }
 }
 
-// After the first radix pass (digit d0 of the top 8 key bits, `above` items
-// above it): the remaining passes, the tie split at the k-th key and the
-// gather of the winners into s.win as (key << 32 | ~idx) (top-k) or (~idx)
-// (pool: ascending ids after the descending sort), sorted. Items of src whose
-// top byte is below d0 may be absent.
+// Once the k-th largest key is known to have the high bits `prefix` (the bits
+// set in `mask`, those above bit first_shift + 8), with above0 items above it:
+// the remaining radix passes, the tie split at the k-th key and the gather of
+// the winners into s.win as (key << 32 | ~idx) (top-k) or (~idx) (pool:
+// ascending ids after the descending sort), sorted. Items of src whose masked
+// high bits are below prefix may be absent.
 template <class Src>
-__device__ int select_finish(const Src& src, SelSmem& s, int k, bool ids_only, bool take_all, uint32_t d0,
-                             uint32_t above0) {
+__device__ int select_finish(const Src& src, SelSmem& s, int k, bool ids_only, bool take_all, uint32_t prefix,
+                             uint32_t mask, int first_shift, uint32_t above0) {
     uint32_t above, at = 0, total;
     uint32_t T = 0, T2 = 0;
     bool tie_split = false;
     if (!take_all) {
         uint32_t need = (uint32_t)k - above0;
-        uint32_t prefix = d0 << 24, mask = 0xFF000000u;
-        for (int shift = 16; shift >= 0; shift -= 8) {
+        for (int shift = first_shift; shift >= 0; shift -= 8) {
             const uint32_t d = radix_pass(src, s, 0, 0, prefix, mask, shift, need, &above, &at, &total);
             need -= above;
             prefix |= d << shift;
             mask |= 0xFFu << shift;
         }
+        SEL_MARK(s, 27);
         T = prefix;             // the k-th largest key
         tie_split = at > need;  // more items equal T than places left
         if (tie_split) {
@@ -404,86 +476,122 @@ __device__ int select_finish(const Src& src, SelSmem& s, int k, bool ids_only, b
             }
             T2 = p2;  // ~index of the last tied item taken
         }
+        SEL_MARK(s, 28);
     }
     if (threadIdx.x == 0) s.bcast[4] = 0;
     __syncthreads();
-    for (int64_t j = threadIdx.x; j < src.n; j += SEL_THREADS) {
-        bool ok;
-        const uint32_t key = src.key(j, ok);
-        if (!ok) continue;
-        bool take;
-        if (take_all) {
-            take = true;
-        } else if (key != T) {
-            take = key > T;
-        } else {
-            take = !tie_split || (~src.idx(j)) >= T2;
+    for (int64_t j0 = 0; j0 < src.n; j0 += SEL_THREADS) {  // uniform trip count per warp
+        const int64_t j = j0 + threadIdx.x;
+        bool take = false;
+        uint32_t key = 0;
+        if (j < src.n) {
+            bool ok;
+            key = src.key(j, ok);
+            if (ok) {
+                if (take_all) take = true;
+                else if (key != T) take = key > T;
+                else take = !tie_split || (~src.idx(j)) >= T2;
+            }
         }
+        const uint32_t pos = warp_append(take, &s.bcast[4]);
         if (take) {
-            const uint32_t pos = atomicAdd(&s.bcast[4], 1u);
             const uint32_t ni = ~src.idx(j);
             s.win[pos] = ids_only ? (unsigned long long)ni : (((unsigned long long)key << 32) | ni);
         }
     }
     __syncthreads();
+    SEL_MARK(s, 29);
     const int count = (int)s.bcast[4];
     __syncthreads();
     sort_desc(s, count);
+    SEL_MARK(s, 30);
     return count;
 }
 
-// The k best eligible items of src (see select_finish). After the first
-// radix pass the items that can still win (top byte >= the threshold digit)
-// are packed into s.keys / s.idx when they fit, so the later passes run over
-// those only. IN_SMEM: src itself lives in s.keys / s.idx (then it always
-// fits; the items go through registers so none is overwritten before it is
-// read).
+// The k best eligible items of src (see select_finish). The first radix pass
+// looks at a window of 256 consecutive values of the keys' top 16 bits that
+// ends at the largest key: scores cluster, so the window spreads them over
+// many digits where the top byte would put nearly all in one; when the k-th
+// key lies below the window, a pass on the top byte is taken instead. Then
+// the items that can still win are packed into s.keys / s.idx when they fit,
+// so the later passes run over those only. IN_SMEM: src itself lives in
+// s.keys / s.idx (then it always fits; the items go through registers so
+// none is overwritten before it is read).
 template <bool IN_SMEM, class Src>
 __device__ int block_select(const Src& src, SelSmem& s, int k, bool ids_only) {
     uint32_t above, at, total;
-    const uint32_t d0 = radix_pass(src, s, 0, 0, 0, 0, 24, (uint32_t)k, &above, &at, &total);
-    const bool take_all = total <= (uint32_t)k;
-    if (take_all) return select_finish(src, s, k, ids_only, true, d0, above);
+    bool any_inf;
+    const uint32_t top = max_key(src, s, &any_inf) >> 16;
+    const uint32_t base = top > 255u ? top - 255u : 0u;
+    // keys above the window (+inf) land in digit 255 with the window's top value
+    uint32_t d0 = radix_pass(src, s, 0, 0, base, 0, 16, (uint32_t)k, &above, &at, &total, true);
+    SEL_MARK(s, 25);
+    if (total <= (uint32_t)k) return select_finish(src, s, k, ids_only, true, 0, 0, 0, 0);
+    uint32_t prefix, mask;
+    int shift;
+    if ((d0 > 0 || base == 0) && (d0 < 255 || !any_inf)) {  // digit d0 is exactly the value base + d0
+        prefix = (base + d0) << 16;
+        mask = 0xFFFF0000u;
+        shift = 8;
+    } else {
+        d0 = radix_pass(src, s, 0, 0, 0, 0, 24, (uint32_t)k, &above, &at, &total);
+        prefix = d0 << 24;
+        mask = 0xFF000000u;
+        shift = 16;
+    }
     if (threadIdx.x == 0) s.bcast[6] = 0;
     if (IN_SMEM) {
-        constexpr int PER = SEL_CAP / SEL_THREADS;
-        uint32_t kk[PER], ii[PER];
-        bool keep[PER];
+        // in place, a chunk of 4 items per thread at a time: a chunk is read into
+        // registers before any of it is overwritten, and the packed list never
+        // reaches past the chunks already read
+        constexpr int PER = 4, CHUNK = PER * SEL_THREADS;
+        for (int64_t c0 = 0; c0 < src.n; c0 += CHUNK) {
+            uint32_t kk[PER], ii[PER];
+            bool keep[PER];
 #pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int64_t j = threadIdx.x + (int64_t)i * SEL_THREADS;
-            keep[i] = false;
-            if (j < src.n) {
-                bool ok;
-                kk[i] = src.key(j, ok);
-                ii[i] = src.idx(j);
-                keep[i] = ok && (kk[i] >> 24) >= d0;
+            for (int i = 0; i < PER; ++i) {
+                const int64_t j = c0 + threadIdx.x + (int64_t)i * SEL_THREADS;
+                keep[i] = false;
+                if (j < src.n) {
+                    bool ok;
+                    kk[i] = src.key(j, ok);
+                    ii[i] = src.idx(j);
+                    keep[i] = ok && (kk[i] & mask) >= prefix;
+                }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const uint32_t pos = warp_append(keep[i], &s.bcast[6]);
+                if (keep[i]) {
+                    s.keys[pos] = kk[i];
+                    s.idx[pos] = ii[i];
+                }
             }
         }
-        __syncthreads();  // every item is in registers before any is overwritten
-#pragma unroll
-        for (int i = 0; i < PER; ++i)
-            if (keep[i]) {
-                const uint32_t pos = atomicAdd(&s.bcast[6], 1u);
-                s.keys[pos] = kk[i];
-                s.idx[pos] = ii[i];
-            }
     } else {
-        if (above + at > (uint32_t)SEL_CAP) return select_finish(src, s, k, ids_only, false, d0, above);
+        if (above + at > (uint32_t)SEL_CAP) return select_finish(src, s, k, ids_only, false, prefix, mask, shift, above);
         __syncthreads();
-        for (int64_t j = threadIdx.x; j < src.n; j += SEL_THREADS) {
-            bool ok;
-            const uint32_t key = src.key(j, ok);
-            if (ok && (key >> 24) >= d0) {
-                const uint32_t pos = atomicAdd(&s.bcast[6], 1u);
+        for (int64_t j0 = 0; j0 < src.n; j0 += SEL_THREADS) {  // uniform trip count per warp
+            const int64_t j = j0 + threadIdx.x;
+            bool keep = false;
+            uint32_t key = 0;
+            if (j < src.n) {
+                bool ok;
+                key = src.key(j, ok);
+                keep = ok && (key & mask) >= prefix;
+            }
+            const uint32_t pos = warp_append(keep, &s.bcast[6]);
+            if (keep) {
                 s.keys[pos] = key;
                 s.idx[pos] = src.idx(j);
             }
         }
     }
     __syncthreads();
+    SEL_MARK(s, 26);
     SmemSrc packed{s.keys, s.idx, (int64_t)s.bcast[6]};
-    return select_finish(packed, s, k, ids_only, false, d0, above);
+    return select_finish(packed, s, k, ids_only, false, prefix, mask, shift, above);
 }
 
 __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) {
@@ -495,6 +603,9 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) 
     const int64_t n = sel_items(p, b);
     int count;
     const bool ids_only = p.mode == SEL_POOL;
+#ifdef HSI_TRACE
+    if (threadIdx.x == 0) s.t_last = clock64();
+#endif
     if (n <= SEL_CAP) {
         for (int64_t j = threadIdx.x; j < n; j += SEL_THREADS) {
             bool ok;
@@ -513,6 +624,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) 
         src.keys = s.keys;
         src.ids = s.idx;
         src.n = n;
+        SEL_MARK(s, 24);
         count = block_select<true>(src, s, p.k, ids_only);
     } else {
         const uint32_t c = p.cand_cnt[b];
@@ -590,6 +702,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) 
             p.n_pool[b] = (int32_t)s.bcast[5];
         }
     }
+    SEL_MARK(s, 31);
 }
 
 // Block maxima of a score row: bmax[b][j] = max of scores[b][j*bs .. j*bs+bs)

@@ -329,6 +329,30 @@ def test_full_and_reindex_layer_match_separate_calls(lengths):
     assert hsi.device_error() == 0
     assert torch.equal(ri_r, ri_sep) and torch.equal(rv_r, rv_sep)
 
+    # the compacted pool: records bit-exact copies, and the streamed Reindex
+    # layer gives the gathered one's scores and selection
+    pool_rec = torch.full((B, 2048 * 576), 0xA5, dtype=torch.uint8, device=DEV)
+    hsi.pool_gather(caches.k_rec, off, nv, ids_f, nk_f, B, pool_rec)
+    assert hsi.device_error() == 0
+    kr = caches.k_rec.cpu().numpy().reshape(-1, 576)
+    pr = pool_rec.cpu().numpy().reshape(B, 2048, 576)
+    for b in range(B):
+        k = int(nk_f[b])
+        want = kr[caches.rec_off[b] + ids_f[b, :k].cpu().numpy()]
+        assert np.array_equal(pr[b, :k], want)
+        assert np.all(pr[b, k:] == 0xA5)  # slots past n_kept untouched
+    ps_c = torch.full((B, 2048 * 8), float("nan"), device=DEV)
+    ri_c = torch.empty(B, 512, dtype=torch.int32, device=DEV)
+    rv_c = torch.empty(B, 512, device=DEV)
+    hsi.reindex_layer(q1, g1, w1, caches.k_rec, caches.g, off, nv, ids_f, nk_f, np_f, B, ps_c, 512, ri_c, rv_c,
+                      pool_rec=pool_rec)
+    assert hsi.device_error() == 0
+    for b in range(B):
+        k8 = 8 * int(nk_f[b])
+        assert torch.equal(ps_c[b, :k8], ps_sep[b, :k8])
+        assert torch.isnan(ps_c[b, k8:]).all()  # slots past the pool untouched
+    assert torch.equal(ri_c, ri_sep) and torch.equal(rv_c, rv_sep)
+
 
 # ------------------------------------------------------- grouped (prefill) --
 
