@@ -420,38 +420,151 @@ __device__ uint32_t max_key(const Src& src, SelSmem& s, bool* any_inf) {
     return r;
 }
 
-// Sort s.win[0 .. count) descending (bitonic over the next power of two).
+// Sort s.win[0 .. count) descending: a bitonic network over m = the next
+// power of two >= max(count, 8). In each round every one of m/8 threads owns
+// the 8 elements whose indices differ only in three bits and applies up to
+// three consecutive compare-exchange layers of the network to them in
+// registers, so one barrier among those threads covers three layers (18
+// rounds for m = 512 instead of 45 block-wide steps). Padding elements are 0,
+// below every real entry.
 __device__ void sort_desc(SelSmem& s, int count) {
-    int m = 1;
+    int m = 8;
     while (m < count) m <<= 1;
     for (int i = count + threadIdx.x; i < m; i += SEL_THREADS) s.win[i] = 0ull;
     __syncthreads();
-    for (int size = 2; size <= m; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = threadIdx.x; i < m / 2; i += SEL_THREADS) {
-                const int lo = 2 * i - (i & (stride - 1));
-                const int hi = lo + stride;
-                const bool desc = ((lo & size) == 0);
-                const unsigned long long a = s.win[lo], c = s.win[hi];
-                if ((a < c) == desc) {
-                    s.win[lo] = c;
-                    s.win[hi] = a;
+    const int groups = m >> 3;
+    const int nthr = groups < 32 ? 32 : groups;  // whole warps meet at the named barrier
+    const int tid = threadIdx.x;
+    if (tid < nthr) {
+        for (int size = 2; size <= m; size <<= 1) {
+            for (int S = size >> 1; S > 0;) {
+                const int nst = S >= 4 ? 3 : (S == 2 ? 2 : 1);  // layers this round: strides S, S/2, S/4
+                // owned index bits p0 > p1 > p2 (element bits 2, 1, 0)
+                const int p0 = S >= 4 ? 31 - __clz(S) : 2, p1 = p0 - 1, p2 = p0 - 2;
+                if (tid < groups) {
+                    uint32_t t = (uint32_t)tid;  // tid with zero bits inserted at p2, p1, p0
+                    t = ((t >> p2) << (p2 + 1)) | (t & ((1u << p2) - 1u));
+                    t = ((t >> p1) << (p1 + 1)) | (t & ((1u << p1) - 1u));
+                    t = ((t >> p0) << (p0 + 1)) | (t & ((1u << p0) - 1u));
+                    uint32_t idx[8];
+                    unsigned long long r[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        idx[e] = t | ((e & 4) ? 1u << p0 : 0u) | ((e & 2) ? 1u << p1 : 0u) | ((e & 1) ? 1u << p2 : 0u);
+                        r[e] = s.win[idx[e]];
+                    }
+                    auto cx = [&](int lo, int hi) {  // lo/hi: element slots, literal at every call
+                        const bool desc = (idx[lo] & (uint32_t)size) == 0;
+                        if ((r[lo] < r[hi]) == desc) {
+                            const unsigned long long x = r[lo];
+                            r[lo] = r[hi];
+                            r[hi] = x;
+                        }
+                    };
+                    for (int l = 0; l < nst; ++l) {
+                        const int eb = (S >= 4 ? 2 : (S == 2 ? 1 : 0)) - l;  // element bit of stride S >> l
+                        if (eb == 2) {
+                            cx(0, 4), cx(1, 5), cx(2, 6), cx(3, 7);
+                        } else if (eb == 1) {
+                            cx(0, 2), cx(1, 3), cx(4, 6), cx(5, 7);
+                        } else {
+                            cx(0, 1), cx(2, 3), cx(4, 5), cx(6, 7);
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) s.win[idx[e]] = r[e];
                 }
+                asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
+                S >>= nst;
             }
-            __syncthreads();
         }
     }
+    __syncthreads();
 }
+
+// Exclusive prefix over the block of one count per thread; *total: the sum.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t c, SelSmem& s, uint32_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) s.hsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t v = lane < SEL_WARPS ? s.hsum[lane] : 0u;
+        uint32_t wi = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+            if (lane >= o) wi += t;
+        }
+        if (lane < SEL_WARPS) s.hsum[lane] = wi - v;
+        if (lane == 31) s.bcast[7] = wi;
+    }
+    __syncthreads();
+    const uint32_t r = s.hsum[warp] + incl - c;
+    *total = s.bcast[7];
+    __syncthreads();
+    return r;
+}
+
+// Sort s.win[0 .. count) descending for count <= 16 * 32: each warp sorts a run
+// of 32 in registers (shuffles), then every element's place is its place in
+// its run plus, for every other run, the number of that run's elements above
+// it (a binary search). Entries are distinct and nonzero.
+__device__ void sort_desc_runs(SelSmem& s, int count) {
+    unsigned long long* run = reinterpret_cast<unsigned long long*>(s.keys);  // free once the winners are out
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int W = (count + 31) / 32;
+    if (warp < W) {
+        unsigned long long v = tid < count ? s.win[tid] : 0ull;  // 0 pads, below every entry
+#pragma unroll
+        for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+            for (int st = size >> 1; st > 0; st >>= 1) {
+                const unsigned long long w = __shfl_xor_sync(0xFFFFFFFFu, v, st);
+                const bool lo = (lane & st) == 0, desc = size == 32 || (lane & size) == 0;
+                const unsigned long long mx = v > w ? v : w, mn = v > w ? w : v;
+                v = (lo == desc) ? mx : mn;
+            }
+        run[tid] = v;
+    }
+    __syncthreads();
+    if (tid < count) {  // the real entries of a run come first
+        const unsigned long long v = run[tid];
+        uint32_t place = (uint32_t)lane;
+        for (int q = 0; q < W; ++q) {
+            if (q == warp) continue;
+            const unsigned long long* R = run + q * 32;
+            int pos = 0;
+#pragma unroll
+            for (int st = 32; st >= 1; st >>= 1)
+                if (pos + st <= 32 && R[pos + st - 1] > v) pos += st;
+            place += (uint32_t)pos;
+        }
+        s.win[place] = v;
+    }
+    __syncthreads();
+}
+
+constexpr int64_t SEL_BITMAP_IDS = SEL_MAXK * 64;  // ids a bitmap over s.win can hold
 
 // Once the k-th largest key is known to have the high bits `prefix` (the bits
 // set in `mask`, those above bit first_shift + 8), with above0 items above it:
 // the remaining radix passes, the tie split at the k-th key and the gather of
-// the winners into s.win as (key << 32 | ~idx) (top-k) or (~idx) (pool:
-// ascending ids after the descending sort), sorted. Items of src whose masked
-// high bits are below prefix may be absent.
+// the winners into s.win, sorted descending: (key << 32 | ~idx) for top-k
+// (id_range 0), or ~idx for a pool of ids below id_range (ascending ids).
+// A pool whose ids fit SEL_BITMAP_IDS is put in order through a bitmap of the
+// winners instead of a sort. Items of src whose masked high bits are below
+// prefix may be absent.
 template <class Src>
-__device__ int select_finish(const Src& src, SelSmem& s, int k, bool ids_only, bool take_all, uint32_t prefix,
+__device__ int select_finish(const Src& src, SelSmem& s, int k, int64_t id_range, bool take_all, uint32_t prefix,
                              uint32_t mask, int first_shift, uint32_t above0) {
+    const bool ids_only = id_range > 0;
+    const bool bitmap = ids_only && id_range <= SEL_BITMAP_IDS;
     uint32_t above, at = 0, total;
     uint32_t T = 0, T2 = 0;
     bool tie_split = false;
@@ -479,6 +592,10 @@ __device__ int select_finish(const Src& src, SelSmem& s, int k, bool ids_only, b
         SEL_MARK(s, 28);
     }
     if (threadIdx.x == 0) s.bcast[4] = 0;
+    uint32_t* bits = reinterpret_cast<uint32_t*>(s.win);
+    const int words = (int)((id_range + 31) / 32);
+    if (bitmap)
+        for (int i = threadIdx.x; i < words; i += SEL_THREADS) bits[i] = 0u;
     __syncthreads();
     for (int64_t j0 = 0; j0 < src.n; j0 += SEL_THREADS) {  // uniform trip count per warp
         const int64_t j = j0 + threadIdx.x;
@@ -493,6 +610,13 @@ __device__ int select_finish(const Src& src, SelSmem& s, int k, bool ids_only, b
                 else take = !tie_split || (~src.idx(j)) >= T2;
             }
         }
+        if (bitmap) {
+            if (take) {
+                const uint32_t id = src.idx(j);
+                atomicOr(&bits[id >> 5], 1u << (id & 31));
+            }
+            continue;
+        }
         const uint32_t pos = warp_append(take, &s.bcast[4]);
         if (take) {
             const uint32_t ni = ~src.idx(j);
@@ -501,9 +625,35 @@ __device__ int select_finish(const Src& src, SelSmem& s, int k, bool ids_only, b
     }
     __syncthreads();
     SEL_MARK(s, 29);
+    if (bitmap) {
+        // the set bits in id order: each thread takes a run of consecutive words
+        constexpr int WPT = (int)(SEL_BITMAP_IDS / 32 / SEL_THREADS);
+        uint32_t wv[WPT], c = 0;
+#pragma unroll
+        for (int i = 0; i < WPT; ++i) {
+            const int wd = threadIdx.x * WPT + i;
+            wv[i] = wd < words ? bits[wd] : 0u;
+            c += (uint32_t)__popc(wv[i]);
+        }
+        uint32_t count;
+        uint32_t pos = block_excl_scan(c, s, &count);  // its barriers also end the reads of the bitmap
+#pragma unroll
+        for (int i = 0; i < WPT; ++i) {
+            const uint32_t base = (uint32_t)(threadIdx.x * WPT + i) * 32u;
+            while (wv[i]) {
+                const uint32_t id = base + (uint32_t)(__ffs(wv[i]) - 1);
+                wv[i] &= wv[i] - 1u;
+                s.win[pos++] = (unsigned long long)(~id);
+            }
+        }
+        __syncthreads();
+        SEL_MARK(s, 30);
+        return (int)count;
+    }
     const int count = (int)s.bcast[4];
     __syncthreads();
-    sort_desc(s, count);
+    if (count <= 16 * 32) sort_desc_runs(s, count);
+    else sort_desc(s, count);
     SEL_MARK(s, 30);
     return count;
 }
@@ -518,7 +668,7 @@ __device__ int select_finish(const Src& src, SelSmem& s, int k, bool ids_only, b
 // s.keys / s.idx (then it always fits; the items go through registers so
 // none is overwritten before it is read).
 template <bool IN_SMEM, class Src>
-__device__ int block_select(const Src& src, SelSmem& s, int k, bool ids_only) {
+__device__ int block_select(const Src& src, SelSmem& s, int k, int64_t id_range) {
     uint32_t above, at, total;
     bool any_inf;
     const uint32_t top = max_key(src, s, &any_inf) >> 16;
@@ -526,7 +676,7 @@ __device__ int block_select(const Src& src, SelSmem& s, int k, bool ids_only) {
     // keys above the window (+inf) land in digit 255 with the window's top value
     uint32_t d0 = radix_pass(src, s, 0, 0, base, 0, 16, (uint32_t)k, &above, &at, &total, true);
     SEL_MARK(s, 25);
-    if (total <= (uint32_t)k) return select_finish(src, s, k, ids_only, true, 0, 0, 0, 0);
+    if (total <= (uint32_t)k) return select_finish(src, s, k, id_range, true, 0, 0, 0, 0);
     uint32_t prefix, mask;
     int shift;
     if ((d0 > 0 || base == 0) && (d0 < 255 || !any_inf)) {  // digit d0 is exactly the value base + d0
@@ -570,7 +720,7 @@ __device__ int block_select(const Src& src, SelSmem& s, int k, bool ids_only) {
             }
         }
     } else {
-        if (above + at > (uint32_t)SEL_CAP) return select_finish(src, s, k, ids_only, false, prefix, mask, shift, above);
+        if (above + at > (uint32_t)SEL_CAP) return select_finish(src, s, k, id_range, false, prefix, mask, shift, above);
         __syncthreads();
         for (int64_t j0 = 0; j0 < src.n; j0 += SEL_THREADS) {  // uniform trip count per warp
             const int64_t j = j0 + threadIdx.x;
@@ -591,7 +741,7 @@ __device__ int block_select(const Src& src, SelSmem& s, int k, bool ids_only) {
     __syncthreads();
     SEL_MARK(s, 26);
     SmemSrc packed{s.keys, s.idx, (int64_t)s.bcast[6]};
-    return select_finish(packed, s, k, ids_only, false, prefix, mask, shift, above);
+    return select_finish(packed, s, k, id_range, false, prefix, mask, shift, above);
 }
 
 __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) {
@@ -602,7 +752,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) 
     const int b = blockIdx.x;
     const int64_t n = sel_items(p, b);
     int count;
-    const bool ids_only = p.mode == SEL_POOL;
+    const int64_t id_range = p.mode == SEL_POOL ? n : 0;  // pool: block ids below n
 #ifdef HSI_TRACE
     if (threadIdx.x == 0) s.t_last = clock64();
 #endif
@@ -625,7 +775,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) 
         src.ids = s.idx;
         src.n = n;
         SEL_MARK(s, 24);
-        count = block_select<true>(src, s, p.k, ids_only);
+        count = block_select<true>(src, s, p.k, id_range);
     } else {
         const uint32_t c = p.cand_cnt[b];
         const uint32_t* ck = p.cand_key + (int64_t)b * p.cap;
@@ -637,13 +787,13 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) 
             }
             __syncthreads();
             SmemSrc src{s.keys, s.idx, (int64_t)c};
-            count = block_select<true>(src, s, p.k, ids_only);
+            count = block_select<true>(src, s, p.k, id_range);
         } else if (c <= (uint32_t)p.cap) {  // all survivors kept: select over them in L2
             GlobalSrc src{ck, ci, (int64_t)c};
-            count = block_select<false>(src, s, p.k, ids_only);
+            count = block_select<false>(src, s, p.k, id_range);
         } else {  // survivors overflowed (heavy ties): select over the whole row
             RowSrc src{&p, b, n};
-            count = block_select<false>(src, s, p.k, ids_only);
+            count = block_select<false>(src, s, p.k, id_range);
         }
     }
     if (p.mode == SEL_TOPK) {
