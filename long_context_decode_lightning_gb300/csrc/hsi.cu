@@ -141,6 +141,31 @@ hsi_status run_select(SelParams sp, int64_t max_items, cudaStream_t s, bool hist
     return launch(sel_final_kernel, dim3(sp.B), dim3(SEL_THREADS), sizeof(SelSmem), s, sp);
 }
 
+SelParams topk_params(const float* scores, int64_t ld, const int32_t* n_valid, int32_t B, int32_t k,
+                      const int32_t* block_ids, int64_t ld_blocks, int32_t block_size, int32_t* out_idx,
+                      float* out_val, const SelWs& wsp) {
+    SelParams sp{};
+    sp.src = scores;
+    sp.ld = ld;
+    sp.n_src = n_valid;
+    sp.div = 1;
+    sp.B = B;
+    sp.k = k;
+    sp.mode = SEL_TOPK;
+    sp.hist = wsp.hist;
+    sp.cand_cnt = wsp.cnt;
+    sp.cand_key = wsp.ckey;
+    sp.cand_idx = wsp.cidx;
+    sp.thr = wsp.cnt ? wsp.cnt + B : nullptr;
+    sp.cap = kCandCap;
+    sp.block_ids = block_ids;
+    sp.ld_blocks = ld_blocks;
+    sp.block_size = block_size;
+    sp.out_idx = out_idx;
+    sp.out_val = out_val;
+    return sp;
+}
+
 template <int NQ, bool GATHER, int STAGES, int UT>
 hsi_status launch_score(const ScoreParams& p, cudaStream_t s) {
     using C = ScoreCfg<NQ, GATHER, STAGES, UT>;
@@ -269,7 +294,8 @@ size_t hsi_workspace_size(hsi_ws_kind kind, int32_t B, int64_t max_n, int32_t k)
             return sel_ws_bytes(B, max_n > nb ? max_n : nb, false, 0) + align_up((size_t)B * HIST_BINS * 4, 256) +
                    align_up((size_t)B * (size_t)nb * 4, 256);
         }
-        case HSI_WS_REINDEX_LAYER: return sel_ws_bytes(B, max_n, false, 0);
+        case HSI_WS_REINDEX_LAYER:  // + the key histogram the pooled scan accumulates
+            return sel_ws_bytes(B, max_n, false, 0) + align_up((size_t)B * HIST_BINS * 4, 256);
         case HSI_WS_POOL: {
             // k is the block size here; block maxima are computed into the
             // workspace when they are not given
@@ -395,25 +421,7 @@ hsi_status hsi_topk(const float* scores, int64_t ld, const int32_t* n_valid, int
     const size_t need = sel_ws_bytes(B, max_valid, false, 0);
     if (need && (!ws || ws_bytes < need || !aligned(ws, 256))) return HSI_ERR_WORKSPACE;
     SelWs wsp = carve_sel(ws, B, max_valid, false, 0);
-    SelParams sp{};
-    sp.src = scores;
-    sp.ld = ld;
-    sp.n_src = n_valid;
-    sp.div = 1;
-    sp.B = B;
-    sp.k = k;
-    sp.mode = SEL_TOPK;
-    sp.hist = wsp.hist;
-    sp.cand_cnt = wsp.cnt;
-    sp.cand_key = wsp.ckey;
-    sp.cand_idx = wsp.cidx;
-    sp.thr = wsp.cnt ? wsp.cnt + B : nullptr;
-    sp.cap = kCandCap;
-    sp.block_ids = block_ids;
-    sp.ld_blocks = ld_blocks;
-    sp.block_size = block_size;
-    sp.out_idx = out_idx;
-    sp.out_val = out_val;
+    const SelParams sp = topk_params(scores, ld, n_valid, B, k, block_ids, ld_blocks, block_size, out_idx, out_val, wsp);
     return run_select(sp, max_valid, stream);
 }
 
@@ -650,6 +658,9 @@ hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float
     if (!pool_rec) {
         st = hsi_score_pool(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, block_ids, n_kept, n_keep, B,
                             pool_scores, ld, nullptr, 0, stream);
+        if (st != HSI_OK) return st;
+        return hsi_topk(pool_scores, ld, n_pool, B, (int64_t)n_keep * 8, k, block_ids, n_keep, 8, top_idx,
+                        top_val, ws, ws_bytes, stream);
     } else {
         // the compacted pool is a contiguous scan: query b's keys are its pool
         // slots (n_pool[b] of them visible, the newest block last), its records
@@ -658,6 +669,14 @@ hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float
             n_keep > (1 << 20) || !pool_scores || ld < (int64_t)n_keep * 8)
             return HSI_ERR_INVALID_ARG;
         if (!aligned(q_rec, 16) || !aligned(pool_rec, 16) || !aligned(w, 16)) return HSI_ERR_INVALID_ARG;
+        if (!top_idx || !top_val || k < 1 || k > 2048) return HSI_ERR_INVALID_ARG;
+        const int64_t max_valid = (int64_t)n_keep * 8;
+        const size_t need = hsi_workspace_size(HSI_WS_REINDEX_LAYER, B, max_valid, k);
+        if (!ws || ws_bytes < need || !aligned(ws, 256)) return HSI_ERR_WORKSPACE;
+        // the scan accumulates the key histogram that the selection starts from
+        SelWs wsp = carve_sel(ws, B, max_valid, false, 0);
+        uint32_t* hist = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + sel_ws_bytes(B, max_valid, false, 0));
+        if (cudaMemsetAsync(hist, 0, (size_t)B * HIST_BINS * 4, stream) != cudaSuccess) return HSI_ERR_CUDA;
         ScoreParams p{};
         p.q_rec = q_rec;
         p.g_q = g_q;
@@ -673,11 +692,14 @@ hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float
         p.ld = ld;
         p.pad_blocks = n_kept;
         p.n_keep = n_keep;
+        p.key_hist = hist;
         st = launch_score<1, false, kDecodeStages, kDecodeUT>(p, stream);
+        if (st != HSI_OK) return st;
+        SelParams sp = topk_params(pool_scores, ld, n_pool, B, k, block_ids, n_keep, 8, top_idx, top_val, wsp);
+        sp.hist = hist;
+        sp.hist_small = 1;
+        return run_select(sp, max_valid, stream, true);
     }
-    if (st != HSI_OK) return st;
-    return hsi_topk(pool_scores, ld, n_pool, B, (int64_t)n_keep * 8, k, block_ids, n_keep, 8, top_idx, top_val, ws,
-                    ws_bytes, stream);
 }
 
 }  // extern "C"

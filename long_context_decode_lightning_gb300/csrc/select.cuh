@@ -52,6 +52,10 @@ struct SelParams {
     uint32_t* cand_idx;  // [B][cap]
     uint32_t* thr;       // [B] bin (top 12 key bits) holding the k-th key
     int32_t cap;
+    // rows of at most SEL_CAP items whose histogram is already in `hist` (TOPK
+    // mode): the final kernel takes the threshold bin from it and loads only
+    // the items at or above that bin
+    int32_t hist_small;
     // top-k outputs
     const int32_t* block_ids;
     int64_t ld_blocks;
@@ -69,6 +73,18 @@ struct SelParams {
 __device__ __forceinline__ int64_t sel_items(const SelParams& p, int b) {
     const int64_t n = p.n_src[b];
     return n <= 0 ? 0 : (n + p.div - 1) / p.div;
+}
+
+// Key of item i of value v (n = item count); `ok`: whether it is eligible.
+__device__ __forceinline__ uint32_t sel_key_of(const SelParams& p, float v, int64_t i, int64_t n, bool& ok) {
+    uint32_t key = order_key(v);
+    if (p.mode == SEL_POOL) {
+        if (i == n - 1) key = KEY_POS_INF;  // the block of the newest position
+        ok = key != KEY_NEG_INF;
+    } else {
+        ok = true;
+    }
+    return key;
 }
 
 // Key of item i (n = item count); `ok` says whether the item is eligible.
@@ -108,6 +124,42 @@ __device__ __forceinline__ void sel_key4(const SelParams& p, int b, const float*
     }
 }
 
+// The items [lo, hi) of a row that one scan CTA covers, SCAN_ROUNDS groups of
+// 4 consecutive items per thread (group r at lo + 4 (r SCAN_THREADS + thread)),
+// all loads issued before any is used: keys and eligibility bits (bit 4r+i).
+constexpr int SCAN_ROUNDS = SCAN_CHUNK / (4 * SCAN_THREADS);
+__device__ __forceinline__ void load_chunk(const SelParams& p, int b, const float* row, bool vec, int64_t lo,
+                                           int64_t hi, int64_t n, uint32_t (&key)[SCAN_ROUNDS][4], uint32_t& okm) {
+    static_assert(SCAN_ROUNDS * 4 <= 32, "eligibility bits");
+    okm = 0;
+    if (vec && lo + SCAN_CHUNK <= hi) {  // a whole chunk (uniform per CTA): unconditional 16-byte loads
+        float4 f[SCAN_ROUNDS];
+#pragma unroll
+        for (int r = 0; r < SCAN_ROUNDS; ++r)
+            f[r] = *reinterpret_cast<const float4*>(row + lo + 4 * ((int64_t)r * SCAN_THREADS + threadIdx.x));
+#pragma unroll
+        for (int r = 0; r < SCAN_ROUNDS; ++r) {
+            const int64_t base = lo + 4 * ((int64_t)r * SCAN_THREADS + threadIdx.x);
+            const float v[4] = {f[r].x, f[r].y, f[r].z, f[r].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                bool ok;
+                key[r][i] = sel_key_of(p, v[i], base + i, n, ok);
+                okm |= (ok ? 1u : 0u) << (4 * r + i);
+            }
+        }
+        return;
+    }
+#pragma unroll
+    for (int r = 0; r < SCAN_ROUNDS; ++r) {
+        const int64_t base = lo + 4 * ((int64_t)r * SCAN_THREADS + threadIdx.x);
+        bool ok[4] = {false, false, false, false};
+        if (base < hi) sel_key4(p, b, row, vec, base, hi, n, key[r], ok);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) okm |= (ok[i] ? 1u : 0u) << (4 * r + i);
+    }
+}
+
 __global__ void __launch_bounds__(SCAN_THREADS) sel_hist_kernel(SelParams p) {
     griddep_wait();
     griddep_launch_dependents();
@@ -121,15 +173,13 @@ __global__ void __launch_bounds__(SCAN_THREADS) sel_hist_kernel(SelParams p) {
     __syncthreads();
     const float* row = p.src + (int64_t)b * p.ld;
     const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
-    for (int64_t base0 = lo; base0 < hi; base0 += 4 * SCAN_THREADS) {  // uniform trip count per warp
-        const int64_t base = base0 + 4 * threadIdx.x;
-        uint32_t key[4];
-        bool ok[4];
-        sel_key4(p, b, row, vec, base, hi, n, key, ok);
+    uint32_t key[SCAN_ROUNDS][4], okm;
+    load_chunk(p, b, row, vec, lo, hi, n, key, okm);
+#pragma unroll
+    for (int r = 0; r < SCAN_ROUNDS; ++r)
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            if (ok[i]) atomicAdd(&sh[key[i] >> 20], 1u);
-    }
+            if (okm >> (4 * r + i) & 1u) atomicAdd(&sh[key[r][i] >> 20], 1u);
     __syncthreads();
     uint32_t* gh = p.hist + (int64_t)b * HIST_BINS;
     for (int i = threadIdx.x; i < HIST_BINS; i += SCAN_THREADS)
@@ -201,16 +251,18 @@ __global__ void __launch_bounds__(SCAN_THREADS) sel_collect_kernel(SelParams p) 
     uint32_t* ci = p.cand_idx + (int64_t)b * p.cap;
     const float* row = p.src + (int64_t)b * p.ld;
     const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
+    uint32_t keys[SCAN_ROUNDS][4], okm;
+    load_chunk(p, b, row, vec, lo, hi, n, keys, okm);
     // 4 items per thread per round; at most one global reservation per warp per round
-    for (int64_t base0 = lo; base0 < hi; base0 += 4 * SCAN_THREADS) {
-        const int64_t base = base0 + 4 * threadIdx.x;
-        uint32_t key[4];
+#pragma unroll
+    for (int r = 0; r < SCAN_ROUNDS; ++r) {
+        const int64_t base = lo + 4 * ((int64_t)r * SCAN_THREADS + threadIdx.x);
+        uint32_t* key = keys[r];
         bool ok[4];
-        sel_key4(p, b, row, vec, base, hi, n, key, ok);
         uint32_t m[4], tot = 0;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            ok[i] = ok[i] && (key[i] >> 20) >= thr;
+            ok[i] = (okm >> (4 * r + i) & 1u) && (key[i] >> 20) >= thr;
             m[i] = __ballot_sync(0xFFFFFFFFu, ok[i]);
             tot += __popc(m[i]);
         }
@@ -570,11 +622,13 @@ __device__ int select_finish(const Src& src, SelSmem& s, int k, int64_t id_range
     bool tie_split = false;
     if (!take_all) {
         uint32_t need = (uint32_t)k - above0;
-        for (int shift = first_shift; shift >= 0; shift -= 8) {
+        for (int shift = first_shift;; shift -= 8) {
+            if (shift < 0) shift = 0;  // the last digit may overlap bits already fixed
             const uint32_t d = radix_pass(src, s, 0, 0, prefix, mask, shift, need, &above, &at, &total);
             need -= above;
             prefix |= d << shift;
             mask |= 0xFFu << shift;
+            if (shift == 0) break;
         }
         SEL_MARK(s, 27);
         T = prefix;             // the k-th largest key
@@ -709,15 +763,23 @@ __device__ int block_select(const Src& src, SelSmem& s, int k, int64_t id_range)
                     keep[i] = ok && (kk[i] & mask) >= prefix;
                 }
             }
-            __syncthreads();
+            // places by a block scan of the per-thread counts (its barriers also
+            // end the chunk's reads)
+            uint32_t mine = 0;
 #pragma unroll
-            for (int i = 0; i < PER; ++i) {
-                const uint32_t pos = warp_append(keep[i], &s.bcast[6]);
+            for (int i = 0; i < PER; ++i) mine += keep[i] ? 1u : 0u;
+            uint32_t kept;
+            const uint32_t excl = block_excl_scan(mine, s, &kept);
+            uint32_t pos = s.bcast[6] + excl;  // read after the scan's barriers
+#pragma unroll
+            for (int i = 0; i < PER; ++i)
                 if (keep[i]) {
                     s.keys[pos] = kk[i];
                     s.idx[pos] = ii[i];
+                    ++pos;
                 }
-            }
+            __syncthreads();  // everyone has read s.bcast[6]
+            if (threadIdx.x == 0) s.bcast[6] += kept;
         }
     } else {
         if (above + at > (uint32_t)SEL_CAP) return select_finish(src, s, k, id_range, false, prefix, mask, shift, above);
@@ -744,6 +806,82 @@ __device__ int block_select(const Src& src, SelSmem& s, int k, int64_t id_range)
     return select_finish(packed, s, k, id_range, false, prefix, mask, shift, above);
 }
 
+// Top-k of a row of n <= SEL_CAP items (TOPK mode) whose 4096-bin histogram
+// of the keys' top 12 bits is at hist (complete: every item counted). The bin
+// holding the k-th key comes from the histogram; only the items at or above
+// it are loaded, and the radix passes resolve the remaining 20 bits. Returns
+// -1 when the row holds fewer than k items (then every item wins).
+__device__ int select_small_hist(const SelParams& p, int b, int64_t n, const uint32_t* hist, SelSmem& s) {
+    static_assert(HIST_BINS == 4 * SEL_THREADS, "four bins per thread");
+    const int t = threadIdx.x;
+    uint32_t c[4], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        c[i] = hist[4 * t + i];
+        sum += c[i];
+    }
+    uint32_t total;
+    const uint32_t below = block_excl_scan(sum, s, &total);  // items in bins under this thread's
+    const uint32_t k = (uint32_t)p.k;
+    if (total < k) return -1;
+    const uint32_t above_t = total - below - sum;  // items in bins over this thread's
+    if (above_t < k && above_t + sum >= k) {
+        uint32_t run = above_t;
+        for (int i = 3; i >= 0; --i) {
+            if (run + c[i] >= k) {
+                s.bcast[0] = (uint32_t)(4 * t + i);
+                s.bcast[1] = run;
+                break;
+            }
+            run += c[i];
+        }
+    }
+    if (t == 0) s.bcast[6] = 0;
+    __syncthreads();
+    SEL_MARK(s, 24);
+    const uint32_t T = s.bcast[0], above = s.bcast[1];
+    // every load first (independent, in flight together), then the appends
+    constexpr int PER = SEL_CAP / SEL_THREADS;
+    uint32_t key[PER];
+    bool keep[PER];
+    const float* row = p.src + (int64_t)b * p.ld;
+    float v[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {  // clamped index: every load issued unconditionally
+        const int64_t j = (int64_t)i * SEL_THREADS + t;
+        v[i] = row[j < n ? j : n - 1];
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int64_t j = (int64_t)i * SEL_THREADS + t;
+        bool ok;
+        key[i] = sel_key_of(p, v[i], j, n, ok);
+        keep[i] = ok && j < n;
+    }
+    // places by a block scan of the per-thread counts (no shared counter)
+    uint32_t mine = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        keep[i] = keep[i] && (key[i] >> 20) >= T;
+        mine += keep[i] ? 1u : 0u;
+    }
+    uint32_t kept;
+    uint32_t pos = block_excl_scan(mine, s, &kept);
+    SEL_MARK(s, 25);
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+        if (keep[i]) {
+            s.keys[pos] = key[i];
+            s.idx[pos] = (uint32_t)(i * SEL_THREADS + t);
+            ++pos;
+        }
+    if (t == 0) s.bcast[6] = kept;
+    __syncthreads();
+    SEL_MARK(s, 26);
+    SmemSrc packed{s.keys, s.idx, (int64_t)s.bcast[6]};
+    return select_finish(packed, s, p.k, 0, false, T << 20, 0xFFF00000u, 12, above);
+}
+
 __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) {
     griddep_wait();
     griddep_launch_dependents();
@@ -756,12 +894,34 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) 
 #ifdef HSI_TRACE
     if (threadIdx.x == 0) s.t_last = clock64();
 #endif
-    if (n <= SEL_CAP) {
-        for (int64_t j = threadIdx.x; j < n; j += SEL_THREADS) {
+    count = -1;
+    if (n <= SEL_CAP && p.hist_small) count = select_small_hist(p, b, n, p.hist + (int64_t)b * HIST_BINS, s);
+    if (count >= 0) {
+        // selected from the histogram
+    } else if (n <= SEL_CAP) {
+        constexpr int PER = SEL_CAP / SEL_THREADS;
+        const float* row = p.src + (int64_t)b * p.ld;
+        float v[PER];
+        uint32_t key[PER];
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {  // clamped index: every load issued unconditionally
+            const int64_t j = (int64_t)i * SEL_THREADS + threadIdx.x;
+            v[i] = n > 0 ? row[j < n ? j : n - 1] : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int64_t j = (int64_t)i * SEL_THREADS + threadIdx.x;
             bool ok;
-            const uint32_t key = sel_key(p, b, j, n, ok);
-            s.keys[j] = ok ? key : 0u;  // key 0 is never a real key (it is a NaN pattern)
-            s.idx[j] = (uint32_t)j;
+            key[i] = sel_key_of(p, v[i], j, n, ok);
+            if (!ok || j >= n) key[i] = 0u;  // key 0 is never a real key (it is a NaN pattern)
+        }
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int64_t j = (int64_t)i * SEL_THREADS + threadIdx.x;
+            if (j < n) {
+                s.keys[j] = key[i];
+                s.idx[j] = (uint32_t)j;
+            }
         }
         __syncthreads();
         struct Filt : SmemSrc {
