@@ -253,35 +253,37 @@ __global__ void __launch_bounds__(SCAN_THREADS) sel_collect_kernel(SelParams p) 
     const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
     uint32_t keys[SCAN_ROUNDS][4], okm;
     load_chunk(p, b, row, vec, lo, hi, n, keys, okm);
-    // 4 items per thread per round; at most one global reservation per warp per round
+    // survivors of this thread (bit 4r+i), then one global reservation per warp
+    // for the whole chunk: its latency is paid once, not once per round
+    uint32_t sm = 0;
 #pragma unroll
-    for (int r = 0; r < SCAN_ROUNDS; ++r) {
-        const int64_t base = lo + 4 * ((int64_t)r * SCAN_THREADS + threadIdx.x);
-        uint32_t* key = keys[r];
-        bool ok[4];
-        uint32_t m[4], tot = 0;
+    for (int r = 0; r < SCAN_ROUNDS; ++r)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            ok[i] = (okm >> (4 * r + i) & 1u) && (key[i] >> 20) >= thr;
-            m[i] = __ballot_sync(0xFFFFFFFFu, ok[i]);
-            tot += __popc(m[i]);
-        }
-        if (tot == 0) continue;
-        uint32_t pos = 0;
-        if (lane == 0) pos = atomicAdd(cnt, tot);
-        pos = __shfl_sync(0xFFFFFFFFu, pos, 0);
+        for (int i = 0; i < 4; ++i)
+            if ((okm >> (4 * r + i) & 1u) && (keys[r][i] >> 20) >= thr) sm |= 1u << (4 * r + i);
+    const uint32_t c = (uint32_t)__popc(sm);
+    uint32_t incl = c;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (ok[i]) {
-                const uint32_t at = pos + __popc(m[i] & ((1u << lane) - 1u));
-                if (at < (uint32_t)p.cap) {
-                    ck[at] = key[i];
-                    ci[at] = (uint32_t)(base + i);
-                }
-            }
-            pos += __popc(m[i]);
-        }
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
     }
+    const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    if (tot == 0) return;
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(cnt, tot);
+    uint32_t at = __shfl_sync(0xFFFFFFFFu, base, 0) + incl - c;
+#pragma unroll
+    for (int r = 0; r < SCAN_ROUNDS; ++r)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (sm >> (4 * r + i) & 1u) {
+                if (at < (uint32_t)p.cap) {
+                    ck[at] = keys[r][i];
+                    ci[at] = (uint32_t)(lo + 4 * ((int64_t)r * SCAN_THREADS + threadIdx.x) + i);
+                }
+                ++at;
+            }
 }
 
 // -------------------------------------------------------- block select --
