@@ -260,16 +260,15 @@ class DeviceWorkload:
                     n_keep=wl.n_keep, ws=self.ws_full, phases=ph)))
         if wl.build_pool:
             def rest():
-                # the pooled K records, compacted once for the step's Reindex layers
-                hsi.pool_gather(self.k_rec[0], self.k_off, self.n_vis, self.ids, self.nk, B, self.pool_rec,
-                                n_keep=wl.n_keep)
+                # the first Reindex layer gathers the pooled K records and leaves them
+                # compacted; the later layers of the step stream the compacted pool
                 for r in range(wl.reindex_layers):
                     l = wl.full_layers + r
                     hsi.quantize_nvfp4(self.q[l], B, 32, signs, self.g_q[l], self.q_rec[l], ws=self.ws_q)
                     hsi.reindex_layer(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0], self.k_off,
                                       self.n_vis, self.ids, self.nk, self.npool, B, self.pool_scores, K_TOP,
                                       self.idx[l], self.val[l], n_keep=wl.n_keep, ws=self.ws_rtopk,
-                                      pool_rec=self.pool_rec)
+                                      pool_rec=self.pool_rec, pool_rec_ready=r > 0)
             segs.append(("post", rest))
         merged = []
         for kind, fn in segs:  # fuse neighbouring non-scoring segments into one graph
@@ -311,9 +310,13 @@ class DeviceWorkload:
         gather = t(lambda: hsi.score_pool(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0],
                                           self.k_off, self.n_vis, self.ids, self.nk, wl.n_keep, B,
                                           self.pool_scores))
+        first = t(lambda: hsi.reindex_layer(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0],
+                                            self.k_off, self.n_vis, self.ids, self.nk, self.npool, B,
+                                            self.pool_scores, K_TOP, self.idx[l], self.val[l], n_keep=wl.n_keep,
+                                            ws=self.ws_rtopk, pool_rec=self.pool_rec, pool_rec_ready=False))
         pooled_bytes = int(self.nk.clamp(max=wl.n_keep).sum().item()) * REC
-        return {"layer_us": layer, "plain_topk_us": topk, "compact_us": compact, "gather_score_us": gather,
-                "pooled_bytes_per_layer": pooled_bytes}
+        return {"layer_us": layer, "first_layer_us": first, "plain_topk_us": topk, "compact_us": compact,
+                "gather_score_us": gather, "pooled_bytes_per_layer": pooled_bytes}
 
     def capture(self):
         torch = self.torch

@@ -298,19 +298,24 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
  * Page: "DeepSeek-V4.1 模型结构（3）", section "用浅层的打分结果限制深层的打分范围"
  * (Reindex layers score only pooled positions and keep their own top-512).
  *
- *  pool_rec NULL: the pooled records are gathered from k_rec (hsi_score_pool).
- *          Otherwise (dev) the records hsi_pool_gather wrote for this pool,
- *          streamed in place of the gather; k_rec is then not read. Both give
- *          the same pool_scores, top_idx and top_val.
+ *  pool_rec, pool_rec_ready: pool_rec NULL: the pooled records are gathered
+ *          from k_rec (as by hsi_score_pool). pool_rec (dev, [B][n_keep][576],
+ *          16-byte aligned) with pool_rec_ready 0: gathered from k_rec, and
+ *          also left in pool_rec in the layout hsi_pool_gather writes, so that
+ *          the step's later Reindex layers can stream them. pool_rec_ready 1:
+ *          pool_rec already holds them (an earlier layer of this pool, or
+ *          hsi_pool_gather); they are streamed and k_rec is not read. All
+ *          forms give the same pool_scores, top_idx and top_val.
  *  n_pool (dev) int32 [B] as written by hsi_candidate_pool / hsi_full_layer.
  *  pool_scores [B][ld], ld >= 8 * n_keep, is written (as by hsi_score_pool).
  *  ws      (dev) hsi_workspace_size(HSI_WS_REINDEX_LAYER, B, 8 * n_keep, k).
  */
 hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
-                             const float* g_k, const int64_t* k_rec_off, const uint8_t* pool_rec,
-                             const int32_t* n_visible, const int32_t* block_ids, const int32_t* n_kept, const int32_t* n_pool, int32_t n_keep,
-                             int32_t B, float* pool_scores, int64_t ld, int32_t k, int32_t* top_idx, float* top_val,
-                             void* ws, size_t ws_bytes, cudaStream_t stream);
+                             const float* g_k, const int64_t* k_rec_off, uint8_t* pool_rec, int32_t pool_rec_ready,
+                             const int32_t* n_visible, const int32_t* block_ids, const int32_t* n_kept,
+                             const int32_t* n_pool, int32_t n_keep, int32_t B, float* pool_scores, int64_t ld,
+                             int32_t k, int32_t* top_idx, float* top_val, void* ws, size_t ws_bytes,
+                             cudaStream_t stream);
 
 typedef enum {
     HSI_WS_QUANTIZE = 0,

@@ -69,8 +69,8 @@ def lib() -> ctypes.CDLL:
         L.hsi_score_pool.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i64, vp, sz, vp]
         L.hsi_full_layer.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, vp, i64, i32, vp, vp, i32, vp, vp, vp,
                                      vp, i64, i32, vp, sz, vp]
-        L.hsi_reindex_layer.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i64, i32, vp, vp,
-                                        vp, sz, vp]
+        L.hsi_reindex_layer.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, vp, i64, i32, vp,
+                                        vp, vp, sz, vp]
         L.hsi_pool_gather.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp, vp]
         L.hsi_topk_noalloc.argtypes = [vp, i64, vp, i32, i64, i32, vp, i64, i32, vp, vp, vp]
         L.hsi_debug_set.argtypes = [ctypes.c_int, ctypes.c_longlong]
@@ -251,14 +251,17 @@ def pool_gather(k_rec, k_rec_off, n_visible, block_ids, n_kept, B, pool_rec, n_k
 
 
 def reindex_layer(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, block_ids, n_kept, n_pool, B, pool_scores, k,
-                  top_idx, top_val, n_keep=2048, ld=None, ws=None, pool_rec=None, stream=None):
+                  top_idx, top_val, n_keep=2048, ld=None, ws=None, pool_rec=None, pool_rec_ready=True, stream=None):
     """Reindex layer: pooled scores and the top-k inside the pool (global positions).
-    pool_rec: the records pool_gather wrote for this pool (streamed), or None (gathered from k_rec)."""
+    pool_rec None: gathered from k_rec. pool_rec with pool_rec_ready: the compacted pool
+    (pool_gather, or an earlier layer) is streamed; without: gathered from k_rec and the
+    compacted pool left in pool_rec."""
     ld = pool_scores.shape[-1] if ld is None else ld
     if ws is None:
         ws = workspace(WS_REINDEX_LAYER, B, 8 * n_keep, k, device=pool_scores.device)
     _check("hsi_reindex_layer", lib().hsi_reindex_layer(
-        _ptr(q_rec), _ptr(g_q), _ptr(w), _ptr(k_rec), _ptr(g_k), _ptr(k_rec_off), _ptr(pool_rec), _ptr(n_visible),
+        _ptr(q_rec), _ptr(g_q), _ptr(w), _ptr(k_rec), _ptr(g_k), _ptr(k_rec_off), _ptr(pool_rec),
+        1 if pool_rec_ready else 0, _ptr(n_visible),
         _ptr(block_ids),
         _ptr(n_kept), _ptr(n_pool), n_keep, B, _ptr(pool_scores), ld, k, _ptr(top_idx), _ptr(top_val), _ptr(ws),
         0 if ws is None else ws.numel(), _stream(stream)))

@@ -325,7 +325,7 @@ hsi_status hsi_quantize_nvfp4(const uint16_t* x, int64_t n_tensors, int64_t rows
     p.rec = rec;
     if (mode == 0 && (!ws || ws_bytes < (size_t)n_tensors * 4 || !aligned(ws, 256))) return HSI_ERR_WORKSPACE;
     if (rows_per_tensor <= QUANT_SMALL_ROWS && n_tensors <= INT32_MAX) {
-        return launch(quant_small_kernel, dim3((unsigned)n_tensors), dim3(256), 0, stream, p, mode);
+        return launch(quant_small_kernel, dim3((unsigned)n_tensors), dim3(32 * QUANT_SMALL_WARPS), 0, stream, p, mode);
     }
     if (mode == 0) {
         p.amax_bits = static_cast<uint32_t*>(ws);
@@ -648,19 +648,51 @@ hsi_status hsi_pool_gather(const uint8_t* k_rec, const int64_t* k_rec_off, const
 }
 
 hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
-                             const float* g_k, const int64_t* k_rec_off, const uint8_t* pool_rec,
+                             const float* g_k, const int64_t* k_rec_off, uint8_t* pool_rec, int32_t pool_rec_ready,
                              const int32_t* n_visible, const int32_t* block_ids, const int32_t* n_kept,
                              const int32_t* n_pool, int32_t n_keep, int32_t B, float* pool_scores, int64_t ld,
                              int32_t k, int32_t* top_idx, float* top_val, void* ws, size_t ws_bytes,
                              cudaStream_t stream) {
     if (!n_pool) return HSI_ERR_INVALID_ARG;
     hsi_status st;
-    if (!pool_rec) {
-        st = hsi_score_pool(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, block_ids, n_kept, n_keep, B,
-                            pool_scores, ld, nullptr, 0, stream);
+    if (!pool_rec || !pool_rec_ready) {
+        // gather from k_rec (and, with pool_rec, leave the compacted pool there)
+        st = check_score_common(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B);
         if (st != HSI_OK) return st;
-        return hsi_topk(pool_scores, ld, n_pool, B, (int64_t)n_keep * 8, k, block_ids, n_keep, 8, top_idx,
-                        top_val, ws, ws_bytes, stream);
+        if (!block_ids || !n_kept || !pool_scores || n_keep <= 0 || n_keep > (1 << 20) ||
+            n_keep % (16 * kGatherUT) || ld < (int64_t)n_keep * 8 || !aligned(block_ids, 16))
+            return HSI_ERR_INVALID_ARG;
+        if (pool_rec && (!aligned(pool_rec, 16) || pool_rec == k_rec)) return HSI_ERR_INVALID_ARG;
+        if (!top_idx || !top_val || k < 1 || k > 2048) return HSI_ERR_INVALID_ARG;
+        const int64_t max_valid = (int64_t)n_keep * 8;
+        const size_t need = hsi_workspace_size(HSI_WS_REINDEX_LAYER, B, max_valid, k);
+        if (!ws || ws_bytes < need || !aligned(ws, 256)) return HSI_ERR_WORKSPACE;
+        SelWs wsp = carve_sel(ws, B, max_valid, false, 0);
+        uint32_t* hist = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + sel_ws_bytes(B, max_valid, false, 0));
+        if (cudaMemsetAsync(hist, 0, (size_t)B * HIST_BINS * 4, stream) != cudaSuccess) return HSI_ERR_CUDA;
+        ScoreParams p{};
+        p.q_rec = q_rec;
+        p.g_q = g_q;
+        p.w = w;
+        p.k_rec = k_rec;
+        p.g_k = g_k;
+        p.k_off = k_rec_off;
+        p.n_vis = n_visible;
+        p.B = B;
+        p.ngroups = B;
+        p.block_ids = block_ids;
+        p.n_kept = n_kept;
+        p.n_keep = n_keep;
+        p.pool_scores = pool_scores;
+        p.ld_pool = ld;
+        p.key_hist = hist;
+        p.pool_out = pool_rec;
+        st = launch_score<1, true, kGatherStages, kGatherUT>(p, stream);
+        if (st != HSI_OK) return st;
+        SelParams sp = topk_params(pool_scores, ld, n_pool, B, k, block_ids, n_keep, 8, top_idx, top_val, wsp);
+        sp.hist = hist;
+        sp.hist_small = 1;
+        return run_select(sp, max_valid, stream, true);
     } else {
         // the compacted pool is a contiguous scan: query b's keys are its pool
         // slots (n_pool[b] of them visible, the newest block last), its records

@@ -161,18 +161,20 @@ __global__ void __launch_bounds__(256) quant_encode_kernel(QuantParams p) {
 // and encodes, in a single launch.
 constexpr int QUANT_SMALL_ROWS = 64;
 
-__global__ void __launch_bounds__(256) quant_small_kernel(QuantParams p, int mode) {
+constexpr int QUANT_SMALL_WARPS = 32;  // one row per warp for a query's 32 heads
+
+__global__ void __launch_bounds__(32 * QUANT_SMALL_WARPS) quant_small_kernel(QuantParams p, int mode) {
     griddep_wait();
     griddep_launch_dependents();
-    __shared__ float wmax[8];
+    __shared__ float wmax[QUANT_SMALL_WARPS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t = blockIdx.x;
-    constexpr int RPW = QUANT_SMALL_ROWS / 8;  // rows per warp
+    constexpr int RPW = QUANT_SMALL_ROWS / QUANT_SMALL_WARPS;  // rows per warp
     float v[RPW][4];
     float m = 0.f;
 #pragma unroll
     for (int i = 0; i < RPW; ++i) {
-        const int64_t r = warp + 8 * i;
+        const int64_t r = warp + QUANT_SMALL_WARPS * i;
         v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.f;
         if (r < p.rpt) {
             rotate_row_warp(p, t * p.rpt + r, v[i]);
@@ -185,9 +187,9 @@ __global__ void __launch_bounds__(256) quant_small_kernel(QuantParams p, int mod
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
         if (lane == 0) wmax[warp] = m;
         __syncthreads();
-        float amax = wmax[0];
+        float amax = wmax[lane];
 #pragma unroll
-        for (int i = 1; i < 8; ++i) amax = fmaxf(amax, wmax[i]);
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
         g = amax > 0.0f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
         if (threadIdx.x == 0) p.g[t] = g;
     } else {
@@ -195,7 +197,7 @@ __global__ void __launch_bounds__(256) quant_small_kernel(QuantParams p, int mod
     }
 #pragma unroll
     for (int i = 0; i < RPW; ++i) {
-        const int64_t r = warp + 8 * i;
+        const int64_t r = warp + QUANT_SMALL_WARPS * i;
         if (r < p.rec_per_tensor * 8) encode_row_warp(p, t, r, v[i], g);
     }
 }

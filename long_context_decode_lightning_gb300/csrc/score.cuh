@@ -77,6 +77,10 @@ struct ScoreParams {
     int32_t n_keep;  // multiple of 16 UT
     float* pool_scores;
     int64_t ld_pool;
+    // optional: the gathered records of each unit are also written here, query
+    // b's pool slots at pool_out[(b n_keep + slot / 8) 576 ..] (the layout of a
+    // compacted pool), records past n_kept[b] not written
+    uint8_t* pool_out;
 };
 
 template <int NQ, bool GATHER, int STAGES, int UT>
@@ -113,7 +117,7 @@ struct ScoreCfg {
     static constexpr int OFF_IDS = OFF_QSLOTS + 2 * QSLOT_BYTES;
     static constexpr int IDS_BYTES = GATHER ? IDS_AHEAD * UNIT_RECS * 4 : 0;
     // histogram slots for the first HIST_SLOTS queries of the CTA's range
-    static constexpr int HIST_SLOTS = (!GATHER && NQ == 1) ? 2 : 0;
+    static constexpr int HIST_SLOTS = NQ == 1 ? 2 : 0;
     static constexpr int OFF_HIST = OFF_IDS + IDS_BYTES;
     static constexpr int HIST_BYTES = HIST_SLOTS * 4096 * 4;
     // multi-query tiles: the scaled head weights of each epilogue warp's queries
@@ -643,6 +647,19 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
             if (!wait_traced(&full[st.i], st.ph, sh, tr, TR_SF_FULL)) break;
             const uint8_t* st_recs = stages + st.i * C::STAGE_BYTES;
             HSI_TSTART(t_sf);
+            if (GATHER && p.pool_out && warp == C::FIRST_SF_WARP && lane == 0) {
+                // the landed unit also goes to the compacted pool; its shared source
+                // is read before this warp releases the stage's scales (so before
+                // the stage can be refilled)
+                const int nk = min(p.n_kept[it.g], p.n_keep);
+                const int nrec = min(C::UNIT_RECS, nk - it.t * C::UNIT_RECS);
+                if (nrec > 0) {
+                    bulk_s2g(p.pool_out + ((int64_t)it.g * p.n_keep + (int64_t)it.t * C::UNIT_RECS) * REC, st_recs,
+                             (uint32_t)(nrec * REC));
+                    bulk_commit();
+                    bulk_wait_read_all();
+                }
+            }
 #pragma unroll
             for (int sub = 0; sub < UT; ++sub) {
                 uint32_t v[8];
@@ -656,6 +673,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
             st.next(STAGES);
             it.next(p);
         }
+        if (GATHER && p.pool_out && warp == C::FIRST_SF_WARP && lane == 0) bulk_wait_all();
     } else {
         // ------------------------------------------------------------ epilogue
         const int grp = (warp - C::FIRST_EPI_WARP) >> 2;
@@ -767,8 +785,14 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                             if ((lane & 7) == 0 && vis) p.bmax[(int64_t)b * p.ldb + key / 8] = m;
                         }
                     } else if (pos[sub] >= 0) {
-                        const float v = pos[sub] < nv[qi] ? sc : __uint_as_float(0xFF800000u);
-                        p.pool_scores[(int64_t)b * p.ld_pool + key] = v;
+                        const bool vis = pos[sub] < nv[qi];
+                        p.pool_scores[(int64_t)b * p.ld_pool + key] = vis ? sc : __uint_as_float(0xFF800000u);
+                        if (fuse_hist && vis) {  // the pool slot's key, for the selection inside the pool
+                            const uint32_t bin = order_key(sc) >> 20;
+                            const int slot = b - b_first;
+                            if (slot >= 0 && slot < C::HIST_SLOTS) atomicAdd(hist_s + slot * 4096 + bin, 1u);
+                            else atomicAdd(p.key_hist + (int64_t)b * 4096 + bin, 1u);
+                        }
                     }
                 }
             }

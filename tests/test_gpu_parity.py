@@ -353,6 +353,23 @@ def test_full_and_reindex_layer_match_separate_calls(lengths):
         assert torch.isnan(ps_c[b, k8:]).all()  # slots past the pool untouched
     assert torch.equal(ri_c, ri_sep) and torch.equal(rv_c, rv_sep)
 
+    # a gathering layer that leaves the compacted pool behind: the same records
+    # as the compaction call, and the same scores and selection
+    pool_rec2 = torch.full((B, 2048 * 576), 0x5A, dtype=torch.uint8, device=DEV)
+    ps_g = torch.full((B, 2048 * 8), float("nan"), device=DEV)
+    ri_g = torch.empty(B, 512, dtype=torch.int32, device=DEV)
+    rv_g = torch.empty(B, 512, device=DEV)
+    hsi.reindex_layer(q1, g1, w1, caches.k_rec, caches.g, off, nv, ids_f, nk_f, np_f, B, ps_g, 512, ri_g, rv_g,
+                      pool_rec=pool_rec2, pool_rec_ready=False)
+    assert hsi.device_error() == 0
+    pr2 = pool_rec2.cpu().numpy().reshape(B, 2048, 576)
+    for b in range(B):
+        k = int(nk_f[b])
+        assert np.array_equal(pr2[b, :k], pr[b, :k])
+        assert np.all(pr2[b, k:] == 0x5A)
+        assert torch.equal(ps_g[b, :8 * k], ps_sep[b, :8 * k])
+    assert torch.equal(ri_g, ri_sep) and torch.equal(rv_g, rv_sep)
+
 
 # ------------------------------------------------------- grouped (prefill) --
 
