@@ -138,6 +138,28 @@ def test_topk_bit_exact(n, k):
         assert np.array_equal(gv[b][ri >= 0], rv[ri >= 0])
 
 
+def test_topk_outliers_and_infinities():
+    """Rows whose k-th key lies far below the largest ones (the selection's
+    first window, which ends at the largest finite key, misses it), rows whose
+    k best are all tied at the top, and rows holding +inf / -inf."""
+    rng = np.random.default_rng(11)
+    n = 40000
+    sc = rng.standard_normal((5, n)).astype(np.float32)
+    sc[0, rng.choice(n, 7, replace=False)] = np.float32(1e30)  # outliers, k-th key below the window
+    sc[1, rng.choice(n, 300, replace=False)] = np.float32(3e5)
+    sc[2, :600] = sc[2].max()  # the k best tied at the top
+    sc[3, rng.choice(n, 20, replace=False)] = np.inf
+    sc[3, rng.choice(n, 20, replace=False)] = -np.inf
+    sc[4, rng.choice(n, 600, replace=False)] = np.inf  # more +inf than k
+    for rows in (sc, sc[:, :9000]):  # long rows (histogram path) and rows that fit shared memory
+        m = rows.shape[1]
+        gi, gv = _gpu_topk(np.ascontiguousarray(rows), [m] * 5, 512)
+        for b in range(5):
+            ri, rv = oracle.topk(rows[b], m, 512)
+            assert np.array_equal(gi[b], ri), f"row {b}, n {m}"
+            assert np.array_equal(gv[b], rv)
+
+
 def test_topk_ragged_rows_and_all_equal():
     # all-equal rows exercise every survivor path: shared memory, survivors in
     # L2 (40000 > 16384), survivor overflow with a re-read of the row (100000)
@@ -202,6 +224,19 @@ def test_pool_bit_exact(n_vis, use_bmax):
         assert gk[b] == rk and gp[b] == rp
         assert np.array_equal(gi[b][:rk], ri[:rk]) and (gi[b][rk:] == -1).all()
         assert np.array_equal(_bits_to_mask(gb[b], n), rm)
+
+
+def test_pool_past_the_bitmap_range():
+    """More blocks than the in-order bitmap of the final selection covers
+    (262144): the kept ids are put in order by a sort instead."""
+    n = 2_100_000
+    rng = np.random.default_rng(21)
+    sc = rng.standard_normal((1, n)).astype(np.float32)
+    gi, gk, gp, gb = _gpu_pool(sc, [n])
+    ri, rk, rp, rm = oracle.pool(sc[0], n)
+    assert gk[0] == rk and gp[0] == rp
+    assert np.array_equal(gi[0][:rk], ri[:rk])
+    assert np.array_equal(_bits_to_mask(gb[0], n), rm)
 
 
 @pytest.mark.parametrize("bs,keep", [(4, 6), (1, 5), (3, 100), (8, 1)])
