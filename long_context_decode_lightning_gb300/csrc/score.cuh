@@ -88,7 +88,9 @@ struct ScoreCfg {
     static constexpr int N = 32 * NQ;
     static constexpr int UNIT_RECS = 16 * UT;
     static constexpr int UNIT_KEYS = TILE_KEYS * UT;
-    static constexpr int NACC = (NQ == 1 && UT <= 2) ? 4 : 2;  // accumulator sets (one set = UT tiles)
+    // accumulator sets (one set = UT tiles); multi-query tiles: three epilogue
+    // groups, one set each, since their fp32 work per key is NQ times larger
+    static constexpr int NACC = (NQ == 1 && UT <= 2) ? 4 : NQ > 1 ? 3 : 2;
     static constexpr int Q_BYTES = NQ * 4 * REC;
     static constexpr int STAGE_BYTES = UNIT_RECS * REC;
     static constexpr int QSLOT_BYTES = ((Q_BYTES + 127) / 128) * 128;
@@ -98,7 +100,7 @@ struct ScoreCfg {
     static constexpr int MMA_WARP = PROD_WARPS;
     static constexpr int FIRST_SF_WARP = PROD_WARPS + 1;
     static constexpr int FIRST_EPI_WARP = FIRST_SF_WARP + 4;
-    static constexpr int EPI_GROUPS = GATHER ? 1 : 2;
+    static constexpr int EPI_GROUPS = GATHER ? 1 : NQ > 1 ? 3 : 2;
     static constexpr int THREADS = 32 * (FIRST_EPI_WARP + 4 * EPI_GROUPS);
 #ifndef HSI_COPY_AHEAD
 #define HSI_COPY_AHEAD 4
