@@ -11,22 +11,26 @@
 // score per key, so per-head logits never leave the SM.
 //
 // Warp roles in a persistent CTA (one per SM):
-//   warp 0       producer: bulk copies (TMA engine) of K records into a ring of
-//                shared-memory stages, one stage per unit, and of the group's q
-//                records into one of two q slots. Full scan: one copy of up to
-//                16 UT consecutive records (18 KB for UT = 2: below that size
-//                the per-copy rate, not HBM, limits a bulk-copy stream). Pool
-//                gather: one 576-byte copy per pooled block (a whole 8-key
-//                block, codes and scales); the block ids themselves are
-//                prefetched IDS_AHEAD units ahead, also by bulk copy.
-//   warp 1       MMA issuer; owns the TMEM allocation.
-//   warps 2..5   scale warpgroup: writes each unit's (and each q group's) E4M3
+//   producer     full scan (warp 0): one bulk copy (TMA engine) per unit of its
+//                16 UT consecutive records (36 KB for UT = 4; below ~18 KB the
+//                per-copy rate, not HBM, limits a bulk-copy stream) into a
+//                ring of shared-memory stages, and of the group's q records
+//                into one of two q slots. Pool gather (warps 0..3): 16-byte
+//                cp.async copies, four threads per pooled 576-byte record (one
+//                bulk copy per record is slower: the engine takes ~77 cycles
+//                per copy); the block ids come IDS_AHEAD units ahead by bulk
+//                copy.
+//   MMA warp     one thread issues every MMA and commit; the warp owns TMEM.
+//   scale warps  a warpgroup that writes each unit's (and each q group's) E4M3
 //                scales from the records in shared memory straight into TMEM
 //                (tcgen05.st, one 32-lane quarter per warp) in the layout the
 //                block-scaled MMA reads, so no copy instruction occupies the
-//                tensor pipe.
-//   warps 6..13  epilogue, two groups of four warps (one per TMEM quarter);
-//                group e takes the units u with u % 2 == e.
+//                tensor pipe. In a gather with pool_out, its first thread also
+//                bulk-stores each landed unit into the compacted pool.
+//   epilogue     groups of four warps (one per TMEM quarter): two for single
+//                queries, three for 4-query tiles, one for the gather; group e
+//                takes the units u with u % groups == e, and frees each tile of
+//                an accumulator set as soon as it holds it in registers.
 // The block records are used in place as the MMA operands: a record is eight
 // rows of four 8x16-byte core matrices (K-major, no swizzle, core matrices
 // 128 B apart along K, records 576 B apart along M/N).
