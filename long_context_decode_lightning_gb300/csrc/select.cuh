@@ -29,7 +29,10 @@ constexpr int SEL_CAP = 16384;      // items held in shared memory by one CTA
 constexpr int SEL_MAXK = 4096;      // largest k (top-k) or n_keep (pool)
 constexpr int HIST_BINS = 4096;     // top 12 bits of the key
 constexpr int SCAN_THREADS = 512;
-constexpr int SCAN_CHUNK = 16384;   // items per CTA in the histogram / collect passes
+#ifndef HSI_SCAN_CHUNK
+#define HSI_SCAN_CHUNK 8192
+#endif
+constexpr int SCAN_CHUNK = HSI_SCAN_CHUNK;  // items per CTA in the histogram / collect passes
 
 constexpr uint32_t KEY_POS_INF = 0xFF800000u;  // order_key(+inf)
 constexpr uint32_t KEY_NEG_INF = 0x007FFFFFu;  // order_key(-inf)
