@@ -328,6 +328,13 @@ class DeviceWorkload:
             with torch.cuda.graph(g):
                 fn()
             self.graphs.append((kind, g))
+        # the end-to-end step as one graph: inputs in from pinned host memory, the
+        # whole path, results out to pinned host memory (one launch per step)
+        self.graph_e2e = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph_e2e):
+            self.in_dev.copy_(self.in_host, non_blocking=True)
+            self.step()
+            self.out_host.copy_(self.out_dev, non_blocking=True)
         torch.cuda.synchronize()
 
     def replay(self, time_score=False):
@@ -343,9 +350,7 @@ class DeviceWorkload:
                 g.replay()
 
     def step_e2e(self):
-        self.in_dev.copy_(self.in_host, non_blocking=True)
-        self.replay()
-        self.out_host.copy_(self.out_dev, non_blocking=True)
+        self.graph_e2e.replay()
 
     def pairs_per_step(self):
         full = self.wl.full_layers * int(sum(self.wl.n_visible))

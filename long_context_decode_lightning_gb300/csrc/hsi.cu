@@ -28,8 +28,16 @@ namespace {
 #define HSI_DECODE_UT 4
 #endif
 constexpr int kDecodeStages = HSI_DECODE_STAGES, kDecodeUT = HSI_DECODE_UT;
+// scans of a compacted pool: 2048 records per query, a few units per CTA
+#ifndef HSI_POOLED_STAGES
+#define HSI_POOLED_STAGES 4
+#endif
+#ifndef HSI_POOLED_UT
+#define HSI_POOLED_UT 4
+#endif
+constexpr int kPooledStages = HSI_POOLED_STAGES, kPooledUT = HSI_POOLED_UT;
 #ifndef HSI_GATHER_STAGES
-#define HSI_GATHER_STAGES 10
+#define HSI_GATHER_STAGES 8
 #endif
 #ifndef HSI_GATHER_UT
 #define HSI_GATHER_UT 2
@@ -725,7 +733,7 @@ hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float
         p.pad_blocks = n_kept;
         p.n_keep = n_keep;
         p.key_hist = hist;
-        st = launch_score<1, false, kDecodeStages, kDecodeUT>(p, stream);
+        st = launch_score<1, false, kPooledStages, kPooledUT>(p, stream);
         if (st != HSI_OK) return st;
         SelParams sp = topk_params(pool_scores, ld, n_pool, B, k, block_ids, n_keep, 8, top_idx, top_val, wsp);
         sp.hist = hist;
