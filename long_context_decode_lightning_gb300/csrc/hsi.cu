@@ -127,12 +127,24 @@ SelWs carve_sel(void* ws, int32_t B, int64_t max_items, bool need_bmax, int64_t 
 
 // The selection passes. With hist_ready, sp.hist already holds the key
 // histogram (fused into the scoring kernel) and the histogram pass is skipped.
+// Zero `bytes` of device memory in stream order: a kernel taking part in the
+// programmatic launch chain when the range is 16-byte granular, else a memset.
+hsi_status zero_async(void* ptr, size_t bytes, cudaStream_t s) {
+    if (bytes == 0) return HSI_OK;
+    if ((reinterpret_cast<uintptr_t>(ptr) & 15) == 0 && bytes % 16 == 0) {
+        const int64_t n16 = (int64_t)(bytes / 16);
+        const int64_t blocks = (n16 + 1023) / 1024;
+        return launch(zero_kernel, dim3((unsigned)(blocks < 1024 ? blocks : 1024)), dim3(256), 0, s,
+                      reinterpret_cast<uint4*>(ptr), n16);
+    }
+    return cudaMemsetAsync(ptr, 0, bytes, s) == cudaSuccess ? HSI_OK : HSI_ERR_CUDA;
+}
+
 hsi_status run_select(SelParams sp, int64_t max_items, cudaStream_t s, bool hist_ready = false) {
     if (max_items > SEL_CAP) {
-        if (cudaMemsetAsync(sp.cand_cnt, 0, (size_t)sp.B * 4, s) != cudaSuccess) return HSI_ERR_CUDA;
         const dim3 grid((unsigned)((max_items + SCAN_CHUNK - 1) / SCAN_CHUNK), (unsigned)sp.B);
         if (!hist_ready) {
-            if (cudaMemsetAsync(sp.hist, 0, (size_t)sp.B * HIST_BINS * 4, s) != cudaSuccess) return HSI_ERR_CUDA;
+            if (zero_async(sp.hist, (size_t)sp.B * HIST_BINS * 4, s) != HSI_OK) return HSI_ERR_CUDA;
             if (launch(sel_hist_kernel, dim3(grid), dim3(SCAN_THREADS), 0, s, sp) != HSI_OK)
                 return HSI_ERR_CUDA;
         }
@@ -582,8 +594,7 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     float* bmax = reinterpret_cast<float*>(tail + align_up((size_t)B * HIST_BINS * 4, 256));
     const bool big_topk = max_visible > SEL_CAP;
     if (phases & 1) {
-    if (big_topk && cudaMemsetAsync(wsp.hist, 0, (size_t)B * HIST_BINS * 4, stream) != cudaSuccess)
-        return HSI_ERR_CUDA;
+    if (big_topk && zero_async(wsp.hist, (size_t)B * HIST_BINS * 4, stream) != HSI_OK) return HSI_ERR_CUDA;
     ScoreParams p{};
     p.q_rec = q_rec;
     p.g_q = g_q;
@@ -677,7 +688,7 @@ hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float
         if (!ws || ws_bytes < need || !aligned(ws, 256)) return HSI_ERR_WORKSPACE;
         SelWs wsp = carve_sel(ws, B, max_valid, false, 0);
         uint32_t* hist = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + sel_ws_bytes(B, max_valid, false, 0));
-        if (cudaMemsetAsync(hist, 0, (size_t)B * HIST_BINS * 4, stream) != cudaSuccess) return HSI_ERR_CUDA;
+        if (zero_async(hist, (size_t)B * HIST_BINS * 4, stream) != HSI_OK) return HSI_ERR_CUDA;
         ScoreParams p{};
         p.q_rec = q_rec;
         p.g_q = g_q;
@@ -716,7 +727,7 @@ hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float
         // the scan accumulates the key histogram that the selection starts from
         SelWs wsp = carve_sel(ws, B, max_valid, false, 0);
         uint32_t* hist = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + sel_ws_bytes(B, max_valid, false, 0));
-        if (cudaMemsetAsync(hist, 0, (size_t)B * HIST_BINS * 4, stream) != cudaSuccess) return HSI_ERR_CUDA;
+        if (zero_async(hist, (size_t)B * HIST_BINS * 4, stream) != HSI_OK) return HSI_ERR_CUDA;
         ScoreParams p{};
         p.q_rec = q_rec;
         p.g_q = g_q;

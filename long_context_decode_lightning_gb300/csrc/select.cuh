@@ -102,6 +102,15 @@ __device__ __forceinline__ uint32_t sel_key(const SelParams& p, int b, int64_t i
     return key;
 }
 
+// Zeroes n16 16-byte words, in stream order (after the previous kernel) like
+// every kernel here, so that the next kernel's launch can still overlap it.
+__global__ void __launch_bounds__(256) zero_kernel(uint4* p, int64_t n16) {
+    griddep_wait();
+    griddep_launch_dependents();
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x)
+        p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 // ------------------------------------------------------------ scan passes --
 
 // Four consecutive items of a row starting at `base` (< hi): keys and eligibility.
@@ -236,7 +245,10 @@ __global__ void __launch_bounds__(SCAN_THREADS) sel_thresh_kernel(SelParams p) {
     __shared__ uint32_t scratch[SCAN_THREADS + 1];
     const int b = blockIdx.x;
     const uint32_t thr = threshold_bin(p.hist + (int64_t)b * HIST_BINS, p.k, scratch);
-    if (threadIdx.x == 0) p.thr[b] = thr;
+    if (threadIdx.x == 0) {
+        p.thr[b] = thr;
+        p.cand_cnt[b] = 0u;  // the collect pass, launched after this one, counts from zero
+    }
 }
 
 __global__ void __launch_bounds__(SCAN_THREADS) sel_collect_kernel(SelParams p) {
