@@ -89,8 +89,13 @@ int sm_count() {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace of the selection passes for B queries of at most max_items items.
+// A histogram region: [B][HIST_BINS] counts, then [B] counters of the
+// histogram CTAs done (zeroed together).
+size_t hist_region_bytes(int32_t B) { return align_up((size_t)B * HIST_BINS * 4 + (size_t)B * 4, 256); }
+
 struct SelWs {
     uint32_t* hist;
+    uint32_t* done;
     uint32_t* cnt;  // [B] survivor counts, then [B] threshold bins
     uint32_t* ckey;
     uint32_t* cidx;
@@ -100,7 +105,7 @@ struct SelWs {
 size_t sel_ws_bytes(int32_t B, int64_t max_items, bool need_bmax, int64_t max_blocks, int cap = kCandCap) {
     size_t s = 0;
     if (max_items > SEL_CAP) {
-        s += align_up((size_t)B * HIST_BINS * 4, 256);
+        s += hist_region_bytes(B);
         s += align_up((size_t)B * 8, 256);
         s += 2 * align_up((size_t)B * cap * 4, 256);
     }
@@ -113,7 +118,8 @@ SelWs carve_sel(void* ws, int32_t B, int64_t max_items, bool need_bmax, int64_t 
     uint8_t* p = static_cast<uint8_t*>(ws);
     if (max_items > SEL_CAP) {
         w.hist = reinterpret_cast<uint32_t*>(p);
-        p += align_up((size_t)B * HIST_BINS * 4, 256);
+        w.done = w.hist + (size_t)B * HIST_BINS;
+        p += hist_region_bytes(B);
         w.cnt = reinterpret_cast<uint32_t*>(p);
         p += align_up((size_t)B * 8, 256);
         w.ckey = reinterpret_cast<uint32_t*>(p);
@@ -144,11 +150,16 @@ hsi_status run_select(SelParams sp, int64_t max_items, cudaStream_t s, bool hist
     if (max_items > SEL_CAP) {
         const dim3 grid((unsigned)((max_items + SCAN_CHUNK - 1) / SCAN_CHUNK), (unsigned)sp.B);
         if (!hist_ready) {
-            if (zero_async(sp.hist, (size_t)sp.B * HIST_BINS * 4, s) != HSI_OK) return HSI_ERR_CUDA;
+            // the histogram pass; its last CTA per query also finds the threshold bin
+            sp.done = sp.hist + (size_t)sp.B * HIST_BINS;
+            if (zero_async(sp.hist, (size_t)sp.B * (HIST_BINS + 1) * 4, s) != HSI_OK) return HSI_ERR_CUDA;
             if (launch(sel_hist_kernel, dim3(grid), dim3(SCAN_THREADS), 0, s, sp) != HSI_OK)
                 return HSI_ERR_CUDA;
+        } else {
+            sp.done = nullptr;
+            if (launch(sel_thresh_kernel, dim3(sp.B), dim3(SCAN_THREADS), 0, s, sp) != HSI_OK)
+                return HSI_ERR_CUDA;
         }
-        if (launch(sel_thresh_kernel, dim3(sp.B), dim3(SCAN_THREADS), 0, s, sp) != HSI_OK) return HSI_ERR_CUDA;
         if (launch(sel_collect_kernel, dim3(grid), dim3(SCAN_THREADS), 0, s, sp) != HSI_OK) return HSI_ERR_CUDA;
     }
     static bool attr_set = false;
@@ -311,7 +322,7 @@ size_t hsi_workspace_size(hsi_ws_kind kind, int32_t B, int64_t max_n, int32_t k)
         case HSI_WS_TOPK: return sel_ws_bytes(B, max_n, false, 0);
         case HSI_WS_FULL_LAYER: {
             const int64_t nb = (max_n + 7) / 8;
-            return sel_ws_bytes(B, max_n > nb ? max_n : nb, false, 0) + align_up((size_t)B * HIST_BINS * 4, 256) +
+            return sel_ws_bytes(B, max_n > nb ? max_n : nb, false, 0) + hist_region_bytes(B) +
                    align_up((size_t)B * (size_t)nb * 4, 256);
         }
         case HSI_WS_REINDEX_LAYER:  // + the key histogram the pooled scan accumulates
@@ -591,7 +602,7 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     SelWs wsp = carve_sel(ws, B, max_visible > nb ? max_visible : nb, false, 0);
     uint8_t* tail = static_cast<uint8_t*>(ws) + sel_ws_bytes(B, max_visible > nb ? max_visible : nb, false, 0);
     uint32_t* bhist = reinterpret_cast<uint32_t*>(tail);
-    float* bmax = reinterpret_cast<float*>(tail + align_up((size_t)B * HIST_BINS * 4, 256));
+    float* bmax = reinterpret_cast<float*>(tail + hist_region_bytes(B));
     const bool big_topk = max_visible > SEL_CAP;
     if (phases & 1) {
     if (big_topk && zero_async(wsp.hist, (size_t)B * HIST_BINS * 4, stream) != HSI_OK) return HSI_ERR_CUDA;

@@ -55,6 +55,9 @@ struct SelParams {
     uint32_t* cand_idx;  // [B][cap]
     uint32_t* thr;       // [B] bin (top 12 key bits) holding the k-th key
     int32_t cap;
+    // optional: [B] counters of histogram CTAs done (zero at the start); the
+    // last CTA of a query computes its threshold bin, so no threshold pass runs
+    uint32_t* done;
     // rows of at most SEL_CAP items whose histogram is already in `hist` (TOPK
     // mode): the final kernel takes the threshold bin from it and loads only
     // the items at or above that bin
@@ -172,32 +175,6 @@ __device__ __forceinline__ void load_chunk(const SelParams& p, int b, const floa
     }
 }
 
-__global__ void __launch_bounds__(SCAN_THREADS) sel_hist_kernel(SelParams p) {
-    griddep_wait();
-    griddep_launch_dependents();
-    __shared__ uint32_t sh[HIST_BINS];
-    const int b = blockIdx.y;
-    const int64_t n = sel_items(p, b);
-    const int64_t lo = (int64_t)blockIdx.x * SCAN_CHUNK;
-    if (lo >= n) return;
-    const int64_t hi = min(n, lo + SCAN_CHUNK);
-    for (int i = threadIdx.x; i < HIST_BINS; i += SCAN_THREADS) sh[i] = 0;
-    __syncthreads();
-    const float* row = p.src + (int64_t)b * p.ld;
-    const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
-    uint32_t key[SCAN_ROUNDS][4], okm;
-    load_chunk(p, b, row, vec, lo, hi, n, key, okm);
-#pragma unroll
-    for (int r = 0; r < SCAN_ROUNDS; ++r)
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            if (okm >> (4 * r + i) & 1u) atomicAdd(&sh[key[r][i] >> 20], 1u);
-    __syncthreads();
-    uint32_t* gh = p.hist + (int64_t)b * HIST_BINS;
-    for (int i = threadIdx.x; i < HIST_BINS; i += SCAN_THREADS)
-        if (sh[i]) atomicAdd(&gh[i], sh[i]);
-}
-
 // The largest bin t such that the items in bins >= t number at least k (0 if
 // there are fewer than k items). Whole block; SCAN_THREADS * 8 == HIST_BINS.
 __device__ uint32_t threshold_bin(const uint32_t* gh, int k, uint32_t* scratch /*SCAN_THREADS+1*/) {
@@ -207,7 +184,7 @@ __device__ uint32_t threshold_bin(const uint32_t* gh, int k, uint32_t* scratch /
     uint32_t s = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        c[i] = gh[t * 8 + i];
+        c[i] = __ldcg(gh + t * 8 + i);  // counts other CTAs added in L2
         s += c[i];
     }
     scratch[t] = s;
@@ -236,6 +213,49 @@ __device__ uint32_t threshold_bin(const uint32_t* gh, int k, uint32_t* scratch /
     }
     __syncthreads();
     return scratch[SCAN_THREADS];
+}
+
+__global__ void __launch_bounds__(SCAN_THREADS) sel_hist_kernel(SelParams p) {
+    griddep_wait();
+    griddep_launch_dependents();
+    __shared__ uint32_t sh[HIST_BINS];
+    const int b = blockIdx.y;
+    const int64_t n = sel_items(p, b);
+    const int64_t lo = (int64_t)blockIdx.x * SCAN_CHUNK;
+    if (lo >= n) return;
+    const int64_t hi = min(n, lo + SCAN_CHUNK);
+    for (int i = threadIdx.x; i < HIST_BINS; i += SCAN_THREADS) sh[i] = 0;
+    __syncthreads();
+    const float* row = p.src + (int64_t)b * p.ld;
+    const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
+    uint32_t key[SCAN_ROUNDS][4], okm;
+    load_chunk(p, b, row, vec, lo, hi, n, key, okm);
+#pragma unroll
+    for (int r = 0; r < SCAN_ROUNDS; ++r)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (okm >> (4 * r + i) & 1u) atomicAdd(&sh[key[r][i] >> 20], 1u);
+    __syncthreads();
+    uint32_t* gh = p.hist + (int64_t)b * HIST_BINS;
+    for (int i = threadIdx.x; i < HIST_BINS; i += SCAN_THREADS)
+        if (sh[i]) atomicAdd(&gh[i], sh[i]);
+    if (!p.done) return;
+    // the query's last CTA to finish computes its threshold bin
+    __shared__ int last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t chunks = (uint32_t)((n + SCAN_CHUNK - 1) / SCAN_CHUNK);
+        last = atomicAdd(p.done + b, 1u) == chunks - 1;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    const uint32_t thr = threshold_bin(gh, p.k, sh);  // sh: scratch now
+    if (threadIdx.x == 0) {
+        p.thr[b] = thr;
+        p.cand_cnt[b] = 0u;  // the collect pass counts from zero
+    }
 }
 
 // One CTA per query: the threshold bin from the merged histogram.
