@@ -160,7 +160,14 @@ hsi_status run_select(SelParams sp, int64_t max_items, cudaStream_t s, bool hist
             if (launch(sel_thresh_kernel, dim3(sp.B), dim3(SCAN_THREADS), 0, s, sp) != HSI_OK)
                 return HSI_ERR_CUDA;
         }
-        if (launch(sel_collect_kernel, dim3(grid), dim3(SCAN_THREADS), 0, s, sp) != HSI_OK) return HSI_ERR_CUDA;
+        if (sp.blk_max) {  // block-guided: reads the block maxima and the few blocks that reach the bin
+            const int64_t nblk = (max_items + 7) / 8;
+            const dim3 bgrid((unsigned)((nblk + SCAN_CHUNK - 1) / SCAN_CHUNK), (unsigned)sp.B);
+            if (launch(sel_collect_blocks_kernel, bgrid, dim3(SCAN_THREADS), 0, s, sp) != HSI_OK)
+                return HSI_ERR_CUDA;
+        } else if (launch(sel_collect_kernel, dim3(grid), dim3(SCAN_THREADS), 0, s, sp) != HSI_OK) {
+            return HSI_ERR_CUDA;
+        }
     }
     static bool attr_set = false;
     if (!attr_set) {
@@ -618,7 +625,9 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     p.ngroups = B;
     p.scores = scores;
     p.ld = ld;
-    p.bmax = pool ? bmax : nullptr;
+    // block maxima: for the pool, and for the top-k's collect pass (it reads the
+    // scores of the blocks whose maximum reaches the threshold bin only)
+    p.bmax = pool || big_topk ? bmax : nullptr;
     p.ldb = nb;
     p.key_hist = big_topk ? wsp.hist : nullptr;
     st = launch_score<1, false, kDecodeStages, kDecodeUT>(p, stream);
@@ -641,9 +650,14 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     sp.cap = kCandCap;
     sp.out_idx = top_idx;
     sp.out_val = top_val;
+    if (big_topk) {
+        sp.blk_max = bmax;
+        sp.ld_bmax = nb;
+    }
     st = run_select(sp, max_visible, stream, true);
     if (st != HSI_OK || !pool) return st;
     SelParams pp = sp;
+    pp.blk_max = nullptr;
     pp.src = bmax;
     pp.ld = nb;
     pp.div = 8;

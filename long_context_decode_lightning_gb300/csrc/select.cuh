@@ -58,6 +58,12 @@ struct SelParams {
     // optional: [B] counters of histogram CTAs done (zero at the start); the
     // last CTA of a query computes its threshold bin, so no threshold pass runs
     uint32_t* done;
+    // optional (TOPK mode): the maxima of the row's blocks of 8 items,
+    // blk_max[b * ld_bmax + j] = max of items 8j .. 8j+7 (the visible ones); the
+    // collect pass then reads only the blocks whose maximum reaches the
+    // threshold bin (a block below it holds no survivor)
+    const float* blk_max;
+    int64_t ld_bmax;
     // rows of at most SEL_CAP items whose histogram is already in `hist` (TOPK
     // mode): the final kernel takes the threshold bin from it and loads only
     // the items at or above that bin
@@ -319,6 +325,87 @@ __global__ void __launch_bounds__(SCAN_THREADS) sel_collect_kernel(SelParams p) 
                 }
                 ++at;
             }
+}
+
+// The collect pass guided by block maxima (TOPK mode, blk_max given): a CTA
+// covers SCAN_CHUNK blocks of 8 items; it reads their maxima (an eighth of
+// the items' bytes) and only the items of blocks whose maximum's bin reaches
+// the threshold, which are few (about one block per survivor).
+__global__ void __launch_bounds__(SCAN_THREADS) sel_collect_blocks_kernel(SelParams p) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int b = blockIdx.y;
+    const int64_t n = sel_items(p, b);
+    const int64_t nb = (n + 7) / 8;
+    const int64_t lo = (int64_t)blockIdx.x * SCAN_CHUNK;  // in blocks
+    if (lo >= nb) return;
+    const int64_t hi = min(nb, lo + SCAN_CHUNK);
+    const uint32_t thr = p.thr[b];
+    const int lane = threadIdx.x & 31;
+    const float* bm = p.blk_max + (int64_t)b * p.ld_bmax;
+    const float* row = p.src + (int64_t)b * p.ld;
+    const bool bvec = (reinterpret_cast<uintptr_t>(bm) & 15) == 0;
+    // the block maxima (as plain TOPK keys: blocks are never pinned or dropped)
+    uint32_t key[SCAN_ROUNDS][4], okm;
+    load_chunk(p, b, bm, bvec, lo, hi, nb, key, okm);  // TOPK mode: every block below hi counts
+    uint32_t hit = 0;
+#pragma unroll
+    for (int r = 0; r < SCAN_ROUNDS; ++r)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if ((okm >> (4 * r + i) & 1u) && (key[r][i] >> 20) >= thr) hit |= 1u << (4 * r + i);
+    // survivors of the hit blocks (few): counted, then written after one
+    // reservation per warp; compact loops over the hit bits (this code runs for
+    // few lanes, and unrolled copies of it cost instruction fetches)
+    const bool rvec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
+    auto block_mask = [&](int64_t blk) -> uint32_t {  // survivors among the block's items
+        const int64_t j0 = 8 * blk;
+        float v[8];
+        if (rvec && j0 + 7 < n) {
+            const float4 a = *reinterpret_cast<const float4*>(row + j0);
+            const float4 c4 = *reinterpret_cast<const float4*>(row + j0 + 4);
+            v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = c4.x, v[5] = c4.y, v[6] = c4.z, v[7] = c4.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = j0 + e < n ? row[j0 + e] : __uint_as_float(0xFF800000u);
+        }
+        uint32_t m = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (j0 + e < n && (order_key(v[e]) >> 20) >= thr) m |= 1u << e;
+        return m;
+    };
+    auto block_of = [&](int q) -> int64_t { return lo + 4 * ((int64_t)(q >> 2) * SCAN_THREADS + threadIdx.x) + (q & 3); };
+    uint32_t c = 0;
+#pragma unroll 1
+    for (uint32_t h = hit; h; h &= h - 1) c += (uint32_t)__popc(block_mask(block_of(__ffs(h) - 1)));
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    if (tot == 0) return;
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(p.cand_cnt + b, tot);
+    uint32_t at = __shfl_sync(0xFFFFFFFFu, base, 0) + incl - c;
+    uint32_t* ck = p.cand_key + (int64_t)b * p.cap;
+    uint32_t* ci = p.cand_idx + (int64_t)b * p.cap;
+#pragma unroll 1
+    for (uint32_t h = hit; h; h &= h - 1) {
+        const int64_t blk = block_of(__ffs(h) - 1);
+        uint32_t m = block_mask(blk);
+#pragma unroll 1
+        for (; m; m &= m - 1) {
+            const int64_t jj = 8 * blk + (__ffs(m) - 1);
+            if (at < (uint32_t)p.cap) {
+                ck[at] = order_key(row[jj]);
+                ci[at] = (uint32_t)jj;
+            }
+            ++at;
+        }
+    }
 }
 
 // -------------------------------------------------------- block select --
