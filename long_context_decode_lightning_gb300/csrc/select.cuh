@@ -791,7 +791,8 @@ __device__ int select_finish(const Src& src, SelSmem& s, int k, int64_t id_range
         if (bitmap) {
             if (take) {
                 const uint32_t id = src.idx(j);
-                atomicOr(&bits[id >> 5], 1u << (id & 31));
+                if (id < (uint64_t)id_range) atomicOr(&bits[id >> 5], 1u << (id & 31));
+                else raise_error(DEVERR_ARG);  // never an id of this row: left out
             }
             continue;
         }

@@ -351,6 +351,21 @@ def test_full_and_reindex_layer_match_separate_calls(lengths):
         oi, onk, onp, _ = oracle.pool(sg[b], n)
         assert int(nk_f[b]) == onk and np.array_equal(ids_f.cpu().numpy()[b][:onk], oi[:onk])
 
+    # the selection phase run again (twice) over the same scores and workspace
+    # starts from the same state and gives the same top-k and pool
+    ws = hsi.workspace(hsi.WS_FULL_LAYER, B, maxv, 512, device=DEV)
+    i_r, v_r, ids_r = torch.empty_like(i_f), torch.empty_like(v_f), torch.empty_like(ids_f)
+    nk_r, np_r, bits_r = torch.empty_like(nk_f), torch.empty_like(np_f), torch.zeros_like(bits_f)
+    s_r = torch.empty_like(s_f)
+    for phases in (1, 2, 2):
+        hsi.full_layer(q_rec, g_q, w, caches.k_rec, caches.g, off, nv, B, maxv, s_r, 512, i_r, v_r, block_ids=ids_r,
+                       n_kept=nk_r, n_pool=np_r, pool_bits=bits_r, ws=ws, phases=phases)
+    assert hsi.device_error() == 0
+    assert torch.equal(i_r, i_f) and torch.equal(v_r, v_f)
+    assert torch.equal(nk_r, nk_f) and torch.equal(np_r, np_f) and torch.equal(bits_r, bits_f)
+    for b in range(B):
+        assert torch.equal(ids_r[b, :int(nk_f[b])], ids_f[b, :int(nk_f[b])])
+
     q1, g1, w1 = gpu_queries(wl, 1, range(B))
     ps_sep = torch.empty(B, 2048 * 8, device=DEV)
     hsi.score_pool(q1, g1, w1, caches.k_rec, caches.g, off, nv, ids_f, nk_f, 2048, B, ps_sep)
