@@ -1,8 +1,9 @@
 """ORACLE -- test infrastructure, not the product.
 
 ctypes binding of ``oracle.c``: a plain single-threaded CPU restatement of the
-Hierarchical Sparse Indexer decode path (NVFP4 codecs, rotation, quantisation,
-fp64 scoring, full-sort top-k, the candidate pool, pooled Reindex scoring).
+Hierarchical Sparse Indexer decode path (NVFP4 and MXFP4 codecs, rotation,
+quantisation, fp64 scoring, full-sort top-k, the candidate pool, pooled
+Reindex scoring).
 Only the tests, the smoke check and the bench's CPU-baseline leg use it; the
 CUDA path never imports it.
 
@@ -25,6 +26,8 @@ _SO = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
 REC_BYTES = 576
+MX_REC_BYTES = 544
+FMTS = {"nvfp4": 0, "mxfp4": 1}
 ROWS_PER_REC = 8
 H = 32
 D = 128
@@ -60,16 +63,25 @@ def lib():
         L.hsio_quantize.restype = i32
         L.hsio_decode_row.argtypes = [vp, i64, f32, vp]
         L.hsio_decode_row.restype = None
-        L.hsio_score_full.argtypes = [vp, f32, vp, vp, f32, i64, vp]
-        L.hsio_score_full.restype = i64
-        L.hsio_score_rows.argtypes = [vp, f32, vp, vp, f32, vp, i64, vp, vp]
-        L.hsio_score_rows.restype = i64
+        L.hsio_e8m0_value.argtypes = [u8]
+        L.hsio_e8m0_value.restype = ctypes.c_double
+        L.hsio_mx_scale_exp.argtypes = [f32]
+        L.hsio_mx_scale_exp.restype = i32
+        L.hsio_quantize_mx.argtypes = [vp, i64, vp, vp]
+        L.hsio_quantize_mx.restype = i32
+        L.hsio_decode_row_mx.argtypes = [vp, i64, vp]
+        L.hsio_decode_row_mx.restype = None
+        L.hsio_score_full_fmt.argtypes = [i32, vp, f32, vp, vp, f32, i64, vp]
+        L.hsio_score_full_fmt.restype = i64
+        L.hsio_score_rows_fmt.argtypes = [i32, vp, f32, vp, vp, f32, vp, i64, vp, vp]
+        L.hsio_score_rows_fmt.restype = i64
+        L.hsio_score_pool_fmt.argtypes = [i32, vp, f32, vp, vp, f32, i64, vp, ctypes.c_int32, ctypes.c_int32,
+                                          i32, vp]
+        L.hsio_score_pool_fmt.restype = i64
         L.hsio_topk.argtypes = [vp, i64, i32, vp, vp]
         L.hsio_topk.restype = i64
         L.hsio_pool.argtypes = [vp, i64, i32, i32, vp, vp, vp, vp]
         L.hsio_pool.restype = i32
-        L.hsio_score_pool.argtypes = [vp, f32, vp, vp, f32, i64, vp, ctypes.c_int32, ctypes.c_int32, i32, vp]
-        L.hsio_score_pool.restype = i64
         L.hsio_topk_pool.argtypes = [vp, i64, vp, i32, i32, vp, vp]
         L.hsio_topk_pool.restype = i64
         L.hsio_topk_masked.argtypes = [vp, i64, vp, i32, vp, vp]
@@ -105,6 +117,15 @@ def e4m3_encode(x: float) -> int:
     return int(lib().hsio_e4m3_encode(float(x)))
 
 
+def e8m0_value(code: int) -> float:
+    return lib().hsio_e8m0_value(code)
+
+
+def mx_scale_exp(amax: float) -> int:
+    """Exponent e of the MXFP4 group scale 2^e for a group whose largest magnitude is amax."""
+    return int(lib().hsio_mx_scale_exp(float(amax)))
+
+
 def fwht128(v: np.ndarray) -> np.ndarray:
     out = _c(v, np.float32).copy()
     assert out.size == D
@@ -133,33 +154,51 @@ def quantize(x_bf16: np.ndarray, signs: np.ndarray, g: float | None = None):
     return rec, float(gg[0])
 
 
-def decode_row(records: np.ndarray, row: int, g: float) -> np.ndarray:
+def quantize_mx(x_bf16: np.ndarray, signs: np.ndarray) -> np.ndarray:
+    """Quantise one tensor (bf16 bits [rows][128]) -> MXFP4 records uint8 [nrec*544] (no tensor scale)."""
+    x = _c(x_bf16, np.uint16).reshape(-1, D)
+    s = _c(signs, np.int8)
+    rec = np.empty(n_records(x.shape[0]) * MX_REC_BYTES, dtype=np.uint8)
+    if lib().hsio_quantize_mx(_p(x), x.shape[0], _p(s), _p(rec)) != 0:
+        raise ValueError("oracle quantize_mx: non-finite input")
+    return rec
+
+
+def decode_row(records: np.ndarray, row: int, g: float = 1.0, fmt: str = "nvfp4") -> np.ndarray:
     out = np.empty(D, dtype=np.float64)
-    lib().hsio_decode_row(_p(records), row, g, _p(out))
+    if fmt == "mxfp4":
+        lib().hsio_decode_row_mx(_p(records), row, _p(out))
+    else:
+        lib().hsio_decode_row(_p(records), row, g, _p(out))
     return out
 
 
-def decode_rows(records: np.ndarray, rows: int, g: float) -> np.ndarray:
-    return np.stack([decode_row(records, r, g) for r in range(rows)])
+def decode_rows(records: np.ndarray, rows: int, g: float = 1.0, fmt: str = "nvfp4") -> np.ndarray:
+    return np.stack([decode_row(records, r, g, fmt) for r in range(rows)])
 
 
 # ----------------------------------------------------------------- score ----
 
-def score_full(q_rec, g_q, w, k_rec, g_k, n_vis):
-    """fp32 scores of keys [0, n_vis) for one query; returns (scores, macs)."""
+def score_full(q_rec, g_q, w, k_rec, g_k, n_vis, fmt="nvfp4"):
+    """fp32 scores of keys [0, n_vis) for one query; returns (scores, macs).
+    fmt "mxfp4": MXFP4 records, g_q and g_k ignored (no tensor scale)."""
     out = np.empty(max(n_vis, 1), dtype=np.float32)
     w = _c(w, np.float32)
-    macs = lib().hsio_score_full(_p(q_rec), g_q, _p(w), _p(k_rec), g_k, n_vis, _p(out))
+    f = FMTS[fmt]
+    g_q, g_k = (1.0, 1.0) if f else (g_q, g_k)
+    macs = lib().hsio_score_full_fmt(f, _p(q_rec), g_q, _p(w), _p(k_rec), g_k, n_vis, _p(out))
     return out[:n_vis], macs
 
 
-def score_rows(q_rec, g_q, w, k_rec, g_k, rows):
+def score_rows(q_rec, g_q, w, k_rec, g_k, rows, fmt="nvfp4"):
     """Scores and parity tolerances of the listed keys for one query."""
     rows = _c(rows, np.int64)
     out = np.empty(max(rows.size, 1), dtype=np.float32)
     tol = np.empty(max(rows.size, 1), dtype=np.float64)
     w = _c(w, np.float32)
-    lib().hsio_score_rows(_p(q_rec), g_q, _p(w), _p(k_rec), g_k, _p(rows), rows.size, _p(out), _p(tol))
+    f = FMTS[fmt]
+    g_q, g_k = (1.0, 1.0) if f else (g_q, g_k)
+    lib().hsio_score_rows_fmt(f, _p(q_rec), g_q, _p(w), _p(k_rec), g_k, _p(rows), rows.size, _p(out), _p(tol))
     return out[:rows.size], tol[:rows.size]
 
 
@@ -191,12 +230,14 @@ def pool(scores: np.ndarray, n_vis: int, block_size: int = 8, n_keep: int = 2048
     return ids, int(nk[0]), int(npool[0]), (mask[:n_vis] if want_mask else None)
 
 
-def score_pool(q_rec, g_q, w, k_rec, g_k, n_vis, block_ids, n_kept, n_keep=2048, block_size=8):
+def score_pool(q_rec, g_q, w, k_rec, g_k, n_vis, block_ids, n_kept, n_keep=2048, block_size=8, fmt="nvfp4"):
     out = np.empty(n_keep * block_size, dtype=np.float32)
     w = _c(w, np.float32)
     ids = _c(block_ids, np.int32)
-    macs = lib().hsio_score_pool(_p(q_rec), g_q, _p(w), _p(k_rec), g_k, n_vis, _p(ids), n_kept, n_keep,
-                                 block_size, _p(out))
+    f = FMTS[fmt]
+    g_q, g_k = (1.0, 1.0) if f else (g_q, g_k)
+    macs = lib().hsio_score_pool_fmt(f, _p(q_rec), g_q, _p(w), _p(k_rec), g_k, n_vis, _p(ids), n_kept, n_keep,
+                                     block_size, _p(out))
     return out, macs
 
 

@@ -37,10 +37,20 @@
  *    first min(n_keep, nblk) blocks in (value desc, block asc) order whose value
  *    is > -inf; the pool is the kept blocks intersected with [0, n_vis).
  *
- * Storage format decoded here (the product's NVFP4 "block record"): rows are
- * grouped 8 to a 576-byte record. In record R (rows 8R .. 8R+7), element e of
- * row r has its 4-bit code in byte (e/32)*128 + r*16 + (e%32)/2, low nibble for
- * even e; the E4M3 scale of row r, group e/16, is byte 512 + r*8 + e/16.
+ *  - MXFP4 (the indexer format the pages describe, [J] table in "scale 的格式
+ *    决定了精度"): 32-element groups, one E8M0 scale each (a power of two, no
+ *    tensor scale). The pages give the ideal scale max|x|/6 and say an E8M0
+ *    scale can only take it rounded up to a power of two; so the group scale is
+ *    the smallest 2^e (e in [-127, 127]) with 6 * 2^e >= amax_group (2^-127
+ *    for an all-zero group), and code = E2M1_RN(y / 2^e), saturating at +-6.
+ *    The score is the same sum with g_q = g_k = 1.
+ *
+ * Storage formats decoded here (the product's "block records"): rows are
+ * grouped 8 to a record. In record R (rows 8R .. 8R+7), element e of row r has
+ * its 4-bit code in byte (e/32)*128 + r*16 + (e%32)/2, low nibble for even e.
+ * NVFP4 records are 576 bytes: the E4M3 scale of row r, group e/16, is byte
+ * 512 + r*8 + e/16. MXFP4 records are 544 bytes: the E8M0 scale of row r,
+ * group e/32, is byte 512 + r*4 + e/32.
  */
 #include <math.h>
 #include <stdint.h>
@@ -48,6 +58,9 @@
 #include <string.h>
 
 #define REC_BYTES 576
+#define MX_REC_BYTES 544
+#define FMT_NVFP4 0
+#define FMT_MXFP4 1
 #define ROWS_PER_REC 8
 #define DIM 128
 #define HEADS 32
@@ -107,10 +120,22 @@ uint8_t hsio_e4m3_encode(float x) {
     return (uint8_t)(c | (signbit(x) ? 0x80 : 0));
 }
 
-uint8_t hsio_e2m1_encode(float x) {
-    double ax = fabs((double)x);
-    int c = nearest_code(ax, E2M1_MAG, 8);
+static uint8_t e2m1_encode_d(double x) {
+    int c = nearest_code(fabs(x), E2M1_MAG, 8);
     return (uint8_t)(c | (signbit(x) ? 8 : 0));
+}
+
+uint8_t hsio_e2m1_encode(float x) { return e2m1_encode_d((double)x); }
+
+/* E8M0 (OCP MX scale): an unsigned biased exponent, value 2^(b - 127); 0xFF is NaN. */
+double hsio_e8m0_value(uint8_t b) { return b == 0xFF ? NAN : ldexp(1.0, (int)b - 127); }
+
+/* The MXFP4 group scale exponent: the smallest e in [-127, 127] with
+ * 6 * 2^e >= amax (the ideal scale amax / 6 rounded up to a power of two). */
+int hsio_mx_scale_exp(float amax) {
+    int e = -127;
+    while (e < 127 && ldexp(6.0, e) < (double)amax) ++e;
+    return e;
 }
 
 static float bf16_to_f32(uint16_t b) {
@@ -155,6 +180,8 @@ static inline void rec_put_code(uint8_t* rec, int r, int e, uint8_t code) {
 
 static inline uint8_t rec_scale(const uint8_t* rec, int r, int g) { return rec[512 + r * 8 + g]; }
 
+static inline uint8_t mx_rec_scale(const uint8_t* rec, int r, int g) { return rec[512 + r * 4 + g]; }
+
 /* Decoded row `row` of a record array: code value * block scale * tensor scale g,
  * in double (exact). */
 void hsio_decode_row(const uint8_t* records, int64_t row, float g, double* out) {
@@ -165,8 +192,20 @@ void hsio_decode_row(const uint8_t* records, int64_t row, float g, double* out) 
                  (double)g;
 }
 
-/* Same without the tensor scale (code value * block scale). */
-static void decode_row_unscaled(const uint8_t* records, int64_t row, double* out) {
+/* Decoded row `row` of an MXFP4 record array: code value * 2^(scale - 127). */
+void hsio_decode_row_mx(const uint8_t* records, int64_t row, double* out) {
+    const uint8_t* rec = records + (row / ROWS_PER_REC) * MX_REC_BYTES;
+    int r = (int)(row % ROWS_PER_REC);
+    for (int e = 0; e < DIM; ++e)
+        out[e] = hsio_e2m1_value(rec_code(rec, r, e)) * hsio_e8m0_value(mx_rec_scale(rec, r, e >> 5));
+}
+
+/* Same without the tensor scale (code value * block scale), either format. */
+static void decode_row_unscaled(int fmt, const uint8_t* records, int64_t row, double* out) {
+    if (fmt == FMT_MXFP4) {
+        hsio_decode_row_mx(records, row, out);
+        return;
+    }
     const uint8_t* rec = records + (row / ROWS_PER_REC) * REC_BYTES;
     int r = (int)(row % ROWS_PER_REC);
     for (int e = 0; e < DIM; ++e)
@@ -227,17 +266,50 @@ int hsio_quantize(const uint16_t* x, int64_t rows, const int8_t* signs, int mode
     return 0;
 }
 
+/* Quantise `rows` bf16 rows of 128 into MXFP4 block records (no tensor
+ * scale): per row the same rotation, then per 32-element group the scale
+ * exponent e of hsio_mx_scale_exp and codes E2M1_RN(y / 2^e) (y / 2^e is exact
+ * in double). records must hold ceil(rows/8) * 544 bytes; padding rows are
+ * zero (codes 0, scale byte 0). Returns 0, or -1 on a non-finite input. */
+int hsio_quantize_mx(const uint16_t* x, int64_t rows, const int8_t* signs, uint8_t* records) {
+    float y[DIM];
+    int64_t nrec = (rows + ROWS_PER_REC - 1) / ROWS_PER_REC;
+    memset(records, 0, (size_t)nrec * MX_REC_BYTES);
+    for (int64_t i = 0; i < rows; ++i) {
+        uint8_t* rec = records + (i / ROWS_PER_REC) * MX_REC_BYTES;
+        int r = (int)(i % ROWS_PER_REC);
+        rotate_row(x + i * DIM, signs, y);
+        for (int grp = 0; grp < DIM / 32; ++grp) {
+            float amax = 0.0f;
+            for (int t = 0; t < 32; ++t) {
+                if (!isfinite(y[grp * 32 + t])) return -1;
+                float a = fabsf(y[grp * 32 + t]);
+                if (a > amax) amax = a;
+            }
+            int e = hsio_mx_scale_exp(amax);
+            rec[512 + r * 4 + grp] = (uint8_t)(e + 127);
+            for (int t = 0; t < 32; ++t) {
+                int el = grp * 32 + t;
+                rec_put_code(rec, r, el, e2m1_encode_d(ldexp((double)y[el], -e)));
+            }
+        }
+    }
+    return 0;
+}
+
 /* ---------------------------------------------------------------- score -- */
 
 typedef struct {
     double qv[HEADS][DIM]; /* decoded q without the tensor scale */
     double w[HEADS];
     double scale;          /* g_q * g_k / 128 */
+    int fmt;               /* FMT_NVFP4 or FMT_MXFP4, for q and K alike */
 } query_ctx;
 
-static void query_setup(query_ctx* c, const uint8_t* q_rec, float g_q, const float* w, float g_k) {
+static void query_setup(query_ctx* c, int fmt, const uint8_t* q_rec, float g_q, const float* w, float g_k) {
+    c->fmt = fmt;
     for (int j = 0; j < HEADS; ++j) {
-        decode_row_unscaled(q_rec, j, c->qv[j]);
+        decode_row_unscaled(fmt, q_rec, j, c->qv[j]);
         c->w[j] = (double)w[j];
     }
     c->scale = (double)g_q * (double)g_k / 128.0;
@@ -247,7 +319,7 @@ static void query_setup(query_ctx* c, const uint8_t* q_rec, float g_q, const flo
  * tensor scales. Adds the multiply-adds done to *macs. */
 static float score_one(const query_ctx* c, const uint8_t* k_rec, int64_t row, int64_t* macs) {
     double kv[DIM];
-    decode_row_unscaled(k_rec, row, kv);
+    decode_row_unscaled(c->fmt, k_rec, row, kv);
     double acc = 0.0;
     int64_t m = 0;
     for (int j = 0; j < HEADS; ++j) {
@@ -262,30 +334,36 @@ static float score_one(const query_ctx* c, const uint8_t* k_rec, int64_t row, in
     return (float)(c->scale * acc);
 }
 
-/* Scores of keys [0, n_vis) of one K cache for one query. Returns MACs done. */
-int64_t hsio_score_full(const uint8_t* q_rec, float g_q, const float* w, const uint8_t* k_rec,
-                        float g_k, int64_t n_vis, float* scores) {
+/* Scores of keys [0, n_vis) of one K cache for one query, records of format
+ * fmt (MXFP4: pass g_q = g_k = 1). Returns MACs done. */
+int64_t hsio_score_full_fmt(int fmt, const uint8_t* q_rec, float g_q, const float* w, const uint8_t* k_rec,
+                            float g_k, int64_t n_vis, float* scores) {
     query_ctx* c = (query_ctx*)malloc(sizeof(query_ctx));
-    query_setup(c, q_rec, g_q, w, g_k);
+    query_setup(c, fmt, q_rec, g_q, w, g_k);
     int64_t macs = 0;
     for (int64_t s = 0; s < n_vis; ++s) scores[s] = score_one(c, k_rec, s, &macs);
     free(c);
     return macs;
 }
 
+int64_t hsio_score_full(const uint8_t* q_rec, float g_q, const float* w, const uint8_t* k_rec, float g_k,
+                        int64_t n_vis, float* scores) {
+    return hsio_score_full_fmt(FMT_NVFP4, q_rec, g_q, w, k_rec, g_k, n_vis, scores);
+}
+
 /* Scores of the listed keys, and for each the parity tolerance
  * 1e-4 * sum_j |w_j| * sum_d |qhat_jd khat_d| (tensor scales and the 2^-7 fold
  * applied, as in the score). */
-int64_t hsio_score_rows(const uint8_t* q_rec, float g_q, const float* w, const uint8_t* k_rec,
-                        float g_k, const int64_t* rows, int64_t n, float* out, double* tol) {
+int64_t hsio_score_rows_fmt(int fmt, const uint8_t* q_rec, float g_q, const float* w, const uint8_t* k_rec,
+                            float g_k, const int64_t* rows, int64_t n, float* out, double* tol) {
     query_ctx* c = (query_ctx*)malloc(sizeof(query_ctx));
-    query_setup(c, q_rec, g_q, w, g_k);
+    query_setup(c, fmt, q_rec, g_q, w, g_k);
     int64_t macs = 0;
     for (int64_t i = 0; i < n; ++i) {
         out[i] = score_one(c, k_rec, rows[i], &macs);
         if (tol) {
             double kv[DIM];
-            decode_row_unscaled(k_rec, rows[i], kv);
+            decode_row_unscaled(c->fmt, k_rec, rows[i], kv);
             double t = 0.0;
             for (int j = 0; j < HEADS; ++j) {
                 double sabs = 0.0;
@@ -297,6 +375,11 @@ int64_t hsio_score_rows(const uint8_t* q_rec, float g_q, const float* w, const u
     }
     free(c);
     return macs;
+}
+
+int64_t hsio_score_rows(const uint8_t* q_rec, float g_q, const float* w, const uint8_t* k_rec, float g_k,
+                        const int64_t* rows, int64_t n, float* out, double* tol) {
+    return hsio_score_rows_fmt(FMT_NVFP4, q_rec, g_q, w, k_rec, g_k, rows, n, out, tol);
 }
 
 /* ---------------------------------------------------------------- top-k -- */
@@ -391,11 +474,11 @@ int hsio_pool(const float* scores, int64_t n_vis, int bs, int n_keep, int32_t* b
 /* Reindex scoring restricted to the pool: slot j*bs + r holds the score of
  * position block_ids[j]*bs + r, -inf where that position is not visible and for
  * every slot at or past n_kept*bs, up to n_keep*bs. Returns MACs done. */
-int64_t hsio_score_pool(const uint8_t* q_rec, float g_q, const float* w, const uint8_t* k_rec,
-                        float g_k, int64_t n_vis, const int32_t* block_ids, int32_t n_kept,
-                        int32_t n_keep, int bs, float* pool_scores) {
+int64_t hsio_score_pool_fmt(int fmt, const uint8_t* q_rec, float g_q, const float* w, const uint8_t* k_rec,
+                            float g_k, int64_t n_vis, const int32_t* block_ids, int32_t n_kept,
+                            int32_t n_keep, int bs, float* pool_scores) {
     query_ctx* c = (query_ctx*)malloc(sizeof(query_ctx));
-    query_setup(c, q_rec, g_q, w, g_k);
+    query_setup(c, fmt, q_rec, g_q, w, g_k);
     int64_t macs = 0;
     for (int64_t slot = 0; slot < (int64_t)n_keep * bs; ++slot) {
         int64_t j = slot / bs, r = slot % bs;
@@ -408,6 +491,13 @@ int64_t hsio_score_pool(const uint8_t* q_rec, float g_q, const float* w, const u
     }
     free(c);
     return macs;
+}
+
+int64_t hsio_score_pool(const uint8_t* q_rec, float g_q, const float* w, const uint8_t* k_rec, float g_k,
+                        int64_t n_vis, const int32_t* block_ids, int32_t n_kept, int32_t n_keep, int bs,
+                        float* pool_scores) {
+    return hsio_score_pool_fmt(FMT_NVFP4, q_rec, g_q, w, k_rec, g_k, n_vis, block_ids, n_kept, n_keep, bs,
+                               pool_scores);
 }
 
 /* Top-k inside the pool, reported as global positions: the pool-local top-k of

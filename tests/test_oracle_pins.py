@@ -167,6 +167,156 @@ def test_quantize_zero_tensor():
     assert g == 1.0 and (rec == 0).all()
 
 
+# ----------------------------------------------------------------- MXFP4 --
+
+def test_fp4_format_sizes_match_page_table():
+    for fmt, group, sbits, bpe, per_key in golden_rows("fp4_formats.txt"):
+        group, sbits, bpe, per_key = int(group), int(sbits), float(bpe), int(per_key)
+        assert 4 + sbits / group == bpe
+        x = np.zeros((8, D), dtype=np.uint16)
+        rec = oracle.quantize_mx(x, np.ones(D, dtype=np.int8)) if fmt == "mxfp4" else \
+            oracle.quantize(x, np.ones(D, dtype=np.int8))[0]
+        assert rec.size == 8 * per_key, fmt
+
+
+def test_e8m0_decode_matches_library_all_codes():
+    codes = list(range(256))
+    if hasattr(torch, "float8_e8m0fnu"):
+        ref = torch.tensor(codes, dtype=torch.uint8).view(torch.float8_e8m0fnu).to(torch.float64).tolist()
+    else:  # the OCP MX definition: 2^(b - 127), 0xFF NaN
+        ref = [math.ldexp(1.0, c - 127) if c != 255 else math.nan for c in codes]
+    for c in codes:
+        v = oracle.e8m0_value(c)
+        assert (math.isnan(v) and math.isnan(ref[c])) or v == ref[c], c
+
+
+def test_mx_scale_is_the_smallest_power_of_two_covering_amax_over_6():
+    # closed forms: 6 * 2^e >= amax > 6 * 2^(e-1)
+    assert oracle.mx_scale_exp(6.0) == 0
+    assert oracle.mx_scale_exp(3.0) == -1
+    assert oracle.mx_scale_exp(1.5) == -2
+    assert oracle.mx_scale_exp(float(np.nextafter(np.float32(1.5), np.float32(2)))) == -1
+    assert oracle.mx_scale_exp(0.0) == -127
+    assert oracle.mx_scale_exp(1e-45) == -127
+    assert oracle.mx_scale_exp(float(np.finfo(np.float32).max)) == 126
+    rng = np.random.default_rng(31)
+    for a in np.exp(rng.uniform(-80, 80, 3000)).astype(np.float32):
+        e = oracle.mx_scale_exp(float(a))
+        assert math.ldexp(6.0, e) >= float(a)
+        assert e == -127 or math.ldexp(6.0, e - 1) < float(a)
+
+
+def _bf16(x):
+    b = (np.asarray(x, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    assert (inputs.bf16_to_f32(b) == np.asarray(x, dtype=np.float32)).all()
+    return b
+
+
+def test_quantize_mx_layout_one_hot_rows():
+    # y = H x is one-hot (6 at element e) when x = 6 H[e] / 128 (+-0.046875, exact in bf16),
+    # so element e must decode to 6 with scale 2^0 and every other group to 0 with scale byte 0
+    Hm = scipy.linalg.hadamard(D).astype(np.float64)
+    cases = [(0, 0), (1, 1), (2, 31), (3, 32), (4, 77), (5, 126), (6, 127), (7, 64), (8, 5)]
+    x = np.zeros((len(cases), D))
+    for r, e in cases:
+        x[r] = 6.0 * Hm[e] / D
+    rec = oracle.quantize_mx(_bf16(x), np.ones(D, dtype=np.int8))
+    assert rec.size == 2 * 544
+    want = np.zeros(2 * 544, dtype=np.uint8)
+    for r, e in cases:
+        base = (r // 8) * 544
+        rr = r % 8
+        byte = base + (e // 32) * 128 + rr * 16 + (e % 32) // 2
+        want[byte] |= 7 << (4 * (e & 1))
+        want[base + 512 + rr * 4 + e // 32] = 127
+    assert (rec == want).all()
+    for r, e in cases:
+        d = oracle.decode_row(rec, r, fmt="mxfp4")
+        assert d[e] == 6.0 and np.count_nonzero(d) == 1
+
+
+def test_quantize_mx_constant_rows_closed_form():
+    # x = c e_0 with signs +1 gives y = c in all 128 elements (first Sylvester column)
+    cs = [6.0, -5.0, 1.0, 0.75, -40.0, 0.0]
+    x = np.zeros((len(cs), D))
+    x[:, 0] = cs
+    rec = oracle.quantize_mx(_bf16(x), np.ones(D, dtype=np.int8))
+    # c = 6: scale 1, code 6.0; -5: scale 1, 5 ties between 4 and 6 -> even code (4);
+    # 1: scale 1/4, code 4.0; 0.75: scale 1/8, 6.0; -40: scale 8, 5 -> 4 (tie to even); 0: zeros
+    want = [(127, 6.0), (127, -4.0), (125, 4.0), (124, 6.0), (130, -4.0), (0, 0.0)]
+    for r, (sb, cv) in enumerate(want):
+        d = oracle.decode_row(rec, r, fmt="mxfp4")
+        assert (rec[512 + r * 4: 512 + r * 4 + 4] == sb).all(), r
+        assert (d == cv * math.ldexp(1.0, sb - 127)).all(), r
+
+
+def test_quantize_mx_codes_are_brute_force_nearest():
+    x = _rand_tensor(12, 24)
+    s = inputs.signs(12)
+    rec = oracle.quantize_mx(x, s)
+    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    xf = inputs.bf16_to_f32(x)
+    for r in range(24):
+        y = oracle.fwht128((xf[r] * s).astype(np.float32)).astype(np.float64)
+        d = oracle.decode_row(rec, r, fmt="mxfp4")
+        for grp in range(4):
+            yg = y[32 * grp: 32 * grp + 32]
+            amax = np.abs(yg).max()
+            sc = math.ldexp(1.0, int(rec[(r // 8) * 544 + 512 + (r % 8) * 4 + grp]) - 127)
+            assert 6 * sc >= amax and (amax == 0 or 3 * sc < amax)
+            for t in range(32):
+                a = abs(yg[t]) / sc
+                dist = np.abs(mags - a)
+                best = np.flatnonzero(dist == dist.min())
+                c = best[0] if best.size == 1 else best[best % 2 == 0][0]  # tie: even code
+                assert d[32 * grp + t] == math.copysign(mags[c] * sc, yg[t]) or (mags[c] == 0 and d[32 * grp + t] == 0)
+
+
+def test_quantize_mx_padding_rows_are_zero():
+    rec = oracle.quantize_mx(_rand_tensor(13, 17), inputs.signs(13))
+    assert rec.size == 3 * 544
+    last = rec[2 * 544:].reshape(-1)
+    for rr in range(1, 8):  # row 16 is real; rows 17..23 are padding
+        for e in range(D):
+            assert last[(e // 32) * 128 + rr * 16 + (e % 32) // 2] == 0
+        assert (last[512 + rr * 4: 512 + rr * 4 + 4] == 0).all()
+
+
+def test_score_mx_equals_unrotated_formula_when_quantisation_is_exact():
+    s, qb, qx, kb, kx = _sparse_exact_case(16)
+    qrec = oracle.quantize_mx(qb, s)
+    krec = oracle.quantize_mx(kb, s)
+    w = np.random.default_rng(17).standard_normal(H).astype(np.float32)
+    scores, macs = oracle.score_full(qrec, 1.0, w, krec, 1.0, 50, fmt="mxfp4")
+    ref = np.maximum(kx @ qx.T, 0.0) @ w.astype(np.float64)
+    assert np.allclose(scores, ref, rtol=2e-6, atol=1e-9)
+    assert macs == 50 * 4096
+    rows = np.array([0, 9, 49])
+    part, tol = oracle.score_rows(qrec, 1.0, w, krec, 1.0, rows, fmt="mxfp4")
+    assert (part == scores[rows]).all() and (tol > 0).all()
+
+
+def test_score_mx_tracks_unquantised_formula_and_pool_slots():
+    wl = inputs.workload(0)
+    s = wl.signs()
+    qb, kb = wl.q_bf16(0, 0), wl.k_bf16(0, 0, rows=2000)
+    qrec, krec = oracle.quantize_mx(qb, s), oracle.quantize_mx(kb, s)
+    w = wl.w(0, 0)
+    sc, _ = oracle.score_full(qrec, 1.0, w, krec, 1.0, 2000, fmt="mxfp4")
+    ref = np.maximum(inputs.bf16_to_f32(kb).astype(np.float64) @ inputs.bf16_to_f32(qb).astype(np.float64).T,
+                     0.0) @ w.astype(np.float64)
+    assert np.corrcoef(sc, ref)[0, 1] > 0.95
+    # the scale is carried: same magnitude as the unquantised score (no stray 2^k)
+    assert 0.5 < np.abs(sc).mean() / np.abs(ref).mean() < 2.0
+    ids = np.array([3, 0, 249, 17] + [-1] * 4, dtype=np.int32)
+    ps, _ = oracle.score_pool(qrec, 1.0, w, krec, 1.0, 1997, ids, 4, n_keep=8, fmt="mxfp4")
+    for j, b in enumerate(ids[:4]):
+        for r in range(8):
+            pos = b * 8 + r
+            assert ps[8 * j + r] == (sc[pos] if pos < 1997 else -np.inf)
+    assert np.isneginf(ps[32:]).all()
+
+
 # ------------------------------------------------------------------- score --
 
 def _sparse_exact_case(seed):
