@@ -8,6 +8,8 @@ One step = one pass of the whole path over the resident workload:
                   (blocks of 8, keep 2048, newest pinned, boolean bit table),
                   and per Reindex layer: quantise q, score only the pooled
                   keys (whole 576-byte blocks gathered), exact top-512.
+The headline runs on NVFP4 records (72 B per key); the `mxfp4` object repeats
+the step on MXFP4 records (68 B per key, the pages' own indexer format).
 The default workload is 64 decode queries at 1,048,576 visible keys each with
 4 Reindex layers. K caches are generated from the seeded recipe, quantised on
 the GPU and stay resident (4.83 GB > L2, so no L2 flush is needed).
@@ -40,8 +42,6 @@ import inputs  # noqa: E402
 METRIC = "indexer (query,key) pairs scored/s + top-512/s at 1M ctx; % FP4-TC/HBM roofline"
 UNIT = "pairs/s"
 K_TOP = 512
-REC = 576
-KEY_BYTES = 72  # NVFP4 indexer key: 64 B of E2M1 codes + 8 B of E4M3 scales
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "score_full_decode_b64_n1m.md")
 KERNEL_SOURCES = ["score.cuh", "ptx.cuh", "common.cuh"]
 
@@ -54,6 +54,7 @@ def parse():
     ap.add_argument("--impl", choices=["hsi", "reference"], default="hsi")
     ap.add_argument("--workload", type=int, default=2, help="0..3 (see inputs.workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-mxfp4", action="store_true", help="skip the step on MXFP4 records")
     ap.add_argument("--profile", action="store_true", help="cudaProfilerStart/Stop around the timed steps")
     ap.add_argument("--queries", type=int, default=0, help="use only the first N queries (profiling captures)")
     return ap.parse_args()
@@ -152,11 +153,16 @@ class ClockSampler:
 class DeviceWorkload:
     """The workload resident on one GPU, and one step of the path over it."""
 
-    def __init__(self, wl: inputs.Workload, dev, log):
+    def __init__(self, wl: inputs.Workload, dev, log, fmt: int = 0):
         import torch
 
         import long_context_decode_lightning_gb300 as hsi
         self.torch, self.hsi, self.wl, self.dev = torch, hsi, wl, dev
+        # record format of q and K: NVFP4 (576-byte records, tensor scales) or
+        # MXFP4 (544-byte records, no tensor scales: g_q and g_k stay None)
+        self.fmt = fmt
+        self.mx = fmt == hsi.FMT_MXFP4
+        REC = self.rec = hsi.rec_bytes(fmt)
         B = wl.B
         self.B = B
         self.maxv = max(wl.n_visible)
@@ -185,15 +191,21 @@ class DeviceWorkload:
                 host = stage[j][: n * 128].numpy().view(np.uint16)
                 inputs.normal_bf16(wl.seed, inputs.tensor_id(inputs.KIND_K, layer, s), n * 128, out=host)
                 stage_dev[j][: n * 128].copy_(stage[j][: n * 128], non_blocking=True)
-                hsi.quantize_nvfp4(stage_dev[j][: n * 128].view(n, 128), 1, n, signs, gseq[si:si + 1],
-                                   krec[rec_off[s] * REC:(rec_off[s] + hsi.n_records(n)) * REC], ws=qws)
+                dst = krec[rec_off[s] * REC:(rec_off[s] + hsi.n_records(n)) * REC]
+                if self.mx:
+                    hsi.quantize_mxfp4(stage_dev[j][: n * 128].view(n, 128), 1, n, signs, dst)
+                else:
+                    hsi.quantize_nvfp4(stage_dev[j][: n * 128].view(n, 128), 1, n, signs, gseq[si:si + 1], dst,
+                                       ws=qws)
                 done[j].record()
                 i += 1
             self.k_rec.append(krec)
-            self.g_k.append(torch.stack([gseq[seqs.index(s)] for s in wl.query_seq]).contiguous())
+            self.g_k.append(None if self.mx else
+                            torch.stack([gseq[seqs.index(s)] for s in wl.query_seq]).contiguous())
         torch.cuda.synchronize()
         del stage, stage_dev
-        log(f"K caches generated and quantised in {time.time() - t0:.1f} s ({off * REC * wl.full_layers / 1e9:.2f} GB)")
+        log(f"K caches generated and quantised ({'MXFP4' if self.mx else 'NVFP4'}) in {time.time() - t0:.1f} s "
+            f"({off * REC * wl.full_layers / 1e9:.2f} GB)")
         self.k_off = torch.tensor([rec_off[s] for s in wl.query_seq], dtype=torch.int64, device=dev)
         self.n_vis = torch.tensor(wl.n_visible, dtype=torch.int32, device=dev)
         # --- per-step inputs: bf16 q and fp32 w of every layer, one contiguous buffer
@@ -210,7 +222,7 @@ class DeviceWorkload:
         self.w = self.in_dev[q_host.nbytes:].view(torch.float32).view(L, B, 32)
         # --- outputs and scratch
         self.q_rec = torch.empty(L, B * 4 * REC, dtype=torch.uint8, device=dev)
-        self.g_q = torch.empty(L, B, dtype=torch.float32, device=dev)
+        self.g_q = [None] * L if self.mx else torch.empty(L, B, dtype=torch.float32, device=dev)
         self.scores = torch.empty(B, self.maxv, dtype=torch.float32, device=dev)
         self.bmax = torch.empty(B, hsi.n_records(self.maxv), dtype=torch.float32, device=dev)
         self.out_dev = torch.empty(L * B * K_TOP * 8, dtype=torch.uint8, device=dev)
@@ -234,6 +246,13 @@ class DeviceWorkload:
         self.wl_signs = signs
         self.graphs = []
 
+    def quant_q(self, l):
+        """Quantise layer l's queries (all B) into q_rec[l]."""
+        if self.mx:
+            self.hsi.quantize_mxfp4(self.q[l], self.B, 32, self.wl_signs, self.q_rec[l])
+        else:
+            self.hsi.quantize_nvfp4(self.q[l], self.B, 32, self.wl_signs, self.g_q[l], self.q_rec[l], ws=self.ws_q)
+
     def step(self):
         """One step as individual launches (the same calls the graphs hold)."""
         for _, fn in self.segments():
@@ -246,8 +265,7 @@ class DeviceWorkload:
         signs = self.wl_signs
         segs = []
         for l in range(wl.full_layers):
-            segs.append(("pre", lambda l=l: hsi.quantize_nvfp4(self.q[l], B, 32, signs, self.g_q[l], self.q_rec[l],
-                                                               ws=self.ws_q)))
+            segs.append(("pre", lambda l=l: self.quant_q(l)))
             # the Full layer (scores, top-512, pool) as the fused call, issued as
             # its two phases so that the scoring kernel can be timed alone
             pool = wl.build_pool and l == wl.full_layers - 1
@@ -257,18 +275,18 @@ class DeviceWorkload:
                     self.maxv, self.scores, K_TOP, self.idx[l], self.val[l],
                     block_ids=self.ids if pool else None, n_kept=self.nk if pool else None,
                     n_pool=self.npool if pool else None, pool_bits=self.bits if pool else None,
-                    n_keep=wl.n_keep, ws=self.ws_full, phases=ph)))
+                    n_keep=wl.n_keep, ws=self.ws_full, phases=ph, fmt=self.fmt)))
         if wl.build_pool:
             def rest():
                 # the first Reindex layer gathers the pooled K records and leaves them
                 # compacted; the later layers of the step stream the compacted pool
                 for r in range(wl.reindex_layers):
                     l = wl.full_layers + r
-                    hsi.quantize_nvfp4(self.q[l], B, 32, signs, self.g_q[l], self.q_rec[l], ws=self.ws_q)
+                    self.quant_q(l)
                     hsi.reindex_layer(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0], self.k_off,
                                       self.n_vis, self.ids, self.nk, self.npool, B, self.pool_scores, K_TOP,
                                       self.idx[l], self.val[l], n_keep=wl.n_keep, ws=self.ws_rtopk,
-                                      pool_rec=self.pool_rec, pool_rec_ready=r > 0)
+                                      pool_rec=self.pool_rec, pool_rec_ready=r > 0, fmt=self.fmt)
             segs.append(("post", rest))
         merged = []
         for kind, fn in segs:  # fuse neighbouring non-scoring segments into one graph
@@ -302,19 +320,20 @@ class DeviceWorkload:
         layer = t(lambda: hsi.reindex_layer(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0],
                                             self.k_off, self.n_vis, self.ids, self.nk, self.npool, B,
                                             self.pool_scores, K_TOP, self.idx[l], self.val[l], n_keep=wl.n_keep,
-                                            ws=self.ws_rtopk, pool_rec=self.pool_rec))
+                                            ws=self.ws_rtopk, pool_rec=self.pool_rec, fmt=self.fmt))
         topk = t(lambda: hsi.topk(self.pool_scores, self.npool, B, wl.n_keep * 8, K_TOP, self.idx[l], self.val[l],
                                   block_ids=self.ids, ws=self.ws_rtopk))
         compact = t(lambda: hsi.pool_gather(self.k_rec[0], self.k_off, self.n_vis, self.ids, self.nk, B,
-                                            self.pool_rec, n_keep=wl.n_keep))
+                                            self.pool_rec, n_keep=wl.n_keep, fmt=self.fmt))
         gather = t(lambda: hsi.score_pool(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0],
                                           self.k_off, self.n_vis, self.ids, self.nk, wl.n_keep, B,
-                                          self.pool_scores))
+                                          self.pool_scores, fmt=self.fmt))
         first = t(lambda: hsi.reindex_layer(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0],
                                             self.k_off, self.n_vis, self.ids, self.nk, self.npool, B,
                                             self.pool_scores, K_TOP, self.idx[l], self.val[l], n_keep=wl.n_keep,
-                                            ws=self.ws_rtopk, pool_rec=self.pool_rec, pool_rec_ready=False))
-        pooled_bytes = int(self.nk.clamp(max=wl.n_keep).sum().item()) * REC
+                                            ws=self.ws_rtopk, pool_rec=self.pool_rec, pool_rec_ready=False,
+                                            fmt=self.fmt))
+        pooled_bytes = int(self.nk.clamp(max=wl.n_keep).sum().item()) * self.rec
         return {"layer_us": layer, "first_layer_us": first, "plain_topk_us": topk, "compact_us": compact,
                 "gather_score_us": gather, "pooled_bytes_per_layer": pooled_bytes}
 
@@ -363,11 +382,14 @@ class DeviceWorkload:
         return full + pooled, full, pooled
 
     def score_bytes_per_launch(self):
-        """Algorithmic bytes of one hsi_score_full launch: 72 B per visible key
-        read, 4 B per score and 4 B per block maximum written, q/w/scales read."""
+        """Algorithmic bytes of one hsi_score_full launch: 72 B (NVFP4) or 68 B
+        (MXFP4) per visible key read, 4 B per score and 4 B per block maximum
+        written, q/w/scales read."""
         n = int(sum(self.wl.n_visible))
         nb = sum((v + 7) // 8 for v in self.wl.n_visible)
-        return n * KEY_BYTES + n * 4 + (nb * 4 if self.wl.build_pool else 0) + self.B * (4 * REC + 32 * 4 + 8)
+        key_bytes = self.rec // 8
+        scales = 0 if self.mx else 8
+        return n * key_bytes + n * 4 + (nb * 4 if self.wl.build_pool else 0) + self.B * (4 * self.rec + 32 * 4 + scales)
 
 
 # ----------------------------------------------------------- CPU oracle --
@@ -569,6 +591,29 @@ def main():
             "gather_score_frac": gbs(reindex["gather_score_us"]) / peak,
             "note": "one layer timed alone on the resident pool; fractions of the measured copy bandwidth for "
                     "the pooled bytes (the layer figure includes its selection)"})
+    if not args.no_mxfp4:
+        # the same step on MXFP4 records (its own K caches and queries)
+        Wm = DeviceWorkload(wl, dev, log, fmt=hsi.FMT_MXFP4)
+        Wm.capture()
+        for _ in range(args.warmup):
+            Wm.replay()
+        torch.cuda.synchronize()
+        assert hsi.device_error() == 0, "device error during the MXFP4 warm-up"
+        ms_mx = timed(lambda: Wm.replay(time_score=True), args.steps)
+        assert hsi.device_error() == 0, "device error during the MXFP4 steps"
+        score_mx = float(np.mean([a.elapsed_time(b) for a, b in Wm.ev_score]))
+        bytes_mx = Wm.score_bytes_per_launch()
+        gbs_mx = bytes_mx / (score_mx / 1e3) / 1e9
+        line["mxfp4"] = {
+            "value": job_value(Wm.pairs_per_step()[0], world, args.steps, ms_mx), "unit": UNIT,
+            "ms_per_step": ms_mx / args.steps, "key_bytes": Wm.rec // 8,
+            "roofline": {"bound": "hbm", "achieved": gbs_mx, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                         "frac": gbs_mx / float(peaks["hbm_gbs"]), "traffic": None,
+                         "kernel": "hsi_score_full (score_kernel<1,false> MXFP4)", "bytes_per_launch": bytes_mx,
+                         "ms_per_launch": score_mx},
+            "note": "the same step and workload on MXFP4 records (32-element groups, E8M0 scales); the "
+                    "pool and selections follow from its own scores"}
+        del Wm
     if rank == 0 and not args.no_cpu_baseline:
         nq = cpu_sample_size(wl)
         log(f"cpu baseline: oracle on {nq} queries")

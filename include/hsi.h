@@ -55,6 +55,13 @@ typedef enum {
 #define HSI_DIM 128       /* head dimension d */
 #define HSI_REC_ROWS 8    /* rows per NVFP4 block record */
 #define HSI_REC_BYTES 576 /* bytes per NVFP4 block record: 8 rows x (64 B codes + 8 B scales) */
+#define HSI_MX_REC_BYTES 544 /* bytes per MXFP4 block record: 8 rows x (64 B codes + 4 B scales) */
+
+/* Record format of the indexer q and K (every scoring call takes one). */
+typedef enum {
+    HSI_FMT_NVFP4 = 0, /* 576-byte records, per-16 E4M3 scales, fp32 tensor scale g */
+    HSI_FMT_MXFP4 = 1  /* 544-byte records, per-32 E8M0 scales, no tensor scale */
+} hsi_format;
 
 /*
  * NVFP4 block-record storage, used for indexer queries and indexer K.
@@ -70,6 +77,15 @@ typedef enum {
  * The decoded value is E2M1(code) * E4M3(scale) * g. A query (32 heads) is
  * 4 records; a K cache of n keys is ceil(n/8) records, and its block of
  * positions 8b .. 8b+7 is exactly record b: 8 keys x 72 B = 576 B.
+ *
+ * MXFP4 block records (HSI_FMT_MXFP4), the indexer format the pages describe
+ * ("DeepSeek-V4.1 模型结构（3）", table in section "scale 的格式决定了精度":
+ * groups of 32, E8M0 scales, 4.25 bits per value; 68 B per indexer key in
+ * section "890 字节的分项"): 544 bytes per 8 rows, no tensor scale.
+ *   bytes [0, 512):   E2M1 codes, placed exactly as in NVFP4 records.
+ *   bytes [512, 544): E8M0 scales. The scale of row r, values 32j .. 32j+31,
+ *                     is byte 512 + r*4 + j; its value is 2^(byte - 127).
+ * The decoded value is E2M1(code) * 2^(scale - 127): 8 keys x 68 B = 544 B.
  */
 
 /* ------------------------------------------------------------------------- */
@@ -103,6 +119,27 @@ hsi_status hsi_quantize_nvfp4(const uint16_t* x, int64_t n_tensors, int64_t rows
                               size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Rotate and quantise bf16 rows to MXFP4 block records (no tensor scale).
+ * Page: "DeepSeek-V4.1 模型结构（3）", section "scale 的格式决定了精度" (groups of
+ * 32 with an E8M0 scale, which can only be a power of two: the ideal scale
+ * max|x|/6 rounded up to one); section "E2M1 只能表示 15 个值" (the codes).
+ *
+ * Per row the same rotation as hsi_quantize_nvfp4; per 32 values the scale
+ * 2^e with e the smallest integer in [-127, 127] such that 6 * 2^e >= amax of
+ * the group (e = -127 for an all-zero group), then code = E2M1_RN(y / 2^e),
+ * ties to even, saturating at 6. Inputs must be finite; a non-finite rotated
+ * value is reported as HSI_ERR_DEVICE_ARG by hsi_device_error.
+ *
+ *  x, signs  as for hsi_quantize_nvfp4.
+ *  rec       (dev) out: n_tensors * ceil(rows_per_tensor/8) 544-byte records;
+ *                  tensor t starts at record t * ceil(rows_per_tensor/8).
+ * Errors: INVALID_ARG for null pointers, non-positive sizes, signs not +-1,
+ * unaligned rec (16 B) or x (16 B).
+ */
+hsi_status hsi_quantize_mxfp4(const uint16_t* x, int64_t n_tensors, int64_t rows_per_tensor,
+                              const int8_t* signs, uint8_t* rec, cudaStream_t stream);
+
+/*
  * Lightning-indexer scores of every visible key (a Full layer).
  * Page: "DeepSeek-V4.1 模型结构（3）", section "Reindex 层每个 token 要给 100 万条打分"
  * (the equation); section "用浅层的打分结果限制深层的打分范围" (the Full layer
@@ -130,12 +167,15 @@ hsi_status hsi_quantize_nvfp4(const uint16_t* x, int64_t n_tensors, int64_t rows
  *          consecutive visible scores (block b8 = positions 8*b8 .. 8*b8+7,
  *          invisible positions count as -inf), for the blocks that hold a
  *          visible position. ldb >= ceil(max_visible/8).
+ *  format  HSI_FMT_NVFP4 (576-byte records, g_q and g_k required) or
+ *          HSI_FMT_MXFP4 (544-byte records; g_q and g_k are not read and may
+ *          be NULL: the formula above with g_q = g_k = 1). q and K share it.
  *  ws      may be NULL (0 bytes needed).
  */
 hsi_status hsi_score_full(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
                           const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible,
                           int32_t B, int64_t max_visible, int32_t group, float* scores, int64_t ld,
-                          float* block_max, int64_t ldb, void* ws, size_t ws_bytes,
+                          float* block_max, int64_t ldb, hsi_format format, void* ws, size_t ws_bytes,
                           cudaStream_t stream);
 
 /*
@@ -229,21 +269,24 @@ hsi_status hsi_candidate_pool(const float* scores, int64_t ld, const float* bloc
  * Slot i = 8j + r of query b holds the score of position block_ids[b][j]*8 + r
  * (same formula as hsi_score_full), -inf if that position is not visible.
  * Slots i < 8 * n_kept[b] are written; the rest are left untouched. Each
- * pooled block is one 576-byte K record, fetched whole.
+ * pooled block is one K record (576 or 544 bytes), fetched whole.
  *
  *  block_ids, n_kept: as written by hsi_candidate_pool with block_size 8;
  *          block_ids 16-byte aligned, n_keep a multiple of 32.
  *  pool_scores (dev) fp32 [B][ld], ld >= 8 * n_keep.
+ *  format  as for hsi_score_full.
  *  ws      may be NULL.
  */
 hsi_status hsi_score_pool(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
                           const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible,
                           const int32_t* block_ids, const int32_t* n_kept, int32_t n_keep, int32_t B,
-                          float* pool_scores, int64_t ld, void* ws, size_t ws_bytes, cudaStream_t stream);
+                          float* pool_scores, int64_t ld, hsi_format format, void* ws, size_t ws_bytes,
+                          cudaStream_t stream);
 
 /*
  * Compaction of each query's candidate pool, once per decode step: the pooled
- * 576-byte K records of query b, in block-list order, into one contiguous run,
+ * K records of query b (576 or 544 bytes), in block-list order, into one
+ * contiguous run,
  *   pool_rec[b][i] = the record k_rec_off[b] + block_ids[b][i],  i < min(n_kept[b], n_keep).
  * Records of slots at or past n_kept[b] are left untouched.
  * Page: "DeepSeek-V4.1 模型结构（3）", section "用浅层的打分结果限制深层的打分范围"
@@ -255,13 +298,14 @@ hsi_status hsi_score_pool(const uint8_t* q_rec, const float* g_q, const float* w
  *
  *  k_rec, k_rec_off, n_visible: as for hsi_score_full.
  *  block_ids, n_kept: as written by hsi_candidate_pool (block_size 8).
- *  pool_rec (dev) [B][n_keep][576] bytes, 16-byte aligned; distinct from k_rec.
+ *  pool_rec (dev) [B][n_keep][record bytes], 16-byte aligned; distinct from k_rec.
+ *  format  the records' format (it fixes their size).
  * A block id outside [0, ceil(n_visible[b] / 8)) is skipped and reported as
  * HSI_ERR_DEVICE_ARG by hsi_device_error.
  */
 hsi_status hsi_pool_gather(const uint8_t* k_rec, const int64_t* k_rec_off, const int32_t* n_visible,
                            const int32_t* block_ids, const int32_t* n_kept, int32_t n_keep, int32_t B,
-                           uint8_t* pool_rec, cudaStream_t stream);
+                           uint8_t* pool_rec, hsi_format format, cudaStream_t stream);
 
 /*
  * A decoder Full layer in one call: hsi_score_full, then the top-k of the
@@ -273,8 +317,8 @@ hsi_status hsi_pool_gather(const uint8_t* k_rec, const int64_t* k_rec_off, const
  * (the Full layer scores every visible position, keeps its top-512 and builds
  * the pool from the same scores).
  *
- *  Arguments as in hsi_score_full (group 1), hsi_topk (n_valid = n_visible)
- *  and hsi_candidate_pool (block_size 8). scores [B][ld] is written.
+ *  Arguments as in hsi_score_full (group 1, format), hsi_topk (n_valid =
+ *  n_visible) and hsi_candidate_pool (block_size 8). scores [B][ld] is written.
  *  block_ids NULL: no pool (n_kept, n_pool, pool_bits ignored).
  *  phases  HSI_PHASE_ALL, or the two halves as separate calls with the same
  *          arguments and workspace, scoring first (the workspace carries the
@@ -288,8 +332,8 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
                           const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible, int32_t B,
                           int64_t max_visible, float* scores, int64_t ld, int32_t k, int32_t* top_idx,
                           float* top_val, int32_t n_keep, int32_t* block_ids, int32_t* n_kept, int32_t* n_pool,
-                          uint32_t* pool_bits, int64_t ld_bits, int32_t phases, void* ws, size_t ws_bytes,
-                          cudaStream_t stream);
+                          uint32_t* pool_bits, int64_t ld_bits, int32_t phases, hsi_format format, void* ws,
+                          size_t ws_bytes, cudaStream_t stream);
 
 /*
  * A decoder Reindex layer in one call: the pooled scores (hsi_score_pool),
@@ -299,8 +343,8 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
  * (Reindex layers score only pooled positions and keep their own top-512).
  *
  *  pool_rec, pool_rec_ready: pool_rec NULL: the pooled records are gathered
- *          from k_rec (as by hsi_score_pool). pool_rec (dev, [B][n_keep][576],
- *          16-byte aligned) with pool_rec_ready 0: gathered from k_rec, and
+ *          from k_rec (as by hsi_score_pool). pool_rec (dev, [B][n_keep][record
+ *          bytes], 16-byte aligned) with pool_rec_ready 0: gathered from k_rec, and
  *          also left in pool_rec in the layout hsi_pool_gather writes, so that
  *          the step's later Reindex layers can stream them. pool_rec_ready 1:
  *          pool_rec already holds them (an earlier layer of this pool, or
@@ -308,14 +352,15 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
  *          forms give the same pool_scores, top_idx and top_val.
  *  n_pool (dev) int32 [B] as written by hsi_candidate_pool / hsi_full_layer.
  *  pool_scores [B][ld], ld >= 8 * n_keep, is written (as by hsi_score_pool).
+ *  format  as for hsi_score_full; the pooled records and q share it.
  *  ws      (dev) hsi_workspace_size(HSI_WS_REINDEX_LAYER, B, 8 * n_keep, k).
  */
 hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
                              const float* g_k, const int64_t* k_rec_off, uint8_t* pool_rec, int32_t pool_rec_ready,
                              const int32_t* n_visible, const int32_t* block_ids, const int32_t* n_kept,
                              const int32_t* n_pool, int32_t n_keep, int32_t B, float* pool_scores, int64_t ld,
-                             int32_t k, int32_t* top_idx, float* top_val, void* ws, size_t ws_bytes,
-                             cudaStream_t stream);
+                             int32_t k, int32_t* top_idx, float* top_val, hsi_format format, void* ws,
+                             size_t ws_bytes, cudaStream_t stream);
 
 typedef enum {
     HSI_WS_QUANTIZE = 0,

@@ -20,7 +20,8 @@ _CSRC = os.path.join(_PKG, "csrc")
 _SO = os.path.join(_PKG, "libhsi.so")
 _lib = None
 
-HEADS, DIM, REC_ROWS, REC_BYTES = 32, 128, 8, 576
+HEADS, DIM, REC_ROWS, REC_BYTES, MX_REC_BYTES = 32, 128, 8, 576, 544
+FMT_NVFP4, FMT_MXFP4 = 0, 1  # hsi_format: NVFP4 (576-byte records, tensor scales) or MXFP4 (544 bytes)
 
 STATUS = {0: "HSI_OK", -1: "HSI_ERR_INVALID_ARG", -2: "HSI_ERR_UNSUPPORTED", -3: "HSI_ERR_CUDA",
           -4: "HSI_ERR_DEVICE_TIMEOUT", -5: "HSI_ERR_WORKSPACE", -6: "HSI_ERR_DEVICE_ARG", -7: "HSI_ERR_TOO_LARGE"}
@@ -29,7 +30,7 @@ WS_QUANTIZE, WS_SCORE, WS_TOPK, WS_POOL, WS_FULL_LAYER, WS_REINDEX_LAYER = 0, 1,
 EXPORTS = ["hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
            "hsi_workspace_size", "hsi_device_error", "hsi_device_check", "hsi_status_string",
            "hsi_kernel_launches", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer", "hsi_reindex_layer",
-           "hsi_topk_noalloc", "hsi_debug_set", "hsi_pool_gather"]
+           "hsi_topk_noalloc", "hsi_debug_set", "hsi_pool_gather", "hsi_quantize_mxfp4"]
 
 
 class HsiError(RuntimeError):
@@ -63,15 +64,18 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(_SO)
         vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
         L.hsi_quantize_nvfp4.argtypes = [vp, i64, i64, vp, ctypes.c_int, vp, vp, vp, sz, vp]
-        L.hsi_score_full.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, vp, i64, vp, i64, vp, sz, vp]
+        L.hsi_quantize_mxfp4.argtypes = [vp, i64, i64, vp, vp, vp]
+        L.hsi_score_full.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, vp, i64, vp, i64, ctypes.c_int, vp,
+                                     sz, vp]
         L.hsi_topk.argtypes = [vp, i64, vp, i32, i64, i32, vp, i64, i32, vp, vp, vp, sz, vp]
         L.hsi_candidate_pool.argtypes = [vp, i64, vp, i64, vp, i32, i64, i32, i32, vp, vp, vp, vp, i64, vp, sz, vp]
-        L.hsi_score_pool.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i64, vp, sz, vp]
+        L.hsi_score_pool.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, i64, ctypes.c_int, vp, sz,
+                                     vp]
         L.hsi_full_layer.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, vp, i64, i32, vp, vp, i32, vp, vp, vp,
-                                     vp, i64, i32, vp, sz, vp]
+                                     vp, i64, i32, ctypes.c_int, vp, sz, vp]
         L.hsi_reindex_layer.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, vp, i64, i32, vp,
-                                        vp, vp, sz, vp]
-        L.hsi_pool_gather.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp, vp]
+                                        vp, ctypes.c_int, vp, sz, vp]
+        L.hsi_pool_gather.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp, ctypes.c_int, vp]
         L.hsi_topk_noalloc.argtypes = [vp, i64, vp, i32, i64, i32, vp, i64, i32, vp, vp, vp]
         L.hsi_debug_set.argtypes = [ctypes.c_int, ctypes.c_longlong]
         L.hsi_workspace_size.argtypes = [ctypes.c_int, i32, i64, i32]
@@ -86,7 +90,8 @@ def lib() -> ctypes.CDLL:
         L.hsi_kernel_launches.restype = ctypes.c_uint64
         for name in ("hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
                      "hsi_device_error", "hsi_device_check", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer",
-                     "hsi_reindex_layer", "hsi_topk_noalloc", "hsi_debug_set", "hsi_pool_gather"):
+                     "hsi_reindex_layer", "hsi_topk_noalloc", "hsi_debug_set", "hsi_pool_gather",
+                     "hsi_quantize_mxfp4"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -168,14 +173,25 @@ def quantize_nvfp4(x: torch.Tensor, n_tensors: int, rows_per_tensor: int, signs,
         0 if ws is None else ws.numel(), _stream(stream)))
 
 
+def quantize_mxfp4(x: torch.Tensor, n_tensors: int, rows_per_tensor: int, signs, rec: torch.Tensor, stream=None):
+    """x: bf16 (or its int16 bits) [n_tensors*rows_per_tensor, 128] -> MXFP4 records (no tensor scale)."""
+    s8 = (ctypes.c_int8 * 128)(*[int(v) for v in signs])
+    _check("hsi_quantize_mxfp4", lib().hsi_quantize_mxfp4(
+        _ptr(x), n_tensors, rows_per_tensor, s8, _ptr(rec), _stream(stream)))
+
+
+def rec_bytes(fmt: int = FMT_NVFP4) -> int:
+    return MX_REC_BYTES if fmt == FMT_MXFP4 else REC_BYTES
+
+
 def score_full(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B, max_visible, scores, ld=None,
-               block_max=None, ldb=0, group=1, stream=None):
+               block_max=None, ldb=0, group=1, fmt=FMT_NVFP4, stream=None):
     ld = scores.shape[-1] if ld is None else ld
     if block_max is not None and not ldb:
         ldb = block_max.shape[-1]
     _check("hsi_score_full", lib().hsi_score_full(
         _ptr(q_rec), _ptr(g_q), _ptr(w), _ptr(k_rec), _ptr(g_k), _ptr(k_rec_off), _ptr(n_visible), B,
-        max_visible, group, _ptr(scores), ld, _ptr(block_max), ldb, None, 0, _stream(stream)))
+        max_visible, group, _ptr(scores), ld, _ptr(block_max), ldb, fmt, None, 0, _stream(stream)))
 
 
 def topk(scores, n_valid, B, max_valid, k, out_idx, out_val, ld=None, block_ids=None, ld_blocks=0,
@@ -220,16 +236,16 @@ def candidate_pool(n_visible, B, max_visible, block_ids, n_kept, n_pool, scores=
 
 
 def score_pool(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, block_ids, n_kept, n_keep, B, pool_scores,
-               ld=None, stream=None):
+               ld=None, fmt=FMT_NVFP4, stream=None):
     ld = pool_scores.shape[-1] if ld is None else ld
     _check("hsi_score_pool", lib().hsi_score_pool(
         _ptr(q_rec), _ptr(g_q), _ptr(w), _ptr(k_rec), _ptr(g_k), _ptr(k_rec_off), _ptr(n_visible),
-        _ptr(block_ids), _ptr(n_kept), n_keep, B, _ptr(pool_scores), ld, None, 0, _stream(stream)))
+        _ptr(block_ids), _ptr(n_kept), n_keep, B, _ptr(pool_scores), ld, fmt, None, 0, _stream(stream)))
 
 
 def full_layer(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B, max_visible, scores, k, top_idx, top_val,
                block_ids=None, n_kept=None, n_pool=None, pool_bits=None, n_keep=2048, ld=None, ld_bits=0, ws=None,
-               phases=3, stream=None):
+               phases=3, fmt=FMT_NVFP4, stream=None):
     """Full layer: scores, top-k and (block_ids given) the candidate pool.
     phases: 1 scoring only, 2 selection only (after 1, same workspace), 3 both."""
     ld = scores.shape[-1] if ld is None else ld
@@ -240,18 +256,20 @@ def full_layer(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B, max_visible, 
     _check("hsi_full_layer", lib().hsi_full_layer(
         _ptr(q_rec), _ptr(g_q), _ptr(w), _ptr(k_rec), _ptr(g_k), _ptr(k_rec_off), _ptr(n_visible), B, max_visible,
         _ptr(scores), ld, k, _ptr(top_idx), _ptr(top_val), n_keep, _ptr(block_ids), _ptr(n_kept), _ptr(n_pool),
-        _ptr(pool_bits), ld_bits, phases, _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+        _ptr(pool_bits), ld_bits, phases, fmt, _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
 
 
-def pool_gather(k_rec, k_rec_off, n_visible, block_ids, n_kept, B, pool_rec, n_keep=2048, stream=None):
-    """Compact each query's pooled K records into pool_rec [B][n_keep][576] (block-list order)."""
+def pool_gather(k_rec, k_rec_off, n_visible, block_ids, n_kept, B, pool_rec, n_keep=2048, fmt=FMT_NVFP4,
+                stream=None):
+    """Compact each query's pooled K records into pool_rec [B][n_keep][record bytes] (block-list order)."""
     _check("hsi_pool_gather", lib().hsi_pool_gather(
         _ptr(k_rec), _ptr(k_rec_off), _ptr(n_visible), _ptr(block_ids), _ptr(n_kept), n_keep, B, _ptr(pool_rec),
-        _stream(stream)))
+        fmt, _stream(stream)))
 
 
 def reindex_layer(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, block_ids, n_kept, n_pool, B, pool_scores, k,
-                  top_idx, top_val, n_keep=2048, ld=None, ws=None, pool_rec=None, pool_rec_ready=True, stream=None):
+                  top_idx, top_val, n_keep=2048, ld=None, ws=None, pool_rec=None, pool_rec_ready=True, fmt=FMT_NVFP4,
+                  stream=None):
     """Reindex layer: pooled scores and the top-k inside the pool (global positions).
     pool_rec None: gathered from k_rec. pool_rec with pool_rec_ready: the compacted pool
     (pool_gather, or an earlier layer) is streamed; without: gathered from k_rec and the
@@ -263,5 +281,5 @@ def reindex_layer(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, block_ids, n_
         _ptr(q_rec), _ptr(g_q), _ptr(w), _ptr(k_rec), _ptr(g_k), _ptr(k_rec_off), _ptr(pool_rec),
         1 if pool_rec_ready else 0, _ptr(n_visible),
         _ptr(block_ids),
-        _ptr(n_kept), _ptr(n_pool), n_keep, B, _ptr(pool_scores), ld, k, _ptr(top_idx), _ptr(top_val), _ptr(ws),
-        0 if ws is None else ws.numel(), _stream(stream)))
+        _ptr(n_kept), _ptr(n_pool), n_keep, B, _ptr(pool_scores), ld, k, _ptr(top_idx), _ptr(top_val), fmt,
+        _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))

@@ -204,20 +204,30 @@ SelParams topk_params(const float* scores, int64_t ld, const int32_t* n_valid, i
     return sp;
 }
 
-template <int NQ, bool GATHER, int STAGES, int UT>
-hsi_status launch_score(const ScoreParams& p, cudaStream_t s) {
-    using C = ScoreCfg<NQ, GATHER, STAGES, UT>;
+template <int NQ, bool GATHER, int STAGES, int UT, int FMT>
+hsi_status launch_score_fmt(const ScoreParams& p, cudaStream_t s) {
+    using C = ScoreCfg<NQ, GATHER, STAGES, UT, FMT>;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(score_kernel<NQ, GATHER, STAGES, UT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(score_kernel<NQ, GATHER, STAGES, UT, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::SMEM_BYTES) != cudaSuccess)
             return HSI_ERR_CUDA;
         attr_set = true;
     }
     const int sms = sm_count();
     if (sms <= 0) return HSI_ERR_CUDA;
-    return launch(score_kernel<NQ, GATHER, STAGES, UT>, dim3(sms), dim3(C::THREADS), C::SMEM_BYTES, s, p);
+    return launch(score_kernel<NQ, GATHER, STAGES, UT, FMT>, dim3(sms), dim3(C::THREADS), C::SMEM_BYTES, s, p);
 }
+
+// The scoring kernel for the records' format (checked by the caller).
+template <int NQ, bool GATHER, int STAGES, int UT>
+hsi_status launch_score(const ScoreParams& p, hsi_format fmt, cudaStream_t s) {
+    if (fmt == HSI_FMT_MXFP4) return launch_score_fmt<NQ, GATHER, STAGES, UT, FMT_MXFP4>(p, s);
+    return launch_score_fmt<NQ, GATHER, STAGES, UT, FMT_NVFP4>(p, s);
+}
+
+bool format_ok(hsi_format fmt) { return fmt == HSI_FMT_NVFP4 || fmt == HSI_FMT_MXFP4; }
+int64_t format_rec_bytes(hsi_format fmt) { return fmt == HSI_FMT_MXFP4 ? 544 : 576; }
 
 // ---- fixed scratch of hsi_topk_noalloc ----------------------------------------
 // A caller that cannot allocate device memory still needs somewhere for the
@@ -379,10 +389,32 @@ hsi_status hsi_quantize_nvfp4(const uint16_t* x, int64_t n_tensors, int64_t rows
     return launch(quant_encode_kernel, dim3((unsigned)((prows + 7) / 8)), dim3(256), 0, stream, p);
 }
 
-static hsi_status check_score_common(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
-                                     const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible,
-                                     int32_t B) {
-    if (!q_rec || !g_q || !w || !k_rec || !g_k || !k_rec_off || !n_visible || B <= 0) return HSI_ERR_INVALID_ARG;
+hsi_status hsi_quantize_mxfp4(const uint16_t* x, int64_t n_tensors, int64_t rows_per_tensor, const int8_t* signs,
+                              uint8_t* rec, cudaStream_t stream) {
+    if (!x || !signs || !rec || n_tensors <= 0 || rows_per_tensor <= 0) return HSI_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(rec, 16)) return HSI_ERR_INVALID_ARG;
+    QuantParams p{};
+    p.x = x;
+    p.n_tensors = n_tensors;
+    p.rpt = rows_per_tensor;
+    p.rec_per_tensor = (rows_per_tensor + 7) / 8;
+    for (int d = 0; d < 128; ++d) {
+        if (signs[d] != 1 && signs[d] != -1) return HSI_ERR_INVALID_ARG;
+        if (signs[d] < 0) p.neg_mask[d >> 5] |= 1u << (d & 31);
+    }
+    p.rec = rec;
+    const int64_t prows = n_tensors * p.rec_per_tensor * 8;
+    if ((prows + 7) / 8 > INT32_MAX) return HSI_ERR_INVALID_ARG;
+    return launch(quant_mx_kernel, dim3((unsigned)((prows + 7) / 8)), dim3(256), 0, stream, p);
+}
+
+// Pointers every scoring call needs; the tensor scales only for NVFP4.
+static hsi_status check_score_common(hsi_format fmt, const uint8_t* q_rec, const float* g_q, const float* w,
+                                     const uint8_t* k_rec, const float* g_k, const int64_t* k_rec_off,
+                                     const int32_t* n_visible, int32_t B) {
+    if (!format_ok(fmt)) return HSI_ERR_INVALID_ARG;
+    if (fmt == HSI_FMT_NVFP4 && (!g_q || !g_k)) return HSI_ERR_INVALID_ARG;
+    if (!q_rec || !w || !k_rec || !k_rec_off || !n_visible || B <= 0) return HSI_ERR_INVALID_ARG;
     if (!aligned(q_rec, 16) || !aligned(k_rec, 16) || !aligned(w, 16)) return HSI_ERR_INVALID_ARG;
     return HSI_OK;
 }
@@ -390,10 +422,10 @@ static hsi_status check_score_common(const uint8_t* q_rec, const float* g_q, con
 hsi_status hsi_score_full(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
                           const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible, int32_t B,
                           int64_t max_visible, int32_t group, float* scores, int64_t ld, float* block_max,
-                          int64_t ldb, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                          int64_t ldb, hsi_format format, void* ws, size_t ws_bytes, cudaStream_t stream) {
     (void)ws;
     (void)ws_bytes;
-    hsi_status st = check_score_common(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B);
+    hsi_status st = check_score_common(format, q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B);
     if (st != HSI_OK) return st;
     if (!scores || max_visible < 0 || max_visible > (int64_t)INT32_MAX - 128 || ld < max_visible)
         return HSI_ERR_INVALID_ARG;
@@ -414,17 +446,18 @@ hsi_status hsi_score_full(const uint8_t* q_rec, const float* g_q, const float* w
     p.ld = ld;
     p.bmax = block_max;
     p.ldb = ldb;
-    if (group == 1) return launch_score<1, false, kDecodeStages, kDecodeUT>(p, stream);
-    return launch_score<4, false, kPrefillStages, kPrefillUT>(p, stream);
+    if (group == 1) return launch_score<1, false, kDecodeStages, kDecodeUT>(p, format, stream);
+    return launch_score<4, false, kPrefillStages, kPrefillUT>(p, format, stream);
 }
 
 hsi_status hsi_score_pool(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
                           const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible,
                           const int32_t* block_ids, const int32_t* n_kept, int32_t n_keep, int32_t B,
-                          float* pool_scores, int64_t ld, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                          float* pool_scores, int64_t ld, hsi_format format, void* ws, size_t ws_bytes,
+                          cudaStream_t stream) {
     (void)ws;
     (void)ws_bytes;
-    hsi_status st = check_score_common(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B);
+    hsi_status st = check_score_common(format, q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B);
     if (st != HSI_OK) return st;
     if (!block_ids || !n_kept || !pool_scores || n_keep <= 0 || n_keep > (1 << 20) || n_keep % (16 * kGatherUT) ||
         ld < (int64_t)n_keep * 8 || !aligned(block_ids, 16))
@@ -444,7 +477,7 @@ hsi_status hsi_score_pool(const uint8_t* q_rec, const float* g_q, const float* w
     p.n_keep = n_keep;
     p.pool_scores = pool_scores;
     p.ld_pool = ld;
-    return launch_score<1, true, kGatherStages, kGatherUT>(p, stream);
+    return launch_score<1, true, kGatherStages, kGatherUT>(p, format, stream);
 }
 
 hsi_status hsi_topk(const float* scores, int64_t ld, const int32_t* n_valid, int32_t B, int64_t max_valid, int32_t k,
@@ -590,10 +623,10 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
                           const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible, int32_t B,
                           int64_t max_visible, float* scores, int64_t ld, int32_t k, int32_t* top_idx,
                           float* top_val, int32_t n_keep, int32_t* block_ids, int32_t* n_kept, int32_t* n_pool,
-                          uint32_t* pool_bits, int64_t ld_bits, int32_t phases, void* ws, size_t ws_bytes,
-                          cudaStream_t stream) {
+                          uint32_t* pool_bits, int64_t ld_bits, int32_t phases, hsi_format format, void* ws,
+                          size_t ws_bytes, cudaStream_t stream) {
     if (phases < 1 || phases > 3) return HSI_ERR_INVALID_ARG;
-    hsi_status st = check_score_common(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B);
+    hsi_status st = check_score_common(format, q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B);
     if (st != HSI_OK) return st;
     if (!scores || !top_idx || !top_val || max_visible < 0 || max_visible > (int64_t)INT32_MAX - 256 ||
         ld < max_visible || k < 1 || k > 2048)
@@ -630,7 +663,7 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     p.bmax = pool || big_topk ? bmax : nullptr;
     p.ldb = nb;
     p.key_hist = big_topk ? wsp.hist : nullptr;
-    st = launch_score<1, false, kDecodeStages, kDecodeUT>(p, stream);
+    st = launch_score<1, false, kDecodeStages, kDecodeUT>(p, format, stream);
     if (st != HSI_OK) return st;
     }
     if (!(phases & 2)) return HSI_OK;
@@ -679,29 +712,30 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
 
 hsi_status hsi_pool_gather(const uint8_t* k_rec, const int64_t* k_rec_off, const int32_t* n_visible,
                            const int32_t* block_ids, const int32_t* n_kept, int32_t n_keep, int32_t B,
-                           uint8_t* pool_rec, cudaStream_t stream) {
+                           uint8_t* pool_rec, hsi_format format, cudaStream_t stream) {
     if (!k_rec || !k_rec_off || !n_visible || !block_ids || !n_kept || !pool_rec || B <= 0 || B > 65535 ||
-        n_keep <= 0 || n_keep > (1 << 20) || pool_rec == k_rec)
+        n_keep <= 0 || n_keep > (1 << 20) || pool_rec == k_rec || !format_ok(format))
         return HSI_ERR_INVALID_ARG;
     if (!aligned(k_rec, 16) || !aligned(pool_rec, 16)) return HSI_ERR_INVALID_ARG;
-    const int64_t chunks = (int64_t)n_keep * GATHER_CHUNKS;
+    const int rec_chunks = (int)(format_rec_bytes(format) / 16);
+    const int64_t chunks = (int64_t)n_keep * rec_chunks;
     const dim3 grid((unsigned)((chunks + GATHER_THREADS * GATHER_PER_THREAD - 1) / (GATHER_THREADS * GATHER_PER_THREAD)),
                     (unsigned)B);
     return launch(pool_gather_kernel, grid, dim3(GATHER_THREADS), 0, stream, reinterpret_cast<const uint4*>(k_rec),
-                  k_rec_off, n_visible, block_ids, n_kept, n_keep, reinterpret_cast<uint4*>(pool_rec));
+                  k_rec_off, n_visible, block_ids, n_kept, n_keep, rec_chunks, reinterpret_cast<uint4*>(pool_rec));
 }
 
 hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
                              const float* g_k, const int64_t* k_rec_off, uint8_t* pool_rec, int32_t pool_rec_ready,
                              const int32_t* n_visible, const int32_t* block_ids, const int32_t* n_kept,
                              const int32_t* n_pool, int32_t n_keep, int32_t B, float* pool_scores, int64_t ld,
-                             int32_t k, int32_t* top_idx, float* top_val, void* ws, size_t ws_bytes,
-                             cudaStream_t stream) {
-    if (!n_pool) return HSI_ERR_INVALID_ARG;
+                             int32_t k, int32_t* top_idx, float* top_val, hsi_format format, void* ws,
+                             size_t ws_bytes, cudaStream_t stream) {
+    if (!n_pool || !format_ok(format)) return HSI_ERR_INVALID_ARG;
     hsi_status st;
     if (!pool_rec || !pool_rec_ready) {
         // gather from k_rec (and, with pool_rec, leave the compacted pool there)
-        st = check_score_common(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B);
+        st = check_score_common(format, q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B);
         if (st != HSI_OK) return st;
         if (!block_ids || !n_kept || !pool_scores || n_keep <= 0 || n_keep > (1 << 20) ||
             n_keep % (16 * kGatherUT) || ld < (int64_t)n_keep * 8 || !aligned(block_ids, 16))
@@ -731,7 +765,7 @@ hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float
         p.ld_pool = ld;
         p.key_hist = hist;
         p.pool_out = pool_rec;
-        st = launch_score<1, true, kGatherStages, kGatherUT>(p, stream);
+        st = launch_score<1, true, kGatherStages, kGatherUT>(p, format, stream);
         if (st != HSI_OK) return st;
         SelParams sp = topk_params(pool_scores, ld, n_pool, B, k, block_ids, n_keep, 8, top_idx, top_val, wsp);
         sp.hist = hist;
@@ -741,9 +775,10 @@ hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float
         // the compacted pool is a contiguous scan: query b's keys are its pool
         // slots (n_pool[b] of them visible, the newest block last), its records
         // n_keep apart; slots up to 8 n_kept[b] past the visible ones get -inf
-        if (!q_rec || !g_q || !w || !g_k || !block_ids || !n_kept || B <= 0 || n_keep <= 0 ||
-            n_keep > (1 << 20) || !pool_scores || ld < (int64_t)n_keep * 8)
+        if (!q_rec || !w || !block_ids || !n_kept || B <= 0 || n_keep <= 0 || n_keep > (1 << 20) ||
+            !pool_scores || ld < (int64_t)n_keep * 8)
             return HSI_ERR_INVALID_ARG;
+        if (format == HSI_FMT_NVFP4 && (!g_q || !g_k)) return HSI_ERR_INVALID_ARG;
         if (!aligned(q_rec, 16) || !aligned(pool_rec, 16) || !aligned(w, 16)) return HSI_ERR_INVALID_ARG;
         if (!top_idx || !top_val || k < 1 || k > 2048) return HSI_ERR_INVALID_ARG;
         const int64_t max_valid = (int64_t)n_keep * 8;
@@ -769,7 +804,7 @@ hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float
         p.pad_blocks = n_kept;
         p.n_keep = n_keep;
         p.key_hist = hist;
-        st = launch_score<1, false, kPooledStages, kPooledUT>(p, stream);
+        st = launch_score<1, false, kPooledStages, kPooledUT>(p, format, stream);
         if (st != HSI_OK) return st;
         SelParams sp = topk_params(pool_scores, ld, n_pool, B, k, block_ids, n_keep, 8, top_idx, top_val, wsp);
         sp.hist = hist;

@@ -153,6 +153,28 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+// The same for MXFP4 operands: E2M1 codes with UE8M0 scales, one per 32
+// elements along K (scale_vec::2X: two per row per K = 64 step). The scale ids
+// stay 0: each K step reads bytes 0 and 1 of its scale words.
+__host__ __device__ constexpr uint32_t idesc_mxf4(uint32_t M, uint32_t N) {
+    return (1u << 7)             // A format: E2M1
+           | (1u << 10)          // B format: E2M1
+           | ((N >> 3) << 17)    // N / 8
+           | (1u << 23)          // scale factor type UE8M0
+           | ((M >> 4) << 24);   // M / 16
+}
+
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 async op issued so far by this thread is done.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(

@@ -156,6 +156,60 @@ __global__ void __launch_bounds__(256) quant_encode_kernel(QuantParams p) {
     encode_row_warp(p, t, r, v, r < p.rpt ? p.g[t] : 1.0f);
 }
 
+// ---- MXFP4 (32-element groups, E8M0 scales, no tensor scale) ----------------
+
+// The exponent e of a group's scale 2^e: the smallest e in [-127, 127] with
+// 6 * 2^e >= amax. With amax = m 2^E (m in [1, 2)), 6 * 2^(E-2) = 1.5 * 2^E, so
+// e = E - 2 when m <= 1.5 and E - 1 otherwise; zero and subnormal amax (below
+// 2^-126 < 6 * 2^-127) take e = -127, as does E - 2 = -128.
+__device__ __forceinline__ int mx_scale_exp(float amax) {
+    const uint32_t u = __float_as_uint(amax);
+    const int E = (int)((u >> 23) & 0xFFu);
+    if (E == 0) return -127;
+    const int e = (E - 127) - ((u & 0x7FFFFFu) <= 0x400000u ? 2 : 1);
+    return e < -127 ? -127 : e;
+}
+
+// One warp per padded row of tensor t (grid over n_tensors * rec_per_tensor * 8
+// rows, 8 per CTA) into 544-byte records: rotation as above, then per group
+// (lanes 8j .. 8j+7 hold values 32j .. 32j+31) the scale exponent and the
+// codes E2M1_RN(v 2^-e). The product by 2^-e (a normal fp32 for every e) is
+// exact unless it falls below the normal range, where every value rounds to a
+// zero code of its sign either way. Rows past rpt are zero (codes 0, scale
+// byte 0). A non-finite rotated value is reported through the error word.
+__global__ void __launch_bounds__(256) quant_mx_kernel(QuantParams p) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int64_t prow = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int64_t padded_rows = p.rec_per_tensor * 8;
+    if (prow >= p.n_tensors * padded_rows) return;
+    const int64_t t = prow / padded_rows;
+    const int64_t r = prow % padded_rows;
+    const int lane = threadIdx.x & 31;
+    uint8_t* rec = p.rec + (t * p.rec_per_tensor + r / 8) * 544;
+    const int rr = (int)(r & 7);
+    uint16_t codes = 0;
+    uint8_t sbyte = 0;
+    if (r < p.rpt) {
+        float v[4];
+        rotate_row_warp(p, t * p.rpt + r, v);
+        const bool finite = isfinite(v[0]) && isfinite(v[1]) && isfinite(v[2]) && isfinite(v[3]);
+        if (!__all_sync(0xFFFFFFFFu, finite) && lane == 0) raise_error(DEVERR_ARG);
+        float a = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));  // max over values 32j .. 32j+31
+        const int e = mx_scale_exp(a);
+        const float inv = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
+        codes = (uint16_t)f32x4_to_e2m1x4(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv), __fmul_rn(v[2], inv),
+                                          __fmul_rn(v[3], inv));
+        sbyte = (uint8_t)(e + 127);
+    }
+    // values 4*lane .. 4*lane+3 -> two bytes at (e/32)*128 + rr*16 + (e%32)/2
+    *reinterpret_cast<uint16_t*>(rec + (lane >> 3) * 128 + rr * 16 + (lane & 7) * 2) = codes;
+    if ((lane & 7) == 0) rec[512 + rr * 4 + (lane >> 3)] = sbyte;
+}
+
 // Small tensors (at most QUANT_SMALL_ROWS rows, e.g. the 32 heads of a query):
 // one CTA per tensor rotates every row once, finds the tensor scale (mode 0)
 // and encodes, in a single launch.

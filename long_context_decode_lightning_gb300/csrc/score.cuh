@@ -35,6 +35,12 @@
 // rows of four 8x16-byte core matrices (K-major, no swizzle, core matrices
 // 128 B apart along K, records 576 B apart along M/N).
 //
+// Record formats (template parameter FMT): NVFP4 records are 576 bytes (codes,
+// then per row eight E4M3 scales of 16 elements; one fp32 tensor scale per
+// query and per cache); MXFP4 records are 544 bytes (codes, then per row four
+// E8M0 scales of 32 elements; no tensor scale) and take the MMA's
+// scale_vec::2X form with UE8M0 scales.
+//
 // Work: units of all queries are numbered in order (query group, then key
 // range) and each CTA takes one contiguous range, so it reloads q only when
 // the group changes. Every wait is bounded; on a timeout the CTA records the
@@ -46,7 +52,12 @@
 
 namespace hsi {
 
-constexpr int REC = 576;
+constexpr int REC = 576;  // NVFP4 record bytes
+enum : int { FMT_NVFP4 = 0, FMT_MXFP4 = 1 };
+template <int FMT>
+__host__ __device__ constexpr int rec_bytes() {
+    return FMT == FMT_MXFP4 ? 544 : 576;
+}
 constexpr int TILE_KEYS = 128;
 constexpr int IDS_AHEAD = 8;  // gather: units of block ids prefetched ahead
 #ifndef HSI_GATHER_BULK
@@ -87,8 +98,9 @@ struct ScoreParams {
     uint8_t* pool_out;
 };
 
-template <int NQ, bool GATHER, int STAGES, int UT>
+template <int NQ, bool GATHER, int STAGES, int UT, int FMT>
 struct ScoreCfg {
+    static constexpr int REC = rec_bytes<FMT>();
     static constexpr int N = 32 * NQ;
     static constexpr int UNIT_RECS = 16 * UT;
     static constexpr int UNIT_KEYS = TILE_KEYS * UT;
@@ -326,21 +338,32 @@ __device__ __forceinline__ void cp_async_wait() {
 
 // The scales of rows r, r+32, r+64, r+96 of records at `recs` (nrows valid
 // rows) in the layout of one 32-lane TMEM quarter: column c holds row r+32c,
-// columns 0-3 the first 64 values (K step 0), columns 4-7 the last 64.
+// columns 0-3 the first 64 values (K step 0), columns 4-7 the last 64. NVFP4:
+// a word holds the step's four E4M3 scales. MXFP4: the step's two E8M0 scales
+// in bytes 0 and 1 (the row's scale word, rotated by 16 bits for step 1).
+template <int FMT>
 __device__ __forceinline__ void sf_quarter(const uint8_t* recs, int nrows, int r, uint32_t (&v)[8]) {
+    constexpr int RB = rec_bytes<FMT>();
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         const int m = r + 32 * c;
-        uint2 x = make_uint2(0u, 0u);
-        if (m < nrows) x = *reinterpret_cast<const uint2*>(recs + (m >> 3) * REC + 512 + (m & 7) * 8);
-        v[c] = x.x;
-        v[4 + c] = x.y;
+        if constexpr (FMT == FMT_MXFP4) {
+            uint32_t x = 0u;
+            if (m < nrows) x = *reinterpret_cast<const uint32_t*>(recs + (m >> 3) * RB + 512 + (m & 7) * 4);
+            v[c] = x;
+            v[4 + c] = __funnelshift_l(x, x, 16);
+        } else {
+            uint2 x = make_uint2(0u, 0u);
+            if (m < nrows) x = *reinterpret_cast<const uint2*>(recs + (m >> 3) * RB + 512 + (m & 7) * 8);
+            v[c] = x.x;
+            v[4 + c] = x.y;
+        }
     }
 }
 
-template <int NQ, bool GATHER, int STAGES, int UT>
-__global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) score_kernel(ScoreParams p) {
-    using C = ScoreCfg<NQ, GATHER, STAGES, UT>;
+template <int NQ, bool GATHER, int STAGES, int UT, int FMT>
+__global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS, 1) score_kernel(ScoreParams p) {
+    using C = ScoreCfg<NQ, GATHER, STAGES, UT, FMT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem + C::OFF_STAGES;
@@ -458,7 +481,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                     if (!wait_traced(&q_empty[slot], ((gc >> 1) & 1) ^ 1, sh, tr, TR_PROD_QEMPTY)) break;
                     if (lane == 0) {
                         mbar_arrive_expect_tx(&q_full[slot], C::Q_BYTES);
-                        bulk_g2s(qslots + slot * C::QSLOT_BYTES, p.q_rec + (int64_t)g * NQ * 4 * REC, C::Q_BYTES,
+                        bulk_g2s(qslots + slot * C::QSLOT_BYTES, p.q_rec + (int64_t)g * NQ * 4 * C::REC, C::Q_BYTES,
                                  &q_full[slot]);
                     }
                     last_q_gc[slot] = gc;
@@ -475,8 +498,8 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                 const int nrec = (int)min((int64_t)C::UNIT_RECS, nrec_all - (int64_t)t * C::UNIT_RECS);
                 const bool skip = u == 0 && *(volatile int*)&g_hsi_skip_first_copy;  // diagnostics only
                 if (lane == 0 && !skip) {
-                    mbar_arrive_expect_tx(&full[st.i], (uint32_t)(nrec * REC));
-                    bulk_g2s(dst, p.k_rec + (k_base + (int64_t)t * C::UNIT_RECS) * REC, (uint32_t)(nrec * REC),
+                    mbar_arrive_expect_tx(&full[st.i], (uint32_t)(nrec * C::REC));
+                    bulk_g2s(dst, p.k_rec + (k_base + (int64_t)t * C::UNIT_RECS) * C::REC, (uint32_t)(nrec * C::REC),
                              &full[st.i]);
                 }
             } else if constexpr (C::GBULK) {
@@ -498,13 +521,13 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&ids_free[islot]);
-                    mbar_arrive_expect_tx(&full[st.i], nvalid * REC);
+                    mbar_arrive_expect_tx(&full[st.i], nvalid * C::REC);
                 }
                 __syncwarp();
 #pragma unroll
                 for (int i = 0; i < PER; ++i)
                     if (ok_l[i])
-                        bulk_g2s(dst + (lane + 32 * i) * REC, p.k_rec + (k_base + ids_l[i]) * REC, REC, &full[st.i]);
+                        bulk_g2s(dst + (lane + 32 * i) * C::REC, p.k_rec + (k_base + ids_l[i]) * C::REC, C::REC, &full[st.i]);
                 if (fetched < count) {
                     if (u >= 1) {
                         const int prev = (int)((u - 1) % IDS_AHEAD);
@@ -516,7 +539,8 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                     fetch_ids();
                 }
             } else {
-                // 4 threads per pooled block, 9 x 16 bytes each (576 B per block)
+                // 4 threads per pooled block, up to 9 x 16 bytes each (36 chunks of an
+                // NVFP4 record, 34 of an MXFP4 one)
                 const int islot = (int)(u % IDS_AHEAD);
                 const int blk = threadIdx.x >> 2, prt = threadIdx.x & 3;
                 const int j = t * C::UNIT_RECS + blk;
@@ -526,10 +550,12 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                 const bool ok = j < nk && id >= 0 && id < nrec_all;
                 if (j < nk && !ok && prt == 0) raise_error(DEVERR_ARG);
                 if (ok) {
-                    const uint8_t* src = p.k_rec + (k_base + id) * REC;
-                    uint8_t* d = dst + blk * REC;
+                    const uint8_t* src = p.k_rec + (k_base + id) * C::REC;
+                    uint8_t* d = dst + blk * C::REC;
+                    constexpr int CH = C::REC / 16;
 #pragma unroll
-                    for (int c = 0; c < 9; ++c) cp_async16(d + (c * 4 + prt) * 16, src + (c * 4 + prt) * 16);
+                    for (int c = 0; c < 9; ++c)
+                        if (c * 4 + prt < CH) cp_async16(d + (c * 4 + prt) * 16, src + (c * 4 + prt) * 16);
                 }
                 cp_async_commit();
                 // refill the id slot of the previous unit once every producer warp has read it
@@ -586,7 +612,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
             UnitIter<NQ, GATHER, UT> it;
             it.init(p, sh);
             int cur_g = -1, gc = -1;
-            constexpr uint32_t idesc = idesc_nvf4(128, C::N);
+            constexpr uint32_t idesc = FMT == FMT_MXFP4 ? idesc_mxf4(128, C::N) : idesc_nvf4(128, C::N);
             Ring st, ac;
             for (long long u = 0; u < count; ++u) {
                 if (it.g != cur_g) {
@@ -611,11 +637,14 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                     tc_fence_after();
                     const uint32_t d = tmem + C::COL_ACC + (ac.i * UT + sub) * C::N;
                     const uint32_t sfa = tmem + C::COL_SFA + (st.i * UT + sub) * 8;
-                    const uint32_t at = a0 + sub * 16 * REC;
+                    const uint32_t at = a0 + sub * 16 * C::REC;
 #pragma unroll
-                    for (int kk = 0; kk < 2; ++kk)
-                        mma_nvf4(d, smem_desc(at + kk * 256, 128, REC), smem_desc(b0 + kk * 256, 128, REC), idesc,
-                                 sfa + kk * 4, sfb + kk * 4, kk);
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const uint64_t ad = smem_desc(at + kk * 256, 128, C::REC);
+                        const uint64_t bd = smem_desc(b0 + kk * 256, 128, C::REC);
+                        if constexpr (FMT == FMT_MXFP4) mma_mxf4(d, ad, bd, idesc, sfa + kk * 4, sfb + kk * 4, kk);
+                        else mma_nvf4(d, ad, bd, idesc, sfa + kk * 4, sfb + kk * 4, kk);
+                    }
                 }
                 if (stop) break;
                 // one commit: the epilogue that sees it also frees the stage
@@ -644,7 +673,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                 const int slot = gc & 1;
                 if (!wait_traced(&q_full[slot], (gc >> 1) & 1, sh, tr, TR_SF_QFULL)) break;
                 uint32_t v[8];
-                sf_quarter(qslots + slot * C::QSLOT_BYTES, C::N, lane, v);
+                sf_quarter<FMT>(qslots + slot * C::QSLOT_BYTES, C::N, lane, v);
                 tmem_st8_wait(tmem + lane_base + C::COL_SFB + slot * 8, v);
                 tc_fence_before();
                 __syncwarp();
@@ -660,8 +689,8 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                 const int nk = min(p.n_kept[it.g], p.n_keep);
                 const int nrec = min(C::UNIT_RECS, nk - it.t * C::UNIT_RECS);
                 if (nrec > 0) {
-                    bulk_s2g(p.pool_out + ((int64_t)it.g * p.n_keep + (int64_t)it.t * C::UNIT_RECS) * REC, st_recs,
-                             (uint32_t)(nrec * REC));
+                    bulk_s2g(p.pool_out + ((int64_t)it.g * p.n_keep + (int64_t)it.t * C::UNIT_RECS) * C::REC, st_recs,
+                             (uint32_t)(nrec * C::REC));
                     bulk_commit();
                     bulk_wait_read_all();
                 }
@@ -669,7 +698,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
 #pragma unroll
             for (int sub = 0; sub < UT; ++sub) {
                 uint32_t v[8];
-                sf_quarter(st_recs + sub * 16 * REC, TILE_KEYS, lane, v);
+                sf_quarter<FMT>(st_recs + sub * 16 * C::REC, TILE_KEYS, lane, v);
                 tmem_st8_wait(tmem + lane_base + C::COL_SFA + (st.i * UT + sub) * 8, v);
             }
             tc_fence_before();
@@ -719,7 +748,8 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT>::THREADS, 1) 
                     const int b = g * NQ + qi;
                     nv[qi] = p.n_vis[b];
                     npad[qi] = p.pad_blocks ? 8 * min(p.pad_blocks[b], p.n_keep) : 0;
-                    const float sc = p.g_q[b] * p.g_k[b] * 0.0078125f;
+                    // the 2^-7 of the two unnormalised rotations; NVFP4 also its tensor scales
+                    const float sc = (FMT == FMT_MXFP4 ? 1.0f : p.g_q[b] * p.g_k[b]) * 0.0078125f;
                     if constexpr (NQ == 1) {
                         const float4* wv = reinterpret_cast<const float4*>(p.w + (int64_t)b * 32);
 #pragma unroll

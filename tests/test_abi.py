@@ -68,10 +68,18 @@ def test_host_validation_rejects_bad_arguments(L):
     assert L.hsi_quantize_nvfp4(fake, 1, 1, s8, 0, fake, fake, None, 0, None) == -5
     # score_full: group 3 unsupported, ld too small, B not a multiple of the group
     args = [fake] * 7
-    assert L.hsi_score_full(*args, 1, 100, 3, fake, 100, None, 0, None, 0, None) == -2
-    assert L.hsi_score_full(*args, 1, 100, 1, fake, 99, None, 0, None, 0, None) == -1
-    assert L.hsi_score_full(*args, 6, 100, 4, fake, 100, None, 0, None, 0, None) == -1
-    assert L.hsi_score_full(*args, 1, 100, 1, fake, 100, fake, 12, None, 0, None) == -1
+    assert L.hsi_score_full(*args, 1, 100, 3, fake, 100, None, 0, 0, None, 0, None) == -2
+    assert L.hsi_score_full(*args, 1, 100, 1, fake, 99, None, 0, 0, None, 0, None) == -1
+    assert L.hsi_score_full(*args, 6, 100, 4, fake, 100, None, 0, 0, None, 0, None) == -1
+    assert L.hsi_score_full(*args, 1, 100, 1, fake, 100, fake, 12, 0, None, 0, None) == -1
+    # record format: unknown format; NVFP4 needs its tensor scales (MXFP4 has none)
+    assert L.hsi_score_full(*args, 1, 100, 1, fake, 100, None, 0, 2, None, 0, None) == -1
+    assert L.hsi_score_full(fake, None, *[fake] * 5, 1, 100, 1, fake, 100, None, 0, 0, None, 0, None) == -1
+    assert L.hsi_pool_gather(fake, fake, fake, fake, fake, 2048, 1, fake + 4096, 3, None) == -1
+    # quantize_mxfp4: null x, bad signs, unaligned records
+    assert L.hsi_quantize_mxfp4(None, 1, 1, s8, fake, None) == -1
+    assert L.hsi_quantize_mxfp4(fake, 1, 1, bad_signs, fake, None) == -1
+    assert L.hsi_quantize_mxfp4(fake, 1, 1, s8, fake + 8, None) == -1
     # topk: k out of range, workspace missing for a long row
     assert L.hsi_topk(fake, 10, fake, 1, 10, 0, None, 0, 8, fake, fake, None, 0, None) == -1
     assert L.hsi_topk(fake, 10, fake, 1, 10, 4096, None, 0, 8, fake, fake, None, 0, None) == -1
@@ -84,4 +92,4 @@ def test_host_validation_rejects_bad_arguments(L):
     assert L.hsi_candidate_pool(None, 0, fake, 100, fake, 1, 100, 4, 16, fake, fake, fake, None, 0, fake, 1 << 20,
                                 None) == -1
     # score_pool: ld shorter than 8 * n_keep
-    assert L.hsi_score_pool(*args, fake, fake, 2048, 1, fake, 2048 * 8 - 1, None, 0, None) == -1
+    assert L.hsi_score_pool(*args, fake, fake, 2048, 1, fake, 2048 * 8 - 1, 0, None, 0, None) == -1

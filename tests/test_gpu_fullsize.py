@@ -36,22 +36,28 @@ def _near_tie_ok(gpu_idx, ora_scores, ora_idx, tol):
 
 
 def _check_query(wl, W, b, full_layer_of_scores):
-    """Checks for one decode query of a resident workload."""
+    """Checks for one decode query of a resident workload (either record format)."""
     signs = wl.signs()
     s = wl.query_seq[b]
     n = wl.n_visible[b]
     off = int(W.k_off[b].item())
     rng = np.random.default_rng(b)
+    R, fmt = W.rec, ("mxfp4" if W.mx else "nvfp4")
+
+    def quant(x):
+        return (oracle.quantize_mx(x, signs), 1.0) if W.mx else oracle.quantize(x, signs)
+
     for l in range(wl.full_layers):
-        krec, gk = oracle.quantize(wl.k_bf16(l, s), signs)
-        got = W.k_rec[l][off * 576:(off + len(krec) // 576) * 576].cpu().numpy()
+        krec, gk = quant(wl.k_bf16(l, s))
+        got = W.k_rec[l][off * R:(off + len(krec) // R) * R].cpu().numpy()
         assert np.array_equal(got, krec), f"K records of sequence {s}, layer {l}"
-        assert np.float32(gk) == W.g_k[l][b].item()
-        qrec, gq = oracle.quantize(wl.q_bf16(l, b), signs)
-        assert np.array_equal(W.q_rec[l][b * 2304:(b + 1) * 2304].cpu().numpy(), qrec)
+        if not W.mx:
+            assert np.float32(gk) == W.g_k[l][b].item()
+        qrec, gq = quant(wl.q_bf16(l, b))
+        assert np.array_equal(W.q_rec[l][b * 4 * R:(b + 1) * 4 * R].cpu().numpy(), qrec)
         w = wl.w(l, b)
-        so, _ = oracle.score_full(qrec, gq, w, krec, gk, n)
-        _, tol = oracle.score_rows(qrec, gq, w, krec, gk, np.arange(n))
+        so, _ = oracle.score_full(qrec, gq, w, krec, gk, n, fmt=fmt)
+        _, tol = oracle.score_rows(qrec, gq, w, krec, gk, np.arange(n), fmt=fmt)
         gi = W.idx[l][b].cpu().numpy()
         oi, _ = oracle.topk(so, n, 512)
         _near_tie_ok(gi, so, oi, tol)
@@ -69,17 +75,17 @@ def _check_query(wl, W, b, full_layer_of_scores):
                 gm = ((bits[np.arange(n) // 32] >> (np.arange(n) % 32)) & 1).astype(np.uint8)
                 assert np.array_equal(gm, mask)
     if wl.build_pool:
-        krec, gk = oracle.quantize(wl.k_bf16(0, s), signs)
+        krec, gk = quant(wl.k_bf16(0, s))
         ids = W.ids[b].cpu().numpy()
         nk, npool = int(W.nk[b]), int(W.npool[b])
         for r in range(wl.reindex_layers):
             l = wl.full_layers + r
-            qrec, gq = oracle.quantize(wl.q_bf16(l, b), signs)
-            assert np.array_equal(W.q_rec[l][b * 2304:(b + 1) * 2304].cpu().numpy(), qrec)
+            qrec, gq = quant(wl.q_bf16(l, b))
+            assert np.array_equal(W.q_rec[l][b * 4 * R:(b + 1) * 4 * R].cpu().numpy(), qrec)
             w = wl.w(l, b)
-            po, _ = oracle.score_pool(qrec, gq, w, krec, gk, n, ids, nk)
+            po, _ = oracle.score_pool(qrec, gq, w, krec, gk, n, ids, nk, fmt=fmt)
             posn = np.array([ids[i // 8] * 8 + i % 8 for i in range(npool)])
-            _, tolp = oracle.score_rows(qrec, gq, w, krec, gk, posn)
+            _, tolp = oracle.score_rows(qrec, gq, w, krec, gk, posn, fmt=fmt)
             oi, _ = oracle.topk_pool(po, npool, ids)
             gi = W.idx[l][b].cpu().numpy()
             # positions: compare through the pooled slots' oracle scores
@@ -95,9 +101,9 @@ def _check_query(wl, W, b, full_layer_of_scores):
                 assert np.array_equal(gi, ti)
 
 
-def _resident(idx):
+def _resident(idx, fmt=hsi.FMT_NVFP4):
     wl = inputs.workload(idx)
-    W = bench.DeviceWorkload(wl, torch.device("cuda"), lambda m: None)
+    W = bench.DeviceWorkload(wl, torch.device("cuda"), lambda m: None, fmt=fmt)
     W.capture()
     W.replay()
     W.replay()
@@ -109,6 +115,13 @@ def _resident(idx):
 def test_fullsize_decode_b64_n1m():
     wl, W = _resident(2)
     samples = [0, 37, 63]
+    oracle.map_queries(lambda b: _check_query(wl, W, b, 0), samples, threads=len(samples))
+
+
+def test_fullsize_decode_b64_n1m_mxfp4():
+    """The benchmark's MXFP4 step (68-byte keys) at full size, sampled queries."""
+    wl, W = _resident(2, fmt=hsi.FMT_MXFP4)
+    samples = [1, 42]
     oracle.map_queries(lambda b: _check_query(wl, W, b, 0), samples, threads=len(samples))
 
 
