@@ -42,7 +42,8 @@ import inputs  # noqa: E402
 METRIC = "indexer (query,key) pairs scored/s + top-512/s at 1M ctx; % FP4-TC/HBM roofline"
 UNIT = "pairs/s"
 K_TOP = 512
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "score_full_decode_b64_n1m.md")
+PROFILE_SUMMARY = {"nvfp4": os.path.join(ROOT, "profiles", "score_full_decode_b64_n1m.md"),
+                   "mxfp4": os.path.join(ROOT, "profiles", "score_full_mxfp4_decode_b64_n1m.md")}
 KERNEL_SOURCES = ["score.cuh", "ptx.cuh", "common.cuh"]
 
 
@@ -54,7 +55,9 @@ def parse():
     ap.add_argument("--impl", choices=["hsi", "reference"], default="hsi")
     ap.add_argument("--workload", type=int, default=2, help="0..3 (see inputs.workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-mxfp4", action="store_true", help="skip the step on MXFP4 records")
+    ap.add_argument("--format", choices=["nvfp4", "mxfp4"], default="nvfp4",
+                    help="record format of the headline step")
+    ap.add_argument("--no-mxfp4", action="store_true", help="skip the extra step on MXFP4 records")
     ap.add_argument("--profile", action="store_true", help="cudaProfilerStart/Stop around the timed steps")
     ap.add_argument("--queries", type=int, default=0, help="use only the first N queries (profiling captures)")
     return ap.parse_args()
@@ -70,11 +73,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """dram bytes per launch of the scoring kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
+def recorded_traffic(fmt: str = "nvfp4"):
+    """dram bytes per launch of the scoring kernel (records of format fmt) from
+    the committed ncu summary, if it was taken on the current kernel source."""
     try:
-        txt = open(PROFILE_SUMMARY).read()
+        txt = open(PROFILE_SUMMARY[fmt]).read()
     except OSError:
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
@@ -513,7 +516,8 @@ def main():
     if world > 1:
         dist.barrier()
     hsi.device_check()
-    W = DeviceWorkload(wl, dev, log)
+    fmt = hsi.FMT_MXFP4 if args.format == "mxfp4" else hsi.FMT_NVFP4
+    W = DeviceWorkload(wl, dev, log, fmt=fmt)
     l0 = hsi.kernel_launches()
     W.step()
     torch.cuda.synchronize()
@@ -563,17 +567,19 @@ def main():
     peaks, peak_kind = measured_peaks()
     bytes_launch = W.score_bytes_per_launch()
     achieved = bytes_launch / (score_ms / 1e3) / 1e9
-    traffic = recorded_traffic()
+    traffic = recorded_traffic(args.format)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, e4m3 block scales, fp32 accumulate)",
+        "vs_baseline": None,
+        "dtype": "mxfp4 (e2m1 x e2m1, e8m0 block scales, fp32 accumulate)" if W.mx else
+                 "nvfp4 (e2m1 x e2m1, e4m3 block scales, fp32 accumulate)",
         "data": "synthetic", "config": config,
         "top512_selections_per_s": sel,
         "pairs_per_step": {"full": pairs_full, "pooled": pairs_pool},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                      "frac": achieved / float(peaks["hbm_gbs"]), "traffic": traffic,
-                     "kernel": "hsi_score_full (score_kernel<1,false>)",
+                     "kernel": f"hsi_score_full (score_kernel<1,false> {args.format.upper()})",
                      "bytes_per_launch": bytes_launch, "ms_per_launch": score_ms,
                      "peak_kind": f"{peak_kind} copy bandwidth"},
         "e2e": {"value": value_e2e, "unit": UNIT, "h2d_bytes_per_step": int(W.in_host.numel()),
@@ -591,7 +597,7 @@ def main():
             "gather_score_frac": gbs(reindex["gather_score_us"]) / peak,
             "note": "one layer timed alone on the resident pool; fractions of the measured copy bandwidth for "
                     "the pooled bytes (the layer figure includes its selection)"})
-    if not args.no_mxfp4:
+    if not args.no_mxfp4 and not W.mx:
         # the same step on MXFP4 records (its own K caches and queries)
         Wm = DeviceWorkload(wl, dev, log, fmt=hsi.FMT_MXFP4)
         Wm.capture()
@@ -608,7 +614,7 @@ def main():
             "value": job_value(Wm.pairs_per_step()[0], world, args.steps, ms_mx), "unit": UNIT,
             "ms_per_step": ms_mx / args.steps, "key_bytes": Wm.rec // 8,
             "roofline": {"bound": "hbm", "achieved": gbs_mx, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
-                         "frac": gbs_mx / float(peaks["hbm_gbs"]), "traffic": None,
+                         "frac": gbs_mx / float(peaks["hbm_gbs"]), "traffic": recorded_traffic("mxfp4"),
                          "kernel": "hsi_score_full (score_kernel<1,false> MXFP4)", "bytes_per_launch": bytes_mx,
                          "ms_per_launch": score_mx},
             "note": "the same step and workload on MXFP4 records (32-element groups, E8M0 scales); the "
