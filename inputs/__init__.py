@@ -29,7 +29,8 @@ _lib = None
 H = 32  # indexer heads
 D = 128  # head dimension
 
-KIND_Q, KIND_K, KIND_W, KIND_LEN, KIND_SIGNS = 1, 2, 3, 4, 5
+KIND_Q, KIND_K, KIND_W, KIND_LEN, KIND_SIGNS, KIND_KV = 1, 2, 3, 4, 5, 6
+DKV = 512  # main-KV entry width
 
 
 def build(force: bool = False) -> str:
@@ -147,6 +148,14 @@ class Workload:
         rows = n - first_row if rows is None else rows
         a = normal_bf16(self.seed, tensor_id(KIND_K, layer, seq), rows * D, 1.0, first_row * D)
         return a.reshape(rows, D)
+
+    def kv_bf16(self, seq: int, first_row: int = 0, rows: int | None = None) -> np.ndarray:
+        """bf16 bits [rows][512] of the main-KV cache of sequence ``seq`` (N(0, 1):
+        entries after an RMSNorm with unit weights have unit RMS)."""
+        n = self.seq_len[seq]
+        rows = n - first_row if rows is None else rows
+        a = normal_bf16(self.seed, tensor_id(KIND_KV, 0, seq), rows * DKV, 1.0, first_row * DKV)
+        return a.reshape(rows, DKV)
 
     def q_bf16(self, layer: int, query: int) -> np.ndarray:
         """bf16 bits [32][128] of the indexer query of ``query`` at ``layer``.

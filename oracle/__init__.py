@@ -78,6 +78,12 @@ def lib():
         L.hsio_score_pool_fmt.argtypes = [i32, vp, f32, vp, vp, f32, i64, vp, ctypes.c_int32, ctypes.c_int32,
                                           i32, vp]
         L.hsio_score_pool_fmt.restype = i64
+        L.hsio_mainkv_quantize.argtypes = [vp, i64, vp]
+        L.hsio_mainkv_quantize.restype = i32
+        L.hsio_mainkv_decode.argtypes = [vp, i64, vp]
+        L.hsio_mainkv_decode.restype = None
+        L.hsio_mainkv_gather.argtypes = [vp, i64, vp, i32, vp]
+        L.hsio_mainkv_gather.restype = i32
         L.hsio_topk.argtypes = [vp, i64, i32, vp, vp]
         L.hsio_topk.restype = i64
         L.hsio_pool.argtypes = [vp, i64, i32, i32, vp, vp, vp, vp]
@@ -175,6 +181,36 @@ def decode_row(records: np.ndarray, row: int, g: float = 1.0, fmt: str = "nvfp4"
 
 def decode_rows(records: np.ndarray, rows: int, g: float = 1.0, fmt: str = "nvfp4") -> np.ndarray:
     return np.stack([decode_row(records, r, g, fmt) for r in range(rows)])
+
+
+# --------------------------------------------------------------- main KV ----
+
+KV_DIM, KV_BYTES = 512, 288
+
+
+def mainkv_quantize(x_bf16: np.ndarray) -> np.ndarray:
+    """bf16 bits [n][512] -> FP4 main-KV entries uint8 [n*288] (E2M1, E4M3 per 16, no global scale)."""
+    x = _c(x_bf16, np.uint16).reshape(-1, KV_DIM)
+    kv = np.empty(x.shape[0] * KV_BYTES, dtype=np.uint8)
+    if lib().hsio_mainkv_quantize(_p(x), x.shape[0], _p(kv)) != 0:
+        raise ValueError("oracle mainkv_quantize: non-finite input")
+    return kv
+
+
+def mainkv_decode(kv: np.ndarray, i: int) -> np.ndarray:
+    out = np.empty(KV_DIM, dtype=np.float64)
+    lib().hsio_mainkv_decode(_p(kv), i, _p(out))
+    return out
+
+
+def mainkv_gather(kv: np.ndarray, n_vis: int, idx: np.ndarray) -> np.ndarray:
+    """gather(main_kv, topk) for one query -> bf16 bits [k][512] (zeros for idx < 0)."""
+    idx = _c(idx, np.int32)
+    out = np.empty((idx.size, KV_DIM), dtype=np.uint16)
+    rc = lib().hsio_mainkv_gather(_p(kv), n_vis, _p(idx), idx.size, _p(out))
+    if rc != 0:
+        raise ValueError(f"oracle mainkv_gather: status {rc}")
+    return out
 
 
 # ----------------------------------------------------------------- score ----

@@ -45,6 +45,17 @@
  *    for an all-zero group), and code = E2M1_RN(y / 2^e), saturating at +-6.
  *    The score is the same sum with g_q = g_k = 1.
  *
+ *  - Main KV for core attention ([J] "scale 的格式决定了精度": groups of 16 with
+ *    an E4M3 scale, the NVFP4 layout without its second, global scale; 512
+ *    values = 256 B of codes + 32 B of scales = 288 B; [J] "官方的参考实现里"
+ *    and [P] section 5.1: dequantised before attention; the gather of the
+ *    selected positions is the pseudocode's gather(main_kv, topk)). Per 16
+ *    values: s = E4M3_RN(amax/6) (division in fp32), code = E2M1_RN(x / s)
+ *    (0 when s decodes to 0), no rotation (the Hadamard rotation belongs to
+ *    the indexer). An entry is stored whole: code of value i in byte i/2 (low
+ *    nibble for even i), the scale of values 16g .. 16g+15 in byte 256 + g.
+ *    Decoded values E2M1 * E4M3 are exact in bf16, which the gather returns.
+ *
  * Storage formats decoded here (the product's "block records"): rows are
  * grouped 8 to a record. In record R (rows 8R .. 8R+7), element e of row r has
  * its 4-bit code in byte (e/32)*128 + r*16 + (e%32)/2, low nibble for even e.
@@ -292,6 +303,71 @@ int hsio_quantize_mx(const uint16_t* x, int64_t rows, const int8_t* signs, uint8
                 int el = grp * 32 + t;
                 rec_put_code(rec, r, el, e2m1_encode_d(ldexp((double)y[el], -e)));
             }
+        }
+    }
+    return 0;
+}
+
+/* -------------------------------------------------------------- main KV -- */
+
+#define KV_DIM 512
+#define KV_BYTES 288
+
+/* Quantise n bf16 main-KV entries of 512 values into 288-byte entries.
+ * Returns 0, or -1 on a non-finite input. */
+int hsio_mainkv_quantize(const uint16_t* x, int64_t n, uint8_t* kv) {
+    for (int64_t i = 0; i < n; ++i) {
+        uint8_t* e = kv + i * KV_BYTES;
+        memset(e, 0, KV_BYTES);
+        for (int g = 0; g < KV_DIM / 16; ++g) {
+            float v[16], amax = 0.0f;
+            for (int t = 0; t < 16; ++t) {
+                v[t] = bf16_to_f32(x[i * KV_DIM + g * 16 + t]);
+                if (!isfinite(v[t])) return -1;
+                if (fabsf(v[t]) > amax) amax = fabsf(v[t]);
+            }
+            uint8_t sb = hsio_e4m3_encode(amax / 6.0f);
+            float sc = (float)hsio_e4m3_value(sb);
+            e[256 + g] = sb;
+            for (int t = 0; t < 16; ++t) {
+                int c = g * 16 + t;
+                uint8_t code = (sc == 0.0f) ? 0 : hsio_e2m1_encode(v[t] / sc);
+                e[c / 2] |= (uint8_t)((c & 1) ? code << 4 : code);
+            }
+        }
+    }
+    return 0;
+}
+
+/* The 512 decoded values of main-KV entry i: E2M1(code) * E4M3(scale). */
+void hsio_mainkv_decode(const uint8_t* kv, int64_t i, double* out) {
+    const uint8_t* e = kv + i * KV_BYTES;
+    for (int c = 0; c < KV_DIM; ++c) {
+        uint8_t code = (c & 1) ? (uint8_t)(e[c / 2] >> 4) : (uint8_t)(e[c / 2] & 15);
+        out[c] = hsio_e2m1_value(code) * hsio_e4m3_value(e[256 + c / 16]);
+    }
+}
+
+/* gather(main_kv, topk) for one query: row t of out (bf16 bits [k][512]) is
+ * entry idx[t] of the cache decoded, zeros where idx[t] < 0 (padding).
+ * Returns 0, -1 if an index is at or past n_vis, -2 if a decoded value is
+ * not exact in bf16 (impossible for these formats; checked anyway). */
+int hsio_mainkv_gather(const uint8_t* kv, int64_t n_vis, const int32_t* idx, int k, uint16_t* out) {
+    double d[KV_DIM];
+    for (int t = 0; t < k; ++t) {
+        uint16_t* row = out + (int64_t)t * KV_DIM;
+        if (idx[t] < 0) {
+            memset(row, 0, KV_DIM * sizeof(uint16_t));
+            continue;
+        }
+        if (idx[t] >= n_vis) return -1;
+        hsio_mainkv_decode(kv, idx[t], d);
+        for (int c = 0; c < KV_DIM; ++c) {
+            float f = (float)d[c];
+            uint32_t u;
+            memcpy(&u, &f, 4);
+            if ((double)f != d[c] || (u & 0xFFFFu)) return -2;
+            row[c] = (uint16_t)(u >> 16);
         }
     }
     return 0;

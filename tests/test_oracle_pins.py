@@ -317,6 +317,101 @@ def test_score_mx_tracks_unquantised_formula_and_pool_slots():
     assert np.isneginf(ps[32:]).all()
 
 
+# ----------------------------------------------------------------- main KV --
+
+def _kv_entry(codes, scales):
+    """One 288-byte main-KV entry from 512 codes and 32 scale bytes (the layout definition)."""
+    e = np.zeros(288, dtype=np.uint8)
+    for c in range(512):
+        e[c // 2] |= (int(codes[c]) & 15) << (4 * (c & 1))
+    e[256:] = scales
+    return e
+
+
+def test_mainkv_entry_size_matches_page():
+    ((dims, group, payload, scales, total),) = golden_rows("mainkv_format.txt")
+    dims, group, payload, scales, total = map(int, (dims, group, payload, scales, total))
+    assert dims * 4 // 8 == payload and dims // group == scales and payload + scales == total
+    kv = oracle.mainkv_quantize(np.zeros((3, dims), dtype=np.uint16))
+    assert kv.size == 3 * total
+
+
+def test_mainkv_decode_every_code_and_scale_against_library():
+    e2m1 = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6] * 2) * np.repeat([1, -1], 8)
+    sc = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for sbase in range(0, 256, 32):
+        scales = np.arange(sbase, sbase + 32, dtype=np.uint8)
+        codes = np.arange(512) % 16
+        e = _kv_entry(codes, scales)
+        d = oracle.mainkv_decode(e, 0)
+        ref = e2m1[codes] * sc[scales[np.arange(512) // 16]]
+        fin = ~np.isnan(ref)
+        assert np.array_equal(d[fin], ref[fin])
+        if fin.all():  # exact in bf16: torch's bf16 cast returns the same value
+            g = oracle.mainkv_gather(e, 1, np.array([0]))[0]
+            tb = torch.from_numpy(ref).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+            assert np.array_equal(g, tb)
+
+
+def test_mainkv_quantize_closed_forms():
+    # group g of entry 0 is constant v_g: scale E4M3_RN(|v|/6), every code the same
+    vals = [6.0, 7.0, 0.0, -3.0, 448.0 * 6, 1e-3, 5.0, -0.75]
+    x = np.zeros((1, 512), dtype=np.float32)
+    for g, v in enumerate(vals):
+        x[0, 16 * g:16 * g + 16] = v
+    xb = (x.view(np.uint32) >> 16).astype(np.uint16)
+    kv = oracle.mainkv_quantize(xb)
+    d = oracle.mainkv_decode(kv, 0)
+    xf = inputs.bf16_to_f32(xb)[0]
+    # 6 -> scale 1, code 6; 7 -> 7/6 rounds to scale 1.125, 7/1.125 saturates to 6 -> 6.75;
+    # 0 -> scale 0, zeros; -3 -> scale 0.5, -6 -> -3; 2688 -> scale 448, 6 -> 2688;
+    # 5 -> scale 0.8125 (5/6 = 0.8333 rounds down), 5/0.8125 = 6.15 -> 6 -> 4.875;
+    # -0.75 -> scale 0.125, -6 -> -0.75
+    want = {0: 6.0, 1: 6.75, 2: 0.0, 3: -3.0, 4: 2688.0, 6: 4.875, 7: -0.75}
+    for g, v in want.items():
+        assert (d[16 * g:16 * g + 16] == v).all(), (g, d[16 * g])
+    # 1e-3 (bf16 0.000999..): a subnormal E4M3 scale; check against the definition
+    a = float(np.abs(xf[80:96]).max())
+    sb = torch.tensor([np.float32(a) / np.float32(6)]).to(torch.float8_e4m3fn).view(torch.uint8).item()
+    assert kv[256 + 5] == sb
+
+
+def test_mainkv_codes_are_brute_force_nearest():
+    x = inputs.normal_bf16(14, 79, 20 * 512).reshape(20, 512)
+    kv = oracle.mainkv_quantize(x)
+    xf = inputs.bf16_to_f32(x)
+    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    for i in range(20):
+        d = oracle.mainkv_decode(kv, i)
+        for g in range(32):
+            xg = xf[i, 16 * g:16 * g + 16]
+            amax = np.float32(np.abs(xg).max())
+            sb = torch.tensor([amax / np.float32(6)]).to(torch.float8_e4m3fn)
+            assert kv[i * 288 + 256 + g] == sb.view(torch.uint8).item()
+            sc = float(sb.to(torch.float64).item())
+            for t in range(16):
+                a = float(np.float32(abs(xg[t])) / np.float32(sc))
+                dist = np.abs(mags - a)
+                best = np.flatnonzero(dist == dist.min())
+                c = best[0] if best.size == 1 else best[best % 2 == 0][0]
+                assert abs(d[16 * g + t]) == mags[c] * sc
+
+
+def test_mainkv_gather_order_padding_and_range():
+    x = inputs.normal_bf16(15, 80, 40 * 512).reshape(40, 512)
+    kv = oracle.mainkv_quantize(x)
+    idx = np.array([7, 0, 39, -1, 7, -1], dtype=np.int32)
+    g = oracle.mainkv_gather(kv, 40, idx)
+    for t, i in enumerate(idx):
+        if i < 0:
+            assert (g[t] == 0).all()
+        else:
+            want = oracle.mainkv_decode(kv, int(i)).astype(np.float32).view(np.uint32) >> 16
+            assert np.array_equal(g[t], want.astype(np.uint16))
+    with pytest.raises(ValueError):
+        oracle.mainkv_gather(kv, 39, idx)  # 39 is past the 39 visible entries
+
+
 # ------------------------------------------------------------------- score --
 
 def _sparse_exact_case(seed):
