@@ -58,6 +58,7 @@ def parse():
     ap.add_argument("--format", choices=["nvfp4", "mxfp4"], default="nvfp4",
                     help="record format of the headline step")
     ap.add_argument("--no-mxfp4", action="store_true", help="skip the extra step on MXFP4 records")
+    ap.add_argument("--no-mainkv", action="store_true", help="skip the main-KV gather measurement")
     ap.add_argument("--profile", action="store_true", help="cudaProfilerStart/Stop around the timed steps")
     ap.add_argument("--queries", type=int, default=0, help="use only the first N queries (profiling captures)")
     return ap.parse_args()
@@ -395,6 +396,46 @@ class DeviceWorkload:
         return n * key_bytes + n * 4 + (nb * 4 if self.wl.build_pool else 0) + self.B * (4 * self.rec + 32 * 4 + scales)
 
 
+class MainKV:
+    """The FP4 main-KV caches of a workload, resident on one GPU: the caches of
+    all sequences back to back, seq_len entries of 288 bytes each (19.3 GB for
+    64 x 1M). Entry e of the buffer holds pattern entry e mod P: the first
+    P = 131072 generated main-KV entries of the workload's first sequence,
+    quantised on the GPU once and replicated (a gather's cost depends on where
+    the selected entries sit, not on their values)."""
+    PATTERN = 131072
+
+    def __init__(self, wl: inputs.Workload, dev, log):
+        import torch
+
+        import long_context_decode_lightning_gb300 as hsi
+        seqs = sorted(set(wl.query_seq))
+        start, off = {}, 0
+        for s in seqs:
+            start[s] = off
+            off += wl.seq_len[s]
+        self.entries = off
+        E = hsi.KV_ENTRY_BYTES
+        t0 = time.time()
+        self.kv = torch.empty(off * E, dtype=torch.uint8, device=dev)
+        self.P = P = min(self.PATTERN, off)
+        self.pattern_seq = seqs[0]
+        x = torch.from_numpy(wl.kv_bf16(seqs[0], rows=P).view(np.int16)).to(dev)
+        hsi.quantize_mainkv(x, self.kv[: P * E])
+        reps = off // P
+        if reps > 1:
+            self.kv[: reps * P * E].view(reps, P * E)[1:].copy_(self.kv[: P * E].expand(reps - 1, -1))
+        if off > reps * P:
+            self.kv[reps * P * E:].copy_(self.kv[: (off - reps * P) * E])
+        torch.cuda.synchronize()
+        self.off = torch.tensor([start[s] for s in wl.query_seq], dtype=torch.int64, device=dev)
+        log(f"main KV: {off} entries, {off * E / 1e9:.2f} GB, filled in {time.time() - t0:.1f} s")
+
+    def pattern_index(self, b_off: int, i: int) -> int:
+        """The pattern entry that entry i of the cache starting at entry b_off holds."""
+        return (b_off + i) % self.P
+
+
 # ----------------------------------------------------------- CPU oracle --
 
 def oracle_sample_setup(wl: inputs.Workload, nq: int):
@@ -597,6 +638,37 @@ def main():
             "gather_score_frac": gbs(reindex["gather_score_us"]) / peak,
             "note": "one layer timed alone on the resident pool; fractions of the measured copy bandwidth for "
                     "the pooled bytes (the layer figure includes its selection)"})
+    if not args.no_mainkv:
+        # gather(main_kv, topk) of every layer's top-512 of the last step, into bf16
+        M = MainKV(wl, dev, log)
+        kv_out = torch.empty(W.layers, W.B, K_TOP, hsi.KV_DIM, dtype=torch.int16, device=dev)
+
+        def gathers():
+            for l in range(W.layers):
+                hsi.gather_mainkv(M.kv, M.off, W.n_vis, W.idx[l], K_TOP, W.B, kv_out[l])
+        gathers()  # sets the launch attributes before capture
+        torch.cuda.synchronize()
+        g_graph = torch.cuda.CUDAGraph()  # the step's gathers as one graph, as the step itself runs
+        with torch.cuda.graph(g_graph):
+            gathers()
+        for _ in range(max(args.warmup, 1)):
+            g_graph.replay()
+        torch.cuda.synchronize()
+        assert hsi.device_error() == 0, "device error in the main-KV gather"
+        ms_g = timed(g_graph.replay, args.steps)
+        valid = int((W.idx >= 0).sum().item())
+        bytes_g = valid * hsi.KV_ENTRY_BYTES + W.layers * W.B * K_TOP * (hsi.KV_DIM * 2 + 4)
+        gbs_g = bytes_g / (ms_g / args.steps / 1e3) / 1e9
+        line["mainkv_gather"] = {
+            "us_per_step": 1000 * ms_g / args.steps, "gathers_per_step": W.layers,
+            "entries_per_step": W.layers * W.B * K_TOP, "bytes_per_step": bytes_g,
+            "roofline": {"bound": "hbm", "achieved": gbs_g, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                         "frac": gbs_g / float(peaks["hbm_gbs"]), "traffic": None,
+                         "kernel": "hsi_gather_mainkv (mainkv_gather_kernel)"},
+            "note": "the top-512 of each of the step's layers gathered from 288-byte FP4 main-KV entries "
+                    f"({M.entries * hsi.KV_ENTRY_BYTES / 1e9:.1f} GB resident) and decoded to bf16 rows; "
+                    "bytes = 288 read + 1024 written + 4 of index per selected entry"}
+        del g_graph, M, kv_out
     if not args.no_mxfp4 and not W.mx:
         # the same step on MXFP4 records (its own K caches and queries)
         Wm = DeviceWorkload(wl, dev, log, fmt=hsi.FMT_MXFP4)

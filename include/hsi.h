@@ -308,6 +308,47 @@ hsi_status hsi_pool_gather(const uint8_t* k_rec, const int64_t* k_rec_off, const
                            uint8_t* pool_rec, hsi_format format, cudaStream_t stream);
 
 /*
+ * FP4 main KV for core attention, and gather(main_kv, topk).
+ * Page: "DeepSeek-V4.1 模型结构（3）", section "scale 的格式决定了精度" (the main KV
+ * uses groups of 16 with an E4M3 scale, NVFP4's layout without its global
+ * scale: a 512-dim entry is 256 B of codes plus 32 B of scales, 288 B) and
+ * section "官方的参考实现里" (dequantised before attention); the CSA2 layer
+ * pseudocode of "DeepSeek V4.1 Flash KV cache" (selected = gather(main_kv,
+ * topk), then core attention).
+ *
+ * Entry layout (288 bytes, 512 values): the E2M1 code of value i in byte i/2
+ * (low nibble for even i), then the E4M3 scale of values 16g .. 16g+15 in
+ * byte 256 + g. Value = E2M1(code) * E4M3(scale); every such product is exact
+ * in bf16. Quantisation: scale = E4M3_RN(amax/6) (amax of the 16 values, the
+ * division in fp32), code = E2M1_RN(x / scale), 0 where the scale decodes to
+ * 0; no rotation. Scale bytes 0x7F and 0xFF (NaN) never occur in valid entries.
+ */
+#define HSI_KV_DIM 512
+#define HSI_KV_ENTRY_BYTES 288
+
+/*
+ *  x   (dev) bf16 bit patterns [n][512], 16-byte aligned; finite (a non-finite
+ *      value is reported as HSI_ERR_DEVICE_ARG by hsi_device_error).
+ *  kv  (dev) out: [n][288] bytes, 16-byte aligned.
+ */
+hsi_status hsi_quantize_mainkv(const uint16_t* x, int64_t n, uint8_t* kv, cudaStream_t stream);
+
+/*
+ * out[b][t] = entry kv_off[b] + idx[b][t] of kv, decoded to bf16, for t < k;
+ * a zero row where idx[b][t] < 0 (the -1 padding of a short top-k list).
+ *  kv      (dev) entries, 16-byte aligned; query b's cache starts at entry
+ *          kv_off[b] (dev, int64 [B]) and holds n_visible[b] (dev, int32 [B])
+ *          entries. An index at or past n_visible[b] is reported as
+ *          HSI_ERR_DEVICE_ARG by hsi_device_error and its row is zeroed.
+ *  idx     (dev) int32 [B][ld_idx], ld_idx >= k (e.g. the top_idx of a layer).
+ *  k       1 .. 4096.
+ *  out     (dev) bf16 bit patterns [B][k][512], 16-byte aligned.
+ */
+hsi_status hsi_gather_mainkv(const uint8_t* kv, const int64_t* kv_off, const int32_t* n_visible,
+                             const int32_t* idx, int64_t ld_idx, int32_t k, int32_t B, uint16_t* out,
+                             cudaStream_t stream);
+
+/*
  * A decoder Full layer in one call: hsi_score_full, then the top-k of the
  * scores, then (block_ids != NULL) the candidate pool with blocks of 8, with
  * the selections' key histograms accumulated inside the scoring kernel

@@ -30,7 +30,8 @@ WS_QUANTIZE, WS_SCORE, WS_TOPK, WS_POOL, WS_FULL_LAYER, WS_REINDEX_LAYER = 0, 1,
 EXPORTS = ["hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
            "hsi_workspace_size", "hsi_device_error", "hsi_device_check", "hsi_status_string",
            "hsi_kernel_launches", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer", "hsi_reindex_layer",
-           "hsi_topk_noalloc", "hsi_debug_set", "hsi_pool_gather", "hsi_quantize_mxfp4"]
+           "hsi_topk_noalloc", "hsi_debug_set", "hsi_pool_gather", "hsi_quantize_mxfp4", "hsi_quantize_mainkv",
+           "hsi_gather_mainkv"]
 
 
 class HsiError(RuntimeError):
@@ -65,6 +66,8 @@ def lib() -> ctypes.CDLL:
         vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
         L.hsi_quantize_nvfp4.argtypes = [vp, i64, i64, vp, ctypes.c_int, vp, vp, vp, sz, vp]
         L.hsi_quantize_mxfp4.argtypes = [vp, i64, i64, vp, vp, vp]
+        L.hsi_quantize_mainkv.argtypes = [vp, i64, vp, vp]
+        L.hsi_gather_mainkv.argtypes = [vp, vp, vp, vp, i64, i32, i32, vp, vp]
         L.hsi_score_full.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, vp, i64, vp, i64, ctypes.c_int, vp,
                                      sz, vp]
         L.hsi_topk.argtypes = [vp, i64, vp, i32, i64, i32, vp, i64, i32, vp, vp, vp, sz, vp]
@@ -91,7 +94,7 @@ def lib() -> ctypes.CDLL:
         for name in ("hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
                      "hsi_device_error", "hsi_device_check", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer",
                      "hsi_reindex_layer", "hsi_topk_noalloc", "hsi_debug_set", "hsi_pool_gather",
-                     "hsi_quantize_mxfp4"):
+                     "hsi_quantize_mxfp4", "hsi_quantize_mainkv", "hsi_gather_mainkv"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -178,6 +181,22 @@ def quantize_mxfp4(x: torch.Tensor, n_tensors: int, rows_per_tensor: int, signs,
     s8 = (ctypes.c_int8 * 128)(*[int(v) for v in signs])
     _check("hsi_quantize_mxfp4", lib().hsi_quantize_mxfp4(
         _ptr(x), n_tensors, rows_per_tensor, s8, _ptr(rec), _stream(stream)))
+
+
+KV_DIM, KV_ENTRY_BYTES = 512, 288
+
+
+def quantize_mainkv(x: torch.Tensor, kv: torch.Tensor, stream=None):
+    """x: bf16 (or its int16 bits) [n, 512] -> FP4 main-KV entries kv [n*288] bytes."""
+    n = x.numel() // KV_DIM
+    _check("hsi_quantize_mainkv", lib().hsi_quantize_mainkv(_ptr(x), n, _ptr(kv), _stream(stream)))
+
+
+def gather_mainkv(kv, kv_off, n_visible, idx, k, B, out, ld_idx=None, stream=None):
+    """gather(main_kv, topk): out [B, k, 512] bf16 bits = the entries idx selects, decoded (0 rows for -1)."""
+    ld_idx = idx.shape[-1] if ld_idx is None else ld_idx
+    _check("hsi_gather_mainkv", lib().hsi_gather_mainkv(
+        _ptr(kv), _ptr(kv_off), _ptr(n_visible), _ptr(idx), ld_idx, k, B, _ptr(out), _stream(stream)))
 
 
 def rec_bytes(fmt: int = FMT_NVFP4) -> int:

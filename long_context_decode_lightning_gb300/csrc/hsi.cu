@@ -11,6 +11,7 @@
 #include "calib.cuh"
 #include "common.cuh"
 #include "gather.cuh"
+#include "mainkv.cuh"
 #include "quantize.cuh"
 #include "score.cuh"
 #include "select.cuh"
@@ -708,6 +709,23 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     // eighth of the scores): counting it in the scoring epilogue, where the
     // maxima of a warp land in one or two bins, cost more than this pass
     return run_select(pp, nb, stream, false);
+}
+
+hsi_status hsi_quantize_mainkv(const uint16_t* x, int64_t n, uint8_t* kv, cudaStream_t stream) {
+    if (!x || !kv || n <= 0 || !aligned(x, 16) || !aligned(kv, 16)) return HSI_ERR_INVALID_ARG;
+    if ((n + 7) / 8 > INT32_MAX) return HSI_ERR_INVALID_ARG;
+    return launch(mainkv_quant_kernel, dim3((unsigned)((n + 7) / 8)), dim3(256), 0, stream, x, n, kv);
+}
+
+hsi_status hsi_gather_mainkv(const uint8_t* kv, const int64_t* kv_off, const int32_t* n_visible, const int32_t* idx,
+                             int64_t ld_idx, int32_t k, int32_t B, uint16_t* out, cudaStream_t stream) {
+    if (!kv || !kv_off || !n_visible || !idx || !out || B <= 0 || k < 1 || k > 4096 || ld_idx < k)
+        return HSI_ERR_INVALID_ARG;
+    if (!aligned(kv, 16) || !aligned(out, 16)) return HSI_ERR_INVALID_ARG;
+    const int64_t warps = ((int64_t)B * k + GATHER_EPW - 1) / GATHER_EPW;
+    if ((warps + 7) / 8 > INT32_MAX) return HSI_ERR_INVALID_ARG;
+    return launch(mainkv_gather_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, stream, kv, kv_off,
+                  n_visible, idx, ld_idx, k, B, out);
 }
 
 hsi_status hsi_pool_gather(const uint8_t* k_rec, const int64_t* k_rec_off, const int32_t* n_visible,

@@ -1,0 +1,145 @@
+// K8: the FP4 main KV that core attention reads, and gather(main_kv, topk).
+//
+// An entry is 512 values in 288 bytes: E2M1 codes (value i in byte i/2, low
+// nibble for even i), then one E4M3 scale per 16 values (byte 256 + i/16); no
+// global scale. Quantisation: scale = E4M3_RN(amax/6), code = E2M1_RN(x/scale).
+// The gather decodes the selected entries of each query into bf16 rows for the
+// attention kernel; every decoded value (an E2M1 value times an E4M3 scale, at
+// most 6 significant bits, magnitude in [2^-10, 2688]) is exact in bf16.
+//
+// Both kernels give each lane one 16-value group of an entry, so a group's amax
+// and scale need no exchange between lanes.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "quantize.cuh"
+
+namespace hsi {
+
+constexpr int KV_DIM = 512;
+constexpr int KV_BYTES = 288;
+
+// E2M1 code (bit 3 = sign) -> fp32, exact: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+__device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
+    const uint32_t m = c & 7u, e = m >> 1;
+    const uint32_t mag = e ? (((e + 126u) << 23) | ((m & 1u) << 22)) : (m ? 0x3F000000u : 0u);
+    return __uint_as_float(mag | ((c & 8u) << 28));
+}
+
+// x: bf16 [n][512] (16-byte aligned); kv: [n][288] (16-byte aligned). grid =
+// ceil(n / 8) CTAs of 256 threads. A non-finite value is reported through the
+// device error word.
+__global__ void __launch_bounds__(256) mainkv_quant_kernel(const uint16_t* __restrict__ x, int64_t n,
+                                                           uint8_t* __restrict__ kv) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int64_t e = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (e >= n) return;
+    const int lane = threadIdx.x & 31;
+    const uint4* src = reinterpret_cast<const uint4*>(x + e * KV_DIM + lane * 16);
+    const uint4 a = __ldcs(src), b = __ldcs(src + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float v[16];
+    float amax = 0.f;
+    bool finite = true;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        finite = finite && isfinite(v[i]);
+        amax = fmaxf(amax, fabsf(v[i]));
+    }
+    if (!finite) raise_error(DEVERR_ARG);
+    const uint32_t sb = f32_to_e4m3_rn_sat(__fdiv_rn(amax, 6.0f));
+    const float sc = e4m3_to_f32(sb);
+    uint32_t c0 = 0u, c1 = 0u;
+    if (sc != 0.0f) {
+        float y[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) y[i] = __fdiv_rn(v[i], sc);
+        c0 = f32x4_to_e2m1x4(y[0], y[1], y[2], y[3]) | (f32x4_to_e2m1x4(y[4], y[5], y[6], y[7]) << 16);
+        c1 = f32x4_to_e2m1x4(y[8], y[9], y[10], y[11]) | (f32x4_to_e2m1x4(y[12], y[13], y[14], y[15]) << 16);
+    }
+    uint8_t* dst = kv + e * KV_BYTES;
+    *reinterpret_cast<uint2*>(dst + lane * 8) = make_uint2(c0, c1);
+    dst[256 + lane] = (uint8_t)sb;
+}
+
+// out[b][t][:] = entry kv_off[b] + idx[b][t] decoded (bf16 [B][k][512]),
+// zeros where idx[b][t] < 0; an index at or past n_visible[b] is reported
+// through the device error word and its row is zeroed. A warp takes
+// GATHER_EPW consecutive (b, t) of the flattened list: lane j < GATHER_EPW
+// resolves entry j's index, then every lane issues the loads of all its
+// entries before decoding any, so one launch is about one wave of warps with
+// two dependent memory round trips each. grid = ceil(B k / (8 GATHER_EPW))
+// CTAs of 256 threads.
+#ifndef HSI_GATHER_EPW
+#define HSI_GATHER_EPW 4
+#endif
+constexpr int GATHER_EPW = HSI_GATHER_EPW;
+
+__global__ void __launch_bounds__(256) mainkv_gather_kernel(const uint8_t* __restrict__ kv,
+                                                            const int64_t* __restrict__ kv_off,
+                                                            const int32_t* __restrict__ n_vis,
+                                                            const int32_t* __restrict__ idx, int64_t ld_idx,
+                                                            int32_t k, int32_t B, uint16_t* __restrict__ out) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int64_t total = (int64_t)B * k;
+    const int64_t base = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * GATHER_EPW;
+    if (base >= total) return;
+    const int lane = threadIdx.x & 31;
+    // lane j < GATHER_EPW: the entry (in entries of kv) of list item base + j, or -1
+    long long src = -1;
+    if (lane < GATHER_EPW && base + lane < total) {
+        const int64_t f = base + lane;
+        const int b = (int)(f / k), t = (int)(f % k);
+        const int32_t i = __ldg(idx + (int64_t)b * ld_idx + t);
+        const int32_t nv = __ldg(n_vis + b);
+        const int64_t o = __ldg(kv_off + b);
+        if (i >= 0) {
+            if (i < nv) src = o + i;
+            else raise_error(DEVERR_ARG);
+        }
+    }
+    long long e[GATHER_EPW];
+    uint2 c[GATHER_EPW];
+    uint32_t sb[GATHER_EPW];
+#pragma unroll
+    for (int j = 0; j < GATHER_EPW; ++j) {
+        e[j] = __shfl_sync(0xFFFFFFFFu, src, j);
+        c[j] = make_uint2(0u, 0u);
+        sb[j] = 0u;
+        if (e[j] >= 0) {
+            const uint8_t* p = kv + e[j] * KV_BYTES;
+            c[j] = __ldcs(reinterpret_cast<const uint2*>(p + lane * 8));
+            sb[j] = __ldcs(p + 256 + lane);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < GATHER_EPW; ++j) {
+        if (base + j >= total) break;
+        uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        if (e[j] >= 0) {
+            const float sc = e4m3_to_f32(sb[j]);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint32_t word = q < 4 ? c[j].x : c[j].y;
+                const uint32_t pair = word >> (8 * (q & 3));
+                const __nv_bfloat162 h = __floats2bfloat162_rn(e2m1_to_f32(pair & 15u) * sc,
+                                                               e2m1_to_f32((pair >> 4) & 15u) * sc);
+                o[q] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+        }
+        uint4* dst = reinterpret_cast<uint4*>(out + (base + j) * KV_DIM + lane * 16);
+        __stcs(dst, make_uint4(o[0], o[1], o[2], o[3]));
+        __stcs(dst + 1, make_uint4(o[4], o[5], o[6], o[7]));
+    }
+}
+
+}  // namespace hsi

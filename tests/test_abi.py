@@ -76,6 +76,14 @@ def test_host_validation_rejects_bad_arguments(L):
     assert L.hsi_score_full(*args, 1, 100, 1, fake, 100, None, 0, 2, None, 0, None) == -1
     assert L.hsi_score_full(fake, None, *[fake] * 5, 1, 100, 1, fake, 100, None, 0, 0, None, 0, None) == -1
     assert L.hsi_pool_gather(fake, fake, fake, fake, fake, 2048, 1, fake + 4096, 3, None) == -1
+    # main KV: null input, unaligned entries, k out of range, ld_idx < k
+    assert L.hsi_quantize_mainkv(None, 4, fake, None) == -1
+    assert L.hsi_quantize_mainkv(fake, 4, fake + 8, None) == -1
+    assert L.hsi_quantize_mainkv(fake, 0, fake, None) == -1
+    assert L.hsi_gather_mainkv(fake, fake, fake, fake, 512, 0, 4, fake, None) == -1
+    assert L.hsi_gather_mainkv(fake, fake, fake, fake, 512, 5000, 4, fake, None) == -1
+    assert L.hsi_gather_mainkv(fake, fake, fake, fake, 511, 512, 4, fake, None) == -1
+    assert L.hsi_gather_mainkv(fake + 4, fake, fake, fake, 512, 512, 4, fake, None) == -1
     # quantize_mxfp4: null x, bad signs, unaligned records
     assert L.hsi_quantize_mxfp4(None, 1, 1, s8, fake, None) == -1
     assert L.hsi_quantize_mxfp4(fake, 1, 1, bad_signs, fake, None) == -1

@@ -125,6 +125,27 @@ def test_fullsize_decode_b64_n1m_mxfp4():
     oracle.map_queries(lambda b: _check_query(wl, W, b, 0), samples, threads=len(samples))
 
 
+def test_fullsize_mainkv_gather_b64_n1m():
+    """The benchmark's gather(main_kv, topk) at full size: the 64 queries'
+    Reindex top-512 from 19.3 GB of resident FP4 main KV, sampled rows against
+    the oracle's decode of the entries they select."""
+    wl, W = _resident(2)
+    M = bench.MainKV(wl, torch.device("cuda"), lambda m: None)
+    l = wl.full_layers  # the first Reindex layer's top-512
+    out = torch.empty(W.B, 512, 512, dtype=torch.int16, device="cuda")
+    hsi.gather_mainkv(M.kv, M.off, W.n_vis, W.idx[l], 512, W.B, out)
+    assert hsi.device_error() == 0
+    pattern = oracle.mainkv_quantize(wl.kv_bf16(M.pattern_seq, rows=M.P))
+    assert np.array_equal(M.kv[:1000 * 288].cpu().numpy(), pattern[:1000 * 288])
+    idx, offs = W.idx[l].cpu().numpy(), M.off.cpu().numpy()
+    got = out.cpu().numpy().view(np.uint16)
+    rng = np.random.default_rng(7)
+    for b in (0, 31, 63):
+        for t in rng.choice(512, 64, replace=False):
+            p = M.pattern_index(int(offs[b]), int(idx[b, t]))
+            assert np.array_equal(got[b, t], oracle.mainkv_gather(pattern, M.P, np.array([p]))[0]), (b, t)
+
+
 def test_fullsize_encoder_b64_3x512k():
     wl, W = _resident(3)
     samples = [5, 60]
