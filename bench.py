@@ -59,6 +59,7 @@ def parse():
                     help="record format of the headline step")
     ap.add_argument("--no-mxfp4", action="store_true", help="skip the extra step on MXFP4 records")
     ap.add_argument("--no-mainkv", action="store_true", help="skip the main-KV gather measurement")
+    ap.add_argument("--no-serve", action="store_true", help="skip the serving-step measurement")
     ap.add_argument("--profile", action="store_true", help="cudaProfilerStart/Stop around the timed steps")
     ap.add_argument("--queries", type=int, default=0, help="use only the first N queries (profiling captures)")
     return ap.parse_args()
@@ -157,6 +158,8 @@ class ClockSampler:
 class DeviceWorkload:
     """The workload resident on one GPU, and one step of the path over it."""
 
+    HEADROOM = 256  # rows of room per cache for appended decode tokens
+
     def __init__(self, wl: inputs.Workload, dev, log, fmt: int = 0):
         import torch
 
@@ -178,7 +181,7 @@ class DeviceWorkload:
         off = 0
         for s in seqs:
             rec_off[s] = off
-            off += hsi.n_records(wl.seq_len[s])
+            off += hsi.n_records(wl.seq_len[s] + self.HEADROOM)
         t0 = time.time()
         stage = [torch.empty(max(wl.seq_len) * 128, dtype=torch.int16).pin_memory() for _ in range(2)]
         stage_dev = [torch.empty(max(wl.seq_len) * 128, dtype=torch.int16, device=dev) for _ in range(2)]
@@ -186,7 +189,7 @@ class DeviceWorkload:
         qws = hsi.workspace(hsi.WS_QUANTIZE, 1, 0, device=dev)
         i = 0
         for layer in range(wl.full_layers):
-            krec = torch.empty(off * REC, dtype=torch.uint8, device=dev)
+            krec = torch.zeros(off * REC, dtype=torch.uint8, device=dev)
             gseq = torch.empty(len(seqs), dtype=torch.float32, device=dev)
             for si, s in enumerate(seqs):
                 n = wl.seq_len[s]
@@ -212,6 +215,10 @@ class DeviceWorkload:
             f"({off * REC * wl.full_layers / 1e9:.2f} GB)")
         self.k_off = torch.tensor([rec_off[s] for s in wl.query_seq], dtype=torch.int64, device=dev)
         self.n_vis = torch.tensor(wl.n_visible, dtype=torch.int32, device=dev)
+        # rows each query's caches hold (appends past the visible rows go up to here)
+        self.capacity = torch.tensor([wl.seq_len[s] + self.HEADROOM for s in wl.query_seq], dtype=torch.int32,
+                                     device=dev)
+        self.maxv_cap = self.maxv + self.HEADROOM
         # --- per-step inputs: bf16 q and fp32 w of every layer, one contiguous buffer
         self.layers = wl.full_layers + (wl.reindex_layers if wl.build_pool else 0)
         L = self.layers
@@ -227,7 +234,7 @@ class DeviceWorkload:
         # --- outputs and scratch
         self.q_rec = torch.empty(L, B * 4 * REC, dtype=torch.uint8, device=dev)
         self.g_q = [None] * L if self.mx else torch.empty(L, B, dtype=torch.float32, device=dev)
-        self.scores = torch.empty(B, self.maxv, dtype=torch.float32, device=dev)
+        self.scores = torch.empty(B, self.maxv_cap, dtype=torch.float32, device=dev)
         self.bmax = torch.empty(B, hsi.n_records(self.maxv), dtype=torch.float32, device=dev)
         self.out_dev = torch.empty(L * B * K_TOP * 8, dtype=torch.uint8, device=dev)
         self.out_host = torch.empty_like(self.out_dev, device="cpu").pin_memory()
@@ -235,12 +242,12 @@ class DeviceWorkload:
         self.val = self.out_dev[L * B * K_TOP * 4:].view(torch.float32).view(L, B, K_TOP)
         self.ws_q = hsi.workspace(hsi.WS_QUANTIZE, B, 0, device=dev)
         self.ws_topk = hsi.workspace(hsi.WS_TOPK, B, self.maxv, K_TOP, device=dev)
-        self.ws_full = hsi.workspace(hsi.WS_FULL_LAYER, B, self.maxv, K_TOP, device=dev)
+        self.ws_full = hsi.workspace(hsi.WS_FULL_LAYER, B, self.maxv_cap, K_TOP, device=dev)
         if wl.build_pool:
             self.ids = torch.empty(B, wl.n_keep, dtype=torch.int32, device=dev)
             self.nk = torch.empty(B, dtype=torch.int32, device=dev)
             self.npool = torch.empty(B, dtype=torch.int32, device=dev)
-            self.bits = torch.empty(B, (self.maxv + 31) // 32, dtype=torch.int32, device=dev)
+            self.bits = torch.empty(B, (self.maxv_cap + 31) // 32, dtype=torch.int32, device=dev)
             self.ws_pool = hsi.workspace(hsi.WS_POOL, B, self.maxv, 8, device=dev)
             self.pool_scores = torch.empty(B, wl.n_keep * 8, dtype=torch.float32, device=dev)
             self.ws_rtopk = hsi.workspace(hsi.WS_REINDEX_LAYER, B, wl.n_keep * 8, K_TOP, device=dev)
@@ -264,8 +271,11 @@ class DeviceWorkload:
 
     # -- the step as CUDA graphs: [q quantisation] [scoring] [selection and the
     # rest], per Full layer, so that the scoring kernel can be timed between replays
-    def segments(self):
+    def segments(self, maxv=None):
+        """The step's calls; maxv: the host bound on the visible lengths (the
+        caches' capacity for a step over growing caches)."""
         hsi, wl, B = self.hsi, self.wl, self.B
+        maxv = self.maxv if maxv is None else maxv
         signs = self.wl_signs
         segs = []
         for l in range(wl.full_layers):
@@ -276,7 +286,7 @@ class DeviceWorkload:
             for kind, ph in (("score", 1), ("post", 2)):
                 segs.append((kind, lambda l=l, pool=pool, ph=ph: hsi.full_layer(
                     self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[l], self.g_k[l], self.k_off, self.n_vis, B,
-                    self.maxv, self.scores, K_TOP, self.idx[l], self.val[l],
+                    maxv, self.scores, K_TOP, self.idx[l], self.val[l],
                     block_ids=self.ids if pool else None, n_kept=self.nk if pool else None,
                     n_pool=self.npool if pool else None, pool_bits=self.bits if pool else None,
                     n_keep=wl.n_keep, ws=self.ws_full, phases=ph, fmt=self.fmt)))
@@ -405,7 +415,7 @@ class MainKV:
     the selected entries sit, not on their values)."""
     PATTERN = 131072
 
-    def __init__(self, wl: inputs.Workload, dev, log):
+    def __init__(self, wl: inputs.Workload, dev, log, headroom: int = 0):
         import torch
 
         import long_context_decode_lightning_gb300 as hsi
@@ -413,7 +423,7 @@ class MainKV:
         start, off = {}, 0
         for s in seqs:
             start[s] = off
-            off += wl.seq_len[s]
+            off += wl.seq_len[s] + headroom
         self.entries = off
         E = hsi.KV_ENTRY_BYTES
         t0 = time.time()
@@ -437,6 +447,68 @@ class MainKV:
 
 
 # ----------------------------------------------------------- CPU oracle --
+
+def serving_steps(W: DeviceWorkload, M: MainKV, wl: inputs.Workload, dev, args, timed, log):
+    """Decode steps over growing caches: each step appends one token per query
+    (its indexer K row into every Full layer's cache, with the cache's fixed
+    tensor scale, and its main-KV entry), then runs the whole path and gathers
+    every layer's top-512 from the main KV; one CUDA graph per step, replayed
+    while the caches grow by one row per step. Returns the JSON object."""
+    import torch
+
+    import long_context_decode_lightning_gb300 as hsi
+    B, T = W.B, max(args.warmup, 1) + args.steps + 1
+    kx = np.empty((T, B, 128), np.uint16)
+    vx = np.empty((T, B, hsi.KV_DIM), np.uint16)
+    for b in range(B):  # the sequences' own next rows
+        s, n = wl.query_seq[b], wl.n_visible[b]
+        kx[:, b] = wl.k_bf16(0, s, first_row=n, rows=T)
+        vx[:, b] = wl.kv_bf16(s, first_row=n, rows=T)
+    new_k = torch.from_numpy(kx.view(np.int16)).to(dev)
+    new_v = torch.from_numpy(vx.view(np.int16)).to(dev)
+    k_stage = torch.empty(B, 128, dtype=torch.int16, device=dev)
+    v_stage = torch.empty(B, hsi.KV_DIM, dtype=torch.int16, device=dev)
+    rows = torch.empty(W.layers, B, K_TOP, hsi.KV_DIM, dtype=torch.int16, device=dev)
+    n_start = int(W.n_vis.max().item())
+
+    assert wl.full_layers == 1, "decoder workloads: one Full layer's K cache per sequence"
+
+    def step():
+        hsi.append_token(k_stage, W.wl_signs, W.g_k[0], W.k_rec[0], W.k_off, W.n_vis, W.capacity, B, kv_x=v_stage,
+                         kv=M.kv, kv_off=M.off, fmt=W.fmt)
+        for _, fn in W.segments(maxv=W.maxv_cap):
+            fn()
+        for l in range(W.layers):
+            hsi.gather_mainkv(M.kv, M.off, W.n_vis, W.idx[l], K_TOP, B, rows[l])
+
+    k_stage.copy_(new_k[0])
+    v_stage.copy_(new_v[0])
+    step()  # the first token outside the graph (sets every launch attribute)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    state = {"i": 1}
+
+    def one():
+        i = state["i"]
+        k_stage.copy_(new_k[i])
+        v_stage.copy_(new_v[i])
+        graph.replay()
+        state["i"] = i + 1
+    for _ in range(max(args.warmup, 1)):
+        one()
+    torch.cuda.synchronize()
+    ms = timed(one, args.steps)
+    n_end = int(W.n_vis.max().item())
+    log(f"serving: {args.steps} steps, context {n_start} -> {n_end}")
+    return {"ms_per_step": ms / args.steps, "tokens_per_s": B * args.steps / (ms / 1e3), "queries": B,
+            "context_start": n_start, "context_end": n_end,
+            "note": "per step: append one token per query (indexer K row with the cache's fixed tensor scale, "
+                    "main-KV entry), the whole indexer path over the grown caches (max_visible = capacity), "
+                    "and the gathers of every layer's top-512 from the main KV; one CUDA graph, inputs staged "
+                    "by two device copies"}
+
 
 def oracle_sample_setup(wl: inputs.Workload, nq: int):
     """Oracle inputs for the first nq queries (quantised by the oracle itself)."""
@@ -638,9 +710,10 @@ def main():
             "gather_score_frac": gbs(reindex["gather_score_us"]) / peak,
             "note": "one layer timed alone on the resident pool; fractions of the measured copy bandwidth for "
                     "the pooled bytes (the layer figure includes its selection)"})
+    serve = not args.no_serve and wl.build_pool and wl.full_layers == 1
+    M = MainKV(wl, dev, log, headroom=DeviceWorkload.HEADROOM) if (not args.no_mainkv or serve) else None
     if not args.no_mainkv:
         # gather(main_kv, topk) of every layer's top-512 of the last step, into bf16
-        M = MainKV(wl, dev, log)
         kv_out = torch.empty(W.layers, W.B, K_TOP, hsi.KV_DIM, dtype=torch.int16, device=dev)
 
         def gathers():
@@ -668,7 +741,7 @@ def main():
             "note": "the top-512 of each of the step's layers gathered from 288-byte FP4 main-KV entries "
                     f"({M.entries * hsi.KV_ENTRY_BYTES / 1e9:.1f} GB resident) and decoded to bf16 rows; "
                     "bytes = 288 read + 1024 written + 4 of index per selected entry"}
-        del g_graph, M, kv_out
+        del g_graph, kv_out
     if not args.no_mxfp4 and not W.mx:
         # the same step on MXFP4 records (its own K caches and queries)
         Wm = DeviceWorkload(wl, dev, log, fmt=hsi.FMT_MXFP4)
@@ -692,6 +765,10 @@ def main():
             "note": "the same step and workload on MXFP4 records (32-element groups, E8M0 scales); the "
                     "pool and selections follow from its own scores"}
         del Wm
+    if serve:
+        line["serve"] = serving_steps(W, M, wl, dev, args, timed, log)
+        assert hsi.device_error() == 0, "device error during the serving steps"
+    del M
     if rank == 0 and not args.no_cpu_baseline:
         nq = cpu_sample_size(wl)
         log(f"cpu baseline: oracle on {nq} queries")

@@ -349,6 +349,40 @@ hsi_status hsi_gather_mainkv(const uint8_t* kv, const int64_t* kv_off, const int
                              cudaStream_t stream);
 
 /*
+ * Append one decode token to every query's caches: the new position's
+ * indexer K row (rotated and quantised as hsi_quantize_nvfp4 does in mode 1,
+ * with the cache's fixed tensor scale g_k[b]; or as hsi_quantize_mxfp4 does)
+ * into row n_visible[b] of query b's K records, and (kv_x given) the new
+ * main-KV entry (as hsi_quantize_mainkv does) into entry n_visible[b] of its
+ * main-KV cache; then n_visible[b] += 1. A cache built token by token is
+ * byte for byte the cache quantised at once with the same tensor scale.
+ * Page: "DeepSeek-V4.1 模型结构（3）", section "去掉全局 scale 之后范围仍然够用"
+ * (a fixed scale is enough for the range of later entries) and section
+ * "用浅层的打分结果限制深层的打分范围" (every decode step scores the visible
+ * positions, including the newest, whose block the pool pins).
+ *
+ * The lengths live on the device, so a CUDA graph that holds this call and
+ * the step's scoring calls (their max_visible set to the caches' capacity)
+ * replays over a growing cache.
+ *  k_x     (dev) bf16 bit patterns [B][128], 16-byte aligned: row b is query b's new K row.
+ *  signs   (host) the rotation's 128 signs (+1 / -1), as for the quantisers.
+ *  g_k     (dev) [B] the K caches' tensor scales (NVFP4; may be NULL for MXFP4).
+ *  k_rec, k_rec_off: the K records and each query's first record, as for
+ *          hsi_score_full; the record of row n_visible[b] must be allocated.
+ *  kv_x    (dev, may be NULL) bf16 [B][512]; kv, kv_off: the main-KV entries
+ *          and each query's first entry, as for hsi_gather_mainkv.
+ *  n_visible (dev) int32 [B], read and advanced.
+ *  capacity  (dev) int32 [B]: rows (entries) each query's caches hold. A query
+ *          whose n_visible is not below its capacity is left unchanged and
+ *          reported as HSI_ERR_DEVICE_ARG by hsi_device_error.
+ * One query per cache: two queries that share a cache would append twice.
+ */
+hsi_status hsi_append_token(const uint16_t* k_x, const int8_t* signs, const float* g_k, uint8_t* k_rec,
+                            const int64_t* k_rec_off, const uint16_t* kv_x, uint8_t* kv, const int64_t* kv_off,
+                            int32_t* n_visible, const int32_t* capacity, int32_t B, hsi_format format,
+                            cudaStream_t stream);
+
+/*
  * A decoder Full layer in one call: hsi_score_full, then the top-k of the
  * scores, then (block_ids != NULL) the candidate pool with blocks of 8, with
  * the selections' key histograms accumulated inside the scoring kernel

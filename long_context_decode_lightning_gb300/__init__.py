@@ -31,7 +31,7 @@ EXPORTS = ["hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_po
            "hsi_workspace_size", "hsi_device_error", "hsi_device_check", "hsi_status_string",
            "hsi_kernel_launches", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer", "hsi_reindex_layer",
            "hsi_topk_noalloc", "hsi_debug_set", "hsi_pool_gather", "hsi_quantize_mxfp4", "hsi_quantize_mainkv",
-           "hsi_gather_mainkv"]
+           "hsi_gather_mainkv", "hsi_append_token"]
 
 
 class HsiError(RuntimeError):
@@ -68,6 +68,7 @@ def lib() -> ctypes.CDLL:
         L.hsi_quantize_mxfp4.argtypes = [vp, i64, i64, vp, vp, vp]
         L.hsi_quantize_mainkv.argtypes = [vp, i64, vp, vp]
         L.hsi_gather_mainkv.argtypes = [vp, vp, vp, vp, i64, i32, i32, vp, vp]
+        L.hsi_append_token.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, ctypes.c_int, vp]
         L.hsi_score_full.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, vp, i64, vp, i64, ctypes.c_int, vp,
                                      sz, vp]
         L.hsi_topk.argtypes = [vp, i64, vp, i32, i64, i32, vp, i64, i32, vp, vp, vp, sz, vp]
@@ -94,7 +95,7 @@ def lib() -> ctypes.CDLL:
         for name in ("hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
                      "hsi_device_error", "hsi_device_check", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer",
                      "hsi_reindex_layer", "hsi_topk_noalloc", "hsi_debug_set", "hsi_pool_gather",
-                     "hsi_quantize_mxfp4", "hsi_quantize_mainkv", "hsi_gather_mainkv"):
+                     "hsi_quantize_mxfp4", "hsi_quantize_mainkv", "hsi_gather_mainkv", "hsi_append_token"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -197,6 +198,15 @@ def gather_mainkv(kv, kv_off, n_visible, idx, k, B, out, ld_idx=None, stream=Non
     ld_idx = idx.shape[-1] if ld_idx is None else ld_idx
     _check("hsi_gather_mainkv", lib().hsi_gather_mainkv(
         _ptr(kv), _ptr(kv_off), _ptr(n_visible), _ptr(idx), ld_idx, k, B, _ptr(out), _stream(stream)))
+
+
+def append_token(k_x, signs, g_k, k_rec, k_rec_off, n_visible, capacity, B, kv_x=None, kv=None, kv_off=None,
+                 fmt=FMT_NVFP4, stream=None):
+    """One decode token into every query's caches (K row, optional main-KV entry); n_visible += 1 on the device."""
+    s8 = (ctypes.c_int8 * 128)(*[int(v) for v in signs])
+    _check("hsi_append_token", lib().hsi_append_token(
+        _ptr(k_x), s8, _ptr(g_k), _ptr(k_rec), _ptr(k_rec_off), _ptr(kv_x), _ptr(kv), _ptr(kv_off),
+        _ptr(n_visible), _ptr(capacity), B, fmt, _stream(stream)))
 
 
 def rec_bytes(fmt: int = FMT_NVFP4) -> int:

@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "../../include/hsi.h"
+#include "append.cuh"
 #include "calib.cuh"
 #include "common.cuh"
 #include "gather.cuh"
@@ -726,6 +727,37 @@ hsi_status hsi_gather_mainkv(const uint8_t* kv, const int64_t* kv_off, const int
     if ((warps + 7) / 8 > INT32_MAX) return HSI_ERR_INVALID_ARG;
     return launch(mainkv_gather_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, stream, kv, kv_off,
                   n_visible, idx, ld_idx, k, B, out);
+}
+
+hsi_status hsi_append_token(const uint16_t* k_x, const int8_t* signs, const float* g_k, uint8_t* k_rec,
+                            const int64_t* k_rec_off, const uint16_t* kv_x, uint8_t* kv, const int64_t* kv_off,
+                            int32_t* n_visible, const int32_t* capacity, int32_t B, hsi_format format,
+                            cudaStream_t stream) {
+    if (!k_x || !signs || !k_rec || !k_rec_off || !n_visible || !capacity || B <= 0 || !format_ok(format))
+        return HSI_ERR_INVALID_ARG;
+    if (format == HSI_FMT_NVFP4 && !g_k) return HSI_ERR_INVALID_ARG;
+    if (kv_x && (!kv || !kv_off)) return HSI_ERR_INVALID_ARG;
+    if (!aligned(k_x, 16) || !aligned(k_rec, 16) || (kv_x && (!aligned(kv_x, 16) || !aligned(kv, 16))))
+        return HSI_ERR_INVALID_ARG;
+    AppendParams p{};
+    p.q.x = k_x;
+    p.q.n_tensors = B;
+    p.q.rpt = 1;
+    p.q.rec_per_tensor = 1;
+    for (int d = 0; d < 128; ++d) {
+        if (signs[d] != 1 && signs[d] != -1) return HSI_ERR_INVALID_ARG;
+        if (signs[d] < 0) p.q.neg_mask[d >> 5] |= 1u << (d & 31);
+    }
+    p.g_k = g_k;
+    p.k_rec = k_rec;
+    p.k_off = k_rec_off;
+    p.kv_x = kv_x;
+    p.kv = kv;
+    p.kv_off = kv_off;
+    p.n_vis = n_visible;
+    p.capacity = capacity;
+    p.mx = format == HSI_FMT_MXFP4;
+    return launch(append_token_kernel, dim3((unsigned)B), dim3(64), 0, stream, p);
 }
 
 hsi_status hsi_pool_gather(const uint8_t* k_rec, const int64_t* k_rec_off, const int32_t* n_visible,

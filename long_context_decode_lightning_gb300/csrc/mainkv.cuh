@@ -28,17 +28,11 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
     return __uint_as_float(mag | ((c & 8u) << 28));
 }
 
-// x: bf16 [n][512] (16-byte aligned); kv: [n][288] (16-byte aligned). grid =
-// ceil(n / 8) CTAs of 256 threads. A non-finite value is reported through the
-// device error word.
-__global__ void __launch_bounds__(256) mainkv_quant_kernel(const uint16_t* __restrict__ x, int64_t n,
-                                                           uint8_t* __restrict__ kv) {
-    griddep_wait();
-    griddep_launch_dependents();
-    const int64_t e = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (e >= n) return;
+// One warp: the bf16 entry at x_row (512 values, 16-byte aligned) into the
+// 288 bytes at dst. A non-finite value is reported through the error word.
+__device__ __forceinline__ void mainkv_encode_warp(const uint16_t* __restrict__ x_row, uint8_t* __restrict__ dst) {
     const int lane = threadIdx.x & 31;
-    const uint4* src = reinterpret_cast<const uint4*>(x + e * KV_DIM + lane * 16);
+    const uint4* src = reinterpret_cast<const uint4*>(x_row + lane * 16);
     const uint4 a = __ldcs(src), b = __ldcs(src + 1);
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     float v[16];
@@ -65,9 +59,19 @@ __global__ void __launch_bounds__(256) mainkv_quant_kernel(const uint16_t* __res
         c0 = f32x4_to_e2m1x4(y[0], y[1], y[2], y[3]) | (f32x4_to_e2m1x4(y[4], y[5], y[6], y[7]) << 16);
         c1 = f32x4_to_e2m1x4(y[8], y[9], y[10], y[11]) | (f32x4_to_e2m1x4(y[12], y[13], y[14], y[15]) << 16);
     }
-    uint8_t* dst = kv + e * KV_BYTES;
     *reinterpret_cast<uint2*>(dst + lane * 8) = make_uint2(c0, c1);
     dst[256 + lane] = (uint8_t)sb;
+}
+
+// x: bf16 [n][512] (16-byte aligned); kv: [n][288] (16-byte aligned). grid =
+// ceil(n / 8) CTAs of 256 threads, one warp per entry.
+__global__ void __launch_bounds__(256) mainkv_quant_kernel(const uint16_t* __restrict__ x, int64_t n,
+                                                           uint8_t* __restrict__ kv) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int64_t e = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (e >= n) return;
+    mainkv_encode_warp(x + e * KV_DIM, kv + e * KV_BYTES);
 }
 
 // out[b][t][:] = entry kv_off[b] + idx[b][t] decoded (bf16 [B][k][512]),

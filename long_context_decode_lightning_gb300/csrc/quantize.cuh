@@ -170,29 +170,19 @@ __device__ __forceinline__ int mx_scale_exp(float amax) {
     return e < -127 ? -127 : e;
 }
 
-// One warp per padded row of tensor t (grid over n_tensors * rec_per_tensor * 8
-// rows, 8 per CTA) into 544-byte records: rotation as above, then per group
-// (lanes 8j .. 8j+7 hold values 32j .. 32j+31) the scale exponent and the
-// codes E2M1_RN(v 2^-e). The product by 2^-e (a normal fp32 for every e) is
-// exact unless it falls below the normal range, where every value rounds to a
-// zero code of its sign either way. Rows past rpt are zero (codes 0, scale
-// byte 0). A non-finite rotated value is reported through the error word.
-__global__ void __launch_bounds__(256) quant_mx_kernel(QuantParams p) {
-    griddep_wait();
-    griddep_launch_dependents();
-    const int64_t prow = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int64_t padded_rows = p.rec_per_tensor * 8;
-    if (prow >= p.n_tensors * padded_rows) return;
-    const int64_t t = prow / padded_rows;
-    const int64_t r = prow % padded_rows;
+// Encode one rotated row (this warp's v, valid = a real row) as row r of the
+// 544-byte MXFP4 records at `recs`: per group (lanes 8j .. 8j+7 hold values
+// 32j .. 32j+31) the scale exponent and the codes E2M1_RN(v 2^-e). The product
+// by 2^-e (a normal fp32 for every e) is exact unless it falls below the
+// normal range, where every value rounds to a zero code of its sign either
+// way. A padding row (valid false) is zero: codes 0, scale byte 0.
+__device__ __forceinline__ void encode_row_mx_warp(uint8_t* recs, int64_t r, const float (&v)[4], bool valid) {
     const int lane = threadIdx.x & 31;
-    uint8_t* rec = p.rec + (t * p.rec_per_tensor + r / 8) * 544;
+    uint8_t* rec = recs + (r / 8) * 544;
     const int rr = (int)(r & 7);
     uint16_t codes = 0;
     uint8_t sbyte = 0;
-    if (r < p.rpt) {
-        float v[4];
-        rotate_row_warp(p, t * p.rpt + r, v);
+    if (valid) {
         const bool finite = isfinite(v[0]) && isfinite(v[1]) && isfinite(v[2]) && isfinite(v[3]);
         if (!__all_sync(0xFFFFFFFFu, finite) && lane == 0) raise_error(DEVERR_ARG);
         float a = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
@@ -208,6 +198,22 @@ __global__ void __launch_bounds__(256) quant_mx_kernel(QuantParams p) {
     // values 4*lane .. 4*lane+3 -> two bytes at (e/32)*128 + rr*16 + (e%32)/2
     *reinterpret_cast<uint16_t*>(rec + (lane >> 3) * 128 + rr * 16 + (lane & 7) * 2) = codes;
     if ((lane & 7) == 0) rec[512 + rr * 4 + (lane >> 3)] = sbyte;
+}
+
+// One warp per padded row of tensor t (grid over n_tensors * rec_per_tensor * 8
+// rows, 8 per CTA) into 544-byte records: rotation as above, then the MXFP4
+// encoding. A non-finite rotated value is reported through the error word.
+__global__ void __launch_bounds__(256) quant_mx_kernel(QuantParams p) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int64_t prow = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int64_t padded_rows = p.rec_per_tensor * 8;
+    if (prow >= p.n_tensors * padded_rows) return;
+    const int64_t t = prow / padded_rows;
+    const int64_t r = prow % padded_rows;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (r < p.rpt) rotate_row_warp(p, t * p.rpt + r, v);
+    encode_row_mx_warp(p.rec + t * p.rec_per_tensor * 544, r, v, r < p.rpt);
 }
 
 // Small tensors (at most QUANT_SMALL_ROWS rows, e.g. the 32 heads of a query):

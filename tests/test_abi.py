@@ -84,6 +84,12 @@ def test_host_validation_rejects_bad_arguments(L):
     assert L.hsi_gather_mainkv(fake, fake, fake, fake, 512, 5000, 4, fake, None) == -1
     assert L.hsi_gather_mainkv(fake, fake, fake, fake, 511, 512, 4, fake, None) == -1
     assert L.hsi_gather_mainkv(fake + 4, fake, fake, fake, 512, 512, 4, fake, None) == -1
+    # append_token: NVFP4 needs the tensor scales; main KV needs its buffer and offsets; unaligned rows
+    assert L.hsi_append_token(fake, s8, None, fake, fake, None, None, None, fake, fake, 4, 0, None) == -1
+    assert L.hsi_append_token(fake, s8, fake, fake, fake, fake, None, None, fake, fake, 4, 0, None) == -1
+    assert L.hsi_append_token(fake + 8, s8, fake, fake, fake, None, None, None, fake, fake, 4, 0, None) == -1
+    assert L.hsi_append_token(fake, bad_signs, fake, fake, fake, None, None, None, fake, fake, 4, 0, None) == -1
+    assert L.hsi_append_token(fake, s8, fake, fake, fake, None, None, None, fake, fake, 0, 0, None) == -1
     # quantize_mxfp4: null x, bad signs, unaligned records
     assert L.hsi_quantize_mxfp4(None, 1, 1, s8, fake, None) == -1
     assert L.hsi_quantize_mxfp4(fake, 1, 1, bad_signs, fake, None) == -1
