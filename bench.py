@@ -347,9 +347,19 @@ class DeviceWorkload:
                                             self.pool_scores, K_TOP, self.idx[l], self.val[l], n_keep=wl.n_keep,
                                             ws=self.ws_rtopk, pool_rec=self.pool_rec, pool_rec_ready=False,
                                             fmt=self.fmt))
+        # the pages' masked form of the same layer, kept for comparison: every
+        # visible position scored with the Reindex query, the pool's bit table
+        # applied as -inf, then the top-512
+        def dense():
+            hsi.score_full(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0], self.k_off,
+                           self.n_vis, B, self.maxv, self.scores, fmt=self.fmt)
+            hsi.mask_scores(self.scores, self.n_vis, self.bits, B, self.maxv)
+            hsi.topk(self.scores, self.n_vis, B, self.maxv, K_TOP, self.idx[l], self.val[l], ws=self.ws_topk)
+        dense_us = t(dense)
         pooled_bytes = int(self.nk.clamp(max=wl.n_keep).sum().item()) * self.rec
         return {"layer_us": layer, "first_layer_us": first, "plain_topk_us": topk, "compact_us": compact,
-                "gather_score_us": gather, "pooled_bytes_per_layer": pooled_bytes}
+                "gather_score_us": gather, "dense_masked_layer_us": dense_us,
+                "dense_over_pooled": dense_us / layer, "pooled_bytes_per_layer": pooled_bytes}
 
     def capture(self):
         torch = self.torch

@@ -260,6 +260,22 @@ hsi_status hsi_candidate_pool(const float* scores, int64_t ld, const float* bloc
                               cudaStream_t stream);
 
 /*
+ * The pages' masked form of a Reindex layer, kept for comparison with the
+ * pooled layers: after hsi_score_full has scored every visible position with
+ * the Reindex layer's query, every score of query b at a visible position s
+ * (< n_visible[b]) whose pool bit is clear (bit s%32 of bits[b][s/32], as
+ * written by hsi_candidate_pool or hsi_full_layer) becomes -inf; hsi_topk of
+ * the result is the layer's top-k. Page: "DeepSeek-V4.1 模型结构（3）", section
+ * "候选池的三个细节在代码里" (the Reindex code masks the full score row with the
+ * pool's boolean table and then takes its top-k) and the last paragraph of
+ * "用浅层的打分结果限制深层的打分范围" (16384 of 1M positions: 1/64 of the work).
+ *  scores  (dev) fp32 [B][ld], ld >= max_visible (host bound on n_visible).
+ *  bits    (dev) uint32 [B][ld_bits], ld_bits >= ceil(max_visible / 32).
+ */
+hsi_status hsi_mask_scores(float* scores, int64_t ld, const int32_t* n_visible, const uint32_t* bits, int64_t ld_bits,
+                           int32_t B, int64_t max_visible, cudaStream_t stream);
+
+/*
  * Reindex-layer scores restricted to the pool, reading only pooled K.
  * Page: "DeepSeek-V4.1 模型结构（3）", section "用浅层的打分结果限制深层的打分范围"
  * (Reindex layers score only pooled positions, 16384 x 4096 MACs per token)

@@ -31,7 +31,7 @@ EXPORTS = ["hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_po
            "hsi_workspace_size", "hsi_device_error", "hsi_device_check", "hsi_status_string",
            "hsi_kernel_launches", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer", "hsi_reindex_layer",
            "hsi_topk_noalloc", "hsi_debug_set", "hsi_pool_gather", "hsi_quantize_mxfp4", "hsi_quantize_mainkv",
-           "hsi_gather_mainkv", "hsi_append_token"]
+           "hsi_gather_mainkv", "hsi_append_token", "hsi_mask_scores"]
 
 
 class HsiError(RuntimeError):
@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
         L.hsi_quantize_mainkv.argtypes = [vp, i64, vp, vp]
         L.hsi_gather_mainkv.argtypes = [vp, vp, vp, vp, i64, i32, i32, vp, vp]
         L.hsi_append_token.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, ctypes.c_int, vp]
+        L.hsi_mask_scores.argtypes = [vp, i64, vp, vp, i64, i32, i64, vp]
         L.hsi_score_full.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, vp, i64, vp, i64, ctypes.c_int, vp,
                                      sz, vp]
         L.hsi_topk.argtypes = [vp, i64, vp, i32, i64, i32, vp, i64, i32, vp, vp, vp, sz, vp]
@@ -95,7 +96,8 @@ def lib() -> ctypes.CDLL:
         for name in ("hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
                      "hsi_device_error", "hsi_device_check", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer",
                      "hsi_reindex_layer", "hsi_topk_noalloc", "hsi_debug_set", "hsi_pool_gather",
-                     "hsi_quantize_mxfp4", "hsi_quantize_mainkv", "hsi_gather_mainkv", "hsi_append_token"):
+                     "hsi_quantize_mxfp4", "hsi_quantize_mainkv", "hsi_gather_mainkv", "hsi_append_token",
+                     "hsi_mask_scores"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -207,6 +209,14 @@ def append_token(k_x, signs, g_k, k_rec, k_rec_off, n_visible, capacity, B, kv_x
     _check("hsi_append_token", lib().hsi_append_token(
         _ptr(k_x), s8, _ptr(g_k), _ptr(k_rec), _ptr(k_rec_off), _ptr(kv_x), _ptr(kv), _ptr(kv_off),
         _ptr(n_visible), _ptr(capacity), B, fmt, _stream(stream)))
+
+
+def mask_scores(scores, n_visible, pool_bits, B, max_visible, ld=None, ld_bits=None, stream=None):
+    """The masked Reindex form: -inf at the visible positions outside each query's pool bit table."""
+    ld = scores.shape[-1] if ld is None else ld
+    ld_bits = pool_bits.shape[-1] if ld_bits is None else ld_bits
+    _check("hsi_mask_scores", lib().hsi_mask_scores(_ptr(scores), ld, _ptr(n_visible), _ptr(pool_bits), ld_bits, B,
+                                                    max_visible, _stream(stream)))
 
 
 def rec_bytes(fmt: int = FMT_NVFP4) -> int:

@@ -588,6 +588,16 @@ hsi_status hsi_candidate_pool(const float* scores, int64_t ld, const float* bloc
     return run_select(sp, max_blocks, stream);
 }
 
+hsi_status hsi_mask_scores(float* scores, int64_t ld, const int32_t* n_visible, const uint32_t* bits, int64_t ld_bits,
+                           int32_t B, int64_t max_visible, cudaStream_t stream) {
+    if (!scores || !n_visible || !bits || B <= 0 || B > 65535 || max_visible < 0 || ld < max_visible ||
+        ld_bits < (max_visible + 31) / 32)
+        return HSI_ERR_INVALID_ARG;
+    if (max_visible == 0) return HSI_OK;
+    const dim3 grid((unsigned)((max_visible + 255) / 256), (unsigned)B);
+    return launch(mask_scores_kernel, grid, dim3(256), 0, stream, scores, ld, n_visible, bits, ld_bits);
+}
+
 hsi_status hsi_calib_read(const void* buf, size_t bytes, int method, int chunk, int stages,
                           unsigned long long* sink, cudaStream_t stream) {
     if (!buf || !sink || bytes < 16 || !aligned(buf, 16)) return HSI_ERR_INVALID_ARG;

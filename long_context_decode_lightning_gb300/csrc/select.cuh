@@ -1158,4 +1158,20 @@ __global__ void block_max_kernel(const float* scores, int64_t ld, const int32_t*
     bmax[(int64_t)b * ldb + j] = m;
 }
 
+// The pages' masked Reindex form, for comparison with the pooled layers: a
+// score of query b at a visible position s (< n_visible[b]) whose pool bit
+// (bit s%32 of bits[b][s/32]) is clear becomes -inf. One thread per position
+// (a warp shares one bit word), grid = (ceil(max_visible / 256), B).
+__global__ void __launch_bounds__(256) mask_scores_kernel(float* __restrict__ scores, int64_t ld,
+                                                          const int32_t* __restrict__ n_vis,
+                                                          const uint32_t* __restrict__ bits, int64_t ld_bits) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int b = blockIdx.y;
+    const int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (s >= n_vis[b]) return;
+    const uint32_t m = __ldg(bits + (int64_t)b * ld_bits + (s >> 5));
+    if (!((m >> (s & 31)) & 1u)) scores[(int64_t)b * ld + s] = __uint_as_float(0xFF800000u);
+}
+
 }  // namespace hsi

@@ -90,6 +90,9 @@ def test_host_validation_rejects_bad_arguments(L):
     assert L.hsi_append_token(fake + 8, s8, fake, fake, fake, None, None, None, fake, fake, 4, 0, None) == -1
     assert L.hsi_append_token(fake, bad_signs, fake, fake, fake, None, None, None, fake, fake, 4, 0, None) == -1
     assert L.hsi_append_token(fake, s8, fake, fake, fake, None, None, None, fake, fake, 0, 0, None) == -1
+    # mask_scores: ld or the bit table's stride too short for max_visible
+    assert L.hsi_mask_scores(fake, 99, fake, fake, 4, 1, 100, None) == -1
+    assert L.hsi_mask_scores(fake, 100, fake, fake, 3, 1, 100, None) == -1
     # quantize_mxfp4: null x, bad signs, unaligned records
     assert L.hsi_quantize_mxfp4(None, 1, 1, s8, fake, None) == -1
     assert L.hsi_quantize_mxfp4(fake, 1, 1, bad_signs, fake, None) == -1
