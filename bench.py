@@ -253,6 +253,10 @@ class DeviceWorkload:
             self.ws_rtopk = hsi.workspace(hsi.WS_REINDEX_LAYER, B, wl.n_keep * 8, K_TOP, device=dev)
             self.pool_rec = torch.empty(B, wl.n_keep * REC, dtype=torch.uint8, device=dev)
         self.ev_score = []
+        # the Full layer's top-512 and its pool run on two streams: the pool and the
+        # Reindex layers (which need only the pool) on `side`, joined at the end
+        self.side = torch.cuda.Stream(device=dev)
+        self.ev_fork, self.ev_join = torch.cuda.Event(), torch.cuda.Event()
         self.pool_sum = None
         self.wl_signs = signs
         self.graphs = []
@@ -278,30 +282,47 @@ class DeviceWorkload:
         maxv = self.maxv if maxv is None else maxv
         signs = self.wl_signs
         segs = []
+        torch = self.torch
+
+        def rest():
+            # the first Reindex layer gathers the pooled K records and leaves them
+            # compacted; the later layers of the step stream the compacted pool
+            for r in range(wl.reindex_layers):
+                l = wl.full_layers + r
+                self.quant_q(l)
+                hsi.reindex_layer(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0], self.k_off,
+                                  self.n_vis, self.ids, self.nk, self.npool, B, self.pool_scores, K_TOP,
+                                  self.idx[l], self.val[l], n_keep=wl.n_keep, ws=self.ws_rtopk,
+                                  pool_rec=self.pool_rec, pool_rec_ready=r > 0, fmt=self.fmt)
+
         for l in range(wl.full_layers):
             segs.append(("pre", lambda l=l: self.quant_q(l)))
-            # the Full layer (scores, top-512, pool) as the fused call, issued as
-            # its two phases so that the scoring kernel can be timed alone
+            # the Full layer (scores, top-512, pool) as the fused call, issued in
+            # phases so that the scoring kernel can be timed alone
             pool = wl.build_pool and l == wl.full_layers - 1
-            for kind, ph in (("score", 1), ("post", 2)):
-                segs.append((kind, lambda l=l, pool=pool, ph=ph: hsi.full_layer(
+
+            def fl(ph, l=l, pool=pool):
+                hsi.full_layer(
                     self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[l], self.g_k[l], self.k_off, self.n_vis, B,
                     maxv, self.scores, K_TOP, self.idx[l], self.val[l],
                     block_ids=self.ids if pool else None, n_kept=self.nk if pool else None,
                     n_pool=self.npool if pool else None, pool_bits=self.bits if pool else None,
-                    n_keep=wl.n_keep, ws=self.ws_full, phases=ph, fmt=self.fmt)))
-        if wl.build_pool:
-            def rest():
-                # the first Reindex layer gathers the pooled K records and leaves them
-                # compacted; the later layers of the step stream the compacted pool
-                for r in range(wl.reindex_layers):
-                    l = wl.full_layers + r
-                    self.quant_q(l)
-                    hsi.reindex_layer(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0], self.k_off,
-                                      self.n_vis, self.ids, self.nk, self.npool, B, self.pool_scores, K_TOP,
-                                      self.idx[l], self.val[l], n_keep=wl.n_keep, ws=self.ws_rtopk,
-                                      pool_rec=self.pool_rec, pool_rec_ready=r > 0, fmt=self.fmt)
-            segs.append(("post", rest))
+                    n_keep=wl.n_keep, ws=self.ws_full, phases=ph, fmt=self.fmt)
+            segs.append(("score", lambda fl=fl: fl(hsi.PHASE_SCORE)))
+            if pool:
+                def post(fl=fl):
+                    main = torch.cuda.current_stream()
+                    self.ev_fork.record(main)
+                    self.side.wait_event(self.ev_fork)
+                    fl(hsi.PHASE_TOPK)
+                    with torch.cuda.stream(self.side):
+                        fl(hsi.PHASE_POOL)
+                        rest()
+                        self.ev_join.record(self.side)
+                    main.wait_event(self.ev_join)
+                segs.append(("post", post))
+            else:
+                segs.append(("post", lambda fl=fl: fl(hsi.PHASE_SELECT)))
         merged = []
         for kind, fn in segs:  # fuse neighbouring non-scoring segments into one graph
             if merged and kind != "score" and merged[-1][0] != "score":

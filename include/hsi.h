@@ -411,14 +411,20 @@ hsi_status hsi_append_token(const uint16_t* k_x, const int8_t* signs, const floa
  *  Arguments as in hsi_score_full (group 1, format), hsi_topk (n_valid =
  *  n_visible) and hsi_candidate_pool (block_size 8). scores [B][ld] is written.
  *  block_ids NULL: no pool (n_kept, n_pool, pool_bits ignored).
- *  phases  HSI_PHASE_ALL, or the two halves as separate calls with the same
+ *  phases  HSI_PHASE_ALL, or the parts as separate calls with the same
  *          arguments and workspace, scoring first (the workspace carries the
- *          histograms from one to the other): HSI_PHASE_SCORE, HSI_PHASE_SELECT.
+ *          histograms and block maxima from one to the other):
+ *          HSI_PHASE_SCORE, then HSI_PHASE_SELECT (the top-k, then the pool),
+ *          or HSI_PHASE_TOPK and HSI_PHASE_POOL, which use separate parts of
+ *          the workspace and may run at the same time on two streams (both
+ *          after the scoring call).
  *  ws      (dev) hsi_workspace_size(HSI_WS_FULL_LAYER, B, max_visible, k).
  */
 #define HSI_PHASE_SCORE 1
 #define HSI_PHASE_SELECT 2
 #define HSI_PHASE_ALL 3
+#define HSI_PHASE_TOPK 4
+#define HSI_PHASE_POOL 8
 hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
                           const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible, int32_t B,
                           int64_t max_visible, float* scores, int64_t ld, int32_t k, int32_t* top_idx,

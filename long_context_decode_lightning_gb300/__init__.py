@@ -21,6 +21,7 @@ _SO = os.path.join(_PKG, "libhsi.so")
 _lib = None
 
 HEADS, DIM, REC_ROWS, REC_BYTES, MX_REC_BYTES = 32, 128, 8, 576, 544
+PHASE_SCORE, PHASE_SELECT, PHASE_ALL, PHASE_TOPK, PHASE_POOL = 1, 2, 3, 4, 8
 FMT_NVFP4, FMT_MXFP4 = 0, 1  # hsi_format: NVFP4 (576-byte records, tensor scales) or MXFP4 (544 bytes)
 
 STATUS = {0: "HSI_OK", -1: "HSI_ERR_INVALID_ARG", -2: "HSI_ERR_UNSUPPORTED", -3: "HSI_ERR_CUDA",
@@ -286,7 +287,8 @@ def full_layer(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B, max_visible, 
                block_ids=None, n_kept=None, n_pool=None, pool_bits=None, n_keep=2048, ld=None, ld_bits=0, ws=None,
                phases=3, fmt=FMT_NVFP4, stream=None):
     """Full layer: scores, top-k and (block_ids given) the candidate pool.
-    phases: 1 scoring only, 2 selection only (after 1, same workspace), 3 both."""
+    phases: 1 scoring only, 2 selection only (after 1, same workspace), 3 both;
+    4 the top-k only, 8 the pool only (after 1; the two may run on two streams)."""
     ld = scores.shape[-1] if ld is None else ld
     if pool_bits is not None and not ld_bits:
         ld_bits = pool_bits.shape[-1]

@@ -339,9 +339,9 @@ size_t hsi_workspace_size(hsi_ws_kind kind, int32_t B, int64_t max_n, int32_t k)
         case HSI_WS_QUANTIZE: return align_up((size_t)B * 4, 256);
         case HSI_WS_SCORE: return 0;
         case HSI_WS_TOPK: return sel_ws_bytes(B, max_n, false, 0);
-        case HSI_WS_FULL_LAYER: {
+        case HSI_WS_FULL_LAYER: {  // the top-k's and the pool's selection buffers, the block maxima
             const int64_t nb = (max_n + 7) / 8;
-            return sel_ws_bytes(B, max_n > nb ? max_n : nb, false, 0) + hist_region_bytes(B) +
+            return sel_ws_bytes(B, max_n, false, 0) + sel_ws_bytes(B, nb, false, 0) +
                    align_up((size_t)B * (size_t)nb * 4, 256);
         }
         case HSI_WS_REINDEX_LAYER:  // + the key histogram the pooled scan accumulates
@@ -637,7 +637,9 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
                           float* top_val, int32_t n_keep, int32_t* block_ids, int32_t* n_kept, int32_t* n_pool,
                           uint32_t* pool_bits, int64_t ld_bits, int32_t phases, hsi_format format, void* ws,
                           size_t ws_bytes, cudaStream_t stream) {
-    if (phases < 1 || phases > 3) return HSI_ERR_INVALID_ARG;
+    if (phases != HSI_PHASE_SCORE && phases != HSI_PHASE_SELECT && phases != HSI_PHASE_ALL &&
+        phases != HSI_PHASE_TOPK && phases != HSI_PHASE_POOL)
+        return HSI_ERR_INVALID_ARG;
     hsi_status st = check_score_common(format, q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B);
     if (st != HSI_OK) return st;
     if (!scores || !top_idx || !top_val || max_visible < 0 || max_visible > (int64_t)INT32_MAX - 256 ||
@@ -645,16 +647,17 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
         return HSI_ERR_INVALID_ARG;
     const bool pool = block_ids != nullptr;
     if (pool && (!n_kept || !n_pool || n_keep < 1 || n_keep > SEL_MAXK)) return HSI_ERR_INVALID_ARG;
+    if (phases == HSI_PHASE_POOL && !pool) return HSI_ERR_INVALID_ARG;
     if (pool_bits && ld_bits < (max_visible + 31) / 32) return HSI_ERR_INVALID_ARG;
     const int64_t nb = (max_visible + 7) / 8;
     const size_t need = hsi_workspace_size(HSI_WS_FULL_LAYER, B, max_visible, k);
     if (!ws || ws_bytes < need || !aligned(ws, 256)) return HSI_ERR_WORKSPACE;
-    // workspace: selection buffers (shared by the two selections, which run in
-    // turn), the block-max histogram, the block maxima
-    SelWs wsp = carve_sel(ws, B, max_visible > nb ? max_visible : nb, false, 0);
-    uint8_t* tail = static_cast<uint8_t*>(ws) + sel_ws_bytes(B, max_visible > nb ? max_visible : nb, false, 0);
-    uint32_t* bhist = reinterpret_cast<uint32_t*>(tail);
-    float* bmax = reinterpret_cast<float*>(tail + hist_region_bytes(B));
+    // workspace: the top-k's selection buffers, the pool's (separate, so that the
+    // two selections may run at the same time on two streams), the block maxima
+    SelWs wsp = carve_sel(ws, B, max_visible, false, 0);
+    uint8_t* wpool = static_cast<uint8_t*>(ws) + sel_ws_bytes(B, max_visible, false, 0);
+    SelWs wpp = carve_sel(wpool, B, nb, false, 0);
+    float* bmax = reinterpret_cast<float*>(wpool + sel_ws_bytes(B, nb, false, 0));
     const bool big_topk = max_visible > SEL_CAP;
     if (phases & 1) {
     if (big_topk && zero_async(wsp.hist, (size_t)B * HIST_BINS * 4, stream) != HSI_OK) return HSI_ERR_CUDA;
@@ -678,7 +681,9 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     st = launch_score<1, false, kDecodeStages, kDecodeUT>(p, format, stream);
     if (st != HSI_OK) return st;
     }
-    if (!(phases & 2)) return HSI_OK;
+    const bool do_topk = phases == HSI_PHASE_ALL || phases == HSI_PHASE_SELECT || phases == HSI_PHASE_TOPK;
+    const bool do_pool = pool && (phases == HSI_PHASE_ALL || phases == HSI_PHASE_SELECT || phases == HSI_PHASE_POOL);
+    if (do_topk) {
     SelParams sp{};
     sp.src = scores;
     sp.ld = ld;
@@ -700,17 +705,23 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
         sp.ld_bmax = nb;
     }
     st = run_select(sp, max_visible, stream, true);
-    if (st != HSI_OK || !pool) return st;
-    SelParams pp = sp;
-    pp.blk_max = nullptr;
+    if (st != HSI_OK) return st;
+    }
+    if (!do_pool) return HSI_OK;
+    SelParams pp{};
     pp.src = bmax;
     pp.ld = nb;
+    pp.n_src = n_visible;
     pp.div = 8;
+    pp.B = B;
     pp.k = n_keep;
     pp.mode = SEL_POOL;
-    pp.hist = bhist;
-    pp.out_idx = nullptr;
-    pp.out_val = nullptr;
+    pp.hist = wpp.hist;
+    pp.cand_cnt = wpp.cnt;
+    pp.cand_key = wpp.ckey;
+    pp.cand_idx = wpp.cidx;
+    pp.thr = wpp.cnt ? wpp.cnt + B : nullptr;
+    pp.cap = kCandCap;
     pp.blk_out = block_ids;
     pp.n_kept = n_kept;
     pp.n_pool = n_pool;

@@ -365,6 +365,17 @@ def test_full_and_reindex_layer_match_separate_calls(lengths):
     assert torch.equal(nk_r, nk_f) and torch.equal(np_r, np_f) and torch.equal(bits_r, bits_f)
     for b in range(B):
         assert torch.equal(ids_r[b, :int(nk_f[b])], ids_f[b, :int(nk_f[b])])
+    # the two selections as separate phases, the pool first: separate parts of
+    # the workspace, so their order (or running them on two streams) is free
+    i_r.fill_(7), v_r.fill_(7), ids_r.fill_(7), nk_r.fill_(7), np_r.fill_(7), bits_r.zero_()
+    for phases in (hsi.PHASE_SCORE, hsi.PHASE_POOL, hsi.PHASE_TOPK):
+        hsi.full_layer(q_rec, g_q, w, caches.k_rec, caches.g, off, nv, B, maxv, s_r, 512, i_r, v_r, block_ids=ids_r,
+                       n_kept=nk_r, n_pool=np_r, pool_bits=bits_r, ws=ws, phases=phases)
+    assert hsi.device_error() == 0
+    assert torch.equal(i_r, i_f) and torch.equal(v_r, v_f)
+    assert torch.equal(nk_r, nk_f) and torch.equal(np_r, np_f) and torch.equal(bits_r, bits_f)
+    for b in range(B):
+        assert torch.equal(ids_r[b, :int(nk_f[b])], ids_f[b, :int(nk_f[b])])
 
     q1, g1, w1 = gpu_queries(wl, 1, range(B))
     ps_sep = torch.empty(B, 2048 * 8, device=DEV)
