@@ -43,7 +43,7 @@ extern "C" {
 typedef enum {
     HSI_OK = 0,
     HSI_ERR_INVALID_ARG = -1,    /* a null pointer, a bad size or a misaligned buffer */
-    HSI_ERR_UNSUPPORTED = -2,    /* a valid request this build does not serve (device, shape) */
+    HSI_ERR_UNSUPPORTED = -2,    /* a valid request the library does not serve (device, shape) */
     HSI_ERR_CUDA = -3,           /* a CUDA runtime call failed (launch, attribute, sync) */
     HSI_ERR_DEVICE_TIMEOUT = -4, /* a kernel's bounded wait ran out (reported by hsi_device_error) */
     HSI_ERR_WORKSPACE = -5,      /* ws is NULL, too small or not 256-byte aligned */
