@@ -60,9 +60,6 @@ __host__ __device__ constexpr int rec_bytes() {
 }
 constexpr int TILE_KEYS = 128;
 constexpr int IDS_AHEAD = 8;  // gather: units of block ids prefetched ahead
-#ifndef HSI_GATHER_BULK
-#define HSI_GATHER_BULK 0
-#endif
 
 struct ScoreParams {
     const uint8_t* q_rec;
@@ -110,9 +107,8 @@ struct ScoreCfg {
     static constexpr int Q_BYTES = NQ * 4 * REC;
     static constexpr int STAGE_BYTES = UNIT_RECS * REC;
     static constexpr int QSLOT_BYTES = ((Q_BYTES + 127) / 128) * 128;
-    // gather: one bulk copy per pooled block from one warp, or a warpgroup of 16-byte async copies
-    static constexpr bool GBULK = GATHER && HSI_GATHER_BULK;
-    static constexpr int PROD_WARPS = GATHER && !GBULK ? 4 : 1;
+    // gather: a warpgroup of 16-byte async copies (4 threads per pooled block)
+    static constexpr int PROD_WARPS = GATHER ? 4 : 1;
     static constexpr int MMA_WARP = PROD_WARPS;
     static constexpr int FIRST_SF_WARP = PROD_WARPS + 1;
     static constexpr int FIRST_EPI_WARP = FIRST_SF_WARP + 4;
@@ -151,9 +147,8 @@ struct ScoreCfg {
     static_assert(NQ <= 4, "B scale rows fit one 128-row layout");
     static_assert(COLS_USED <= 512, "TMEM");
     static_assert(NACC % EPI_GROUPS == 0, "accumulator sets split evenly between epilogue groups");
-    static_assert(!GATHER || (NQ == 1 && (GBULK ? UNIT_RECS % 32 == 0 : UNIT_RECS == 32)),
-                  "gather: one lane per block (bulk) or 4 producer threads per block");
-    static_assert(!GATHER || GBULK || COPY_AHEAD < STAGES, "gather: copies in flight fit the ring");
+    static_assert(!GATHER || (NQ == 1 && UNIT_RECS == 32), "gather: 4 producer threads per block");
+    static_assert(!GATHER || COPY_AHEAD < STAGES, "gather: copies in flight fit the ring");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
@@ -395,7 +390,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS
 
     if (warp == 0) {
         for (int s = lane; s < STAGES; s += 32) {
-            mbar_init(&full[s], GATHER && !C::GBULK ? C::PROD_WARPS : 1);
+            mbar_init(&full[s], GATHER ? C::PROD_WARPS : 1);
             mbar_init(&sfready[s], 4);
             mbar_init(&empty[s], 1);
         }
@@ -502,42 +497,6 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS
                     bulk_g2s(dst, p.k_rec + (k_base + (int64_t)t * C::UNIT_RECS) * C::REC, (uint32_t)(nrec * C::REC),
                              &full[st.i]);
                 }
-            } else if constexpr (C::GBULK) {
-                // one lane per pooled block: a 576-byte bulk copy of the whole record
-                constexpr int PER = C::UNIT_RECS / 32;
-                const int islot = (int)(u % IDS_AHEAD);
-                int64_t ids_l[PER];
-                bool ok_l[PER];
-                uint32_t nvalid = 0;
-#pragma unroll
-                for (int i = 0; i < PER; ++i) {
-                    const int blk = lane + 32 * i;
-                    const int j = t * C::UNIT_RECS + blk;
-                    ids_l[i] = ids_ring[islot * C::UNIT_RECS + blk];
-                    ok_l[i] = j < nk && ids_l[i] >= 0 && ids_l[i] < nrec_all;
-                    if (j < nk && !ok_l[i]) raise_error(DEVERR_ARG);
-                    nvalid += __popc(__ballot_sync(0xFFFFFFFFu, ok_l[i]));
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&ids_free[islot]);
-                    mbar_arrive_expect_tx(&full[st.i], nvalid * C::REC);
-                }
-                __syncwarp();
-#pragma unroll
-                for (int i = 0; i < PER; ++i)
-                    if (ok_l[i])
-                        bulk_g2s(dst + (lane + 32 * i) * C::REC, p.k_rec + (k_base + ids_l[i]) * C::REC, C::REC, &full[st.i]);
-                if (fetched < count) {
-                    if (u >= 1) {
-                        const int prev = (int)((u - 1) % IDS_AHEAD);
-                        if (!wait_traced(&ids_free[prev], (uint32_t)(((u - 1) / IDS_AHEAD) & 1), sh, tr,
-                                         TR_PROD_IDS))
-                            break;
-                        fence_proxy_async_smem();  // the slot's reads precede the copy that refills it
-                    }
-                    fetch_ids();
-                }
             } else {
                 // 4 threads per pooled block, up to 9 x 16 bytes each (36 chunks of an
                 // NVFP4 record, 34 of an MXFP4 one)
@@ -584,7 +543,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS
             st.next(STAGES);
             it.next(p);
         }
-        if (GATHER && !C::GBULK) {
+        if (GATHER) {
             // publish the units still in flight, then nothing is left pending
             cp_async_wait<0>();
             fence_proxy_async_smem();
@@ -596,7 +555,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS
         }
         // drain: every bulk copy issued must have landed before the CTA exits
         if (leader) {
-            if (!GATHER || C::GBULK)
+            if (!GATHER)
                 for (long long v = issued_units > STAGES ? issued_units - STAGES : 0; v < issued_units; ++v)
                     wait_drain(&full[(int)(v % STAGES)], (uint32_t)((v / STAGES) & 1));
             for (int slot = 0; slot < 2; ++slot)
