@@ -8,8 +8,12 @@ One step = one pass of the whole path over the resident workload:
                   (blocks of 8, keep 2048, newest pinned, boolean bit table),
                   and per Reindex layer: quantise q, score only the pooled
                   keys (whole 576-byte blocks gathered), exact top-512.
-The headline runs on NVFP4 records (72 B per key); the `mxfp4` object repeats
-the step on MXFP4 records (68 B per key, the pages' own indexer format).
+The headline runs on NVFP4 records (72 B per key). After the timed steps the
+JSON line also carries:
+  mxfp4          the step on MXFP4 records (68 B per key, the pages' own format);
+  reindex        one Reindex layer timed alone, and the pages' dense masked form;
+  mainkv_gather  gather(main_kv, topk) of every layer's top-512 from the FP4 main KV;
+  serve          decode steps over growing caches (append, step, gathers per token).
 The default workload is 64 decode queries at 1,048,576 visible keys each with
 4 Reindex layers. K caches are generated from the seeded recipe, quantised on
 the GPU and stay resident (4.83 GB > L2, so no L2 flush is needed).
