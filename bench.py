@@ -284,7 +284,6 @@ class DeviceWorkload:
         caches' capacity for a step over growing caches)."""
         hsi, wl, B = self.hsi, self.wl, self.B
         maxv = self.maxv if maxv is None else maxv
-        signs = self.wl_signs
         segs = []
         torch = self.torch
 

@@ -55,7 +55,6 @@ def test_workspace_sizes(L):
 
 @needs_nvcc
 def test_host_validation_rejects_bad_arguments(L):
-    vp = ctypes.c_void_p
     fake = 1 << 20  # never dereferenced: validation fails first
     s8 = (ctypes.c_int8 * 128)(*([1] * 128))
     bad_signs = (ctypes.c_int8 * 128)(*([2] * 128))

@@ -89,7 +89,6 @@ def test_gather_topk_of_several_caches():
     wider index buffer (ld 600) holds a top-512-style list: its own positions,
     -1 padding past a short cache."""
     lengths = [5, 300, 20000]
-    wl = inputs.workload(1)
     xs = [inputs.normal_bf16(40 + j, 82, n * 512).reshape(n, 512) for j, n in enumerate(lengths)]
     kv_h = [oracle.mainkv_quantize(x) for x in xs]
     kv = torch.cat([_gpu_kv(x) for x in xs])
@@ -106,7 +105,6 @@ def test_gather_topk_of_several_caches():
     got = out.cpu().numpy().view(np.uint16)
     for b, n in enumerate(lengths):
         assert np.array_equal(got[b], oracle.mainkv_gather(kv_h[b], n, idx[b, :512])), b
-    del wl
 
 
 def test_gather_index_past_the_cache_is_reported_and_zeroed():

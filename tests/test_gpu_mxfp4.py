@@ -14,7 +14,7 @@ import torch
 
 import inputs
 import oracle
-from cases import DEV, Caches, dev_bf16, gpu_queries, gpu_quantize_mx, i32, i64, oracle_query
+from cases import DEV, Caches, gpu_queries, gpu_quantize_mx, i32, i64, oracle_query
 
 import long_context_decode_lightning_gb300 as hsi
 

@@ -4,7 +4,6 @@ Each test checks the oracle against something other than itself: values printed
 on the pages (tests/golden), library routines (torch's fp8 cast, scipy's
 Hadamard matrix, Python's sort), closed forms, invariants and brute force.
 """
-import itertools
 import math
 
 import numpy as np
