@@ -544,22 +544,26 @@ def serving_steps(W: DeviceWorkload, M: MainKV, wl: inputs.Workload, dev, args, 
                     "by two device copies"}
 
 
-def oracle_sample_setup(wl: inputs.Workload, nq: int):
-    """Oracle inputs for the first nq queries (quantised by the oracle itself)."""
+def oracle_sample_setup(wl: inputs.Workload, nq: int, fmt: str = "nvfp4"):
+    """Oracle inputs for the first nq queries (quantised by the oracle itself, in
+    the record format fmt: "nvfp4" or "mxfp4")."""
     import oracle
     signs = wl.signs()
     L = wl.full_layers + (wl.reindex_layers if wl.build_pool else 0)
 
+    def quant(x):
+        return (oracle.quantize_mx(x, signs), 1.0) if fmt == "mxfp4" else oracle.quantize(x, signs)
+
     def prep(b):
         s = wl.query_seq[b]
-        ks = [oracle.quantize(wl.k_bf16(l, s), signs) for l in range(wl.full_layers)]
-        qs = [oracle.quantize(wl.q_bf16(l, b), signs) + (wl.w(l, b),) for l in range(L)]
+        ks = [quant(wl.k_bf16(l, s)) for l in range(wl.full_layers)]
+        qs = [quant(wl.q_bf16(l, b)) + (wl.w(l, b),) for l in range(L)]
         return ks, qs
 
     return oracle.map_queries(prep, list(range(nq)), threads=nq)
 
 
-def oracle_query_step(wl: inputs.Workload, b: int, ks, qs):
+def oracle_query_step(wl: inputs.Workload, b: int, ks, qs, fmt: str = "nvfp4"):
     """The whole path for one query on the oracle; returns pairs scored."""
     import oracle
     n = wl.n_visible[b]
@@ -568,7 +572,7 @@ def oracle_query_step(wl: inputs.Workload, b: int, ks, qs):
     for l in range(wl.full_layers):
         qrec, gq, w = qs[l]
         krec, gk = ks[l]
-        scores, _ = oracle.score_full(qrec, gq, w, krec, gk, n)
+        scores, _ = oracle.score_full(qrec, gq, w, krec, gk, n, fmt=fmt)
         oracle.topk(scores, n, K_TOP)
         pairs += n
     if wl.build_pool:
@@ -576,16 +580,17 @@ def oracle_query_step(wl: inputs.Workload, b: int, ks, qs):
         krec, gk = ks[0]
         for r in range(wl.reindex_layers):
             qrec, gq, w = qs[wl.full_layers + r]
-            ps, _ = oracle.score_pool(qrec, gq, w, krec, gk, n, ids, nk, wl.n_keep, wl.block_size)
+            ps, _ = oracle.score_pool(qrec, gq, w, krec, gk, n, ids, nk, wl.n_keep, wl.block_size, fmt=fmt)
             oracle.topk_pool(ps, npool, ids, K_TOP, wl.block_size)
             pairs += npool
     return pairs
 
 
-def oracle_timed(wl, prepared, nq):
+def oracle_timed(wl, prepared, nq, fmt: str = "nvfp4"):
     import oracle
     t0 = time.perf_counter()
-    pairs = oracle.map_queries(lambda b: oracle_query_step(wl, b, *prepared[b]), list(range(nq)), threads=nq)
+    pairs = oracle.map_queries(lambda b: oracle_query_step(wl, b, *prepared[b], fmt=fmt), list(range(nq)),
+                               threads=nq)
     return sum(pairs), time.perf_counter() - t0
 
 
@@ -626,19 +631,19 @@ def main():
     config = {"workload": wl.name, "queries": wl.B, "context": max(wl.n_visible), "full_layers": wl.full_layers,
               "reindex_layers": wl.reindex_layers if wl.build_pool else 0, "k": K_TOP,
               "block": wl.block_size if wl.build_pool else None, "keep": wl.n_keep if wl.build_pool else None,
-              "l2": "no flush: resident inputs exceed L2"}
+              "format": args.format, "l2": "no flush: resident inputs exceed L2"}
 
     if args.impl == "reference":
         if rank != 0:
             return
         nq = cpu_sample_size(wl)
         log(f"oracle sample: {nq} queries of {wl.name}")
-        prepared = oracle_sample_setup(wl, nq)
+        prepared = oracle_sample_setup(wl, nq, args.format)
         for _ in range(args.warmup):
-            oracle_timed(wl, prepared, nq)
+            oracle_timed(wl, prepared, nq, args.format)
         tot_pairs, tot_t = 0, 0.0
         for _ in range(args.steps):
-            p, t = oracle_timed(wl, prepared, nq)
+            p, t = oracle_timed(wl, prepared, nq, args.format)
             tot_pairs += p
             tot_t += t
         v = tot_pairs / tot_t
@@ -806,8 +811,8 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         nq = cpu_sample_size(wl)
         log(f"cpu baseline: oracle on {nq} queries")
-        prepared = oracle_sample_setup(wl, nq)
-        p, t = oracle_timed(wl, prepared, nq)
+        prepared = oracle_sample_setup(wl, nq, args.format)
+        p, t = oracle_timed(wl, prepared, nq, args.format)
         line["cpu_baseline"] = {"value": p / t, "unit": UNIT, "cores": nq, "kind": "oracle",
                                 "sample": f"{nq} of {wl.B} queries, whole path per query (one thread each), "
                                           f"{t:.1f} s wall"}
