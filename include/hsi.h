@@ -220,6 +220,10 @@ hsi_status hsi_topk(const float* scores, int64_t ld, const int32_t* n_valid, int
  *    zero itself; calls whose work overlaps on the GPU (other streams, other
  *    host threads) race on the array and must be ordered by the caller.
  *  - No call allocates or frees memory.
+ *  - The fixed scratch keeps at most 16384 survivors of the histogram pass
+ *    per query (hsi_topk keeps 65536). A row with more (heavy ties near the
+ *    k-th score) is selected by re-reading it from `scores`: the same result,
+ *    more slowly than hsi_topk.
  */
 hsi_status hsi_topk_noalloc(const float* scores, int64_t ld, const int32_t* n_valid, int32_t B, int64_t max_valid,
                             int32_t k, const int32_t* block_ids, int64_t ld_blocks, int32_t block_size,

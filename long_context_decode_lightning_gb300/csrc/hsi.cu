@@ -90,6 +90,25 @@ int sm_count() {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+constexpr int kMaxDevices = 64;
+
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per device: the attribute is a property of the kernel on one
+// device, so a process that drives several GPUs sets it on each. `done` is
+// the caller's per-kernel table of devices already set; a race between host
+// threads only sets the same value twice.
+template <typename Kernel>
+hsi_status smem_attr_once(Kernel kernel, int bytes, std::atomic<bool> (&done)[kMaxDevices]) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return HSI_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return HSI_ERR_UNSUPPORTED;
+    if (done[dev].load(std::memory_order_acquire)) return HSI_OK;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return HSI_ERR_CUDA;
+    done[dev].store(true, std::memory_order_release);
+    return HSI_OK;
+}
+
 // Workspace of the selection passes for B queries of at most max_items items.
 // A histogram region: [B][HIST_BINS] counts, then [B] counters of the
 // histogram CTAs done (zeroed together).
@@ -171,13 +190,8 @@ hsi_status run_select(SelParams sp, int64_t max_items, cudaStream_t s, bool hist
             return HSI_ERR_CUDA;
         }
     }
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(sel_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)sizeof(SelSmem)) != cudaSuccess)
-            return HSI_ERR_CUDA;
-        attr_set = true;
-    }
+    static std::atomic<bool> attr_set[kMaxDevices];
+    if (smem_attr_once(sel_final_kernel, (int)sizeof(SelSmem), attr_set) != HSI_OK) return HSI_ERR_CUDA;
     return launch(sel_final_kernel, dim3(sp.B), dim3(SEL_THREADS), sizeof(SelSmem), s, sp);
 }
 
@@ -209,13 +223,9 @@ SelParams topk_params(const float* scores, int64_t ld, const int32_t* n_valid, i
 template <int NQ, bool GATHER, int STAGES, int UT, int FMT>
 hsi_status launch_score_fmt(const ScoreParams& p, cudaStream_t s) {
     using C = ScoreCfg<NQ, GATHER, STAGES, UT, FMT>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(score_kernel<NQ, GATHER, STAGES, UT, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::SMEM_BYTES) != cudaSuccess)
-            return HSI_ERR_CUDA;
-        attr_set = true;
-    }
+    static std::atomic<bool> attr_set[kMaxDevices];
+    if (smem_attr_once(score_kernel<NQ, GATHER, STAGES, UT, FMT>, C::SMEM_BYTES, attr_set) != HSI_OK)
+        return HSI_ERR_CUDA;
     const int sms = sm_count();
     if (sms <= 0) return HSI_ERR_CUDA;
     return launch(score_kernel<NQ, GATHER, STAGES, UT, FMT>, dim3(sms), dim3(C::THREADS), C::SMEM_BYTES, s, p);
@@ -238,10 +248,13 @@ int64_t format_rec_bytes(hsi_format fmt) { return fmt == HSI_FMT_MXFP4 ? 544 : 5
 // library holds it (8 MiB) until the process exits, and every call of
 // hsi_topk_noalloc on a device shares it.
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
-constexpr int kNoAllocCandCap = 16384;  // survivors kept per query (more: the row is re-read)
+// Survivors of the histogram pass kept per query. It equals the final kernel's
+// shared-memory capacity, so a noalloc call never takes the final kernel's
+// middle branch (survivors selected in global memory): a query with more
+// survivors than this (heavy ties near the k-th key) re-reads its row instead.
+constexpr int kNoAllocCandCap = 16384;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
 void* g_noalloc_ptr[kMaxDevices] = {};
 std::mutex g_noalloc_mu;
 

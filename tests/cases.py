@@ -84,3 +84,19 @@ def i32(v):
 
 def i64(v):
     return torch.tensor(v, dtype=torch.int64, device=DEV)
+
+
+def assert_sets_match_except_near_ties(got, want, value, tol, kth):
+    """End-to-end selections from two score computations that each lie within
+    a per-item tolerance of the exact value: the sets may differ only in items
+    whose oracle value lies near the k-th value. If item x is in one set but
+    not the other, some item y of the symmetric difference was ranked the other
+    way round, and |v_x - kth| <= |v_x - v_y| <= tol(x) + tol(y); so every item
+    x of the difference must satisfy |v_x - kth| <= tol(x) + max_y tol(y).
+    value(x), tol(x): the oracle's value and tolerance of item x."""
+    diff = set(int(x) for x in got) ^ set(int(x) for x in want)
+    if not diff:
+        return
+    slack = max(tol(x) for x in diff)
+    for x in diff:
+        assert abs(value(x) - kth) <= tol(x) + slack, (x, value(x), kth, tol(x), slack)

@@ -10,7 +10,7 @@ import torch
 
 import inputs
 import oracle
-from cases import DEV, Caches, gpu_queries, gpu_quantize, i32, i64, oracle_query
+from cases import DEV, Caches, assert_sets_match_except_near_ties, gpu_queries, gpu_quantize, i32, i64, oracle_query
 
 import long_context_decode_lightning_gb300 as hsi
 
@@ -285,9 +285,12 @@ def test_score_pool_within_tolerance_and_reindex_topk(lengths):
 
 # ---------------------------------------------------------------- end to end --
 
-def test_end_to_end_topk_sets_match_except_near_ties():
-    """Oracle's own path vs the GPU path: sets agree except positions whose
-    oracle score is within the tolerance of the k-th score."""
+def test_end_to_end_topk_and_pool_match_except_near_ties():
+    """Oracle's own path vs the GPU path: top-512 sets agree except positions
+    whose oracle score is within tolerance of the k-th score, and pools agree
+    except blocks whose oracle block maximum is within tolerance of the
+    2048th block value (a block maximum's tolerance is the largest of its
+    positions')."""
     wl = inputs.workload(0)
     n = 32768
     caches, sg, _ = _score_case(wl, [n])
@@ -297,10 +300,23 @@ def test_end_to_end_topk_sets_match_except_near_ties():
     so, _ = oracle.score_full(qrec, gq, w, krec, gk, n)
     _, tol = oracle.score_rows(qrec, gq, w, krec, gk, np.arange(n))
     oidx, oval = oracle.topk(so, n, 512)
-    kth = oval[-1]
-    diff = set(gidx[0].tolist()) ^ set(oidx.tolist())
-    for p in diff:
-        assert abs(so[p] - kth) <= 2 * tol[p], p
+    assert_sets_match_except_near_ties(gidx[0], oidx, lambda p: so[p], lambda p: tol[p], oval[-1])
+    # pools: the GPU's pool of its own scores vs the oracle's pool of its scores
+    nv = i32([n])
+    gids = torch.empty(1, 2048, dtype=torch.int32, device=DEV)
+    gnk, gnp = torch.empty(1, dtype=torch.int32, device=DEV), torch.empty(1, dtype=torch.int32, device=DEV)
+    hsi.candidate_pool(nv, 1, n, gids, gnk, gnp, scores=torch.from_numpy(sg).to(DEV))
+    oids, onk, _, _ = oracle.pool(so, n)
+    nblk = (n + 7) // 8
+    bmax_o = so[: nblk * 8].reshape(nblk, 8).max(1)
+    btol = tol[: nblk * 8].reshape(nblk, 8).max(1)
+    ranked = np.lexsort((np.arange(nblk), -bmax_o))
+    ranked = ranked[ranked != nblk - 1]  # the pinned newest block ranks first on both sides
+    kth_block = bmax_o[ranked[2048 - 2]]
+    assert int(gnk[0]) == onk == 2048
+    assert nblk - 1 in set(gids[0].tolist()) and nblk - 1 in set(oids[:onk].tolist())
+    assert_sets_match_except_near_ties(gids[0].cpu().numpy(), oids[:onk], lambda j: bmax_o[j], lambda j: btol[j],
+                                       kth_block)
 
 
 # ------------------------------------------------------- composite layers --

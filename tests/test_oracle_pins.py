@@ -148,6 +148,43 @@ def test_quantize_error_within_half_step():
             del sc
 
 
+def test_quantize_codes_and_scales_are_brute_force_nearest():
+    """Every NVFP4 scale byte is torch's E4M3 cast (round to nearest even,
+    saturating at 448) of amax_b / (6 g) in fp32, and every code is the nearest
+    E2M1 magnitude (ties to the even code, saturating at 6) of y / (E4M3(sb) g)
+    with the sign of y; g = amax_T / 2688 in fp32."""
+    rows = 24
+    x = _rand_tensor(13, rows)
+    x[5] = 0  # an all-zero row: every block scale 0, every code 0
+    s = inputs.signs(13)
+    rec, g = oracle.quantize(x, s)
+    xf = inputs.bf16_to_f32(x)
+    y = np.stack([oracle.fwht128((xf[r] * s).astype(np.float32)) for r in range(rows)])
+    assert np.float32(g) == np.float32(np.abs(y).max()) / np.float32(2688)
+    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    six_g = np.float32(6) * np.float32(g)
+    for r in range(rows):
+        d = oracle.decode_row(rec, r, g)
+        for grp in range(8):
+            yb = y[r, 16 * grp:16 * grp + 16]
+            ratio = min(np.float32(np.abs(yb).max()) / six_g, np.float32(448))
+            sb = torch.tensor([ratio], dtype=torch.float32).to(torch.float8_e4m3fn)
+            assert rec[(r // 8) * 576 + 512 + (r % 8) * 8 + grp] == sb.view(torch.uint8).item()
+            sbv = float(sb.to(torch.float64).item())
+            sc = np.float32(np.float32(sbv) * np.float32(g))
+            for t in range(16):
+                if sc == 0:
+                    c = 0
+                else:
+                    a = float(np.abs(yb[t]) / sc)  # fp32 division, as the recipe states
+                    dist = np.abs(mags - a)
+                    best = np.flatnonzero(dist == dist.min())
+                    c = best[0] if best.size == 1 else best[best % 2 == 0][0]
+                want = math.copysign(mags[c] * sbv * g, float(yb[t]))
+                assert d[16 * grp + t] == want or (mags[c] == 0 and d[16 * grp + t] == 0)
+    assert np.all(oracle.decode_row(rec, 5, g) == 0)
+
+
 def test_quantize_mode1_reuses_scale_and_is_deterministic():
     x = _rand_tensor(5, 17)
     s = inputs.signs(5)

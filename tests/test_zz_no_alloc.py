@@ -55,6 +55,37 @@ def test_noalloc_matches_topk_on_two_calls_in_a_row():
     assert torch.equal(g_i, r_i) and torch.equal(g_v, r_v)
 
 
+def test_noalloc_heavy_ties_take_the_row_reread_path():
+    # 20000 items of row 1 tie above every other item: more survivors than the
+    # fixed scratch keeps per query (16384), so this call selects by re-reading
+    # the row while hsi_topk selects over the survivors it kept in its
+    # workspace; both must give the same exact order (index ascending in ties)
+    s = _rows(5, 3, 100000)
+    s[1, ::5] = s[1].max() + 1.0
+    r_i, r_v, g_i, g_v = _both(s, [100000, 100000, 99000], 512)
+    assert torch.equal(g_i, r_i) and torch.equal(g_v, r_v)
+    assert torch.equal(r_i[1].cpu(), torch.arange(0, 5 * 512, 5, dtype=torch.int32))
+
+
+def test_noalloc_with_block_map():
+    # pool-local rows reported as global positions through a block map
+    B, n_keep, bs = 4, 2048, 8
+    s = _rows(6, B, n_keep * bs)
+    g = torch.Generator(device="cpu").manual_seed(7)
+    ids = torch.stack([torch.sort(torch.randperm(40000, generator=g)[:n_keep]).values for _ in range(B)])
+    ids = ids.to(torch.int32).cuda()
+    nv = torch.tensor([n_keep * bs, 9000, n_keep * bs - 3, 17000], dtype=torch.int32, device="cuda")
+    for k in (512, 100):
+        ref_i = torch.empty(B, k, dtype=torch.int32, device="cuda")
+        ref_v = torch.empty(B, k, device="cuda")
+        hsi.topk(s, nv, B, n_keep * bs, k, ref_i, ref_v, block_ids=ids, block_size=bs)
+        got_i = torch.full((B, k), 7, dtype=torch.int32, device="cuda")
+        got_v = torch.full((B, k), 7.0, device="cuda")
+        hsi.topk_noalloc(s, nv, B, n_keep * bs, k, got_i, got_v, block_ids=ids, block_size=bs)
+        assert hsi.device_error() == 0
+        assert torch.equal(got_i, ref_i) and torch.equal(got_v, ref_v)
+
+
 def test_noalloc_short_rows_need_no_scratch_and_oversize_is_refused():
     s = _rows(3, 200, 4000)  # rows of at most 16384 items: any number of queries
     r_i, r_v, g_i, g_v = _both(s, [4000] * 200, 512)
