@@ -437,6 +437,33 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
                           size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * A chunked-prefill layer in one call: the scores of every visible key with
+ * groups of `group` consecutive queries sharing one cache and one tensor-core
+ * tile (as hsi_score_full), then per query its top-k and (block_ids != NULL)
+ * its candidate pool, equal to what hsi_topk and hsi_candidate_pool give on
+ * the same scores. The selection reads the block maxima the scoring kernel
+ * writes, not the score rows: a top-k position lies in one of the first k
+ * blocks by (block max desc, block asc), since the maximum of every block
+ * ranked ahead of its own outranks it, so only the scores of the first k + 1
+ * blocks of the pool's order (the newest block pinned first) are read.
+ * Page: "DeepSeek-V4.1 模型结构（3）", sections "Reindex 层每个 token 要给 100 万条
+ * 打分" (the score), "用浅层的打分结果限制深层的打分范围" (top-512 and the pool of
+ * every query) and "候选池的三个细节在代码里" (pinning, -inf blocks dropped).
+ *
+ *  Arguments as in hsi_score_full (group 1 or 4; max_visible <= 524288) and
+ *  hsi_full_layer (k <= 2048; block_ids NULL: no pool; block size 8).
+ *  phases  HSI_PHASE_ALL, or HSI_PHASE_SCORE then HSI_PHASE_SELECT with the
+ *          same arguments and workspace.
+ *  ws      (dev) hsi_workspace_size(HSI_WS_PREFILL_LAYER, B, max_visible, k).
+ */
+hsi_status hsi_prefill_layer(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
+                             const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible, int32_t B,
+                             int64_t max_visible, int32_t group, float* scores, int64_t ld, int32_t k,
+                             int32_t* top_idx, float* top_val, int32_t n_keep, int32_t* block_ids, int32_t* n_kept,
+                             int32_t* n_pool, uint32_t* pool_bits, int64_t ld_bits, int32_t phases,
+                             hsi_format format, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * A decoder Reindex layer in one call: the pooled scores (hsi_score_pool),
  * then the top-k inside the pool reported as global positions (hsi_topk with
  * the block map).
@@ -469,13 +496,14 @@ typedef enum {
     HSI_WS_TOPK = 2,
     HSI_WS_POOL = 3,
     HSI_WS_FULL_LAYER = 4,
-    HSI_WS_REINDEX_LAYER = 5
+    HSI_WS_REINDEX_LAYER = 5,
+    HSI_WS_PREFILL_LAYER = 6
 } hsi_ws_kind;
 
 /* Scratch bytes a call needs for B queries of at most max_n entries.
  * QUANTIZE: B = number of tensors (max_n, k unused). SCORE: 0. TOPK: max_n =
  * max_valid (k unused). POOL: max_n = max_visible and k = block_size.
- * FULL_LAYER: max_n = max_visible. REINDEX_LAYER: max_n = 8 * n_keep. */
+ * FULL_LAYER, PREFILL_LAYER: max_n = max_visible. REINDEX_LAYER: max_n = 8 * n_keep. */
 size_t hsi_workspace_size(hsi_ws_kind kind, int32_t B, int64_t max_n, int32_t k);
 
 /* Synchronise `stream`, then report and clear the sticky device error word of

@@ -26,13 +26,13 @@ FMT_NVFP4, FMT_MXFP4 = 0, 1  # hsi_format: NVFP4 (576-byte records, tensor scale
 
 STATUS = {0: "HSI_OK", -1: "HSI_ERR_INVALID_ARG", -2: "HSI_ERR_UNSUPPORTED", -3: "HSI_ERR_CUDA",
           -4: "HSI_ERR_DEVICE_TIMEOUT", -5: "HSI_ERR_WORKSPACE", -6: "HSI_ERR_DEVICE_ARG", -7: "HSI_ERR_TOO_LARGE"}
-WS_QUANTIZE, WS_SCORE, WS_TOPK, WS_POOL, WS_FULL_LAYER, WS_REINDEX_LAYER = 0, 1, 2, 3, 4, 5
+WS_QUANTIZE, WS_SCORE, WS_TOPK, WS_POOL, WS_FULL_LAYER, WS_REINDEX_LAYER, WS_PREFILL_LAYER = 0, 1, 2, 3, 4, 5, 6
 
 EXPORTS = ["hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_pool", "hsi_score_pool",
            "hsi_workspace_size", "hsi_device_error", "hsi_device_check", "hsi_status_string",
            "hsi_kernel_launches", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer", "hsi_reindex_layer",
            "hsi_topk_noalloc", "hsi_debug_set", "hsi_pool_gather", "hsi_quantize_mxfp4", "hsi_quantize_mainkv",
-           "hsi_gather_mainkv", "hsi_append_token", "hsi_mask_scores"]
+           "hsi_gather_mainkv", "hsi_append_token", "hsi_mask_scores", "hsi_prefill_layer"]
 
 
 class HsiError(RuntimeError):
@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
                                      vp]
         L.hsi_full_layer.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, vp, i64, i32, vp, vp, i32, vp, vp, vp,
                                      vp, i64, i32, ctypes.c_int, vp, sz, vp]
+        L.hsi_prefill_layer.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, vp, i64, i32, vp, vp, i32, vp, vp,
+                                        vp, vp, i64, i32, ctypes.c_int, vp, sz, vp]
         L.hsi_reindex_layer.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, vp, i64, i32, vp,
                                         vp, ctypes.c_int, vp, sz, vp]
         L.hsi_pool_gather.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp, ctypes.c_int, vp]
@@ -98,7 +100,7 @@ def lib() -> ctypes.CDLL:
                      "hsi_device_error", "hsi_device_check", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer",
                      "hsi_reindex_layer", "hsi_topk_noalloc", "hsi_debug_set", "hsi_pool_gather",
                      "hsi_quantize_mxfp4", "hsi_quantize_mainkv", "hsi_gather_mainkv", "hsi_append_token",
-                     "hsi_mask_scores"):
+                     "hsi_mask_scores", "hsi_prefill_layer"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -298,6 +300,24 @@ def full_layer(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B, max_visible, 
         _ptr(q_rec), _ptr(g_q), _ptr(w), _ptr(k_rec), _ptr(g_k), _ptr(k_rec_off), _ptr(n_visible), B, max_visible,
         _ptr(scores), ld, k, _ptr(top_idx), _ptr(top_val), n_keep, _ptr(block_ids), _ptr(n_kept), _ptr(n_pool),
         _ptr(pool_bits), ld_bits, phases, fmt, _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def prefill_layer(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B, max_visible, scores, k, top_idx, top_val,
+                  group=4, block_ids=None, n_kept=None, n_pool=None, pool_bits=None, n_keep=2048, ld=None, ld_bits=0,
+                  ws=None, phases=3, fmt=FMT_NVFP4, stream=None):
+    """Chunked-prefill layer: scores (groups of `group` queries share a cache), then each
+    query's top-k and (block_ids given) pool from the block maxima.
+    phases: 1 scoring only, 2 selection only (after 1, same workspace), 3 both."""
+    ld = scores.shape[-1] if ld is None else ld
+    if pool_bits is not None and not ld_bits:
+        ld_bits = pool_bits.shape[-1]
+    if ws is None:
+        ws = workspace(WS_PREFILL_LAYER, B, max_visible, k, device=scores.device)
+    _check("hsi_prefill_layer", lib().hsi_prefill_layer(
+        _ptr(q_rec), _ptr(g_q), _ptr(w), _ptr(k_rec), _ptr(g_k), _ptr(k_rec_off), _ptr(n_visible), B, max_visible,
+        group, _ptr(scores), ld, k, _ptr(top_idx), _ptr(top_val), n_keep, _ptr(block_ids), _ptr(n_kept),
+        _ptr(n_pool), _ptr(pool_bits), ld_bits, phases, fmt, _ptr(ws), 0 if ws is None else ws.numel(),
+        _stream(stream)))
 
 
 def pool_gather(k_rec, k_rec_off, n_visible, block_ids, n_kept, B, pool_rec, n_keep=2048, fmt=FMT_NVFP4,

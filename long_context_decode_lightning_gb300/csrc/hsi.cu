@@ -14,6 +14,7 @@
 #include "gather.cuh"
 #include "mainkv.cuh"
 #include "quantize.cuh"
+#include "rowsel.cuh"
 #include "score.cuh"
 #include "select.cuh"
 
@@ -195,13 +196,14 @@ hsi_status run_select(SelParams sp, int64_t max_items, cudaStream_t s, bool hist
     return launch(sel_final_kernel, dim3(sp.B), dim3(SEL_THREADS), sizeof(SelSmem), s, sp);
 }
 
-SelParams topk_params(const float* scores, int64_t ld, const int32_t* n_valid, int32_t B, int32_t k,
-                      const int32_t* block_ids, int64_t ld_blocks, int32_t block_size, int32_t* out_idx,
+SelParams topk_params(const float* scores, int64_t ld, const int32_t* n_valid, int64_t max_valid, int32_t B,
+                      int32_t k, const int32_t* block_ids, int64_t ld_blocks, int32_t block_size, int32_t* out_idx,
                       float* out_val, const SelWs& wsp) {
     SelParams sp{};
     sp.src = scores;
     sp.ld = ld;
     sp.n_src = n_valid;
+    sp.max_src = max_valid;
     sp.div = 1;
     sp.B = B;
     sp.k = k;
@@ -357,6 +359,8 @@ size_t hsi_workspace_size(hsi_ws_kind kind, int32_t B, int64_t max_n, int32_t k)
             return sel_ws_bytes(B, max_n, false, 0) + sel_ws_bytes(B, nb, false, 0) +
                    align_up((size_t)B * (size_t)nb * 4, 256);
         }
+        case HSI_WS_PREFILL_LAYER:  // the block maxima
+            return align_up((size_t)B * (size_t)((max_n + 7) / 8) * 4, 256);
         case HSI_WS_REINDEX_LAYER:  // + the key histogram the pooled scan accumulates
             return sel_ws_bytes(B, max_n, false, 0) + align_up((size_t)B * HIST_BINS * 4, 256);
         case HSI_WS_POOL: {
@@ -455,6 +459,7 @@ hsi_status hsi_score_full(const uint8_t* q_rec, const float* g_q, const float* w
     p.g_k = g_k;
     p.k_off = k_rec_off;
     p.n_vis = n_visible;
+    p.max_vis = (int32_t)max_visible;
     p.B = B;
     p.ngroups = B / group;
     p.scores = scores;
@@ -485,6 +490,7 @@ hsi_status hsi_score_pool(const uint8_t* q_rec, const float* g_q, const float* w
     p.g_k = g_k;
     p.k_off = k_rec_off;
     p.n_vis = n_visible;
+    p.max_vis = INT32_MAX;  // gathered ids are checked against ceil(n_vis / 8) records
     p.B = B;
     p.ngroups = B;
     p.block_ids = block_ids;
@@ -507,7 +513,8 @@ hsi_status hsi_topk(const float* scores, int64_t ld, const int32_t* n_valid, int
     const size_t need = sel_ws_bytes(B, max_valid, false, 0);
     if (need && (!ws || ws_bytes < need || !aligned(ws, 256))) return HSI_ERR_WORKSPACE;
     SelWs wsp = carve_sel(ws, B, max_valid, false, 0);
-    const SelParams sp = topk_params(scores, ld, n_valid, B, k, block_ids, ld_blocks, block_size, out_idx, out_val, wsp);
+    const SelParams sp =
+        topk_params(scores, ld, n_valid, max_valid, B, k, block_ids, ld_blocks, block_size, out_idx, out_val, wsp);
     return run_select(sp, max_valid, stream);
 }
 
@@ -532,6 +539,7 @@ hsi_status hsi_topk_noalloc(const float* scores, int64_t ld, const int32_t* n_va
     sp.src = scores;
     sp.ld = ld;
     sp.n_src = n_valid;
+    sp.max_src = max_valid;
     sp.div = 1;
     sp.B = B;
     sp.k = k;
@@ -573,8 +581,8 @@ hsi_status hsi_candidate_pool(const float* scores, int64_t ld, const float* bloc
     int64_t bld = ldb;
     if (need_bmax) {
         const dim3 grid((unsigned)((max_blocks + 255) / 256 > 0 ? (max_blocks + 255) / 256 : 1), (unsigned)B);
-        if (launch(block_max_kernel, dim3(grid), dim3(256), 0, stream, scores, ld, n_visible, block_size, wsp.bmax,
-                   max_blocks) != HSI_OK)
+        if (launch(block_max_kernel, dim3(grid), dim3(256), 0, stream, scores, ld, n_visible, max_visible, block_size,
+                   wsp.bmax, max_blocks) != HSI_OK)
             return HSI_ERR_CUDA;
         bm = wsp.bmax;
         bld = max_blocks;
@@ -583,6 +591,7 @@ hsi_status hsi_candidate_pool(const float* scores, int64_t ld, const float* bloc
     sp.src = bm;
     sp.ld = bld;
     sp.n_src = n_visible;
+    sp.max_src = max_visible;
     sp.div = block_size;
     sp.B = B;
     sp.k = n_keep;
@@ -608,7 +617,7 @@ hsi_status hsi_mask_scores(float* scores, int64_t ld, const int32_t* n_visible, 
         return HSI_ERR_INVALID_ARG;
     if (max_visible == 0) return HSI_OK;
     const dim3 grid((unsigned)((max_visible + 255) / 256), (unsigned)B);
-    return launch(mask_scores_kernel, grid, dim3(256), 0, stream, scores, ld, n_visible, bits, ld_bits);
+    return launch(mask_scores_kernel, grid, dim3(256), 0, stream, scores, ld, n_visible, max_visible, bits, ld_bits);
 }
 
 hsi_status hsi_calib_read(const void* buf, size_t bytes, int method, int chunk, int stages,
@@ -682,6 +691,7 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     p.g_k = g_k;
     p.k_off = k_rec_off;
     p.n_vis = n_visible;
+    p.max_vis = (int32_t)max_visible;
     p.B = B;
     p.ngroups = B;
     p.scores = scores;
@@ -701,6 +711,7 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     sp.src = scores;
     sp.ld = ld;
     sp.n_src = n_visible;
+    sp.max_src = max_visible;
     sp.div = 1;
     sp.B = B;
     sp.k = k;
@@ -725,6 +736,7 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     pp.src = bmax;
     pp.ld = nb;
     pp.n_src = n_visible;
+    pp.max_src = max_visible;
     pp.div = 8;
     pp.B = B;
     pp.k = n_keep;
@@ -744,6 +756,71 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     // eighth of the scores): counting it in the scoring epilogue, where the
     // maxima of a warp land in one or two bins, cost more than this pass
     return run_select(pp, nb, stream, false);
+}
+
+hsi_status hsi_prefill_layer(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,
+                             const float* g_k, const int64_t* k_rec_off, const int32_t* n_visible, int32_t B,
+                             int64_t max_visible, int32_t group, float* scores, int64_t ld, int32_t k,
+                             int32_t* top_idx, float* top_val, int32_t n_keep, int32_t* block_ids, int32_t* n_kept,
+                             int32_t* n_pool, uint32_t* pool_bits, int64_t ld_bits, int32_t phases,
+                             hsi_format format, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (phases != HSI_PHASE_SCORE && phases != HSI_PHASE_SELECT && phases != HSI_PHASE_ALL)
+        return HSI_ERR_INVALID_ARG;
+    hsi_status st = check_score_common(format, q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B);
+    if (st != HSI_OK) return st;
+    if (!scores || !top_idx || !top_val || max_visible < 0 || ld < max_visible || k < 1 || k > RS_MAXK)
+        return HSI_ERR_INVALID_ARG;
+    if (max_visible > (int64_t)RS_MAX_BLOCKS * 8) return HSI_ERR_UNSUPPORTED;
+    if (group != 1 && group != 4) return HSI_ERR_UNSUPPORTED;
+    if (B % group) return HSI_ERR_INVALID_ARG;
+    const bool pool = block_ids != nullptr;
+    if (pool && (!n_kept || !n_pool || n_keep < 1 || n_keep > SEL_MAXK)) return HSI_ERR_INVALID_ARG;
+    if (pool_bits && ld_bits < (max_visible + 31) / 32) return HSI_ERR_INVALID_ARG;
+    const int64_t nb = (max_visible + 7) / 8;
+    const size_t need = hsi_workspace_size(HSI_WS_PREFILL_LAYER, B, max_visible, k);
+    if (!ws || ws_bytes < need || !aligned(ws, 256)) return HSI_ERR_WORKSPACE;
+    float* bmax = static_cast<float*>(ws);
+    if (phases & HSI_PHASE_SCORE) {
+        ScoreParams p{};
+        p.q_rec = q_rec;
+        p.g_q = g_q;
+        p.w = w;
+        p.k_rec = k_rec;
+        p.g_k = g_k;
+        p.k_off = k_rec_off;
+        p.n_vis = n_visible;
+        p.max_vis = (int32_t)max_visible;
+        p.B = B;
+        p.ngroups = B / group;
+        p.scores = scores;
+        p.ld = ld;
+        p.bmax = bmax;
+        p.ldb = nb;
+        st = group == 1 ? launch_score<1, false, kDecodeStages, kDecodeUT>(p, format, stream)
+                        : launch_score<4, false, kPrefillStages, kPrefillUT>(p, format, stream);
+        if (st != HSI_OK) return st;
+    }
+    if (!(phases & HSI_PHASE_SELECT)) return HSI_OK;
+    RowSelParams rp{};
+    rp.bmax = bmax;
+    rp.ldb = nb;
+    rp.scores = scores;
+    rp.ld = ld;
+    rp.n_vis = n_visible;
+    rp.max_vis = max_visible;
+    rp.B = B;
+    rp.k = k;
+    rp.out_idx = top_idx;
+    rp.out_val = top_val;
+    rp.n_keep = pool ? n_keep : 0;
+    rp.blk_out = block_ids;
+    rp.n_kept = n_kept;
+    rp.n_pool = n_pool;
+    rp.bits = pool_bits;
+    rp.ld_bits = ld_bits;
+    static std::atomic<bool> attr_set[kMaxDevices];
+    if (smem_attr_once(rowsel_kernel, (int)sizeof(RowSelSmem), attr_set) != HSI_OK) return HSI_ERR_CUDA;
+    return launch(rowsel_kernel, dim3((unsigned)B), dim3(RS_THREADS), sizeof(RowSelSmem), stream, rp);
 }
 
 hsi_status hsi_quantize_mainkv(const uint16_t* x, int64_t n, uint8_t* kv, cudaStream_t stream) {
@@ -840,6 +917,7 @@ hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float
         p.g_k = g_k;
         p.k_off = k_rec_off;
         p.n_vis = n_visible;
+        p.max_vis = INT32_MAX;  // gathered ids are checked against ceil(n_vis / 8) records
         p.B = B;
         p.ngroups = B;
         p.block_ids = block_ids;
@@ -851,7 +929,8 @@ hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float
         p.pool_out = pool_rec;
         st = launch_score<1, true, kGatherStages, kGatherUT>(p, format, stream);
         if (st != HSI_OK) return st;
-        SelParams sp = topk_params(pool_scores, ld, n_pool, B, k, block_ids, n_keep, 8, top_idx, top_val, wsp);
+        SelParams sp =
+            topk_params(pool_scores, ld, n_pool, max_valid, B, k, block_ids, n_keep, 8, top_idx, top_val, wsp);
         sp.hist = hist;
         sp.hist_small = 1;
         return run_select(sp, max_valid, stream, true);
@@ -881,6 +960,7 @@ hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float
         p.k_off = nullptr;
         p.k_stride = n_keep;
         p.n_vis = n_pool;
+        p.max_vis = (int32_t)max_valid;  // slots of the compacted pool
         p.B = B;
         p.ngroups = B;
         p.scores = pool_scores;
@@ -890,7 +970,8 @@ hsi_status hsi_reindex_layer(const uint8_t* q_rec, const float* g_q, const float
         p.key_hist = hist;
         st = launch_score<1, false, kPooledStages, kPooledUT>(p, format, stream);
         if (st != HSI_OK) return st;
-        SelParams sp = topk_params(pool_scores, ld, n_pool, B, k, block_ids, n_keep, 8, top_idx, top_val, wsp);
+        SelParams sp =
+            topk_params(pool_scores, ld, n_pool, max_valid, B, k, block_ids, n_keep, 8, top_idx, top_val, wsp);
         sp.hist = hist;
         sp.hist_small = 1;
         return run_select(sp, max_valid, stream, true);

@@ -70,6 +70,7 @@ struct ScoreParams {
     const int64_t* k_off;  // first record of query b's keys; NULL: b * k_stride
     int64_t k_stride;
     const int32_t* n_vis;
+    int32_t max_vis;  // the caller's bound on n_vis[b]; a larger value is clamped and reported
     int32_t B;
     int32_t ngroups;
     // full scan
@@ -101,8 +102,7 @@ struct ScoreCfg {
     static constexpr int N = 32 * NQ;
     static constexpr int UNIT_RECS = 16 * UT;
     static constexpr int UNIT_KEYS = TILE_KEYS * UT;
-    // accumulator sets (one set = UT tiles); multi-query tiles: three epilogue
-    // groups, one set each, since their fp32 work per key is NQ times larger
+    // accumulator sets (one set = UT tiles)
     static constexpr int NACC = (NQ == 1 && UT <= 2) ? 4 : NQ > 1 ? 3 : 2;
     static constexpr int Q_BYTES = NQ * 4 * REC;
     static constexpr int STAGE_BYTES = UNIT_RECS * REC;
@@ -112,7 +112,11 @@ struct ScoreCfg {
     static constexpr int MMA_WARP = PROD_WARPS;
     static constexpr int FIRST_SF_WARP = PROD_WARPS + 1;
     static constexpr int FIRST_EPI_WARP = FIRST_SF_WARP + 4;
-    static constexpr int EPI_GROUPS = GATHER ? 1 : NQ > 1 ? 3 : 2;
+    // single queries: two groups taking alternate units; multi-query tiles: one
+    // group per query, every group reading its query's 32 columns of every tile
+    static constexpr int EPI_GROUPS = GATHER ? 1 : NQ > 1 ? NQ : 2;
+    // warps that read a tile before the MMAs may overwrite it
+    static constexpr int ACC_READERS = NQ > 1 ? 4 * NQ : 4;
     static constexpr int THREADS = 32 * (FIRST_EPI_WARP + 4 * EPI_GROUPS);
 #ifndef HSI_COPY_AHEAD
 #define HSI_COPY_AHEAD 4
@@ -134,11 +138,7 @@ struct ScoreCfg {
     static constexpr int HIST_SLOTS = NQ == 1 ? 2 : 0;
     static constexpr int OFF_HIST = OFF_IDS + IDS_BYTES;
     static constexpr int HIST_BYTES = HIST_SLOTS * 4096 * 4;
-    // multi-query tiles: the scaled head weights of each epilogue warp's queries
-    // live in shared memory (one copy per warp) instead of 32 NQ registers
-    static constexpr int OFF_WQ = OFF_HIST + HIST_BYTES;
-    static constexpr int WQ_BYTES = NQ > 1 ? 4 * EPI_GROUPS * NQ * 32 * 4 : 0;
-    static constexpr int OFF_BARS = OFF_WQ + WQ_BYTES;
+    static constexpr int OFF_BARS = OFF_HIST + HIST_BYTES;
     // full, sfready, empty per stage; acc_full per accumulator set, acc_empty per
     // tile of a set (the epilogue frees each tile as soon as it has read it);
     // q_full, q_ready, q_empty per slot; ids_full, ids_free per id slot; drain
@@ -146,7 +146,7 @@ struct ScoreCfg {
     static constexpr int SMEM_BYTES = OFF_BARS + NBARS * 8 + 64 + 1024;  // + alignment slack
     static_assert(NQ <= 4, "B scale rows fit one 128-row layout");
     static_assert(COLS_USED <= 512, "TMEM");
-    static_assert(NACC % EPI_GROUPS == 0, "accumulator sets split evenly between epilogue groups");
+    static_assert(NQ > 1 || NACC % EPI_GROUPS == 0, "accumulator sets split evenly between epilogue groups");
     static_assert(!GATHER || (NQ == 1 && UNIT_RECS == 32), "gather: 4 producer threads per block");
     static_assert(!GATHER || COPY_AHEAD < STAGES, "gather: copies in flight fit the ring");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
@@ -278,6 +278,17 @@ __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
     }
 }
 
+// n_vis[b] within [0, max_vis] (the bound that sized the score rows and the
+// caches); `report`: record a larger value as a device-side argument error.
+__device__ __forceinline__ int vis_of(const ScoreParams& p, int b, bool report = false) {
+    int n = p.n_vis[b];
+    if (n > p.max_vis) {
+        if (report) raise_error(DEVERR_ARG);
+        n = p.max_vis;
+    }
+    return n < 0 ? 0 : n;
+}
+
 template <int NQ, bool GATHER, int UT>
 __device__ __forceinline__ int group_units(const ScoreParams& p, int g) {
     if (GATHER) {
@@ -286,7 +297,7 @@ __device__ __forceinline__ int group_units(const ScoreParams& p, int g) {
     } else {
         int m = 0;
 #pragma unroll
-        for (int i = 0; i < NQ; ++i) m = max(m, p.n_vis[g * NQ + i]);
+        for (int i = 0; i < NQ; ++i) m = max(m, vis_of(p, g * NQ + i));
         return (m + TILE_KEYS * UT - 1) / (TILE_KEYS * UT);
     }
 }
@@ -356,6 +367,24 @@ __device__ __forceinline__ void sf_quarter(const uint8_t* recs, int nrows, int r
     }
 }
 
+// The weighted ReLU head sum of one key, sum_j w_j * max(x_j, 0) over the 32
+// heads, evaluated as ((s0 + s1) + (s2 + s3)) where s_r is the fma chain over
+// the heads j = r (mod 4) in increasing j. The chains run in pairs, (s0, s1)
+// and (s2, s3), as packed f32x2 fmas (w2[i] = w_2i, w_2i+1): 32 max and 16
+// fma instructions per key instead of 32 + 32, bit for bit the same result.
+__device__ __forceinline__ float head_sum(const float (&x)[32], const uint64_t (&w2)[16]) {
+    uint64_t a = f2_pack(0.f, 0.f), b = a;
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+        a = f2_fma(w2[j >> 1], f2_pack(fmaxf(x[j], 0.f), fmaxf(x[j + 1], 0.f)), a);
+        b = f2_fma(w2[(j >> 1) + 1], f2_pack(fmaxf(x[j + 2], 0.f), fmaxf(x[j + 3], 0.f)), b);
+    }
+    float s0, s1, s2, s3;
+    f2_unpack(a, s0, s1);
+    f2_unpack(b, s2, s3);
+    return (s0 + s1) + (s2 + s3);
+}
+
 template <int NQ, bool GATHER, int STAGES, int UT, int FMT>
 __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS, 1) score_kernel(ScoreParams p) {
     using C = ScoreCfg<NQ, GATHER, STAGES, UT, FMT>;
@@ -398,7 +427,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS
     }
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NACC; ++i) mbar_init(&acc_full[i], 1);
-        for (int i = 0; i < C::NACC * UT; ++i) mbar_init(&acc_empty[i], 4);
+        for (int i = 0; i < C::NACC * UT; ++i) mbar_init(&acc_empty[i], C::ACC_READERS);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&q_full[i], 1);
             mbar_init(&q_ready[i], 4);
@@ -468,7 +497,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS
                 k_base = p.k_off ? p.k_off[b0] : (int64_t)b0 * p.k_stride;
                 int maxv = 0;
 #pragma unroll
-                for (int i = 0; i < NQ; ++i) maxv = max(maxv, p.n_vis[b0 + i]);
+                for (int i = 0; i < NQ; ++i) maxv = max(maxv, vis_of(p, b0 + i));
                 nrec_all = (maxv + 7) / 8;
                 if (GATHER) nk = min(p.n_kept[b0], p.n_keep);
                 const int slot = gc & 1;
@@ -683,12 +712,71 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS
             if (slot >= 0 && slot < C::HIST_SLOTS) return hist_s + slot * 4096;
             return p.key_hist + (int64_t)b * 4096;
         };
+        // the scaled head weights of this warp's query, in f32x2 pairs
+        uint64_t w2[16];
+        auto load_w = [&](int b) {
+            // the 2^-7 of the two unnormalised rotations; NVFP4 also its tensor scales
+            const float sc = (FMT == FMT_MXFP4 ? 1.0f : p.g_q[b] * p.g_k[b]) * 0.0078125f;
+            const float4* wv = reinterpret_cast<const float4*>(p.w + (int64_t)b * 32);
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4) {
+                const float4 v = __ldg(wv + j4);
+                w2[2 * j4] = f2_pack(v.x * sc, v.y * sc);
+                w2[2 * j4 + 1] = f2_pack(v.z * sc, v.w * sc);
+            }
+        };
+        // one key's score: written, its 8-key block maximum, its histogram bin
+        auto emit = [&](int b, int key, int nv, int npad, float sc) {
+            const bool vis = key < nv;
+            if (vis) p.scores[(int64_t)b * p.ld + key] = sc;
+            else if (key < npad) p.scores[(int64_t)b * p.ld + key] = __uint_as_float(0xFF800000u);
+            if (fuse_hist && vis) atomicAdd(hist_of(b) + (order_key(sc) >> 20), 1u);
+            if (p.bmax) {
+                float m = vis ? sc : __uint_as_float(0xFF800000u);
+                m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+                m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+                m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+                if ((lane & 7) == 0 && vis) p.bmax[(int64_t)b * p.ldb + key / 8] = m;
+            }
+        };
         int cur_g = -1;
-        float wq[32];  // single query: its scaled head weights
-        float* wq_s = reinterpret_cast<float*>(smem + C::OFF_WQ) + (warp - C::FIRST_EPI_WARP) * NQ * 32;
-        int nv[NQ], npad[NQ];
-        int nk = 0;
         Ring st, ac;
+        if constexpr (NQ > 1) {
+            // one group per query: every group takes every unit, reads its query's
+            // 32 columns of each tile and frees the tile once all groups hold it,
+            // so a tile stays allocated for one TMEM load, not a whole epilogue
+            int nv = 0, npad = 0, b = 0;
+            for (long long u = 0; u < count; ++u) {
+                const int g = it.g, t = it.t;
+                if (g != cur_g) {
+                    cur_g = g;
+                    b = g * NQ + grp;
+                    nv = vis_of(p, b, lane == 0);
+                    npad = p.pad_blocks ? 8 * min(p.pad_blocks[b], p.n_keep) : 0;
+                    load_w(b);
+                }
+                if (!wait_traced(&acc_full[ac.i], ac.ph, sh, tr, TR_EPI_ACCFULL)) break;
+                HSI_TSTART(t_epi);
+                tc_fence_after();
+                if (grp == 0 && group_leader) mbar_arrive(&empty[st.i]);  // the MMAs have read the stage
+#pragma unroll
+                for (int sub = 0; sub < UT; ++sub) {
+                    float x[32];
+                    tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + C::COL_ACC + (ac.i * UT + sub) * C::N + grp * 32,
+                              x);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&acc_empty[ac.i * UT + sub]);
+                    emit(b, (t * UT + sub) * TILE_KEYS + row, nv, npad, head_sum(x, w2));
+                }
+                HSI_TEND(t_epi, TR_EPI_WORK);
+                st.next(STAGES);
+                ac.next(C::NACC);
+                it.next(p);
+            }
+        } else {
+        int nv = 0, npad = 0;
+        int nk = 0;
         int turn = 0;
         for (long long u = 0; u < count; ++u) {
             if (turn != grp) {
@@ -702,29 +790,9 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS
             const int g = it.g, t = it.t;
             if (g != cur_g) {
                 cur_g = g;
-#pragma unroll
-                for (int qi = 0; qi < NQ; ++qi) {
-                    const int b = g * NQ + qi;
-                    nv[qi] = p.n_vis[b];
-                    npad[qi] = p.pad_blocks ? 8 * min(p.pad_blocks[b], p.n_keep) : 0;
-                    // the 2^-7 of the two unnormalised rotations; NVFP4 also its tensor scales
-                    const float sc = (FMT == FMT_MXFP4 ? 1.0f : p.g_q[b] * p.g_k[b]) * 0.0078125f;
-                    if constexpr (NQ == 1) {
-                        const float4* wv = reinterpret_cast<const float4*>(p.w + (int64_t)b * 32);
-#pragma unroll
-                        for (int j4 = 0; j4 < 8; ++j4) {
-                            const float4 v = __ldg(wv + j4);
-                            wq[4 * j4 + 0] = v.x * sc;
-                            wq[4 * j4 + 1] = v.y * sc;
-                            wq[4 * j4 + 2] = v.z * sc;
-                            wq[4 * j4 + 3] = v.w * sc;
-                        }
-                    } else {
-                        __syncwarp();  // the previous query's weights are no longer read
-                        wq_s[qi * 32 + lane] = __ldg(p.w + (int64_t)b * 32 + lane) * sc;
-                    }
-                }
-                if constexpr (NQ > 1) __syncwarp();
+                nv = vis_of(p, g, lane == 0);
+                npad = p.pad_blocks ? 8 * min(p.pad_blocks[g], p.n_keep) : 0;
+                load_w(g);
                 if (GATHER) nk = min(p.n_kept[g], p.n_keep);
             }
             // gather: the positions of this thread's slots, loaded before the wait
@@ -742,52 +810,24 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS
             if (group_leader) mbar_arrive(&empty[st.i]);  // the MMAs have read the stage
 #pragma unroll
             for (int sub = 0; sub < UT; ++sub) {
-                const uint32_t dbase =
-                    tmem + ((uint32_t)(quarter * 32) << 16) + C::COL_ACC + (ac.i * UT + sub) * C::N;
                 const int key = (t * UT + sub) * TILE_KEYS + row;  // key (full scan) or pool slot (gather)
-#pragma unroll
-                for (int qi = 0; qi < NQ; ++qi) {
-                    float x[32];
-                    tmem_ld32(dbase + qi * 32, x);
-                    if (qi == NQ - 1) {  // the tile is in registers: the MMA may overwrite it
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&acc_empty[ac.i * UT + sub]);
-                    }
-                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        float4 w4;
-                        if constexpr (NQ == 1) w4 = make_float4(wq[j], wq[j + 1], wq[j + 2], wq[j + 3]);
-                        else w4 = *reinterpret_cast<const float4*>(wq_s + qi * 32 + j);
-                        s0 = fmaf(w4.x, fmaxf(x[j], 0.f), s0);
-                        s1 = fmaf(w4.y, fmaxf(x[j + 1], 0.f), s1);
-                        s2 = fmaf(w4.z, fmaxf(x[j + 2], 0.f), s2);
-                        s3 = fmaf(w4.w, fmaxf(x[j + 3], 0.f), s3);
-                    }
-                    const float sc = (s0 + s1) + (s2 + s3);
-                    const int b = g * NQ + qi;
-                    if (!GATHER) {
-                        const bool vis = key < nv[qi];
-                        if (vis) p.scores[(int64_t)b * p.ld + key] = sc;
-                        else if (key < npad[qi]) p.scores[(int64_t)b * p.ld + key] = __uint_as_float(0xFF800000u);
-                        if (fuse_hist && vis) atomicAdd(hist_of(b) + (order_key(sc) >> 20), 1u);
-                        if (p.bmax) {
-                            float m = vis ? sc : __uint_as_float(0xFF800000u);
-                            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-                            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-                            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-                            if ((lane & 7) == 0 && vis) p.bmax[(int64_t)b * p.ldb + key / 8] = m;
-                        }
-                    } else if (pos[sub] >= 0) {
-                        const bool vis = pos[sub] < nv[qi];
-                        p.pool_scores[(int64_t)b * p.ld_pool + key] = vis ? sc : __uint_as_float(0xFF800000u);
-                        if (fuse_hist && vis) {  // the pool slot's key, for the selection inside the pool
-                            const uint32_t bin = order_key(sc) >> 20;
-                            const int slot = b - b_first;
-                            if (slot >= 0 && slot < C::HIST_SLOTS) atomicAdd(hist_s + slot * 4096 + bin, 1u);
-                            else atomicAdd(p.key_hist + (int64_t)b * 4096 + bin, 1u);
-                        }
+                float x[32];
+                tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + C::COL_ACC + (ac.i * UT + sub) * C::N, x);
+                // the tile is in registers: the MMA may overwrite it
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[ac.i * UT + sub]);
+                const float sc = head_sum(x, w2);
+                if (!GATHER) {
+                    emit(g, key, nv, npad, sc);
+                } else if (pos[sub] >= 0) {
+                    const bool vis = pos[sub] < nv;
+                    p.pool_scores[(int64_t)g * p.ld_pool + key] = vis ? sc : __uint_as_float(0xFF800000u);
+                    if (fuse_hist && vis) {  // the pool slot's key, for the selection inside the pool
+                        const uint32_t bin = order_key(sc) >> 20;
+                        const int slot = g - b_first;
+                        if (slot >= 0 && slot < C::HIST_SLOTS) atomicAdd(hist_s + slot * 4096 + bin, 1u);
+                        else atomicAdd(p.key_hist + (int64_t)g * 4096 + bin, 1u);
                     }
                 }
             }
@@ -795,6 +835,7 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS
             st.next(STAGES);
             ac.next(C::NACC);
             it.next(p);
+        }
         }
     }
 #ifdef HSI_TRACE

@@ -44,6 +44,7 @@ struct SelParams {
     const float* src;
     int64_t ld;
     const int32_t* n_src;  // [B]; n_items(b) = ceil(n_src[b] / div)
+    int64_t max_src;       // the caller's bound on n_src[b]; a larger value is clamped and reported
     int32_t div;
     int32_t B;
     int32_t k;
@@ -82,9 +83,21 @@ struct SelParams {
     int64_t ld_bits;
 };
 
+// n_src[b] within [0, max_src]: a length past the caller's bound (which sized
+// the rows and buffers) is reported as a device-side argument error and
+// clamped, so that no pass reads or writes past a row.
+__device__ __forceinline__ int64_t sel_len(const SelParams& p, int b) {
+    int64_t n = p.n_src[b];
+    if (n > p.max_src) {
+        raise_error(DEVERR_ARG);
+        n = p.max_src;
+    }
+    return n < 0 ? 0 : n;
+}
+
 __device__ __forceinline__ int64_t sel_items(const SelParams& p, int b) {
-    const int64_t n = p.n_src[b];
-    return n <= 0 ? 0 : (n + p.div - 1) / p.div;
+    const int64_t n = sel_len(p, b);
+    return (n + p.div - 1) / p.div;
 }
 
 // Key of item i of value v (n = item count); `ok`: whether it is eligible.
@@ -1102,7 +1115,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) 
     } else {
         // pool: ascending block ids, the visible-position count and the bit table
         const int bs = p.div;
-        const int64_t n_vis = p.n_src[b];
+        const int64_t n_vis = sel_len(p, b);
         int32_t* bo = p.blk_out + (int64_t)b * p.k;
         if (threadIdx.x == 0) s.bcast[5] = 0;
         uint32_t* bits = p.bits ? p.bits + (int64_t)b * p.ld_bits : nullptr;
@@ -1140,14 +1153,24 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) 
     SEL_MARK(s, 31);
 }
 
+// A visible length within [0, max_n], the caller's bound that sized the rows;
+// a larger value is clamped and reported as a device-side argument error.
+__device__ __forceinline__ int64_t clamp_len(int64_t n, int64_t max_n) {
+    if (n > max_n) {
+        raise_error(DEVERR_ARG);
+        n = max_n;
+    }
+    return n < 0 ? 0 : n;
+}
+
 // Block maxima of a score row: bmax[b][j] = max of scores[b][j*bs .. j*bs+bs)
 // over visible positions (< n_visible[b]), for j < ceil(n_visible[b]/bs).
-__global__ void block_max_kernel(const float* scores, int64_t ld, const int32_t* n_vis, int32_t bs, float* bmax,
-                                 int64_t ldb) {
+__global__ void block_max_kernel(const float* scores, int64_t ld, const int32_t* n_vis, int64_t max_n, int32_t bs,
+                                 float* bmax, int64_t ldb) {
     griddep_wait();
     griddep_launch_dependents();
     const int b = blockIdx.y;
-    const int64_t n = n_vis[b];
+    const int64_t n = clamp_len(n_vis[b], max_n);
     const int64_t nblk = (n + bs - 1) / bs;
     const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (j >= nblk) return;
@@ -1163,13 +1186,15 @@ __global__ void block_max_kernel(const float* scores, int64_t ld, const int32_t*
 // (bit s%32 of bits[b][s/32]) is clear becomes -inf. One thread per position
 // (a warp shares one bit word), grid = (ceil(max_visible / 256), B).
 __global__ void __launch_bounds__(256) mask_scores_kernel(float* __restrict__ scores, int64_t ld,
-                                                          const int32_t* __restrict__ n_vis,
+                                                          const int32_t* __restrict__ n_vis, int64_t max_n,
                                                           const uint32_t* __restrict__ bits, int64_t ld_bits) {
     griddep_wait();
     griddep_launch_dependents();
     const int b = blockIdx.y;
     const int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (s >= n_vis[b]) return;
+    const int64_t n = n_vis[b];
+    if (blockIdx.x == 0 && threadIdx.x == 0 && n > max_n) raise_error(DEVERR_ARG);
+    if (s >= min(n, max_n)) return;
     const uint32_t m = __ldg(bits + (int64_t)b * ld_bits + (s >> 5));
     if (!((m >> (s & 31)) & 1u)) scores[(int64_t)b * ld + s] = __uint_as_float(0xFF800000u);
 }

@@ -53,3 +53,26 @@ def test_wait_that_never_completes_times_out_and_context_survives():
     qrec, gq, wo = oracle_query(wl, 0, 0)
     ref, tol = oracle.score_rows(qrec, gq, wo, krec, gk, np.arange(n))
     assert np.all(np.abs(scores.cpu().numpy()[0] - ref) <= tol)
+
+
+def test_length_past_the_host_bound_is_clamped_and_reported():
+    """A device-side length larger than the bound the caller gave on the host
+    (which sized the rows) is a malformed argument: the selection kernels clamp
+    it to the bound, so no pass reads past a row, and report it through the
+    sticky word; the results are those of the clamped length."""
+    B, n = 3, 20000
+    g = torch.Generator(device="cpu").manual_seed(11)
+    s = (torch.randn(B, n, generator=g) * 3).to(DEV)
+    k = 512
+    bad = i32([n, n + 5, 2 * n])  # rows 1 and 2 claim more than max_valid = n items
+    ok = i32([n, n, n])
+    gi = torch.empty(B, k, dtype=torch.int32, device=DEV)
+    gv = torch.empty(B, k, device=DEV)
+    assert hsi.device_error() == 0
+    hsi.topk(s, bad, B, n, k, gi, gv)
+    assert hsi.device_error() == -6  # HSI_ERR_DEVICE_ARG
+    ri = torch.empty_like(gi)
+    rv = torch.empty_like(gv)
+    hsi.topk(s, ok, B, n, k, ri, rv)
+    assert hsi.device_error() == 0
+    assert torch.equal(gi, ri) and torch.equal(gv, rv)
