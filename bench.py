@@ -64,6 +64,8 @@ def parse():
     ap.add_argument("--no-mxfp4", action="store_true", help="skip the extra step on MXFP4 records")
     ap.add_argument("--no-mainkv", action="store_true", help="skip the main-KV gather measurement")
     ap.add_argument("--no-serve", action="store_true", help="skip the serving-step measurement")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the calibration, the other workloads and the chunked-prefill workload")
     ap.add_argument("--profile", action="store_true", help="cudaProfilerStart/Stop around the timed steps")
     ap.add_argument("--queries", type=int, default=0, help="use only the first N queries (profiling captures)")
     return ap.parse_args()
@@ -595,7 +597,239 @@ def oracle_timed(wl, prepared, nq, fmt: str = "nvfp4"):
 
 
 def cpu_sample_size(wl: inputs.Workload):
-    return max(1, min(16, os.cpu_count() or 1, wl.B))
+    """All host cores, one query per thread (at most the workload's queries)."""
+    return max(1, min(os.cpu_count() or 1, wl.B))
+
+
+# ------------------------------------------------------------ calibration --
+
+def calibrate(dev, log, n_sm: int):
+    """The rooflines of this GPU measured with the path's own instructions: a
+    read-only stream of 4 GB (16-byte loads from every SM, and bulk copies of
+    18 KB through a shared-memory ring), and back-to-back block-scaled FP4
+    MMAs (M = 128, K = 64, N = 32 .. 256) on every SM. Best of 5 launches each."""
+    import torch
+
+    import long_context_decode_lightning_gb300 as hsi
+    buf = torch.ones(4 << 30, dtype=torch.uint8, device=dev)
+    sink = torch.zeros(1, dtype=torch.int64, device=dev)
+
+    def best(fn, reps=5):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return min(ts)
+
+    out = {"hbm_read_gbs": {}, "fp4_mma_tflops": {}}
+    ms = best(lambda: hsi.calib_read(buf, 0, sink=sink))
+    out["hbm_read_gbs"]["ldg16"] = buf.numel() / (ms / 1e3) / 1e9
+    ms = best(lambda: hsi.calib_read(buf, 1, chunk=18432, stages=8, sink=sink))
+    out["hbm_read_gbs"]["bulk18k"] = buf.numel() / (ms / 1e3) / 1e9
+    del buf
+    for n in (32, 64, 128, 256):
+        iters = 16000 * 256 // n if n < 256 else 24000
+        ms = best(lambda: hsi.calib_mma(n, iters, sink=sink, device=dev))
+        out["fp4_mma_tflops"][str(n)] = 2.0 * 128 * n * 64 * iters * n_sm / (ms / 1e3) / 1e12
+    assert hsi.device_error() == 0, "device error during calibration"
+    log(f"calibration: read {out['hbm_read_gbs']}, FP4 MMA {out['fp4_mma_tflops']}")
+    out["note"] = ("read-only HBM bandwidth (4 GB, 16-byte loads / 18 KB bulk copies) and dense block-scaled FP4 "
+                   "tensor throughput (tcgen05.mma kind::mxf4nvf4, M=128, K=64, shared-memory operands), measured "
+                   "in this run by hsi_calib_read / hsi_calib_mma; best of 5")
+    return out
+
+
+def flush_l2(dev, _buf={}):
+    """Write 256 MB (twice the L2) so that the next step reads its inputs from HBM."""
+    import torch
+    if "b" not in _buf:
+        _buf["b"] = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    _buf["b"].zero_()
+
+
+def time_steps_flushed(fn, K: int, dev) -> list:
+    """K replays of fn, each timed alone with events after an L2 flush (ms each)."""
+    import torch
+    out = []
+    for _ in range(K):
+        flush_l2(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1))
+    return out
+
+
+def decode_config(idx: int, dev, args, log, peaks):
+    """One of the other decode / encoder workloads, as the headline step runs
+    (CUDA graphs), each step timed alone after an L2 flush (their caches can fit
+    in L2). Roofline: the scans' key bytes (72 per visible key per Full layer,
+    576 per pooled block per Reindex layer) over the step time."""
+    import torch
+
+    import long_context_decode_lightning_gb300 as hsi
+    wl = inputs.workload(idx)
+    W = DeviceWorkload(wl, dev, log)
+    W.capture()
+    for _ in range(max(args.warmup, 1)):
+        W.replay()
+    torch.cuda.synchronize()
+    assert hsi.device_error() == 0, f"device error in workload {wl.name}"
+    ts = time_steps_flushed(W.replay, args.steps, dev)
+    ms = float(np.median(ts))
+    pairs, full, pooled = W.pairs_per_step()
+    key_bytes = wl.full_layers * sum(wl.n_visible) * 72
+    if wl.build_pool:
+        key_bytes += wl.reindex_layers * int(W.nk.clamp(max=wl.n_keep).sum().item()) * W.rec
+    peak = float(peaks["hbm_gbs"])
+    gbs = key_bytes / (ms / 1e3) / 1e9
+    res = {"workload": wl.name, "notes": wl.notes, "ms_per_step": ms, "pairs_per_s": pairs / (ms / 1e3),
+           "top512_selections_per_s": W.B * W.layers / (ms / 1e3), "pairs_per_step": pairs,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                        "bytes_per_step": key_bytes, "peak_kind": "measured copy bandwidth",
+                        "ideal_ms": key_bytes / (peak * 1e9) * 1e3},
+           "timing": "median of per-step CUDA-event times, L2 flushed (256 MB written) before each step"}
+    if idx == 0:
+        res["note"] = ("latency-bound: 2.4 MB of keys is well under one microsecond of HBM time, so the step is "
+                       "the launch and dependency chain of its kernels, not bandwidth")
+    del W
+    torch.cuda.empty_cache()
+    return res
+
+
+class PrefillWorkload:
+    """Chunked prefill: 8192 consecutive queries on one 131,072-key cache (query
+    t sees 122,881 + t keys). One step: quantise the 8192 queries' q, then
+    hsi_prefill_layer: four queries per tensor-core tile, scores and block maxima
+    written, then each query's top-512 and pool from the block maxima and the
+    candidate blocks' scores."""
+
+    def __init__(self, wl: inputs.Workload, dev, log):
+        import torch
+
+        import long_context_decode_lightning_gb300 as hsi
+        self.torch, self.hsi, self.wl = torch, hsi, wl
+        signs = wl.signs()
+        self.signs = signs
+        n = wl.seq_len[0]
+        B = self.B = wl.B
+        self.n = n
+        t0 = time.time()
+        kb = torch.from_numpy(wl.k_bf16(0, 0).view(np.int16)).to(dev)
+        self.k_rec = torch.empty(hsi.n_records(n) * hsi.REC_BYTES, dtype=torch.uint8, device=dev)
+        g1 = torch.empty(1, device=dev)
+        hsi.quantize_nvfp4(kb, 1, n, signs, g1, self.k_rec)
+        del kb
+        self.g_k = g1.repeat(B)
+        self.k_off = torch.zeros(B, dtype=torch.int64, device=dev)
+        q_host = np.concatenate([wl.q_bf16(0, t) for t in range(B)])
+        self.q = torch.from_numpy(q_host.view(np.int16)).to(dev)
+        self.w = torch.from_numpy(np.stack([wl.w(0, t) for t in range(B)])).to(dev)
+        self.q_rec = torch.empty(B * 4 * hsi.REC_BYTES, dtype=torch.uint8, device=dev)
+        self.g_q = torch.empty(B, device=dev)
+        self.ws_q = hsi.workspace(hsi.WS_QUANTIZE, B, 0, device=dev)
+        self.nv = torch.tensor(wl.n_visible, dtype=torch.int32, device=dev)
+        self.scores = torch.empty(B, n, device=dev)
+        self.idx = torch.empty(B, K_TOP, dtype=torch.int32, device=dev)
+        self.val = torch.empty(B, K_TOP, device=dev)
+        self.ids = torch.empty(B, wl.n_keep, dtype=torch.int32, device=dev)
+        self.nk = torch.empty(B, dtype=torch.int32, device=dev)
+        self.npool = torch.empty(B, dtype=torch.int32, device=dev)
+        self.bits = torch.empty(B, (n + 31) // 32, dtype=torch.int32, device=dev)
+        self.ws = hsi.workspace(hsi.WS_PREFILL_LAYER, B, n, K_TOP, device=dev)
+        log(f"prefill workload ready in {time.time() - t0:.1f} s")
+
+    def quant(self):
+        self.hsi.quantize_nvfp4(self.q, self.B, 32, self.signs, self.g_q, self.q_rec, ws=self.ws_q)
+
+    def layer(self, phases):
+        self.hsi.prefill_layer(self.q_rec, self.g_q, self.w, self.k_rec, self.g_k, self.k_off, self.nv, self.B,
+                               self.n, self.scores, K_TOP, self.idx, self.val, group=4, block_ids=self.ids,
+                               n_kept=self.nk, n_pool=self.npool, pool_bits=self.bits, n_keep=self.wl.n_keep,
+                               ws=self.ws, phases=phases)
+
+
+def prefill_config(dev, args, log, peaks, calib, clk_mhz, n_sm):
+    """The chunked-prefill workload (compute-bound), timed as graphs of its
+    three segments with the scoring segment timed on its own, against the
+    larger of its three bounds: dense FP4 tensor time at the calibrated rate of
+    the kernel's MMA shape (N = 128), the epilogue's issue time (per (query,
+    key) pair 32 ReLU maxima and 16 packed fp32 fmas, 4 warp instructions per
+    cycle per SM at the sampled SM clock) and the HBM time of its bytes."""
+    import torch
+
+    import long_context_decode_lightning_gb300 as hsi
+    wl = inputs.workload(4)
+    P = PrefillWorkload(wl, dev, log)
+    segs = [("pre", P.quant), ("score", lambda: P.layer(hsi.PHASE_SCORE)),
+            ("post", lambda: P.layer(hsi.PHASE_SELECT))]
+    for _, fn in segs:
+        fn()
+    torch.cuda.synchronize()
+    assert hsi.device_error() == 0, "device error in the prefill workload"
+    graphs = []
+    for kind, fn in segs:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs.append((kind, g))
+    ev = []
+
+    def replay():
+        for kind, g in graphs:
+            if kind == "score":
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                g.replay()
+                e1.record()
+                ev.append((e0, e1))
+            else:
+                g.replay()
+    for _ in range(max(args.warmup, 1)):
+        replay()
+    torch.cuda.synchronize()
+    ev.clear()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        replay()
+    e1.record()
+    torch.cuda.synchronize()
+    assert hsi.device_error() == 0, "device error in the prefill steps"
+    ms = e0.elapsed_time(e1) / args.steps
+    score_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    pairs = int(sum(wl.n_visible))
+    flop = pairs * 32 * 128 * 2
+    t_tensor = flop / (calib["fp4_mma_tflops"]["128"] * 1e12) * 1e3
+    t_alu = pairs * 48 / 32 / (4 * n_sm * clk_mhz * 1e6) * 1e3
+    nb = sum((v + 7) // 8 for v in wl.n_visible)
+    hbm_bytes = (hsi.n_records(P.n) * hsi.REC_BYTES + P.B * (4 * hsi.REC_BYTES + 32 * 4 + 32 * 128 * 2)
+                 + pairs * 4 + nb * 4 * 2 + P.B * (513 * 8 * 4 + (P.n + 31) // 32 * 4 + K_TOP * 8 + wl.n_keep * 4))
+    t_hbm = hbm_bytes / (float(peaks["hbm_gbs"]) * 1e9) * 1e3
+    bounds = {"tensor": t_tensor, "alu": t_alu, "hbm": t_hbm}
+    bind = max(bounds, key=bounds.get)
+    res = {"workload": wl.name, "notes": wl.notes, "ms_per_step": ms, "pairs_per_s": pairs / (ms / 1e3),
+           "top512_selections_per_s": P.B / (ms / 1e3), "pool_builds_per_s": P.B / (ms / 1e3),
+           "pairs_per_step": pairs, "score_ms": score_ms, "select_and_quant_ms": ms - score_ms,
+           "fp4_pflops_achieved": flop / (score_ms / 1e3) / 1e15,
+           "roofline": {"bound": bind, "achieved": pairs / (ms / 1e3), "peak": pairs / (bounds[bind] / 1e3),
+                        "unit": "pairs/s", "frac": bounds[bind] / ms, "bounds_ms": bounds,
+                        "score_kernel_frac": bounds[bind] / score_ms,
+                        "tensor_peak_tflops": calib["fp4_mma_tflops"]["128"], "sm_clock_mhz": clk_mhz,
+                        "hbm_bytes_per_step": hbm_bytes,
+                        "note": "frac = the binding bound's time over the whole layer's time (q quantisation, "
+                                "scoring, selection); score_kernel_frac over the scoring kernel alone"}}
+    del P, graphs
+    torch.cuda.empty_cache()
+    return res
 
 
 # ----------------------------------------------------------- multi-rank --
@@ -808,14 +1042,31 @@ def main():
         line["serve"] = serving_steps(W, M, wl, dev, args, timed, log)
         assert hsi.device_error() == 0, "device error during the serving steps"
     del M
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    if not args.no_configs:
+        del W
+        torch.cuda.empty_cache()
+        calib = calibrate(dev, log, n_sm)
+        line["peaks"] = calib
+        clk = line["clocks"].get("sm_mhz") or 2070.0
+        line["configs"] = {}
+        for idx in (0, 1, 3):
+            line["configs"][str(idx)] = decode_config(idx, dev, args, log, peaks)
+        with ClockSampler(local) as pclk:
+            line["prefill"] = prefill_config(dev, args, log, peaks, calib, clk, n_sm)
+        line["prefill"]["clocks"] = pclk.summary()
     if rank == 0 and not args.no_cpu_baseline:
         nq = cpu_sample_size(wl)
-        log(f"cpu baseline: oracle on {nq} queries")
+        log(f"cpu baseline: oracle on {nq} queries, one per host core, then one query on one core")
         prepared = oracle_sample_setup(wl, nq, args.format)
         p, t = oracle_timed(wl, prepared, nq, args.format)
-        line["cpu_baseline"] = {"value": p / t, "unit": UNIT, "cores": nq, "kind": "oracle",
-                                "sample": f"{nq} of {wl.B} queries, whole path per query (one thread each), "
-                                          f"{t:.1f} s wall"}
+        p1, t1 = oracle_timed(wl, prepared, 1, args.format)
+        line["cpu_baseline"] = {"value": p / t, "unit": UNIT, "cores": nq, "host_cores": os.cpu_count(),
+                                "kind": "oracle",
+                                "sample": f"{nq} of {wl.B} queries, whole path per query, one thread per query "
+                                          f"on {nq} cores, {t:.1f} s wall",
+                                "one_core": {"value": p1 / t1, "unit": UNIT, "cores": 1,
+                                             "sample": f"1 query, whole path, one thread, {t1:.1f} s wall"}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -13,6 +13,7 @@
 #include "common.cuh"
 #include "gather.cuh"
 #include "mainkv.cuh"
+#include "prefill.cuh"
 #include "quantize.cuh"
 #include "rowsel.cuh"
 #include "score.cuh"
@@ -233,6 +234,22 @@ hsi_status launch_score_fmt(const ScoreParams& p, cudaStream_t s) {
     return launch(score_kernel<NQ, GATHER, STAGES, UT, FMT>, dim3(sms), dim3(C::THREADS), C::SMEM_BYTES, s, p);
 }
 
+// The chunked-prefill scorer (all queries on one cache), cache chunks spread
+// over every SM, at most PF_KT_MAX tiles each.
+template <int FMT>
+hsi_status launch_prefill_fmt(const PrefillParams& p, int64_t max_visible, cudaStream_t s) {
+    using C = PfCfg<FMT>;
+    const int sms = sm_count();
+    if (sms <= 0) return HSI_ERR_CUDA;
+    const size_t smem = C::smem_bytes(p.ngroups);
+    static std::atomic<bool> attr_set[kMaxDevices];
+    if (smem_attr_once(prefill_kernel<FMT>, (int)smem, attr_set) != HSI_OK) return HSI_ERR_CUDA;
+    const int64_t ntiles = (max_visible + TILE_KEYS - 1) / TILE_KEYS;
+    const int64_t rounds = (ntiles + (int64_t)sms * PF_KT_MAX - 1) / ((int64_t)sms * PF_KT_MAX);
+    const int64_t nchunks = (int64_t)sms * (rounds > 0 ? rounds : 1);
+    return launch(prefill_kernel<FMT>, dim3(sms), dim3(C::THREADS), smem, s, p, (int)ntiles, (int)nchunks);
+}
+
 // The scoring kernel for the records' format (checked by the caller).
 template <int NQ, bool GATHER, int STAGES, int UT>
 hsi_status launch_score(const ScoreParams& p, hsi_format fmt, cudaStream_t s) {
@@ -359,8 +376,8 @@ size_t hsi_workspace_size(hsi_ws_kind kind, int32_t B, int64_t max_n, int32_t k)
             return sel_ws_bytes(B, max_n, false, 0) + sel_ws_bytes(B, nb, false, 0) +
                    align_up((size_t)B * (size_t)nb * 4, 256);
         }
-        case HSI_WS_PREFILL_LAYER:  // the block maxima
-            return align_up((size_t)B * (size_t)((max_n + 7) / 8) * 4, 256);
+        case HSI_WS_PREFILL_LAYER:  // the block maxima, rows padded to 16 bytes
+            return align_up((size_t)B * align_up((size_t)((max_n + 7) / 8), 4) * 4, 256);
         case HSI_WS_REINDEX_LAYER:  // + the key histogram the pooled scan accumulates
             return sel_ws_bytes(B, max_n, false, 0) + align_up((size_t)B * HIST_BINS * 4, 256);
         case HSI_WS_POOL: {
@@ -773,10 +790,14 @@ hsi_status hsi_prefill_layer(const uint8_t* q_rec, const float* g_q, const float
     if (max_visible > (int64_t)RS_MAX_BLOCKS * 8) return HSI_ERR_UNSUPPORTED;
     if (group != 1 && group != 4) return HSI_ERR_UNSUPPORTED;
     if (B % group) return HSI_ERR_INVALID_ARG;
+    if (group == 4) {  // the queries' tensor scales are copied 16 bytes at a time with their records
+        if (B / 4 > PF_MAX_GROUPS) return HSI_ERR_UNSUPPORTED;
+        if (format == HSI_FMT_NVFP4 && (!aligned(g_q, 16) || !aligned(g_k, 16))) return HSI_ERR_INVALID_ARG;
+    }
     const bool pool = block_ids != nullptr;
     if (pool && (!n_kept || !n_pool || n_keep < 1 || n_keep > SEL_MAXK)) return HSI_ERR_INVALID_ARG;
     if (pool_bits && ld_bits < (max_visible + 31) / 32) return HSI_ERR_INVALID_ARG;
-    const int64_t nb = (max_visible + 7) / 8;
+    const int64_t nb = (int64_t)align_up((size_t)((max_visible + 7) / 8), 4);  // rows of block maxima, 16-byte aligned
     const size_t need = hsi_workspace_size(HSI_WS_PREFILL_LAYER, B, max_visible, k);
     if (!ws || ws_bytes < need || !aligned(ws, 256)) return HSI_ERR_WORKSPACE;
     float* bmax = static_cast<float*>(ws);
@@ -796,8 +817,27 @@ hsi_status hsi_prefill_layer(const uint8_t* q_rec, const float* g_q, const float
         p.ld = ld;
         p.bmax = bmax;
         p.ldb = nb;
-        st = group == 1 ? launch_score<1, false, kDecodeStages, kDecodeUT>(p, format, stream)
-                        : launch_score<4, false, kPrefillStages, kPrefillUT>(p, format, stream);
+        if (group == 1) {
+            st = launch_score<1, false, kDecodeStages, kDecodeUT>(p, format, stream);
+        } else {
+            PrefillParams pp{};
+            pp.q_rec = q_rec;
+            pp.g_q = g_q;
+            pp.w = w;
+            pp.k_rec = k_rec;
+            pp.g_k = g_k;
+            pp.k_off = k_rec_off;
+            pp.n_vis = n_visible;
+            pp.max_vis = (int32_t)max_visible;
+            pp.B = B;
+            pp.ngroups = B / 4;
+            pp.scores = scores;
+            pp.ld = ld;
+            pp.bmax = bmax;
+            pp.ldb = nb;
+            st = format == HSI_FMT_MXFP4 ? launch_prefill_fmt<FMT_MXFP4>(pp, max_visible, stream)
+                                         : launch_prefill_fmt<FMT_NVFP4>(pp, max_visible, stream);
+        }
         if (st != HSI_OK) return st;
     }
     if (!(phases & HSI_PHASE_SELECT)) return HSI_OK;

@@ -27,7 +27,7 @@ namespace hsi {
 
 constexpr int RS_THREADS = 256;
 constexpr int RS_WARPS = RS_THREADS / 32;
-constexpr int RS_CAP = 4104;             // staged items: blocks after the 12-bit filter, then candidate scores
+constexpr int RS_CAP = 3072;             // staged items: blocks after the 12-bit filter, then candidate positions
 constexpr int RS_MAX_BLOCKS = 65536;     // blocks per row (n_visible <= 524288)
 constexpr int RS_MAXK = 2048;            // largest k
 constexpr uint32_t RS_ALL = 0xFFFFFFFFu;  // index cutoff that takes every tied item
@@ -70,12 +70,12 @@ struct RowSelSmem {
 };
 
 // Item sources: n items, item j's order key (and whether it is eligible) and index.
-struct RsBlockRow {  // the row of block maxima in global memory, newest block pinned
+struct RsBlockRow {  // the row of block maxima in global memory, all but the newest block
     const float* row;
     int64_t n;
     __device__ uint32_t key(int64_t j, bool& ok) const {
         ok = true;
-        return j == n - 1 ? RS_KEY_POS_INF : order_key(row[j]);
+        return order_key(row[j]);
     }
     __device__ uint32_t idx(int64_t j) const { return (uint32_t)j; }
 };
@@ -94,10 +94,13 @@ struct RsCandScores {  // the 8 positions of each candidate block, scores in glo
     const int32_t* blocks;
     int64_t n;  // 8 x candidate blocks
     int64_t n_vis;
+    uint32_t lo;  // positions whose key is below lo are not eligible
     __device__ uint32_t key(int64_t j, bool& ok) const {
         const int64_t pos = (int64_t)blocks[j >> 3] * 8 + (j & 7);
         ok = pos < n_vis;
-        return ok ? order_key(row[pos]) : 0u;
+        const uint32_t k = ok ? order_key(row[pos]) : 0u;
+        ok = ok && k >= lo;
+        return k;
     }
     __device__ uint32_t idx(int64_t j) const { return (uint32_t)((int64_t)blocks[j >> 3] * 8 + (j & 7)); }
 };
@@ -248,18 +251,67 @@ __device__ __forceinline__ int rs_bits_for(int64_t n) {  // bits holding every i
     return n <= 1 ? 1 : 64 - __clzll((unsigned long long)(n - 1));
 }
 
-// Slot of this lane's item in a shared-memory list counted by *counter (one
-// atomic per warp; every lane of the warp calls it).
-__device__ __forceinline__ uint32_t rs_append(bool take, uint32_t* counter) {
-    const uint32_t m = __ballot_sync(0xFFFFFFFFu, take);
+// Slot of this thread's first item in a shared-memory list counted by
+// *counter, for the items it marks in `take` (one bit each; its items follow
+// consecutively): one warp scan and one atomic per warp. Every lane of the
+// warp calls it.
+__device__ __forceinline__ uint32_t rs_append_mask(uint32_t take, uint32_t* counter) {
     const int lane = threadIdx.x & 31;
-    uint32_t base = 0;
-    if (m) {
-        const int leader = __ffs(m) - 1;
-        if (lane == leader) base = atomicAdd(counter, (uint32_t)__popc(m));
-        base = __shfl_sync(0xFFFFFFFFu, base, leader);
+    const uint32_t c = (uint32_t)__popc(take);
+    uint32_t inc = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o) inc += t;
     }
-    return base + (uint32_t)__popc(m & ((1u << lane) - 1u));
+    uint32_t base = 0;
+    if (lane == 31 && inc) base = atomicAdd(counter, inc);
+    base = __shfl_sync(0xFFFFFFFFu, base, 31);
+    return base + inc - c;
+}
+
+// A bitonic compare-exchange of element e (value x) with its partner e ^ str
+// (value y) inside merges of `size`: the final order is descending.
+__device__ __forceinline__ unsigned long long rs_cmpx(unsigned long long x, unsigned long long y, int e, int str,
+                                                      int size) {
+    const bool keep_max = ((e & size) == 0) == ((e & str) == 0);
+    return keep_max ? (x > y ? x : y) : (x < y ? x : y);
+}
+
+// Whole block: sort s.win[0 .. 512) descending (entries past count must be
+// 0, below every real entry). Thread t holds elements t and t + 256 in
+// registers: partners 256 apart are in the same thread, partners 1 .. 16
+// apart in the same warp (shuffles), only strides 32 .. 128 go through
+// shared memory.
+__device__ void rs_sort512(RowSelSmem& s) {
+    const int t = threadIdx.x;
+    unsigned long long x[2] = {s.win[t], s.win[t + 256]};
+    __syncthreads();
+    for (int size = 2; size <= 512; size <<= 1) {
+        for (int str = size >> 1; str > 0; str >>= 1) {
+            if (str == 256) {
+                const unsigned long long a = rs_cmpx(x[0], x[1], t, 256, size);
+                x[1] = rs_cmpx(x[1], x[0], t + 256, 256, size);
+                x[0] = a;
+            } else if (str < 32) {
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const unsigned long long y = __shfl_xor_sync(0xFFFFFFFFu, x[r], str);
+                    x[r] = rs_cmpx(x[r], y, t + 256 * r, str, size);
+                }
+            } else {
+                s.win[t] = x[0];
+                s.win[t + 256] = x[1];
+                __syncthreads();
+#pragma unroll
+                for (int r = 0; r < 2; ++r) x[r] = rs_cmpx(x[r], s.win[(t + 256 * r) ^ str], t + 256 * r, str, size);
+                __syncthreads();
+            }
+        }
+    }
+    s.win[t] = x[0];
+    s.win[t + 256] = x[1];
+    __syncthreads();
 }
 
 // Whole block: sort s.win[0 .. count) descending (bitonic network over the
@@ -300,34 +352,90 @@ __global__ void __launch_bounds__(RS_THREADS) rowsel_kernel(RowSelParams p) {
     }
     if (n_vis < 0) n_vis = 0;
     const int64_t nblk = (n_vis + 7) / 8;
-    const RsBlockRow rowsrc{p.bmax + (int64_t)b * p.ldb, nblk};
+    const RsBlockRow rowsrc{p.bmax + (int64_t)b * p.ldb, nblk > 0 ? nblk - 1 : 0};
 
-    // 1. 4096-bin histogram of the blocks' keys (top 12 bits)
-    for (int i = tid; i < 4096; i += RS_THREADS) s.hist[i] = 0u;
-    if (tid == 0) s.count = 0;
-    __syncthreads();
-    for (int64_t j = tid; j < nblk; j += RS_THREADS) {
-        bool ok;
-        atomicAdd(&s.hist[rowsrc.key(j, ok) >> 20], 1u);
-    }
-    __syncthreads();
-    // 2. threshold bins of the pool's rank and of the top-k's candidate blocks
+    // The newest block is pinned first in both orders, so it is taken apart:
+    // the selections run over the other nu = nblk - 1 blocks for ranks r - 1.
+    const int64_t nu = nblk > 0 ? nblk - 1 : 0;
     const uint32_t r_pool = (uint32_t)min((int64_t)p.n_keep, nblk);
     const uint32_t r_cand = (uint32_t)min((int64_t)p.k + 1, nblk);
-    uint32_t tb_pool = 4095, ab_pool = 0, tb_cand = 4095, ab_cand = 0, at;
-    if (r_pool > 0) tb_pool = rs_find(s, 4096, r_pool, true, &ab_pool, &at);
-    if (r_cand > 0) tb_cand = rs_find(s, 4096, r_cand, true, &ab_cand, &at);
-    const uint32_t lo_bin = min(r_pool > 0 ? tb_pool : 4095u, r_cand > 0 ? tb_cand : 4095u);
-    // 3. stage the blocks at or above the lower bin
-    for (int64_t j0 = 0; j0 < nblk; j0 += RS_THREADS) {
-        const int64_t j = j0 + tid;
-        bool ok;
-        const uint32_t key = j < nblk ? rowsrc.key(j, ok) : 0u;
-        const bool take = j < nblk && (key >> 20) >= lo_bin;
-        const uint32_t slot = rs_append(take, &s.count);
-        if (take && slot < RS_CAP) {
-            s.ckey[slot] = key;
-            s.cidx[slot] = (uint32_t)j;
+    const uint32_t rp = r_pool > 0 ? r_pool - 1 : 0, rc = r_cand > 0 ? r_cand - 1 : 0;
+    constexpr int U = 8;  // 16-byte loads per thread issued before any is used
+    const float4* row4 = reinterpret_cast<const float4*>(rowsrc.row);
+    const int64_t n4 = (nu + 3) / 4;
+    // fn(bit, j, key) for the 32 unpinned blocks of this thread in round q0
+    auto round = [&](int64_t q0, auto fn) {
+        float4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t q = q0 + u * RS_THREADS + tid;
+            v[u] = q < n4 ? row4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t j0 = 4 * (q0 + u * RS_THREADS + tid);
+            const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) fn(4 * u + e, j0 + e, j0 + e < nu, order_key(f[e]));
+        }
+    };
+    // 1. the largest key M of the unpinned blocks
+    uint32_t mx = 0;
+    for (int64_t q0 = 0; q0 < n4; q0 += (int64_t)U * RS_THREADS)
+        round(q0, [&](int, int64_t, bool in, uint32_t key) {
+            if (in) mx = max(mx, key);
+        });
+    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+    if ((tid & 31) == 0) s.scan[tid >> 5] = mx;
+    if (tid == 0) s.count = 0;
+    __syncthreads();
+    uint32_t M = 0;
+#pragma unroll
+    for (int w = 0; w < RS_WARPS; ++w) M = max(M, s.scan[w]);
+    __syncthreads();
+    // 2. histogram of the keys relative to M: bin (M >> sh) - (key >> sh), 4096
+    // bins from the top (scores cluster: relative bins of 1/2048 octave spread
+    // the top ranks where bins of the keys' top 12 bits would not); bins capped
+    // at 4095. If a rank falls in the capped bin, again with sh = 20, where no
+    // bin is capped.
+    uint32_t tb_pool = 0, ab_pool = 0, tb_cand = 0, ab_cand = 0, at;
+    int sh = 12;
+    for (int attempt = 0; attempt < 2 && (rp > 0 || rc > 0); ++attempt) {
+        for (int i = tid; i < 4096; i += RS_THREADS) s.hist[i] = 0u;
+        __syncthreads();
+        const uint32_t Ms = M >> sh;
+        for (int64_t q0 = 0; q0 < n4; q0 += (int64_t)U * RS_THREADS)
+            round(q0, [&](int, int64_t, bool in, uint32_t key) {
+                if (in) atomicAdd(&s.hist[min(Ms - (key >> sh), 4095u)], 1u);
+            });
+        __syncthreads();
+        if (rp > 0) tb_pool = rs_find(s, 4096, rp, false, &ab_pool, &at);
+        if (rc > 0) tb_cand = rs_find(s, 4096, rc, false, &ab_cand, &at);
+        if (sh == 20 || ((rp == 0 || tb_pool < 4095) && (rc == 0 || tb_cand < 4095))) break;
+        sh = 20;
+    }
+    const uint32_t Ms = M >> sh;
+    const uint32_t hi_bin = max(rp > 0 ? tb_pool : 0u, rc > 0 ? tb_cand : 0u);
+    // 3. stage the blocks in bins 0 .. hi_bin (the row is read again, from L2)
+    if (rp > 0 || rc > 0) {
+        for (int64_t q0 = 0; q0 < n4; q0 += (int64_t)U * RS_THREADS) {
+            uint32_t keys[4 * U];
+            uint32_t take = 0;
+            round(q0, [&](int bit, int64_t, bool in, uint32_t key) {
+                keys[bit] = key;
+                if (in && Ms - (key >> sh) <= hi_bin) take |= 1u << bit;
+            });
+            uint32_t slot = rs_append_mask(take, &s.count);
+#pragma unroll
+            for (int i = 0; i < 4 * U; ++i) {
+                if ((take >> i) & 1u) {
+                    if (slot < RS_CAP) {
+                        s.ckey[slot] = keys[i];
+                        s.cidx[slot] = (uint32_t)(4 * (q0 + (i / 4) * RS_THREADS + tid) + (i % 4));
+                    }
+                    ++slot;
+                }
+            }
         }
     }
     __syncthreads();
@@ -335,13 +443,15 @@ __global__ void __launch_bounds__(RS_THREADS) rowsel_kernel(RowSelParams p) {
     const bool fits = staged <= RS_CAP;
     const int blk_bits = rs_bits_for(nblk);
     const RsStaged stsrc{s.ckey, s.cidx, (int64_t)staged};
-    RsCut c_pool{0u, 0u}, c_cand{0u, 0u};
-    if (r_pool > 0)
-        c_pool = fits ? rs_select(stsrc, s, r_pool, tb_pool, 12, ab_pool, blk_bits)
-                      : rs_select(rowsrc, s, r_pool, tb_pool, 12, ab_pool, blk_bits);
-    if (r_cand > 0)
-        c_cand = fits ? rs_select(stsrc, s, r_cand, tb_cand, 12, ab_cand, blk_bits)
-                      : rs_select(rowsrc, s, r_cand, tb_cand, 12, ab_cand, blk_bits);
+    constexpr RsCut none{0xFFFFFFFFu, 0u};  // no unpinned block taken (order keys never reach it)
+    RsCut c_pool = none, c_cand = none;
+    if (rp > 0)
+        c_pool = fits ? rs_select(stsrc, s, rp, Ms - tb_pool, 32 - sh, ab_pool, blk_bits)
+                      : rs_select(rowsrc, s, rp, Ms - tb_pool, 32 - sh, ab_pool, blk_bits);
+    if (rc > 0)
+        c_cand = fits ? rs_select(stsrc, s, rc, Ms - tb_cand, 32 - sh, ab_cand, blk_bits)
+                      : rs_select(rowsrc, s, rc, Ms - tb_cand, 32 - sh, ab_cand, blk_bits);
+    const int64_t nsrc = fits ? (int64_t)staged : nu;  // unpinned blocks the pool and the candidates come from
 
     // 4. the pool: kept blocks (dropping -inf ones) as a bitmap, then their ids
     // ascending, the visible-position count and the boolean table
@@ -351,13 +461,12 @@ __global__ void __launch_bounds__(RS_THREADS) rowsel_kernel(RowSelParams p) {
         const int64_t zwords = max(words, ((n_vis + 31) / 32 + 7) / 8);
         for (int64_t w = tid; w < zwords; w += RS_THREADS) s.bitmap[w] = 0u;
         __syncthreads();
-        const int64_t nsrc = fits ? (int64_t)staged : nblk;
+        if (tid == 0 && r_pool > 0) atomicOr(&s.bitmap[(nblk - 1) >> 5], 1u << ((nblk - 1) & 31));  // pinned
         for (int64_t j = tid; j < nsrc; j += RS_THREADS) {
             bool ok;
             const uint32_t key = fits ? s.ckey[j] : rowsrc.key(j, ok);
             const uint32_t id = fits ? s.cidx[j] : (uint32_t)j;
-            if (r_pool > 0 && rs_taken(key, id, c_pool) && key != RS_KEY_NEG_INF)
-                atomicOr(&s.bitmap[id >> 5], 1u << (id & 31));
+            if (rs_taken(key, id, c_pool) && key != RS_KEY_NEG_INF) atomicOr(&s.bitmap[id >> 5], 1u << (id & 31));
         }
         __syncthreads();
         // ids ascending: thread t owns words [t per, t per + per)
@@ -391,11 +500,9 @@ __global__ void __launch_bounds__(RS_THREADS) rowsel_kernel(RowSelParams p) {
             uint32_t* bits = p.bits + (int64_t)b * p.ld_bits;
             const int64_t pw = (n_vis + 31) / 32;
             for (int64_t w = tid; w < pw; w += RS_THREADS) {
-                const uint32_t nib = (s.bitmap[w >> 3] >> ((w & 7) * 4)) & 0xFu;  // blocks 4w .. 4w+3
-                uint32_t v = 0;
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    if ((nib >> q) & 1u) v |= 0xFFu << (8 * q);
+                // blocks 4w .. 4w+3: bit q of the nibble becomes byte q of the word
+                const uint32_t nib = (s.bitmap[w >> 3] >> ((w & 7) * 4)) & 0xFu;
+                uint32_t v = ((nib * 0x00204081u) & 0x01010101u) * 0xFFu;
                 const int64_t left = n_vis - w * 32;
                 if (left < 32) v &= (1u << left) - 1u;
                 bits[w] = v;
@@ -406,86 +513,121 @@ __global__ void __launch_bounds__(RS_THREADS) rowsel_kernel(RowSelParams p) {
 
     // 5. the top-k among the candidate blocks' positions
     if (p.k > 0) {
-        if (tid == 0) s.count = 0;
+        if (tid == 0) {
+            s.count = r_cand > 0 ? 1u : 0u;
+            if (r_cand > 0) s.cblk[0] = (int32_t)(nblk - 1);  // the pinned block
+        }
         __syncthreads();
-        const int64_t nsrc = fits ? (int64_t)staged : nblk;
-        for (int64_t j0 = 0; j0 < nsrc; j0 += RS_THREADS) {
-            const int64_t j = j0 + tid;
-            bool ok;
-            uint32_t key = 0, id = 0;
-            if (j < nsrc) {
-                key = fits ? s.ckey[j] : rowsrc.key(j, ok);
-                id = fits ? s.cidx[j] : (uint32_t)j;
+        for (int64_t j0 = 0; j0 < nsrc; j0 += 8 * RS_THREADS) {
+            uint32_t take = 0, id[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int64_t j = j0 + u * RS_THREADS + tid;
+                bool ok = false;
+                uint32_t key = 0;
+                id[u] = 0;
+                if (j < nsrc) {
+                    key = fits ? s.ckey[j] : rowsrc.key(j, ok);
+                    id[u] = fits ? s.cidx[j] : (uint32_t)j;
+                    if (rs_taken(key, id[u], c_cand)) take |= 1u << u;
+                }
             }
-            const bool take = j < nsrc && r_cand > 0 && rs_taken(key, id, c_cand);
-            const uint32_t slot = rs_append(take, &s.count);
-            if (take && slot <= (uint32_t)RS_MAXK) s.cblk[slot] = (int32_t)id;
+            uint32_t slot = rs_append_mask(take, &s.count);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if ((take >> u) & 1u) {
+                    if (slot <= (uint32_t)RS_MAXK) s.cblk[slot] = (int32_t)id[u];
+                    ++slot;
+                }
         }
         __syncthreads();
         const int64_t ncb = min((int64_t)s.count, (int64_t)RS_MAXK + 1);
         __syncthreads();
-        // stage the candidates' scores when they fit (their keys and positions)
+        // Every top-k position has a score at or above the k-th largest block
+        // maximum, which is at least the key of the last candidate block (the
+        // (k+1)-th of the pinned order) when there are more than k blocks; only
+        // the candidate positions at or above that key are staged. With k + 1
+        // blocks or fewer every visible position is a candidate.
+        const uint32_t lo = r_cand == (uint32_t)p.k + 1 ? c_cand.key : 0u;
         const float* row = p.scores + (int64_t)b * p.ld;
-        const RsCandScores gsrc{row, s.cblk, ncb * 8, n_vis};
-        const bool fits2 = ncb * 8 <= RS_CAP;
-        uint32_t eligible = 0;
-        if (fits2) {
-            if (tid == 0) s.count = 0;
-            __syncthreads();
-            for (int64_t j0 = 0; j0 < ncb * 8; j0 += RS_THREADS) {
-                const int64_t j = j0 + tid;
-                bool ok = false;
-                uint32_t key = 0;
-                if (j < ncb * 8) key = gsrc.key(j, ok);
-                const uint32_t slot = rs_append(ok, &s.count);
-                if (ok) {
-                    s.ckey[slot] = key;
-                    s.cidx[slot] = gsrc.idx(j);
+        if (tid == 0) s.count = 0;
+        __syncthreads();
+        for (int64_t c0 = 0; c0 < ncb; c0 += 2 * RS_THREADS) {  // two blocks (16 positions) per thread per round
+            float v[16];
+            int64_t base[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int64_t ci = c0 + u * RS_THREADS + tid;
+                base[u] = ci < ncb ? (int64_t)s.cblk[ci] * 8 : -1;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[8 * u + e] = base[u] >= 0 && base[u] + e < n_vis ? row[base[u] + e] : 0.f;
+            }
+            uint32_t take = 0;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (base[i / 8] >= 0 && base[i / 8] + (i % 8) < n_vis && order_key(v[i]) >= lo) take |= 1u << i;
+            uint32_t slot = rs_append_mask(take, &s.count);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if ((take >> i) & 1u) {
+                    if (slot < RS_CAP) {
+                        s.ckey[slot] = order_key(v[i]);
+                        s.cidx[slot] = (uint32_t)(base[i / 8] + (i % 8));
+                    }
+                    ++slot;
                 }
-            }
-            __syncthreads();
-            eligible = s.count;
-        } else {
-            uint32_t e = 0;
-            for (int64_t j = tid; j < ncb * 8; j += RS_THREADS) {
-                bool ok;
-                gsrc.key(j, ok);
-                e += ok;
-            }
-            uint32_t tot;
-            rs_scan(e, false, s, &tot);
-            eligible = tot;
         }
-        const uint32_t kk = min((uint32_t)p.k, eligible);
-        const RsStaged st2{s.ckey, s.cidx, (int64_t)eligible};
+        __syncthreads();
+        const uint32_t staged2 = s.count;
+        const bool fits2 = staged2 <= RS_CAP;
+        const RsCandScores gsrc{row, s.cblk, ncb * 8, n_vis, lo};
+        const uint32_t kk = (uint32_t)min((int64_t)p.k, n_vis);  // all of them lie among the staged positions
+        const RsStaged st2{s.ckey, s.cidx, (int64_t)staged2};
         const int pos_bits = rs_bits_for(n_vis);
         RsCut c{0u, 0u};
         if (kk > 0) c = fits2 ? rs_select(st2, s, kk, 0u, 0, 0u, pos_bits) : rs_select(gsrc, s, kk, 0u, 0, 0u, pos_bits);
         // winners, then sorted by (key desc, position asc)
         if (tid == 0) s.count = 0;
         __syncthreads();
-        const int64_t n2 = fits2 ? (int64_t)eligible : ncb * 8;
-        for (int64_t j0 = 0; j0 < n2; j0 += RS_THREADS) {
-            const int64_t j = j0 + tid;
-            bool ok = false;
-            uint32_t key = 0, id = 0;
-            if (j < n2) {
-                if (fits2) {
-                    ok = true;
-                    key = s.ckey[j];
-                    id = s.cidx[j];
-                } else {
-                    key = gsrc.key(j, ok);
-                    id = gsrc.idx(j);
+        const int64_t n2 = fits2 ? (int64_t)staged2 : ncb * 8;
+        for (int64_t j0 = 0; j0 < n2; j0 += 8 * RS_THREADS) {
+            uint32_t take = 0;
+            unsigned long long w8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int64_t j = j0 + u * RS_THREADS + tid;
+                bool ok = false;
+                uint32_t key = 0, id = 0;
+                if (j < n2) {
+                    if (fits2) {
+                        ok = true;
+                        key = s.ckey[j];
+                        id = s.cidx[j];
+                    } else {
+                        key = gsrc.key(j, ok);
+                        id = gsrc.idx(j);
+                    }
                 }
+                if (ok && kk > 0 && rs_taken(key, id, c)) take |= 1u << u;
+                w8[u] = ((unsigned long long)key << 32) | (uint32_t)~id;
             }
-            const bool take = ok && kk > 0 && rs_taken(key, id, c);
-            const uint32_t slot = rs_append(take, &s.count);
-            if (take && slot < (uint32_t)RS_MAXK) s.win[slot] = ((unsigned long long)key << 32) | (uint32_t)~id;
+            uint32_t slot = rs_append_mask(take, &s.count);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if ((take >> u) & 1u) {
+                    if (slot < (uint32_t)RS_MAXK) s.win[slot] = w8[u];
+                    ++slot;
+                }
         }
         __syncthreads();
         const int cnt = (int)min(s.count, kk);
-        rs_sort_desc(s, cnt);
+        if (cnt <= 512) {
+            for (int i = cnt + tid; i < 512; i += RS_THREADS) s.win[i] = 0ull;
+            __syncthreads();
+            rs_sort512(s);
+        } else {
+            rs_sort_desc(s, cnt);
+        }
         int32_t* oi = p.out_idx + (int64_t)b * p.k;
         float* ov = p.out_val + (int64_t)b * p.k;
         for (int t = tid; t < p.k; t += RS_THREADS) {

@@ -109,8 +109,15 @@ struct ScoreCfg {
     static constexpr int QSLOT_BYTES = ((Q_BYTES + 127) / 128) * 128;
     // gather: a warpgroup of 16-byte async copies (4 threads per pooled block)
     static constexpr int PROD_WARPS = GATHER ? 4 : 1;
+    // MMA-issuing warps (one thread each), taking alternate units: a single
+    // thread's issue sequence (waits, descriptors, MMAs, commit) per unit is
+    // longer than the tensor work of a 4-query tile
+#ifndef HSI_DECODE_ISSUERS
+#define HSI_DECODE_ISSUERS 1
+#endif
+    static constexpr int MMA_ISSUERS = GATHER ? 1 : NQ > 1 ? 2 : HSI_DECODE_ISSUERS;
     static constexpr int MMA_WARP = PROD_WARPS;
-    static constexpr int FIRST_SF_WARP = PROD_WARPS + 1;
+    static constexpr int FIRST_SF_WARP = PROD_WARPS + MMA_ISSUERS;
     static constexpr int FIRST_EPI_WARP = FIRST_SF_WARP + 4;
     // single queries: two groups taking alternate units; multi-query tiles: one
     // group per query, every group reading its query's 32 columns of every tile
@@ -385,6 +392,26 @@ __device__ __forceinline__ float head_sum(const float (&x)[32], const uint64_t (
     return (s0 + s1) + (s2 + s3);
 }
 
+// The same sum in two halves of 16 heads (h = 0: heads 0 .. 15, h = 1: heads
+// 16 .. 31), carrying the chains (a = (s0, s1), b = (s2, s3)) from one half to
+// the next: head_sum_final after both gives bit for bit head_sum's result.
+__device__ __forceinline__ void head_sum_half(const uint32_t (&r)[16], const uint64_t (&w2)[16], int h, uint64_t& a,
+                                              uint64_t& b) {
+#pragma unroll
+    for (int j = 0; j < 16; j += 4) {
+        const int jw = (16 * h + j) >> 1;
+        a = f2_fma(w2[jw], f2_pack(fmaxf(__uint_as_float(r[j]), 0.f), fmaxf(__uint_as_float(r[j + 1]), 0.f)), a);
+        b = f2_fma(w2[jw + 1], f2_pack(fmaxf(__uint_as_float(r[j + 2]), 0.f), fmaxf(__uint_as_float(r[j + 3]), 0.f)),
+                   b);
+    }
+}
+__device__ __forceinline__ float head_sum_final(uint64_t a, uint64_t b) {
+    float s0, s1, s2, s3;
+    f2_unpack(a, s0, s1);
+    f2_unpack(b, s2, s3);
+    return (s0 + s1) + (s2 + s3);
+}
+
 template <int NQ, bool GATHER, int STAGES, int UT, int FMT>
 __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS, 1) score_kernel(ScoreParams p) {
     using C = ScoreCfg<NQ, GATHER, STAGES, UT, FMT>;
@@ -431,14 +458,14 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS
         for (int i = 0; i < 2; ++i) {
             mbar_init(&q_full[i], 1);
             mbar_init(&q_ready[i], 4);
-            mbar_init(&q_empty[i], 1);
+            mbar_init(&q_empty[i], C::MMA_ISSUERS);
         }
         if (GATHER)
             for (int i = 0; i < IDS_AHEAD; ++i) {
                 mbar_init(&ids_full[i], 1);
                 mbar_init(&ids_free[i], C::PROD_WARPS);
             }
-        mbar_init(drain, 1);
+        mbar_init(drain, C::MMA_ISSUERS);
         sh->abort = 0;
         fence_mbar_init();
     }
@@ -593,9 +620,11 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS
                 for (long long v = fetched > IDS_AHEAD ? fetched - IDS_AHEAD : 0; v < fetched; ++v)
                     wait_drain(&ids_full[(int)(v % IDS_AHEAD)], (uint32_t)((v / IDS_AHEAD) & 1));
         }
-    } else if (warp == C::MMA_WARP) {
+    } else if (warp < C::MMA_WARP + C::MMA_ISSUERS) {
         // ----------------------------------------------------------------- MMA
-        // one thread issues everything; the rest of the warp waits at the end
+        // lane 0 of each MMA warp issues the MMAs and commits of every
+        // MMA_ISSUERS-th unit; the rest of the warp waits at the end
+        const int issuer = warp - C::MMA_WARP;
         if (lane == 0) {
             UnitIter<NQ, GATHER, UT> it;
             it.init(p, sh);
@@ -604,10 +633,18 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS
             Ring st, ac;
             for (long long u = 0; u < count; ++u) {
                 if (it.g != cur_g) {
-                    if (cur_g >= 0) tc_commit(&q_empty[gc & 1]);  // old slot free once its MMAs finish
+                    // the old q slot is free once this thread's MMAs on it finish (every
+                    // issuer commits, whether it issued on the slot or not)
+                    if (cur_g >= 0) tc_commit(&q_empty[gc & 1]);
                     cur_g = it.g;
                     ++gc;
                     if (!wait_one(&q_ready[gc & 1], (gc >> 1) & 1, sh, tr, TR_MMA_QREADY)) break;
+                }
+                if (C::MMA_ISSUERS > 1 && (int)(u % C::MMA_ISSUERS) != issuer) {  // another issuer's unit
+                    st.next(STAGES);
+                    ac.next(C::NACC);
+                    it.next(p);
+                    continue;
                 }
                 if (!wait_one(&sfready[st.i], st.ph, sh, tr, TR_MMA_SFREADY)) break;
                 HSI_TSTART(t_issue);

@@ -87,11 +87,12 @@ def _select_on(scores, lengths, k=512, n_keep=2048):
     into the workspace where the scoring phase leaves them."""
     B, maxv = scores.shape
     nb = (maxv + 7) // 8
+    ldb = (nb + 3) // 4 * 4  # rows of block maxima padded to 16 bytes
     ws = hsi.workspace(hsi.WS_PREFILL_LAYER, B, maxv, k, device=DEV)
     pad = torch.full((B, nb * 8), float("-inf"), device=DEV)
     for b, n in enumerate(lengths):
         pad[b, :n] = scores[b, :n]
-    ws[: B * nb * 4].view(torch.float32).view(B, nb)[:] = pad.view(B, nb, 8).amax(2)
+    ws[: B * ldb * 4].view(torch.float32).view(B, ldb)[:, :nb] = pad.view(B, nb, 8).amax(2)
     out = _outputs(B, maxv, k, n_keep)
     dummy = torch.zeros(16, dtype=torch.uint8, device=DEV)
     hsi.prefill_layer(dummy, torch.ones(B, device=DEV), torch.zeros(B, 32, device=DEV), dummy,
