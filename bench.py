@@ -514,8 +514,7 @@ def serving_steps(W: DeviceWorkload, M: MainKV, wl: inputs.Workload, dev, args, 
                          kv=M.kv, kv_off=M.off, fmt=W.fmt)
         for _, fn in W.segments(maxv=W.maxv_cap):
             fn()
-        for l in range(W.layers):
-            hsi.gather_mainkv(M.kv, M.off, W.n_vis, W.idx[l], K_TOP, B, rows[l])
+        hsi.gather_mainkv_layers(M.kv, M.off, W.n_vis, W.idx, K_TOP, B, rows)  # every layer's top-512, one launch
 
     k_stage.copy_(new_k[0])
     v_stage.copy_(new_v[0])
@@ -989,9 +988,8 @@ def main():
         # gather(main_kv, topk) of every layer's top-512 of the last step, into bf16
         kv_out = torch.empty(W.layers, W.B, K_TOP, hsi.KV_DIM, dtype=torch.int16, device=dev)
 
-        def gathers():
-            for l in range(W.layers):
-                hsi.gather_mainkv(M.kv, M.off, W.n_vis, W.idx[l], K_TOP, W.B, kv_out[l])
+        def gathers():  # every layer's top-512 in one launch
+            hsi.gather_mainkv_layers(M.kv, M.off, W.n_vis, W.idx, K_TOP, W.B, kv_out)
         gathers()  # sets the launch attributes before capture
         torch.cuda.synchronize()
         g_graph = torch.cuda.CUDAGraph()  # the step's gathers as one graph, as the step itself runs
@@ -1010,7 +1008,7 @@ def main():
             "entries_per_step": W.layers * W.B * K_TOP, "bytes_per_step": bytes_g,
             "roofline": {"bound": "hbm", "achieved": gbs_g, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                          "frac": gbs_g / float(peaks["hbm_gbs"]), "traffic": None,
-                         "kernel": "hsi_gather_mainkv (mainkv_gather_kernel)"},
+                         "kernel": "hsi_gather_mainkv_layers (mainkv_gather_kernel), all layers in one launch"},
             "note": "the top-512 of each of the step's layers gathered from 288-byte FP4 main-KV entries "
                     f"({M.entries * hsi.KV_ENTRY_BYTES / 1e9:.1f} GB resident) and decoded to bf16 rows; "
                     "bytes = 288 read + 1024 written + 4 of index per selected entry"}

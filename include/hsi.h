@@ -369,6 +369,20 @@ hsi_status hsi_gather_mainkv(const uint8_t* kv, const int64_t* kv_off, const int
                              cudaStream_t stream);
 
 /*
+ * hsi_gather_mainkv for the top-k lists of L layers of one decode step in
+ * one launch (the pages' step gathers the selected entries of every layer;
+ * one launch has one ramp where L launches have L): list l is read at
+ * idx + l * idx_stride ([B][ld_idx]) and its rows are written at
+ * out + l * out_stride (bf16 elements, [B][k][512]), against the same caches.
+ * Results equal L calls of hsi_gather_mainkv.
+ *  idx_stride >= B * ld_idx and out_stride >= B * k * 512 (a multiple of 8)
+ *  when L > 1; other arguments as for hsi_gather_mainkv.
+ */
+hsi_status hsi_gather_mainkv_layers(const uint8_t* kv, const int64_t* kv_off, const int32_t* n_visible,
+                                    const int32_t* idx, int64_t ld_idx, int64_t idx_stride, int32_t L, int32_t k,
+                                    int32_t B, uint16_t* out, int64_t out_stride, cudaStream_t stream);
+
+/*
  * Append one decode token to every query's caches: the new position's
  * indexer K row (rotated and quantised as hsi_quantize_nvfp4 does in mode 1,
  * with the cache's fixed tensor scale g_k[b]; or as hsi_quantize_mxfp4 does)

@@ -32,7 +32,8 @@ EXPORTS = ["hsi_quantize_nvfp4", "hsi_score_full", "hsi_topk", "hsi_candidate_po
            "hsi_workspace_size", "hsi_device_error", "hsi_device_check", "hsi_status_string",
            "hsi_kernel_launches", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer", "hsi_reindex_layer",
            "hsi_topk_noalloc", "hsi_debug_set", "hsi_pool_gather", "hsi_quantize_mxfp4", "hsi_quantize_mainkv",
-           "hsi_gather_mainkv", "hsi_append_token", "hsi_mask_scores", "hsi_prefill_layer"]
+           "hsi_gather_mainkv", "hsi_append_token", "hsi_mask_scores", "hsi_prefill_layer",
+           "hsi_gather_mainkv_layers"]
 
 
 class HsiError(RuntimeError):
@@ -69,6 +70,7 @@ def lib() -> ctypes.CDLL:
         L.hsi_quantize_mxfp4.argtypes = [vp, i64, i64, vp, vp, vp]
         L.hsi_quantize_mainkv.argtypes = [vp, i64, vp, vp]
         L.hsi_gather_mainkv.argtypes = [vp, vp, vp, vp, i64, i32, i32, vp, vp]
+        L.hsi_gather_mainkv_layers.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, i32, vp, i64, vp]
         L.hsi_append_token.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, ctypes.c_int, vp]
         L.hsi_mask_scores.argtypes = [vp, i64, vp, vp, i64, i32, i64, vp]
         L.hsi_score_full.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, vp, i64, vp, i64, ctypes.c_int, vp,
@@ -100,7 +102,7 @@ def lib() -> ctypes.CDLL:
                      "hsi_device_error", "hsi_device_check", "hsi_calib_read", "hsi_calib_mma", "hsi_full_layer",
                      "hsi_reindex_layer", "hsi_topk_noalloc", "hsi_debug_set", "hsi_pool_gather",
                      "hsi_quantize_mxfp4", "hsi_quantize_mainkv", "hsi_gather_mainkv", "hsi_append_token",
-                     "hsi_mask_scores", "hsi_prefill_layer"):
+                     "hsi_mask_scores", "hsi_prefill_layer", "hsi_gather_mainkv_layers"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -203,6 +205,14 @@ def gather_mainkv(kv, kv_off, n_visible, idx, k, B, out, ld_idx=None, stream=Non
     ld_idx = idx.shape[-1] if ld_idx is None else ld_idx
     _check("hsi_gather_mainkv", lib().hsi_gather_mainkv(
         _ptr(kv), _ptr(kv_off), _ptr(n_visible), _ptr(idx), ld_idx, k, B, _ptr(out), _stream(stream)))
+
+
+def gather_mainkv_layers(kv, kv_off, n_visible, idx, k, B, out, stream=None):
+    """gather(main_kv, topk) for L layers in one launch: idx [L, B, ld_idx] int32, out [L, B, k, 512] bf16 bits."""
+    L, ld_idx = idx.shape[0], idx.shape[-1]
+    _check("hsi_gather_mainkv_layers", lib().hsi_gather_mainkv_layers(
+        _ptr(kv), _ptr(kv_off), _ptr(n_visible), _ptr(idx), ld_idx, idx.stride(0), L, k, B, _ptr(out),
+        out.stride(0), _stream(stream)))
 
 
 def append_token(k_x, signs, g_k, k_rec, k_rec_off, n_visible, capacity, B, kv_x=None, kv=None, kv_off=None,

@@ -869,15 +869,23 @@ hsi_status hsi_quantize_mainkv(const uint16_t* x, int64_t n, uint8_t* kv, cudaSt
     return launch(mainkv_quant_kernel, dim3((unsigned)((n + 7) / 8)), dim3(256), 0, stream, x, n, kv);
 }
 
-hsi_status hsi_gather_mainkv(const uint8_t* kv, const int64_t* kv_off, const int32_t* n_visible, const int32_t* idx,
-                             int64_t ld_idx, int32_t k, int32_t B, uint16_t* out, cudaStream_t stream) {
-    if (!kv || !kv_off || !n_visible || !idx || !out || B <= 0 || k < 1 || k > 4096 || ld_idx < k)
+hsi_status hsi_gather_mainkv_layers(const uint8_t* kv, const int64_t* kv_off, const int32_t* n_visible,
+                                    const int32_t* idx, int64_t ld_idx, int64_t idx_stride, int32_t L, int32_t k,
+                                    int32_t B, uint16_t* out, int64_t out_stride, cudaStream_t stream) {
+    if (!kv || !kv_off || !n_visible || !idx || !out || B <= 0 || L <= 0 || k < 1 || k > 4096 || ld_idx < k)
+        return HSI_ERR_INVALID_ARG;
+    if (L > 1 && (idx_stride < (int64_t)B * ld_idx || out_stride < (int64_t)B * k * HSI_KV_DIM || out_stride % 8))
         return HSI_ERR_INVALID_ARG;
     if (!aligned(kv, 16) || !aligned(out, 16)) return HSI_ERR_INVALID_ARG;
-    const int64_t warps = ((int64_t)B * k + GATHER_EPW - 1) / GATHER_EPW;
+    const int64_t warps = ((int64_t)L * B * k + GATHER_EPW - 1) / GATHER_EPW;
     if ((warps + 7) / 8 > INT32_MAX) return HSI_ERR_INVALID_ARG;
     return launch(mainkv_gather_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, stream, kv, kv_off,
-                  n_visible, idx, ld_idx, k, B, out);
+                  n_visible, idx, ld_idx, idx_stride, L, k, B, out, out_stride);
+}
+
+hsi_status hsi_gather_mainkv(const uint8_t* kv, const int64_t* kv_off, const int32_t* n_visible, const int32_t* idx,
+                             int64_t ld_idx, int32_t k, int32_t B, uint16_t* out, cudaStream_t stream) {
+    return hsi_gather_mainkv_layers(kv, kv_off, n_visible, idx, ld_idx, 0, 1, k, B, out, 0, stream);
 }
 
 hsi_status hsi_append_token(const uint16_t* k_x, const int8_t* signs, const float* g_k, uint8_t* k_rec,

@@ -87,14 +87,19 @@ __global__ void __launch_bounds__(256) mainkv_quant_kernel(const uint16_t* __res
 #endif
 constexpr int GATHER_EPW = HSI_GATHER_EPW;
 
+// L lists of B x k indices (list l at idx + l idx_stride, its rows written
+// at out + l out_stride) are one flattened list of L B k items, so a step's
+// gathers for several layers run as one launch, one ramp instead of L.
 __global__ void __launch_bounds__(256) mainkv_gather_kernel(const uint8_t* __restrict__ kv,
                                                             const int64_t* __restrict__ kv_off,
                                                             const int32_t* __restrict__ n_vis,
                                                             const int32_t* __restrict__ idx, int64_t ld_idx,
-                                                            int32_t k, int32_t B, uint16_t* __restrict__ out) {
+                                                            int64_t idx_stride, int32_t L, int32_t k, int32_t B,
+                                                            uint16_t* __restrict__ out, int64_t out_stride) {
     griddep_wait();
     griddep_launch_dependents();
-    const int64_t total = (int64_t)B * k;
+    const int64_t per = (int64_t)B * k;
+    const int64_t total = per * L;
     const int64_t base = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * GATHER_EPW;
     if (base >= total) return;
     const int lane = threadIdx.x & 31;
@@ -102,8 +107,9 @@ __global__ void __launch_bounds__(256) mainkv_gather_kernel(const uint8_t* __res
     long long src = -1;
     if (lane < GATHER_EPW && base + lane < total) {
         const int64_t f = base + lane;
-        const int b = (int)(f / k), t = (int)(f % k);
-        const int32_t i = __ldg(idx + (int64_t)b * ld_idx + t);
+        const int64_t l = f / per, r = f % per;
+        const int b = (int)(r / k), t = (int)(r % k);
+        const int32_t i = __ldg(idx + l * idx_stride + (int64_t)b * ld_idx + t);
         const int32_t nv = __ldg(n_vis + b);
         const int64_t o = __ldg(kv_off + b);
         if (i >= 0) {
@@ -140,7 +146,8 @@ __global__ void __launch_bounds__(256) mainkv_gather_kernel(const uint8_t* __res
                 o[q] = *reinterpret_cast<const uint32_t*>(&h);
             }
         }
-        uint4* dst = reinterpret_cast<uint4*>(out + (base + j) * KV_DIM + lane * 16);
+        const int64_t f = base + j;
+        uint4* dst = reinterpret_cast<uint4*>(out + (f / per) * out_stride + (f % per) * KV_DIM + lane * 16);
         __stcs(dst, make_uint4(o[0], o[1], o[2], o[3]));
         __stcs(dst + 1, make_uint4(o[4], o[5], o[6], o[7]));
     }

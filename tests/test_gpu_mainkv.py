@@ -135,3 +135,23 @@ def test_gather_ragged_list_lengths(B, k):
     got = out.cpu().numpy().view(np.uint16)
     for b in range(B):
         assert np.array_equal(got[b], oracle.mainkv_gather(kv_h, n, idx[b, :k])), b
+
+
+@pytest.mark.parametrize("L,B,k", [(5, 3, 7), (2, 1, 1), (3, 4, 513)])
+def test_gather_layers_in_one_launch(L, B, k):
+    """Every layer's list in one launch (hsi_gather_mainkv_layers): each layer's
+    rows equal the oracle's gather of that layer's list, ragged ends included."""
+    n = 1000
+    x = inputs.normal_bf16(70 + k, 85, n * 512).reshape(n, 512)
+    kv_h = oracle.mainkv_quantize(x)
+    kv = _gpu_kv(x)
+    rng = np.random.default_rng(L * 100 + k)
+    lengths = [n - 7 * b for b in range(B)]
+    idx = np.stack([rng.integers(-1, lengths[b], (L, k)) for b in range(B)], 1).astype(np.int32)  # [L][B][k]
+    out = torch.full((L, B, k, 512), 0x5A5A, dtype=torch.int16, device=DEV)
+    hsi.gather_mainkv_layers(kv, i64([0] * B), i32(lengths), torch.from_numpy(idx).to(DEV), k, B, out)
+    assert hsi.device_error() == 0
+    got = out.cpu().numpy().view(np.uint16)
+    for l in range(L):
+        for b in range(B):
+            assert np.array_equal(got[l, b], oracle.mainkv_gather(kv_h, lengths[b], idx[l, b])), (l, b)
