@@ -113,7 +113,7 @@ struct ScoreCfg {
     // thread's issue sequence (waits, descriptors, MMAs, commit) per unit is
     // longer than the tensor work of a 4-query tile
 #ifndef HSI_DECODE_ISSUERS
-#define HSI_DECODE_ISSUERS 1
+#define HSI_DECODE_ISSUERS 2
 #endif
     static constexpr int MMA_ISSUERS = GATHER ? 1 : NQ > 1 ? 2 : HSI_DECODE_ISSUERS;
     static constexpr int MMA_WARP = PROD_WARPS;
