@@ -68,6 +68,10 @@ def parse():
                     help="skip the calibration, the other workloads and the chunked-prefill workload")
     ap.add_argument("--profile", action="store_true", help="cudaProfilerStart/Stop around the timed steps")
     ap.add_argument("--queries", type=int, default=0, help="use only the first N queries (profiling captures)")
+    ap.add_argument("--case", choices=["prefill_score", "prefill_layer", "rowsel", "gather"], default=None,
+                    help="run only one kernel's case, --steps times, and exit (profiling captures): the chunked-"
+                         "prefill scoring phase, the whole prefill layer, the prefill selection phase, or the "
+                         "main-KV gather of five layers' top-512 lists")
     return ap.parse_args()
 
 
@@ -711,10 +715,13 @@ class PrefillWorkload:
     written, then each query's top-512 and pool from the block maxima and the
     candidate blocks' scores."""
 
-    def __init__(self, wl: inputs.Workload, dev, log):
+    def __init__(self, wl: inputs.Workload, dev, log, queries: int = 0):
         import torch
 
         import long_context_decode_lightning_gb300 as hsi
+        if queries:  # the first `queries` queries only (a multiple of 4), for profiling captures
+            wl.query_seq = wl.query_seq[:queries]
+            wl.n_visible = wl.n_visible[:queries]
         self.torch, self.hsi, self.wl = torch, hsi, wl
         signs = wl.signs()
         self.signs = signs
@@ -754,6 +761,42 @@ class PrefillWorkload:
                                self.n, self.scores, K_TOP, self.idx, self.val, group=4, block_ids=self.ids,
                                n_kept=self.nk, n_pool=self.npool, pool_bits=self.bits, n_keep=self.wl.n_keep,
                                ws=self.ws, phases=phases)
+
+
+def run_case(args, dev, log):
+    """One kernel's case for a profiling capture: set up, run it --steps times, check the device status."""
+    import torch
+
+    import long_context_decode_lightning_gb300 as hsi
+    if args.case in ("prefill_score", "prefill_layer", "rowsel"):
+        P = PrefillWorkload(inputs.workload(4), dev, log, queries=args.queries)
+        P.quant()
+        if args.case == "rowsel":
+            P.layer(hsi.PHASE_SCORE)
+        for _ in range(args.steps):
+            if args.case == "prefill_score":
+                P.layer(hsi.PHASE_SCORE)
+            elif args.case == "rowsel":
+                P.layer(hsi.PHASE_SELECT)
+            else:
+                P.quant()
+                P.layer(hsi.PHASE_ALL)
+    else:  # the five layers' gathers of a decode step, random selections, one launch each
+        wl = inputs.workload(2)
+        if args.queries:
+            wl.query_seq = wl.query_seq[: args.queries]
+            wl.n_visible = wl.n_visible[: args.queries]
+        M = MainKV(wl, dev, log)
+        B, L = wl.B, 5
+        g = torch.Generator(device="cpu").manual_seed(1)
+        idx = torch.randint(0, min(wl.n_visible), (L, B, K_TOP), generator=g, dtype=torch.int32).to(dev)
+        nv = torch.tensor(wl.n_visible, dtype=torch.int32, device=dev)
+        out = torch.empty(L, B, K_TOP, hsi.KV_DIM, dtype=torch.int16, device=dev)
+        for _ in range(args.steps):
+            hsi.gather_mainkv_layers(M.kv, M.off, nv, idx, K_TOP, B, out)
+    torch.cuda.synchronize()
+    assert hsi.device_error() == 0, f"device error in case {args.case}"
+    log(f"case {args.case}: {args.steps} runs ok")
 
 
 def prefill_config(dev, args, log, peaks, calib, clk_mhz, n_sm):
@@ -901,6 +944,9 @@ def main():
     if world > 1:
         dist.barrier()
     hsi.device_check()
+    if args.case:
+        run_case(args, dev, log)
+        return
     fmt = hsi.FMT_MXFP4 if args.format == "mxfp4" else hsi.FMT_NVFP4
     W = DeviceWorkload(wl, dev, log, fmt=fmt)
     l0 = hsi.kernel_launches()
