@@ -68,7 +68,7 @@ def parse():
                     help="skip the calibration, the other workloads and the chunked-prefill workload")
     ap.add_argument("--profile", action="store_true", help="cudaProfilerStart/Stop around the timed steps")
     ap.add_argument("--queries", type=int, default=0, help="use only the first N queries (profiling captures)")
-    ap.add_argument("--case", choices=["prefill_score", "prefill_layer", "rowsel", "gather"], default=None,
+    ap.add_argument("--case", choices=["prefill_score", "prefill_layer", "rowsel", "gather", "reindex", "reindex_gather", "pool"], default=None,
                     help="run only one kernel's case, --steps times, and exit (profiling captures): the chunked-"
                          "prefill scoring phase, the whole prefill layer, the prefill selection phase, or the "
                          "main-KV gather of five layers' top-512 lists")
@@ -781,6 +781,25 @@ def run_case(args, dev, log):
             else:
                 P.quant()
                 P.layer(hsi.PHASE_ALL)
+    elif args.case in ("reindex", "reindex_gather", "pool"):
+        # the decode step's Reindex layer (streaming the compacted pool, or gathering
+        # it), or the pool selection, on the resident state one step left behind
+        wl = inputs.workload(2)
+        if args.queries:
+            wl.query_seq = wl.query_seq[: args.queries]
+            wl.n_visible = wl.n_visible[: args.queries]
+        W = DeviceWorkload(wl, dev, log)
+        W.step()
+        l = wl.full_layers
+        for _ in range(args.steps):
+            if args.case == "pool":
+                hsi.full_layer(W.q_rec[0], W.g_q[0], W.w[0], W.k_rec[0], W.g_k[0], W.k_off, W.n_vis, W.B, W.maxv,
+                               W.scores, K_TOP, W.idx[0], W.val[0], block_ids=W.ids, n_kept=W.nk, n_pool=W.npool,
+                               pool_bits=W.bits, n_keep=wl.n_keep, ws=W.ws_full, phases=hsi.PHASE_POOL)
+            else:
+                hsi.reindex_layer(W.q_rec[l], W.g_q[l], W.w[l], W.k_rec[0], W.g_k[0], W.k_off, W.n_vis, W.ids,
+                                  W.nk, W.npool, W.B, W.pool_scores, K_TOP, W.idx[l], W.val[l], n_keep=wl.n_keep,
+                                  ws=W.ws_rtopk, pool_rec=W.pool_rec, pool_rec_ready=args.case == "reindex")
     else:  # the five layers' gathers of a decode step, random selections, one launch each
         wl = inputs.workload(2)
         if args.queries:

@@ -66,6 +66,18 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
     }
 }
 
+// Bounded wait that ignores the abort flag (teardown: drain what is in flight).
+__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    const uint64_t limit = *(volatile unsigned long long*)&g_hsi_wait_limit_ns;
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > limit) {
+            raise_error(DEVERR_TIMEOUT);
+            return;
+        }
+    }
+}
+
 // Order-preserving map of an fp32 score to a uint32 key (larger score ->
 // larger key); -0 maps like +0. Scores must not be NaN.
 __device__ __forceinline__ uint32_t order_key(float f) {

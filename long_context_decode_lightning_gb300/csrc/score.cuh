@@ -273,18 +273,6 @@ __device__ __forceinline__ bool wait_one(uint64_t* bar, uint32_t parity, ScoreSh
 #endif
 }
 
-// Bounded wait that ignores the abort flag (teardown: drain what is in flight).
-__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
-    const uint64_t t0 = globaltimer_ns();
-    const uint64_t limit = *(volatile unsigned long long*)&g_hsi_wait_limit_ns;
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > limit) {
-            raise_error(DEVERR_TIMEOUT);
-            return;
-        }
-    }
-}
-
 // n_vis[b] within [0, max_vis] (the bound that sized the score rows and the
 // caches); `report`: record a larger value as a device-side argument error.
 __device__ __forceinline__ int vis_of(const ScoreParams& p, int b, bool report = false) {

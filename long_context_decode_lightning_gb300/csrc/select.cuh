@@ -28,6 +28,7 @@ constexpr int SEL_WARPS = SEL_THREADS / 32;
 constexpr int SEL_CAP = 16384;      // items held in shared memory by one CTA
 constexpr int SEL_MAXK = 4096;      // largest k (top-k) or n_keep (pool)
 constexpr int HIST_BINS = 4096;     // top 12 bits of the key
+constexpr int SEL_B2 = 2048;        // second-level bins of the kept keys (select_small_hist)
 constexpr int SCAN_THREADS = 512;
 #ifndef HSI_SCAN_CHUNK
 #define HSI_SCAN_CHUNK 8192
@@ -427,9 +428,11 @@ struct SelSmem {
     uint32_t whist[SEL_WARPS][256];
     uint32_t hsum[256];
     unsigned long long win[SEL_MAXK];
+    uint64_t bar;  // completion of the bulk copies of a row (select_small_hist)
+    int abort;
     uint32_t bcast[8];
-    uint32_t keys[SEL_CAP];
-    uint32_t idx[SEL_CAP];
+    alignas(16) uint32_t keys[SEL_CAP];
+    alignas(16) uint32_t idx[SEL_CAP];
 #ifdef HSI_TRACE
     long long t_last;
 #endif
@@ -944,65 +947,87 @@ __device__ int block_select(const Src& src, SelSmem& s, int k, int64_t id_range)
     return select_finish(packed, s, k, id_range, false, prefix, mask, shift, above);
 }
 
-// Top-k of a row of n <= SEL_CAP items (TOPK mode) whose 4096-bin histogram
-// of the keys' top 12 bits is at hist (complete: every item counted). The bin
-// holding the k-th key comes from the histogram; only the items at or above
-// it are loaded, and the radix passes resolve the remaining 20 bits. Returns
-// -1 when the row holds fewer than k items (then every item wins).
-__device__ int select_small_hist(const SelParams& p, int b, int64_t n, const uint32_t* hist, SelSmem& s) {
-    static_assert(HIST_BINS == 4 * SEL_THREADS, "four bins per thread");
-    const int t = threadIdx.x;
-    uint32_t c[4], sum = 0;
+// The dynamic shared memory of the selection kernels, reached from any
+// function through the shared-memory symbol itself (so that every access is a
+// shared-memory access, also in functions that are not inlined).
+__device__ __forceinline__ SelSmem& sel_smem() {
+    extern __shared__ __align__(16) unsigned char sel_smem_raw[];
+    return *reinterpret_cast<SelSmem*>(sel_smem_raw);
+}
+
+// The k best of a row of n <= SEL_CAP items (either mode): every item loaded
+// into shared memory, then the block select. Returns the winners' count.
+__device__ __noinline__ int select_row_smem(const SelParams& p, int b, int64_t n, int64_t id_range) {
+    SelSmem& s = sel_smem();
+    constexpr int PER = SEL_CAP / SEL_THREADS;
+    const float* row = p.src + (int64_t)b * p.ld;
+    float v[PER];
+    uint32_t key[PER];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        c[i] = hist[4 * t + i];
-        sum += c[i];
+    for (int i = 0; i < PER; ++i) {  // clamped index: every load issued unconditionally
+        const int64_t j = (int64_t)i * SEL_THREADS + threadIdx.x;
+        v[i] = n > 0 ? row[j < n ? j : n - 1] : 0.f;
     }
-    uint32_t total;
-    const uint32_t below = block_excl_scan(sum, s, &total);  // items in bins under this thread's
-    const uint32_t k = (uint32_t)p.k;
-    if (total < k) return -1;
-    const uint32_t above_t = total - below - sum;  // items in bins over this thread's
-    if (above_t < k && above_t + sum >= k) {
-        uint32_t run = above_t;
-        for (int i = 3; i >= 0; --i) {
-            if (run + c[i] >= k) {
-                s.bcast[0] = (uint32_t)(4 * t + i);
-                s.bcast[1] = run;
-                break;
-            }
-            run += c[i];
+    __syncthreads();  // the caller's reads of shared memory are done
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int64_t j = (int64_t)i * SEL_THREADS + threadIdx.x;
+        bool ok;
+        key[i] = sel_key_of(p, v[i], j, n, ok);
+        if (!ok || j >= n) key[i] = 0u;  // key 0 is never a real key (it is a NaN pattern)
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int64_t j = (int64_t)i * SEL_THREADS + threadIdx.x;
+        if (j < n) {
+            s.keys[j] = key[i];
+            s.idx[j] = (uint32_t)j;
         }
     }
-    if (t == 0) s.bcast[6] = 0;
     __syncthreads();
+    struct Filt : SmemSrc {
+        __device__ uint32_t key(int64_t j, bool& ok) const {
+            ok = keys[j] != 0u;
+            return keys[j];
+        }
+    };
+    Filt src;
+    src.keys = s.keys;
+    src.ids = s.idx;
+    src.n = n;
     SEL_MARK(s, 24);
+    return block_select<true>(src, s, p.k, id_range);
+}
+
+// The radix route of select_small (TOPK mode, n <= SEL_CAP items, T = the bin
+// of the k-th key and `above` = the items in higher bins in s.bcast[0..1]):
+// the items of bins >= T packed into s.keys / s.idx, then radix passes over
+// the remaining 20 key bits. `in_smem`: the row is in s.keys.
+__device__ __noinline__ int select_small_radix(const SelParams& p, int b, int64_t n, bool in_smem) {
+    SelSmem& s = sel_smem();
+    const int t = threadIdx.x;
     const uint32_t T = s.bcast[0], above = s.bcast[1];
-    // every load first (independent, in flight together), then the appends
     constexpr int PER = SEL_CAP / SEL_THREADS;
+    const float* row = in_smem ? reinterpret_cast<const float*>(s.keys) : p.src + (int64_t)b * p.ld;
     uint32_t key[PER];
     bool keep[PER];
-    const float* row = p.src + (int64_t)b * p.ld;
     float v[PER];
 #pragma unroll
     for (int i = 0; i < PER; ++i) {  // clamped index: every load issued unconditionally
         const int64_t j = (int64_t)i * SEL_THREADS + t;
         v[i] = row[j < n ? j : n - 1];
     }
+    uint32_t mine = 0;
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
         const int64_t j = (int64_t)i * SEL_THREADS + t;
         bool ok;
         key[i] = sel_key_of(p, v[i], j, n, ok);
-        keep[i] = ok && j < n;
-    }
-    // places by a block scan of the per-thread counts (no shared counter)
-    uint32_t mine = 0;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        keep[i] = keep[i] && (key[i] >> 20) >= T;
+        keep[i] = ok && j < n && (key[i] >> 20) >= T;
         mine += keep[i] ? 1u : 0u;
     }
+    // places by a block scan of the per-thread counts (its barriers also end
+    // every read of the row in shared memory)
     uint32_t kept;
     uint32_t pos = block_excl_scan(mine, s, &kept);
     SEL_MARK(s, 25);
@@ -1020,6 +1045,232 @@ __device__ int select_small_hist(const SelParams& p, int b, int64_t n, const uin
     return select_finish(packed, s, p.k, 0, false, T << 20, 0xFFF00000u, 12, above);
 }
 
+enum : int { SMALL_WHOLE_ROW = -1, SMALL_RADIX = -2 };
+
+// Top-k of a row of n <= SEL_CAP items (TOPK mode) whose 4096-bin histogram
+// of the keys' top 12 bits is at hist (complete: every item counted). The bin
+// T holding the k-th key comes from the histogram; only the items at or above
+// it are kept. Returns the number of winners placed in s.win in order, or
+// SMALL_WHOLE_ROW (the row holds fewer than k items) or SMALL_RADIX (the kept
+// items are many or heavily tied: T and the items above bin T are left in
+// s.bcast[0..1] for select_small_radix).
+//
+// When the row (and its block ids) start on 16-byte boundaries they come into
+// shared memory by bulk copies, issued first so that they land while the
+// histogram is scanned (*in_smem then says that s.keys holds the row, and
+// *ids_in_smem that s.idx holds the block ids for the output). When the kept
+// items are few (at most one per thread), they are ordered without radix
+// passes or a sort: compared as floats against bin T's least value, they go
+// into one list; a second histogram of SEL_B2 bins spans the kept keys' range
+// (from bin T's least key to the largest key), its scan gives every bin's
+// first rank (the items in the bins above it), each item goes to a slot of
+// its bin's range, and its rank within the bin is the number of the bin's
+// items that beat it. More than 64 items in one second-level bin (heavy ties)
+// take the radix route instead.
+__device__ __forceinline__ int select_small_fast(const SelParams& p, int b, int64_t n, const uint32_t* hist,
+                                                 SelSmem& s, bool* in_smem, bool* ids_in_smem) {
+    static_assert(HIST_BINS == 4 * SEL_THREADS, "four bins per thread");
+    static_assert(3 * SEL_B2 + SEL_WARPS <= SEL_WARPS * 256, "second-level bins, offsets and counters fit in s.whist");
+    static_assert(SEL_B2 == 2 * SEL_THREADS && SEL_MAXK - 2 * SEL_THREADS >= 2048,
+                  "two bins per thread; the candidate lists past the k <= 2048 winners");
+    static_assert(SEL_CAP == 16 * SEL_THREADS, "four float4 of the row per thread");
+    const int t = threadIdx.x;
+    const float* row = p.src + (int64_t)b * p.ld;
+    const int64_t nb = p.block_ids ? (n + p.block_size - 1) / p.block_size : 0;
+    const bool bulk = n > 0 && ((reinterpret_cast<uintptr_t>(p.src) & 15) | (p.ld & 3)) == 0;
+    const bool bulk_ids = bulk && nb > 0 && ((reinterpret_cast<uintptr_t>(p.block_ids) & 15) | (p.ld_blocks & 3)) == 0 &&
+                          nb <= p.ld_blocks && ((nb + 3) & ~3ll) <= SEL_CAP;
+    *in_smem = bulk;
+    *ids_in_smem = false;
+    if (t == 0) {
+        s.abort = 0;
+        s.bcast[6] = 0;
+        if (bulk) {
+            const uint32_t bytes = (uint32_t)(((n + 3) & ~3ll) * 4);  // within the row: ld is a multiple of 4
+            const uint32_t id_bytes = bulk_ids ? (uint32_t)(((nb + 3) & ~3ll) * 4) : 0u;
+            mbar_init(&s.bar, 1);
+            fence_mbar_init();
+            mbar_arrive_expect_tx(&s.bar, bytes + id_bytes);
+            for (uint32_t o = 0; o < bytes; o += 16384u)
+                bulk_g2s(reinterpret_cast<uint8_t*>(s.keys) + o, reinterpret_cast<const uint8_t*>(row) + o,
+                         min(16384u, bytes - o), &s.bar);
+            if (id_bytes) bulk_g2s(s.idx, p.block_ids + (int64_t)b * p.ld_blocks, id_bytes, &s.bar);
+        }
+    }
+    uint32_t c[4], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        c[i] = hist[4 * t + i];
+        sum += c[i];
+    }
+    uint32_t total;
+    const uint32_t below = block_excl_scan(sum, s, &total);  // items in bins under this thread's
+    const uint32_t k = (uint32_t)p.k;
+    SEL_MARK(s, 28);
+    const uint32_t above_t = total - below - sum;  // items in bins over this thread's
+    if (total >= k && above_t < k && above_t + sum >= k) {
+        uint32_t run = above_t;
+        for (int i = 3; i >= 0; --i) {
+            if (run + c[i] >= k) {
+                s.bcast[0] = (uint32_t)(4 * t + i);
+                s.bcast[1] = run;
+                s.bcast[2] = c[i];
+                break;
+            }
+            run += c[i];
+        }
+    }
+    // the row has landed (every thread waits; a wait that runs out aborts all)
+    const bool ok = !bulk || wait_bounded(&s.bar, 0, &s.abort);
+    if (!__syncthreads_and(ok)) {
+        if (t == 0) wait_drain(&s.bar, 0);  // nothing may still be writing shared memory at exit
+        __syncthreads();
+        *in_smem = false;
+        return 0;
+    }
+    SEL_MARK(s, 24);
+    if (total < k) return SMALL_WHOLE_ROW;
+    const uint32_t T = s.bcast[0], above = s.bcast[1], at_T = s.bcast[2];
+    const uint32_t kept_all = above + at_T;
+    if (!bulk || kept_all > (uint32_t)SEL_THREADS) return SMALL_RADIX;
+
+    uint32_t* h2 = &s.whist[0][0];  // second-level bins of the kept keys
+    uint32_t* start2 = h2 + SEL_B2;
+    uint32_t* fill2 = start2 + SEL_B2;
+    uint32_t* wmax = fill2 + SEL_B2;                                  // [SEL_WARPS]
+    unsigned long long* clist = s.win + (SEL_MAXK - 2 * SEL_THREADS);  // the kept items, in no order
+    unsigned long long* cand = s.win + (SEL_MAXK - SEL_THREADS);       // the kept items, grouped by bin
+    const int lane = t & 31, warp = t >> 5;
+    const uint32_t base = T << 20;
+    const float fT = key_to_float(base);  // the least value whose key lies in bin T or above
+    // the kept items into one list: item j = 4 (i SEL_THREADS + t) + e, a ballot
+    // per item slot, one reservation per warp
+    float4 q[4];
+    const float4* r4 = reinterpret_cast<const float4*>(s.keys);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = r4[i * SEL_THREADS + t];
+    uint32_t bal[16], nw = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t j0 = 4 * ((int64_t)i * SEL_THREADS + t);
+        const float e4[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            bal[4 * i + e] = __ballot_sync(0xFFFFFFFFu, j0 + e < n && e4[e] >= fT);
+            nw += (uint32_t)__popc(bal[4 * i + e]);
+        }
+    }
+    uint32_t wpos = 0;
+    if (lane == 0 && nw) wpos = atomicAdd(&s.bcast[6], nw);
+    wpos = __shfl_sync(0xFFFFFFFFu, wpos, 0);
+    const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t j0 = 4u * (uint32_t)(i * SEL_THREADS + t);
+        const float e4[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t m = bal[4 * i + e];
+            if ((m >> lane) & 1u) {
+                const uint32_t pos = wpos + (uint32_t)__popc(m & lt);
+                if (pos < (uint32_t)SEL_THREADS)
+                    clist[pos] = ((unsigned long long)order_key(e4[e]) << 32) | (uint32_t)~(j0 + (uint32_t)e);
+            }
+            wpos += (uint32_t)__popc(m);
+        }
+    }
+    h2[2 * t] = 0u;
+    h2[2 * t + 1] = 0u;
+    __syncthreads();
+    SEL_MARK(s, 27);
+    const uint32_t cnt = s.bcast[6];
+    if (cnt != kept_all) return SMALL_RADIX;  // the histogram does not describe the row (uniform)
+    // SEL_B2 bins over [T << 20, largest kept key], fine enough that few items share one
+    const bool mine = t < (int)cnt;
+    const unsigned long long me = mine ? clist[t] : 0ull;
+    const uint32_t key = (uint32_t)(me >> 32);
+    const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, mine ? key : 0u);
+    if (lane == 0) wmax[warp] = mx;
+    __syncthreads();
+    const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, wmax[lane]);
+    const uint32_t range = top - base;
+    const int sh2 = range >= (uint32_t)SEL_B2 ? 32 - __clz((int)(range / SEL_B2)) : 0;  // range >> sh2 < SEL_B2
+    const uint32_t x = mine ? (key - base) >> sh2 : 0u;
+    if (mine) atomicAdd(&h2[x], 1u);
+    __syncthreads();
+    const uint32_t c0 = h2[2 * t], c1 = h2[2 * t + 1];
+    uint32_t tot2;
+    const uint32_t below2 = block_excl_scan(c0 + c1, s, &tot2);  // items in bins under 2t
+    start2[2 * t] = tot2 - below2 - c0;  // items in the bins above
+    start2[2 * t + 1] = tot2 - below2 - c0 - c1;
+    fill2[2 * t] = 0u;
+    fill2[2 * t + 1] = 0u;
+    const uint32_t wc = __reduce_max_sync(0xFFFFFFFFu, max(c0, c1));
+    if (lane == 0) wmax[warp] = wc;
+    __syncthreads();
+    SEL_MARK(s, 26);
+    if (__reduce_max_sync(0xFFFFFFFFu, wmax[lane]) > 64u) {  // heavy ties (uniform)
+        __syncthreads();  // every read of the bins is done before the radix passes reuse them
+        return SMALL_RADIX;
+    }
+    if (mine) cand[start2[x] + atomicAdd(&fill2[x], 1u)] = me;
+    __syncthreads();
+    SEL_MARK(s, 25);
+    if (mine) {  // rank: the items of the bins above, then those of its own bin that beat it
+        const uint32_t lo = start2[x], hi = lo + fill2[x];
+        uint32_t r = lo;
+        for (uint32_t i = lo; i < hi; ++i) r += cand[i] > me ? 1u : 0u;
+        if (r < k) s.win[r] = me;
+    }
+    __syncthreads();
+    SEL_MARK(s, 30);
+    *ids_in_smem = bulk_ids;
+    return (int)k;
+}
+
+// Top-k outputs of query b from the `count` winners in s.win (key << 32 |
+// ~local index), padded with -1 / -inf; local indices mapped through the block
+// ids when given (from s.idx when ids_in_smem).
+__device__ __forceinline__ void write_topk(const SelParams& p, int b, int count, const SelSmem& s, bool ids_in_smem) {
+    int32_t* oi = p.out_idx + (int64_t)b * p.k;
+    float* ov = p.out_val + (int64_t)b * p.k;
+    for (int t = threadIdx.x; t < p.k; t += SEL_THREADS) {
+        if (t < count) {
+            const unsigned long long w = s.win[t];
+            int64_t i = (int64_t)(uint32_t)~(uint32_t)(w & 0xFFFFFFFFull);
+            if (p.block_ids) {
+                const int64_t blk = ids_in_smem ? (int64_t)(int32_t)s.idx[i / p.block_size]
+                                                : p.block_ids[(int64_t)b * p.ld_blocks + i / p.block_size];
+                i = blk * p.block_size + i % p.block_size;
+            }
+            oi[t] = (int32_t)i;
+            ov[t] = key_to_float((uint32_t)(w >> 32));
+        } else {
+            oi[t] = -1;
+            ov[t] = __uint_as_float(0xFF800000u);
+        }
+    }
+}
+
+// Top-k of rows of at most SEL_CAP items whose histograms are complete
+// (hist_small, TOPK mode): the Reindex layers' selection inside the pool.
+__global__ void __launch_bounds__(SEL_THREADS, 1) sel_small_kernel(SelParams p) {
+    griddep_wait();
+    griddep_launch_dependents();
+    SelSmem& s = sel_smem();
+    const int b = blockIdx.x;
+    const int64_t n = sel_items(p, b);
+#ifdef HSI_TRACE
+    if (threadIdx.x == 0) s.t_last = clock64();
+#endif
+    bool in_smem = false, ids_in_smem = false;
+    int count = select_small_fast(p, b, n, p.hist + (int64_t)b * HIST_BINS, s, &in_smem, &ids_in_smem);
+    if (count == SMALL_RADIX) count = select_small_radix(p, b, n, in_smem);
+    else if (count == SMALL_WHOLE_ROW) count = select_row_smem(p, b, n, 0);
+    write_topk(p, b, count, s, ids_in_smem);
+    SEL_MARK(s, 31);
+}
+
 __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) {
     griddep_wait();
     griddep_launch_dependents();
@@ -1032,48 +1283,8 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) 
 #ifdef HSI_TRACE
     if (threadIdx.x == 0) s.t_last = clock64();
 #endif
-    count = -1;
-    if (n <= SEL_CAP && p.hist_small) count = select_small_hist(p, b, n, p.hist + (int64_t)b * HIST_BINS, s);
-    if (count >= 0) {
-        // selected from the histogram
-    } else if (n <= SEL_CAP) {
-        constexpr int PER = SEL_CAP / SEL_THREADS;
-        const float* row = p.src + (int64_t)b * p.ld;
-        float v[PER];
-        uint32_t key[PER];
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {  // clamped index: every load issued unconditionally
-            const int64_t j = (int64_t)i * SEL_THREADS + threadIdx.x;
-            v[i] = n > 0 ? row[j < n ? j : n - 1] : 0.f;
-        }
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int64_t j = (int64_t)i * SEL_THREADS + threadIdx.x;
-            bool ok;
-            key[i] = sel_key_of(p, v[i], j, n, ok);
-            if (!ok || j >= n) key[i] = 0u;  // key 0 is never a real key (it is a NaN pattern)
-        }
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int64_t j = (int64_t)i * SEL_THREADS + threadIdx.x;
-            if (j < n) {
-                s.keys[j] = key[i];
-                s.idx[j] = (uint32_t)j;
-            }
-        }
-        __syncthreads();
-        struct Filt : SmemSrc {
-            __device__ uint32_t key(int64_t j, bool& ok) const {
-                ok = keys[j] != 0u;
-                return keys[j];
-            }
-        };
-        Filt src;
-        src.keys = s.keys;
-        src.ids = s.idx;
-        src.n = n;
-        SEL_MARK(s, 24);
-        count = block_select<true>(src, s, p.k, id_range);
+    if (n <= SEL_CAP) {
+        count = select_row_smem(p, b, n, id_range);
     } else {
         const uint32_t c = p.cand_cnt[b];
         const uint32_t* ck = p.cand_key + (int64_t)b * p.cap;
@@ -1095,23 +1306,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) 
         }
     }
     if (p.mode == SEL_TOPK) {
-        int32_t* oi = p.out_idx + (int64_t)b * p.k;
-        float* ov = p.out_val + (int64_t)b * p.k;
-        for (int t = threadIdx.x; t < p.k; t += SEL_THREADS) {
-            if (t < count) {
-                const unsigned long long w = s.win[t];
-                int64_t i = (int64_t)(uint32_t)~(uint32_t)(w & 0xFFFFFFFFull);
-                if (p.block_ids) {
-                    const int64_t blk = p.block_ids[(int64_t)b * p.ld_blocks + i / p.block_size];
-                    i = blk * p.block_size + i % p.block_size;
-                }
-                oi[t] = (int32_t)i;
-                ov[t] = key_to_float((uint32_t)(w >> 32));
-            } else {
-                oi[t] = -1;
-                ov[t] = __uint_as_float(0xFF800000u);
-            }
-        }
+        write_topk(p, b, count, s, false);
     } else {
         // pool: ascending block ids, the visible-position count and the bit table
         const int bs = p.div;

@@ -448,6 +448,68 @@ def test_full_and_reindex_layer_match_separate_calls(lengths):
     assert torch.equal(ri_g, ri_sep) and torch.equal(rv_g, rv_sep)
 
 
+def _caches_from_rows(wl, rows_per_cache):
+    """K caches built from given bf16 rows (one array [n][128] per cache)."""
+    parts, gs, offs, off = [], [], [], 0
+    for kb in rows_per_cache:
+        rec, g = gpu_quantize(kb, 1, kb.shape[0], wl.signs())
+        parts.append(rec)
+        gs.append(g)
+        offs.append(off)
+        off += hsi.n_records(kb.shape[0])
+    return torch.cat(parts), torch.cat(gs), offs
+
+
+@pytest.mark.parametrize("case", ["repeated_keys", "one_key", "three_keys", "unaligned_rows"])
+def test_reindex_layer_selection_paths(case):
+    """The Reindex layer's selection takes the k-th key's bin from the
+    histogram its scoring kernel fills, then orders few kept items by their
+    bins' ranks, many (heavy ties) by radix passes, and reads rows that are
+    not 16-byte aligned with plain loads. Every route gives what the general
+    top-k (hsi_topk) gives on the same pooled scores, and the oracle's top-k."""
+    wl = inputs.workload(1)
+    lengths = [40000, 20000, 16390]
+    B = len(lengths)
+    rng = np.random.default_rng(11)
+    base = [wl.k_bf16(0, b, rows=n) for b, n in enumerate(lengths)]
+    if case == "repeated_keys":  # exact score ties spread over the whole range
+        rows = [kb[rng.integers(0, 3000, kb.shape[0])] for kb in base]
+    elif case == "one_key":  # every score of a query equal
+        rows = [np.repeat(kb[:1], kb.shape[0], axis=0) for kb in base]
+    elif case == "three_keys":
+        rows = [kb[rng.integers(0, 3, kb.shape[0])] for kb in base]
+    else:
+        rows = base
+    k_rec, gk, offs = _caches_from_rows(wl, rows)
+    q_rec, g_q, w = gpu_queries(wl, 0, range(B))
+    nv, off = i32(lengths), i64(offs)
+    maxv = max(lengths)
+    s_f = torch.empty(B, maxv, device=DEV)
+    i_f, v_f = torch.empty(B, 512, dtype=torch.int32, device=DEV), torch.empty(B, 512, device=DEV)
+    ids = torch.empty(B, 2048, dtype=torch.int32, device=DEV)
+    nk, npl = torch.empty(B, dtype=torch.int32, device=DEV), torch.empty(B, dtype=torch.int32, device=DEV)
+    hsi.full_layer(q_rec, g_q, w, k_rec, gk, off, nv, B, maxv, s_f, 512, i_f, v_f, block_ids=ids, n_kept=nk,
+                   n_pool=npl)
+    q1, g1, w1 = gpu_queries(wl, 1, range(B))
+    ld = 2048 * 8 + (1 if case == "unaligned_rows" else 0)
+    ps_sep = torch.empty(B, ld, device=DEV)[:, :2048 * 8]
+    hsi.score_pool(q1, g1, w1, k_rec, gk, off, nv, ids, nk, 2048, B, ps_sep, ld=ld)
+    ri_sep, rv_sep = torch.empty(B, 512, dtype=torch.int32, device=DEV), torch.empty(B, 512, device=DEV)
+    hsi.topk(ps_sep, npl, B, 2048 * 8, 512, ri_sep, rv_sep, block_ids=ids, ld=ld)
+    pool_rec = torch.empty(B, 2048 * 576, dtype=torch.uint8, device=DEV)
+    for ready in (False, True):  # gathering (leaves the compacted pool), then streaming it
+        ps = torch.empty(B, ld, device=DEV)[:, :2048 * 8]
+        ri, rv = torch.full((B, 512), 7, dtype=torch.int32, device=DEV), torch.full((B, 512), 7.0, device=DEV)
+        hsi.reindex_layer(q1, g1, w1, k_rec, gk, off, nv, ids, nk, npl, B, ps, 512, ri, rv, ld=ld,
+                          pool_rec=pool_rec, pool_rec_ready=ready)
+        assert hsi.device_error() == 0
+        assert torch.equal(ri, ri_sep) and torch.equal(rv, rv_sep), (case, ready)
+    sg, idn, nkh, nph = ps_sep.cpu().numpy(), ids.cpu().numpy(), nk.cpu().numpy(), npl.cpu().numpy()
+    for b in range(B):
+        oi, ov = oracle.topk_pool(sg[b], int(nph[b]), idn[b], 512)
+        assert np.array_equal(ri_sep.cpu().numpy()[b], oi), (case, b)
+
+
 # ------------------------------------------------------- grouped (prefill) --
 
 @pytest.mark.parametrize("n_cache,n_vis", [(3000, [2990, 2991, 2992, 3000, 5, 6, 7, 8]),
