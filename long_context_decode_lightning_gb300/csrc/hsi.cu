@@ -376,10 +376,10 @@ size_t hsi_workspace_size(hsi_ws_kind kind, int32_t B, int64_t max_n, int32_t k)
         case HSI_WS_QUANTIZE: return align_up((size_t)B * 4, 256);
         case HSI_WS_SCORE: return 0;
         case HSI_WS_TOPK: return sel_ws_bytes(B, max_n, false, 0);
-        case HSI_WS_FULL_LAYER: {  // the top-k's and the pool's selection buffers, the block maxima
+        case HSI_WS_FULL_LAYER: {  // the top-k's and the pool's selection buffers, the block maxima (rows padded to 16 bytes)
             const int64_t nb = (max_n + 7) / 8;
             return sel_ws_bytes(B, max_n, false, 0) + sel_ws_bytes(B, nb, false, 0) +
-                   align_up((size_t)B * (size_t)nb * 4, 256);
+                   align_up((size_t)B * align_up((size_t)nb, 4) * 4, 256);
         }
         case HSI_WS_PREFILL_LAYER:  // the block maxima, rows padded to 16 bytes
             return align_up((size_t)B * align_up((size_t)((max_n + 7) / 8), 4) * 4, 256);
@@ -694,6 +694,7 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     if (phases == HSI_PHASE_POOL && !pool) return HSI_ERR_INVALID_ARG;
     if (pool_bits && ld_bits < (max_visible + 31) / 32) return HSI_ERR_INVALID_ARG;
     const int64_t nb = (max_visible + 7) / 8;
+    const int64_t ldb = (nb + 3) & ~(int64_t)3;  // rows of block maxima start on 16-byte boundaries
     const size_t need = hsi_workspace_size(HSI_WS_FULL_LAYER, B, max_visible, k);
     if (!ws || ws_bytes < need || !aligned(ws, 256)) return HSI_ERR_WORKSPACE;
     // workspace: the top-k's selection buffers, the pool's (separate, so that the
@@ -704,7 +705,11 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     float* bmax = reinterpret_cast<float*>(wpool + sel_ws_bytes(B, nb, false, 0));
     const bool big_topk = max_visible > SEL_CAP;
     if (phases & 1) {
+    // the pool's threshold comes from a histogram of the block maxima the scan
+    // fills, like the top-k's from the scores' (rows past SEL_CAP blocks)
+    const bool bmax_hist = pool && nb > SEL_CAP;
     if (big_topk && zero_async(wsp.hist, (size_t)B * HIST_BINS * 4, stream) != HSI_OK) return HSI_ERR_CUDA;
+    if (bmax_hist && zero_async(wpp.hist, (size_t)B * HIST_BINS * 4, stream) != HSI_OK) return HSI_ERR_CUDA;
     ScoreParams p{};
     p.q_rec = q_rec;
     p.g_q = g_q;
@@ -721,8 +726,9 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     // block maxima: for the pool, and for the top-k's collect pass (it reads the
     // scores of the blocks whose maximum reaches the threshold bin only)
     p.bmax = pool || big_topk ? bmax : nullptr;
-    p.ldb = nb;
+    p.ldb = ldb;
     p.key_hist = big_topk ? wsp.hist : nullptr;
+    p.bmax_hist = bmax_hist ? wpp.hist : nullptr;
     st = launch_score<1, false, kDecodeStages, kDecodeUT>(p, format, stream);
     if (st != HSI_OK) return st;
     }
@@ -748,7 +754,7 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     sp.out_val = top_val;
     if (big_topk) {
         sp.blk_max = bmax;
-        sp.ld_bmax = nb;
+        sp.ld_bmax = ldb;
     }
     st = run_select(sp, max_visible, stream, true);
     if (st != HSI_OK) return st;
@@ -756,7 +762,7 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     if (!do_pool) return HSI_OK;
     SelParams pp{};
     pp.src = bmax;
-    pp.ld = nb;
+    pp.ld = ldb;
     pp.n_src = n_visible;
     pp.max_src = max_visible;
     pp.div = 8;
@@ -774,10 +780,11 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     pp.n_pool = n_pool;
     pp.bits = pool_bits;
     pp.ld_bits = ld_bits;
-    // the block-max histogram is a separate pass over the block maxima (an
-    // eighth of the scores): counting it in the scoring epilogue, where the
-    // maxima of a warp land in one or two bins, cost more than this pass
-    return run_select(pp, nb, stream, false);
+    // rows past SEL_CAP blocks: the histogram of the block maxima comes from the
+    // scoring phase (its pinned block counted at its own maximum, one bin too
+    // low at most: the threshold bin can only drop, the candidates still hold
+    // the pool); shorter rows are selected in shared memory whole
+    return run_select(pp, nb, stream, nb > SEL_CAP);
 }
 
 hsi_status hsi_prefill_layer(const uint8_t* q_rec, const float* g_q, const float* w, const uint8_t* k_rec,

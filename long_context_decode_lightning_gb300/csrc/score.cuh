@@ -84,6 +84,9 @@ struct ScoreParams {
     // optional (single-query groups): 4096-bin histogram of the top 12 bits of
     // the order keys of the scores, [B][4096], added to
     uint32_t* key_hist;
+    // optional (single-query groups, with bmax): the same histogram of the
+    // block maxima, [B][4096], added to
+    uint32_t* bmax_hist;
     // pool gather
     const int32_t* block_ids;
     const int32_t* n_kept;
@@ -141,10 +144,11 @@ struct ScoreCfg {
     static constexpr int OFF_QSLOTS = STAGES * STAGE_BYTES;
     static constexpr int OFF_IDS = OFF_QSLOTS + 2 * QSLOT_BYTES;
     static constexpr int IDS_BYTES = GATHER ? IDS_AHEAD * UNIT_RECS * 4 : 0;
-    // histogram slots for the first HIST_SLOTS queries of the CTA's range
+    // histogram slots for the first HIST_SLOTS queries of the CTA's range: the
+    // scores' keys, then the block maxima's
     static constexpr int HIST_SLOTS = NQ == 1 ? 2 : 0;
     static constexpr int OFF_HIST = OFF_IDS + IDS_BYTES;
-    static constexpr int HIST_BYTES = HIST_SLOTS * 4096 * 4;
+    static constexpr int HIST_BYTES = 2 * HIST_SLOTS * 4096 * 4;
     static constexpr int OFF_BARS = OFF_HIST + HIST_BYTES;
     // full, sfready, empty per stage; acc_full per accumulator set, acc_empty per
     // tile of a set (the epilogue frees each tile as soon as it has read it);
@@ -408,9 +412,10 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS
     uint8_t* stages = smem + C::OFF_STAGES;
     uint8_t* qslots = smem + C::OFF_QSLOTS;
     int32_t* ids_ring = reinterpret_cast<int32_t*>(smem + C::OFF_IDS);
-    uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + C::OFF_HIST);  // [slot][4096]
+    uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + C::OFF_HIST);  // [2][slot][4096]
     const bool fuse_hist = C::HIST_SLOTS > 0 && p.key_hist;
-    if (fuse_hist)
+    const bool fuse_bhist = C::HIST_SLOTS > 0 && p.bmax_hist && p.bmax;
+    if (fuse_hist || fuse_bhist)
         for (int i = threadIdx.x; i < C::HIST_BYTES / 4; i += blockDim.x) hist_s[i] = 0u;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
     uint64_t* full = bars;
@@ -737,6 +742,11 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS
             if (slot >= 0 && slot < C::HIST_SLOTS) return hist_s + slot * 4096;
             return p.key_hist + (int64_t)b * 4096;
         };
+        auto bhist_of = [&](int b) -> uint32_t* {
+            const int slot = b - b_first;
+            if (slot >= 0 && slot < C::HIST_SLOTS) return hist_s + (C::HIST_SLOTS + slot) * 4096;
+            return p.bmax_hist + (int64_t)b * 4096;
+        };
         // the scaled head weights of this warp's query, in f32x2 pairs
         uint64_t w2[16];
         auto load_w = [&](int b) {
@@ -761,7 +771,10 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS
                 m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
                 m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
                 m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-                if ((lane & 7) == 0 && vis) p.bmax[(int64_t)b * p.ldb + key / 8] = m;
+                if ((lane & 7) == 0 && vis) {
+                    p.bmax[(int64_t)b * p.ldb + key / 8] = m;
+                    if (fuse_bhist) atomicAdd(bhist_of(b) + (order_key(m) >> 20), 1u);
+                }
             }
         };
         int cur_g = -1;
@@ -879,12 +892,15 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS
     __syncthreads();
     tc_fence_after();
     if (warp == C::MMA_WARP) tmem_dealloc(tmem, C::TMEM_COLS);
-    if (fuse_hist) {  // merge the shared-memory slots into the global histograms
+    if constexpr (C::HIST_SLOTS > 0)
+    if (fuse_hist || fuse_bhist) {  // merge the shared-memory slots into the global histograms
         const int b_first = sh->g0 * NQ;
-        for (int i = threadIdx.x; i < C::HIST_SLOTS * 4096; i += blockDim.x) {
+        for (int i = threadIdx.x; i < 2 * C::HIST_SLOTS * 4096; i += blockDim.x) {
             const uint32_t v = hist_s[i];
-            const int b = b_first + i / 4096;
-            if (v && b < p.B) atomicAdd(p.key_hist + (int64_t)b * 4096 + (i & 4095), v);
+            const bool bm = i >= C::HIST_SLOTS * 4096;
+            const int b = b_first + (i / 4096) % C::HIST_SLOTS;
+            uint32_t* gh = bm ? p.bmax_hist : p.key_hist;
+            if (v && b < p.B && gh) atomicAdd(gh + (int64_t)b * 4096 + (i & 4095), v);
         }
     }
 #ifdef HSI_TRACE

@@ -316,6 +316,10 @@ __global__ void __launch_bounds__(SCAN_THREADS) sel_collect_kernel(SelParams p) 
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             if ((okm >> (4 * r + i) & 1u) && (keys[r][i] >> 20) >= thr) sm |= 1u << (4 * r + i);
+    // one reservation in the query's list per CTA (per warp, the CTAs of all
+    // queries crowded the few cache lines of the counters)
+    __shared__ uint32_t wsum[SCAN_THREADS / 32 + 1];
+    const int warp = threadIdx.x >> 5;
     const uint32_t c = (uint32_t)__popc(sm);
     uint32_t incl = c;
 #pragma unroll
@@ -323,11 +327,20 @@ __global__ void __launch_bounds__(SCAN_THREADS) sel_collect_kernel(SelParams p) 
         const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
         if (lane >= o) incl += t;
     }
-    const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-    if (tot == 0) return;
-    uint32_t base = 0;
-    if (lane == 0) base = atomicAdd(cnt, tot);
-    uint32_t at = __shfl_sync(0xFFFFFFFFu, base, 0) + incl - c;
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t run = 0;
+        for (int w = 0; w < SCAN_THREADS / 32; ++w) {
+            const uint32_t x = wsum[w];
+            wsum[w] = run;
+            run += x;
+        }
+        wsum[SCAN_THREADS / 32] = run ? atomicAdd(cnt, run) : 0u;
+    }
+    __syncthreads();
+    if (c == 0) return;
+    uint32_t at = wsum[SCAN_THREADS / 32] + wsum[warp] + incl - c;
 #pragma unroll
     for (int r = 0; r < SCAN_ROUNDS; ++r)
 #pragma unroll
@@ -393,17 +406,29 @@ __global__ void __launch_bounds__(SCAN_THREADS) sel_collect_blocks_kernel(SelPar
     uint32_t c = 0;
 #pragma unroll 1
     for (uint32_t h = hit; h; h &= h - 1) c += (uint32_t)__popc(block_mask(block_of(__ffs(h) - 1)));
+    // one reservation in the query's list per CTA
+    __shared__ uint32_t wsum[SCAN_THREADS / 32 + 1];
+    const int warp = threadIdx.x >> 5;
     uint32_t incl = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
         if (lane >= o) incl += t;
     }
-    const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-    if (tot == 0) return;
-    uint32_t base = 0;
-    if (lane == 0) base = atomicAdd(p.cand_cnt + b, tot);
-    uint32_t at = __shfl_sync(0xFFFFFFFFu, base, 0) + incl - c;
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t run = 0;
+        for (int w = 0; w < SCAN_THREADS / 32; ++w) {
+            const uint32_t x = wsum[w];
+            wsum[w] = run;
+            run += x;
+        }
+        wsum[SCAN_THREADS / 32] = run ? atomicAdd(p.cand_cnt + b, run) : 0u;
+    }
+    __syncthreads();
+    if (c == 0) return;
+    uint32_t at = wsum[SCAN_THREADS / 32] + wsum[warp] + incl - c;
     uint32_t* ck = p.cand_key + (int64_t)b * p.cap;
     uint32_t* ci = p.cand_idx + (int64_t)b * p.cap;
 #pragma unroll 1
@@ -428,7 +453,7 @@ struct SelSmem {
     uint32_t whist[SEL_WARPS][256];
     uint32_t hsum[256];
     unsigned long long win[SEL_MAXK];
-    uint64_t bar;  // completion of the bulk copies of a row (select_small_hist)
+    uint64_t bar;  // completion of the bulk copies of a row (select_small_fast)
     int abort;
     uint32_t bcast[8];
     alignas(16) uint32_t keys[SEL_CAP];
@@ -1271,6 +1296,63 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) sel_small_kernel(SelParams p) 
     SEL_MARK(s, 31);
 }
 
+// Pool outputs of query b from the `count` winners in s.win (block ids in the
+// low words, ~id): the ids in ascending order (s.win holds them so), -1
+// padded; the visible-position count; the position bit table when given.
+__device__ __noinline__ void write_pool(const SelParams& p, int b, int count) {
+    SelSmem& s = sel_smem();
+    const int bs = p.div;
+    const int64_t n_vis = sel_len(p, b);
+    const int64_t nb = (n_vis + bs - 1) / bs;
+    int32_t* bo = p.blk_out + (int64_t)b * p.k;
+    for (int t = threadIdx.x; t < p.k; t += SEL_THREADS)
+        bo[t] = t < count ? (int32_t)(uint32_t)~(uint32_t)(s.win[t] & 0xFFFFFFFFull) : -1;
+    if (threadIdx.x == 0) {
+        p.n_kept[b] = count;
+        // every kept block holds bs visible positions but the newest, which may hold fewer
+        const int64_t last = count ? (int64_t)(uint32_t)~(uint32_t)(s.win[count - 1] & 0xFFFFFFFFull) : -1;
+        p.n_pool[b] = (int32_t)((int64_t)bs * count - (last == nb - 1 ? (int64_t)bs * nb - n_vis : 0));
+    }
+    uint32_t* bits = p.bits ? p.bits + (int64_t)b * p.ld_bits : nullptr;
+    if (!bits) return;
+    const int64_t words = (n_vis + 31) / 32;
+    if (bs == 8 && nb <= 32 * (int64_t)SEL_CAP) {
+        // the kept blocks into a bitmap (s.keys), then every word of the table
+        // at once: word w holds blocks 4w .. 4w+3, 8 bits each
+        uint32_t* bm = s.keys;
+        const int64_t bw = (nb + 31) / 32;
+        for (int64_t w = threadIdx.x; w < bw; w += SEL_THREADS) bm[w] = 0u;
+        __syncthreads();
+        for (int t = threadIdx.x; t < count; t += SEL_THREADS) {
+            const uint32_t id = ~(uint32_t)(s.win[t] & 0xFFFFFFFFull);
+            atomicOr(&bm[id >> 5], 1u << (id & 31));
+        }
+        __syncthreads();
+        for (int64_t w = threadIdx.x; w < words; w += SEL_THREADS) {
+            const uint32_t nib = (bm[w >> 3] >> (4 * (w & 7))) & 0xFu;
+            uint32_t v = ((nib * 0x00204081u) & 0x01010101u) * 0xFFu;
+            const int64_t end = n_vis - 32 * w;  // visible positions in this word
+            if (end < 32) v &= (1u << end) - 1u;
+            bits[w] = v;
+        }
+        return;
+    }
+    for (int64_t wd = threadIdx.x; wd < words; wd += SEL_THREADS) bits[wd] = 0u;
+    __syncthreads();
+    for (int t = threadIdx.x; t < count; t += SEL_THREADS) {
+        const int64_t blk = (int64_t)(uint32_t)~(uint32_t)(s.win[t] & 0xFFFFFFFFull);
+        const int64_t a = blk * bs, e = min(n_vis, a + bs);
+        for (int64_t pos = a; pos < e;) {
+            const int64_t wd = pos >> 5;
+            const int64_t we = min(e, (wd + 1) << 5);
+            const int lo = (int)(pos & 31), cnt = (int)(we - pos);
+            const uint32_t m = (cnt == 32) ? 0xFFFFFFFFu : (((1u << cnt) - 1u) << lo);
+            atomicOr(&bits[wd], m);
+            pos = we;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) {
     griddep_wait();
     griddep_launch_dependents();
@@ -1308,42 +1390,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) 
     if (p.mode == SEL_TOPK) {
         write_topk(p, b, count, s, false);
     } else {
-        // pool: ascending block ids, the visible-position count and the bit table
-        const int bs = p.div;
-        const int64_t n_vis = sel_len(p, b);
-        int32_t* bo = p.blk_out + (int64_t)b * p.k;
-        if (threadIdx.x == 0) s.bcast[5] = 0;
-        uint32_t* bits = p.bits ? p.bits + (int64_t)b * p.ld_bits : nullptr;
-        if (bits) {
-            const int64_t words = (n_vis + 31) / 32;
-            for (int64_t wd = threadIdx.x; wd < words; wd += SEL_THREADS) bits[wd] = 0u;
-        }
-        __syncthreads();
-        for (int t = threadIdx.x; t < p.k; t += SEL_THREADS) {
-            if (t < count) {
-                const int64_t blk = (int64_t)(uint32_t)~(uint32_t)(s.win[t] & 0xFFFFFFFFull);
-                bo[t] = (int32_t)blk;
-                const int64_t a = blk * bs, e = min(n_vis, a + bs);
-                atomicAdd(&s.bcast[5], (uint32_t)(e - a));
-                if (bits) {
-                    for (int64_t pos = a; pos < e;) {
-                        const int64_t wd = pos >> 5;
-                        const int64_t we = min(e, (wd + 1) << 5);
-                        const int lo = (int)(pos & 31), cnt = (int)(we - pos);
-                        const uint32_t m = (cnt == 32) ? 0xFFFFFFFFu : (((1u << cnt) - 1u) << lo);
-                        atomicOr(&bits[wd], m);
-                        pos = we;
-                    }
-                }
-            } else {
-                bo[t] = -1;
-            }
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            p.n_kept[b] = count;
-            p.n_pool[b] = (int32_t)s.bcast[5];
-        }
+        write_pool(p, b, count);
     }
     SEL_MARK(s, 31);
 }

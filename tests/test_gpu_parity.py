@@ -468,7 +468,7 @@ def test_reindex_layer_selection_paths(case):
     not 16-byte aligned with plain loads. Every route gives what the general
     top-k (hsi_topk) gives on the same pooled scores, and the oracle's top-k."""
     wl = inputs.workload(1)
-    lengths = [40000, 20000, 16390]
+    lengths = [140000, 20000, 16390]  # the first row's 17,500 blocks take the Full layer's bounded pool route
     B = len(lengths)
     rng = np.random.default_rng(11)
     base = [wl.k_bf16(0, b, rows=n) for b, n in enumerate(lengths)]
@@ -488,8 +488,23 @@ def test_reindex_layer_selection_paths(case):
     i_f, v_f = torch.empty(B, 512, dtype=torch.int32, device=DEV), torch.empty(B, 512, device=DEV)
     ids = torch.empty(B, 2048, dtype=torch.int32, device=DEV)
     nk, npl = torch.empty(B, dtype=torch.int32, device=DEV), torch.empty(B, dtype=torch.int32, device=DEV)
+    bits = torch.full((B, (maxv + 31) // 32), 7, dtype=torch.int32, device=DEV)
     hsi.full_layer(q_rec, g_q, w, k_rec, gk, off, nv, B, maxv, s_f, 512, i_f, v_f, block_ids=ids, n_kept=nk,
-                   n_pool=npl)
+                   n_pool=npl, pool_bits=bits)
+    assert hsi.device_error() == 0
+    # the Full layer's pool equals the stand-alone pool selection on its scores
+    ids_sep = torch.full((B, 2048), 7, dtype=torch.int32, device=DEV)
+    nk_sep, np_sep = torch.empty(B, dtype=torch.int32, device=DEV), torch.empty(B, dtype=torch.int32, device=DEV)
+    bits_sep = torch.zeros(B, (maxv + 31) // 32, dtype=torch.int32, device=DEV)
+    hsi.candidate_pool(nv, B, maxv, ids_sep, nk_sep, np_sep, scores=s_f, pool_bits=bits_sep)
+    assert torch.equal(nk, nk_sep) and torch.equal(npl, np_sep), case
+    for b, n in enumerate(lengths):
+        kb = int(nk_sep[b])
+        assert torch.equal(ids[b, :kb], ids_sep[b, :kb]) and bool((ids[b, kb:] == -1).all()), (case, b)
+        words = (n + 31) // 32
+        assert torch.equal(bits[b, :words], bits_sep[b, :words]), (case, b)
+    oi, onk, onp, _ = oracle.pool(s_f[0].cpu().numpy(), lengths[0])
+    assert int(nk[0]) == onk and int(npl[0]) == onp and np.array_equal(ids[0].cpu().numpy()[:onk], oi[:onk])
     q1, g1, w1 = gpu_queries(wl, 1, range(B))
     ld = 2048 * 8 + (1 if case == "unaligned_rows" else 0)
     ps_sep = torch.empty(B, ld, device=DEV)[:, :2048 * 8]
