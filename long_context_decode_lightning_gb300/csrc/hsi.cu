@@ -192,6 +192,11 @@ hsi_status run_select(SelParams sp, int64_t max_items, cudaStream_t s, bool hist
             return HSI_ERR_CUDA;
         }
     }
+    if (sp.mode == SEL_POOL && max_items > SEL_CAP) {
+        static std::atomic<bool> pool_attr_set[kMaxDevices];
+        if (smem_attr_once(pool_final_kernel, (int)sizeof(SelSmem), pool_attr_set) != HSI_OK) return HSI_ERR_CUDA;
+        return launch(pool_final_kernel, dim3(sp.B), dim3(SEL_THREADS), sizeof(SelSmem), s, sp);
+    }
     if (sp.hist_small && sp.mode == SEL_TOPK && max_items <= SEL_CAP) {
         static std::atomic<bool> small_attr_set[kMaxDevices];
         if (smem_attr_once(sel_small_kernel, (int)sizeof(SelSmem), small_attr_set) != HSI_OK) return HSI_ERR_CUDA;

@@ -1395,6 +1395,203 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) sel_final_kernel(SelParams p) 
     SEL_MARK(s, 31);
 }
 
+// Pool rows of more than SEL_CAP blocks by the general route: the candidates
+// of the collect pass (or the whole row when they overflowed) through the
+// block select, then the pool outputs. Every thread of the block calls it.
+__device__ __noinline__ void pool_generic(const SelParams& p, int b) {
+    SelSmem& s = sel_smem();
+    const int64_t n = sel_items(p, b);
+    const uint32_t c = p.cand_cnt[b];
+    const uint32_t* ck = p.cand_key + (int64_t)b * p.cap;
+    const uint32_t* ci = p.cand_idx + (int64_t)b * p.cap;
+    __syncthreads();  // the caller's reads of shared memory are done
+    int count;
+    if (c <= (uint32_t)SEL_CAP) {
+        for (uint32_t j = threadIdx.x; j < c; j += SEL_THREADS) {
+            s.keys[j] = ck[j];
+            s.idx[j] = ci[j];
+        }
+        __syncthreads();
+        SmemSrc src{s.keys, s.idx, (int64_t)c};
+        count = block_select<true>(src, s, p.k, n);
+    } else if (c <= (uint32_t)p.cap) {
+        GlobalSrc src{ck, ci, (int64_t)c};
+        count = block_select<false>(src, s, p.k, n);
+    } else {
+        RowSrc src{&p, b, n};
+        count = block_select<false>(src, s, p.k, n);
+    }
+    write_pool(p, b, count);
+}
+
+constexpr int POOL_B2 = 2 * SEL_THREADS;  // second-level bins of the candidates' keys
+constexpr int POOL_TIED_CAP = 2048;       // candidates of the threshold's second-level bin, ranked
+
+// The candidate pool of rows of more than SEL_CAP blocks of 8 (SEL_POOL),
+// after the threshold bin T (p.thr) and the collect pass (p.cand_*: every
+// block whose maximum's key reaches bin T, the pinned newest block at key
+// +inf). The candidates go into shared memory; a second histogram of POOL_B2
+// bins spans their finite keys (from bin T's least key to the largest); its
+// scan gives the bin T2 of the last place: the candidates at +inf and above
+// T2 win, those in T2 are ranked among themselves (key, then lower id). The
+// winners' bitmap gives the ids in ascending order, the pooled position count
+// and the position bit table. Overflowing lists, more candidates at +inf than
+// places and heavy ties in T2 take the general route.
+__global__ void __launch_bounds__(SEL_THREADS, 1) pool_final_kernel(SelParams p) {
+    static_assert(POOL_B2 + 2 * POOL_TIED_CAP + 2 * SEL_WARPS <= SEL_WARPS * 256, "bins, tied list, reductions in s.whist");
+    static_assert(SEL_BITMAP_IDS / 64 <= SEL_MAXK, "the block bitmap fits in s.win");
+    griddep_wait();
+    griddep_launch_dependents();
+    SelSmem& s = sel_smem();
+    const int b = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int64_t n_vis = sel_len(p, b);
+    const int64_t nb = (n_vis + 7) / 8;
+    const uint32_t c = p.cand_cnt[b];
+    if (p.div != 8 || c > (uint32_t)SEL_CAP || nb > SEL_BITMAP_IDS) {
+        pool_generic(p, b);
+        return;
+    }
+    const uint32_t base = p.thr[b] << 20;
+    const uint32_t* ck = p.cand_key + (int64_t)b * p.cap;
+    const uint32_t* ci = p.cand_idx + (int64_t)b * p.cap;
+    uint32_t* h2 = &s.whist[0][0];
+    unsigned long long* tied = reinterpret_cast<unsigned long long*>(h2 + POOL_B2);
+    uint32_t* wred = h2 + POOL_B2 + 2 * POOL_TIED_CAP;  // [2][SEL_WARPS]
+    uint32_t* bm = reinterpret_cast<uint32_t*>(s.win);   // block bitmap
+    const int words = (int)((nb + 31) / 32);
+    uint32_t mx = 0, ninf = 0;
+    for (uint32_t j = t; j < c; j += SEL_THREADS) {
+        const uint32_t key = ck[j];
+        s.keys[j] = key;
+        s.idx[j] = ci[j];
+        if (key >= KEY_POS_INF) ++ninf;
+        else mx = max(mx, key);
+    }
+    h2[2 * t] = 0u;
+    h2[2 * t + 1] = 0u;
+    for (int w = t; w < words; w += SEL_THREADS) bm[w] = 0u;
+    if (t == 0) s.bcast[6] = 0u;
+    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+    ninf = __reduce_add_sync(0xFFFFFFFFu, ninf);
+    if (lane == 0) {
+        wred[warp] = mx;
+        wred[SEL_WARPS + warp] = ninf;
+    }
+    __syncthreads();
+    const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, wred[lane]);
+    const uint32_t n_inf = __reduce_add_sync(0xFFFFFFFFu, wred[SEL_WARPS + lane]);
+    const uint32_t k = (uint32_t)p.k;
+    if (n_inf >= k && c > k) {  // more +inf keys than places (uniform)
+        pool_generic(p, b);
+        return;
+    }
+    const uint32_t kk = k > n_inf ? k - n_inf : 0u;  // places for the finite keys
+    const uint32_t range = top > base ? top - base : 0u;
+    const int sh2 = range >= (uint32_t)POOL_B2 ? 32 - __clz((int)(range / POOL_B2)) : 0;  // range >> sh2 < POOL_B2
+    for (uint32_t j = t; j < c; j += SEL_THREADS) {
+        const uint32_t key = s.keys[j];
+        if (key < KEY_POS_INF) atomicAdd(&h2[min(key > base ? (key - base) >> sh2 : 0u, (uint32_t)(POOL_B2 - 1))], 1u);
+    }
+    __syncthreads();
+    const uint32_t c0 = h2[2 * t], c1 = h2[2 * t + 1];
+    uint32_t fin;
+    const uint32_t below = block_excl_scan(c0 + c1, s, &fin);  // finite candidates in bins under 2t
+    const bool take_all = fin <= kk;
+    const uint32_t over = fin - below - c0 - c1;  // in the bins above 2t + 1
+    if (!take_all && over < kk && over + c0 + c1 >= kk) {
+        if (over + c1 >= kk) {
+            s.bcast[2] = (uint32_t)(2 * t + 1);
+            s.bcast[3] = over;
+            s.bcast[4] = c1;
+        } else {
+            s.bcast[2] = (uint32_t)(2 * t);
+            s.bcast[3] = over + c1;
+            s.bcast[4] = c0;
+        }
+    }
+    __syncthreads();
+    const uint32_t T2 = take_all ? 0u : s.bcast[2], above = take_all ? 0u : s.bcast[3];
+    if (!take_all && s.bcast[4] > (uint32_t)POOL_TIED_CAP) {  // heavy ties (uniform)
+        pool_generic(p, b);
+        return;
+    }
+    for (uint32_t j0 = 0; j0 < c; j0 += SEL_THREADS) {  // uniform trip count per warp
+        const uint32_t j = j0 + (uint32_t)t;
+        bool tie = false;
+        uint32_t key = 0, id = 0;
+        if (j < c) {
+            key = s.keys[j];
+            id = s.idx[j];
+            bool win = key >= KEY_POS_INF || take_all;
+            if (!win) {
+                const uint32_t bin = min(key > base ? (key - base) >> sh2 : 0u, (uint32_t)(POOL_B2 - 1));
+                win = bin > T2;
+                tie = bin == T2;
+            }
+            if (win) {
+                if (id < (uint32_t)nb) atomicOr(&bm[id >> 5], 1u << (id & 31));
+                else raise_error(DEVERR_ARG);  // never a block of this row
+            }
+        }
+        const uint32_t pos = warp_append(tie, &s.bcast[6]);
+        if (tie && pos < (uint32_t)POOL_TIED_CAP) tied[pos] = ((unsigned long long)key << 32) | (uint32_t)~id;
+    }
+    __syncthreads();
+    if (!take_all) {  // the tied candidates: the first (kk - above) by key, then lower id
+        const uint32_t nt = min(s.bcast[6], (uint32_t)POOL_TIED_CAP);
+        const uint32_t want = kk > above ? kk - above : 0u;
+        for (uint32_t j = t; j < nt; j += SEL_THREADS) {
+            const unsigned long long me = tied[j];
+            uint32_t r = 0;
+            for (uint32_t i = 0; i < nt; ++i) r += tied[i] > me ? 1u : 0u;
+            const uint32_t id = ~(uint32_t)(me & 0xFFFFFFFFull);
+            if (r < want && id < (uint32_t)nb) atomicOr(&bm[id >> 5], 1u << (id & 31));
+        }
+        __syncthreads();
+    }
+    // outputs: the ids in ascending order (each thread a run of consecutive words)
+    constexpr int WPT = (int)(SEL_BITMAP_IDS / 32 / SEL_THREADS);
+    uint32_t wv[WPT], mine = 0;
+#pragma unroll
+    for (int i = 0; i < WPT; ++i) {
+        const int wd = t * WPT + i;
+        wv[i] = wd < words ? bm[wd] : 0u;
+        mine += (uint32_t)__popc(wv[i]);
+    }
+    uint32_t kept;
+    uint32_t pos = block_excl_scan(mine, s, &kept);
+    int32_t* bo = p.blk_out + (int64_t)b * p.k;
+#pragma unroll
+    for (int i = 0; i < WPT; ++i) {
+        const uint32_t wbase = (uint32_t)(t * WPT + i) * 32u;
+        uint32_t w = wv[i];
+        while (w) {
+            const uint32_t id = wbase + (uint32_t)(__ffs(w) - 1);
+            w &= w - 1u;
+            if (pos < k) bo[pos] = (int32_t)id;
+            ++pos;
+        }
+    }
+    for (uint32_t j = kept + (uint32_t)t; j < k; j += SEL_THREADS) bo[j] = -1;
+    if (t == 0) {
+        const bool last = nb > 0 && ((bm[(nb - 1) >> 5] >> ((nb - 1) & 31)) & 1u);
+        p.n_kept[b] = (int32_t)min(kept, k);
+        // every kept block holds 8 visible positions but the newest, which may hold fewer
+        p.n_pool[b] = (int32_t)(8 * (int64_t)kept - (last ? 8 * nb - n_vis : 0));
+    }
+    if (p.bits) {  // word w of the position bit table holds blocks 4w .. 4w+3, 8 bits each
+        uint32_t* bits = p.bits + (int64_t)b * p.ld_bits;
+        const int64_t pw = (n_vis + 31) / 32;
+        for (int64_t w = t; w < pw; w += SEL_THREADS) {
+            const uint32_t nib = (bm[w >> 3] >> (4 * (w & 7))) & 0xFu;
+            uint32_t v = ((nib * 0x00204081u) & 0x01010101u) * 0xFFu;
+            const int64_t end = n_vis - 32 * w;  // visible positions in this word
+            if (end < 32) v &= (1u << end) - 1u;
+            bits[w] = v;
+        }
+    }
+}
+
 // A visible length within [0, max_n], the caller's bound that sized the rows;
 // a larger value is clamped and reported as a device-side argument error.
 __device__ __forceinline__ int64_t clamp_len(int64_t n, int64_t max_n) {
