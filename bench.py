@@ -266,7 +266,10 @@ class DeviceWorkload:
         # the Full layer's top-512 and its pool run on two streams: the pool and the
         # Reindex layers (which need only the pool) on `side`, joined at the end
         self.side = torch.cuda.Stream(device=dev)
-        self.ev_fork, self.ev_join = torch.cuda.Event(), torch.cuda.Event()
+        self.ev_fork, self.ev_join, self.ev_pool = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+        # the Full layer that builds the pool writes no score row: its top-512 is
+        # taken from the pool's blocks, scored again (the same scores, the same top-512)
+        self.pooled_topk = wl.build_pool
         self.pool_sum = None
         self.wl_signs = signs
         self.graphs = []
@@ -313,21 +316,25 @@ class DeviceWorkload:
             def fl(ph, l=l, pool=pool):
                 hsi.full_layer(
                     self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[l], self.g_k[l], self.k_off, self.n_vis, B,
-                    maxv, self.scores, K_TOP, self.idx[l], self.val[l],
+                    maxv, None if (pool and self.pooled_topk) else self.scores, K_TOP, self.idx[l], self.val[l],
                     block_ids=self.ids if pool else None, n_kept=self.nk if pool else None,
                     n_pool=self.npool if pool else None, pool_bits=self.bits if pool else None,
                     n_keep=wl.n_keep, ws=self.ws_full, phases=ph, fmt=self.fmt)
             segs.append(("score", lambda fl=fl: fl(hsi.PHASE_SCORE)))
             if pool:
                 def post(fl=fl):
+                    # the pool and the Reindex layers on `side`; the Full layer's
+                    # top-512 (from the pool) beside them on the main stream
                     main = torch.cuda.current_stream()
                     self.ev_fork.record(main)
                     self.side.wait_event(self.ev_fork)
-                    fl(hsi.PHASE_TOPK)
                     with torch.cuda.stream(self.side):
                         fl(hsi.PHASE_POOL)
+                        self.ev_pool.record(self.side)
                         rest()
                         self.ev_join.record(self.side)
+                    main.wait_event(self.ev_pool)
+                    fl(hsi.PHASE_TOPK)
                     main.wait_event(self.ev_join)
                 segs.append(("post", post))
             else:
@@ -436,14 +443,16 @@ class DeviceWorkload:
         return full + pooled, full, pooled
 
     def score_bytes_per_launch(self):
-        """Algorithmic bytes of one hsi_score_full launch: 72 B (NVFP4) or 68 B
-        (MXFP4) per visible key read, 4 B per score and 4 B per block maximum
-        written, q/w/scales read."""
+        """Algorithmic bytes of one Full-layer scoring launch: 72 B (NVFP4) or 68 B
+        (MXFP4) per visible key read, 4 B per block maximum written, 4 B per
+        score written unless the top-512 comes from the pool, q/w/scales read."""
         n = int(sum(self.wl.n_visible))
         nb = sum((v + 7) // 8 for v in self.wl.n_visible)
         key_bytes = self.rec // 8
         scales = 0 if self.mx else 8
-        return n * key_bytes + n * 4 + (nb * 4 if self.wl.build_pool else 0) + self.B * (4 * self.rec + 32 * 4 + scales)
+        score_row = 0 if (self.wl.build_pool and self.pooled_topk) else n * 4
+        return (n * key_bytes + score_row + (nb * 4 if self.wl.build_pool else 0)
+                + self.B * (4 * self.rec + 32 * 4 + scales))
 
 
 class MainKV:
@@ -794,7 +803,7 @@ def run_case(args, dev, log):
         for _ in range(args.steps):
             if args.case == "pool":
                 hsi.full_layer(W.q_rec[0], W.g_q[0], W.w[0], W.k_rec[0], W.g_k[0], W.k_off, W.n_vis, W.B, W.maxv,
-                               W.scores, K_TOP, W.idx[0], W.val[0], block_ids=W.ids, n_kept=W.nk, n_pool=W.npool,
+                               None if W.pooled_topk else W.scores, K_TOP, W.idx[0], W.val[0], block_ids=W.ids, n_kept=W.nk, n_pool=W.npool,
                                pool_bits=W.bits, n_keep=wl.n_keep, ws=W.ws_full, phases=hsi.PHASE_POOL)
             else:
                 hsi.reindex_layer(W.q_rec[l], W.g_q[l], W.w[l], W.k_rec[0], W.g_k[0], W.k_off, W.n_vis, W.ids,

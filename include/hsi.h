@@ -162,7 +162,8 @@ hsi_status hsi_quantize_mxfp4(const uint16_t* x, int64_t n_tensors, int64_t rows
  *          g_k) and are scored in one tensor-core tile (chunked prefill);
  *          B must then be a multiple of 4.
  *  scores  (dev) fp32 [B][ld]; entries s < n_visible[b] are written, the
- *          rest are left untouched. ld >= max_visible.
+ *          rest are left untouched. ld >= max_visible. May be NULL when
+ *          block_max is given (the block maxima only).
  *  block_max (dev, may be NULL) fp32 [B][ldb]: the max of each run of 8
  *          consecutive visible scores (block b8 = positions 8*b8 .. 8*b8+7,
  *          invisible positions count as -inf), for the blocks that hold a
@@ -429,6 +430,17 @@ hsi_status hsi_append_token(const uint16_t* k_x, const int8_t* signs, const floa
  *  Arguments as in hsi_score_full (group 1, format), hsi_topk (n_valid =
  *  n_visible) and hsi_candidate_pool (block_size 8). scores [B][ld] is written.
  *  block_ids NULL: no pool (n_kept, n_pool, pool_bits ignored).
+ *  scores NULL (with a pool, n_keep - 1 >= k, n_keep <= 2048 and a multiple
+ *          of 32): no score row is written, and the top-k is taken from the
+ *          pool. The pool's n_keep - 1 unpinned blocks are the first by
+ *          (maximum desc, index asc), and every top-k position lies in the
+ *          first k blocks of that order (a position outside them is outranked
+ *          by each of those blocks' maxima), so the pool holds the top-k. The
+ *          pooled blocks are scored again from k_rec with the layer's query
+ *          (the same fp32 scores as the full scan) and their top-k taken as in
+ *          hsi_reindex_layer: the same top_idx and top_val as with scores.
+ *          HSI_PHASE_TOPK then needs the pool first (HSI_PHASE_POOL, or
+ *          HSI_PHASE_SELECT / HSI_PHASE_ALL, which run it first).
  *  phases  HSI_PHASE_ALL, or the parts as separate calls with the same
  *          arguments and workspace, scoring first (the workspace carries the
  *          histograms and block maxima from one to the other):

@@ -238,7 +238,8 @@ def rec_bytes(fmt: int = FMT_NVFP4) -> int:
 
 def score_full(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B, max_visible, scores, ld=None,
                block_max=None, ldb=0, group=1, fmt=FMT_NVFP4, stream=None):
-    ld = scores.shape[-1] if ld is None else ld
+    """scores None (block_max given): the block maxima only, no score row."""
+    ld = (scores.shape[-1] if scores is not None else 0) if ld is None else ld
     if block_max is not None and not ldb:
         ldb = block_max.shape[-1]
     _check("hsi_score_full", lib().hsi_score_full(
@@ -300,12 +301,13 @@ def full_layer(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B, max_visible, 
                phases=3, fmt=FMT_NVFP4, stream=None):
     """Full layer: scores, top-k and (block_ids given) the candidate pool.
     phases: 1 scoring only, 2 selection only (after 1, same workspace), 3 both;
-    4 the top-k only, 8 the pool only (after 1; the two may run on two streams)."""
-    ld = scores.shape[-1] if ld is None else ld
+    4 the top-k only, 8 the pool only (after 1; the two may run on two streams).
+    scores None: no score row; the top-k is taken from the pool (phase 4 after 8)."""
+    ld = (scores.shape[-1] if scores is not None else 0) if ld is None else ld
     if pool_bits is not None and not ld_bits:
         ld_bits = pool_bits.shape[-1]
     if ws is None:
-        ws = workspace(WS_FULL_LAYER, B, max_visible, k, device=scores.device)
+        ws = workspace(WS_FULL_LAYER, B, max_visible, k, device=top_idx.device)
     _check("hsi_full_layer", lib().hsi_full_layer(
         _ptr(q_rec), _ptr(g_q), _ptr(w), _ptr(k_rec), _ptr(g_k), _ptr(k_rec_off), _ptr(n_visible), B, max_visible,
         _ptr(scores), ld, k, _ptr(top_idx), _ptr(top_val), n_keep, _ptr(block_ids), _ptr(n_kept), _ptr(n_pool),

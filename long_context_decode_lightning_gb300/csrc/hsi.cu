@@ -305,6 +305,15 @@ hsi_status noalloc_scratch(void** out) {
     return HSI_OK;
 }
 
+// Scratch of the Full layer's top-k taken from its pool (scores == NULL): the
+// pooled scores [B][8 kPooledTopkMaxKeep] and the key histogram the gathering
+// scan fills (the Reindex layer's workspace for 8 kPooledTopkMaxKeep items).
+constexpr int32_t kPooledTopkMaxKeep = SEL_CAP / 8;
+size_t pooled_topk_ws_bytes(int32_t B) {
+    return align_up((size_t)B * SEL_CAP * 4, 256) + sel_ws_bytes(B, SEL_CAP, false, 0) +
+           align_up((size_t)B * HIST_BINS * 4, 256);
+}
+
 }  // namespace
 
 extern "C" {
@@ -381,10 +390,11 @@ size_t hsi_workspace_size(hsi_ws_kind kind, int32_t B, int64_t max_n, int32_t k)
         case HSI_WS_QUANTIZE: return align_up((size_t)B * 4, 256);
         case HSI_WS_SCORE: return 0;
         case HSI_WS_TOPK: return sel_ws_bytes(B, max_n, false, 0);
-        case HSI_WS_FULL_LAYER: {  // the top-k's and the pool's selection buffers, the block maxima (rows padded to 16 bytes)
+        case HSI_WS_FULL_LAYER: {  // the top-k's and the pool's selection buffers, the block maxima (rows padded
+                                   // to 16 bytes), and for the top-k from the pool its scores and key histogram
             const int64_t nb = (max_n + 7) / 8;
             return sel_ws_bytes(B, max_n, false, 0) + sel_ws_bytes(B, nb, false, 0) +
-                   align_up((size_t)B * align_up((size_t)nb, 4) * 4, 256);
+                   align_up((size_t)B * align_up((size_t)nb, 4) * 4, 256) + pooled_topk_ws_bytes(B);
         }
         case HSI_WS_PREFILL_LAYER:  // the block maxima, rows padded to 16 bytes
             return align_up((size_t)B * align_up((size_t)((max_n + 7) / 8), 4) * 4, 256);
@@ -473,7 +483,8 @@ hsi_status hsi_score_full(const uint8_t* q_rec, const float* g_q, const float* w
     (void)ws_bytes;
     hsi_status st = check_score_common(format, q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B);
     if (st != HSI_OK) return st;
-    if (!scores || max_visible < 0 || max_visible > (int64_t)INT32_MAX - 128 || ld < max_visible)
+    if ((!scores && !block_max) || max_visible < 0 || max_visible > (int64_t)INT32_MAX - 128 ||
+        (scores && ld < max_visible))
         return HSI_ERR_INVALID_ARG;
     if (block_max && ldb < (max_visible + 7) / 8) return HSI_ERR_INVALID_ARG;
     if (group != 1 && group != 4) return HSI_ERR_UNSUPPORTED;
@@ -691,11 +702,16 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
         return HSI_ERR_INVALID_ARG;
     hsi_status st = check_score_common(format, q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B);
     if (st != HSI_OK) return st;
-    if (!scores || !top_idx || !top_val || max_visible < 0 || max_visible > (int64_t)INT32_MAX - 256 ||
-        ld < max_visible || k < 1 || k > 2048)
+    if (!top_idx || !top_val || max_visible < 0 || max_visible > (int64_t)INT32_MAX - 256 ||
+        (scores && ld < max_visible) || k < 1 || k > 2048)
         return HSI_ERR_INVALID_ARG;
     const bool pool = block_ids != nullptr;
     if (pool && (!n_kept || !n_pool || n_keep < 1 || n_keep > SEL_MAXK)) return HSI_ERR_INVALID_ARG;
+    // without scores the top-k comes from the pool: its n_keep - 1 unpinned
+    // blocks hold the first k blocks by maximum, so the top-k lies in the pool
+    const bool pooled_topk = scores == nullptr;
+    if (pooled_topk && (!pool || n_keep - 1 < k)) return HSI_ERR_INVALID_ARG;
+    if (pooled_topk && (n_keep > kPooledTopkMaxKeep || n_keep % (16 * kGatherUT))) return HSI_ERR_UNSUPPORTED;
     if (phases == HSI_PHASE_POOL && !pool) return HSI_ERR_INVALID_ARG;
     if (pool_bits && ld_bits < (max_visible + 31) / 32) return HSI_ERR_INVALID_ARG;
     const int64_t nb = (max_visible + 7) / 8;
@@ -708,7 +724,7 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     uint8_t* wpool = static_cast<uint8_t*>(ws) + sel_ws_bytes(B, max_visible, false, 0);
     SelWs wpp = carve_sel(wpool, B, nb, false, 0);
     float* bmax = reinterpret_cast<float*>(wpool + sel_ws_bytes(B, nb, false, 0));
-    const bool big_topk = max_visible > SEL_CAP;
+    const bool big_topk = max_visible > SEL_CAP && !pooled_topk;  // the top-k's selection over the scores
     if (phases & 1) {
     // the pool's threshold comes from a histogram of the block maxima the scan
     // fills, like the top-k's from the scores' (rows past SEL_CAP blocks)
@@ -730,7 +746,7 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     p.ld = ld;
     // block maxima: for the pool, and for the top-k's collect pass (it reads the
     // scores of the blocks whose maximum reaches the threshold bin only)
-    p.bmax = pool || big_topk ? bmax : nullptr;
+    p.bmax = pool || big_topk ? bmax : nullptr;  // scores == NULL: block maxima only
     p.ldb = ldb;
     p.key_hist = big_topk ? wsp.hist : nullptr;
     p.bmax_hist = bmax_hist ? wpp.hist : nullptr;
@@ -739,6 +755,23 @@ hsi_status hsi_full_layer(const uint8_t* q_rec, const float* g_q, const float* w
     }
     const bool do_topk = phases == HSI_PHASE_ALL || phases == HSI_PHASE_SELECT || phases == HSI_PHASE_TOPK;
     const bool do_pool = pool && (phases == HSI_PHASE_ALL || phases == HSI_PHASE_SELECT || phases == HSI_PHASE_POOL);
+    if (do_topk && pooled_topk) {
+        // the pool's records re-scored with this layer's query (the same fp32
+        // scores as the full scan's), its top-k mapped back to positions
+        uint8_t* wt = reinterpret_cast<uint8_t*>(bmax) + align_up((size_t)B * ldb * 4, 256);
+        float* pscores = reinterpret_cast<float*>(wt);
+        uint8_t* rws = wt + align_up((size_t)B * SEL_CAP * 4, 256);
+        const size_t rws_bytes = pooled_topk_ws_bytes(B) - align_up((size_t)B * SEL_CAP * 4, 256);
+        if (phases == HSI_PHASE_ALL || phases == HSI_PHASE_SELECT) {  // the pool first
+            st = hsi_full_layer(q_rec, g_q, w, k_rec, g_k, k_rec_off, n_visible, B, max_visible, scores, ld, k,
+                                top_idx, top_val, n_keep, block_ids, n_kept, n_pool, pool_bits, ld_bits,
+                                HSI_PHASE_POOL, format, ws, ws_bytes, stream);
+            if (st != HSI_OK) return st;
+        }
+        return hsi_reindex_layer(q_rec, g_q, w, k_rec, g_k, k_rec_off, nullptr, 0, n_visible, block_ids, n_kept,
+                                 n_pool, n_keep, B, pscores, (int64_t)n_keep * 8, k, top_idx, top_val, format, rws,
+                                 rws_bytes, stream);
+    }
     if (do_topk) {
     SelParams sp{};
     sp.src = scores;

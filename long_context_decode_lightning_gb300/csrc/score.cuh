@@ -763,8 +763,10 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS
         // one key's score: written, its 8-key block maximum, its histogram bin
         auto emit = [&](int b, int key, int nv, int npad, float sc) {
             const bool vis = key < nv;
-            if (vis) p.scores[(int64_t)b * p.ld + key] = sc;
-            else if (key < npad) p.scores[(int64_t)b * p.ld + key] = __uint_as_float(0xFF800000u);
+            if (p.scores) {  // (block maxima only without a score row)
+                if (vis) p.scores[(int64_t)b * p.ld + key] = sc;
+                else if (key < npad) p.scores[(int64_t)b * p.ld + key] = __uint_as_float(0xFF800000u);
+            }
             if (fuse_hist && vis) atomicAdd(hist_of(b) + (order_key(sc) >> 20), 1u);
             if (p.bmax) {
                 float m = vis ? sc : __uint_as_float(0xFF800000u);

@@ -109,3 +109,14 @@ def test_host_validation_rejects_bad_arguments(L):
                                 None) == -1
     # score_pool: ld shorter than 8 * n_keep
     assert L.hsi_score_pool(*args, fake, fake, 2048, 1, fake, 2048 * 8 - 1, 0, None, 0, None) == -1
+    # score_full: neither a score row nor block maxima
+    assert L.hsi_score_full(*args, 1, 100, 1, None, 0, None, 0, 0, None, 0, None) == -1
+    # full_layer without scores: needs the pool, n_keep - 1 >= k; n_keep <= 2048, a multiple of 32
+    ws_big = 1 << 40
+    def fl(scores, k, n_keep, ids):
+        return L.hsi_full_layer(*args, 1, 1 << 20, scores, 0, k, fake, fake, n_keep, ids, fake, fake, None, 0, 3, 0,
+                                fake, ws_big, None)
+    assert fl(None, 512, 2048, None) == -1
+    assert fl(None, 512, 512, fake) == -1
+    assert fl(None, 512, 4096, fake) == -2
+    assert fl(None, 512, 2047, fake) == -2

@@ -106,6 +106,13 @@ def _resident(idx, fmt=hsi.FMT_NVFP4):
     W.capture()
     W.replay()
     W.replay()
+    if W.pooled_topk:
+        # the step's pool layer writes no score row (its top-512 comes from the
+        # pool): score it once more for the checks, by the same kernel, to the
+        # same fp32 values
+        l = wl.full_layers - 1
+        hsi.score_full(W.q_rec[l], W.g_q[l], W.w[l], W.k_rec[l], W.g_k[l], W.k_off, W.n_vis, W.B, W.maxv, W.scores,
+                       fmt=W.fmt)
     torch.cuda.synchronize()
     assert hsi.device_error() == 0
     return wl, W

@@ -448,6 +448,60 @@ def test_full_and_reindex_layer_match_separate_calls(lengths):
     assert torch.equal(ri_g, ri_sep) and torch.equal(rv_g, rv_sep)
 
 
+@pytest.mark.parametrize("lengths", [[3, 20000, 200003], [16384, 131073, 9000]])
+def test_full_layer_without_scores(lengths):
+    """With scores = NULL the Full layer writes no score row and takes its
+    top-k from the pool's re-scored blocks: the same top-k, pool and table as
+    with the score row, in one call and as separate phases."""
+    wl = inputs.workload(1)
+    B, maxv = len(lengths), max(lengths)
+    caches = Caches(wl, 0, range(B), lengths)
+    q_rec, g_q, w = gpu_queries(wl, 0, range(B))
+    nv, off = i32(lengths), i64(caches.rec_off)
+
+    def outs():
+        return (torch.full((B, 512), 7, dtype=torch.int32, device=DEV), torch.full((B, 512), 7.0, device=DEV),
+                torch.full((B, 2048), 7, dtype=torch.int32, device=DEV), torch.full((B,), 7, dtype=torch.int32,
+                device=DEV), torch.full((B,), 7, dtype=torch.int32, device=DEV),
+                torch.zeros(B, (maxv + 31) // 32, dtype=torch.int32, device=DEV))
+
+    s_ref = torch.empty(B, maxv, device=DEV)
+    ref = outs()
+    hsi.full_layer(q_rec, g_q, w, caches.k_rec, caches.g, off, nv, B, maxv, s_ref, 512, ref[0], ref[1],
+                   block_ids=ref[2], n_kept=ref[3], n_pool=ref[4], pool_bits=ref[5])
+    ws = hsi.workspace(hsi.WS_FULL_LAYER, B, maxv, 512, device=DEV)
+    for split in (False, True):
+        got = outs()
+        kw = dict(block_ids=got[2], n_kept=got[3], n_pool=got[4], pool_bits=got[5], ws=ws)
+        if split:
+            for ph in (hsi.PHASE_SCORE, hsi.PHASE_POOL, hsi.PHASE_TOPK):
+                hsi.full_layer(q_rec, g_q, w, caches.k_rec, caches.g, off, nv, B, maxv, None, 512, got[0], got[1],
+                               phases=ph, **kw)
+        else:
+            hsi.full_layer(q_rec, g_q, w, caches.k_rec, caches.g, off, nv, B, maxv, None, 512, got[0], got[1], **kw)
+        assert hsi.device_error() == 0
+        assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1]), split
+        assert torch.equal(got[3], ref[3]) and torch.equal(got[4], ref[4]), split
+        for b, n in enumerate(lengths):
+            kb = int(ref[3][b])
+            assert torch.equal(got[2][b, :kb], ref[2][b, :kb]), (split, b)
+            assert torch.equal(got[5][b, :(n + 31) // 32], ref[5][b, :(n + 31) // 32]), (split, b)
+    # the oracle's top-k on the score row
+    sg = s_ref.cpu().numpy()
+    for b, n in enumerate(lengths):
+        oi, _ = oracle.topk(sg[b], n, 512)
+        assert np.array_equal(ref[0].cpu().numpy()[b], oi)
+    # block maxima without a score row
+    bm_ref = torch.empty(B, hsi.n_records(maxv), device=DEV)
+    hsi.score_full(q_rec, g_q, w, caches.k_rec, caches.g, off, nv, B, maxv, s_ref, block_max=bm_ref)
+    bm = torch.full_like(bm_ref, float("nan"))
+    hsi.score_full(q_rec, g_q, w, caches.k_rec, caches.g, off, nv, B, maxv, None, block_max=bm)
+    assert hsi.device_error() == 0
+    for b, n in enumerate(lengths):
+        nb = (n + 7) // 8
+        assert torch.equal(bm[b, :nb], bm_ref[b, :nb])
+
+
 def _caches_from_rows(wl, rows_per_cache):
     """K caches built from given bf16 rows (one array [n][128] per cache)."""
     parts, gs, offs, off = [], [], [], 0
