@@ -480,6 +480,18 @@ struct SelSmem {
     } while (0)
 #endif
 
+// Counts of the routes select_small_fast leaves by (only with -DHSI_TRACE).
+#ifdef HSI_TRACE
+#define SEL_COUNT(slot)                                        \
+    do {                                                       \
+        if (threadIdx.x == 0) atomicAdd(&g_hsi_trace[slot], 1ull); \
+    } while (0)
+#else
+#define SEL_COUNT(slot) \
+    do {                \
+    } while (0)
+#endif
+
 // Sources of items for the block select.
 struct SmemSrc {  // keys and indices in shared memory
     const uint32_t* keys;
@@ -1084,14 +1096,14 @@ enum : int { SMALL_WHOLE_ROW = -1, SMALL_RADIX = -2 };
 // shared memory by bulk copies, issued first so that they land while the
 // histogram is scanned (*in_smem then says that s.keys holds the row, and
 // *ids_in_smem that s.idx holds the block ids for the output). When the kept
-// items are few (at most one per thread), they are ordered without radix
+// items are few (at most two per thread), they are ordered without radix
 // passes or a sort: compared as floats against bin T's least value, they go
 // into one list; a second histogram of SEL_B2 bins spans the kept keys' range
 // (from bin T's least key to the largest key), its scan gives every bin's
 // first rank (the items in the bins above it), each item goes to a slot of
 // its bin's range, and its rank within the bin is the number of the bin's
-// items that beat it. More than 64 items in one second-level bin (heavy ties)
-// take the radix route instead.
+// items that beat it. More than 256 items in one second-level bin (heavy
+// ties) take the radix route instead.
 __device__ __forceinline__ int select_small_fast(const SelParams& p, int b, int64_t n, const uint32_t* hist,
                                                  SelSmem& s, bool* in_smem, bool* ids_in_smem) {
     static_assert(HIST_BINS == 4 * SEL_THREADS, "four bins per thread");
@@ -1154,17 +1166,27 @@ __device__ __forceinline__ int select_small_fast(const SelParams& p, int b, int6
         return 0;
     }
     SEL_MARK(s, 24);
-    if (total < k) return SMALL_WHOLE_ROW;
+    if (total < k) {
+        SEL_COUNT(21);
+        return SMALL_WHOLE_ROW;
+    }
     const uint32_t T = s.bcast[0], above = s.bcast[1], at_T = s.bcast[2];
     const uint32_t kept_all = above + at_T;
-    if (!bulk || kept_all > (uint32_t)SEL_THREADS) return SMALL_RADIX;
+    constexpr int KPT = 2;                        // kept items per thread
+    constexpr int SMALL_CAP = KPT * SEL_THREADS;  // kept items ranked without radix passes
+    static_assert(SEL_CAP / 8 <= 4096 && 8192 + 2 * SMALL_CAP <= SEL_CAP,
+                  "block ids, the kept list and the grouped list share s.idx");
+    if (!bulk || kept_all > (uint32_t)SMALL_CAP) {
+        SEL_COUNT(bulk ? 22 : 21);
+        return SMALL_RADIX;
+    }
 
     uint32_t* h2 = &s.whist[0][0];  // second-level bins of the kept keys
     uint32_t* start2 = h2 + SEL_B2;
     uint32_t* fill2 = start2 + SEL_B2;
-    uint32_t* wmax = fill2 + SEL_B2;                                  // [SEL_WARPS]
-    unsigned long long* clist = s.win + (SEL_MAXK - 2 * SEL_THREADS);  // the kept items, in no order
-    unsigned long long* cand = s.win + (SEL_MAXK - SEL_THREADS);       // the kept items, grouped by bin
+    uint32_t* wmax = fill2 + SEL_B2;                                                  // [SEL_WARPS]
+    unsigned long long* clist = reinterpret_cast<unsigned long long*>(s.idx + 4096);  // the kept items, in no order
+    unsigned long long* cand = reinterpret_cast<unsigned long long*>(s.idx + 8192);   // the kept items, grouped by bin
     const int lane = t & 31, warp = t >> 5;
     const uint32_t base = T << 20;
     const float fT = key_to_float(base);  // the least value whose key lies in bin T or above
@@ -1198,7 +1220,7 @@ __device__ __forceinline__ int select_small_fast(const SelParams& p, int b, int6
             const uint32_t m = bal[4 * i + e];
             if ((m >> lane) & 1u) {
                 const uint32_t pos = wpos + (uint32_t)__popc(m & lt);
-                if (pos < (uint32_t)SEL_THREADS)
+                if (pos < (uint32_t)SMALL_CAP)
                     clist[pos] = ((unsigned long long)order_key(e4[e]) << 32) | (uint32_t)~(j0 + (uint32_t)e);
             }
             wpos += (uint32_t)__popc(m);
@@ -1209,19 +1231,33 @@ __device__ __forceinline__ int select_small_fast(const SelParams& p, int b, int6
     __syncthreads();
     SEL_MARK(s, 27);
     const uint32_t cnt = s.bcast[6];
-    if (cnt != kept_all) return SMALL_RADIX;  // the histogram does not describe the row (uniform)
+    if (cnt != kept_all) {  // the histogram does not describe the row (uniform)
+        SEL_COUNT(21);
+        return SMALL_RADIX;
+    }
     // SEL_B2 bins over [T << 20, largest kept key], fine enough that few items share one
-    const bool mine = t < (int)cnt;
-    const unsigned long long me = mine ? clist[t] : 0ull;
-    const uint32_t key = (uint32_t)(me >> 32);
-    const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, mine ? key : 0u);
+    bool mine[KPT];
+    unsigned long long me[KPT];
+    uint32_t key[KPT], x[KPT], mx = 0;
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+        const uint32_t j = (uint32_t)(t + i * SEL_THREADS);
+        mine[i] = j < cnt;
+        me[i] = mine[i] ? clist[j] : 0ull;
+        key[i] = (uint32_t)(me[i] >> 32);
+        if (mine[i]) mx = max(mx, key[i]);
+    }
+    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
     if (lane == 0) wmax[warp] = mx;
     __syncthreads();
     const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, wmax[lane]);
     const uint32_t range = top - base;
     const int sh2 = range >= (uint32_t)SEL_B2 ? 32 - __clz((int)(range / SEL_B2)) : 0;  // range >> sh2 < SEL_B2
-    const uint32_t x = mine ? (key - base) >> sh2 : 0u;
-    if (mine) atomicAdd(&h2[x], 1u);
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+        x[i] = mine[i] ? (key[i] - base) >> sh2 : 0u;
+        if (mine[i]) atomicAdd(&h2[x[i]], 1u);
+    }
     __syncthreads();
     const uint32_t c0 = h2[2 * t], c1 = h2[2 * t + 1];
     uint32_t tot2;
@@ -1234,19 +1270,26 @@ __device__ __forceinline__ int select_small_fast(const SelParams& p, int b, int6
     if (lane == 0) wmax[warp] = wc;
     __syncthreads();
     SEL_MARK(s, 26);
-    if (__reduce_max_sync(0xFFFFFFFFu, wmax[lane]) > 64u) {  // heavy ties (uniform)
+    // a crowded bin costs its items one comparison per item of the bin: heavy
+    // ties (more than 256 in one bin) take the radix passes (uniform)
+    if (__reduce_max_sync(0xFFFFFFFFu, wmax[lane]) > 256u) {
         __syncthreads();  // every read of the bins is done before the radix passes reuse them
+        SEL_COUNT(23);
         return SMALL_RADIX;
     }
-    if (mine) cand[start2[x] + atomicAdd(&fill2[x], 1u)] = me;
+#pragma unroll
+    for (int i = 0; i < KPT; ++i)
+        if (mine[i]) cand[start2[x[i]] + atomicAdd(&fill2[x[i]], 1u)] = me[i];
     __syncthreads();
     SEL_MARK(s, 25);
-    if (mine) {  // rank: the items of the bins above, then those of its own bin that beat it
-        const uint32_t lo = start2[x], hi = lo + fill2[x];
-        uint32_t r = lo;
-        for (uint32_t i = lo; i < hi; ++i) r += cand[i] > me ? 1u : 0u;
-        if (r < k) s.win[r] = me;
-    }
+#pragma unroll
+    for (int i = 0; i < KPT; ++i)
+        if (mine[i]) {  // rank: the items of the bins above, then those of its own bin that beat it
+            const uint32_t lo = start2[x[i]], hi = lo + fill2[x[i]];
+            uint32_t r = lo;
+            for (uint32_t c = lo; c < hi; ++c) r += cand[c] > me[i] ? 1u : 0u;
+            if (r < k) s.win[r] = me[i];
+        }
     __syncthreads();
     SEL_MARK(s, 30);
     *ids_in_smem = bulk_ids;
