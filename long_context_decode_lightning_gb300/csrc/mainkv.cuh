@@ -7,11 +7,13 @@
 // attention kernel; every decoded value (an E2M1 value times an E4M3 scale, at
 // most 6 significant bits, magnitude in [2^-10, 2688]) is exact in bf16.
 //
-// Both kernels give each lane one 16-value group of an entry, so a group's amax
-// and scale need no exchange between lanes.
+// The quantiser gives each lane one 16-value group of an entry, so a group's
+// amax and scale need no exchange between lanes; the gather gives each lane 8
+// values of two groups, so that the warp's stores of a row are contiguous.
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "quantize.cuh"
@@ -21,11 +23,25 @@ namespace hsi {
 constexpr int KV_DIM = 512;
 constexpr int KV_BYTES = 288;
 
-// E2M1 code (bit 3 = sign) -> fp32, exact: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.
-__device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
-    const uint32_t m = c & 7u, e = m >> 1;
-    const uint32_t mag = e ? (((e + 126u) << 23) | ((m & 1u) << 22)) : (m ? 0x3F000000u : 0u);
-    return __uint_as_float(mag | ((c & 8u) << 28));
+// Eight codes (four bytes; value 2i in the low nibble of byte i) times one
+// E4M3 scale, as four bf16 pairs. The hardware conversions give the E2M1
+// values and the scale exactly in f16, and their product (at most 6
+// significant bits, magnitude in [2^-10, 2688]) is exact in f16, so in fp32
+// and in bf16: the same bits as decoding in fp32.
+__device__ __forceinline__ void decode8_bf16(uint32_t codes, uint32_t scale_byte, uint32_t (&o)[4]) {
+    uint32_t sc2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(sc2) : "h"((unsigned short)(scale_byte * 0x101u)));
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t v;
+        asm("{ .reg .b8 t; cvt.u8.u16 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }"
+            : "=r"(v)
+            : "h"((unsigned short)((codes >> (8 * q)) & 0xFFu)));
+        const __half2 prod = __hmul2(*reinterpret_cast<const __half2*>(&v), *reinterpret_cast<const __half2*>(&sc2));
+        const float2 f = __half22float2(prod);
+        const __nv_bfloat162 h = __floats2bfloat162_rn(f.x, f.y);
+        o[q] = *reinterpret_cast<const uint32_t*>(&h);
+    }
 }
 
 // One warp: the bf16 entry at x_row (512 values, 16-byte aligned) into the
@@ -117,39 +133,35 @@ __global__ void __launch_bounds__(256) mainkv_gather_kernel(const uint8_t* __res
             else raise_error(DEVERR_ARG);
         }
     }
+    // lane: values [8 lane, 8 lane + 8) and [256 + 8 lane, 256 + 8 lane + 8) of
+    // each entry, so that each of the warp's two 16-byte stores per entry
+    // covers 512 contiguous bytes of the row
     long long e[GATHER_EPW];
-    uint2 c[GATHER_EPW];
-    uint32_t sb[GATHER_EPW];
+    uint32_t c0[GATHER_EPW], c1[GATHER_EPW], s0[GATHER_EPW], s1[GATHER_EPW];
 #pragma unroll
     for (int j = 0; j < GATHER_EPW; ++j) {
         e[j] = __shfl_sync(0xFFFFFFFFu, src, j);
-        c[j] = make_uint2(0u, 0u);
-        sb[j] = 0u;
+        c0[j] = c1[j] = s0[j] = s1[j] = 0u;
         if (e[j] >= 0) {
             const uint8_t* p = kv + e[j] * KV_BYTES;
-            c[j] = __ldcs(reinterpret_cast<const uint2*>(p + lane * 8));
-            sb[j] = __ldcs(p + 256 + lane);
+            c0[j] = __ldcs(reinterpret_cast<const uint32_t*>(p) + lane);
+            c1[j] = __ldcs(reinterpret_cast<const uint32_t*>(p + 128) + lane);
+            s0[j] = __ldcs(p + 256 + (lane >> 1));
+            s1[j] = __ldcs(p + 272 + (lane >> 1));
         }
     }
 #pragma unroll
     for (int j = 0; j < GATHER_EPW; ++j) {
         if (base + j >= total) break;
-        uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        uint32_t o0[4] = {0u, 0u, 0u, 0u}, o1[4] = {0u, 0u, 0u, 0u};
         if (e[j] >= 0) {
-            const float sc = e4m3_to_f32(sb[j]);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const uint32_t word = q < 4 ? c[j].x : c[j].y;
-                const uint32_t pair = word >> (8 * (q & 3));
-                const __nv_bfloat162 h = __floats2bfloat162_rn(e2m1_to_f32(pair & 15u) * sc,
-                                                               e2m1_to_f32((pair >> 4) & 15u) * sc);
-                o[q] = *reinterpret_cast<const uint32_t*>(&h);
-            }
+            decode8_bf16(c0[j], s0[j], o0);
+            decode8_bf16(c1[j], s1[j], o1);
         }
         const int64_t f = base + j;
-        uint4* dst = reinterpret_cast<uint4*>(out + (f / per) * out_stride + (f % per) * KV_DIM + lane * 16);
-        __stcs(dst, make_uint4(o[0], o[1], o[2], o[3]));
-        __stcs(dst + 1, make_uint4(o[4], o[5], o[6], o[7]));
+        uint16_t* row = out + (f / per) * out_stride + (f % per) * KV_DIM;
+        __stcs(reinterpret_cast<uint4*>(row + lane * 8), make_uint4(o0[0], o0[1], o0[2], o0[3]));
+        __stcs(reinterpret_cast<uint4*>(row + 256 + lane * 8), make_uint4(o1[0], o1[1], o1[2], o1[3]));
     }
 }
 
