@@ -448,6 +448,36 @@ def test_full_and_reindex_layer_match_separate_calls(lengths):
     assert torch.equal(ri_g, ri_sep) and torch.equal(rv_g, rv_sep)
 
 
+@pytest.mark.parametrize("k,n_keep", [(512, 544), (64, 96), (1, 32)])
+def test_full_layer_without_scores_small_pools(k, n_keep):
+    """The top-k from the pool when the pool is barely larger than k blocks
+    (n_keep - 1 >= k): still the top-k of the whole row."""
+    wl = inputs.workload(1)
+    lengths = [20000, 140000, 4000]
+    B, maxv = len(lengths), max(lengths)
+    caches = Caches(wl, 0, range(B), lengths)
+    q_rec, g_q, w = gpu_queries(wl, 0, range(B))
+    nv, off = i32(lengths), i64(caches.rec_off)
+    s_ref = torch.empty(B, maxv, device=DEV)
+    ri, rv = torch.empty(B, k, dtype=torch.int32, device=DEV), torch.empty(B, k, device=DEV)
+    ids = torch.empty(B, n_keep, dtype=torch.int32, device=DEV)
+    nk, npl = torch.empty(B, dtype=torch.int32, device=DEV), torch.empty(B, dtype=torch.int32, device=DEV)
+    hsi.full_layer(q_rec, g_q, w, caches.k_rec, caches.g, off, nv, B, maxv, s_ref, k, ri, rv, block_ids=ids,
+                   n_kept=nk, n_pool=npl, n_keep=n_keep)
+    gi, gv = torch.full((B, k), 7, dtype=torch.int32, device=DEV), torch.full((B, k), 7.0, device=DEV)
+    ids2 = torch.empty_like(ids)
+    nk2, np2 = torch.empty_like(nk), torch.empty_like(npl)
+    hsi.full_layer(q_rec, g_q, w, caches.k_rec, caches.g, off, nv, B, maxv, None, k, gi, gv, block_ids=ids2,
+                   n_kept=nk2, n_pool=np2, n_keep=n_keep)
+    assert hsi.device_error() == 0
+    assert torch.equal(gi, ri) and torch.equal(gv, rv)
+    assert torch.equal(nk2, nk) and torch.equal(np2, npl)
+    sg = s_ref.cpu().numpy()
+    for b, n in enumerate(lengths):
+        oi, _ = oracle.topk(sg[b], n, k)
+        assert np.array_equal(gi.cpu().numpy()[b], oi), b
+
+
 @pytest.mark.parametrize("lengths", [[3, 20000, 200003], [16384, 131073, 9000]])
 def test_full_layer_without_scores(lengths):
     """With scores = NULL the Full layer writes no score row and takes its
