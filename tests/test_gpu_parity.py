@@ -239,6 +239,36 @@ def test_pool_past_the_bitmap_range():
     assert np.array_equal(_bits_to_mask(gb[0], n), rm)
 
 
+@pytest.mark.parametrize("case", ["few_values", "neg_inf_blocks", "pos_inf", "one_value", "keep_1"])
+def test_pool_crafted_rows_past_the_shared_memory_size(case):
+    """Rows of more than 16384 blocks take the candidate list and the pool's
+    final kernel (second-level bins, the tied bin ranked) or, for heavy ties and
+    more +inf keys than places, the general block select: crafted rows for
+    every route, against the oracle."""
+    rng = np.random.default_rng(len(case))
+    n_vis = [300001, 140003, 131072]
+    ld = max(n_vis)
+    sc = rng.standard_normal((len(n_vis), ld)).astype(np.float32)
+    keep = 2048
+    if case == "few_values":
+        sc = np.round(sc * 4) / 4
+    elif case == "neg_inf_blocks":
+        sc[:, 8 * 1000:8 * 60000] = -np.inf  # whole blocks dropped
+    elif case == "pos_inf":
+        sc[0, rng.integers(0, n_vis[0], 3000)] = np.inf  # more +inf blocks than places
+        sc[1, rng.integers(0, n_vis[1], 100)] = np.inf
+    elif case == "one_value":
+        sc[:] = 0.5
+    else:
+        keep = 1
+    gi, gk, gp, gb = _gpu_pool(sc, n_vis, keep=keep)
+    for b, n in enumerate(n_vis):
+        ri, rk, rp, rm = oracle.pool(sc[b], n, 8, keep)
+        assert gk[b] == rk and gp[b] == rp, (case, b)
+        assert np.array_equal(gi[b][:rk], ri[:rk]) and (gi[b][rk:] == -1).all(), (case, b)
+        assert np.array_equal(_bits_to_mask(gb[b], n), rm), (case, b)
+
+
 @pytest.mark.parametrize("bs,keep", [(4, 6), (1, 5), (3, 100), (8, 1)])
 def test_pool_small_block_and_keep(bs, keep):
     rng = np.random.default_rng(bs * 100 + keep)
