@@ -382,6 +382,12 @@ class DeviceWorkload:
         gather = t(lambda: hsi.score_pool(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0],
                                           self.k_off, self.n_vis, self.ids, self.nk, wl.n_keep, B,
                                           self.pool_scores, fmt=self.fmt))
+        # the scan of the compacted pool alone (query b's n_pool[b] keys at record
+        # b n_keep, left there by the compaction above): the scoring of the
+        # Reindex layers that stream the pool
+        pool_off = torch.arange(B, dtype=torch.int64, device=self.dev) * wl.n_keep
+        stream = t(lambda: hsi.score_full(self.q_rec[l], self.g_q[l], self.w[l], self.pool_rec, self.g_k[0],
+                                          pool_off, self.npool, B, wl.n_keep * 8, self.pool_scores, fmt=self.fmt))
         first = t(lambda: hsi.reindex_layer(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0],
                                             self.k_off, self.n_vis, self.ids, self.nk, self.npool, B,
                                             self.pool_scores, K_TOP, self.idx[l], self.val[l], n_keep=wl.n_keep,
@@ -398,7 +404,7 @@ class DeviceWorkload:
         dense_us = t(dense)
         pooled_bytes = int(self.nk.clamp(max=wl.n_keep).sum().item()) * self.rec
         return {"layer_us": layer, "first_layer_us": first, "plain_topk_us": topk, "compact_us": compact,
-                "gather_score_us": gather, "dense_masked_layer_us": dense_us,
+                "gather_score_us": gather, "stream_score_us": stream, "dense_masked_layer_us": dense_us,
                 "dense_over_pooled": dense_us / layer, "pooled_bytes_per_layer": pooled_bytes}
 
     def capture(self):
@@ -1071,6 +1077,8 @@ def main():
             "layer_gbs": gbs(reindex["layer_us"]), "layer_frac": gbs(reindex["layer_us"]) / peak,
             "gather_score_gbs": gbs(reindex["gather_score_us"]),
             "gather_score_frac": gbs(reindex["gather_score_us"]) / peak,
+            "stream_score_gbs": gbs(reindex["stream_score_us"]),
+            "stream_score_frac": gbs(reindex["stream_score_us"]) / peak,
             "note": "one layer timed alone on the resident pool; fractions of the measured copy bandwidth for "
                     "the pooled bytes (the layer figure includes its selection)"})
     serve = not args.no_serve and wl.build_pool and wl.full_layers == 1
