@@ -352,21 +352,29 @@ class DeviceWorkload:
         return merged
 
     def reindex_timings(self, reps=20):
-        """One Reindex layer, timed alone on the resident pool (CUDA events around
-        `reps` back-to-back calls): the whole layer through the compacted pool
-        (scan with the fused key histogram, then the selection), a plain top-k
-        of the pooled scores (no histogram), the compaction, and the gathering
-        scorer."""
+        """One Reindex layer, timed alone on the resident pool: the whole layer
+        through the compacted pool (scan with the fused key histogram, then the
+        selection), a plain top-k of the pooled scores (no histogram), the
+        compaction, and the gathering scorer. Each figure is one CUDA graph of
+        `reps` back-to-back calls (as the step runs them: graphs, programmatic
+        dependent launch), timed with events around its replay, so that the
+        host's per-call launch cost, which exceeds these layers' device time,
+        is not what is measured."""
         torch, hsi, wl, B = self.torch, self.hsi, self.wl, self.B
         l = wl.full_layers
 
         def t(fn):
             fn()
             torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for _ in range(reps):
+                    fn()
+            g.replay()
+            torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
-            for _ in range(reps):
-                fn()
+            g.replay()
             e1.record()
             torch.cuda.synchronize()
             return 1000.0 * e0.elapsed_time(e1) / reps
@@ -402,8 +410,17 @@ class DeviceWorkload:
             hsi.mask_scores(self.scores, self.n_vis, self.bits, B, self.maxv)
             hsi.topk(self.scores, self.n_vis, B, self.maxv, K_TOP, self.idx[l], self.val[l], ws=self.ws_topk)
         dense_us = t(dense)
+        # the pool phase alone on the block maxima and their histogram the step's
+        # Full scan left in the workspace: threshold bin, candidates, the pool
+        pool_us = t(lambda: hsi.full_layer(self.q_rec[0], self.g_q[0], self.w[0], self.k_rec[0], self.g_k[0],
+                                           self.k_off, self.n_vis, B, self.maxv,
+                                           None if self.pooled_topk else self.scores, K_TOP, self.idx[0],
+                                           self.val[0], block_ids=self.ids, n_kept=self.nk, n_pool=self.npool,
+                                           pool_bits=self.bits, n_keep=wl.n_keep, ws=self.ws_full,
+                                           phases=hsi.PHASE_POOL, fmt=self.fmt))
         pooled_bytes = int(self.nk.clamp(max=wl.n_keep).sum().item()) * self.rec
         return {"layer_us": layer, "first_layer_us": first, "plain_topk_us": topk, "compact_us": compact,
+                "pool_phase_us": pool_us,
                 "gather_score_us": gather, "stream_score_us": stream, "dense_masked_layer_us": dense_us,
                 "dense_over_pooled": dense_us / layer, "pooled_bytes_per_layer": pooled_bytes}
 

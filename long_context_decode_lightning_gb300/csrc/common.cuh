@@ -91,4 +91,38 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
     return __uint_as_float(u);
 }
 
+// Four pooled-block flags (bits 0..3 of nib) as the 32 position bits of their
+// blocks of eight positions: bit q of the nibble fills byte q of the word.
+__device__ __forceinline__ uint32_t expand_nibble(uint32_t nib) { return ((nib * 0x00204081u) & 0x01010101u) * 0xFFu; }
+
+// The position bit table of one row (words 0 .. ceil(n_vis / 32) - 1) from the
+// bitmap of its pooled blocks of eight positions (bit j of bm[j / 32] for
+// block j): word w covers blocks 4w .. 4w + 3; bits of positions at or past
+// n_vis are 0. Threads tid of nthreads share the words; when the row is
+// 16-byte aligned the fully visible words go four to a store.
+__device__ __forceinline__ void write_pos_bits8(uint32_t* bits, const uint32_t* bm, int64_t n_vis, int tid,
+                                                int nthreads) {
+    const int64_t pw = (n_vis + 31) / 32;
+    int64_t w0 = 0;
+    if ((reinterpret_cast<uintptr_t>(bits) & 15) == 0) {
+        const int64_t quads = n_vis / 128;  // groups of four fully visible words: 16 blocks, half a bitmap word
+        for (int64_t g = tid; g < quads; g += nthreads) {
+            const uint32_t half = bm[g >> 1] >> (16 * (int)(g & 1));
+            uint4 o;
+            o.x = expand_nibble(half & 0xFu);
+            o.y = expand_nibble((half >> 4) & 0xFu);
+            o.z = expand_nibble((half >> 8) & 0xFu);
+            o.w = expand_nibble((half >> 12) & 0xFu);
+            reinterpret_cast<uint4*>(bits)[g] = o;
+        }
+        w0 = 4 * quads;
+    }
+    for (int64_t w = w0 + tid; w < pw; w += nthreads) {
+        uint32_t v = expand_nibble((bm[w >> 3] >> (4 * (int)(w & 7))) & 0xFu);
+        const int64_t left = n_vis - 32 * w;  // visible positions in this word
+        if (left < 32) v &= (1u << left) - 1u;
+        bits[w] = v;
+    }
+}
+
 }  // namespace hsi

@@ -496,18 +496,7 @@ __global__ void __launch_bounds__(RS_THREADS) rowsel_kernel(RowSelParams p) {
             // the newest block is pinned, so it is kept; its positions past n_vis are not in the pool
             p.n_pool[b] = (int32_t)(kept ? (int64_t)kept * 8 - (nblk * 8 - n_vis) : 0);
         }
-        if (p.bits) {
-            uint32_t* bits = p.bits + (int64_t)b * p.ld_bits;
-            const int64_t pw = (n_vis + 31) / 32;
-            for (int64_t w = tid; w < pw; w += RS_THREADS) {
-                // blocks 4w .. 4w+3: bit q of the nibble becomes byte q of the word
-                const uint32_t nib = (s.bitmap[w >> 3] >> ((w & 7) * 4)) & 0xFu;
-                uint32_t v = ((nib * 0x00204081u) & 0x01010101u) * 0xFFu;
-                const int64_t left = n_vis - w * 32;
-                if (left < 32) v &= (1u << left) - 1u;
-                bits[w] = v;
-            }
-        }
+        if (p.bits) write_pos_bits8(p.bits + (int64_t)b * p.ld_bits, s.bitmap, n_vis, tid, RS_THREADS);
         __syncthreads();  // the bitmap is reused for the candidate blocks
     }
 

@@ -1371,13 +1371,7 @@ __device__ __noinline__ void write_pool(const SelParams& p, int b, int count) {
             atomicOr(&bm[id >> 5], 1u << (id & 31));
         }
         __syncthreads();
-        for (int64_t w = threadIdx.x; w < words; w += SEL_THREADS) {
-            const uint32_t nib = (bm[w >> 3] >> (4 * (w & 7))) & 0xFu;
-            uint32_t v = ((nib * 0x00204081u) & 0x01010101u) * 0xFFu;
-            const int64_t end = n_vis - 32 * w;  // visible positions in this word
-            if (end < 32) v &= (1u << end) - 1u;
-            bits[w] = v;
-        }
+        write_pos_bits8(bits, bm, n_vis, threadIdx.x, SEL_THREADS);
         return;
     }
     for (int64_t wd = threadIdx.x; wd < words; wd += SEL_THREADS) bits[wd] = 0u;
@@ -1622,17 +1616,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) pool_final_kernel(SelParams p)
         // every kept block holds 8 visible positions but the newest, which may hold fewer
         p.n_pool[b] = (int32_t)(8 * (int64_t)kept - (last ? 8 * nb - n_vis : 0));
     }
-    if (p.bits) {  // word w of the position bit table holds blocks 4w .. 4w+3, 8 bits each
-        uint32_t* bits = p.bits + (int64_t)b * p.ld_bits;
-        const int64_t pw = (n_vis + 31) / 32;
-        for (int64_t w = t; w < pw; w += SEL_THREADS) {
-            const uint32_t nib = (bm[w >> 3] >> (4 * (w & 7))) & 0xFu;
-            uint32_t v = ((nib * 0x00204081u) & 0x01010101u) * 0xFFu;
-            const int64_t end = n_vis - 32 * w;  // visible positions in this word
-            if (end < 32) v &= (1u << end) - 1u;
-            bits[w] = v;
-        }
-    }
+    if (p.bits) write_pos_bits8(p.bits + (int64_t)b * p.ld_bits, bm, n_vis, t, SEL_THREADS);
 }
 
 // A visible length within [0, max_n], the caller's bound that sized the rows;
