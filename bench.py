@@ -266,10 +266,6 @@ class DeviceWorkload:
             self.ws_rtopk = hsi.workspace(hsi.WS_REINDEX_LAYER, B, wl.n_keep * 8, K_TOP, device=dev)
             self.pool_rec = torch.empty(B, wl.n_keep * REC, dtype=torch.uint8, device=dev)
         self.ev_score = []
-        # the Full layer's top-512 and its pool run on two streams: the pool and the
-        # Reindex layers (which need only the pool) on `side`, joined at the end
-        self.side = torch.cuda.Stream(device=dev)
-        self.ev_fork, self.ev_join, self.ev_pool = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
         # the Full layer that builds the pool writes no score row: its top-512 is
         # taken from the pool's blocks, scored again (the same scores, the same top-512)
         self.pooled_topk = wl.build_pool
@@ -297,18 +293,17 @@ class DeviceWorkload:
         hsi, wl, B = self.hsi, self.wl, self.B
         maxv = self.maxv if maxv is None else maxv
         segs = []
-        torch = self.torch
 
         def rest():
-            # the first Reindex layer gathers the pooled K records and leaves them
-            # compacted; the later layers of the step stream the compacted pool
+            # the Reindex layers stream the compacted pool, each query quantised
+            # right before its layer
             for r in range(wl.reindex_layers):
                 l = wl.full_layers + r
                 self.quant_q(l)
                 hsi.reindex_layer(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[0], self.g_k[0], self.k_off,
                                   self.n_vis, self.ids, self.nk, self.npool, B, self.pool_scores, K_TOP,
                                   self.idx[l], self.val[l], n_keep=wl.n_keep, ws=self.ws_rtopk,
-                                  pool_rec=self.pool_rec, pool_rec_ready=r > 0, fmt=self.fmt)
+                                  pool_rec=self.pool_rec, pool_rec_ready=True, fmt=self.fmt)
 
         for l in range(wl.full_layers):
             segs.append(("pre", lambda l=l: self.quant_q(l)))
@@ -325,20 +320,20 @@ class DeviceWorkload:
                     n_keep=wl.n_keep, ws=self.ws_full, phases=ph, fmt=self.fmt)
             segs.append(("score", lambda fl=fl: fl(hsi.PHASE_SCORE)))
             if pool:
-                def post(fl=fl):
-                    # the pool and the Reindex layers on `side`; the Full layer's
-                    # top-512 (from the pool) beside them on the main stream
-                    main = torch.cuda.current_stream()
-                    self.ev_fork.record(main)
-                    self.side.wait_event(self.ev_fork)
-                    with torch.cuda.stream(self.side):
-                        fl(hsi.PHASE_POOL)
-                        self.ev_pool.record(self.side)
-                        rest()
-                        self.ev_join.record(self.side)
-                    main.wait_event(self.ev_pool)
-                    fl(hsi.PHASE_TOPK)
-                    main.wait_event(self.ev_join)
+                def post(fl=fl, l=l):
+                    # model order on one stream: the pool; the Full layer's top-512
+                    # from it (the pool's blocks gathered and scored again with the
+                    # Full query: the full row's scores and top-512), which leaves
+                    # the gathered records compacted for the Reindex layers; then
+                    # those layers, whose queries a model computes only after the
+                    # Full layer's attention over that top-512
+                    fl(hsi.PHASE_POOL)
+                    hsi.reindex_layer(self.q_rec[l], self.g_q[l], self.w[l], self.k_rec[l], self.g_k[l], self.k_off,
+                                      self.n_vis, self.ids, self.nk, self.npool, B, self.pool_scores, K_TOP,
+                                      self.idx[l], self.val[l], n_keep=wl.n_keep, ws=self.ws_rtopk,
+                                      pool_rec=self.pool_rec if wl.reindex_layers else None,
+                                      pool_rec_ready=False, fmt=self.fmt)
+                    rest()
                 segs.append(("post", post))
             else:
                 segs.append(("post", lambda fl=fl: fl(hsi.PHASE_SELECT)))

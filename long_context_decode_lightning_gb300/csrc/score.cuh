@@ -110,8 +110,12 @@ struct ScoreCfg {
     static constexpr int Q_BYTES = NQ * 4 * REC;
     static constexpr int STAGE_BYTES = UNIT_RECS * REC;
     static constexpr int QSLOT_BYTES = ((Q_BYTES + 127) / 128) * 128;
-    // gather: a warpgroup of 16-byte async copies (4 threads per pooled block)
-    static constexpr int PROD_WARPS = GATHER ? 4 : 1;
+    // gather: producer warps of 16-byte async copies (TPR threads per pooled block)
+#ifndef HSI_GATHER_PROD_WARPS
+#define HSI_GATHER_PROD_WARPS 4
+#endif
+    static constexpr int PROD_WARPS = GATHER ? HSI_GATHER_PROD_WARPS : 1;
+    static constexpr int TPR = GATHER ? 32 * PROD_WARPS / UNIT_RECS : 1;  // gather: producer threads per record
     // MMA-issuing warps (one thread each), taking alternate units: a single
     // thread's issue sequence (waits, descriptors, MMAs, commit) per unit is
     // longer than the tensor work of a 4-query tile
@@ -158,7 +162,8 @@ struct ScoreCfg {
     static_assert(NQ <= 4, "B scale rows fit one 128-row layout");
     static_assert(COLS_USED <= 512, "TMEM");
     static_assert(NQ > 1 || NACC % EPI_GROUPS == 0, "accumulator sets split evenly between epilogue groups");
-    static_assert(!GATHER || (NQ == 1 && UNIT_RECS == 32), "gather: 4 producer threads per block");
+    static_assert(!GATHER || (NQ == 1 && UNIT_RECS == 32 && TPR * UNIT_RECS == 32 * PROD_WARPS),
+                  "gather: single queries, units of 32 records, whole producer warps per record group");
     static_assert(!GATHER || COPY_AHEAD < STAGES, "gather: copies in flight fit the ring");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
@@ -547,10 +552,10 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS
                              &full[st.i]);
                 }
             } else {
-                // 4 threads per pooled block, up to 9 x 16 bytes each (36 chunks of an
-                // NVFP4 record, 34 of an MXFP4 one)
+                // TPR threads per pooled block, 36 chunks of 16 bytes per NVFP4 record
+                // (34 per MXFP4 one) shared among them
                 const int islot = (int)(u % IDS_AHEAD);
-                const int blk = threadIdx.x >> 2, prt = threadIdx.x & 3;
+                const int blk = threadIdx.x / C::TPR, prt = threadIdx.x % C::TPR;
                 const int j = t * C::UNIT_RECS + blk;
                 const int64_t id = ids_ring[islot * C::UNIT_RECS + blk];
                 __syncwarp();
@@ -562,8 +567,9 @@ __global__ void __launch_bounds__(ScoreCfg<NQ, GATHER, STAGES, UT, FMT>::THREADS
                     uint8_t* d = dst + blk * C::REC;
                     constexpr int CH = C::REC / 16;
 #pragma unroll
-                    for (int c = 0; c < 9; ++c)
-                        if (c * 4 + prt < CH) cp_async16(d + (c * 4 + prt) * 16, src + (c * 4 + prt) * 16);
+                    for (int c = 0; c < (CH + C::TPR - 1) / C::TPR; ++c)
+                        if (c * C::TPR + prt < CH)
+                            cp_async16(d + (c * C::TPR + prt) * 16, src + (c * C::TPR + prt) * 16);
                 }
                 cp_async_commit();
                 // refill the id slot of the previous unit once every producer warp has read it
