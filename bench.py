@@ -1091,8 +1091,10 @@ def main():
             "gather_score_frac": gbs(reindex["gather_score_us"]) / peak,
             "stream_score_gbs": gbs(reindex["stream_score_us"]),
             "stream_score_frac": gbs(reindex["stream_score_us"]) / peak,
-            "note": "one layer timed alone on the resident pool; fractions of the measured copy bandwidth for "
-                    "the pooled bytes (the layer figure includes its selection)"})
+            "note": "one layer timed alone on the resident pool, each figure a CUDA graph of 20 calls; fractions "
+                    "of the measured copy bandwidth for the pooled bytes (the layer figure includes its zeroing "
+                    "and selection; stream_score is the Reindex layers' scoring, which reads the compacted pool; "
+                    "gather_score the one gather per step)"})
     serve = not args.no_serve and wl.build_pool and wl.full_layers == 1
     M = MainKV(wl, dev, log, headroom=DeviceWorkload.HEADROOM) if (not args.no_mainkv or serve) else None
     if not args.no_mainkv:
