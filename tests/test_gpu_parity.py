@@ -562,6 +562,45 @@ def test_full_layer_without_scores(lengths):
         assert torch.equal(bm[b, :nb], bm_ref[b, :nb])
 
 
+def test_step_in_model_order():
+    """The decode step's composition: the Full layer's top-512 taken from the
+    pool by the gathering Reindex call (which leaves the pool compacted) is the
+    Full layer's own pooled top-512, and a Reindex layer that streams that
+    compacted pool gives what it gives when it gathers the records."""
+    wl = inputs.workload(1)
+    lengths = [3, 20000, 200003]
+    B, maxv, n_keep, k = len(lengths), max(lengths), 2048, 512
+    caches = Caches(wl, 0, range(B), lengths)
+    nv, off = i32(lengths), i64(caches.rec_off)
+    q0, g0, w0 = gpu_queries(wl, 0, range(B))  # the Full layer's query
+    q1, g1, w1 = gpu_queries(wl, 1, range(B))  # a Reindex layer's query
+    ids = torch.empty(B, n_keep, dtype=torch.int32, device=DEV)
+    nk, npl = torch.empty(B, dtype=torch.int32, device=DEV), torch.empty(B, dtype=torch.int32, device=DEV)
+
+    def outs():
+        return torch.full((B, k), 7, dtype=torch.int32, device=DEV), torch.full((B, k), 7.0, device=DEV)
+
+    ri, rv = outs()
+    hsi.full_layer(q0, g0, w0, caches.k_rec, caches.g, off, nv, B, maxv, None, k, ri, rv, block_ids=ids,
+                   n_kept=nk, n_pool=npl, n_keep=n_keep)
+    pool_rec = torch.zeros(B, n_keep * 576, dtype=torch.uint8, device=DEV)
+    ps = torch.empty(B, n_keep * 8, device=DEV)
+    ws = hsi.workspace(hsi.WS_REINDEX_LAYER, B, n_keep * 8, k, device=DEV)
+    fi, fv = outs()
+    hsi.reindex_layer(q0, g0, w0, caches.k_rec, caches.g, off, nv, ids, nk, npl, B, ps, k, fi, fv, n_keep=n_keep,
+                      ws=ws, pool_rec=pool_rec, pool_rec_ready=False)
+    assert hsi.device_error() == 0
+    assert torch.equal(fi, ri) and torch.equal(fv, rv)
+    si, sv = outs()
+    hsi.reindex_layer(q1, g1, w1, caches.k_rec, caches.g, off, nv, ids, nk, npl, B, ps, k, si, sv, n_keep=n_keep,
+                      ws=ws, pool_rec=pool_rec, pool_rec_ready=True)
+    gi, gv = outs()
+    hsi.reindex_layer(q1, g1, w1, caches.k_rec, caches.g, off, nv, ids, nk, npl, B, ps, k, gi, gv, n_keep=n_keep,
+                      ws=ws)
+    assert hsi.device_error() == 0
+    assert torch.equal(si, gi) and torch.equal(sv, gv)
+
+
 def _caches_from_rows(wl, rows_per_cache):
     """K caches built from given bf16 rows (one array [n][128] per cache)."""
     parts, gs, offs, off = [], [], [], 0
